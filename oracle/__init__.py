@@ -1,0 +1,323 @@
+"""Oracle of the speech-token decode step -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes front end to ``sd_oracle.c`` (plain C, double-precision sums), plus
+drivers that run a whole workload the way the method describes it: a prompt
+processed position by position, then decode steps that each sample a token
+(or, for the Talker + code predictor, frames of 16 codes).  The drivers record
+every step's logits, sampled token and decision margin so that the CUDA
+library can be checked against them with teacher forcing.
+
+Only ``tests/``, the smoke entry and the benchmark's CPU-baseline leg import
+this package.  It shares no code with the CUDA library.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+ARCH_GPT2, ARCH_LLAMA, ARCH_QWEN_TTS = 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "sd_oracle.h"))):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = C.CDLL(build())
+        _declare(_lib)
+    return _lib
+
+
+def _declare(L):
+    f32p, i32p, u8p, u16p = (C.POINTER(C.c_float), C.POINTER(C.c_int32), C.POINTER(C.c_uint8),
+                             C.POINTER(C.c_uint16))
+    L.orc_half_to_float.argtypes = [C.c_uint16]; L.orc_half_to_float.restype = C.c_float
+    L.orc_float_to_half.argtypes = [C.c_float]; L.orc_float_to_half.restype = C.c_uint16
+    L.orc_dequant.argtypes = [C.c_int, u8p, C.c_int64, C.c_int64, f32p]
+    L.orc_linear.argtypes = [C.c_int, u8p, C.c_int64, C.c_int64, f32p, f32p, f32p]
+    L.orc_layernorm.argtypes = [f32p, C.c_int, f32p, f32p, C.c_float, f32p]; L.orc_layernorm.restype = None
+    L.orc_rmsnorm.argtypes = [f32p, C.c_int, f32p, C.c_float, f32p]; L.orc_rmsnorm.restype = None
+    L.orc_gelu_tanh.argtypes = [C.c_float]; L.orc_gelu_tanh.restype = C.c_float
+    L.orc_silu.argtypes = [C.c_float]; L.orc_silu.restype = C.c_float
+    L.orc_rope.argtypes = [f32p, C.c_int, C.c_int, C.c_float]; L.orc_rope.restype = None
+    L.orc_attend.argtypes = [f32p, u16p, u16p, C.c_int, C.c_int, f32p]; L.orc_attend.restype = None
+    L.orc_sample.argtypes = [f32p, C.c_int32, C.c_float, C.c_int32, C.c_float, C.c_int32, C.c_double,
+                             C.POINTER(C.c_double)]
+    L.orc_sample.restype = C.c_int32
+    L.orc_open.argtypes = [u8p, C.c_uint64, C.POINTER(C.c_void_p)]
+    L.orc_close.argtypes = [C.c_void_p]; L.orc_close.restype = None
+    L.orc_reset.argtypes = [C.c_void_p]; L.orc_reset.restype = None
+    L.orc_set_threads.argtypes = [C.c_int]
+    L.orc_pos.argtypes = [C.c_void_p, C.c_int]
+    L.orc_token_forward.argtypes = [C.c_void_p, C.c_int, C.c_int32, f32p]
+    L.orc_talker_forward.argtypes = [C.c_void_p, C.c_int, f32p, f32p, f32p]
+    L.orc_talker_embed.argtypes = [C.c_void_p, C.c_int32, f32p]
+    L.orc_cp_forward.argtypes = [C.c_void_p, C.c_int, f32p, C.c_int, f32p]
+    L.orc_cp_reset.argtypes = [C.c_void_p, C.c_int]; L.orc_cp_reset.restype = None
+    L.orc_code_embed.argtypes = [C.c_void_p, C.c_int, C.c_int32, f32p]
+    L.orc_code_embed_sum.argtypes = [C.c_void_p, i32p, f32p]
+
+
+def _p(a, ct):
+    return a.ctypes.data_as(C.POINTER(ct)) if a is not None else None
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+# ----------------------------------------------------------------------------- op-level
+
+def half_to_float(h) -> np.ndarray:
+    h = np.asarray(h, np.uint16).ravel()
+    return np.array([lib().orc_half_to_float(int(v)) for v in h], np.float32)
+
+
+def float_to_half(x) -> np.ndarray:
+    x = np.asarray(x, np.float32).ravel()
+    return np.array([lib().orc_float_to_half(float(v)) for v in x], np.uint16)
+
+
+def dequant(kind: int, data: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    d = np.ascontiguousarray(data, np.uint8)
+    out = np.empty((rows, cols), np.float32)
+    rc = lib().orc_dequant(kind, _p(d, C.c_uint8), rows, cols, _p(out, C.c_float))
+    if rc:
+        raise ValueError("orc_dequant rejected its arguments")
+    return out
+
+
+def linear(kind: int, data: np.ndarray, rows: int, cols: int, x, bias=None) -> np.ndarray:
+    d = np.ascontiguousarray(data, np.uint8 if kind else np.float32)
+    xx = _f32(x)
+    b = None if bias is None else _f32(bias)
+    y = np.empty(rows, np.float32)
+    rc = lib().orc_linear(kind, d.ctypes.data_as(C.POINTER(C.c_uint8)), rows, cols, _p(xx, C.c_float),
+                          _p(b, C.c_float), _p(y, C.c_float))
+    if rc:
+        raise ValueError("orc_linear rejected its arguments")
+    return y
+
+
+def layernorm(x, g, b, eps=1e-5):
+    x, g, b = _f32(x), _f32(g), _f32(b)
+    out = np.empty_like(x)
+    lib().orc_layernorm(_p(x, C.c_float), x.size, _p(g, C.c_float), _p(b, C.c_float), eps, _p(out, C.c_float))
+    return out
+
+
+def rmsnorm(x, g, eps=1e-5):
+    x, g = _f32(x), _f32(g)
+    out = np.empty_like(x)
+    lib().orc_rmsnorm(_p(x, C.c_float), x.size, _p(g, C.c_float), eps, _p(out, C.c_float))
+    return out
+
+
+def gelu_tanh(t):
+    return np.array([lib().orc_gelu_tanh(float(v)) for v in np.ravel(t)], np.float32)
+
+
+def silu(t):
+    return np.array([lib().orc_silu(float(v)) for v in np.ravel(t)], np.float32)
+
+
+def rope(x, pos: int, theta: float = 10000.0):
+    x = _f32(x).copy()
+    lib().orc_rope(_p(x, C.c_float), x.size, pos, theta)
+    return x
+
+
+def attend(q, k_half, v_half):
+    q = _f32(q)
+    k = np.ascontiguousarray(k_half, np.uint16)
+    v = np.ascontiguousarray(v_half, np.uint16)
+    n, hd = k.shape
+    out = np.empty(hd, np.float32)
+    lib().orc_attend(_p(q, C.c_float), _p(k, C.c_uint16), _p(v, C.c_uint16), n, hd, _p(out, C.c_float))
+    return out
+
+
+def sample(z, temperature=1.0, top_k=1, top_p=1.0, greedy=True, u=0.0):
+    """Returns (token, margin)."""
+    z = _f32(z)
+    m = C.c_double()
+    tok = lib().orc_sample(_p(z, C.c_float), z.size, float(temperature), int(top_k), float(top_p),
+                           int(bool(greedy)), float(u), C.byref(m))
+    return int(tok), float(m.value)
+
+
+# ----------------------------------------------------------------------------- model-level
+
+class Model:
+    """One oracle model bound to a weight blob (kept alive by this object)."""
+
+    def __init__(self, blob: np.ndarray, threads: int | None = None):
+        self._blob = np.ascontiguousarray(blob, np.uint8)
+        h = C.c_void_p()
+        if lib().orc_open(_p(self._blob, C.c_uint8), self._blob.size, C.byref(h)):
+            raise ValueError("oracle could not parse the weight blob")
+        self._h = h
+        self.threads = lib().orc_set_threads(threads if threads else 1)
+
+    def close(self):
+        if self._h:
+            lib().orc_close(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        lib().orc_reset(self._h)
+
+    def pos(self, row=0):
+        return lib().orc_pos(self._h, row)
+
+    def token_forward(self, row: int, tok: int, vocab: int, want_logits=True):
+        z = np.empty(vocab, np.float32) if want_logits else None
+        if lib().orc_token_forward(self._h, row, int(tok), _p(z, C.c_float)):
+            raise ValueError("orc_token_forward failed (bad token, row or full context)")
+        return z
+
+    def talker_embed(self, tok: int, d: int):
+        e = np.empty(d, np.float32)
+        if lib().orc_talker_embed(self._h, int(tok), _p(e, C.c_float)):
+            raise ValueError("bad talker token")
+        return e
+
+    def talker_forward(self, row: int, e, vocab: int, d: int):
+        e = _f32(e)
+        z = np.empty(vocab, np.float32)
+        h = np.empty(d, np.float32)
+        if lib().orc_talker_forward(self._h, row, _p(e, C.c_float), _p(z, C.c_float), _p(h, C.c_float)):
+            raise ValueError("orc_talker_forward failed")
+        return z, h
+
+    def cp_forward(self, row: int, v, head: int, vocab: int):
+        v = _f32(v)
+        z = np.empty(vocab, np.float32) if head >= 1 else None
+        if lib().orc_cp_forward(self._h, row, _p(v, C.c_float), head, _p(z, C.c_float)):
+            raise ValueError("orc_cp_forward failed")
+        return z
+
+    def cp_reset(self, row: int):
+        lib().orc_cp_reset(self._h, row)
+
+    def code_embed(self, j: int, code: int, d: int):
+        e = np.empty(d, np.float32)
+        if lib().orc_code_embed(self._h, j, int(code), _p(e, C.c_float)):
+            raise ValueError("bad code")
+        return e
+
+    def code_embed_sum(self, codes, d: int):
+        c = np.ascontiguousarray(codes, np.int32)
+        e = np.empty(d, np.float32)
+        if lib().orc_code_embed_sum(self._h, _p(c, C.c_int32), _p(e, C.c_float)):
+            raise ValueError("bad codes")
+        return e
+
+
+@dataclass
+class Trace:
+    """What the oracle computed over one run of one row."""
+    tokens: list = field(default_factory=list)     # sampled token (or [16] codes) per step
+    logits: list = field(default_factory=list)     # logits per step (or [16][V] per frame)
+    margins: list = field(default_factory=list)    # decision margin per sampled token
+
+
+def _sampler_args(s):
+    return dict(temperature=s.temperature, top_k=s.top_k, top_p=s.top_p, greedy=s.greedy)
+
+
+def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: int, sampler,
+           keep_logits=True) -> list:
+    """GPT-2 / Llama: prompt then n_steps free-running decode steps per row.
+
+    prompt [B][P]; draws [n_steps+1][B] (draw 0 samples the prefill's token).
+    Step i consumes the token sampled at step i-1 (the prefill's for i=0).
+    Returns one Trace per row; trace.tokens[0] is the prefill's token and
+    trace.logits[0] the logits of the last prompt position."""
+    B = prompt.shape[0]
+    V = spec.vocab
+    traces = []
+    sa = _sampler_args(sampler)
+    for b in range(B):
+        tr = Trace()
+        z = None
+        for i, tok in enumerate(prompt[b]):
+            z = model.token_forward(b, int(tok), V, want_logits=(i == prompt.shape[1] - 1))
+        for i in range(n_steps + 1):
+            tok, margin = sample(z, u=float(draws[i][b]), **sa)
+            tr.tokens.append(tok)
+            tr.margins.append(margin)
+            if keep_logits:
+                tr.logits.append(z)
+            if i < n_steps:
+                z = model.token_forward(b, tok, V)
+        traces.append(tr)
+    return traces
+
+
+def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames: int, talker_sampler,
+             cp_sampler, keep_logits=True) -> list:
+    """Talker + code predictor: prompt then frames per row.
+
+    Frame 0 is produced by the prompt: the last prompt position's Talker logits
+    give code 0 and its hidden state seeds the code predictor.  Frame f >= 1
+    runs the Talker on the sum of frame f-1's 16 code embeddings.  Within a
+    frame: code-predictor position 0 takes Pr*h_T, position 1 takes Pr*E_0[c0]
+    and head 1 samples c1; position j takes Pr*E_{j-1}[c_{j-1}] and head j
+    samples c_j.  draws [n_frames+1][B][16].  Returns one Trace per row with
+    tokens [16] per frame and logits as a list of 16 arrays per frame."""
+    B = prompt.shape[0]
+    d, V0, Vc, ncb = spec.d_model, spec.vocab, spec.cp_vocab, spec.n_codebooks
+    ta, ca = _sampler_args(talker_sampler), _sampler_args(cp_sampler)
+    traces = []
+    for b in range(B):
+        tr = Trace()
+        z0 = h = None
+        for tok in prompt[b]:
+            z0, h = model.talker_forward(b, model.talker_embed(int(tok), d), V0, d)
+        for f in range(n_frames + 1):
+            codes, zs, ms = [], [z0], []
+            c0, m0 = sample(z0, u=float(draws[f][b][0]), **ta)
+            codes.append(c0); ms.append(m0)
+            model.cp_reset(b)
+            model.cp_forward(b, h, 0, Vc)
+            for j in range(1, ncb):
+                z = model.cp_forward(b, model.code_embed(j - 1, codes[j - 1], d), j, Vc)
+                cj, mj = sample(z, u=float(draws[f][b][j]), **ca)
+                codes.append(cj); ms.append(mj); zs.append(z)
+            tr.tokens.append(codes)
+            tr.margins.append(ms)
+            if keep_logits:
+                tr.logits.append(zs)
+            if f < n_frames:
+                z0, h = model.talker_forward(b, model.code_embed_sum(codes, d), V0, d)
+        traces.append(tr)
+    return traces

@@ -1,0 +1,629 @@
+/*
+ * Oracle of the speech-token decode step -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain C restatement of the decode step of three speech-token transformers:
+ *   - GPT-2-Medium-style T3 ("Chatterbox -> ggml Port: Development Journal",
+ *     section 3.2: prompt graph and step graph sharing one KV cache);
+ *   - the Llama-style multilingual T3 (journal section 3.19: RMSNorm, SwiGLU,
+ *     separate Q/K/V projections, NEOX RoPE);
+ *   - the Qwen3-style Talker plus 15-pass code predictor ("Every Frame Is a
+ *     Memory Read", section 1).
+ * Weights are block-quantised (journal Tier A item A3, section 3.23 for the
+ * Q4_0 byte layout; the blog's section 3 for affine group-64).
+ *
+ * Nothing here is blocked, fused or reordered: each linear layer dequantises a
+ * row and takes one double-precision dot product; attention scores, softmax and
+ * the weighted value sum are plain loops.  Prefill is the same per-position
+ * routine as decode.  The only concurrency is an optional OpenMP split over
+ * independent output rows of a linear layer, which leaves every sum unchanged.
+ *
+ * Only the tests, the smoke entry and the benchmark's CPU-baseline leg load
+ * this file's library.
+ */
+#include "sd_oracle.h"
+
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
+enum { A_GPT2 = 1, A_LLAMA = 2, A_QWEN = 3 };
+
+/* ------------------------------------------------------------------ fp16 */
+
+float orc_half_to_float(uint16_t h) {
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 0x1f, man = h & 0x3ff;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)man, -24);                   /* subnormal: man * 2^-24 */
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + man), ex - 25);      /* (1 + man/1024) * 2^(ex-15) */
+    return (float)(sign ? -v : v);
+}
+
+uint16_t orc_float_to_half(float f) {
+    double a = fabs((double)f);
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    if (isnan(f)) return 0x7e00;
+    if (a >= 65520.0) return sign | 0x7c00;            /* rounds past the largest finite half */
+    if (a < ldexp(1.0, -14)) {                          /* subnormal range: units of 2^-24 */
+        double m = rint(a * ldexp(1.0, 24));            /* round half to even */
+        return sign | (uint16_t)m;                      /* m == 1024 is the smallest normal */
+    }
+    int e;
+    frexp(a, &e);                                       /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                             /* a in [2^e, 2^(e+1)) */
+    double m = rint(ldexp(a, 10 - e));                  /* in [1024, 2048] */
+    if (m == 2048.0) { m = 1024.0; e += 1; }
+    if (e + 15 >= 31) return sign | 0x7c00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)m - 1024));
+}
+
+/* ------------------------------------------------------------------ dequantisation */
+
+static void dequant_row(int kind, const uint8_t* data, int64_t r, int64_t cols, float* out) {
+    if (kind == K_Q8_0) {
+        const uint8_t* row = data + r * (cols / 32) * 34;
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 34;
+            float d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+            for (int j = 0; j < 32; ++j) out[b * 32 + j] = d * (float)(int8_t)blk[2 + j];
+        }
+    } else if (kind == K_Q4_0) {
+        const uint8_t* row = data + r * (cols / 32) * 18;
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 18;
+            float d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+            for (int j = 0; j < 32; ++j) {
+                int byte = blk[2 + (j % 16)];
+                int nib = j < 16 ? (byte & 0xf) : (byte >> 4);
+                out[b * 32 + j] = d * (float)(nib - 8);
+            }
+        }
+    }
+}
+
+typedef struct {
+    int kind;
+    int64_t rows, cols;
+    const uint8_t* data;      /* quantised codes, or fp32 values */
+    const uint16_t* scale;    /* A8G64 only */
+    const uint16_t* bias;     /* A8G64 only */
+} qmat;
+
+static void qmat_row(const qmat* W, int64_t r, float* out) {
+    if (W->kind == K_A8G64) {
+        const uint8_t* q = W->data + r * W->cols;
+        const uint16_t* s = W->scale + r * (W->cols / 64);
+        const uint16_t* b = W->bias + r * (W->cols / 64);
+        for (int64_t k = 0; k < W->cols; ++k)
+            out[k] = fmaf(orc_half_to_float(s[k / 64]), (float)q[k], orc_half_to_float(b[k / 64]));
+    } else if (W->kind == K_F32) {
+        memcpy(out, (const float*)W->data + r * W->cols, (size_t)W->cols * sizeof(float));
+    } else {
+        dequant_row(W->kind, W->data, r, W->cols, out);
+    }
+}
+
+static qmat make_qmat(int kind, const uint8_t* data, int64_t rows, int64_t cols) {
+    qmat W = {kind, rows, cols, data, NULL, NULL};
+    if (kind == K_A8G64) {
+        W.scale = (const uint16_t*)(data + rows * cols);
+        W.bias = W.scale + rows * (cols / 64);
+    }
+    return W;
+}
+
+int orc_dequant(int kind, const uint8_t* data, int64_t rows, int64_t cols, float* out) {
+    if (kind < K_Q8_0 || kind > K_A8G64 || cols % (kind == K_A8G64 ? 64 : 32)) return -1;
+    qmat W = make_qmat(kind, data, rows, cols);
+    for (int64_t r = 0; r < rows; ++r) qmat_row(&W, r, out + r * cols);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ linear */
+
+static int g_threads = 1;
+
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+    g_threads = n > 0 ? n : 1;
+    return g_threads;
+#else
+    (void)n;
+    g_threads = 1;
+    return 1;
+#endif
+}
+
+static void linear_q(const qmat* W, const float* x, const float* bias, float* y) {
+    int64_t rows = W->rows, cols = W->cols;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(g_threads)
+#endif
+    {
+        float* w = (float*)malloc((size_t)cols * sizeof(float));
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int64_t r = 0; r < rows; ++r) {
+            qmat_row(W, r, w);
+            double acc = 0.0;
+            for (int64_t k = 0; k < cols; ++k) acc += (double)w[k] * (double)x[k];
+            if (bias) acc += (double)bias[r];
+            y[r] = (float)acc;
+        }
+        free(w);
+    }
+}
+
+int orc_linear(int kind, const uint8_t* data, int64_t rows, int64_t cols,
+               const float* x, const float* b, float* y) {
+    if (kind < K_F32 || kind > K_A8G64) return -1;
+    qmat W = make_qmat(kind, data, rows, cols);
+    linear_q(&W, x, b, y);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ elementwise */
+
+void orc_layernorm(const float* x, int n, const float* g, const float* b, float eps, float* out) {
+    double mu = 0.0, var = 0.0;
+    for (int i = 0; i < n; ++i) mu += x[i];
+    mu /= n;
+    for (int i = 0; i < n; ++i) var += ((double)x[i] - mu) * ((double)x[i] - mu);
+    var /= n;                                       /* biased variance */
+    double r = 1.0 / sqrt(var + (double)eps);
+    for (int i = 0; i < n; ++i) out[i] = (float)(((double)x[i] - mu) * r * (double)g[i] + (double)b[i]);
+}
+
+void orc_rmsnorm(const float* x, int n, const float* g, float eps, float* out) {
+    double ms = 0.0;
+    for (int i = 0; i < n; ++i) ms += (double)x[i] * (double)x[i];
+    ms /= n;
+    double r = 1.0 / sqrt(ms + (double)eps);
+    for (int i = 0; i < n; ++i) out[i] = (float)((double)x[i] * r * (double)g[i]);
+}
+
+float orc_gelu_tanh(float t) {
+    double x = t;
+    return (float)(0.5 * x * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (x + 0.044715 * x * x * x))));
+}
+
+float orc_silu(float t) {
+    double x = t;
+    return (float)(x / (1.0 + exp(-x)));
+}
+
+void orc_rope(float* x, int hd, int pos, float theta) {
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double freq = pow((double)theta, -2.0 * i / hd);
+        double phi = (double)pos * freq;
+        double c = cos(phi), s = sin(phi);
+        double a = x[i], b = x[i + half];
+        x[i] = (float)(a * c - b * s);
+        x[i + half] = (float)(a * s + b * c);
+    }
+}
+
+void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int hd, float* out) {
+    double* s = (double*)malloc((size_t)n * sizeof(double));
+    double scale = 1.0 / sqrt((double)hd);
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < hd; ++d) acc += (double)q[d] * (double)orc_half_to_float(k[(size_t)j * hd + d]);
+        s[j] = acc * scale;
+        if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) { s[j] = exp(s[j] - m); z += s[j]; }
+    for (int d = 0; d < hd; ++d) {
+        double acc = 0.0;
+        for (int j = 0; j < n; ++j) acc += s[j] * (double)orc_half_to_float(v[(size_t)j * hd + d]);
+        out[d] = (float)(acc / z);
+    }
+    free(s);
+}
+
+/* ------------------------------------------------------------------ sampler */
+
+typedef struct { double z; int32_t i; } zi;
+
+static int cmp_desc(const void* a, const void* b) {
+    const zi* x = (const zi*)a; const zi* y = (const zi*)b;
+    if (x->z > y->z) return -1;
+    if (x->z < y->z) return 1;
+    return (x->i > y->i) - (x->i < y->i);           /* ties: lower index first */
+}
+
+int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
+                   int32_t greedy, double u, double* margin) {
+    if (V <= 0) return -1;
+    if (greedy || top_k == 1 || temperature <= 0.0f) {
+        int32_t best = 0;
+        for (int32_t i = 1; i < V; ++i) if (z[i] > z[best]) best = i;
+        double second = -INFINITY;
+        for (int32_t i = 0; i < V; ++i) if (i != best && (double)z[i] > second) second = z[i];
+        if (margin) *margin = V > 1 ? (double)z[best] - second : INFINITY;
+        return best;
+    }
+    double inv_t = 1.0 / (double)temperature;
+    zi* s = (zi*)malloc((size_t)V * sizeof(zi));
+    for (int32_t i = 0; i < V; ++i) { s[i].z = (double)z[i] * inv_t; s[i].i = i; }
+    qsort(s, (size_t)V, sizeof(zi), cmp_desc);
+    /* top-k: keep every value >= the k-th largest (ties at the threshold kept) */
+    int32_t k = top_k < 1 || top_k > V ? V : top_k;
+    double thr = s[k - 1].z;
+    double m_k = k < V ? s[k - 1].z - s[k].z : INFINITY;
+    int32_t n_keep = 0;
+    while (n_keep < V && s[n_keep].z >= thr) ++n_keep;
+    /* softmax over the survivors (s is already in (p desc, index asc) order) */
+    double zmax = s[0].z, Z = 0.0;
+    double* p = (double*)malloc((size_t)V * sizeof(double));  /* indexed by vocabulary id */
+    char* in_s = (char*)calloc((size_t)V, 1);
+    for (int32_t t = 0; t < n_keep; ++t) p[s[t].i] = exp(s[t].z - zmax);
+    for (int32_t t = 0; t < n_keep; ++t) in_s[s[t].i] = 1;
+    for (int32_t i = 0; i < V; ++i) if (in_s[i]) Z += p[i];
+    /* top-p: the shortest (p desc, index asc) prefix whose cumulative mass >= top_p */
+    double m_p = INFINITY;
+    if (top_p < 1.0f) {
+        double cum = 0.0, prev = 0.0;
+        int32_t cut = n_keep - 1;
+        for (int32_t t = 0; t < n_keep; ++t) {
+            prev = cum;
+            cum += p[s[t].i] / Z;
+            if (cum >= (double)top_p) { cut = t; break; }
+        }
+        m_p = fabs(cum - (double)top_p);
+        if (cut > 0 && fabs((double)top_p - prev) < m_p) m_p = fabs((double)top_p - prev);
+        for (int32_t t = cut + 1; t < n_keep; ++t) in_s[s[t].i] = 0;
+    }
+    /* draw in vocabulary order */
+    double zs = 0.0;
+    for (int32_t i = 0; i < V; ++i) if (in_s[i]) zs += p[i];
+    double target = u * zs, c = 0.0, c_lo = 0.0;
+    int32_t tok = -1, last = -1;
+    for (int32_t i = 0; i < V; ++i) {
+        if (!in_s[i]) continue;
+        last = i;
+        c_lo = c;
+        c += p[i];
+        if (c > target) { tok = i; break; }
+    }
+    if (tok < 0) { tok = last; c_lo = c - p[last]; }
+    double m_u = fmin(target - c_lo, c - target) / zs;
+    if (margin) *margin = fmin(m_u, fmin(m_k, m_p));
+    free(s); free(p); free(in_s);
+    return tok;
+}
+
+/* ------------------------------------------------------------------ blob */
+
+#define BLOB_MAGIC 0x31574453u
+#define ENTRY_BYTES 96
+
+typedef struct {
+    char name[64];
+    uint32_t kind, rows, cols;
+    const uint8_t* data;
+    uint64_t nbytes;
+} otensor;
+
+typedef struct {
+    int32_t arch, n_layer, d_model, n_head, n_kv_head, head_dim, d_ff, vocab, max_ctx, batch, quant;
+    float rope_theta, norm_eps;
+    int32_t cp_layer, cp_d_model, cp_n_head, cp_n_kv_head, cp_head_dim, cp_d_ff, cp_vocab, n_codebooks, cp_max_ctx;
+} ocfg;
+
+typedef struct {
+    const float *n1g, *n1b, *bqkv, *bo, *n2g, *n2b, *bfc, *bproj;
+    qmat wqkv, wo, wfc, wproj;     /* wfc = stacked gate/up and wproj = down for SwiGLU stacks */
+} olayer;
+
+typedef struct {
+    int gpt2;                      /* LayerNorm + biases + GELU, else RMSNorm + SwiGLU + RoPE */
+    int n_layer, d, n_head, n_kv, hd, ff, max_ctx, batch;
+    float eps, theta;
+    olayer* L;
+    const float *nfg, *nfb;
+    uint16_t *kc, *vc;             /* [batch][layer][kv_head][max_ctx][hd] fp16 */
+    int32_t* pos;                  /* [batch] */
+    float *x, *h, *qkv, *o, *t, *u, *y;  /* scratch */
+} ostack;
+
+struct orc_model {
+    ocfg c;
+    uint32_t n_t;
+    otensor* t;
+    ostack s, cp;
+    const float *wte, *wpe;
+    qmat head, cp_proj;
+    const float* emb[16];
+    qmat cp_head[16];
+};
+
+static const otensor* find(const orc_model* m, const char* name) {
+    for (uint32_t i = 0; i < m->n_t; ++i)
+        if (strcmp(m->t[i].name, name) == 0) return &m->t[i];
+    return NULL;
+}
+
+static int get_f32(const orc_model* m, const char* name, int64_t n, const float** out) {
+    const otensor* t = find(m, name);
+    if (!t || t->kind != K_F32 || (int64_t)t->rows * t->cols != n) {
+        fprintf(stderr, "oracle: missing or mis-shaped fp32 tensor %s\n", name);
+        return -1;
+    }
+    *out = (const float*)t->data;
+    return 0;
+}
+
+static int get_q(const orc_model* m, const char* name, int64_t rows, int64_t cols, qmat* out) {
+    const otensor* t = find(m, name);
+    if (!t || t->kind == K_F32 || t->rows != rows || t->cols != cols) {
+        fprintf(stderr, "oracle: missing or mis-shaped matrix %s\n", name);
+        return -1;
+    }
+    *out = make_qmat((int)t->kind, t->data, rows, cols);
+    return 0;
+}
+
+static uint32_t rd32(const uint8_t* p) { return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24); }
+static uint64_t rd64(const uint8_t* p) { return (uint64_t)rd32(p) | ((uint64_t)rd32(p + 4) << 32); }
+
+static int stack_alloc(ostack* s) {
+    size_t kv = (size_t)s->batch * s->n_layer * s->n_kv * s->max_ctx * s->hd;
+    int qkv_rows = (s->n_head + 2 * s->n_kv) * s->hd;
+    int wide = s->ff * 2 > qkv_rows ? s->ff * 2 : qkv_rows;
+    s->kc = (uint16_t*)calloc(kv, 2);
+    s->vc = (uint16_t*)calloc(kv, 2);
+    s->pos = (int32_t*)calloc((size_t)s->batch, 4);
+    s->x = (float*)calloc((size_t)s->d, 4);
+    s->h = (float*)calloc((size_t)s->d, 4);
+    s->qkv = (float*)calloc((size_t)wide, 4);
+    s->o = (float*)calloc((size_t)s->n_head * s->hd, 4);
+    s->t = (float*)calloc((size_t)wide, 4);
+    s->u = (float*)calloc((size_t)s->ff, 4);
+    s->y = (float*)calloc((size_t)(s->d > s->ff ? s->d : s->ff), 4);
+    return (s->kc && s->vc && s->pos && s->x && s->h && s->qkv && s->o && s->t && s->u && s->y) ? 0 : -1;
+}
+
+static void stack_free(ostack* s) {
+    free(s->L); free(s->kc); free(s->vc); free(s->pos);
+    free(s->x); free(s->h); free(s->qkv); free(s->o); free(s->t); free(s->u); free(s->y);
+}
+
+static int load_layers(orc_model* m, ostack* s, const char* pfx) {
+    char nm[96];
+    int d = s->d, qd = s->n_head * s->hd, qkv_rows = (s->n_head + 2 * s->n_kv) * s->hd;
+    s->L = (olayer*)calloc((size_t)s->n_layer, sizeof(olayer));
+    for (int l = 0; l < s->n_layer; ++l) {
+        olayer* L = &s->L[l];
+        int rc = 0;
+#define F32(field, suffix, n) snprintf(nm, sizeof nm, "%s%d." suffix, pfx, l); rc |= get_f32(m, nm, n, &L->field)
+#define QM(field, suffix, r, c) snprintf(nm, sizeof nm, "%s%d." suffix, pfx, l); rc |= get_q(m, nm, r, c, &L->field)
+        if (s->gpt2) {
+            F32(n1g, "ln1.g", d); F32(n1b, "ln1.b", d);
+            QM(wqkv, "wqkv", qkv_rows, d); F32(bqkv, "bqkv", qkv_rows);
+            QM(wo, "wo", d, qd); F32(bo, "bo", d);
+            F32(n2g, "ln2.g", d); F32(n2b, "ln2.b", d);
+            QM(wfc, "wfc", s->ff, d); F32(bfc, "bfc", s->ff);
+            QM(wproj, "wproj", d, s->ff); F32(bproj, "bproj", d);
+        } else {
+            F32(n1g, "rms1.g", d); QM(wqkv, "wqkv", qkv_rows, d); QM(wo, "wo", d, qd);
+            F32(n2g, "rms2.g", d); QM(wfc, "wgu", 2 * s->ff, d); QM(wproj, "wdown", d, s->ff);
+        }
+#undef F32
+#undef QM
+        if (rc) return -1;
+    }
+    return stack_alloc(s);
+}
+
+int orc_open(const uint8_t* blob, uint64_t nbytes, orc_model** out) {
+    *out = NULL;
+    if (nbytes < 144 || rd32(blob) != BLOB_MAGIC || rd32(blob + 4) != 1) return -1;
+    orc_model* m = (orc_model*)calloc(1, sizeof(orc_model));
+    memcpy(&m->c, blob + 16, sizeof(ocfg));
+    m->n_t = rd32(blob + 8);
+    uint32_t toff = rd32(blob + 12);
+    if (toff + (uint64_t)m->n_t * ENTRY_BYTES > nbytes) { free(m); return -1; }
+    m->t = (otensor*)calloc(m->n_t, sizeof(otensor));
+    for (uint32_t i = 0; i < m->n_t; ++i) {
+        const uint8_t* e = blob + toff + (uint64_t)i * ENTRY_BYTES;
+        memcpy(m->t[i].name, e, 63);
+        m->t[i].kind = rd32(e + 64); m->t[i].rows = rd32(e + 68); m->t[i].cols = rd32(e + 72);
+        uint64_t off = rd64(e + 80), nb = rd64(e + 88);
+        if (off + nb > nbytes) { orc_close(m); return -1; }
+        m->t[i].data = blob + off; m->t[i].nbytes = nb;
+    }
+    ocfg* c = &m->c;
+    ostack* s = &m->s;
+    s->gpt2 = c->arch == A_GPT2;
+    s->n_layer = c->n_layer; s->d = c->d_model; s->n_head = c->n_head; s->n_kv = c->n_kv_head;
+    s->hd = c->head_dim; s->ff = c->d_ff; s->max_ctx = c->max_ctx; s->batch = c->batch;
+    s->eps = c->norm_eps; s->theta = c->rope_theta;
+    int rc = 0;
+    if (c->arch == A_GPT2) {
+        rc |= get_f32(m, "wte", (int64_t)c->vocab * c->d_model, &m->wte);
+        rc |= get_f32(m, "wpe", (int64_t)c->max_ctx * c->d_model, &m->wpe);
+        rc |= load_layers(m, s, "l");
+        rc |= get_f32(m, "lnf.g", c->d_model, &s->nfg) | get_f32(m, "lnf.b", c->d_model, &s->nfb);
+        rc |= get_q(m, "whead", c->vocab, c->d_model, &m->head);
+    } else if (c->arch == A_LLAMA) {
+        rc |= get_f32(m, "wte", (int64_t)c->vocab * c->d_model, &m->wte);
+        rc |= load_layers(m, s, "l");
+        rc |= get_f32(m, "normf.g", c->d_model, &s->nfg);
+        rc |= get_q(m, "whead", c->vocab, c->d_model, &m->head);
+    } else if (c->arch == A_QWEN) {
+        char nm[64];
+        if (c->n_codebooks < 2 || c->n_codebooks > 16) rc = -1;
+        for (int j = 0; j < c->n_codebooks && !rc; ++j) {
+            snprintf(nm, sizeof nm, "emb.%d", j);
+            rc |= get_f32(m, nm, (int64_t)(j ? c->cp_vocab : c->vocab) * c->d_model, &m->emb[j]);
+        }
+        rc |= load_layers(m, s, "t");
+        rc |= get_f32(m, "t.normf.g", c->d_model, &s->nfg);
+        rc |= get_q(m, "t.head", c->vocab, c->d_model, &m->head);
+        rc |= get_q(m, "cp.proj", c->cp_d_model, c->d_model, &m->cp_proj);
+        ostack* p = &m->cp;
+        p->gpt2 = 0;
+        p->n_layer = c->cp_layer; p->d = c->cp_d_model; p->n_head = c->cp_n_head; p->n_kv = c->cp_n_kv_head;
+        p->hd = c->cp_head_dim; p->ff = c->cp_d_ff; p->max_ctx = c->cp_max_ctx; p->batch = c->batch;
+        p->eps = c->norm_eps; p->theta = c->rope_theta;
+        rc |= load_layers(m, p, "c");
+        rc |= get_f32(m, "cp.normf.g", c->cp_d_model, &p->nfg);
+        for (int j = 1; j < c->n_codebooks && !rc; ++j) {
+            snprintf(nm, sizeof nm, "cp.head.%d", j);
+            rc |= get_q(m, nm, c->cp_vocab, c->cp_d_model, &m->cp_head[j]);
+        }
+    } else {
+        rc = -1;
+    }
+    if (rc) { orc_close(m); return -1; }
+    *out = m;
+    return 0;
+}
+
+void orc_close(orc_model* m) {
+    if (!m) return;
+    stack_free(&m->s);
+    stack_free(&m->cp);
+    free(m->t);
+    free(m);
+}
+
+void orc_reset(orc_model* m) {
+    for (int b = 0; b < m->s.batch; ++b) m->s.pos[b] = 0;
+    if (m->cp.pos) for (int b = 0; b < m->cp.batch; ++b) m->cp.pos[b] = 0;
+}
+
+int orc_pos(const orc_model* m, int row) { return m->s.pos[row]; }
+
+/* ------------------------------------------------------------------ one transformer position */
+
+/* Runs the stack on input x (d floats, overwritten) at the row's next position
+ * and leaves the final-normed hidden state in s->h.  Returns -1 when full. */
+static int stack_forward(ostack* s, int row, float* x) {
+    int pos = s->pos[row];
+    if (pos >= s->max_ctx) return -1;
+    int d = s->d, hd = s->hd, H = s->n_head, Hk = s->n_kv, qd = H * hd, kd = Hk * hd;
+    for (int l = 0; l < s->n_layer; ++l) {
+        olayer* L = &s->L[l];
+        /* attention block */
+        if (s->gpt2) orc_layernorm(x, d, L->n1g, L->n1b, s->eps, s->h);
+        else orc_rmsnorm(x, d, L->n1g, s->eps, s->h);
+        linear_q(&L->wqkv, s->h, s->gpt2 ? L->bqkv : NULL, s->qkv);
+        float *q = s->qkv, *k = s->qkv + qd, *v = s->qkv + qd + kd;
+        if (!s->gpt2) {
+            for (int h = 0; h < H; ++h) orc_rope(q + h * hd, hd, pos, s->theta);
+            for (int h = 0; h < Hk; ++h) orc_rope(k + h * hd, hd, pos, s->theta);
+        }
+        size_t layer_base = ((size_t)row * s->n_layer + l) * Hk;
+        for (int g = 0; g < Hk; ++g) {
+            size_t base = ((layer_base + g) * s->max_ctx + pos) * hd;
+            for (int i = 0; i < hd; ++i) {
+                s->kc[base + i] = orc_float_to_half(k[g * hd + i]);
+                s->vc[base + i] = orc_float_to_half(v[g * hd + i]);
+            }
+        }
+        for (int h = 0; h < H; ++h) {
+            int g = h / (H / Hk);                   /* contiguous query-head groups */
+            size_t base = (layer_base + g) * s->max_ctx * hd;
+            orc_attend(q + h * hd, s->kc + base, s->vc + base, pos + 1, hd, s->o + h * hd);
+        }
+        linear_q(&L->wo, s->o, s->gpt2 ? L->bo : NULL, s->y);
+        for (int i = 0; i < d; ++i) x[i] = (float)((double)x[i] + (double)s->y[i]);
+        /* MLP block */
+        if (s->gpt2) {
+            orc_layernorm(x, d, L->n2g, L->n2b, s->eps, s->h);
+            linear_q(&L->wfc, s->h, L->bfc, s->t);
+            for (int i = 0; i < s->ff; ++i) s->u[i] = orc_gelu_tanh(s->t[i]);
+        } else {
+            orc_rmsnorm(x, d, L->n2g, s->eps, s->h);
+            linear_q(&L->wfc, s->h, NULL, s->t);    /* rows [0, ff) gate, [ff, 2ff) up */
+            for (int i = 0; i < s->ff; ++i)
+                s->u[i] = (float)((double)orc_silu(s->t[i]) * (double)s->t[s->ff + i]);
+        }
+        linear_q(&L->wproj, s->u, s->gpt2 ? L->bproj : NULL, s->y);
+        for (int i = 0; i < d; ++i) x[i] = (float)((double)x[i] + (double)s->y[i]);
+    }
+    if (s->gpt2) orc_layernorm(x, d, s->nfg, s->nfb, s->eps, s->h);
+    else orc_rmsnorm(x, d, s->nfg, s->eps, s->h);
+    s->pos[row] = pos + 1;
+    return 0;
+}
+
+int orc_token_forward(orc_model* m, int row, int32_t tok, float* logits) {
+    ostack* s = &m->s;
+    if (m->c.arch == A_QWEN || row < 0 || row >= s->batch || tok < 0 || tok >= m->c.vocab) return -1;
+    int pos = s->pos[row], d = s->d;
+    if (pos >= s->max_ctx) return -1;
+    for (int i = 0; i < d; ++i) {
+        float e = m->wte[(size_t)tok * d + i];
+        s->x[i] = m->c.arch == A_GPT2 ? e + m->wpe[(size_t)pos * d + i] : e;
+    }
+    if (stack_forward(s, row, s->x)) return -1;
+    if (logits) linear_q(&m->head, s->h, NULL, logits);
+    return 0;
+}
+
+int orc_talker_embed(orc_model* m, int32_t tok, float* e) {
+    if (m->c.arch != A_QWEN || tok < 0 || tok >= m->c.vocab) return -1;
+    memcpy(e, m->emb[0] + (size_t)tok * m->c.d_model, (size_t)m->c.d_model * 4);
+    return 0;
+}
+
+int orc_talker_forward(orc_model* m, int row, const float* e, float* logits0, float* hidden) {
+    ostack* s = &m->s;
+    if (m->c.arch != A_QWEN || row < 0 || row >= s->batch) return -1;
+    memcpy(s->x, e, (size_t)s->d * 4);
+    if (stack_forward(s, row, s->x)) return -1;
+    if (logits0) linear_q(&m->head, s->h, NULL, logits0);
+    if (hidden) memcpy(hidden, s->h, (size_t)s->d * 4);
+    return 0;
+}
+
+int orc_cp_forward(orc_model* m, int row, const float* v, int head, float* logits) {
+    ostack* p = &m->cp;
+    if (m->c.arch != A_QWEN || row < 0 || row >= p->batch || head >= m->c.n_codebooks) return -1;
+    linear_q(&m->cp_proj, v, NULL, p->x);
+    if (stack_forward(p, row, p->x)) return -1;
+    if (head >= 1 && logits) linear_q(&m->cp_head[head], p->h, NULL, logits);
+    return 0;
+}
+
+void orc_cp_reset(orc_model* m, int row) {
+    if (m->cp.pos && row >= 0 && row < m->cp.batch) m->cp.pos[row] = 0;
+}
+
+int orc_code_embed(orc_model* m, int j, int32_t code, float* out) {
+    if (m->c.arch != A_QWEN || j < 0 || j >= m->c.n_codebooks) return -1;
+    int32_t V = j ? m->c.cp_vocab : m->c.vocab;
+    if (code < 0 || code >= V) return -1;
+    memcpy(out, m->emb[j] + (size_t)code * m->c.d_model, (size_t)m->c.d_model * 4);
+    return 0;
+}
+
+int orc_code_embed_sum(orc_model* m, const int32_t* codes, float* e) {
+    if (m->c.arch != A_QWEN) return -1;
+    int d = m->c.d_model;
+    for (int j = 0; j < m->c.n_codebooks; ++j) {
+        int32_t V = j ? m->c.cp_vocab : m->c.vocab;
+        if (codes[j] < 0 || codes[j] >= V) return -1;
+    }
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < m->c.n_codebooks; ++j) acc += (double)m->emb[j][(size_t)codes[j] * d + i];
+        e[i] = (float)acc;
+    }
+    return 0;
+}

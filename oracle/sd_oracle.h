@@ -1,0 +1,79 @@
+/*
+ * Oracle of the speech-token decode step -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-pass CPU restatement of what one decode step of the
+ * GPT-2-style T3, the Llama-style T3 and the Qwen3-style Talker + code
+ * predictor computes, used to check the CUDA library.  Only the tests, the
+ * package's smoke entry and the CPU-baseline leg of the benchmark may load it;
+ * the product path never does.  It shares no source with the CUDA library.
+ *
+ * Arithmetic convention: every activation is stored as fp32 after each
+ * operation; every reduction (dot products, norm statistics, softmax sums,
+ * attention) accumulates in double and is rounded once; transcendental
+ * functions are the C library's double versions.  The KV cache holds fp16
+ * (round-to-nearest-even) values, widened to double when read.
+ */
+#ifndef SD_ORACLE_H
+#define SD_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct orc_model orc_model;
+
+/* fp16 <-> fp32 conversions written from the IEEE 754 binary16 definition. */
+float    orc_half_to_float(uint16_t h);
+uint16_t orc_float_to_half(float f);
+
+/* Dequantise rows x cols weights stored in blob kind `kind` (1 Q8_0, 2 Q4_0,
+ * 3 A8G64) to fp32. */
+int orc_dequant(int kind, const uint8_t* data, int64_t rows, int64_t cols, float* out);
+
+/* y[r] = fp32( sum_k w[r][k] * x[k] (+ b[r]) ), the sum in double. b may be NULL. */
+int orc_linear(int kind, const uint8_t* data, int64_t rows, int64_t cols,
+               const float* x, const float* b, float* y);
+
+void orc_layernorm(const float* x, int n, const float* g, const float* b, float eps, float* out);
+void orc_rmsnorm(const float* x, int n, const float* g, float eps, float* out);
+float orc_gelu_tanh(float t);
+float orc_silu(float t);
+/* NEOX (half-split) rotary embedding of one head vector, in place. */
+void orc_rope(float* x, int hd, int pos, float theta);
+/* One query against n cached fp16 keys/values (stride hd): softmax(q.K/sqrt(hd)) V. */
+void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int hd, float* out);
+
+/* Sampler: temperature -> top-k -> top-p -> draw in vocabulary order with u.
+ * margin (may be NULL) receives the decision margin. */
+int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
+                   int32_t greedy, double u, double* margin);
+
+/* Model.  The blob must outlive the model. */
+int  orc_open(const uint8_t* blob, uint64_t nbytes, orc_model** out);
+void orc_close(orc_model* m);
+void orc_reset(orc_model* m);
+int  orc_set_threads(int n);
+int  orc_pos(const orc_model* m, int row);
+
+/* GPT-2 / Llama: process token `tok` at row `row`'s next position; logits may be NULL. */
+int orc_token_forward(orc_model* m, int row, int32_t tok, float* logits);
+
+/* Qwen Talker: process input vector e (d_model) at the row's next Talker
+ * position; logits0 (codebook-0 vocab) and hidden (final-normed state) may be NULL. */
+int orc_talker_forward(orc_model* m, int row, const float* e, float* logits0, float* hidden);
+/* Talker input for a prompt token: row `tok` of the codebook-0 embedding. */
+int orc_talker_embed(orc_model* m, int32_t tok, float* e);
+/* Code predictor: project v (Talker width) with Pr, run the CP stack at the
+ * row's next CP position, and if head >= 1 write head `head`'s logits. */
+int orc_cp_forward(orc_model* m, int row, const float* v, int head, float* logits);
+void orc_cp_reset(orc_model* m, int row);
+/* Row `code` of codebook j's embedding (Talker width). */
+int orc_code_embed(orc_model* m, int j, int32_t code, float* out);
+/* e = sum_{j=0..n_codebooks-1} E_j[codes[j]], summed in j order in double, rounded once. */
+int orc_code_embed_sum(orc_model* m, const int32_t* codes, float* e);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,144 @@
+"""Whole-forward pins of the oracle: its incremental KV-cache decode against an
+independent full causal recompute in torch float64 (tests/torch_ref.py), on
+small GPT-2, Llama (with grouped KV heads) and Talker + code-predictor models,
+plus closed-form special cases."""
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from synth import get_preset, uniform_draws, prompt_tokens
+from synth import presets as P
+from synth.presets import SamplerSpec
+from synth.weights import build_model_blob
+from tests import torch_ref
+
+TOL = 2e-5   # fp32 rounding noise, relative to the largest logit magnitude
+
+
+def _rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return np.max(np.abs(a - b)) / np.max(np.abs(b))
+
+
+def _small_llama():
+    return P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=2, d_model=256, n_head=4, n_kv_head=2, head_dim=64,
+                       d_ff=512, vocab=300, max_ctx=64, batch=2, quant=P.Q4_0)
+
+
+def _small_qwen():
+    return P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=256, n_head=4, n_kv_head=2, head_dim=64,
+                       d_ff=512, vocab=128, max_ctx=64, batch=1, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=128, cp_n_head=2, cp_n_kv_head=2, cp_head_dim=64,
+                       cp_d_ff=256, cp_vocab=64, n_codebooks=16, cp_max_ctx=16)
+
+
+def test_tiny_gpt2_incremental_equals_full_recompute():
+    run = get_preset("tiny")
+    m = run.model
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    prompt = prompt_tokens(run)
+    n = 16
+    draws = uniform_draws(run.draw_seed, n + 1, 1)[..., 0]
+    tr = oracle.run_t3(model, m, prompt, draws, n, run.sampler)[0]
+    seq = list(prompt[0]) + tr.tokens[:n]
+    ref = torch_ref.t3_logits(blob, m, seq)
+    P_ = prompt.shape[1]
+    for i in range(n + 1):
+        assert _rel(tr.logits[i], ref[P_ - 1 + i]) < TOL, i
+    # greedy tokens are the argmax of the recomputed logits wherever the margin is clear
+    for i in range(n + 1):
+        if tr.margins[i] > 1e-4:
+            assert tr.tokens[i] == int(np.argmax(ref[P_ - 1 + i]))
+
+
+def test_q4_gpt2_sampled_run_matches_recompute():
+    run = get_preset("tiny").with_model(quant=P.Q4_0, n_layer=1)
+    m = run.model
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    prompt = prompt_tokens(run)[:, :10]
+    n = 8
+    draws = uniform_draws(3, n + 1, 1)[..., 0]
+    s = SamplerSpec(temperature=0.8, top_k=1000, top_p=0.95, greedy=False)
+    tr = oracle.run_t3(model, m, prompt, draws, n, s)[0]
+    ref = torch_ref.t3_logits(blob, m, list(prompt[0]) + tr.tokens[:n])
+    for i in range(n + 1):
+        assert _rel(tr.logits[i], ref[9 + i]) < TOL
+
+
+def test_llama_gqa_rows_match_full_recompute():
+    m = _small_llama()
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    rng = np.random.default_rng(5)
+    prompt = rng.integers(0, m.vocab, size=(2, 12)).astype(np.int32)
+    n = 10
+    draws = uniform_draws(3, n + 1, 2)[..., 0]
+    s = SamplerSpec(temperature=0.8, top_k=50, top_p=0.9, greedy=False)
+    trs = oracle.run_t3(model, m, prompt, draws, n, s)
+    for b in range(2):
+        ref = torch_ref.t3_logits(blob, m, list(prompt[b]) + trs[b].tokens[:n])
+        for i in range(n + 1):
+            assert _rel(trs[b].logits[i], ref[11 + i]) < TOL, (b, i)
+
+
+def test_qwen_frames_match_full_recompute():
+    m = _small_qwen()
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    prompt = np.random.default_rng(6).integers(0, m.vocab, size=(1, 9)).astype(np.int32)
+    nf = 3
+    draws = uniform_draws(3, nf + 1, 1, 16)
+    s = SamplerSpec(temperature=0.9, top_k=50, top_p=0.95, greedy=False)
+    tr = oracle.run_qwen(model, m, prompt, draws, nf, s, s)[0]
+    ref = torch_ref.qwen_frame_logits(blob, m, prompt[0], tr.tokens)
+    for f in range(nf + 1):
+        for j in range(16):
+            assert _rel(tr.logits[f][j], ref[f][j]) < TOL, (f, j)
+
+
+def test_zero_layer_model_is_head_of_norm_of_embedding():
+    m = P.ModelSpec(arch=P.ARCH_GPT2, n_layer=0, d_model=128, n_head=2, n_kv_head=2, head_dim=64,
+                    d_ff=256, vocab=200, max_ctx=16, batch=1, quant=P.Q8_0)
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    W = torch_ref.Weights(blob)
+    for pos, tok in enumerate([5, 199, 0]):
+        z = model.token_forward(0, tok, m.vocab)
+        x = (W.get("wte")[tok].float() + W.get("wpe")[pos].float()).double()
+        h = F.layer_norm(x, (128,), W.vec("lnf.g"), W.vec("lnf.b"), eps=1e-5).float().double()
+        ref = (h @ W.get("whead").T).numpy()
+        assert _rel(z, ref) < 1e-6
+
+
+def test_threads_do_not_change_results():
+    run = get_preset("tiny")
+    blob, _ = build_model_blob(run.model)
+    prompt = prompt_tokens(run)[:, :6]
+    out = []
+    for th in (1, 4):
+        model = oracle.Model(blob, threads=th)
+        z = None
+        for t in prompt[0]:
+            z = model.token_forward(0, int(t), run.model.vocab)
+        out.append(z)
+    assert np.array_equal(out[0], out[1])
+
+
+def test_context_full_and_bad_token_rejected():
+    m = P.ModelSpec(arch=P.ARCH_GPT2, n_layer=1, d_model=64, n_head=1, n_kv_head=1, head_dim=64,
+                    d_ff=128, vocab=50, max_ctx=3, batch=1, quant=P.Q8_0)
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    with pytest.raises(ValueError):
+        model.token_forward(0, 50, 50)
+    for t in range(3):
+        model.token_forward(0, t, 50)
+    with pytest.raises(ValueError):
+        model.token_forward(0, 1, 50)
+    model.reset()
+    assert model.pos(0) == 0

@@ -1,0 +1,345 @@
+"""Pins of the oracle's operations against things other than itself:
+library routines (numpy fp16 conversion, torch float64 functional ops),
+closed forms, hand-built blocks with known values, invariants and brute force."""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64
+
+KQ8, KQ4, KA8 = 1, 2, 3
+
+
+# ----------------------------------------------------------------------------- fp16
+
+def test_fp16_conversions_match_numpy():
+    rng = np.random.default_rng(0)
+    special = np.array([0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 1e9, -1e9, 6.1035156e-05,
+                        6.0975552e-05, 5.9604645e-08, 2.9802322e-08, 2.98023259e-08, 1e-10, 0.1, 1 / 3,
+                        2049.0, 2051.0, 2050.0, 1.00048828125, 1.000732421875], np.float32)
+    x = np.concatenate([special, rng.standard_normal(4000).astype(np.float32) * 3,
+                        rng.standard_normal(2000).astype(np.float32) * 1e-5,
+                        rng.standard_normal(500).astype(np.float32) * 3e4])
+    got = oracle.float_to_half(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+    allh = np.arange(0, 65536, dtype=np.uint16)
+    allh = allh[~np.isnan(allh.view(np.float16))]
+    back = oracle.half_to_float(allh)
+    assert np.array_equal(back.view(np.uint32), allh.view(np.float16).astype(np.float32).view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- dequantisation
+
+def test_q4_0_hand_block():
+    """Block with d = 0.25 and byte j = j | (15-j) << 4: element j (j<16) is
+    0.25*(j-8) and element 16+j is 0.25*(7-j) (nibble order of the Q4_0 block)."""
+    blk = np.zeros(18, np.uint8)
+    blk[0:2] = np.array([0.25], np.float16).view(np.uint8)
+    for j in range(16):
+        blk[2 + j] = j | ((15 - j) << 4)
+    out = oracle.dequant(KQ4, blk, 1, 32)[0]
+    exp = np.array([0.25 * (j - 8) for j in range(16)] + [0.25 * (7 - j) for j in range(16)], np.float32)
+    assert np.array_equal(out, exp)
+
+
+def test_q8_0_hand_block():
+    blk = np.zeros(34, np.uint8)
+    blk[0:2] = np.array([-0.5], np.float16).view(np.uint8)
+    codes = np.arange(-16, 16, dtype=np.int8) * 4 + 3
+    blk[2:] = codes.view(np.uint8)
+    out = oracle.dequant(KQ8, blk, 1, 32)[0]
+    assert np.array_equal(out, (-0.5 * codes.astype(np.float32)).astype(np.float32))
+
+
+def test_a8g64_hand_group():
+    q = np.arange(64, dtype=np.uint8) * 4
+    scale = np.array([0.125], np.float16)
+    bias = np.array([-3.0], np.float16)
+    data = np.concatenate([q, scale.view(np.uint8), bias.view(np.uint8)])
+    out = oracle.dequant(KA8, data, 1, 64)[0]
+    assert np.array_equal(out, (0.125 * q.astype(np.float32) - 3.0).astype(np.float32))
+
+
+def _roundtrip_case(kind, w):
+    if kind == KQ8:
+        q1 = quantize_q8_0(w)
+        deq = oracle.dequant(KQ8, q1, *w.shape)
+        q2 = quantize_q8_0(deq)
+        assert np.array_equal(q1, q2)
+        d = q1[..., 0:2].copy().view(np.float16).astype(np.float32)[..., 0]
+        err = np.abs(deq - w).reshape(w.shape[0], -1, 32).max(-1)
+        assert np.all(err <= np.abs(d) * (0.5 + 127 * 2 ** -11) + 1e-12)
+    elif kind == KQ4:
+        q1 = quantize_q4_0(w)
+        deq = oracle.dequant(KQ4, q1, *w.shape)
+        q2 = quantize_q4_0(deq)
+        assert np.array_equal(q1, q2)
+        d = q1[..., 0:2].copy().view(np.float16).astype(np.float32)[..., 0]
+        err = np.abs(deq - w).reshape(w.shape[0], -1, 32).max(-1)
+        assert np.all(err <= np.abs(d) * (1 + 8 * 2 ** -11) + 1e-12)
+    else:
+        q, s, b = quantize_a8g64(w)
+        data = np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
+        deq = oracle.dequant(KA8, data, *w.shape)
+        q2, s2, b2 = quantize_a8g64(deq)
+        assert np.array_equal(q, q2)
+        err = np.abs(deq - w).reshape(w.shape[0], -1, 64).max(-1)
+        sc = s.astype(np.float32)
+        # half a step, plus the fp16 rounding of bias and scale (up to 255 steps)
+        bound = 0.5 * sc + np.abs(b.astype(np.float32)) * 2 ** -11 + 255 * sc * 2 ** -11 + 1e-7
+        assert np.all(err <= bound)
+    return deq
+
+
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+def test_dequant_roundtrip_and_bounds(kind):
+    rng = np.random.default_rng(kind)
+    w = (rng.standard_normal((37, 256)) * 0.02).astype(np.float32)
+    _roundtrip_case(kind, w)
+    # special cases: an all-zero block/group, a constant group, an extreme element
+    w2 = w.copy()
+    w2[0, :64] = 0
+    w2[1, :64] = 0.0123
+    w2[2, 5] = 0.5
+    w2[3, 40] = -0.5
+    deq = _roundtrip_case(kind, w2)
+    assert np.all(deq[0, :64] == 0)
+    if kind == KQ8:
+        assert abs(deq[2, 5] - 0.5) <= 0.5 * 2 ** -11      # code +127 hits the max exactly up to fp16 d
+    if kind == KQ4:
+        assert abs(deq[3, 40] + 0.5) <= 0.5 * 2 ** -11     # code 0 -> -8 d = m up to fp16 d
+    if kind == KA8:
+        assert np.all(deq[1, :64] == deq[1, 0])
+
+
+# ----------------------------------------------------------------------------- linear
+
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+def test_linear_against_float64_dot(kind):
+    rng = np.random.default_rng(10 + kind)
+    rows, cols = 70, 384
+    w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    if kind == KQ8:
+        data = quantize_q8_0(w)
+    elif kind == KQ4:
+        data = quantize_q4_0(w)
+    else:
+        q, s, b = quantize_a8g64(w)
+        data = np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
+    deq = oracle.dequant(kind, data, rows, cols).astype(np.float64)
+    x = rng.standard_normal(cols).astype(np.float32)
+    bias = rng.standard_normal(rows).astype(np.float32)
+    y = oracle.linear(kind, data, rows, cols, x, bias)
+    ref = deq @ x.astype(np.float64) + bias
+    gamma = cols * 2.0 ** -53 / (1 - cols * 2.0 ** -53)
+    bound = gamma * (np.abs(deq) @ np.abs(x.astype(np.float64)) + np.abs(bias)) + np.abs(ref) * 2.0 ** -24
+    assert np.all(np.abs(y - ref) <= bound * 1.01 + 1e-30)
+    # one-hot input selects a column exactly
+    e = np.zeros(cols, np.float32)
+    e[17] = 1.0
+    assert np.array_equal(oracle.linear(kind, data, rows, cols, e), deq[:, 17].astype(np.float32))
+
+
+def test_linear_f32_kind():
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((5, 8)).astype(np.float32)
+    x = rng.standard_normal(8).astype(np.float32)
+    y = oracle.linear(0, w, 5, 8, x)
+    assert np.allclose(y, w.astype(np.float64) @ x, rtol=1e-7, atol=0)
+
+
+# ----------------------------------------------------------------------------- norms and activations
+
+def test_layernorm_invariants_and_torch():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal(1024) * 3 + 1.5).astype(np.float32)
+    one, zero = np.ones(1024, np.float32), np.zeros(1024, np.float32)
+    h = oracle.layernorm(x, one, zero, 1e-5).astype(np.float64)
+    var = np.var(x.astype(np.float64))
+    assert abs(h.mean()) < 1e-6
+    assert abs(h.var() - var / (var + 1e-5)) < 1e-6
+    g = (1 + 0.02 * rng.standard_normal(1024)).astype(np.float32)
+    b = (0.02 * rng.standard_normal(1024)).astype(np.float32)
+    h2 = oracle.layernorm(x, g, b, 1e-5)
+    ref = F.layer_norm(torch.tensor(x, dtype=torch.float64), (1024,), torch.tensor(g, dtype=torch.float64),
+                       torch.tensor(b, dtype=torch.float64), eps=1e-5).numpy()
+    assert np.max(np.abs(h2 - ref)) <= 4 * 2.0 ** -24 * np.max(np.abs(ref))
+
+
+def test_rmsnorm_invariants_and_torch():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(2048) * 2).astype(np.float32)
+    one = np.ones(2048, np.float32)
+    h = oracle.rmsnorm(x, one, 1e-5).astype(np.float64)
+    ms = np.mean(x.astype(np.float64) ** 2)
+    assert abs(np.mean(h ** 2) - ms / (ms + 1e-5)) < 1e-6
+    g = (1 + 0.02 * rng.standard_normal(2048)).astype(np.float32)
+    ref = F.rms_norm(torch.tensor(x, dtype=torch.float64), (2048,), torch.tensor(g, dtype=torch.float64),
+                     eps=1e-5).numpy()
+    assert np.max(np.abs(oracle.rmsnorm(x, g, 1e-5) - ref)) <= 4 * 2.0 ** -24 * np.max(np.abs(ref))
+
+
+def test_activations_against_torch():
+    t = np.concatenate([np.linspace(-12, 12, 2001), [0.0, 1e-8, -1e-8, 30.0, -30.0]]).astype(np.float32)
+    tt = torch.tensor(t, dtype=torch.float64)
+    g = oracle.gelu_tanh(t)
+    # 1 + tanh(.) cancels for t below about -7: there only an absolute bound is meaningful
+    assert np.allclose(g, F.gelu(tt, approximate="tanh").numpy(), rtol=2 ** -23, atol=1e-14)
+    assert g[2001] == 0.0 and g[2004] == 30.0
+    s = oracle.silu(t)
+    assert np.allclose(s, F.silu(tt).numpy(), rtol=2 ** -23, atol=1e-37)
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+def test_rope_identity_norms_and_complex_form():
+    rng = np.random.default_rng(6)
+    for hd in (64, 128):
+        x = rng.standard_normal(hd).astype(np.float32)
+        assert np.array_equal(oracle.rope(x, 0), x)              # pos 0 is the identity
+        for pos in (1, 7, 399, 2047):
+            y = oracle.rope(x, pos).astype(np.float64)
+            half = hd // 2
+            # rotation of each (i, i + hd/2) pair: norms preserved
+            n0 = x[:half].astype(np.float64) ** 2 + x[half:].astype(np.float64) ** 2
+            n1 = y[:half] ** 2 + y[half:] ** 2
+            assert np.allclose(n0, n1, rtol=1e-6)
+            # the half-split convention as a complex product (a + ib) e^{i phi}
+            i = np.arange(half)
+            phi = pos * 10000.0 ** (-2.0 * i / hd)
+            z = (x[:half].astype(np.float64) + 1j * x[half:].astype(np.float64)) * np.exp(1j * phi)
+            assert np.allclose(y[:half], z.real, rtol=0, atol=4e-7 * np.abs(z).max())
+            assert np.allclose(y[half:], z.imag, rtol=0, atol=4e-7 * np.abs(z).max())
+
+
+# ----------------------------------------------------------------------------- attention
+
+def test_attention_closed_forms_and_sdpa():
+    rng = np.random.default_rng(7)
+    hd = 64
+    k = rng.standard_normal((9, hd)).astype(np.float16).view(np.uint16)
+    v = rng.standard_normal((9, hd)).astype(np.float16).view(np.uint16)
+    q = rng.standard_normal(hd).astype(np.float32)
+    vf = v.view(np.float16).astype(np.float64)
+    # one cached position: the output is that value row exactly
+    assert np.array_equal(oracle.attend(q, k[:1], v[:1]), vf[0].astype(np.float32))
+    # zero query: uniform weights, the mean of V
+    o = oracle.attend(np.zeros(hd, np.float32), k, v)
+    assert np.allclose(o, vf.mean(0), rtol=0, atol=2e-7 * np.abs(vf).max())
+    # against torch's float64 scaled-dot-product attention
+    o = oracle.attend(q, k, v)
+    kf = torch.tensor(k.view(np.float16).astype(np.float64))
+    ref = F.scaled_dot_product_attention(torch.tensor(q, dtype=torch.float64)[None, None],
+                                         kf[None], torch.tensor(vf)[None])[0, 0].numpy()
+    assert np.allclose(o, ref, rtol=0, atol=2 ** -23 * np.abs(ref).max())
+
+
+def test_attention_softmax_weights_sum_to_one():
+    rng = np.random.default_rng(8)
+    hd = 128
+    n = 50
+    k = (rng.standard_normal((n, hd)) * 3).astype(np.float16).view(np.uint16)
+    ones = np.ones((n, hd), np.float16).view(np.uint16)
+    q = rng.standard_normal(hd).astype(np.float32)
+    # V = 1 everywhere: the output is the sum of the softmax weights
+    o = oracle.attend(q, k, ones)
+    assert np.all(np.abs(o.astype(np.float64) - 1.0) <= 2.0 ** -24)
+
+
+# ----------------------------------------------------------------------------- sampler
+
+def _enumerated_probs(z, T, k, p):
+    """Selection probabilities straight from the definitions, without sorting."""
+    V = len(z)
+    zz = z.astype(np.float64) / T
+    kept = [sum(zz[j] > zz[i] for j in range(V)) < k for i in range(V)]
+    m = max(zz[i] for i in range(V) if kept[i])
+    w = np.array([math.exp(zz[i] - m) if kept[i] else 0.0 for i in range(V)])
+    Z = w.sum()
+    if p < 1.0:
+        S = []
+        for i in range(V):
+            if not kept[i]:
+                S.append(False)
+                continue
+            before = sum(w[j] for j in range(V) if kept[j] and (w[j] > w[i] or (w[j] == w[i] and j < i)))
+            S.append(before / Z < p)
+    else:
+        S = kept
+    w = np.where(S, w, 0.0)
+    return w / w.sum()
+
+
+def _check_sampler(z, T, k, p, n_grid=1 << 16):
+    probs = _enumerated_probs(z, T, k, p)
+    cdf = np.cumsum(probs)
+    counts = np.zeros(len(z))
+    for g in range(n_grid):
+        u = g / n_grid
+        tok, margin = oracle.sample(z, T, k, p, False, u)
+        exp = int(np.searchsorted(cdf, u, side="right"))
+        exp = min(exp, len(z) - 1)
+        while probs[exp] == 0:
+            exp -= 1
+        if tok != exp:
+            assert margin < 1e-9, (z, T, k, p, u, tok, exp)
+        counts[tok] += 1
+    assert np.all(np.abs(counts / n_grid - probs) <= 1.5 / n_grid + 1e-12)
+
+
+def test_sampler_bruteforce_random_logits():
+    rng = np.random.default_rng(9)
+    for trial in range(6):
+        z = (rng.standard_normal(16) * 2).astype(np.float32)
+        for T, k, p in [(0.8, 16, 1.0), (0.8, 5, 1.0), (1.3, 16, 0.7), (0.5, 7, 0.9), (1.0, 3, 0.95)]:
+            _check_sampler(z, T, k, p, n_grid=1 << 12 if trial else 1 << 16)
+
+
+def test_sampler_adversarial_ties_and_boundaries():
+    # ties at the top-k threshold are all kept
+    z = np.array([3, 1, 2, 2, 2, 0, -1, 2, 1, 1, 0, 0, -2, -3, 5, 2], np.float32)
+    _check_sampler(z, 1.0, 3, 1.0, n_grid=1 << 13)
+    probs = _enumerated_probs(z, 1.0, 3, 1.0)
+    assert (probs > 0).sum() == 2 + 5           # 5 and 3, then every 2 tie
+    # a top-p cut exactly on a boundary: two equal leaders with p = 1/2 each
+    z2 = np.full(16, -80.0, np.float32)
+    z2[4] = z2[9] = 10.0
+    probs2 = _enumerated_probs(z2, 1.0, 16, 0.5)
+    assert probs2[4] == 1.0                       # the lower index wins the tie
+    for u in (0.0, 0.3, 0.99):
+        assert oracle.sample(z2, 1.0, 16, 0.5, False, u)[0] == 4
+    _check_sampler(z2, 1.0, 16, 0.5, n_grid=1 << 12)
+
+
+def test_sampler_special_cases():
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal(16).astype(np.float32)
+    am = int(np.argmax(z))
+    for u in (0.0, 0.5, 0.999):
+        assert oracle.sample(z, 0.8, 1, 0.95, False, u)[0] == am            # top_k = 1 is argmax
+        assert oracle.sample(z, 0.8, 1000, 0.95, True, u)[0] == am          # greedy flag
+    # ties under greedy go to the lowest index
+    zt = np.zeros(16, np.float32)
+    zt[[3, 8, 12]] = 2.0
+    tok, m = oracle.sample(zt, 1.0, 1, 1.0, True, 0.0)
+    assert tok == 3 and m == 0.0
+    # top_k >= V and top_p = 1 is plain softmax sampling (inverse CDF in index order)
+    p = np.exp(z.astype(np.float64) / 0.7 - np.max(z) / 0.7)
+    p /= p.sum()
+    cdf = np.cumsum(p)
+    for u in np.linspace(0, 0.999, 37):
+        assert oracle.sample(z, 0.7, 16, 1.0, False, float(u))[0] == int(np.searchsorted(cdf, u, side="right"))
+
+
+def test_sampler_margin_greedy():
+    z = np.array([0.0, 1.5, 1.25, -2.0], np.float32)
+    tok, m = oracle.sample(z, 1.0, 1, 1.0, True, 0.0)
+    assert tok == 1 and m == 0.25
