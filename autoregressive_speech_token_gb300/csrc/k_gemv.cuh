@@ -1,0 +1,372 @@
+// Quantised GEMV with fused norm prologue and bias/activation/residual
+// epilogue: the weight-streaming matvec of the decode step.
+//
+// One decode step multiplies every quantised matrix once by a 1- or 2-row
+// activation ("Every Frame Is a Memory Read", section 3: decode is a memory
+// read; "Chatterbox -> ggml Port: Development Journal", sections 3.15-3.16:
+// the matvec carries the bias and the residual add in its epilogue).
+//
+// Work split: a warp owns a 1024-element slice of K (lane l holds the 32
+// activation values of its 16-byte weight units in registers, reused for
+// every row it visits) and R rows per tile; K > 1024 is split across WK warps
+// whose partial sums meet in shared memory in a fixed order (deterministic).
+// Weights are read once with 128-bit streaming loads; dequantisation happens
+// in registers: Q4_0 nibbles and Q8_0 bytes become exact floats through the
+// 2^23 exponent trick, the block scale multiplies the block's partial sum.
+#pragma once
+#include "sd_internal.cuh"
+
+namespace sd {
+namespace gemv_detail {
+
+constexpr float kMagic = 8388608.0f;  // 2^23: float bits 0x4B000000 | n == 2^23 + n for n < 2^23
+
+__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// sum over the block of NB values; every thread gets the totals.
+template <int NB>
+__device__ __forceinline__ void block_sum(float (&v)[NB], float* scratch) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        float s = warp_sum(v[b]);
+        if (lane == 0) scratch[warp * NB + b] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < NB) {
+        float s = 0.f;
+        for (int w = 0; w < nw; ++w) s += scratch[w * NB + threadIdx.x];
+        scratch[32 * NB + threadIdx.x] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < NB; ++b) v[b] = scratch[32 * NB + b];
+    __syncthreads();
+}
+
+template <int QK>
+struct Unit {
+    // 16-byte weight units per lane per 1024-element warp slice
+    static constexpr int kU = (QK == SD_Q4_0) ? 1 : 2;
+};
+
+// Partial dot product of one 16-byte unit with the lane's activations.
+__device__ __forceinline__ float dot_q4(const uint4 w, const float* x) {
+    // bytes 0..15 -> elements 0..15 (low nibble) and 16..31 (high nibble)
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = (wd[i] >> (8 * k)) & 0xFu;
+            const uint32_t hi = (wd[i] >> (8 * k + 4)) & 0xFu;
+            const float flo = __int_as_float(0x4B000000u | lo) - (kMagic + 8.0f);  // q - 8, exact
+            const float fhi = __int_as_float(0x4B000000u | hi) - (kMagic + 8.0f);
+            s = fmaf(flo, x[4 * i + k], s);
+            s = fmaf(fhi, x[16 + 4 * i + k], s);
+        }
+    }
+    return s;
+}
+
+__device__ __forceinline__ float dot_s8(const uint4 w, const float* x) {
+    const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u = (wd[i] >> (8 * k)) & 0xFFu;  // q + 128 for two's-complement q
+            s = fmaf(__int_as_float(0x4B000000u | u) - (kMagic + 128.0f), x[4 * i + k], s);
+        }
+    }
+    return s;
+}
+
+__device__ __forceinline__ float dot_u8(const uint4 w, const float* x) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u = (wd[i] >> (8 * k)) & 0xFFu;
+            s = fmaf(__int_as_float(0x4B000000u | u) - kMagic, x[4 * i + k], s);
+        }
+    }
+    return s;
+}
+
+__device__ __forceinline__ float gelu_tanh(float t) {
+    const float c = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * t * (1.0f + tanhf(c * (t + 0.044715f * t * t * t)));
+}
+
+__device__ __forceinline__ float silu(float t) { return t / (1.0f + expf(-t)); }
+
+template <int QK, int R, int U>
+__device__ __forceinline__ void load_tile(uint4 (&w)[R][U], const uint8_t* q, int tt, int WR, int rg, int rows,
+                                          int row_bytes, const int (&ebase)[U], int K) {
+    const int r0 = tt * WR * R + rg * R;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int r = r0 + i;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (r < rows && ebase[u] < K) {
+                const int boff = (QK == SD_Q4_0) ? (ebase[u] >> 1) : ebase[u];
+                w[i][u] = ld_stream(q + (size_t)r * row_bytes + boff);
+            } else {
+                w[i][u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+}
+
+template <int QK, int NB, int R>
+__global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
+    constexpr int U = Unit<QK>::kU;
+    const int K = a.W.cols, rows = a.W.rows;
+    const int WK = (K + 1023) >> 10;
+    const int nw = blockDim.x >> 5;
+    const int WR = nw / WK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kw = warp % WK, rg = warp / WK;
+    const int tiles = (rows + WR * R - 1) / (WR * R);
+    const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
+    const int spr = (QK == SD_A8G64) ? (K >> 6) : (K >> 5);
+
+    __shared__ float s_scr[33 * NB];
+    __shared__ float s_tot[8 * R * NB];
+    __shared__ float s_stat[2 * NB];
+    __shared__ float s_cw[NB * 512];
+    extern __shared__ float s_x[];  // [NB][K] transformed activations
+
+    // element index of the lane's unit u (units lie wholly inside or outside K)
+    int ebase[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        ebase[u] = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
+    constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;  // elements per unit
+
+    // issue the first tile's weight loads before the prologue: they do not
+    // depend on the activations.
+    uint4 w[R][U];
+    int t = blockIdx.x;
+    pdl_trigger();
+    if (t < tiles) load_tile<QK, R, U>(w, a.W.q, t, WR, rg, rows, row_bytes, ebase, K);
+    pdl_wait();  // activations come from the previous kernel
+
+    // ---------------------------------------------------------------- prologue
+    if (a.pro == PRO_LN || a.pro == PRO_RMS) {
+        float v[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float s = 0.f;
+            for (int k = threadIdx.x; k < K; k += blockDim.x) {
+                const float xv = a.x[(size_t)b * a.x_stride + k];
+                s += (a.pro == PRO_LN) ? xv : xv * xv;
+            }
+            v[b] = s;
+        }
+        block_sum<NB>(v, s_scr);
+        if (a.pro == PRO_LN) {
+            float mu[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) mu[b] = v[b] / (float)K;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float s = 0.f;
+                for (int k = threadIdx.x; k < K; k += blockDim.x) {
+                    const float dx = a.x[(size_t)b * a.x_stride + k] - mu[b];
+                    s = fmaf(dx, dx, s);
+                }
+                v[b] = s;
+            }
+            block_sum<NB>(v, s_scr);
+            if (threadIdx.x < NB) {
+                s_stat[threadIdx.x] = mu[threadIdx.x];
+                s_stat[NB + threadIdx.x] = 1.0f / sqrtf(v[threadIdx.x] / (float)K + a.eps);
+            }
+        } else if (threadIdx.x < NB) {
+            s_stat[threadIdx.x] = 0.f;
+            s_stat[NB + threadIdx.x] = 1.0f / sqrtf(v[threadIdx.x] / (float)K + a.eps);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
+            const int b = i / K, k = i - b * K;
+            const float xv = a.x[(size_t)b * a.x_stride + k];
+            s_x[i] = (a.pro == PRO_LN) ? fmaf((xv - s_stat[b]) * s_stat[NB + b], a.ng[k], a.nbias[k])
+                                       : xv * s_stat[NB + b] * a.ng[k];
+        }
+    } else if (a.pro == PRO_ATTN) {
+        // log-sum-exp combine weights of the split-KV partials, per (row, head)
+        const int H = a.n_head, S = a.nsplit, hd = a.head_dim, ps = part_stride(hd);
+        for (int bh = threadIdx.x; bh < NB * H; bh += blockDim.x) {
+            const float* p = a.part + (size_t)bh * S * ps;
+            float M = -INFINITY;
+            for (int s = 0; s < S; ++s) M = fmaxf(M, p[s * ps + hd]);
+            float L = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float e = (p[s * ps + hd + 1] > 0.f) ? expf(p[s * ps + hd] - M) : 0.f;
+                s_cw[bh * S + s] = e;
+                L = fmaf(e, p[s * ps + hd + 1], L);
+            }
+            const float inv = 1.0f / L;
+            for (int s = 0; s < S; ++s) s_cw[bh * S + s] *= inv;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
+            const int b = i / K, e = i - b * K, h = e / hd, dd = e - h * hd;
+            const float* p = a.part + ((size_t)(b * H + h) * S) * ps + dd;
+            const float* cw = s_cw + (b * H + h) * S;
+            float v = 0.f;
+            for (int s = 0; s < S; ++s) v = fmaf(cw[s], p[s * ps], v);
+            s_x[i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
+            const int b = i / K, k = i - b * K;
+            s_x[i] = a.x[(size_t)b * a.x_stride + k];
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- activations -> registers
+    float xr[NB][32];
+    float xsum[NB][U];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float s = 0.f;
+            const bool in = ebase[u] < K;
+#pragma unroll
+            for (int j = 0; j < EPU; j += 4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * K + ebase[u] + j]);
+                xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
+                xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
+                s += (v.x + v.y) + (v.z + v.w);
+            }
+            xsum[b][u] = s;
+        }
+    }
+
+    // ---------------------------------------------------------------- main loop
+    for (; t < tiles; t += gridDim.x) {
+        const int r0 = t * WR * R + rg * R;
+        float acc[R][NB];
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
+
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = r0 + i;
+            if (r >= rows) continue;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (ebase[u] >= K) continue;
+                if (QK == SD_A8G64) {
+                    const __half2 sb = reinterpret_cast<const __half2*>(a.W.s)[(size_t)r * spr + (ebase[u] >> 6)];
+                    const float sc = __low2float(sb), bi = __high2float(sb);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const float dq = dot_u8(w[i][u], &xr[b][u * EPU]);
+                        acc[i][b] = fmaf(sc, dq, fmaf(bi, xsum[b][u], acc[i][b]));
+                    }
+                } else {
+                    const float d = __half2float(reinterpret_cast<const __half*>(a.W.s)[(size_t)r * spr + (ebase[u] >> 5)]);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const float dq = (QK == SD_Q4_0) ? dot_q4(w[i][u], &xr[b][0]) : dot_s8(w[i][u], &xr[b][u * EPU]);
+                        acc[i][b] = fmaf(d, dq, acc[i][b]);
+                    }
+                }
+            }
+        }
+        // prefetch the next tile while reducing this one
+        const int tn = t + gridDim.x;
+        if (tn < tiles) load_tile<QK, R, U>(w, a.W.q, tn, WR, rg, rows, row_bytes, ebase, K);
+
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float s = warp_sum(acc[i][b]);
+                if (lane == 0) s_tot[((rg * R + i) * NB + b) * WK + kw] = s;
+            }
+        __syncthreads();
+        const int n_out = WR * R * NB;
+        if (threadIdx.x < n_out) {
+            const int b = threadIdx.x % NB;
+            const int i = (threadIdx.x / NB) % R;
+            const int g = threadIdx.x / (NB * R);
+            const int r = t * WR * R + g * R + i;
+            float v = 0.f;
+            for (int k = 0; k < WK; ++k) v += s_tot[((g * R + i) * NB + b) * WK + k];
+            if (r < rows) {
+                if (a.epi == EPI_SWIGLU) {
+                    // rows are interleaved (gate 2j, up 2j+1); the even row's thread writes
+                    if ((i & 1) == 0) {
+                        float up = 0.f;
+                        for (int k = 0; k < WK; ++k) up += s_tot[((g * R + i + 1) * NB + b) * WK + k];
+                        const int j = r >> 1;
+                        float o = silu(v) * up;
+                        if (a.resid) o += a.resid[(size_t)b * a.y_stride + j];
+                        a.y[(size_t)b * a.y_stride + j] = o;
+                    }
+                } else {
+                    if (a.bias) v += a.bias[r];
+                    if (a.epi == EPI_GELU) v = gelu_tanh(v);
+                    if (a.resid) v += a.resid[(size_t)b * a.y_stride + r];
+                    a.y[(size_t)b * a.y_stride + r] = v;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int QK, int NB>
+cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
+    constexpr int R = (NB == 1) ? 4 : 2;
+    const int K = a.W.cols;
+    const int WK = (K + 1023) / 1024;
+    if (WK > 8) return cudaErrorInvalidValue;
+    int WR = 8 / WK;
+    if (WR < 1) WR = 1;
+    // fewer rows per CTA when the matrix is short, so that every SM gets work
+    while (WR > 1 && (a.W.rows + WR * R - 1) / (WR * R) < 2 * sm_count) WR >>= 1;
+    const int tiles = (a.W.rows + WR * R - 1) / (WR * R);
+    const int grid = tiles < 32 * sm_count ? tiles : 32 * sm_count;
+    const size_t smem = sizeof(float) * (size_t)NB * K;
+    if (smem > 32 * 1024) {  // with the static arrays the total passes the 48 KB default
+        cudaError_t e = cudaFuncSetAttribute(k_gemv<QK, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_k(k_gemv<QK, NB, R>, dim3(grid), dim3(32 * WK * WR), smem, st, a);
+}
+
+inline cudaError_t check_gemv(const GemvArgs& a) {
+    if (a.W.cols % 32 || (a.W.kind == SD_A8G64 && a.W.cols % 64) || a.W.cols > 8192) return cudaErrorInvalidValue;
+    if (a.epi == EPI_SWIGLU && a.W.rows % 2) return cudaErrorInvalidValue;
+    if (a.pro == PRO_ATTN && (a.n_head * a.nsplit > 512 || a.n_head * a.head_dim != a.W.cols))
+        return cudaErrorInvalidValue;
+    if (a.nb != 1 && a.nb != 2) return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+}  // namespace gemv_detail
+}  // namespace sd

@@ -1,0 +1,985 @@
+// Host runtime of libsd.so: context and memory plan, weight-blob reader and
+// repack, CUDA-graph capture of the decode step / frame, and the C ABI of
+// include/sd.h and include/sd_ops.h.
+//
+// Structure follows "Chatterbox -> ggml Port: Development Journal", section
+// 3.2 (a prompt graph and a step graph sharing one persistent KV cache) and
+// "Every Frame Is a Memory Read", section 5.2 (the whole code-predictor frame
+// -- fifteen passes, heads, sampling, code-embedding sum -- as one captured
+// graph with the random draws as inputs).  Everything that changes from step
+// to step (position, tokens, draws, sampler settings) lives in device memory,
+// so a captured graph is replayed unchanged; attention reads the position on
+// the device and covers only [0, pos] ("Every Frame Is a Memory Read",
+// section 5.3: attending over the whole fixed capacity is a loss).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstddef>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/sd_ops.h"
+#include "sd_internal.cuh"
+
+using namespace sd;
+
+namespace {
+
+thread_local std::string g_err = "";
+
+constexpr uint32_t kBlobMagic = 0x31574453u;
+constexpr int kEntryBytes = 96;
+constexpr int kConfigFields = 22;
+
+struct alignas(16) DevState {
+    // device-owned counters
+    int32_t pos, cp_pos, step_idx, err;
+    // host-written inputs (uploaded per call)
+    int32_t prompt_on, force_on, pad0, pad1;
+    const float* u_seq;
+    int32_t* out_seq;
+    SampParams samp[2];
+    int32_t tok[kMaxRows];
+    float u1[kMaxRows];                 // GPT-2/Llama step draws
+    float u[kMaxRows * kMaxCodebooks];  // frame draws [row][codebook]
+    int32_t codes_in[kMaxRows * kMaxCodebooks];
+    int32_t force[kMaxRows * kMaxCodebooks];
+    // device-written outputs
+    int32_t codes[kMaxRows * kMaxCodebooks];
+};
+
+struct BlobTensor {
+    uint32_t kind, rows, cols;
+    uint64_t off, nbytes;
+};
+
+struct DLayer {
+    const float *n1g = nullptr, *n1b = nullptr, *bqkv = nullptr, *bo = nullptr;
+    const float *n2g = nullptr, *n2b = nullptr, *bfc = nullptr, *bproj = nullptr;
+    QMat wqkv, wo, wfc, wproj;
+};
+
+struct DStack {
+    bool gpt2 = false;
+    int n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, n_ctx = 0, nsplit = 1;
+    float eps = 1e-5f, theta = 10000.f;
+    std::vector<DLayer> L;
+    const float *nfg = nullptr, *nfb = nullptr;
+    __half *kc = nullptr, *vc = nullptr;
+    float *rope_cos = nullptr, *rope_sin = nullptr;
+    float *x = nullptr, *qkv = nullptr, *part = nullptr, *u = nullptr;
+    int qkv_rows() const { return (H + 2 * Hkv) * hd; }
+};
+
+enum class Phase { Created, Loaded, Running };
+
+}  // namespace
+
+struct sd_ctx {
+    sd_model_config cfg{};
+    int device = 0, sm_count = 0, B = 1;
+    cudaStream_t stream = nullptr;      // launches
+    cudaStream_t cap = nullptr;         // private capture stream
+    bool own_stream = false;
+    std::string err;
+    Phase phase = Phase::Created;
+    int host_pos = 0;
+
+    DStack main, cp;
+    std::vector<void*> allocs;          // activations, caches, tables
+    uint8_t* weights = nullptr;         // weight arena
+    int64_t weight_bytes = 0, kv_bytes = 0;
+    const float *wte = nullptr, *wpe = nullptr;
+    QMat head, cp_proj;
+    const float* emb[kMaxCodebooks] = {};
+    QMat cp_head[kMaxCodebooks];
+    float* logits = nullptr;            // [B][V] or [B][16][Vmax]
+    int logits_ld = 0, vmax = 0;
+    float* ebuf = nullptr;              // [B][d] code-embedding staging (Qwen)
+    int32_t* prompt = nullptr;          // [B][max_ctx]
+
+    DevState* ds = nullptr;             // device
+    DevState* hs = nullptr;             // pinned host mirror
+    bool force_pending = false;
+
+    cudaGraphExec_t g_step = nullptr, g_body = nullptr, g_frame = nullptr, g_prompt_last = nullptr;
+    int kernels_per_step = 0;
+    int count_launch = 0;
+};
+
+namespace {
+
+int fail(sd_ctx* c, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) c->err = buf;
+    g_err = buf;
+    return code;
+}
+
+#define CK(call)                                                                                   \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess) return fail(c, SD_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+    } while (0)
+
+template <typename T>
+int dalloc(sd_ctx* c, T** p, size_t bytes) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+    if (e != cudaSuccess) return fail(c, SD_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+    CK(cudaMemset(q, 0, bytes ? bytes : 16));
+    c->allocs.push_back(q);
+    *p = reinterpret_cast<T*>(q);
+    return SD_OK;
+}
+
+int validate_cfg(const sd_model_config& m) {
+    if (m.arch < SD_ARCH_GPT2 || m.arch > SD_ARCH_QWEN_TTS) return 0;
+    if (m.quant < SD_Q8_0 || m.quant > SD_A8G64) return 0;
+    if (m.n_layer < 0 || m.d_model <= 0 || m.n_head <= 0 || m.n_kv_head <= 0 || m.head_dim <= 0) return 0;
+    if (m.head_dim != 64 && m.head_dim != 128) return 0;
+    if (m.n_head % m.n_kv_head || m.n_head / m.n_kv_head > 4) return 0;
+    if (m.d_ff <= 0 || m.vocab <= 0 || m.vocab > 16384 || m.max_ctx <= 0 || m.batch < 1 || m.batch > kMaxRows) return 0;
+    const int gs = m.quant == SD_A8G64 ? 64 : 32;
+    if (m.d_model % gs || m.d_ff % gs || (m.n_head * m.head_dim) % gs) return 0;
+    if (m.d_model > 8192 || m.d_ff > 8192) return 0;
+    if (m.arch == SD_ARCH_GPT2 && m.n_head != m.n_kv_head) return 0;
+    if (m.arch == SD_ARCH_QWEN_TTS) {
+        if (m.n_codebooks < 2 || m.n_codebooks > kMaxCodebooks || m.cp_layer < 0 || m.cp_d_model <= 0) return 0;
+        if (m.cp_head_dim != 64 && m.cp_head_dim != 128) return 0;
+        if (m.cp_n_kv_head <= 0 || m.cp_n_head % m.cp_n_kv_head || m.cp_n_head / m.cp_n_kv_head > 4) return 0;
+        if (m.cp_vocab <= 0 || m.cp_vocab > 16384 || m.cp_max_ctx < m.n_codebooks) return 0;
+        if (m.cp_d_model % gs || m.cp_d_ff % gs) return 0;
+    }
+    return 1;
+}
+
+void init_stack(DStack& s, bool gpt2, int n_layer, int d, int H, int Hkv, int hd, int ff, int n_ctx, float eps,
+                float theta) {
+    s.gpt2 = gpt2;
+    s.n_layer = n_layer; s.d = d; s.H = H; s.Hkv = Hkv; s.hd = hd; s.ff = ff; s.n_ctx = n_ctx;
+    s.eps = eps; s.theta = theta;
+    // split-KV chunks: enough CTAs for the grid at typical lengths, never more than the capacity needs
+    s.nsplit = n_ctx >= 256 ? 8 : (n_ctx >= 64 ? 4 : 1);
+    if (H * s.nsplit > 512) s.nsplit = 512 / H;
+}
+
+int alloc_stack(sd_ctx* c, DStack& s) {
+    const int B = c->B;
+    const size_t kv = (size_t)B * s.n_layer * s.Hkv * s.n_ctx * s.hd;
+    int rc;
+    if ((rc = dalloc(c, &s.kc, kv * 2)) || (rc = dalloc(c, &s.vc, kv * 2))) return rc;
+    c->kv_bytes += (int64_t)kv * 4;
+    const int wide = std::max(s.qkv_rows(), 2 * s.ff);
+    if ((rc = dalloc(c, &s.x, sizeof(float) * B * s.d)) || (rc = dalloc(c, &s.qkv, sizeof(float) * B * wide)) ||
+        (rc = dalloc(c, &s.part, sizeof(float) * B * s.H * s.nsplit * part_stride(s.hd))) ||
+        (rc = dalloc(c, &s.u, sizeof(float) * B * std::max(s.ff, s.d))))
+        return rc;
+    if (!s.gpt2) {
+        // NEOX RoPE table in double, rounded to fp32: theta_i = base^(-2i/hd), phi = pos * theta_i
+        const int half = s.hd / 2;
+        std::vector<float> cs((size_t)s.n_ctx * half), sn((size_t)s.n_ctx * half);
+        for (int p = 0; p < s.n_ctx; ++p)
+            for (int i = 0; i < half; ++i) {
+                const double phi = (double)p * std::pow((double)s.theta, -2.0 * i / s.hd);
+                cs[(size_t)p * half + i] = (float)std::cos(phi);
+                sn[(size_t)p * half + i] = (float)std::sin(phi);
+            }
+        if ((rc = dalloc(c, &s.rope_cos, cs.size() * 4)) || (rc = dalloc(c, &s.rope_sin, sn.size() * 4))) return rc;
+        CK(cudaMemcpy(s.rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+        CK(cudaMemcpy(s.rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+    }
+    return SD_OK;
+}
+
+// ------------------------------------------------------------------ enqueue helpers
+
+int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
+    cudaError_t e = launch_gemv(a, c->sm_count, st);
+    c->count_launch++;
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
+// One transformer position through every layer of stack s (input already in s.x).
+int enqueue_layers(sd_ctx* c, DStack& s, const int* pos_ptr, cudaStream_t st) {
+    const int B = c->B, d = s.d, qd = s.H * s.hd, kd = s.Hkv * s.hd, qr = s.qkv_rows();
+    int rc;
+    for (int l = 0; l < s.n_layer; ++l) {
+        DLayer& L = s.L[l];
+        GemvArgs g;
+        g.W = L.wqkv; g.nb = B; g.x = s.x; g.x_stride = d;
+        g.pro = s.gpt2 ? PRO_LN : PRO_RMS; g.ng = L.n1g; g.nbias = L.n1b; g.eps = s.eps;
+        g.epi = EPI_LINEAR; g.bias = L.bqkv; g.y = s.qkv; g.y_stride = qr;
+        if ((rc = gemv(c, g, st))) return rc;
+
+        AttnArgs a;
+        a.q = s.qkv; a.q_stride = qr; a.knew = s.qkv + qd; a.vnew = s.qkv + qd + kd;
+        a.kc = s.kc; a.vc = s.vc; a.row_heads = s.n_layer * s.Hkv; a.head_off = l * s.Hkv;
+        a.n_head = s.H; a.n_kv = s.Hkv; a.hd = s.hd; a.n_ctx = s.n_ctx; a.nsplit = s.nsplit;
+        a.pos_ptr = pos_ptr; a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.part = s.part;
+        a.err = &c->ds->err;
+        cudaError_t e = launch_attention(a, B, st);
+        c->count_launch++;
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+
+        GemvArgs o;
+        o.W = L.wo; o.nb = B; o.pro = PRO_ATTN; o.part = s.part; o.n_head = s.H; o.head_dim = s.hd;
+        o.nsplit = s.nsplit; o.epi = EPI_LINEAR; o.bias = L.bo; o.resid = s.x; o.y = s.x; o.y_stride = d;
+        if ((rc = gemv(c, o, st))) return rc;
+
+        GemvArgs f;
+        f.W = L.wfc; f.nb = B; f.x = s.x; f.x_stride = d;
+        f.pro = s.gpt2 ? PRO_LN : PRO_RMS; f.ng = L.n2g; f.nbias = L.n2b; f.eps = s.eps;
+        f.epi = s.gpt2 ? EPI_GELU : EPI_SWIGLU; f.bias = L.bfc; f.y = s.u; f.y_stride = s.ff;
+        if ((rc = gemv(c, f, st))) return rc;
+
+        GemvArgs p;
+        p.W = L.wproj; p.nb = B; p.x = s.u; p.x_stride = s.ff; p.pro = PRO_NONE;
+        p.epi = EPI_LINEAR; p.bias = L.bproj; p.resid = s.x; p.y = s.x; p.y_stride = d;
+        if ((rc = gemv(c, p, st))) return rc;
+    }
+    return SD_OK;
+}
+
+// logits = head(final_norm(s.x)) written to c->logits + slot * vmax
+int enqueue_head(sd_ctx* c, DStack& s, const QMat& W, int slot, cudaStream_t st) {
+    GemvArgs h;
+    h.W = W; h.nb = c->B; h.x = s.x; h.x_stride = s.d;
+    h.pro = s.gpt2 ? PRO_LN : PRO_RMS; h.ng = s.nfg; h.nbias = s.nfb; h.eps = s.eps;
+    h.epi = EPI_LINEAR; h.y = c->logits + (size_t)slot * c->vmax; h.y_stride = c->logits_ld;
+    return gemv(c, h, st);
+}
+
+int enqueue_sample(sd_ctx* c, int which, int slot, int V, bool t3, cudaStream_t st) {
+    SampleArgs a;
+    a.logits = c->logits + (size_t)slot * c->vmax; a.ld = c->logits_ld; a.V = V;
+    a.sp = &c->ds->samp[which];
+    a.err = &c->ds->err;
+    if (t3) {
+        a.u = c->ds->u1; a.u_stride = 1; a.u_off = 0;
+        a.u_seq = &c->ds->u_seq; a.step_idx = &c->ds->step_idx;
+        a.out = c->ds->tok; a.out_stride = 1; a.out_off = 0;
+        a.out_seq = &c->ds->out_seq;
+    } else {
+        a.u = c->ds->u; a.u_stride = kMaxCodebooks; a.u_off = slot;
+        a.out = c->ds->codes; a.out_stride = kMaxCodebooks; a.out_off = slot;
+    }
+    cudaError_t e = launch_sample(a, c->B, st);
+    c->count_launch++;
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sampler launch: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
+int advance(sd_ctx* c, int* a, int add_a, int* b, int add_b, int* cc, int set_c, cudaStream_t st) {
+    cudaError_t e = launch_advance(a, add_a, b, add_b, cc, set_c, st);
+    c->count_launch++;
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "advance launch: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
+// Input embedding of the main stack at the current position: token table
+// (+ learned positions), reading the prompt buffer while prompt_on is set.
+int enqueue_embed(sd_ctx* c, cudaStream_t st) {
+    EmbedArgs e;
+    e.table = c->cfg.arch == SD_ARCH_QWEN_TTS ? c->emb[0] : c->wte;
+    e.pos_table = c->wpe; e.pos_ptr = &c->ds->pos; e.tok = c->ds->tok;
+    e.prompt = c->prompt; e.prompt_on = &c->ds->prompt_on; e.prompt_ld = c->cfg.max_ctx;
+    e.d = c->main.d; e.V = c->cfg.vocab; e.n_ctx = c->cfg.max_ctx; e.x = c->main.x; e.err = &c->ds->err;
+    cudaError_t err = launch_embed(e, c->B, st);
+    c->count_launch++;
+    if (err != cudaSuccess) return fail(c, SD_ERR_CUDA, "embed launch: %s", cudaGetErrorString(err));
+    return SD_OK;
+}
+
+// The code-predictor part of a frame: 16 positions, heads 1..15, samplers.
+int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
+    DStack& t = c->main;
+    DStack& p = c->cp;
+    const int B = c->B;
+    int rc;
+    if ((rc = advance(c, nullptr, 0, nullptr, 0, &c->ds->cp_pos, 0, st))) return rc;
+    for (int j = 0; j < c->cfg.n_codebooks; ++j) {
+        GemvArgs g;
+        g.W = c->cp_proj; g.nb = B; g.epi = EPI_LINEAR; g.y = p.x; g.y_stride = p.d;
+        if (j == 0) {  // Pr * final_norm(h_T)
+            g.x = t.x; g.x_stride = t.d; g.pro = PRO_RMS; g.ng = t.nfg; g.eps = t.eps;
+        } else {       // Pr * E_{j-1}[c_{j-1}]
+            EmbedCodeArgs ec;
+            ec.table = c->emb[j - 1]; ec.V = j - 1 == 0 ? c->cfg.vocab : c->cfg.cp_vocab; ec.d = t.d; ec.j = j - 1;
+            ec.codes = c->ds->codes; ec.force = c->ds->force; ec.force_on = &c->ds->force_on; ec.x = c->ebuf;
+            ec.err = &c->ds->err;
+            cudaError_t e = launch_embed_code(ec, B, st);
+            c->count_launch++;
+            if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "embed_code launch: %s", cudaGetErrorString(e));
+            g.x = c->ebuf; g.x_stride = t.d; g.pro = PRO_NONE;
+        }
+        if ((rc = gemv(c, g, st))) return rc;
+        if ((rc = enqueue_layers(c, p, &c->ds->cp_pos, st))) return rc;
+        if (j >= 1) {
+            if ((rc = enqueue_head(c, p, c->cp_head[j], j, st))) return rc;
+            if ((rc = enqueue_sample(c, 1, j, c->cfg.cp_vocab, false, st))) return rc;
+        }
+        if ((rc = advance(c, &c->ds->cp_pos, 1, nullptr, 0, nullptr, 0, st))) return rc;
+    }
+    return SD_OK;
+}
+
+enum class GraphKind { T3Step, T3Body, QwenFrame, QwenBody, QwenPromptLast };
+
+int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
+    int rc;
+    const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
+    if (k == GraphKind::QwenFrame) {
+        EmbedSumArgs es;
+        for (int j = 0; j < c->cfg.n_codebooks; ++j) {
+            es.tables[j] = c->emb[j];
+            es.vocab[j] = j ? c->cfg.cp_vocab : c->cfg.vocab;
+        }
+        es.ncb = c->cfg.n_codebooks; es.d = c->main.d; es.codes = c->ds->codes_in; es.e = c->main.x;
+        es.err = &c->ds->err;
+        cudaError_t e = launch_embed_sum(es, c->B, st);
+        c->count_launch++;
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "embed_sum launch: %s", cudaGetErrorString(e));
+    } else {
+        if ((rc = enqueue_embed(c, st))) return rc;
+    }
+    if ((rc = enqueue_layers(c, c->main, &c->ds->pos, st))) return rc;
+    if (k == GraphKind::T3Body || k == GraphKind::QwenBody)
+        return advance(c, &c->ds->pos, 1, nullptr, 0, nullptr, 0, st);
+    if ((rc = enqueue_head(c, c->main, c->head, 0, st))) return rc;
+    if ((rc = enqueue_sample(c, 0, 0, c->cfg.vocab, !qwen, st))) return rc;
+    if (qwen && (rc = enqueue_cp_frame(c, st))) return rc;
+    return advance(c, &c->ds->pos, 1, &c->ds->step_idx, 1, nullptr, 0, st);
+}
+
+int capture(sd_ctx* c, GraphKind k, cudaGraphExec_t* out, int* n_kernels) {
+    cudaGraph_t g = nullptr;
+    c->count_launch = 0;
+    CK(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+    int rc = enqueue_graph(c, k, c->cap);
+    cudaError_t e = cudaStreamEndCapture(c->cap, &g);
+    if (rc) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "end capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(out, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    if (n_kernels) *n_kernels = c->count_launch;
+    return SD_OK;
+}
+
+// ------------------------------------------------------------------ weights
+
+struct Blob {
+    std::unordered_map<std::string, BlobTensor> t;
+    const uint8_t* base = nullptr;  // device pointer to the blob bytes
+};
+
+int find_f32(sd_ctx* c, Blob& b, const std::string& name, int64_t n, uint8_t*& arena, const float** out) {
+    auto it = b.t.find(name);
+    if (it == b.t.end() || it->second.kind != 0 || (int64_t)it->second.rows * it->second.cols != n)
+        return fail(c, SD_ERR_BLOB, "blob: missing or mis-shaped fp32 tensor '%s'", name.c_str());
+    CK(cudaMemcpyAsync(arena, b.base + it->second.off, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    *out = reinterpret_cast<const float*>(arena);
+    arena += (n * 4 + 255) / 256 * 256;
+    return SD_OK;
+}
+
+size_t qbytes(int kind, int rows, int cols) {
+    const size_t q = kind == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+    const size_t s = kind == SD_A8G64 ? (size_t)rows * (cols / 64) * 4 : (size_t)rows * (cols / 32) * 2;
+    return (q + 255) / 256 * 256 + (s + 255) / 256 * 256;
+}
+
+int find_q(sd_ctx* c, Blob& b, const std::string& name, int rows, int cols, int swiglu_ff, uint8_t*& arena,
+           QMat* out) {
+    auto it = b.t.find(name);
+    if (it == b.t.end() || (int)it->second.kind != c->cfg.quant || (int)it->second.rows != rows ||
+        (int)it->second.cols != cols)
+        return fail(c, SD_ERR_BLOB, "blob: missing or mis-shaped matrix '%s'", name.c_str());
+    const int kind = c->cfg.quant;
+    const size_t qsz = kind == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+    uint8_t* q = arena;
+    uint8_t* s = arena + (qsz + 255) / 256 * 256;
+    cudaError_t e = launch_repack(kind, b.base + it->second.off, rows, cols, swiglu_ff, q, s, c->stream);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "repack: %s", cudaGetErrorString(e));
+    arena += qbytes(kind, rows, cols);
+    out->kind = kind; out->rows = rows; out->cols = cols; out->q = q; out->s = s;
+    return SD_OK;
+}
+
+// Walks every tensor of the model either to size the arena (dry) or to fill it.
+int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
+    const sd_model_config& m = c->cfg;
+    const bool dry = arena == nullptr;
+    size_t sum = 0;
+    int rc = SD_OK;
+    auto F = [&](const std::string& n, int64_t cnt, const float** out) {
+        if (rc) return;
+        if (dry) { sum += (cnt * 4 + 255) / 256 * 256; return; }
+        rc = find_f32(c, b, n, cnt, arena, out);
+    };
+    auto Q = [&](const std::string& n, int rows, int cols, int swiglu_ff, QMat* out) {
+        if (rc) return;
+        if (dry) { sum += qbytes(m.quant, rows, cols); return; }
+        rc = find_q(c, b, n, rows, cols, swiglu_ff, arena, out);
+    };
+    auto stack = [&](DStack& s, const char* pfx) {
+        s.L.resize(s.n_layer);
+        const int d = s.d, qd = s.H * s.hd;
+        for (int l = 0; l < s.n_layer; ++l) {
+            DLayer& L = s.L[l];
+            const std::string p = pfx + std::to_string(l) + ".";
+            if (s.gpt2) {
+                F(p + "ln1.g", d, &L.n1g); F(p + "ln1.b", d, &L.n1b);
+                Q(p + "wqkv", s.qkv_rows(), d, 0, &L.wqkv); F(p + "bqkv", s.qkv_rows(), &L.bqkv);
+                Q(p + "wo", d, qd, 0, &L.wo); F(p + "bo", d, &L.bo);
+                F(p + "ln2.g", d, &L.n2g); F(p + "ln2.b", d, &L.n2b);
+                Q(p + "wfc", s.ff, d, 0, &L.wfc); F(p + "bfc", s.ff, &L.bfc);
+                Q(p + "wproj", d, s.ff, 0, &L.wproj); F(p + "bproj", d, &L.bproj);
+            } else {
+                F(p + "rms1.g", d, &L.n1g);
+                Q(p + "wqkv", s.qkv_rows(), d, 0, &L.wqkv);
+                Q(p + "wo", d, qd, 0, &L.wo);
+                F(p + "rms2.g", d, &L.n2g);
+                Q(p + "wgu", 2 * s.ff, d, s.ff, &L.wfc);
+                Q(p + "wdown", d, s.ff, 0, &L.wproj);
+            }
+        }
+    };
+    if (m.arch == SD_ARCH_GPT2) {
+        F("wte", (int64_t)m.vocab * m.d_model, &c->wte);
+        F("wpe", (int64_t)m.max_ctx * m.d_model, &c->wpe);
+        stack(c->main, "l");
+        F("lnf.g", m.d_model, &c->main.nfg); F("lnf.b", m.d_model, &c->main.nfb);
+        Q("whead", m.vocab, m.d_model, 0, &c->head);
+    } else if (m.arch == SD_ARCH_LLAMA) {
+        F("wte", (int64_t)m.vocab * m.d_model, &c->wte);
+        stack(c->main, "l");
+        F("normf.g", m.d_model, &c->main.nfg);
+        Q("whead", m.vocab, m.d_model, 0, &c->head);
+    } else {
+        for (int j = 0; j < m.n_codebooks; ++j)
+            F("emb." + std::to_string(j), (int64_t)(j ? m.cp_vocab : m.vocab) * m.d_model, &c->emb[j]);
+        stack(c->main, "t");
+        F("t.normf.g", m.d_model, &c->main.nfg);
+        Q("t.head", m.vocab, m.d_model, 0, &c->head);
+        Q("cp.proj", m.cp_d_model, m.d_model, 0, &c->cp_proj);
+        stack(c->cp, "c");
+        F("cp.normf.g", m.cp_d_model, &c->cp.nfg);
+        for (int j = 1; j < m.n_codebooks; ++j)
+            Q("cp.head." + std::to_string(j), m.cp_vocab, m.cp_d_model, 0, &c->cp_head[j]);
+    }
+    if (total) *total = sum;
+    return rc;
+}
+
+// Per-call inputs: a GPT-2/Llama step uploads [prompt_on, u) (flags, sequence
+// pointers, samplers, tokens, step draws); a frame also uploads the frame draws,
+// previous codes and forced codes.
+constexpr size_t kStepH2D = offsetof(DevState, u) - offsetof(DevState, prompt_on);
+constexpr size_t kStepD2H = offsetof(DevState, u1);
+int upload_inputs(sd_ctx* c, bool full) {
+    const size_t a = offsetof(DevState, prompt_on);
+    const size_t e = full ? offsetof(DevState, codes) : offsetof(DevState, u);
+    CK(cudaMemcpyAsync(reinterpret_cast<char*>(c->ds) + a, reinterpret_cast<char*>(c->hs) + a, e - a,
+                       cudaMemcpyHostToDevice, c->stream));
+    return SD_OK;
+}
+
+int check_device_err(sd_ctx* c) {
+    if (c->hs->err) {
+        const int code = c->hs->err;
+        c->hs->err = 0;
+        cudaMemsetAsync(&c->ds->err, 0, sizeof(int32_t), c->stream);
+        return fail(c, SD_ERR_DEVICE, "a kernel flagged an out-of-range index (code %d)", code);
+    }
+    return SD_OK;
+}
+
+int download_counters(sd_ctx* c, bool codes) {
+    CK(cudaMemcpyAsync(c->hs, c->ds, kStepD2H, cudaMemcpyDeviceToHost, c->stream));
+    if (codes)
+        CK(cudaMemcpyAsync(c->hs->codes, c->ds->codes, sizeof(c->hs->codes), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return check_device_err(c);
+}
+
+int set_sampler(sd_ctx* c, int which, const sd_sampler* s) {
+    if (!s) return fail(c, SD_ERR_INVALID_ARG, "sampler is NULL");
+    if (!(s->temperature >= 0.f) || s->top_k < 1 || !(s->top_p > 0.f && s->top_p <= 1.f))
+        return fail(c, SD_ERR_INVALID_ARG, "sampler out of range (T=%g k=%d p=%g)", s->temperature, s->top_k,
+                    s->top_p);
+    c->hs->samp[which].temperature = s->temperature;
+    c->hs->samp[which].top_k = s->top_k;
+    c->hs->samp[which].top_p = s->top_p;
+    c->hs->samp[which].greedy = s->greedy;
+    return SD_OK;
+}
+
+int check_draws(sd_ctx* c, const float* u, int n) {
+    if (!u) return fail(c, SD_ERR_INVALID_ARG, "draws are NULL");
+    for (int i = 0; i < n; ++i)
+        if (!(u[i] >= 0.f && u[i] < 1.f)) return fail(c, SD_ERR_INVALID_ARG, "draw %d = %g outside [0,1)", i, u[i]);
+    return SD_OK;
+}
+
+}  // namespace
+
+// ======================================================================= C ABI
+
+extern "C" {
+
+const char* sd_last_error(const sd_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
+
+int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out) {
+    sd_ctx* c = nullptr;
+    if (!cfg || !out) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_create: NULL argument");
+    *out = nullptr;
+    if (!validate_cfg(*cfg)) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_create: invalid model config");
+    if (cfg->batch > 2)
+        return fail(nullptr, SD_ERR_UNSUPPORTED, "sd_create: batch %d > 2 is not implemented by the GEMV path", cfg->batch);
+    c = new sd_ctx();
+    c->cfg = *cfg;
+    c->device = device;
+    c->B = cfg->batch;
+    auto bail = [&](int rc) { g_err = c->err; sd_destroy(c); return rc; };
+    if (cudaSetDevice(device) != cudaSuccess) return bail(fail(c, SD_ERR_CUDA, "cudaSetDevice(%d) failed", device));
+    if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return bail(fail(c, SD_ERR_CUDA, "device query failed"));
+    if (stream) {
+        c->stream = reinterpret_cast<cudaStream_t>(stream);
+    } else {
+        if (cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking) != cudaSuccess)
+            return bail(fail(c, SD_ERR_CUDA, "stream create failed"));
+        c->own_stream = true;
+    }
+    if (cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess)
+        return bail(fail(c, SD_ERR_CUDA, "stream create failed"));
+    const sd_model_config& m = *cfg;
+    init_stack(c->main, m.arch == SD_ARCH_GPT2, m.n_layer, m.d_model, m.n_head, m.n_kv_head, m.head_dim, m.d_ff,
+               m.max_ctx, m.norm_eps, m.rope_theta);
+    int rc;
+    if ((rc = alloc_stack(c, c->main))) return bail(rc);
+    if (m.arch == SD_ARCH_QWEN_TTS) {
+        init_stack(c->cp, false, m.cp_layer, m.cp_d_model, m.cp_n_head, m.cp_n_kv_head, m.cp_head_dim, m.cp_d_ff,
+                   m.cp_max_ctx, m.norm_eps, m.rope_theta);
+        if ((rc = alloc_stack(c, c->cp))) return bail(rc);
+        c->vmax = std::max(m.vocab, m.cp_vocab);
+        c->logits_ld = kMaxCodebooks * c->vmax;
+        if ((rc = dalloc(c, &c->ebuf, sizeof(float) * c->B * m.d_model))) return bail(rc);
+    } else {
+        c->vmax = m.vocab;
+        c->logits_ld = m.vocab;
+    }
+    if ((rc = dalloc(c, &c->logits, sizeof(float) * c->B * c->logits_ld))) return bail(rc);
+    if ((rc = dalloc(c, &c->prompt, sizeof(int32_t) * c->B * m.max_ctx))) return bail(rc);
+    if ((rc = dalloc(c, &c->ds, sizeof(DevState)))) return bail(rc);
+    if (cudaHostAlloc(&c->hs, sizeof(DevState), cudaHostAllocDefault) != cudaSuccess)
+        return bail(fail(c, SD_ERR_OOM, "pinned staging allocation failed"));
+    memset(c->hs, 0, sizeof(DevState));
+    *out = c;
+    return SD_OK;
+}
+
+int sd_load_weights(sd_ctx* c, const void* blob, size_t nbytes, int blob_on_device) {
+    if (!c || !blob) return fail(c, SD_ERR_INVALID_ARG, "sd_load_weights: NULL argument");
+    if (c->phase != Phase::Created) return fail(c, SD_ERR_STATE, "weights already loaded");
+    CK(cudaSetDevice(c->device));
+    // header + table on the host
+    uint8_t hdr[16];
+    if (nbytes < 16 + 4 * 32) return fail(c, SD_ERR_BLOB, "blob too small");
+    if (blob_on_device) CK(cudaMemcpy(hdr, blob, 16, cudaMemcpyDeviceToHost));
+    else memcpy(hdr, blob, 16);
+    uint32_t magic, ver, n, toff;
+    memcpy(&magic, hdr, 4); memcpy(&ver, hdr + 4, 4); memcpy(&n, hdr + 8, 4); memcpy(&toff, hdr + 12, 4);
+    if (magic != kBlobMagic || ver != 1) return fail(c, SD_ERR_BLOB, "blob: bad magic or version");
+    const size_t tend = (size_t)toff + (size_t)n * kEntryBytes;
+    if (tend > nbytes || toff < 16 + 4 * 32) return fail(c, SD_ERR_BLOB, "blob: table out of range");
+    std::vector<uint8_t> head(tend);
+    if (blob_on_device) CK(cudaMemcpy(head.data(), blob, tend, cudaMemcpyDeviceToHost));
+    else memcpy(head.data(), blob, tend);
+    if (memcmp(head.data() + 16, &c->cfg, kConfigFields * 4) != 0)
+        return fail(c, SD_ERR_BLOB, "blob: config echo does not match the context's config");
+    Blob b;
+    for (uint32_t i = 0; i < n; ++i) {
+        const uint8_t* e = head.data() + toff + (size_t)i * kEntryBytes;
+        char name[65] = {0};
+        memcpy(name, e, 64);
+        BlobTensor t;
+        memcpy(&t.kind, e + 64, 4); memcpy(&t.rows, e + 68, 4); memcpy(&t.cols, e + 72, 4);
+        memcpy(&t.off, e + 80, 8); memcpy(&t.nbytes, e + 88, 8);
+        if (t.off + t.nbytes > nbytes || t.off % 16) return fail(c, SD_ERR_BLOB, "blob: tensor '%s' out of range", name);
+        b.t[name] = t;
+    }
+    // blob bytes on the device (staging copy when the caller's blob is on the host)
+    uint8_t* staging = nullptr;
+    if (blob_on_device) {
+        b.base = reinterpret_cast<const uint8_t*>(blob);
+    } else {
+        cudaError_t e = cudaMalloc(&staging, nbytes);
+        if (e != cudaSuccess) return fail(c, SD_ERR_OOM, "staging cudaMalloc(%zu) failed", nbytes);
+        e = cudaMemcpy(staging, blob, nbytes, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) { cudaFree(staging); return fail(c, SD_ERR_CUDA, "blob upload: %s", cudaGetErrorString(e)); }
+        b.base = staging;
+    }
+    size_t total = 0;
+    int rc = load_all(c, b, nullptr, &total);
+    if (!rc) {
+        cudaError_t e = cudaMalloc(&c->weights, total);
+        if (e != cudaSuccess) rc = fail(c, SD_ERR_OOM, "weight arena cudaMalloc(%zu) failed", total);
+    }
+    if (!rc) rc = load_all(c, b, c->weights, nullptr);
+    cudaError_t se = cudaStreamSynchronize(c->stream);
+    if (staging) cudaFree(staging);
+    if (rc) return rc;
+    if (se != cudaSuccess) return fail(c, SD_ERR_CUDA, "weight repack: %s", cudaGetErrorString(se));
+    c->weight_bytes = (int64_t)total;
+    // graphs
+    if (c->cfg.arch == SD_ARCH_QWEN_TTS) {
+        if ((rc = capture(c, GraphKind::QwenFrame, &c->g_frame, &c->kernels_per_step))) return rc;
+        if ((rc = capture(c, GraphKind::QwenBody, &c->g_body, nullptr))) return rc;
+        if ((rc = capture(c, GraphKind::QwenPromptLast, &c->g_prompt_last, nullptr))) return rc;
+    } else {
+        if ((rc = capture(c, GraphKind::T3Step, &c->g_step, &c->kernels_per_step))) return rc;
+        if ((rc = capture(c, GraphKind::T3Body, &c->g_body, nullptr))) return rc;
+    }
+    c->phase = Phase::Loaded;
+    c->host_pos = 0;
+    return SD_OK;
+}
+
+int sd_reset(sd_ctx* c) {
+    if (!c) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_reset: NULL context");
+    if (cudaSetDevice(c->device) != cudaSuccess) return fail(c, SD_ERR_CUDA, "cudaSetDevice failed");
+    cudaStreamSynchronize(c->stream);
+    cudaGetLastError();
+    if (c->ds) {
+        cudaMemsetAsync(c->ds, 0, offsetof(DevState, prompt_on), c->stream);
+        if (cudaStreamSynchronize(c->stream) != cudaSuccess) return fail(c, SD_ERR_CUDA, "reset failed");
+    }
+    if (c->hs) memset(c->hs, 0, sizeof(DevState));
+    c->host_pos = 0;
+    c->force_pending = false;
+    if (c->phase == Phase::Running) c->phase = Phase::Loaded;
+    return SD_OK;
+}
+
+int sd_set_forced_codes(sd_ctx* c, const int32_t* codes) {
+    if (!c) return fail(nullptr, SD_ERR_INVALID_ARG, "NULL context");
+    if (c->cfg.arch != SD_ARCH_QWEN_TTS) return fail(c, SD_ERR_UNSUPPORTED, "forced codes need a Talker+CP model");
+    if (!codes) { c->force_pending = false; return SD_OK; }
+    for (int b = 0; b < c->B; ++b)
+        for (int j = 0; j < c->cfg.n_codebooks; ++j) {
+            const int v = codes[b * kMaxCodebooks + j], V = j ? c->cfg.cp_vocab : c->cfg.vocab;
+            if (v < 0 || v >= V) return fail(c, SD_ERR_INVALID_ARG, "forced code [%d][%d]=%d out of range", b, j, v);
+            c->hs->force[b * kMaxCodebooks + j] = v;
+        }
+    c->force_pending = true;
+    return SD_OK;
+}
+
+int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+               int32_t* out_tok) {
+    if (!c || !tokens || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_prefill: NULL argument");
+    if (c->phase != Phase::Loaded || c->host_pos != 0) return fail(c, SD_ERR_STATE, "sd_prefill needs a loaded, reset context");
+    if (n < 1 || n > c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "prompt length %d outside [1, %d]", n, c->cfg.max_ctx);
+    CK(cudaSetDevice(c->device));
+    const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
+    const int B = c->B, ns = qwen ? c->cfg.n_codebooks : 1;
+    for (int i = 0; i < B * n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
+            return fail(c, SD_ERR_INVALID_ARG, "prompt token %d = %d outside [0, %d)", i, tokens[i], c->cfg.vocab);
+    int rc;
+    if ((rc = set_sampler(c, 0, sampler))) return rc;
+    if (qwen) {
+        if ((rc = set_sampler(c, 1, sampler))) return rc;
+    }
+    if (!u) return fail(c, SD_ERR_INVALID_ARG, "draws are NULL");
+    for (int b = 0; b < B; ++b) {
+        if ((rc = check_draws(c, u + b * ns, ns))) return rc;
+        for (int j = 0; j < ns; ++j) c->hs->u[b * kMaxCodebooks + j] = u[b * ns + j];
+        c->hs->u1[b] = u[b * ns];
+    }
+    // prompt tokens, row-major with a max_ctx leading dimension
+    for (int b = 0; b < B; ++b)
+        CK(cudaMemcpyAsync(c->prompt + (size_t)b * c->cfg.max_ctx, tokens + (size_t)b * n, sizeof(int32_t) * n,
+                           cudaMemcpyHostToDevice, c->stream));
+    c->hs->prompt_on = 1;
+    c->hs->force_on = c->force_pending ? 1 : 0;
+    c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
+    if ((rc = upload_inputs(c, qwen))) return rc;
+    for (int i = 0; i < n - 1; ++i) CK(cudaGraphLaunch(c->g_body, c->stream));
+    CK(cudaGraphLaunch(qwen ? c->g_prompt_last : c->g_step, c->stream));
+    c->force_pending = false;
+    rc = download_counters(c, qwen);   // synchronises: the staging mirror may change after this
+    c->hs->prompt_on = 0;
+    c->hs->force_on = 0;
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < ns; ++j)
+            out_tok[b * ns + j] = qwen ? c->hs->codes[b * kMaxCodebooks + j] : c->hs->tok[b];
+    c->host_pos = n;
+    c->phase = Phase::Running;
+    return SD_OK;
+}
+
+int sd_step(sd_ctx* c, const int32_t* tok, const sd_sampler* sampler, const float* u, int32_t* out_tok) {
+    if (!c || !tok || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_step: NULL argument");
+    if (c->cfg.arch == SD_ARCH_QWEN_TTS) return fail(c, SD_ERR_UNSUPPORTED, "use sd_frame for a Talker+CP model");
+    if (c->phase != Phase::Running) return fail(c, SD_ERR_STATE, "sd_step before sd_prefill");
+    if (c->host_pos >= c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "context full (%d)", c->host_pos);
+    CK(cudaSetDevice(c->device));
+    int rc;
+    if ((rc = set_sampler(c, 0, sampler))) return rc;
+    if ((rc = check_draws(c, u, c->B))) return rc;
+    for (int b = 0; b < c->B; ++b) {
+        if (tok[b] < 0 || tok[b] >= c->cfg.vocab)
+            return fail(c, SD_ERR_INVALID_ARG, "token %d outside [0, %d)", tok[b], c->cfg.vocab);
+        c->hs->tok[b] = tok[b];
+        c->hs->u1[b] = u[b];
+    }
+    c->hs->prompt_on = 0; c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
+    if ((rc = upload_inputs(c, false))) return rc;
+    CK(cudaGraphLaunch(c->g_step, c->stream));
+    if ((rc = download_counters(c, false))) return rc;
+    for (int b = 0; b < c->B; ++b) out_tok[b] = c->hs->tok[b];
+    c->host_pos++;
+    return SD_OK;
+}
+
+int sd_decode_n(sd_ctx* c, int32_t n_steps, const sd_sampler* sampler, const float* u_dev, int32_t* out_dev) {
+    if (!c || !u_dev || !out_dev) return fail(c, SD_ERR_INVALID_ARG, "sd_decode_n: NULL argument");
+    if (c->cfg.arch == SD_ARCH_QWEN_TTS) return fail(c, SD_ERR_UNSUPPORTED, "sd_decode_n needs a GPT-2/Llama model");
+    if (c->phase != Phase::Running) return fail(c, SD_ERR_STATE, "sd_decode_n before sd_prefill");
+    if (n_steps < 0) return fail(c, SD_ERR_INVALID_ARG, "negative step count");
+    if (c->host_pos + n_steps > c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "context would overflow");
+    CK(cudaSetDevice(c->device));
+    int rc;
+    if ((rc = set_sampler(c, 0, sampler))) return rc;
+    c->hs->prompt_on = 0; c->hs->u_seq = u_dev; c->hs->out_seq = out_dev;
+    if ((rc = upload_inputs(c, false))) return rc;
+    CK(cudaMemsetAsync(&c->ds->step_idx, 0, sizeof(int32_t), c->stream));
+    for (int i = 0; i < n_steps; ++i) CK(cudaGraphLaunch(c->g_step, c->stream));
+    rc = download_counters(c, false);  // synchronises before the staging mirror changes
+    // later per-step calls upload null sequence pointers
+    c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
+    if (rc) return rc;
+    c->host_pos += n_steps;
+    return SD_OK;
+}
+
+int sd_frame(sd_ctx* c, const int32_t* codes_in, const sd_sampler* talker, const sd_sampler* cp, const float* u,
+             int32_t* codes_out) {
+    if (!c || !codes_in || !u || !codes_out) return fail(c, SD_ERR_INVALID_ARG, "sd_frame: NULL argument");
+    if (c->cfg.arch != SD_ARCH_QWEN_TTS) return fail(c, SD_ERR_UNSUPPORTED, "sd_frame needs a Talker+CP model");
+    if (c->phase != Phase::Running) return fail(c, SD_ERR_STATE, "sd_frame before sd_prefill");
+    if (c->host_pos >= c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "context full (%d)", c->host_pos);
+    CK(cudaSetDevice(c->device));
+    const int B = c->B, ns = c->cfg.n_codebooks;
+    int rc;
+    if ((rc = set_sampler(c, 0, talker)) || (rc = set_sampler(c, 1, cp))) return rc;
+    for (int b = 0; b < B; ++b) {
+        if ((rc = check_draws(c, u + b * ns, ns))) return rc;
+        for (int j = 0; j < ns; ++j) {
+            const int v = codes_in[b * ns + j], V = j ? c->cfg.cp_vocab : c->cfg.vocab;
+            if (v < 0 || v >= V) return fail(c, SD_ERR_INVALID_ARG, "code [%d][%d]=%d out of range", b, j, v);
+            c->hs->codes_in[b * kMaxCodebooks + j] = v;
+            c->hs->u[b * kMaxCodebooks + j] = u[b * ns + j];
+        }
+    }
+    c->hs->prompt_on = 0;
+    c->hs->force_on = c->force_pending ? 1 : 0;
+    if ((rc = upload_inputs(c, true))) return rc;
+    CK(cudaGraphLaunch(c->g_frame, c->stream));
+    c->force_pending = false;
+    rc = download_counters(c, true);
+    c->hs->force_on = 0;
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < ns; ++j) codes_out[b * ns + j] = c->hs->codes[b * kMaxCodebooks + j];
+    c->host_pos++;
+    return SD_OK;
+}
+
+int sd_get_logits(sd_ctx* c, float* host_out, size_t n_floats) {
+    if (!c || !host_out) return fail(c, SD_ERR_INVALID_ARG, "sd_get_logits: NULL argument");
+    const size_t need = (size_t)c->B * c->logits_ld;
+    if (n_floats < need) return fail(c, SD_ERR_INVALID_ARG, "need %zu floats", need);
+    CK(cudaSetDevice(c->device));
+    CK(cudaMemcpyAsync(host_out, c->logits, need * sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return SD_OK;
+}
+
+int sd_get_info(const sd_ctx* c, sd_info* out) {
+    if (!c || !out) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_get_info: NULL argument");
+    out->pos = c->host_pos;
+    out->sm_count = c->sm_count;
+    out->kernels_per_step = c->kernels_per_step;
+    out->attn_splits = c->main.nsplit;
+    out->weight_bytes = c->weight_bytes;
+    out->kv_bytes = c->kv_bytes;
+    out->step_h2d_bytes = (int64_t)kStepH2D;
+    out->step_d2h_bytes = (int64_t)kStepD2H;
+    return SD_OK;
+}
+
+void sd_destroy(sd_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    for (cudaGraphExec_t g : {c->g_step, c->g_body, c->g_frame, c->g_prompt_last})
+        if (g) cudaGraphExecDestroy(g);
+    for (void* p : c->allocs) cudaFree(p);
+    if (c->weights) cudaFree(c->weights);
+    if (c->hs) cudaFreeHost(c->hs);
+    if (c->cap) cudaStreamDestroy(c->cap);
+    if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+    delete c;
+}
+
+// ======================================================================= op-level ABI
+
+struct sd_qmat {
+    QMat m;
+    void* buf = nullptr;
+    int device = 0;
+};
+
+int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int on_device, int device, sd_qmat** out) {
+    sd_ctx* c = nullptr;
+    if (!canon || !out) return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_create: NULL argument");
+    *out = nullptr;
+    if (quant < SD_Q8_0 || quant > SD_A8G64 || rows < 1 || cols < 1 || rows > (1 << 24) || cols > 65536 ||
+        cols % (quant == SD_A8G64 ? 64 : 32))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_create: bad shape or kind");
+    CK(cudaSetDevice(device));
+    const size_t canon_bytes = quant == SD_Q8_0   ? (size_t)rows * (cols / 32) * 34
+                               : quant == SD_Q4_0 ? (size_t)rows * (cols / 32) * 18
+                                                  : (size_t)rows * cols + (size_t)rows * (cols / 64) * 4;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(canon);
+    void* staging = nullptr;
+    if (!on_device) {
+        CK(cudaMalloc(&staging, canon_bytes));
+        CK(cudaMemcpy(staging, canon, canon_bytes, cudaMemcpyHostToDevice));
+        src = reinterpret_cast<const uint8_t*>(staging);
+    }
+    sd_qmat* q = new sd_qmat();
+    q->device = device;
+    const size_t total = qbytes(quant, (int)rows, (int)cols);
+    if (cudaMalloc(&q->buf, total) != cudaSuccess) {
+        delete q;
+        if (staging) cudaFree(staging);
+        return fail(c, SD_ERR_OOM, "sd_qmat_create: cudaMalloc failed");
+    }
+    const size_t qsz = quant == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+    q->m.kind = quant; q->m.rows = (int)rows; q->m.cols = (int)cols;
+    q->m.q = reinterpret_cast<uint8_t*>(q->buf);
+    q->m.s = reinterpret_cast<uint8_t*>(q->buf) + (qsz + 255) / 256 * 256;
+    cudaError_t e = launch_repack(quant, src, (int)rows, (int)cols, 0, const_cast<uint8_t*>(q->m.q),
+                                  const_cast<void*>(q->m.s), nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (staging) cudaFree(staging);
+    if (e != cudaSuccess) {
+        cudaFree(q->buf);
+        delete q;
+        return fail(c, SD_ERR_CUDA, "sd_qmat_create: repack failed: %s", cudaGetErrorString(e));
+    }
+    *out = q;
+    return SD_OK;
+}
+
+void sd_qmat_destroy(sd_qmat* m) {
+    if (!m) return;
+    cudaSetDevice(m->device);
+    cudaFree(m->buf);
+    delete m;
+}
+
+int sd_qmat_dequant(const sd_qmat* m, float* out_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!m || !out_dev) return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_dequant: NULL argument");
+    CK(launch_dequant(m->m, out_dev, reinterpret_cast<cudaStream_t>(stream)));
+    return SD_OK;
+}
+
+int sd_qmat_gemv(const sd_qmat* m, const float* x_dev, int32_t nb, const float* bias_dev, float* y_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!m || !x_dev || !y_dev || (nb != 1 && nb != 2)) return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemv: bad argument");
+    if (m->m.cols > 8192) return fail(c, SD_ERR_UNSUPPORTED, "sd_qmat_gemv: cols > 8192");
+    int sms = 0;
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, m->device));
+    GemvArgs a;
+    a.W = m->m; a.nb = nb; a.x = x_dev; a.x_stride = m->m.cols; a.pro = PRO_NONE;
+    a.epi = EPI_LINEAR; a.bias = bias_dev; a.y = y_dev; a.y_stride = m->m.rows;
+    CK(launch_gemv(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+    return SD_OK;
+}
+
+int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* s, const float* u_dev,
+                   int32_t* out_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!logits_dev || !s || !u_dev || !out_dev || rows < 1 || rows > 65535 || V < 1 || V > 16384)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows: bad argument");
+    if (!(s->temperature >= 0.f) || s->top_k < 1 || !(s->top_p > 0.f && s->top_p <= 1.f))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows: sampler out of range");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    SampParams* sp = nullptr;
+    int* err = nullptr;
+    CK(cudaMalloc(&sp, sizeof(SampParams) + 16));
+    err = reinterpret_cast<int*>(reinterpret_cast<char*>(sp) + sizeof(SampParams));
+    SampParams h{s->temperature, s->top_k, s->top_p, s->greedy};
+    cudaError_t e = cudaMemcpyAsync(sp, &h, sizeof h, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, 4, st);
+    SampleArgs a;
+    a.logits = logits_dev; a.ld = V; a.V = V; a.sp = sp; a.u = u_dev; a.u_stride = 1; a.u_off = 0;
+    a.out = out_dev; a.out_stride = 1; a.out_off = 0; a.err = err;
+    if (e == cudaSuccess) e = launch_sample(a, rows, st);
+    int herr = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(sp);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sd_sample_rows: %s", cudaGetErrorString(e));
+    if (herr) return fail(c, SD_ERR_DEVICE, "sd_sample_rows: kernel flagged code %d", herr);
+    return SD_OK;
+}
+
+int sd_attend_rows(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_dev, int32_t B, int32_t H, int32_t Hkv,
+                   int32_t hd, int32_t n_ctx, int32_t n, int32_t nsplit, float* out_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!q_dev || !k_dev || !v_dev || !out_dev || B < 1 || H < 1 || Hkv < 1 || H % Hkv || H / Hkv > 4 ||
+        (hd != 64 && hd != 128) || n < 1 || n > n_ctx || nsplit < 1 || nsplit > 64 || H * nsplit > 4096)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_attend_rows: bad argument");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* part = nullptr;
+    const size_t pbytes = sizeof(float) * B * H * nsplit * part_stride(hd);
+    CK(cudaMalloc(&part, pbytes + 16));
+    int* pos = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + pbytes);
+    const int pm1 = n - 1;
+    cudaError_t e = cudaMemcpyAsync(pos, &pm1, 4, cudaMemcpyHostToDevice, st);
+    AttnArgs a;
+    a.q = q_dev; a.q_stride = H * hd; a.knew = nullptr; a.vnew = nullptr;
+    a.kc = reinterpret_cast<__half*>(const_cast<uint16_t*>(k_dev));
+    a.vc = reinterpret_cast<__half*>(const_cast<uint16_t*>(v_dev));
+    a.row_heads = Hkv; a.head_off = 0; a.n_head = H; a.n_kv = Hkv; a.hd = hd; a.n_ctx = n_ctx; a.nsplit = nsplit;
+    a.pos_ptr = pos; a.part = part;
+    if (e == cudaSuccess) e = launch_attention(a, B, st);
+    if (e == cudaSuccess) e = launch_attn_combine(part, B, H, hd, nsplit, out_dev, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(part);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sd_attend_rows: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sd.h"
+
+namespace sd {
+
+// Programmatic dependent launch: a kernel lets its successor launch as soon as
+// all of its CTAs are running, and waits for its predecessor's results before
+// its first dependent read.  Both are no-ops when launched without the
+// attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with the programmatic-serialization attribute (set when use_pdl()).
+bool use_pdl();
+template <typename Kern, typename... Args>
+cudaError_t launch_k(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = use_pdl() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+constexpr int kMaxRows = SD_MAX_ROWS;
+constexpr int kMaxCodebooks = SD_MAX_CODEBOOKS;
+
+// Device copy of a quantised matrix in the repacked layout:
+//   Q8_0 : q = int8 [rows][cols],   s = __half  [rows][cols/32]
+//   Q4_0 : q = bytes [rows][cols/2] (16-byte block of nibbles, element j low /
+//          j+16 high nibble of byte j), s = __half [rows][cols/32]
+//   A8G64: q = uint8 [rows][cols],  s = __half2 [rows][cols/64] = (scale, bias)
+struct QMat {
+    int kind = 0;
+    int rows = 0, cols = 0;
+    const uint8_t* q = nullptr;
+    const void* s = nullptr;
+};
+
+enum Prologue : int { PRO_NONE = 0, PRO_LN = 1, PRO_RMS = 2, PRO_ATTN = 3 };
+enum Epilogue : int { EPI_LINEAR = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
+
+// Split-KV partial record: o[hd] (unnormalised), then m (running max) and l
+// (sum of exp) -- stride hd + 4 floats.
+__host__ __device__ inline int part_stride(int hd) { return hd + 4; }
+
+struct GemvArgs {
+    QMat W;
+    int nb = 1;                    // activation rows (1 or 2)
+    const float* x = nullptr;      // [nb][x_stride] input (ignored for PRO_ATTN)
+    int x_stride = 0;
+    int pro = PRO_NONE;
+    const float* ng = nullptr;     // norm gain   (PRO_LN / PRO_RMS)
+    const float* nbias = nullptr;  // norm offset (PRO_LN)
+    float eps = 1e-5f;
+    const float* part = nullptr;   // PRO_ATTN: [nb][n_head][nsplit][hd+4]
+    int n_head = 0, head_dim = 0, nsplit = 0;
+    int epi = EPI_LINEAR;
+    const float* bias = nullptr;   // [rows] (or [rows/2] after SwiGLU) -- optional
+    const float* resid = nullptr;  // [nb][y_stride] added after bias -- optional, may alias y
+    float* y = nullptr;            // [nb][y_stride]
+    int y_stride = 0;
+};
+
+struct AttnArgs {
+    const float* q = nullptr;      // query of row b, head h at q[b*q_stride + h*hd]
+    int q_stride = 0;
+    const float* knew = nullptr;   // new key   of row b, kv head g at knew[b*q_stride + g*hd] (nullable)
+    const float* vnew = nullptr;   // new value (same layout); appended at position `pos`
+    __half* kc = nullptr;          // cache [B][kv_rows][n_ctx][hd], row b, kv head g of this layer at
+    __half* vc = nullptr;          //   ((b*row_heads + head_off + g) * n_ctx) * hd
+    int row_heads = 0;             // kv heads per row in the cache (layers * Hkv)
+    int head_off = 0;              // layer * Hkv
+    int n_head = 0, n_kv = 0, hd = 0, n_ctx = 0, nsplit = 0;
+    const int* pos_ptr = nullptr;  // device: attend to positions [0, *pos_ptr + pos_add]
+    int pos_add = 0;
+    const float* rope_cos = nullptr;  // [n_ctx][hd/2] or null (no RoPE)
+    const float* rope_sin = nullptr;
+    float* part = nullptr;         // [B][n_head][nsplit][hd+4]
+    int* err = nullptr;
+};
+
+struct SampParams {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+    int32_t greedy;
+};
+
+struct SampleArgs {
+    const float* logits = nullptr;  // row b at logits + b*ld
+    int ld = 0;
+    int V = 0;
+    const SampParams* sp = nullptr;  // device
+    // draw of row b: (*u_seq)[(*step_idx) * rows + b] when *u_seq is set, else u[b*u_stride + u_off]
+    const float* u = nullptr;
+    const float* const* u_seq = nullptr;  // device pointer to a device pointer (may hold null)
+    const int* step_idx = nullptr;
+    int u_stride = 1, u_off = 0;
+    int32_t* out = nullptr;                 // out[b*out_stride + out_off]
+    int out_stride = 1, out_off = 0;
+    int32_t* const* out_seq = nullptr;      // if *out_seq: (*out_seq)[(*step_idx) * rows + b] = token
+    int* err = nullptr;
+};
+
+// ------------------------------------------------------------------ launchers
+// (implemented in the kernels' translation units; all enqueue on `st`)
+cudaError_t launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_gemv_q8(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_gemv_q4(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_gemv_a8(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t st);
+cudaError_t launch_attn_combine(const float* part, int B, int H, int hd, int nsplit, float* out,
+                                cudaStream_t st);
+cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t st);
+size_t sample_smem_bytes(int V);
+
+cudaError_t launch_repack(int kind, const uint8_t* canon, int rows, int cols, int swiglu_ff, uint8_t* q,
+                          void* s, cudaStream_t st);
+cudaError_t launch_dequant(const QMat& W, float* out, cudaStream_t st);
+
+struct EmbedArgs {
+    const float* table = nullptr;     // [V][d]
+    const float* pos_table = nullptr; // [n_ctx][d] learned positions or null
+    const int* pos_ptr = nullptr;
+    const int32_t* tok = nullptr;     // token of row b at tok[b*tok_stride + tok_off]
+    int tok_stride = 1, tok_off = 0;
+    const int32_t* prompt = nullptr;  // if non-null and *prompt_on: token = prompt[b*prompt_ld + pos]
+    const int* prompt_on = nullptr;
+    int prompt_ld = 0;
+    int d = 0, V = 0, n_ctx = 0;
+    float* x = nullptr;               // [B][d]
+    int* err = nullptr;
+};
+cudaError_t launch_embed(const EmbedArgs& a, int B, cudaStream_t st);
+
+// e[b] = sum_j E_j[codes[b*16 + j]] for j < ncb (double accumulation).
+struct EmbedSumArgs {
+    const float* tables[kMaxCodebooks] = {};
+    int vocab[kMaxCodebooks] = {};
+    int ncb = 0, d = 0;
+    const int32_t* codes = nullptr;   // [B][16]
+    float* e = nullptr;               // [B][d]
+    int* err = nullptr;
+};
+cudaError_t launch_embed_sum(const EmbedSumArgs& a, int B, cudaStream_t st);
+
+// x[b] = table[code(b)] with code(b) = force_on && *force_on ? force[b*16+j] : codes[b*16+j]
+struct EmbedCodeArgs {
+    const float* table = nullptr;
+    int V = 0, d = 0, j = 0;
+    const int32_t* codes = nullptr;
+    const int32_t* force = nullptr;
+    const int* force_on = nullptr;
+    float* x = nullptr;
+    int* err = nullptr;
+};
+cudaError_t launch_embed_code(const EmbedCodeArgs& a, int B, cudaStream_t st);
+
+// *p += add for each listed counter (single thread).
+cudaError_t launch_advance(int* a, int add_a, int* b, int add_b, int* c, int set_c, cudaStream_t st);
+
+}  // namespace sd

@@ -1,0 +1,376 @@
+#!/usr/bin/env python3
+"""Decode benchmark: batch-1 speech-token decode tokens/s and achieved HBM GB/s.
+
+Workload (default `gpt2m_q4`): GPT-2-Medium-shaped T3 (24 layers, d 1024,
+16x64 heads, FFN 4096, vocab 6563) with Q4_0 weights, a 150-token prompt,
+then sampled decode steps (temperature 0.8, top-k 1000, top-p 0.95) with
+seeded Philox draws.  A "step" is one decode step of the whole hot path:
+embedding, 24 layers (norm, quantised GEMVs with fused epilogues, RoPE/KV
+append, split-KV attention), final norm, head GEMV, on-device sampler.
+
+value: K steps with device-resident draws and device-side token feedback
+(sd_decode_n), timed with CUDA events on the launching stream.
+e2e:   the same metric through sd_step with host buffers (each step copies
+its token and draw host->device and its token device->host).
+roofline: the decode step is the unit: algorithmic bytes per step (quantised
+weights + small fp32 tensors + KV cache read and written at that position) over
+the event-timed step duration, against the measured HBM copy bandwidth.
+
+Multi-GPU: batch-1 decode does not shard; `--gpus N` runs N independent
+replicas (one process per GPU) and reports the aggregate tokens/s over the
+slowest rank's time ("scaling": "weak").
+
+`--impl reference` times the oracle (plain C, fp64 sums) on the host cores on
+a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import get_preset, prompt_tokens, uniform_draws  # noqa: E402
+from synth import presets as P  # noqa: E402
+
+METRIC = "decode tokens/s at batch 1 and achieved HBM GB/s vs ~8 TB/s roofline"
+L2_BYTES = 129 * 2 ** 20
+
+
+def workload_text(run) -> str:
+    m = run.model
+    s = run.sampler
+    samp = "greedy" if s.greedy else f"T {s.temperature}, top-k {s.top_k}, top-p {s.top_p}"
+    return (f"{run.name}: {m.n_layer}x{m.d_model} {'GPT-2' if m.arch == P.ARCH_GPT2 else 'Llama'} T3, "
+            f"{m.n_head}x{m.head_dim} heads, FFN {m.d_ff}, vocab {m.vocab}, {P.QUANT_NAMES[m.quant]} weights, "
+            f"fp16 KV; prompt {run.prompt_len} + {run.n_steps} decode steps ({samp}), batch {m.batch}")
+
+
+def step_bytes(m: P.ModelSpec, pos: int) -> int:
+    """Algorithmic HBM bytes of one decode step at position `pos` (0-based)."""
+    wq = int(m.quantised_params_per_step() * P.BYTES_PER_WEIGHT[m.quant])
+    d, f = m.d_model, m.d_ff
+    if m.arch == P.ARCH_GPT2:
+        small = m.n_layer * (4 * d + m.qkv_rows + d + f + d) + 2 * d   # norm gains/offsets + biases
+        small += 2 * d                                                  # token and position rows
+    else:
+        small = m.n_layer * 2 * d + d + d
+    small *= 4
+    kv = m.batch * m.kv_bytes_per_position() * (pos + 1) + m.batch * m.kv_bytes_per_position()  # read + write
+    return wq + small + kv
+
+
+def mean_step_bytes(m, p0, n):
+    return sum(step_bytes(m, p) for p in range(p0, p0 + n)) / n
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [x.strip() for x in line.split(",")]
+                    if len(p) >= 9:
+                        rows.append(p)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks not sampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, ws):
+    if ws > 1:
+        dist.barrier()
+
+
+def max_over_ranks(dist, ws, value: float, device=None) -> float:
+    """Largest value over ranks (the slowest rank's time)."""
+    if ws == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import autoregressive_speech_token_gb300 as sdpkg
+    from autoregressive_speech_token_gb300 import build as sdbuild
+    from synth.weights import build_model_blob
+
+    ws, rank, local = dist_env()
+    dist = init_dist(ws, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sdbuild.build()
+
+    run = get_preset(args.config)
+    m = run.model
+    K, W = args.steps, args.warmup
+    if run.prompt_len + max(K, W) > m.max_ctx:
+        raise SystemExit(f"steps must keep prompt + steps <= {m.max_ctx}")
+    blob, _ = build_model_blob(m, seed=run.weight_seed)
+    stream = torch.cuda.current_stream(dev)
+    dec = sdpkg.Decoder(m, blob, device=local, stream=stream.cuda_stream)
+    del blob
+    info = dec.info()
+    prompt = prompt_tokens(run)
+    s = sdpkg.Sampler.from_spec(run.sampler)
+    B = m.batch
+    n_dr = max(K, W)
+    draws = uniform_draws(run.draw_seed, n_dr + 1, B)[..., 0]
+    u_dev = torch.from_numpy(np.ascontiguousarray(draws[1:])).to(dev)
+    out_dev = torch.zeros(n_dr, B, dtype=torch.int32, device=dev)
+
+    # warm-up: W untimed steps after a fresh prefill
+    dec.reset()
+    dec.prefill(prompt, s, draws[0])
+    dec.decode_n(W, s, u_dev, out_dev)
+    torch.cuda.synchronize()
+
+    # timed: K steps from position prompt_len
+    dec.reset()
+    dec.prefill(prompt, s, draws[0])
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
+        ev0.record(stream)
+        dec.decode_n(K, s, u_dev, out_dev)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    barrier(dist, ws)
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(dist, ws, ms, dev)
+    value = ws * K * B / (ms_max / 1e3)
+
+    # end to end through sd_step with host buffers
+    dec.reset()
+    tok = dec.prefill(prompt, s, draws[0])
+    Ke = min(K, 64) if args.e2e_steps is None else args.e2e_steps
+    for i in range(min(3, Ke)):                       # warm the host path
+        tok = dec.step(tok, s, draws[1 + i])
+    dec.reset()
+    tok = dec.prefill(prompt, s, draws[0])
+    barrier(dist, ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        tok = dec.step(tok, s, draws[1 + i])
+    t1 = time.perf_counter()
+    e2e_s = max_over_ranks(dist, ws, t1 - t0, dev)
+    e2e = ws * Ke * B / e2e_s
+
+    # roofline of the decode step
+    peaks, peak_kind = load_peaks()
+    bytes_step = mean_step_bytes(m, run.prompt_len, K)
+    achieved = bytes_step / (ms / K / 1e3) / 1e9
+    traffic = load_traffic(args.config)
+    dec.close()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.02) weights, uniform prompt IDs, "
+        "Philox draws)",
+        "config": {"workload": workload_text(run), "batch": B, "prompt_len": run.prompt_len,
+                   "positions": [run.prompt_len, run.prompt_len + K - 1], "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2: {bytes_step / 1e6:.1f} MB streamed per step vs "
+                         f"{L2_BYTES / 2 ** 20:.0f} MiB L2",
+                   "kernels_per_step": info.kernels_per_step, "attn_splits": info.attn_splits},
+        "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": int(info.step_h2d_bytes),
+                "d2h_bytes_per_step": int(info.step_d2h_bytes), "steps": Ke},
+        "roofline": {"bound": "hbm", "kernel": f"decode step ({info.kernels_per_step} kernels, one CUDA graph)",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+                     "bytes_per_step": int(bytes_step),
+                     "traffic": traffic},
+        "gpu_launches": int(info.kernels_per_step * K),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(run, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def load_traffic(config):
+    """Per-step DRAM bytes from the committed ncu summary of this workload, if any."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{config}.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("dram_bytes_per_step")
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+def cpu_baseline(run, seconds: float = 15.0):
+    """The oracle as it stands on the host cores: prompt processed untimed,
+    then decode steps timed until about `seconds` of CPU work."""
+    import oracle
+    from synth.weights import build_model_blob
+    m = run.model
+    blob, _ = build_model_blob(m, seed=run.weight_seed)
+    cores = os.cpu_count() or 1
+    model = oracle.Model(blob, threads=cores)
+    prompt = prompt_tokens(run)
+    draws = uniform_draws(run.draw_seed, run.n_steps + 1, m.batch)[..., 0]
+    z = None
+    for b in range(m.batch):
+        for t in prompt[b]:
+            z = model.token_forward(b, int(t), m.vocab)
+    sa = dict(temperature=run.sampler.temperature, top_k=run.sampler.top_k, top_p=run.sampler.top_p,
+              greedy=run.sampler.greedy)
+    tok = [oracle.sample(z, u=float(draws[0][b]), **sa)[0] for b in range(m.batch)]
+    n = 0
+    t0 = time.perf_counter()
+    while n < run.n_steps:
+        for b in range(m.batch):
+            z = model.token_forward(b, tok[b], m.vocab)
+            tok[b] = oracle.sample(z, u=float(draws[n + 1][b]), **sa)[0]
+        n += 1
+        if time.perf_counter() - t0 > seconds and n >= 3:
+            break
+    dt = time.perf_counter() - t0
+    model.close()
+    return {"value": round(n * m.batch / dt, 3), "unit": "tokens/s", "cores": model.threads, "kind": "oracle",
+            "sample": f"{n} decode steps at positions {run.prompt_len}..{run.prompt_len + n - 1} after an untimed "
+                      f"{run.prompt_len}-token prompt, batch {m.batch}, {model.threads} OpenMP threads"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    run = get_preset(args.config)
+    K, W = args.steps, args.warmup
+    # each "step" of this arm is a bounded sample of the same workload
+    per = max(2.0, min(20.0, 150.0 / max(1, K + W)))
+    for _ in range(W):
+        cpu_baseline(run, seconds=per / 4)
+    vals = []
+    t0 = time.perf_counter()
+    cb = None
+    for _ in range(K):
+        cb = cpu_baseline(run, seconds=per)
+        vals.append(cb["value"])
+    dt = time.perf_counter() - t0
+    value = statistics.median(vals)
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": W, "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform prompt IDs, "
+            "Philox draws)", "config": {"workload": workload_text(run), "batch": run.model.batch,
+                                        "prompt_len": run.prompt_len, "wall_s": round(dt, 1)},
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=250)
+    ap.add_argument("--warmup", type=int, default=25)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="gpt2m_q4", choices=["gpt2m_q4", "gpt2m_q8", "llama_q4", "tiny"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * sd.h -- C ABI of the single-stream speech-token decode library (libsd.so).
+ *
+ * The library runs, on one GB300 (sm_103a), the autoregressive decode step of
+ * three speech-token transformers:
+ *   - the GPT-2-Medium-style T3 of "Chatterbox -> ggml Port: Development
+ *     Journal" (section 3.2: a prompt graph and a step graph sharing one
+ *     persistent KV cache; section 3.13: the cache laid out the way the
+ *     attention reads it);
+ *   - the Llama-style T3 of the journal's section 3.19 (RMSNorm, SwiGLU, NEOX
+ *     RoPE; section 3.21: two rows decoded in one batched step);
+ *   - the Qwen3-style Talker plus code predictor of "Every Frame Is a Memory
+ *     Read" (section 1: the Talker predicts codebook 0, the code predictor runs
+ *     15 sequential passes for codebooks 1-15, and the sum of the 16 code
+ *     embeddings is the next Talker input).
+ * Weights are block quantised (Q8_0, Q4_0: journal Tier A item A3 and section
+ * 3.23; 8-bit affine groups of 64: the blog's section 3).
+ *
+ * Conventions shared by every entry point:
+ *   - Return value: SD_OK (0) or a negative SD_ERR_* code.  Nothing aborts or
+ *     exits; after an error sd_last_error() describes it, and sd_reset() or
+ *     sd_destroy() are always allowed.
+ *   - Pointers named *_dev are device pointers; every other pointer is host
+ *     memory.  The caller owns every pointer it passes; the library copies
+ *     what it keeps.
+ *   - A context is bound to one CUDA device and one stream (the caller's, or
+ *     one the library creates when `stream` is NULL).  Calls on one context
+ *     must not overlap.
+ *   - Rows: `batch` independent sequences decoded in lockstep (B <= 16); all
+ *     rows share one position counter.
+ */
+#ifndef SD_H
+#define SD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SD_OK 0
+#define SD_ERR_INVALID_ARG (-1)  /* null pointer, token out of [0, vocab), bad sampler, bad size */
+#define SD_ERR_STATE (-2)        /* call out of order (e.g. sd_step before sd_prefill) */
+#define SD_ERR_CTX_FULL (-3)     /* the position would reach max_ctx */
+#define SD_ERR_OOM (-4)          /* device or pinned allocation failed */
+#define SD_ERR_CUDA (-5)         /* a CUDA runtime call failed */
+#define SD_ERR_TIMEOUT (-6)      /* a device-side bounded wait expired */
+#define SD_ERR_UNSUPPORTED (-7)  /* valid request this build does not implement */
+#define SD_ERR_BLOB (-8)         /* weight blob malformed or not matching the config */
+#define SD_ERR_DEVICE (-9)       /* a kernel flagged an out-of-range index and skipped it */
+
+enum { SD_ARCH_GPT2 = 1, SD_ARCH_LLAMA = 2, SD_ARCH_QWEN_TTS = 3 };
+enum { SD_Q8_0 = 1, SD_Q4_0 = 2, SD_A8G64 = 3 };
+
+#define SD_MAX_ROWS 16
+#define SD_MAX_CODEBOOKS 16
+
+/* Model shape.  The field order equals the config echo stored in the weight
+ * blob header.  GPT-2 uses LayerNorm, biases, tanh GELU and learned positions;
+ * Llama and the Qwen Talker/code predictor use RMSNorm, no biases, SwiGLU and
+ * NEOX RoPE with base rope_theta.  The cp_* fields describe the code
+ * predictor and are zero for the other architectures. */
+typedef struct sd_model_config {
+    int32_t arch, n_layer, d_model, n_head, n_kv_head, head_dim, d_ff, vocab, max_ctx, batch, quant;
+    float rope_theta, norm_eps;
+    int32_t cp_layer, cp_d_model, cp_n_head, cp_n_kv_head, cp_head_dim, cp_d_ff, cp_vocab, n_codebooks,
+        cp_max_ctx;
+} sd_model_config;
+
+/* Sampler (journal section 3.2: temperature -> top-k -> top-p).  greedy != 0,
+ * top_k == 1 or temperature == 0 selects argmax (ties: lowest index).
+ * Otherwise: keep every logit >= the top_k-th largest (ties kept); softmax of
+ * logit/temperature over the kept set; if top_p < 1 keep the shortest prefix,
+ * in (probability desc, index asc) order, whose mass reaches top_p; draw the
+ * smallest vocabulary index whose cumulative kept mass (index order) exceeds
+ * u times the kept total.  Valid: temperature >= 0, top_k >= 1,
+ * 0 < top_p <= 1. */
+typedef struct sd_sampler {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+    int32_t greedy;
+} sd_sampler;
+
+typedef struct sd_ctx sd_ctx;
+
+/* Create a context on CUDA device `device`.  `stream` is a cudaStream_t or
+ * NULL.  Allocates the KV cache ([row][layer][kv_head][pos][dim] fp16),
+ * activations and pinned staging; weights come later. */
+int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out);
+
+/* Load the weight blob (the flat format written by the seeded generator:
+ * header + config echo + tensor table + canonical tensors).  `blob` is host
+ * memory, or device memory when blob_on_device != 0.  The tensors are
+ * repacked into the library's device layout; the blob may be freed after the
+ * call.  The config echo must equal the context's config. */
+int sd_load_weights(sd_ctx* ctx, const void* blob, size_t nbytes, int blob_on_device);
+
+/* Process a prompt of n tokens per row (tokens [batch][n], host) at positions
+ * 0..n-1 and sample the first generated token of each row with draw u[row].
+ * GPT-2/Llama: out_tok[batch].  Qwen Talker+CP: u and out_tok are
+ * [batch][16]: the codes of frame 0 (code 0 from the Talker's last prompt
+ * position, codes 1..15 from the code predictor).  Requires a reset context
+ * (position 0). */
+int sd_prefill(sd_ctx* ctx, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+               int32_t* out_tok);
+
+/* One decode step (GPT-2/Llama): consume tok[row] at the current position,
+ * sample the next token with draw u[row] into out_tok[row], advance. */
+int sd_step(sd_ctx* ctx, const int32_t* tok, const sd_sampler* sampler, const float* u, int32_t* out_tok);
+
+/* One frame (Qwen Talker+CP): the Talker consumes the sum of the 16 code
+ * embeddings of codes_in[row][0..15] (the previous frame), samples code 0 with
+ * `talker`; the code predictor then samples codes 1..15 with `cp`.  Draws
+ * u[row][j] feed code j.  Output codes_out[row][16]. */
+int sd_frame(sd_ctx* ctx, const int32_t* codes_in, const sd_sampler* talker, const sd_sampler* cp,
+             const float* u, int32_t* codes_out);
+
+/* Teacher forcing for the next sd_prefill/sd_frame of a Qwen context: within
+ * the frame the code fed to the next code-predictor pass is codes[row][j]
+ * instead of the sampled one (the sampled codes are still returned).  NULL
+ * clears it.  Applies to one call only. */
+int sd_set_forced_codes(sd_ctx* ctx, const int32_t* codes);
+
+/* n_steps decode steps with device-side token feedback (GPT-2/Llama): step i
+ * samples with u_dev[i][row] and writes out_dev[i][row]; its input is the
+ * previous step's token (the last sd_prefill/sd_step output for i = 0).  No
+ * host round trip between steps. */
+int sd_decode_n(sd_ctx* ctx, int32_t n_steps, const sd_sampler* sampler, const float* u_dev, int32_t* out_dev);
+
+/* Copy the last step's logits to host: [batch][vocab] (GPT-2/Llama) or
+ * [batch][16][max(vocab, cp_vocab)] (Qwen, pass j in slot j).  n_floats must
+ * be at least that size. */
+int sd_get_logits(sd_ctx* ctx, float* host_out, size_t n_floats);
+
+/* Back to position 0; weights are kept, cache contents become undefined. */
+int sd_reset(sd_ctx* ctx);
+
+void sd_destroy(sd_ctx* ctx);
+
+/* Last error message of the context (never NULL); with ctx == NULL the last
+ * error of a failed sd_create or of an op-level call on this thread. */
+const char* sd_last_error(const sd_ctx* ctx);
+
+/* Introspection for benchmarks and tests. */
+typedef struct sd_info {
+    int32_t pos;               /* current position (Talker position for Qwen) */
+    int32_t sm_count;          /* streaming multiprocessors of the device */
+    int32_t kernels_per_step;  /* kernel launches in one decode step or frame */
+    int32_t attn_splits;       /* split-KV chunks per (row, kv head) */
+    int64_t weight_bytes;      /* repacked weight bytes resident on the device */
+    int64_t kv_bytes;          /* KV cache bytes allocated */
+    int64_t step_h2d_bytes;    /* host->device bytes one sd_step copies (pinned staging) */
+    int64_t step_d2h_bytes;    /* device->host bytes one sd_step copies back */
+} sd_info;
+int sd_get_info(const sd_ctx* ctx, sd_info* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SD_H */

@@ -1,0 +1,59 @@
+/*
+ * sd_ops.h -- op-level C ABI of libsd.so: the individual decode-step kernels,
+ * exposed so that each can be checked on its own at full workload shapes.
+ * Same conventions as sd.h (SD_* return codes; *_dev pointers are device
+ * memory owned by the caller; `stream` is a cudaStream_t or NULL for the
+ * legacy default stream).  Errors are reported through sd_last_error(NULL).
+ */
+#ifndef SD_OPS_H
+#define SD_OPS_H
+
+#include "sd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A block-quantised matrix [rows][cols] (one row per output feature, cols
+ * contiguous: the orientation of "Chatterbox -> ggml Port: Development
+ * Journal", section 3.2, issue 5) repacked into the device layout the GEMV
+ * streams: codes of a row contiguous (16-byte units) and the fp16 scales (and
+ * affine biases) in a separate array.  `canon` holds the canonical blob
+ * bytes of one tensor: Q8_0 34-byte blocks, Q4_0 18-byte blocks (journal
+ * section 3.23), or affine codes + scales + biases; host memory, or device
+ * memory when on_device != 0.  cols must be a multiple of 32 (64 for
+ * SD_A8G64). */
+typedef struct sd_qmat sd_qmat;
+int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int on_device, int device,
+                   sd_qmat** out);
+void sd_qmat_destroy(sd_qmat* m);
+
+/* Dequantise to fp32 out_dev[rows][cols]: Q8_0 d*q, Q4_0 d*(q-8), affine
+ * fma(scale, q, bias) -- bit-exact definitions of the formats. */
+int sd_qmat_dequant(const sd_qmat* m, float* out_dev, void* stream);
+
+/* y_dev[b][r] = sum_k W[r][k] x_dev[b][k] (+ bias_dev[r]) for b < nb (nb 1 or
+ * 2), fp32 accumulation.  bias_dev may be NULL. */
+int sd_qmat_gemv(const sd_qmat* m, const float* x_dev, int32_t nb, const float* bias_dev, float* y_dev,
+                 void* stream);
+
+/* Sample one token per row from logits_dev[rows][V] with draws u_dev[rows];
+ * tokens to out_dev[rows].  Sampler semantics as in sd.h.  V <= 16384. */
+int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,
+                   const float* u_dev, int32_t* out_dev, void* stream);
+
+/* Decode attention for one query per head against n cached positions
+ * (journal section 3.13 flash attention over a cache laid out
+ * [head][pos][dim]): out[b][h] = softmax(q[b][h] . K[b][g][0:n] / sqrt(hd))
+ * V[b][g][0:n] with g = h / (H / Hkv).  q_dev [B][H][hd] fp32, k_dev/v_dev
+ * [B][Hkv][n_ctx][hd] fp16, out_dev [B][H][hd] fp32.  Split-KV over
+ * `nsplit` chunks per (row, kv head) then a log-sum-exp combine.  hd is 64 or
+ * 128; 1 <= n <= n_ctx. */
+int sd_attend_rows(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_dev, int32_t B, int32_t H,
+                   int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n, int32_t nsplit, float* out_dev,
+                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SD_OPS_H */

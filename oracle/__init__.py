@@ -255,13 +255,15 @@ def _sampler_args(s):
 
 
 def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: int, sampler,
-           keep_logits=True) -> list:
-    """GPT-2 / Llama: prompt then n_steps free-running decode steps per row.
+           keep_logits=True, forced=None, logit_steps=None) -> list:
+    """GPT-2 / Llama: prompt then n_steps decode steps per row.
 
     prompt [B][P]; draws [n_steps+1][B] (draw 0 samples the prefill's token).
-    Step i consumes the token sampled at step i-1 (the prefill's for i=0).
+    Step i consumes the token sampled at step i-1 (the prefill's for i=0), or,
+    with teacher forcing, forced[b][i-1] (the other implementation's token).
     Returns one Trace per row; trace.tokens[0] is the prefill's token and
-    trace.logits[0] the logits of the last prompt position."""
+    trace.logits[0] the logits of the last prompt position.  With logit_steps
+    given, only those steps keep their logits (others hold None)."""
     B = prompt.shape[0]
     V = spec.vocab
     traces = []
@@ -276,15 +278,16 @@ def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: i
             tr.tokens.append(tok)
             tr.margins.append(margin)
             if keep_logits:
-                tr.logits.append(z)
+                tr.logits.append(z if (logit_steps is None or i in logit_steps) else None)
             if i < n_steps:
-                z = model.token_forward(b, tok, V)
+                feed = tok if forced is None else int(forced[b][i])
+                z = model.token_forward(b, feed, V)
         traces.append(tr)
     return traces
 
 
 def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames: int, talker_sampler,
-             cp_sampler, keep_logits=True) -> list:
+             cp_sampler, keep_logits=True, forced=None) -> list:
     """Talker + code predictor: prompt then frames per row.
 
     Frame 0 is produced by the prompt: the last prompt position's Talker logits
@@ -292,8 +295,10 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
     runs the Talker on the sum of frame f-1's 16 code embeddings.  Within a
     frame: code-predictor position 0 takes Pr*h_T, position 1 takes Pr*E_0[c0]
     and head 1 samples c1; position j takes Pr*E_{j-1}[c_{j-1}] and head j
-    samples c_j.  draws [n_frames+1][B][16].  Returns one Trace per row with
-    tokens [16] per frame and logits as a list of 16 arrays per frame."""
+    samples c_j.  draws [n_frames+1][B][16].  With teacher forcing the codes
+    fed forward (inside the frame and into the next frame) are forced[b][f]
+    instead of the sampled ones.  Returns one Trace per row with tokens [16]
+    per frame and logits as a list of 16 arrays per frame."""
     B = prompt.shape[0]
     d, V0, Vc, ncb = spec.d_model, spec.vocab, spec.cp_vocab, spec.n_codebooks
     ta, ca = _sampler_args(talker_sampler), _sampler_args(cp_sampler)
@@ -309,8 +314,9 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
             codes.append(c0); ms.append(m0)
             model.cp_reset(b)
             model.cp_forward(b, h, 0, Vc)
+            feed = codes if forced is None else [int(c) for c in forced[b][f]]
             for j in range(1, ncb):
-                z = model.cp_forward(b, model.code_embed(j - 1, codes[j - 1], d), j, Vc)
+                z = model.cp_forward(b, model.code_embed(j - 1, feed[j - 1], d), j, Vc)
                 cj, mj = sample(z, u=float(draws[f][b][j]), **ca)
                 codes.append(cj); ms.append(mj); zs.append(z)
             tr.tokens.append(codes)
@@ -318,6 +324,7 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
             if keep_logits:
                 tr.logits.append(zs)
             if f < n_frames:
-                z0, h = model.talker_forward(b, model.code_embed_sum(codes, d), V0, d)
+                feed = codes if forced is None else [int(c) for c in forced[b][f]]
+                z0, h = model.talker_forward(b, model.code_embed_sum(feed, d), V0, d)
         traces.append(tr)
     return traces

@@ -262,7 +262,7 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     /* top-k: keep every value >= the k-th largest (ties at the threshold kept) */
     int32_t k = top_k < 1 || top_k > V ? V : top_k;
     double thr = s[k - 1].z;
-    double m_k = k < V ? s[k - 1].z - s[k].z : INFINITY;
+    double gap_k = k < V ? s[k - 1].z - s[k].z : INFINITY;
     int32_t n_keep = 0;
     while (n_keep < V && s[n_keep].z >= thr) ++n_keep;
     /* softmax over the survivors (s is already in (p desc, index asc) order) */
@@ -272,8 +272,11 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     for (int32_t t = 0; t < n_keep; ++t) p[s[t].i] = exp(s[t].z - zmax);
     for (int32_t t = 0; t < n_keep; ++t) in_s[s[t].i] = 1;
     for (int32_t i = 0; i < V; ++i) if (in_s[i]) Z += p[i];
+    /* the elements whose top-k membership a small perturbation could flip */
+    double pk_flip = 0.0;
+    if (k < V) pk_flip = exp((k < n_keep ? s[k].z : s[k - 1].z) - zmax);
     /* top-p: the shortest (p desc, index asc) prefix whose cumulative mass >= top_p */
-    double m_p = INFINITY;
+    double gap_p = INFINITY, pp_flip = 0.0;
     if (top_p < 1.0f) {
         double cum = 0.0, prev = 0.0;
         int32_t cut = n_keep - 1;
@@ -282,8 +285,10 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
             cum += p[s[t].i] / Z;
             if (cum >= (double)top_p) { cut = t; break; }
         }
-        m_p = fabs(cum - (double)top_p);
-        if (cut > 0 && fabs((double)top_p - prev) < m_p) m_p = fabs((double)top_p - prev);
+        gap_p = fabs(cum - (double)top_p);
+        if (cut > 0 && fabs((double)top_p - prev) < gap_p) gap_p = fabs((double)top_p - prev);
+        pp_flip = p[s[cut].i];
+        if (cut + 1 < n_keep && p[s[cut + 1].i] > pp_flip) pp_flip = p[s[cut + 1].i];
         for (int32_t t = cut + 1; t < n_keep; ++t) in_s[s[t].i] = 0;
     }
     /* draw in vocabulary order */
@@ -299,8 +304,16 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         if (c > target) { tok = i; break; }
     }
     if (tok < 0) { tok = last; c_lo = c - p[last]; }
+    /* Decision margin: the distance of the draw to the chosen token's CDF edges
+     * (normalised).  A top-k or top-p membership flip of element e moves the
+     * normalised draw position by at most p_e / zs, so a near-tie at those
+     * boundaries only matters when the draw lies within that distance of an edge;
+     * then the boundary gap bounds the margin too. */
     double m_u = fmin(target - c_lo, c - target) / zs;
-    if (margin) *margin = fmin(m_u, fmin(m_k, m_p));
+    double m = m_u;
+    if (m_u <= pk_flip / zs && gap_k < m) m = gap_k;
+    if (m_u <= pp_flip / zs && gap_p < m) m = gap_p;
+    if (margin) *margin = m;
     free(s); free(p); free(in_s);
     return tok;
 }

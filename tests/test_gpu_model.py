@@ -1,0 +1,253 @@
+"""Model-level parity of libsd.so against the oracle, through the C ABI.
+
+Teacher forcing: every GPU step consumes the oracle's token (or, for the
+bench's free-running run, the oracle replays the GPU's tokens), so a flip at a
+low-margin step cannot cascade.  Acceptance, per step: logits relative L2 <=
+1e-3; sampled tokens identical unless the oracle's decision margin is < 1e-4.
+"""
+
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import get_preset, prompt_tokens, uniform_draws
+from synth import presets as P
+from synth.presets import SamplerSpec
+from synth.weights import build_model_blob
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-3
+MARGIN = 1e-4
+SAMPLER_MARGIN = 1e-5   # same logits on both sides: fp32 vs fp64 sampler arithmetic only
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def sd():
+    import __graft_entry__
+    __graft_entry__.build()
+    import autoregressive_speech_token_gb300 as pkg
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    return pkg
+
+
+_BLOBS = {}
+
+
+def _blob(spec):
+    key = repr(spec)
+    if key not in _BLOBS:
+        _BLOBS.clear()
+        _BLOBS[key] = build_model_blob(spec)[0]
+    return _BLOBS[key]
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / np.linalg.norm(np.asarray(b, np.float64)))
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check_t3(sd, run, n_steps, prompt=None, spec=None):
+    spec = spec or run.model
+    blob = _blob(spec)
+    prompt = prompt_tokens(run) if prompt is None else prompt
+    B = spec.batch
+    draws = uniform_draws(run.draw_seed, n_steps + 1, B)[..., 0]
+    ref = oracle.run_t3(oracle.Model(blob, THREADS), spec, prompt, draws, n_steps, run.sampler)
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    s = sd.Sampler.from_spec(run.sampler)
+    got = dec.prefill(prompt, s, draws[0])
+    worst, clear = 0.0, 0
+    sa = dict(temperature=run.sampler.temperature, top_k=run.sampler.top_k, top_p=run.sampler.top_p,
+              greedy=run.sampler.greedy)
+    for i in range(n_steps + 1):
+        z = dec.logits()
+        for b in range(B):
+            r = _rel(z[b], ref[b].logits[i])
+            worst = max(worst, r)
+            assert r <= REL_L2, (i, b, r)
+            # the device sampler decides like the oracle's sampler on the same (device) logits
+            tg, mg = oracle.sample(z[b], u=float(draws[i][b]), **sa)
+            if mg >= SAMPLER_MARGIN:
+                assert int(got[b]) == tg, ("sampler", i, b, int(got[b]), tg, mg)
+            if ref[b].margins[i] >= MARGIN:
+                clear += 1
+                assert int(got[b]) == ref[b].tokens[i], ("parity", i, b, int(got[b]), ref[b].tokens[i],
+                                                         ref[b].margins[i], r, tg, mg)
+        if i < n_steps:
+            fed = np.array([ref[b].tokens[i] for b in range(B)], np.int32)
+            got = dec.step(fed, s, draws[i + 1])
+    dec.close()
+    print(f"[{run.name} {P.QUANT_NAMES[spec.quant]}] steps {n_steps + 1} x rows {B}: worst logits rel L2 "
+          f"{worst:.2e}, clear-margin steps {clear}")
+    return worst
+
+
+def test_tiny_full_run(sd):
+    run = get_preset("tiny")
+    worst = _check_t3(sd, run, run.n_steps)
+    assert worst < 1e-4
+
+
+def test_tiny_q4_sampled(sd):
+    run = get_preset("tiny").with_model(quant=P.Q4_0)
+    run = dataclasses.replace(run, sampler=SamplerSpec(0.8, 1000, 0.95, False))
+    _check_t3(sd, run, 40)
+
+
+def test_gpt2m_q8_greedy(sd):
+    _check_t3(sd, get_preset("gpt2m_q8"), 6)
+
+
+def test_gpt2m_q4_sampled(sd):
+    _check_t3(sd, get_preset("gpt2m_q4"), 6)
+
+
+def test_llama_q4_two_rows(sd):
+    _check_t3(sd, get_preset("llama_q4"), 6)
+
+
+def test_llama_gqa_small(sd):
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=3, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q8_0)
+    run = get_preset("llama_q4").with_model(**{f: getattr(spec, f) for f in
+                                               ("n_layer", "d_model", "n_head", "n_kv_head", "d_ff", "vocab",
+                                                "max_ctx", "quant")})
+    prompt = np.random.default_rng(1).integers(0, 1000, size=(2, 40)).astype(np.int32)
+    _check_t3(sd, run, 30, prompt=prompt)
+
+
+def test_bench_configuration_gpt2m_q4(sd):
+    """The benchmark's launch configuration: prompt 150, then 250 steps with
+    device-side feedback (sd_decode_n, draws resident on the device).  The
+    oracle replays the GPU's token stream; tokens must agree at every step
+    with a clear margin, and the final step's logits within tolerance."""
+    run = get_preset("gpt2m_q4")
+    spec = run.model
+    blob = _blob(spec)
+    prompt = prompt_tokens(run)
+    n = run.n_steps
+    draws = uniform_draws(run.draw_seed, n + 1, 1)[..., 0]
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    s = sd.Sampler.from_spec(run.sampler)
+    first = dec.prefill(prompt, s, draws[0])
+    u_dev = torch.from_numpy(np.ascontiguousarray(draws[1:])).cuda()
+    out_dev = torch.zeros(n, 1, dtype=torch.int32, device="cuda")
+    dec.decode_n(n, s, u_dev, out_dev)
+    toks = [int(first[0])] + [int(t) for t in out_dev.cpu().numpy()[:, 0]]
+    z_last = dec.logits()[0]
+    dec.close()
+    forced = [toks[:n]]
+    ref = oracle.run_t3(oracle.Model(blob, THREADS), spec, prompt, draws, n, run.sampler, forced=forced,
+                        logit_steps={n})[0]
+    clear = [i for i in range(n + 1) if ref.margins[i] >= MARGIN]
+    print(f"[bench config] clear-margin steps {len(clear)}/{n + 1}, final logits rel L2 "
+          f"{_rel(z_last, ref.logits[n]):.2e}")
+    assert len(clear) >= 0.9 * (n + 1)
+    for i in clear:
+        assert toks[i] == ref.tokens[i], (i, toks[i], ref.tokens[i], ref.margins[i])
+    # the final step consumed toks[n-1] at position 150 + n - 1
+    assert _rel(z_last, ref.logits[n]) <= REL_L2
+
+
+def test_decode_n_equals_step_chain_bitwise(sd):
+    run = get_preset("tiny").with_model(quant=P.Q4_0)
+    spec = run.model
+    blob = _blob(spec)
+    prompt = prompt_tokens(run)
+    n = 20
+    draws = uniform_draws(7, n + 1, 1)[..., 0]
+    s = sd.Sampler(0.8, 1000, 0.95, 0)
+    a = sd.Decoder(spec, blob, stream=_stream())
+    t = a.prefill(prompt, s, draws[0])
+    chain = [int(t[0])]
+    for i in range(n):
+        t = a.step(np.array([chain[-1]], np.int32), s, draws[i + 1])
+        chain.append(int(t[0]))
+    za = a.logits()
+    a.reset()
+    t = a.prefill(prompt, s, draws[0])
+    assert int(t[0]) == chain[0]
+    out = torch.zeros(n, 1, dtype=torch.int32, device="cuda")
+    a.decode_n(n, s, torch.from_numpy(np.ascontiguousarray(draws[1:])).cuda(), out)
+    assert [int(x) for x in out.cpu().numpy()[:, 0]] == chain[1:]
+    assert np.array_equal(a.logits().view(np.uint32), za.view(np.uint32))
+    a.close()
+
+
+def test_errors_and_context_limit(sd):
+    spec = P.ModelSpec(arch=P.ARCH_GPT2, n_layer=1, d_model=256, n_head=4, n_kv_head=4, head_dim=64,
+                       d_ff=512, vocab=300, max_ctx=40, batch=1, quant=P.Q8_0)
+    blob = _blob(spec)
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    s = sd.Sampler(1.0, 1, 1.0, 1)
+    u = np.zeros(1, np.float32)
+    with pytest.raises(sd.SdError) as e:
+        dec.step(np.array([1], np.int32), s, u)
+    assert e.value.code == -2                                        # SD_ERR_STATE
+    with pytest.raises(sd.SdError) as e:
+        dec.prefill(np.array([[1, 300]], np.int32), s, u)
+    assert e.value.code == -1                                        # token out of range
+    with pytest.raises(sd.SdError) as e:
+        dec.prefill(np.array([[1, 2]], np.int32), sd.Sampler(0.5, 0, 0.9, 0), u)
+    assert e.value.code == -1                                        # top_k < 1
+    t = dec.prefill(np.arange(38, dtype=np.int32)[None], s, u)
+    first = int(t[0])
+    t = dec.step(t, s, u)
+    t = dec.step(t, s, u)                                            # position 39: the last slot
+    with pytest.raises(sd.SdError) as e:
+        dec.step(t, s, u)
+    assert e.value.code == -3                                        # SD_ERR_CTX_FULL
+    dec.reset()                                                      # recovers after the error
+    assert int(dec.prefill(np.arange(38, dtype=np.int32)[None], s, u)[0]) == first
+    dec.close()
+
+
+# ----------------------------------------------------------------------------- Talker + code predictor
+
+def _check_qwen(sd, spec, prompt, n_frames, sampler, free_run_frames=0):
+    blob = _blob(spec)
+    B = spec.batch
+    draws = uniform_draws(3, n_frames + 1, B, 16)
+    ref = oracle.run_qwen(oracle.Model(blob, THREADS), spec, prompt, draws, n_frames, sampler, sampler)
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    s = sd.Sampler.from_spec(sampler)
+    dec.force(np.array([ref[b].tokens[0] for b in range(B)], np.int32))
+    codes = dec.prefill(prompt, s, draws[0])
+    for f in range(n_frames + 1):
+        z = dec.logits()
+        for b in range(B):
+            for j in range(16):
+                V = spec.vocab if j == 0 else spec.cp_vocab
+                r = _rel(z[b, j, :V], ref[b].logits[f][j])
+                assert r <= REL_L2, (f, b, j, r)
+                if ref[b].margins[f][j] >= MARGIN:
+                    assert int(codes[b, j]) == ref[b].tokens[f][j], (f, b, j)
+        if f < n_frames:
+            prev = np.array([ref[b].tokens[f] for b in range(B)], np.int32)
+            dec.force(np.array([ref[b].tokens[f + 1] for b in range(B)], np.int32))
+            codes = dec.frame(prev, s, s, draws[f + 1])
+    dec.close()
+
+
+def test_qwen_small(sd):
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=2, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
+    prompt = np.random.default_rng(3).integers(0, 300, size=(2, 12)).astype(np.int32)
+    _check_qwen(sd, spec, prompt, 4, SamplerSpec(0.9, 50, 0.95, False))
+
+
+def test_qwen_full_size(sd):
+    run = get_preset("qwen_a8")
+    _check_qwen(sd, run.model, prompt_tokens(run), 2, run.sampler)
