@@ -147,8 +147,6 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
 
     __shared__ float s_scr[33 * NB];
     __shared__ float s_tot[8 * R * NB];
-    __shared__ float s_stat[2 * NB];
-    __shared__ float s_cw[NB * 512];
     extern __shared__ float s_x[];  // [NB][K] transformed activations
 
     // element index of the lane's unit u (units lie wholly inside or outside K)
@@ -167,76 +165,75 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
     pdl_wait();  // activations come from the previous kernel
 
     // ---------------------------------------------------------------- prologue
+    // stage the activation rows in shared memory with 16-byte loads (one pass
+    // over global memory), then normalise in place
+    {
+        const int K4 = K >> 2;
+        const float4* xg = reinterpret_cast<const float4*>(a.x);
+        float4* xs4 = reinterpret_cast<float4*>(s_x);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
+            const int b = i / K4, k4 = i - b * K4;
+            xs4[i] = xg[(size_t)b * (a.x_stride >> 2) + k4];
+        }
+    }
+    __syncthreads();
     if (a.pro == PRO_LN || a.pro == PRO_RMS) {
         float v[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float s = 0.f;
             for (int k = threadIdx.x; k < K; k += blockDim.x) {
-                const float xv = a.x[(size_t)b * a.x_stride + k];
+                const float xv = s_x[b * K + k];
                 s += (a.pro == PRO_LN) ? xv : xv * xv;
             }
             v[b] = s;
         }
         block_sum<NB>(v, s_scr);
+        float mu[NB], rs[NB];
         if (a.pro == PRO_LN) {
-            float mu[NB];
 #pragma unroll
             for (int b = 0; b < NB; ++b) mu[b] = v[b] / (float)K;
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 float s = 0.f;
                 for (int k = threadIdx.x; k < K; k += blockDim.x) {
-                    const float dx = a.x[(size_t)b * a.x_stride + k] - mu[b];
+                    const float dx = s_x[b * K + k] - mu[b];
                     s = fmaf(dx, dx, s);
                 }
                 v[b] = s;
             }
             block_sum<NB>(v, s_scr);
-            if (threadIdx.x < NB) {
-                s_stat[threadIdx.x] = mu[threadIdx.x];
-                s_stat[NB + threadIdx.x] = 1.0f / sqrtf(v[threadIdx.x] / (float)K + a.eps);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) rs[b] = 1.0f / sqrtf(v[b] / (float)K + a.eps);
+        } else {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                mu[b] = 0.f;
+                rs[b] = 1.0f / sqrtf(v[b] / (float)K + a.eps);
             }
-        } else if (threadIdx.x < NB) {
-            s_stat[threadIdx.x] = 0.f;
-            s_stat[NB + threadIdx.x] = 1.0f / sqrtf(v[threadIdx.x] / (float)K + a.eps);
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
-            const int b = i / K, k = i - b * K;
-            const float xv = a.x[(size_t)b * a.x_stride + k];
-            s_x[i] = (a.pro == PRO_LN) ? fmaf((xv - s_stat[b]) * s_stat[NB + b], a.ng[k], a.nbias[k])
-                                       : xv * s_stat[NB + b] * a.ng[k];
-        }
-    } else if (a.pro == PRO_ATTN) {
-        // log-sum-exp combine weights of the split-KV partials, per (row, head)
-        const int H = a.n_head, S = a.nsplit, hd = a.head_dim, ps = part_stride(hd);
-        for (int bh = threadIdx.x; bh < NB * H; bh += blockDim.x) {
-            const float* p = a.part + (size_t)bh * S * ps;
-            float M = -INFINITY;
-            for (int s = 0; s < S; ++s) M = fmaxf(M, p[s * ps + hd]);
-            float L = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float e = (p[s * ps + hd + 1] > 0.f) ? expf(p[s * ps + hd] - M) : 0.f;
-                s_cw[bh * S + s] = e;
-                L = fmaf(e, p[s * ps + hd + 1], L);
+        const int K4 = K >> 2;
+        const float4* g4 = reinterpret_cast<const float4*>(a.ng);
+        const float4* b4 = reinterpret_cast<const float4*>(a.nbias);
+        float4* xs4 = reinterpret_cast<float4*>(s_x);
+        for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
+            const int b = i / K4, k4 = i - b * K4;
+            const float4 g = g4[k4];
+            float4 x = xs4[i];
+            if (a.pro == PRO_LN) {
+                const float4 o = b4[k4];
+                x.x = fmaf((x.x - mu[b]) * rs[b], g.x, o.x);
+                x.y = fmaf((x.y - mu[b]) * rs[b], g.y, o.y);
+                x.z = fmaf((x.z - mu[b]) * rs[b], g.z, o.z);
+                x.w = fmaf((x.w - mu[b]) * rs[b], g.w, o.w);
+            } else {
+                x.x = x.x * rs[b] * g.x;
+                x.y = x.y * rs[b] * g.y;
+                x.z = x.z * rs[b] * g.z;
+                x.w = x.w * rs[b] * g.w;
             }
-            const float inv = 1.0f / L;
-            for (int s = 0; s < S; ++s) s_cw[bh * S + s] *= inv;
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
-            const int b = i / K, e = i - b * K, h = e / hd, dd = e - h * hd;
-            const float* p = a.part + ((size_t)(b * H + h) * S) * ps + dd;
-            const float* cw = s_cw + (b * H + h) * S;
-            float v = 0.f;
-            for (int s = 0; s < S; ++s) v = fmaf(cw[s], p[s * ps], v);
-            s_x[i] = v;
-        }
-    } else {
-        for (int i = threadIdx.x; i < NB * K; i += blockDim.x) {
-            const int b = i / K, k = i - b * K;
-            s_x[i] = a.x[(size_t)b * a.x_stride + k];
+            xs4[i] = x;
         }
     }
     __syncthreads();
@@ -348,7 +345,7 @@ cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
     int WR = 8 / WK;
     if (WR < 1) WR = 1;
     // fewer rows per CTA when the matrix is short, so that every SM gets work
-    while (WR > 1 && (a.W.rows + WR * R - 1) / (WR * R) < 2 * sm_count) WR >>= 1;
+    while (WR > 1 && (a.W.rows + WR * R - 1) / (WR * R) < sm_count) WR >>= 1;
     const int tiles = (a.W.rows + WR * R - 1) / (WR * R);
     const int grid = tiles < 32 * sm_count ? tiles : 32 * sm_count;
     const size_t smem = sizeof(float) * (size_t)NB * K;
@@ -362,8 +359,7 @@ cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
 inline cudaError_t check_gemv(const GemvArgs& a) {
     if (a.W.cols % 32 || (a.W.kind == SD_A8G64 && a.W.cols % 64) || a.W.cols > 8192) return cudaErrorInvalidValue;
     if (a.epi == EPI_SWIGLU && a.W.rows % 2) return cudaErrorInvalidValue;
-    if (a.pro == PRO_ATTN && (a.n_head * a.nsplit > 512 || a.n_head * a.head_dim != a.W.cols))
-        return cudaErrorInvalidValue;
+    if (a.x_stride % 4 || (reinterpret_cast<uintptr_t>(a.x) & 15)) return cudaErrorInvalidValue;
     if (a.nb != 1 && a.nb != 2) return cudaErrorInvalidValue;
     return cudaSuccess;
 }

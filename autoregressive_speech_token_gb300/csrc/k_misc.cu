@@ -77,9 +77,19 @@ __global__ void k_embed(const EmbedArgs a) {
         if (threadIdx.x == 0 && a.err) atomicExch(a.err, 3);
         tok = 0;
     }
-    const float* e = a.table + (size_t)tok * a.d;
-    const float* p = a.pos_table ? a.pos_table + (size_t)min(max(pos, 0), a.n_ctx - 1) * a.d : nullptr;
-    for (int i = threadIdx.x; i < a.d; i += blockDim.x) a.x[(size_t)b * a.d + i] = p ? e[i] + p[i] : e[i];
+    const float4* e = reinterpret_cast<const float4*>(a.table + (size_t)tok * a.d);
+    const float4* p = a.pos_table
+                          ? reinterpret_cast<const float4*>(a.pos_table + (size_t)min(max(pos, 0), a.n_ctx - 1) * a.d)
+                          : nullptr;
+    float4* x = reinterpret_cast<float4*>(a.x + (size_t)b * a.d);
+    for (int i = threadIdx.x; i < (a.d >> 2); i += blockDim.x) {
+        float4 v = e[i];
+        if (p) {
+            const float4 q = p[i];
+            v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+        }
+        x[i] = v;
+    }
 }
 
 __global__ void k_embed_sum(const EmbedSumArgs a) {
@@ -112,7 +122,9 @@ __global__ void k_embed_code(const EmbedCodeArgs a) {
         if (threadIdx.x == 0 && a.err) atomicExch(a.err, 5);
         c = 0;
     }
-    for (int i = threadIdx.x; i < a.d; i += blockDim.x) a.x[(size_t)b * a.d + i] = a.table[(size_t)c * a.d + i];
+    const float4* src = reinterpret_cast<const float4*>(a.table + (size_t)c * a.d);
+    float4* dst = reinterpret_cast<float4*>(a.x + (size_t)b * a.d);
+    for (int i = threadIdx.x; i < (a.d >> 2); i += blockDim.x) dst[i] = src[i];
 }
 
 __global__ void k_advance(int* a, int add_a, int* b, int add_b, int* c, int set_c) {

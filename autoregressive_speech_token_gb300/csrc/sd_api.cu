@@ -16,6 +16,7 @@
 #include <cstdarg>
 #include <cstddef>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <unordered_map>
@@ -70,7 +71,8 @@ struct DStack {
     const float *nfg = nullptr, *nfb = nullptr;
     __half *kc = nullptr, *vc = nullptr;
     float *rope_cos = nullptr, *rope_sin = nullptr;
-    float *x = nullptr, *qkv = nullptr, *part = nullptr, *u = nullptr;
+    float *x = nullptr, *qkv = nullptr, *part = nullptr, *u = nullptr, *o = nullptr;
+    int* counters = nullptr;
     int qkv_rows() const { return (H + 2 * Hkv) * hd; }
 };
 
@@ -108,6 +110,14 @@ struct sd_ctx {
     cudaGraphExec_t g_step = nullptr, g_body = nullptr, g_frame = nullptr, g_prompt_last = nullptr;
     int kernels_per_step = 0;
     int count_launch = 0;
+
+    // persistent step kernel (GPT-2/Llama): one cooperative launch per step or per decode_n
+    bool persistent = false;
+    StepArgs step;
+    std::string trace_path;             // SD_TRACE: per-phase timings of the persistent step
+    StepLayer* step_layers = nullptr;   // device [n_layer]
+    unsigned* bar = nullptr;
+    int step_grid = 0;
 };
 
 namespace {
@@ -168,7 +178,7 @@ void init_stack(DStack& s, bool gpt2, int n_layer, int d, int H, int Hkv, int hd
     s.eps = eps; s.theta = theta;
     // split-KV chunks: enough CTAs for the grid at typical lengths, never more than the capacity needs
     s.nsplit = n_ctx >= 256 ? 8 : (n_ctx >= 64 ? 4 : 1);
-    if (H * s.nsplit > 512) s.nsplit = 512 / H;
+
 }
 
 int alloc_stack(sd_ctx* c, DStack& s) {
@@ -180,6 +190,7 @@ int alloc_stack(sd_ctx* c, DStack& s) {
     const int wide = std::max(s.qkv_rows(), 2 * s.ff);
     if ((rc = dalloc(c, &s.x, sizeof(float) * B * s.d)) || (rc = dalloc(c, &s.qkv, sizeof(float) * B * wide)) ||
         (rc = dalloc(c, &s.part, sizeof(float) * B * s.H * s.nsplit * part_stride(s.hd))) ||
+        (rc = dalloc(c, &s.o, sizeof(float) * B * s.H * s.hd)) || (rc = dalloc(c, &s.counters, sizeof(int) * B * s.Hkv)) ||
         (rc = dalloc(c, &s.u, sizeof(float) * B * std::max(s.ff, s.d))))
         return rc;
     if (!s.gpt2) {
@@ -225,14 +236,15 @@ int enqueue_layers(sd_ctx* c, DStack& s, const int* pos_ptr, cudaStream_t st) {
         a.kc = s.kc; a.vc = s.vc; a.row_heads = s.n_layer * s.Hkv; a.head_off = l * s.Hkv;
         a.n_head = s.H; a.n_kv = s.Hkv; a.hd = s.hd; a.n_ctx = s.n_ctx; a.nsplit = s.nsplit;
         a.pos_ptr = pos_ptr; a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.part = s.part;
+        a.counters = s.counters; a.out = s.o; a.out_stride = qd;
         a.err = &c->ds->err;
         cudaError_t e = launch_attention(a, B, st);
         c->count_launch++;
         if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
 
         GemvArgs o;
-        o.W = L.wo; o.nb = B; o.pro = PRO_ATTN; o.part = s.part; o.n_head = s.H; o.head_dim = s.hd;
-        o.nsplit = s.nsplit; o.epi = EPI_LINEAR; o.bias = L.bo; o.resid = s.x; o.y = s.x; o.y_stride = d;
+        o.W = L.wo; o.nb = B; o.x = s.o; o.x_stride = qd; o.pro = PRO_NONE;
+        o.epi = EPI_LINEAR; o.bias = L.bo; o.resid = s.x; o.y = s.x; o.y_stride = d;
         if ((rc = gemv(c, o, st))) return rc;
 
         GemvArgs f;
@@ -332,10 +344,24 @@ int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
     return SD_OK;
 }
 
+// One persistent step: zero the barrier counter, launch the cooperative kernel.
+int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
+    StepArgs a = c->step;
+    a.n_steps = n_steps;
+    a.u_seq = u_seq;
+    a.out_seq = out_seq;
+    CK(cudaMemsetAsync(c->bar, 0, sizeof(unsigned), st));
+    cudaError_t e = launch_step(a, c->step_grid, st);
+    c->count_launch++;
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
 enum class GraphKind { T3Step, T3Body, QwenFrame, QwenBody, QwenPromptLast };
 
 int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
     int rc;
+    if (k == GraphKind::T3Step && c->persistent) return enqueue_persistent(c, 1, nullptr, nullptr, st);
     const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
     if (k == GraphKind::QwenFrame) {
         EmbedSumArgs es;
@@ -489,6 +515,80 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
 // previous codes and forced codes.
 constexpr size_t kStepH2D = offsetof(DevState, u) - offsetof(DevState, prompt_on);
 constexpr size_t kStepD2H = offsetof(DevState, u1);
+bool persistent_wanted() {
+    const char* e = getenv("SD_PERSISTENT");
+    return !(e && e[0] == '0');
+}
+
+// Persistent step plan for GPT-2/Llama with Q8_0/Q4_0 weights and B <= 2.
+int setup_persistent(sd_ctx* c) {
+    const sd_model_config& m = c->cfg;
+    c->persistent = false;
+    if (!persistent_wanted() || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
+    if (m.d_model % 256 || m.d_ff % 256 || (m.n_head * m.head_dim) % 256 || m.d_model > 8192 || m.d_ff > 8192)
+        return SD_OK;
+    DStack& s = c->main;
+    std::vector<StepLayer> L(s.n_layer);
+    for (int l = 0; l < s.n_layer; ++l) {
+        const DLayer& D = s.L[l];
+        L[l].n1g = D.n1g; L[l].n1b = D.n1b; L[l].bqkv = D.bqkv; L[l].bo = D.bo;
+        L[l].n2g = D.n2g; L[l].n2b = D.n2b; L[l].bfc = D.bfc; L[l].bproj = D.bproj;
+        L[l].wqkv = D.wqkv; L[l].wo = D.wo; L[l].wfc = D.wfc; L[l].wproj = D.wproj;
+    }
+    int rc;
+    if ((rc = dalloc(c, &c->step_layers, sizeof(StepLayer) * std::max(1, s.n_layer)))) return rc;
+    if (s.n_layer) CK(cudaMemcpy(c->step_layers, L.data(), sizeof(StepLayer) * s.n_layer, cudaMemcpyHostToDevice));
+    if ((rc = dalloc(c, &c->bar, 256))) return rc;
+    StepArgs& a = c->step;
+    a.gpt2 = s.gpt2 ? 1 : 0; a.n_layer = s.n_layer; a.d = s.d; a.H = s.H; a.Hkv = s.Hkv; a.hd = s.hd; a.ff = s.ff;
+    a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.nsplit = s.nsplit; a.quant = m.quant; a.eps = s.eps;
+    a.layers = c->step_layers; a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
+    a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.kc = s.kc; a.vc = s.vc;
+    a.x = s.x; a.qkv = s.qkv; a.o = s.o; a.u = s.u; a.logits = c->logits; a.part = s.part; a.counters = s.counters;
+    a.pos = &c->ds->pos; a.tok = c->ds->tok; a.u1 = c->ds->u1; a.sp = &c->ds->samp[0]; a.err = &c->ds->err;
+    a.bar = c->bar;
+    int clock_khz = 0;
+    cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
+    a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per barrier wait
+    if (step_smem_bytes(a) > 220 * 1024) return SD_OK;
+    c->step_grid = step_max_grid(a, c->sm_count);
+    cudaGetLastError();
+    c->persistent = c->step_grid > 0;
+    if (const char* tp = getenv("SD_TRACE")) {
+        c->trace_path = tp;
+        a.trace_cap = (1 + 5 * s.n_layer + 2) * 512;  // up to 512 steps per launch
+        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * (a.trace_cap + 1)))) return rc;
+    }
+    return SD_OK;
+}
+
+// Per-phase mean durations of the last persistent launch, appended to SD_TRACE.
+void write_trace(sd_ctx* c, int n_steps) {
+    if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
+    const int L = c->step.n_layer, per = 1 + 5 * L + 2;
+    const int n = std::min(n_steps * per, c->step.trace_cap);
+    std::vector<unsigned long long> t(c->step.trace_cap + 1);
+    if (cudaMemcpy(t.data(), c->step.trace, sizeof(unsigned long long) * t.size(), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+        return;
+    const char* names[8] = {"embed", "qkv", "attn", "o", "fc", "proj", "head", "sample"};
+    double acc[8] = {0}, cnt[8] = {0};
+    unsigned long long prev = t[c->step.trace_cap];
+    for (int i = 0; i < n; ++i) {
+        const int k = i % per;
+        const int kind = k == 0 ? 0 : (k <= 5 * L ? 1 + (k - 1) % 5 : (k == 5 * L + 1 ? 6 : 7));
+        acc[kind] += (double)(t[i] - prev);
+        cnt[kind] += 1;
+        prev = t[i];
+    }
+    FILE* f = fopen(c->trace_path.c_str(), "a");
+    if (!f) return;
+    fprintf(f, "steps=%d total_us_per_step=%.2f", n / per, (double)(t[n - 1] - t[c->step.trace_cap]) / 1e3 / (n / per));
+    for (int k = 0; k < 8; ++k) fprintf(f, " %s=%.3f", names[k], cnt[k] ? acc[k] / cnt[k] / 1e3 : 0.0);
+    fprintf(f, "  (us per phase instance; qkv..proj per layer)\n");
+    fclose(f);
+}
+
 int upload_inputs(sd_ctx* c, bool full) {
     const size_t a = offsetof(DevState, prompt_on);
     const size_t e = full ? offsetof(DevState, codes) : offsetof(DevState, u);
@@ -502,6 +602,7 @@ int check_device_err(sd_ctx* c) {
         const int code = c->hs->err;
         c->hs->err = 0;
         cudaMemsetAsync(&c->ds->err, 0, sizeof(int32_t), c->stream);
+        if (code == 6) return fail(c, SD_ERR_TIMEOUT, "a grid barrier of the persistent step timed out");
         return fail(c, SD_ERR_DEVICE, "a kernel flagged an out-of-range index (code %d)", code);
     }
     return SD_OK;
@@ -535,6 +636,8 @@ int check_draws(sd_ctx* c, const float* u, int n) {
 }
 
 }  // namespace
+
+void sd::set_last_error(const char* msg) { g_err = msg; }
 
 // ======================================================================= C ABI
 
@@ -645,6 +748,7 @@ int sd_load_weights(sd_ctx* c, const void* blob, size_t nbytes, int blob_on_devi
     if (rc) return rc;
     if (se != cudaSuccess) return fail(c, SD_ERR_CUDA, "weight repack: %s", cudaGetErrorString(se));
     c->weight_bytes = (int64_t)total;
+    if ((rc = setup_persistent(c))) return rc;
     // graphs
     if (c->cfg.arch == SD_ARCH_QWEN_TTS) {
         if ((rc = capture(c, GraphKind::QwenFrame, &c->g_frame, &c->kernels_per_step))) return rc;
@@ -718,6 +822,7 @@ int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sa
     c->hs->prompt_on = 1;
     c->hs->force_on = c->force_pending ? 1 : 0;
     c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
+    for (int b = 0; b < B; ++b) c->hs->tok[b] = tokens[(size_t)b * n + n - 1];  // read by the persistent step
     if ((rc = upload_inputs(c, qwen))) return rc;
     for (int i = 0; i < n - 1; ++i) CK(cudaGraphLaunch(c->g_body, c->stream));
     CK(cudaGraphLaunch(qwen ? c->g_prompt_last : c->g_step, c->stream));
@@ -770,11 +875,16 @@ int sd_decode_n(sd_ctx* c, int32_t n_steps, const sd_sampler* sampler, const flo
     c->hs->prompt_on = 0; c->hs->u_seq = u_dev; c->hs->out_seq = out_dev;
     if ((rc = upload_inputs(c, false))) return rc;
     CK(cudaMemsetAsync(&c->ds->step_idx, 0, sizeof(int32_t), c->stream));
-    for (int i = 0; i < n_steps; ++i) CK(cudaGraphLaunch(c->g_step, c->stream));
+    if (c->persistent) {
+        if (n_steps > 0 && (rc = enqueue_persistent(c, n_steps, u_dev, out_dev, c->stream))) return rc;
+    } else {
+        for (int i = 0; i < n_steps; ++i) CK(cudaGraphLaunch(c->g_step, c->stream));
+    }
     rc = download_counters(c, false);  // synchronises before the staging mirror changes
     // later per-step calls upload null sequence pointers
     c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
     if (rc) return rc;
+    if (c->persistent) write_trace(c, n_steps);
     c->host_pos += n_steps;
     return SD_OK;
 }
@@ -828,6 +938,7 @@ int sd_get_info(const sd_ctx* c, sd_info* out) {
     out->sm_count = c->sm_count;
     out->kernels_per_step = c->kernels_per_step;
     out->attn_splits = c->main.nsplit;
+    out->persistent = c->persistent ? c->step_grid : 0;
     out->weight_bytes = c->weight_bytes;
     out->kv_bytes = c->kv_bytes;
     out->step_h2d_bytes = (int64_t)kStepH2D;
@@ -959,23 +1070,25 @@ int sd_attend_rows(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_
                    int32_t hd, int32_t n_ctx, int32_t n, int32_t nsplit, float* out_dev, void* stream) {
     sd_ctx* c = nullptr;
     if (!q_dev || !k_dev || !v_dev || !out_dev || B < 1 || H < 1 || Hkv < 1 || H % Hkv || H / Hkv > 4 ||
-        (hd != 64 && hd != 128) || n < 1 || n > n_ctx || nsplit < 1 || nsplit > 64 || H * nsplit > 4096)
+        (hd != 64 && hd != 128) || n < 1 || n > n_ctx || nsplit < 1 || nsplit > 64)
         return fail(c, SD_ERR_INVALID_ARG, "sd_attend_rows: bad argument");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* part = nullptr;
     const size_t pbytes = sizeof(float) * B * H * nsplit * part_stride(hd);
-    CK(cudaMalloc(&part, pbytes + 16));
-    int* pos = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + pbytes);
+    const size_t cbytes = sizeof(int) * (size_t)B * Hkv;
+    CK(cudaMalloc(&part, pbytes + cbytes + 16));
+    int* counters = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + pbytes);
+    int* pos = counters + (size_t)B * Hkv;
     const int pm1 = n - 1;
     cudaError_t e = cudaMemcpyAsync(pos, &pm1, 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, cbytes, st);
     AttnArgs a;
     a.q = q_dev; a.q_stride = H * hd; a.knew = nullptr; a.vnew = nullptr;
     a.kc = reinterpret_cast<__half*>(const_cast<uint16_t*>(k_dev));
     a.vc = reinterpret_cast<__half*>(const_cast<uint16_t*>(v_dev));
     a.row_heads = Hkv; a.head_off = 0; a.n_head = H; a.n_kv = Hkv; a.hd = hd; a.n_ctx = n_ctx; a.nsplit = nsplit;
-    a.pos_ptr = pos; a.part = part;
+    a.pos_ptr = pos; a.part = part; a.counters = counters; a.out = out_dev; a.out_stride = H * hd; a.max_len = n;
     if (e == cudaSuccess) e = launch_attention(a, B, st);
-    if (e == cudaSuccess) e = launch_attn_combine(part, B, H, hd, nsplit, out_dev, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     cudaFree(part);
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sd_attend_rows: %s", cudaGetErrorString(e));

@@ -48,7 +48,7 @@ struct QMat {
     const void* s = nullptr;
 };
 
-enum Prologue : int { PRO_NONE = 0, PRO_LN = 1, PRO_RMS = 2, PRO_ATTN = 3 };
+enum Prologue : int { PRO_NONE = 0, PRO_LN = 1, PRO_RMS = 2 };
 enum Epilogue : int { EPI_LINEAR = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
 
 // Split-KV partial record: o[hd] (unnormalised), then m (running max) and l
@@ -58,14 +58,12 @@ __host__ __device__ inline int part_stride(int hd) { return hd + 4; }
 struct GemvArgs {
     QMat W;
     int nb = 1;                    // activation rows (1 or 2)
-    const float* x = nullptr;      // [nb][x_stride] input (ignored for PRO_ATTN)
+    const float* x = nullptr;      // [nb][x_stride] input
     int x_stride = 0;
     int pro = PRO_NONE;
     const float* ng = nullptr;     // norm gain   (PRO_LN / PRO_RMS)
     const float* nbias = nullptr;  // norm offset (PRO_LN)
     float eps = 1e-5f;
-    const float* part = nullptr;   // PRO_ATTN: [nb][n_head][nsplit][hd+4]
-    int n_head = 0, head_dim = 0, nsplit = 0;
     int epi = EPI_LINEAR;
     const float* bias = nullptr;   // [rows] (or [rows/2] after SwiGLU) -- optional
     const float* resid = nullptr;  // [nb][y_stride] added after bias -- optional, may alias y
@@ -85,9 +83,13 @@ struct AttnArgs {
     int n_head = 0, n_kv = 0, hd = 0, n_ctx = 0, nsplit = 0;
     const int* pos_ptr = nullptr;  // device: attend to positions [0, *pos_ptr + pos_add]
     int pos_add = 0;
+    int max_len = 0;               // upper bound of *pos_ptr + pos_add + 1 (0: n_ctx); sizes the staging
     const float* rope_cos = nullptr;  // [n_ctx][hd/2] or null (no RoPE)
     const float* rope_sin = nullptr;
-    float* part = nullptr;         // [B][n_head][nsplit][hd+4]
+    float* part = nullptr;         // [B][n_head][nsplit][hd+4] scratch
+    int* counters = nullptr;       // [B][n_kv] zero between launches (the last CTA resets its entry)
+    float* out = nullptr;          // o of row b, head h at out[b*out_stride + h*hd]
+    int out_stride = 0;
     int* err = nullptr;
 };
 
@@ -121,8 +123,7 @@ cudaError_t launch_gemv_q8(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_gemv_q4(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_gemv_a8(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t st);
-cudaError_t launch_attn_combine(const float* part, int B, int H, int hd, int nsplit, float* out,
-                                cudaStream_t st);
+size_t attention_smem_bytes(const AttnArgs& a);
 cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t st);
 size_t sample_smem_bytes(int V);
 
@@ -167,6 +168,42 @@ struct EmbedCodeArgs {
     int* err = nullptr;
 };
 cudaError_t launch_embed_code(const EmbedCodeArgs& a, int B, cudaStream_t st);
+
+// Persistent decode step (k_step.cu): per-layer weights and buffers.
+struct StepLayer {
+    const float *n1g = nullptr, *n1b = nullptr, *bqkv = nullptr, *bo = nullptr;
+    const float *n2g = nullptr, *n2b = nullptr, *bfc = nullptr, *bproj = nullptr;
+    QMat wqkv, wo, wfc, wproj;
+};
+struct StepArgs {
+    int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, nsplit = 1, quant = 0;
+    float eps = 1e-5f;
+    const StepLayer* layers = nullptr;  // device array [n_layer]
+    QMat head;
+    const float *nfg = nullptr, *nfb = nullptr, *wte = nullptr, *wpe = nullptr;
+    const float *rope_cos = nullptr, *rope_sin = nullptr;
+    __half *kc = nullptr, *vc = nullptr;
+    float *x = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr, *logits = nullptr, *part = nullptr;
+    int* counters = nullptr;
+    int* pos = nullptr;                  // incremented once per step
+    int32_t* tok = nullptr;              // [B] input token, overwritten with the sampled one
+    const float* u1 = nullptr;           // [B] draws when u_seq is null
+    const float* u_seq = nullptr;        // [n_steps][B] draws, or null
+    int32_t* out_seq = nullptr;          // [n_steps][B] sampled tokens, or null
+    const SampParams* sp = nullptr;
+    int* err = nullptr;
+    unsigned* bar = nullptr;             // grid-barrier counter, zero at launch
+    int n_steps = 1;
+    long long spin_budget = 0;           // clock64 cycles per barrier wait
+    unsigned long long* trace = nullptr; // optional: %globaltimer after each barrier of CTA 0
+    int trace_cap = 0;                   // entries in `trace`
+};
+size_t step_smem_bytes(const StepArgs& a);
+int step_max_grid(const StepArgs& a, int sm_count);
+cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
+
+// Message returned by sd_last_error(NULL) on this thread.
+void set_last_error(const char* msg);
 
 // *p += add for each listed counter (single thread).
 cudaError_t launch_advance(int* a, int add_a, int* b, int add_b, int* c, int set_c, cudaStream_t st);

@@ -287,6 +287,9 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         }
         gap_p = fabs(cum - (double)top_p);
         if (cut > 0 && fabs((double)top_p - prev) < gap_p) gap_p = fabs((double)top_p - prev);
+        /* the last kept and the first dropped element swap places when their
+         * logits cross: that gap bounds the cut too */
+        if (cut + 1 < n_keep && s[cut].z - s[cut + 1].z < gap_p) gap_p = s[cut].z - s[cut + 1].z;
         pp_flip = p[s[cut].i];
         if (cut + 1 < n_keep && p[s[cut + 1].i] > pp_flip) pp_flip = p[s[cut + 1].i];
         for (int32_t t = cut + 1; t < n_keep; ++t) in_s[s[t].i] = 0;
