@@ -28,7 +28,7 @@ MAX_CODEBOOKS = 16
 EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes",
            "sd_decode_n", "sd_get_logits", "sd_reset", "sd_destroy", "sd_last_error", "sd_get_info",
            "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_sample_rows",
-           "sd_attend_rows"]
+           "sd_attend_rows", "sd_attend_rows_static"]
 
 
 class SdError(RuntimeError):
@@ -97,6 +97,7 @@ def load_library(path: str | None = None):
         "sd_qmat_gemv": ([vp, vp, i32, vp, vp, vp], C.c_int),
         "sd_sample_rows": ([vp, i32, i32, C.POINTER(Sampler), vp, vp, vp], C.c_int),
         "sd_attend_rows": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp], C.c_int),
+        "sd_attend_rows_static": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp], C.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -255,6 +256,12 @@ def sd_sample_rows(logits_dev, rows: int, V: int, sampler: Sampler, u_dev, out_d
 def sd_attend_rows(q_dev, k_dev, v_dev, B, H, Hkv, hd, n_ctx, n, nsplit, out_dev, stream=None) -> None:
     _check(load_library().sd_attend_rows(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), B, H, Hkv, hd, n_ctx, n, nsplit,
                                          _ptr(out_dev), stream), None)
+
+
+def sd_attend_rows_static(q_dev, k_dev, v_dev, B, H, Hkv, hd, n_ctx, n, nsplit, out_dev, stream=None) -> None:
+    """sd_attend_rows without any device allocation (fixed scratch array)."""
+    _check(load_library().sd_attend_rows_static(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), B, H, Hkv, hd, n_ctx, n,
+                                                nsplit, _ptr(out_dev), stream), None)
 
 
 # ------------------------------------------------------------------ convenience wrapper
