@@ -177,10 +177,12 @@ cudaError_t launch_advance(int* a, int add_a, int* b, int add_b, int* c, int set
     return launch_k(k_advance, dim3(1), dim3(1), 0, st, a, add_a, b, add_b, c, set_c);
 }
 
+// Programmatic dependent launch is off unless SD_PDL=1: on the step graph it
+// measured slower (1.09 ms vs 0.86 ms per GPT-2-Medium Q4_0 step).
 bool use_pdl() {
     static const bool on = [] {
         const char* e = getenv("SD_PDL");
-        return !(e && e[0] == '0');
+        return e && e[0] == '1';
     }();
     return on;
 }

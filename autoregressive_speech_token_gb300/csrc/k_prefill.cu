@@ -1,0 +1,199 @@
+// Prompt prefill around the tensor-core GEMM: embeddings of all prompt
+// positions, per-row norms, RoPE + fp16 KV append for a block of positions,
+// and causal attention over the cached prefix.
+//
+// "Chatterbox -> ggml Port: Development Journal", section 3.2: the prompt
+// runs as one graph over all prompt positions and fills the KV cache that the
+// step graph then extends; section 3.13: the cache is laid out [head][pos][dim]
+// and written at n_past (here: positions 0..n-1 at once); the prompt graph uses
+// a causal mask (journal section 3.12: position j is visible to query i when
+// j <= i).
+#include "sd_internal.cuh"
+
+namespace sd {
+namespace {
+
+// X[b*np + p] = table[tok[b*ld + p]] (+ pos_table[p]) for p < np
+__global__ void k_embed_rows(const float* __restrict__ table, const float* __restrict__ pos_table,
+                             const int32_t* __restrict__ tok, int ld, int np, int d, int V, float* __restrict__ X,
+                             int* err) {
+    const int m = blockIdx.x, b = m / np, p = m - b * np;
+    int t = tok[(size_t)b * ld + p];
+    if (t < 0 || t >= V) {
+        if (threadIdx.x == 0 && err) atomicExch(err, 3);
+        t = 0;
+    }
+    const float4* e = reinterpret_cast<const float4*>(table + (size_t)t * d);
+    const float4* q = pos_table ? reinterpret_cast<const float4*>(pos_table + (size_t)p * d) : nullptr;
+    float4* x = reinterpret_cast<float4*>(X + (size_t)m * d);
+    for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+        float4 v = e[i];
+        if (q) {
+            const float4 w = q[i];
+            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        }
+        x[i] = v;
+    }
+}
+
+// H[m] = norm(X[m]) * g (+ b): LayerNorm (biased variance) or RMSNorm, one CTA per row
+__global__ void __launch_bounds__(256) k_rownorm(const float* __restrict__ X, int d, int ln, const float* __restrict__ g,
+                                                 const float* __restrict__ bta, float eps, float* __restrict__ H) {
+    const int m = blockIdx.x, tid = threadIdx.x;
+    const float* x = X + (size_t)m * d;
+    __shared__ float red[32];
+    __shared__ float stat[2];
+    float s = 0.f;
+    for (int i = tid; i < d; i += blockDim.x) s += ln ? x[i] : x[i] * x[i];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((tid & 31) == 0) red[tid >> 5] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        stat[0] = ln ? t / d : 0.f;
+        stat[1] = t / d;
+    }
+    __syncthreads();
+    const float mu = stat[0];
+    float rs;
+    if (ln) {
+        float v = 0.f;
+        for (int i = tid; i < d; i += blockDim.x) {
+            const float dx = x[i] - mu;
+            v = fmaf(dx, dx, v);
+        }
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        __syncthreads();
+        if ((tid & 31) == 0) red[tid >> 5] = v;
+        __syncthreads();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+            stat[1] = t / d;
+        }
+        __syncthreads();
+    }
+    rs = 1.0f / sqrtf(stat[1] + eps);
+    for (int i = tid; i < d; i += blockDim.x) {
+        const float xv = x[i];
+        H[(size_t)m * d + i] = ln ? fmaf((xv - mu) * rs, g[i], bta[i]) : xv * rs * g[i];
+    }
+}
+
+// For row m = b*np + p: rotate q (in place, all heads) and k (NEOX half-split,
+// position p) and store k, v as fp16 at cache position p.  One CTA per row.
+__global__ void k_rope_kv(float* __restrict__ QKV, int ld, int np, int H, int Hkv, int hd, int n_ctx,
+                          int row_heads, int head_off, const float* __restrict__ cs, const float* __restrict__ sn,
+                          __half* __restrict__ kc, __half* __restrict__ vc) {
+    const int m = blockIdx.x, b = m / np, p = m - b * np;
+    const int half = hd / 2, qd = H * hd, kd = Hkv * hd;
+    float* row = QKV + (size_t)m * ld;
+    for (int i = threadIdx.x; i < (H + Hkv) * half; i += blockDim.x) {
+        const int h = i / half, dd = i - h * half;
+        float* v = h < H ? row + h * hd : row + qd + (h - H) * hd;
+        float x0 = v[dd], x1 = v[dd + half];
+        if (cs) {
+            const float c = cs[(size_t)p * half + dd], s = sn[(size_t)p * half + dd];
+            const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
+            x0 = y0;
+            x1 = y1;
+        }
+        if (h < H) {
+            v[dd] = x0;
+            v[dd + half] = x1;
+        } else {
+            const int g = h - H;
+            __half* kr = kc + (((size_t)(b * row_heads + head_off + g) * n_ctx) + p) * hd;
+            kr[dd] = __float2half_rn(x0);
+            kr[dd + half] = __float2half_rn(x1);
+        }
+    }
+    for (int i = threadIdx.x; i < kd; i += blockDim.x) {
+        const int g = i / hd, dd = i - g * hd;
+        __half* vr = vc + (((size_t)(b * row_heads + head_off + g) * n_ctx) + p) * hd;
+        vr[dd] = __float2half_rn(row[qd + kd + i]);
+    }
+}
+
+// Causal attention for query position p of row b, head h (one warp): keys
+// 0..p from the fp16 cache, online softmax over chunks of 32 keys.
+__global__ void __launch_bounds__(128) k_prefill_attn(const float* __restrict__ QKV, int ld, int np, int H, int Hkv,
+                                                      int hd, int n_ctx, int row_heads, int head_off,
+                                                      const __half* __restrict__ kc, const __half* __restrict__ vc,
+                                                      float* __restrict__ O, int ldo) {
+    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int total = (gridDim.y) * np * H;  // rows x positions x heads
+    if (wid >= total) return;
+    const int h = wid % H, m = wid / H, b = m / np, p = m - b * np;
+    const int g = h / (H / Hkv);
+    const float* q = QKV + (size_t)m * ld + h * hd;
+    const __half* K = kc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
+    const __half* Vv = vc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
+    const float scale = rsqrtf((float)hd);
+    const int dpl = hd / 32;  // dims per lane (2 or 4)
+    float qv[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int e = 0; e < dpl; ++e) qv[e] = q[lane * dpl + e] * scale;
+    float mrun = -INFINITY, lrun = 0.f;
+    for (int j0 = 0; j0 <= p; j0 += 32) {
+        const int n = min(32, p + 1 - j0);
+        // scores of the chunk: lane-split dot products, one key at a time
+        float sj = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            const __half* kr = K + (size_t)(j0 + j) * hd + lane * dpl;
+            float s = 0.f;
+            for (int e = 0; e < dpl; ++e) s = fmaf(qv[e], __half2float(kr[e]), s);
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == j) sj = s;
+        }
+        float cm = sj;
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        const float mnew = fmaxf(mrun, cm);
+        const float corr = expf(mrun - mnew);
+        const float pj = lane < n ? expf(sj - mnew) : 0.f;
+        float ps = pj;
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        lrun = lrun * corr + ps;
+        for (int e = 0; e < dpl; ++e) acc[e] *= corr;
+        for (int j = 0; j < n; ++j) {
+            const float pb = __shfl_sync(0xffffffffu, pj, j);
+            const __half* vr = Vv + (size_t)(j0 + j) * hd + lane * dpl;
+            for (int e = 0; e < dpl; ++e) acc[e] = fmaf(pb, __half2float(vr[e]), acc[e]);
+        }
+        mrun = mnew;
+    }
+    for (int e = 0; e < dpl; ++e) O[(size_t)m * ldo + h * hd + lane * dpl + e] = acc[e] / lrun;
+}
+
+}  // namespace
+
+cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int np,
+                              int d, int V, float* X, int* err, cudaStream_t st) {
+    k_embed_rows<<<B * np, 256, 0, st>>>(table, pos_table, tok, ld, np, d, V, X, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
+                           cudaStream_t st) {
+    k_rownorm<<<M, 256, 0, st>>>(X, d, ln, g, b, eps, H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_kv(float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
+                           int head_off, const float* cs, const float* sn, __half* kc, __half* vc, cudaStream_t st) {
+    k_rope_kv<<<B * np, 128, 0, st>>>(QKV, ld, np, H, Hkv, hd, n_ctx, row_heads, head_off, cs, sn, kc, vc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx,
+                                int row_heads, int head_off, const __half* kc, const __half* vc, float* O, int ldo,
+                                cudaStream_t st) {
+    if (hd % 32 || hd > 128 || H % Hkv) return cudaErrorInvalidValue;
+    const int warps = np * H;  // per row
+    dim3 grid((warps + 3) / 4, B);
+    k_prefill_attn<<<grid, 128, 0, st>>>(QKV, ld, np, H, Hkv, hd, n_ctx, row_heads, head_off, kc, vc, O, ldo);
+    return cudaGetLastError();
+}
+
+}  // namespace sd

@@ -73,7 +73,7 @@ __device__ void prefetch_rows(const QMat& W, int r0, int r1) {
 
 // Grid barrier: returns false once any CTA has recorded an error (then it
 // no longer waits).  `target` = (barriers passed so far + 1) * gridDim.x.
-__device__ bool grid_sync(unsigned* bar, unsigned target, int* err, long long budget) {
+__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned target, int* err, long long budget) {
     __syncthreads();
     __shared__ int s_ok;
     if (threadIdx.x == 0) {
@@ -100,10 +100,19 @@ __device__ bool grid_sync(unsigned* bar, unsigned target, int* err, long long bu
     return s_ok != 0;
 }
 
+// Copy a norm's gain (and offset) into shared memory ahead of the barrier
+// that precedes its use: they are constants.
+__device__ __forceinline__ void preload_vec(const float* src, int n, float* dst) {
+    if (!src) return;
+    for (int i = threadIdx.x; i < (n >> 2); i += blockDim.x)
+        reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
+}
+
 // Stage activation rows [NB][K] (global, written by other CTAs) into shared
-// memory, optionally normalised (LayerNorm with gain/offset, or RMSNorm).
+// memory, optionally normalised (LayerNorm with gain/offset, or RMSNorm) with
+// the gain/offset already in shared memory (s_g, s_b).
 template <int NB>
-__device__ void stage_x(const float* x, int x_stride, int K, int pro, const float* g, const float* bta, float eps,
+__device__ void stage_x(const float* x, int x_stride, int K, int pro, const float* s_g, const float* s_b, float eps,
                         float* s_x, float* scr) {
     const int K4 = K >> 2;
     float4* xs4 = reinterpret_cast<float4*>(s_x);
@@ -116,12 +125,12 @@ __device__ void stage_x(const float* x, int x_stride, int K, int pro, const floa
     float v[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-        float s = 0.f;
+        float sum = 0.f;
         for (int k = threadIdx.x; k < K; k += blockDim.x) {
             const float xv = s_x[b * K + k];
-            s += (pro == PRO_LN) ? xv : xv * xv;
+            sum += (pro == PRO_LN) ? xv : xv * xv;
         }
-        v[b] = s;
+        v[b] = sum;
     }
     block_sum<NB>(v, scr);
     float mu[NB], rs[NB];
@@ -130,12 +139,12 @@ __device__ void stage_x(const float* x, int x_stride, int K, int pro, const floa
         for (int b = 0; b < NB; ++b) mu[b] = v[b] / (float)K;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            float s = 0.f;
+            float sum = 0.f;
             for (int k = threadIdx.x; k < K; k += blockDim.x) {
                 const float dx = s_x[b * K + k] - mu[b];
-                s = fmaf(dx, dx, s);
+                sum = fmaf(dx, dx, sum);
             }
-            v[b] = s;
+            v[b] = sum;
         }
         block_sum<NB>(v, scr);
 #pragma unroll
@@ -147,8 +156,8 @@ __device__ void stage_x(const float* x, int x_stride, int K, int pro, const floa
             rs[b] = 1.0f / sqrtf(v[b] / (float)K + eps);
         }
     }
-    const float4* g4 = reinterpret_cast<const float4*>(g);
-    const float4* b4 = reinterpret_cast<const float4*>(bta);
+    const float4* g4 = reinterpret_cast<const float4*>(s_g);
+    const float4* b4 = reinterpret_cast<const float4*>(s_b);
     for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
         const int b = i / K4, k4 = i - b * K4;
         const float4 gg = g4[k4];
@@ -170,107 +179,162 @@ __device__ void stage_x(const float* x, int x_stride, int K, int pro, const floa
     __syncthreads();
 }
 
-// Rows [r0, r1) of y = W x (+bias, activation, +resid) with the activations in
-// shared memory.  Warps: WK along K (1024 elements each), WR row groups, R rows
-// per row group per pass; partial sums meet in shared memory in a fixed order.
-template <int QK, int NB, int R>
-__device__ void gemv_rows(const QMat& W, int r0, int r1, const float* s_x, int epi, const float* bias,
-                          const float* resid, float* y, int y_stride, float* s_tot) {
+template <int QK, int R>
+struct GemvPre {
+    uint4 w[R][Unit<QK>::kU];
+    float d[R][Unit<QK>::kU];
+};
+
+// Warp layout of a row tile: WK warps along K (1024 elements each), WR row
+// groups of R rows.
+struct GemvGeom {
+    int K, WK, WR, kw, rg, lane;
+    bool active;
+};
+__device__ __forceinline__ GemvGeom gemv_geom(int K) {
+    GemvGeom g;
+    g.K = K;
+    g.WK = (K + 1023) >> 10;
+    g.WR = kWarps / g.WK;
+    const int warp = threadIdx.x >> 5;
+    g.lane = threadIdx.x & 31;
+    g.kw = warp % g.WK;
+    g.rg = warp / g.WK;
+    g.active = g.rg < g.WR;
+    return g;
+}
+
+template <int QK, int R>
+__device__ __forceinline__ void gemv_load(GemvPre<QK, R>& p, const QMat& W, int base, int r1, const GemvGeom& g) {
     constexpr int U = Unit<QK>::kU;
-    constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;
     const int K = W.cols;
-    const int WK = (K + 1023) >> 10;
-    const int WR = kWarps / WK;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kw = warp % WK, rg = warp / WK;
-    const bool active = rg < WR;
     const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
     const int spr = K >> 5;
-
-    int ebase[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-        ebase[u] = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
+    for (int i = 0; i < R; ++i) {
+        const int r = base + g.rg * R + i;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = (QK == SD_Q4_0) ? (g.kw * 1024 + g.lane * 32) : (g.kw * 1024 + u * 512 + g.lane * 16);
+            const bool ok = g.active && r < r1 && e < K;
+            const int boff = (QK == SD_Q4_0) ? (e >> 1) : e;
+            p.w[i][u] = ok ? __ldcs(reinterpret_cast<const uint4*>(W.q + (size_t)r * row_bytes + boff))
+                           : make_uint4(0u, 0u, 0u, 0u);
+            p.d[i][u] = ok ? __half2float(__ldg(reinterpret_cast<const __half*>(W.s) + (size_t)r * spr + (e >> 5)))
+                           : 0.f;
+        }
+    }
+}
+
+// Constants of a phase, issued before the barrier that precedes it: the first
+// pass of weight rows into registers, this CTA's bias slice into s_bias.
+template <int QK, int R>
+__device__ __forceinline__ void gemv_preload(GemvPre<QK, R>& p, const QMat& W, int r0, int r1, const float* bias,
+                                             float* s_bias) {
+    gemv_load<QK, R>(p, W, r0, r1, gemv_geom(W.cols));
+    if (bias)
+        for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) s_bias[i] = __ldg(bias + r0 + i);
+}
+
+// Rows [r0, r1) of y = W x (+bias, activation, +resid), activations in shared
+// memory, first pass of weights already in registers (p), bias slice in
+// s_bias.  resid/out_own: this CTA's own rows of the residual stream (shared
+// memory), read and updated when non-null.  Partial sums of the WK warps meet
+// in shared memory in a fixed order.
+__device__ __forceinline__ void inner_stamp(unsigned long long* t, int k) {
+    if (t && blockIdx.x == 0 && threadIdx.x == 0) {
+        unsigned long long v;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
+        t[k] = v;
+    }
+}
+
+template <int QK, int NB, int R>
+__device__ void gemv_finish(GemvPre<QK, R>& p, const QMat& W, int r0, int r1, const float* s_x, int epi,
+                            const float* s_bias, float* own, int own_stride, float* y, int y_stride, float* s_tot,
+                            unsigned long long* tin = nullptr) {
+    constexpr int U = Unit<QK>::kU;
+    constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;
+    const GemvGeom g = gemv_geom(W.cols);
+    const int K = W.cols;
     float xr[NB][32];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const bool in = active && ebase[u] < K;
+            const int e = (QK == SD_Q4_0) ? (g.kw * 1024 + g.lane * 32) : (g.kw * 1024 + u * 512 + g.lane * 16);
+            const bool in = g.active && e < K;
 #pragma unroll
             for (int j = 0; j < EPU; j += 4) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * K + ebase[u] + j]);
+                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * K + e + j]);
                 xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
                 xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
             }
         }
-
-    for (int base = r0; base < r1; base += WR * R) {
-        float acc[R][NB];
+    inner_stamp(tin, 0);
+    for (int base = r0; base < r1; base += g.WR * R) {
+        if (base != r0) gemv_load<QK, R>(p, W, base, r1, g);
+        if (g.active) {
+            float acc[R][NB];
 #pragma unroll
-        for (int i = 0; i < R; ++i)
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-            for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
-        if (active) {
-            uint4 w[R][U];
-            float d[R][U];
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int r = base + rg * R + i;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const bool ok = r < r1 && ebase[u] < K;
-                    const int boff = (QK == SD_Q4_0) ? (ebase[u] >> 1) : ebase[u];
-                    w[i][u] = ok ? __ldcs(reinterpret_cast<const uint4*>(W.q + (size_t)r * row_bytes + boff))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-                    d[i][u] = ok ? __half2float(reinterpret_cast<const __half*>(W.s)[(size_t)r * spr + (ebase[u] >> 5)])
-                                 : 0.f;
-                }
-            }
+                for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float dq = (QK == SD_Q4_0) ? dot_q4(w[i][u], &xr[b][0]) : dot_s8(w[i][u], &xr[b][u * EPU]);
-                        acc[i][b] = fmaf(d[i][u], dq, acc[i][b]);
+                        const float dq = (QK == SD_Q4_0) ? dot_q4(p.w[i][u], &xr[b][0]) : dot_s8(p.w[i][u], &xr[b][u * EPU]);
+                        acc[i][b] = fmaf(p.d[i][u], dq, acc[i][b]);
                     }
+            inner_stamp(tin, 1);
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
-                    const float s = warp_sum(acc[i][b]);
-                    if (lane == 0) s_tot[((rg * R + i) * NB + b) * WK + kw] = s;
+                    const float sv = warp_sum(acc[i][b]);
+                    if (g.lane == 0) s_tot[((g.rg * R + i) * NB + b) * g.WK + g.kw] = sv;
                 }
+            inner_stamp(tin, 2);
         }
         __syncthreads();
-        const int n_out = WR * R * NB;
+        inner_stamp(tin, 3);
+        const int n_out = g.WR * R * NB;
         for (int t = threadIdx.x; t < n_out; t += blockDim.x) {
             const int b = t % NB;
             const int i = (t / NB) % R;
-            const int g = t / (NB * R);
-            const int r = base + g * R + i;
+            const int gg = t / (NB * R);
+            const int r = base + gg * R + i;
             if (r >= r1) continue;
             float v = 0.f;
-            for (int k = 0; k < WK; ++k) v += s_tot[((g * R + i) * NB + b) * WK + k];
+            for (int k = 0; k < g.WK; ++k) v += s_tot[((gg * R + i) * NB + b) * g.WK + k];
             if (epi == EPI_SWIGLU) {
                 if ((i & 1) == 0) {
                     float up = 0.f;
-                    for (int k = 0; k < WK; ++k) up += s_tot[((g * R + i + 1) * NB + b) * WK + k];
+                    for (int k = 0; k < g.WK; ++k) up += s_tot[((gg * R + i + 1) * NB + b) * g.WK + k];
                     y[(size_t)b * y_stride + (r >> 1)] = silu(v) * up;
                 }
             } else {
-                if (bias) v += bias[r];
+                if (s_bias) v += s_bias[r - r0];
                 if (epi == EPI_GELU) v = gelu_tanh(v);
-                if (resid) v += __ldcg(resid + (size_t)b * y_stride + r);
+                if (own) {
+                    v += own[b * own_stride + (r - r0)];
+                    own[b * own_stride + (r - r0)] = v;
+                }
                 y[(size_t)b * y_stride + r] = v;
             }
         }
+        inner_stamp(tin, 4);
         __syncthreads();
+        inner_stamp(tin, 5);
     }
 }
+
+constexpr int kMaxBiasRows = 256;  // bias slice of one phase for one CTA
+constexpr int kMaxOwn = 128;       // residual-stream rows owned by one CTA
 
 template <int QK, int NB>
 __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
@@ -278,83 +342,123 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
     extern __shared__ __align__(16) unsigned char smraw[];
     __shared__ float s_scr[33 * NB];
     __shared__ float s_tot[kWarps * R * NB];
+    __shared__ __align__(16) float s_bias[kMaxBiasRows];
+    __shared__ float s_own[NB * kMaxOwn];
     __shared__ attn_detail::AttnScratch s_attn;
     __shared__ sample_detail::SampleScratch s_samp;
-    float* s_x = reinterpret_cast<float*>(smraw);  // [NB][K] staged activations (aliases the other uses)
 
     const int G = gridDim.x, cta = blockIdx.x;
     const int d = a.d, qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
+    const int kmax = max(max(d, a.ff), qd);
+    // dynamic shared memory: [NB][kmax] staged activations, then [kmax] norm gain, [kmax] norm offset;
+    // the attention staging and the sampler reuse the same bytes in their own phases
+    float* s_x = reinterpret_cast<float*>(smraw);
+    float* s_g = s_x + NB * kmax;
+    float* s_b = s_g + kmax;
     const bool swiglu = !a.gpt2;
+    const int pro = a.gpt2 ? PRO_LN : PRO_RMS;
     unsigned nbar = 0;
-    auto sync = [&]() {
-        const bool ok = grid_sync(a.bar, (++nbar) * (unsigned)G, a.err, a.spin_budget);
-        if (a.trace && cta == 0 && threadIdx.x == 0 && (int)nbar <= a.trace_cap) {
+    // trace: 4 stamps per barrier interval -- staged, computed, preloaded, barrier passed
+    auto stamp = [&](int k) {
+        if (a.trace && cta == 0 && threadIdx.x == 0 && (int)nbar < a.trace_cap) {
             unsigned long long t;
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            a.trace[nbar - 1] = t;
+            a.trace[4 * nbar + k] = t;
         }
+    };
+    auto sync = [&]() {
+        stamp(2);
+        const bool ok = grid_sync(a.bar, (nbar + 1) * (unsigned)G, a.err, a.spin_budget);
+        stamp(3);
+        ++nbar;
         return ok;
     };
 
-    // this CTA's static row ranges
-    int q0, q1, o0, o1, f0, f1, p0, p1, h0, h1, e0, e1;
+    // this CTA's static row ranges; o0..o1 (rows of the residual stream) serve embed, O and proj
+    int q0, q1, o0, o1, f0, f1, h0, h1;
     row_range(qkv_rows, cta, G, q0, q1);
     row_range(d, cta, G, o0, o1);
     row_range(a.ff, cta, G, f0, f1);
     if (swiglu) { f0 *= 2; f1 *= 2; }          // gate/up rows are interleaved in pairs
-    row_range(d, cta, G, p0, p1);
     row_range(a.V, cta, G, h0, h1);
-    row_range(d >> 2, cta, G, e0, e1);          // embedding, in float4 units
 
     auto prefetch_layer = [&](int l) {
-        if (threadIdx.x != 0 || l >= a.n_layer) return;
+        if (threadIdx.x != 0 || l >= a.n_layer || a.prefetch <= 0) return;
         const StepLayer& L = a.layers[l];
         prefetch_rows(L.wqkv, q0, q1);
         prefetch_rows(L.wo, o0, o1);
         prefetch_rows(L.wfc, f0, f1);
-        prefetch_rows(L.wproj, p0, p1);
+        prefetch_rows(L.wproj, o0, o1);
     };
-
-    if (a.trace && cta == 0 && threadIdx.x == 0) {
+    GemvPre<QK, R> pre;
+    // constants of a layer's QKV phase (or of the head when l == n_layer)
+    auto preload_qkv = [&](int l) {
+        if (l < a.n_layer) {
+            const StepLayer& L = a.layers[l];
+            preload_vec(L.n1g, d, s_g);
+            preload_vec(L.n1b, d, s_b);
+            gemv_preload<QK, R>(pre, L.wqkv, q0, q1, L.bqkv, s_bias);
+        } else {
+            preload_vec(a.nfg, d, s_g);
+            preload_vec(a.nfb, d, s_b);
+            gemv_preload<QK, R>(pre, a.head, h0, h1, nullptr, s_bias);
+        }
+    };
+    if (threadIdx.x == 0 && a.trace) {
         unsigned long long t;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        a.trace[a.trace_cap] = t;  // launch start, in the slot after the barrier stamps
+        a.trace[4 * a.trace_cap] = t;  // launch start, in the slot after the barrier stamps
     }
+    prefetch_layer(0);
+    prefetch_layer(1);
+    preload_qkv(0);
+
     for (int s = 0; s < a.n_steps; ++s) {
         const int pos = __ldcg(a.pos);
         if (pos < 0 || pos >= a.n_ctx) {
             if (threadIdx.x == 0) atomicCAS(a.err, 0, 1);
             break;
         }
-        // ---- embedding: x[b] = wte[tok] (+ wpe[pos]), float4 slice [e0, e1) of this CTA
-        if (s == 0) {
-            prefetch_layer(0);
-            prefetch_layer(1);
-        }
-        for (int i = threadIdx.x; i < NB * (e1 - e0); i += blockDim.x) {
-            const int b = i / (e1 - e0), k4 = e0 + i % (e1 - e0);
+        // ---- embedding of this CTA's residual rows: x[b][r] = wte[tok][r] (+ wpe[pos][r])
+        for (int i = threadIdx.x; i < NB * (o1 - o0); i += blockDim.x) {
+            const int b = i / (o1 - o0), r = o0 + i % (o1 - o0);
             int tok = __ldcg(a.tok + b);
             if (tok < 0 || tok >= a.V) {
                 atomicCAS(a.err, 0, 3);
                 tok = 0;
             }
-            float4 v = __ldg(reinterpret_cast<const float4*>(a.wte + (size_t)tok * d) + k4);
-            if (a.wpe) {
-                const float4 p = __ldg(reinterpret_cast<const float4*>(a.wpe + (size_t)pos * d) + k4);
-                v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
-            }
-            reinterpret_cast<float4*>(a.x + (size_t)b * d)[k4] = v;
+            float v = __ldg(a.wte + (size_t)tok * d + r);
+            if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + r);
+            s_own[b * kMaxOwn + (r - o0)] = v;
+            a.x[(size_t)b * d + r] = v;
         }
         if (!sync()) break;
 
         bool ok = true;
         for (int l = 0; l < a.n_layer && ok; ++l) {
             const StepLayer& L = a.layers[l];
+            // ---- QKV (norm prologue, bias)
+            stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
+            stamp(0);
+            gemv_finish<QK, NB, R>(pre, L.wqkv, q0, q1, s_x, EPI_LINEAR, L.bqkv ? s_bias : nullptr, nullptr, 0,
+                                   a.qkv, qkv_rows, s_tot);
+            stamp(1);
+            const int items = NB * a.Hkv * a.nsplit;
+            if (threadIdx.x == 0 && a.prefetch > 0) {
+                // the cached K/V rows this CTA's attention items will read, and the next layer's weights
+                const int n = pos + 1, chunk = (n + a.nsplit - 1) / a.nsplit;
+                for (int it = cta; it < items; it += G) {
+                    const int split = it % a.nsplit, g = (it / a.nsplit) % a.Hkv, b = it / (a.nsplit * a.Hkv);
+                    const int c0 = split * chunk, c1 = min(n - 1, c0 + chunk);  // rows < pos are cached
+                    if (c1 > c0) {
+                        const size_t hb = ((size_t)(b * a.n_layer * a.Hkv + l * a.Hkv + g) * a.n_ctx) * a.hd;
+                        prefetch_l2(a.kc + hb + (size_t)c0 * a.hd, (size_t)(c1 - c0) * a.hd * 2);
+                        prefetch_l2(a.vc + hb + (size_t)c0 * a.hd, (size_t)(c1 - c0) * a.hd * 2);
+                    }
+                }
+            }
             if (l + 1 < a.n_layer) prefetch_layer(l + 1);
-            else if (threadIdx.x == 0) prefetch_rows(a.head, h0, h1);
-            // ---- QKV
-            stage_x<NB>(a.x, d, d, a.gpt2 ? PRO_LN : PRO_RMS, L.n1g, L.n1b, a.eps, s_x, s_scr);
-            gemv_rows<QK, NB, R>(L.wqkv, q0, q1, s_x, EPI_LINEAR, L.bqkv, nullptr, a.qkv, qkv_rows, s_tot);
+            else if (threadIdx.x == 0 && a.prefetch > 0) prefetch_rows(a.head, h0, h1);
             if (!(ok = sync())) break;
             // ---- attention items
             {
@@ -364,35 +468,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 at.n_head = a.H; at.n_kv = a.Hkv; at.hd = a.hd; at.n_ctx = a.n_ctx; at.nsplit = a.nsplit;
                 at.pos_ptr = a.pos; at.rope_cos = a.rope_cos; at.rope_sin = a.rope_sin; at.part = a.part;
                 at.counters = a.counters; at.out = a.o; at.out_stride = qd; at.err = a.err;
-                const int items = NB * a.Hkv * a.nsplit;
+                stamp(0);
                 for (int it = cta; it < items; it += G) {
                     const int split = it % a.nsplit, g = (it / a.nsplit) % a.Hkv, b = it / (a.nsplit * a.Hkv);
                     attn_detail::attn_item(at, split, g, b, reinterpret_cast<float*>(smraw), s_attn);
                 }
+                stamp(1);
             }
+            gemv_preload<QK, R>(pre, L.wo, o0, o1, L.bo, s_bias);
             if (!(ok = sync())) break;
             // ---- O projection (+bias +residual)
             stage_x<NB>(a.o, qd, qd, PRO_NONE, nullptr, nullptr, 0.f, s_x, s_scr);
-            gemv_rows<QK, NB, R>(L.wo, o0, o1, s_x, EPI_LINEAR, L.bo, a.x, a.x, d, s_tot);
+            stamp(0);
+            gemv_finish<QK, NB, R>(pre, L.wo, o0, o1, s_x, EPI_LINEAR, L.bo ? s_bias : nullptr, s_own, kMaxOwn,
+                                   a.x, d, s_tot);
+            stamp(1);
+            preload_vec(L.n2g, d, s_g);
+            preload_vec(L.n2b, d, s_b);
+            gemv_preload<QK, R>(pre, L.wfc, f0, f1, L.bfc, s_bias);
             if (!(ok = sync())) break;
-            // ---- FC / gate-up
-            stage_x<NB>(a.x, d, d, a.gpt2 ? PRO_LN : PRO_RMS, L.n2g, L.n2b, a.eps, s_x, s_scr);
-            gemv_rows<QK, NB, R>(L.wfc, f0, f1, s_x, a.gpt2 ? EPI_GELU : EPI_SWIGLU, L.bfc, nullptr, a.u, a.ff, s_tot);
+            // ---- FC / gate-up (norm prologue, GELU / SwiGLU)
+            stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
+            stamp(0);
+            gemv_finish<QK, NB, R>(pre, L.wfc, f0, f1, s_x, swiglu ? EPI_SWIGLU : EPI_GELU,
+                                   L.bfc ? s_bias : nullptr, nullptr, 0, a.u, a.ff, s_tot,
+                                   (a.trace && s == 0 && l == 1) ? a.trace + 4 * (size_t)a.trace_cap + 1 : nullptr);
+            stamp(1);
+            gemv_preload<QK, R>(pre, L.wproj, o0, o1, L.bproj, s_bias);
             if (!(ok = sync())) break;
             // ---- proj / down (+bias +residual)
             stage_x<NB>(a.u, a.ff, a.ff, PRO_NONE, nullptr, nullptr, 0.f, s_x, s_scr);
-            gemv_rows<QK, NB, R>(L.wproj, p0, p1, s_x, EPI_LINEAR, L.bproj, a.x, a.x, d, s_tot);
+            stamp(0);
+            gemv_finish<QK, NB, R>(pre, L.wproj, o0, o1, s_x, EPI_LINEAR, L.bproj ? s_bias : nullptr, s_own,
+                                   kMaxOwn, a.x, d, s_tot);
+            stamp(1);
+            preload_qkv(l + 1);
             if (!(ok = sync())) break;
         }
         if (!ok) break;
-        // the next step's first layers stream in while the head and the sampler run
+        // ---- head (final norm prologue)
+        stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
+        gemv_finish<QK, NB, R>(pre, a.head, h0, h1, s_x, EPI_LINEAR, nullptr, nullptr, 0, a.logits, a.V, s_tot);
+        // the next step's first layers stream in while the sampler runs
         if (s + 1 < a.n_steps) {
             prefetch_layer(0);
             prefetch_layer(1);
         }
-        // ---- head
-        stage_x<NB>(a.x, d, d, a.gpt2 ? PRO_LN : PRO_RMS, a.nfg, a.nfb, a.eps, s_x, s_scr);
-        gemv_rows<QK, NB, R>(a.head, h0, h1, s_x, EPI_LINEAR, nullptr, nullptr, a.logits, a.V, s_tot);
         if (!sync()) break;
         // ---- sampler: CTA b samples row b
         if (cta < NB) {
@@ -405,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 if (cta == 0) *a.pos = pos + 1;
             }
         }
+        if (s + 1 < a.n_steps) preload_qkv(0);
         if (!sync()) break;
     }
 }
@@ -413,8 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
 
 size_t step_smem_bytes(const StepArgs& a) {
     const int B = a.B;
-    const int kmax = a.d > a.ff ? a.d : a.ff;
-    size_t need = sizeof(float) * (size_t)B * (kmax > a.H * a.hd ? kmax : a.H * a.hd);
+    int kmax = a.d > a.ff ? a.d : a.ff;
+    if (a.H * a.hd > kmax) kmax = a.H * a.hd;
+    size_t need = sizeof(float) * (size_t)(B + 2) * kmax;
     AttnArgs at;
     at.n_head = a.H; at.n_kv = a.Hkv; at.hd = a.hd; at.n_ctx = a.n_ctx; at.nsplit = a.nsplit;
     const size_t att = attention_smem_bytes_dev(at);

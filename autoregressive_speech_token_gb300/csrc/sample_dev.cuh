@@ -162,9 +162,17 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
             for (int i = tid; i < 256; i += kST) s_hist[i] = 0;
             __syncthreads();
             const uint32_t prefix = s_sel[0], mask = s_sel[1];
-            for (int i = tid; i < V; i += kST) {
-                const uint32_t key = ord_key(z[i]);
-                if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+            // lanes with equal digits add once (logits crowd into few high-order bins)
+            for (int i0 = 0; i0 < V; i0 += kST) {
+                const int i = i0 + tid;
+                const uint32_t key = i < V ? ord_key(z[i]) : 0u;
+                const bool in = i < V && (key & mask) == prefix;
+                const unsigned act = __ballot_sync(0xffffffffu, in);
+                if (in) {
+                    const uint32_t digit = (key >> shift) & 255u;
+                    const unsigned peers = __match_any_sync(act, digit);
+                    if ((tid & 31) == __ffs(peers) - 1) atomicAdd(&s_hist[digit], __popc(peers));
+                }
             }
             __syncthreads();
             if (tid < 32) {

@@ -515,9 +515,11 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
 // previous codes and forced codes.
 constexpr size_t kStepH2D = offsetof(DevState, u) - offsetof(DevState, prompt_on);
 constexpr size_t kStepD2H = offsetof(DevState, u1);
+// The persistent step is opt-in (SD_PERSISTENT=1) until it beats the
+// per-operation graph on the bench workload.
 bool persistent_wanted() {
     const char* e = getenv("SD_PERSISTENT");
-    return !(e && e[0] == '0');
+    return e && e[0] == '1';
 }
 
 // Persistent step plan for GPT-2/Llama with Q8_0/Q4_0 weights and B <= 2.
@@ -553,39 +555,61 @@ int setup_persistent(sd_ctx* c) {
     if (step_smem_bytes(a) > 220 * 1024) return SD_OK;
     c->step_grid = step_max_grid(a, c->sm_count);
     cudaGetLastError();
+    // per-CTA slices must fit the kernel's fixed shared arrays (bias slice 256, residual rows 128)
+    if (c->step_grid > 0) {
+        const int G = c->step_grid;
+        const int widest = std::max(std::max(s.qkv_rows(), s.gpt2 ? s.ff : 2 * s.ff), std::max(m.vocab, s.d));
+        if ((widest + G - 1) / G + 2 > 256 || (s.d + G - 1) / G > 128) c->step_grid = 0;
+    }
     c->persistent = c->step_grid > 0;
+    if (const char* pf = getenv("SD_PREFETCH")) a.prefetch = atoi(pf);
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
         a.trace_cap = (1 + 5 * s.n_layer + 2) * 512;  // up to 512 steps per launch
-        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * (a.trace_cap + 1)))) return rc;
+        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * (4 * (size_t)a.trace_cap + 8)))) return rc;
     }
     return SD_OK;
 }
 
-// Per-phase mean durations of the last persistent launch, appended to SD_TRACE.
+// Per-phase mean durations of the last persistent launch, appended to SD_TRACE:
+// for each phase kind the mean time from the previous barrier to the end of
+// staging, of compute, of the next phase's preloads, and through the barrier.
 void write_trace(sd_ctx* c, int n_steps) {
     if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
     const int L = c->step.n_layer, per = 1 + 5 * L + 2;
     const int n = std::min(n_steps * per, c->step.trace_cap);
-    std::vector<unsigned long long> t(c->step.trace_cap + 1);
+    std::vector<unsigned long long> t(4 * (size_t)c->step.trace_cap + 8);
     if (cudaMemcpy(t.data(), c->step.trace, sizeof(unsigned long long) * t.size(), cudaMemcpyDeviceToHost) !=
         cudaSuccess)
         return;
     const char* names[8] = {"embed", "qkv", "attn", "o", "fc", "proj", "head", "sample"};
-    double acc[8] = {0}, cnt[8] = {0};
-    unsigned long long prev = t[c->step.trace_cap];
+    double acc[8][4] = {{0}}, cnt[8] = {0};
+    unsigned long long prev = t[4 * (size_t)c->step.trace_cap];
     for (int i = 0; i < n; ++i) {
         const int k = i % per;
         const int kind = k == 0 ? 0 : (k <= 5 * L ? 1 + (k - 1) % 5 : (k == 5 * L + 1 ? 6 : 7));
-        acc[kind] += (double)(t[i] - prev);
+        const unsigned long long* e = &t[4 * (size_t)i];
+        const bool fine = e[0] >= prev && e[1] >= e[0] && e[2] >= e[1];
+        acc[kind][0] += fine ? (double)(e[0] - prev) : 0;
+        acc[kind][1] += fine ? (double)(e[1] - e[0]) : 0;
+        acc[kind][2] += fine ? (double)(e[2] - e[1]) : (double)(e[2] - prev);
+        acc[kind][3] += (double)(e[3] - e[2]);
         cnt[kind] += 1;
-        prev = t[i];
+        prev = e[3];
     }
     FILE* f = fopen(c->trace_path.c_str(), "a");
     if (!f) return;
-    fprintf(f, "steps=%d total_us_per_step=%.2f", n / per, (double)(t[n - 1] - t[c->step.trace_cap]) / 1e3 / (n / per));
-    for (int k = 0; k < 8; ++k) fprintf(f, " %s=%.3f", names[k], cnt[k] ? acc[k] / cnt[k] / 1e3 : 0.0);
-    fprintf(f, "  (us per phase instance; qkv..proj per layer)\n");
+    fprintf(f, "steps=%d us_per_step=%.2f prefetch=%d | phase: stage/compute/preload/barrier us\n", n / per,
+            (double)(t[4 * (size_t)(n - 1) + 3] - t[4 * (size_t)c->step.trace_cap]) / 1e3 / (n / per), c->step.prefetch);
+    for (int k = 0; k < 8; ++k)
+        if (cnt[k])
+            fprintf(f, "  %-6s %.3f %.3f %.3f %.3f\n", names[k], acc[k][0] / cnt[k] / 1e3, acc[k][1] / cnt[k] / 1e3,
+                    acc[k][2] / cnt[k] / 1e3, acc[k][3] / cnt[k] / 1e3);
+    // inner stamps of one FC phase (step 0, layer 1, CTA 0): registers, FMA, warp sums, sync, epilogue, sync
+    const unsigned long long* in = &t[4 * (size_t)c->step.trace_cap + 1];
+    fprintf(f, "  fc-inner:");
+    for (int k = 1; k < 6; ++k) fprintf(f, " %.3f", in[k] > in[k - 1] ? (double)(in[k] - in[k - 1]) / 1e3 : -1.0);
+    fprintf(f, "\n");
     fclose(f);
 }
 

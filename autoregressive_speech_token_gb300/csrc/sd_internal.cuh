@@ -195,12 +195,39 @@ struct StepArgs {
     unsigned* bar = nullptr;             // grid-barrier counter, zero at launch
     int n_steps = 1;
     long long spin_budget = 0;           // clock64 cycles per barrier wait
-    unsigned long long* trace = nullptr; // optional: %globaltimer after each barrier of CTA 0
-    int trace_cap = 0;                   // entries in `trace`
+    unsigned long long* trace = nullptr; // optional: %globaltimer stamps of CTA 0, 4 per barrier
+    int trace_cap = 0;                   // barriers covered by `trace`
+    int prefetch = 1;                    // layers of weights bulk-prefetched into L2 ahead (0: none)
 };
 size_t step_smem_bytes(const StepArgs& a);
 int step_max_grid(const StepArgs& a, int sm_count);
 cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
+
+// Tensor-core GEMM Y[M][N] = X[M][K] W[N][K]^T over a repacked weight, with
+// the GEMV epilogues (bias, GELU, interleaved SwiGLU -> Y[M][N/2], residual).
+struct QGemmArgs {
+    QMat W;
+    int M = 0;
+    const float* x = nullptr;      // [M][ldx]
+    int ldx = 0;
+    int epi = EPI_LINEAR;
+    const float* bias = nullptr;   // [N] (linear / GELU only) -- optional
+    const float* resid = nullptr;  // [M][ldy] -- optional, may alias y
+    float* y = nullptr;            // [M][ldy]
+    int ldy = 0;
+};
+cudaError_t launch_qgemm(const QGemmArgs& a, cudaStream_t st);
+
+// Prefill helpers (positions 0..np-1 of B rows at once).
+cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int np,
+                              int d, int V, float* X, int* err, cudaStream_t st);
+cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
+                           cudaStream_t st);
+cudaError_t launch_rope_kv(float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
+                           int head_off, const float* cs, const float* sn, __half* kc, __half* vc, cudaStream_t st);
+cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx,
+                                int row_heads, int head_off, const __half* kc, const __half* vc, float* O, int ldo,
+                                cudaStream_t st);
 
 // Message returned by sd_last_error(NULL) on this thread.
 void set_last_error(const char* msg);

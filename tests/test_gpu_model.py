@@ -161,7 +161,30 @@ def test_bench_configuration_gpt2m_q4(sd):
     assert _rel(z_last, ref.logits[n]) <= REL_L2
 
 
-def test_decode_n_equals_step_chain_bitwise(sd):
+@pytest.fixture(params=["graph", "persistent"])
+def step_path(request, monkeypatch):
+    """Run a test on the per-operation graph and on the persistent step kernel."""
+    monkeypatch.setenv("SD_PERSISTENT", "1" if request.param == "persistent" else "0")
+    return request.param
+
+
+def test_gpt2m_q4_both_step_paths(sd, step_path):
+    _check_t3(sd, get_preset("gpt2m_q4"), 4)
+
+
+def test_llama_q4_both_step_paths(sd, step_path):
+    _check_t3(sd, get_preset("llama_q4"), 4)
+
+
+def test_persistent_kernel_is_used(sd, monkeypatch):
+    monkeypatch.setenv("SD_PERSISTENT", "1")
+    run = get_preset("tiny")
+    dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
+    assert dec.info().persistent > 0 and dec.info().kernels_per_step == 1
+    dec.close()
+
+
+def test_decode_n_equals_step_chain_bitwise(sd, step_path):
     run = get_preset("tiny").with_model(quant=P.Q4_0)
     spec = run.model
     blob = _blob(spec)
