@@ -13,18 +13,18 @@
 namespace sd {
 namespace {
 
-// X[b*np + p] = table[tok[b*ld + p]] (+ pos_table[p]) for p < np
+// X[b*np + p] = table[tok[b*ld + p0 + p]] (+ pos_table[p0 + p]) for p < np
 __global__ void k_embed_rows(const float* __restrict__ table, const float* __restrict__ pos_table,
-                             const int32_t* __restrict__ tok, int ld, int np, int d, int V, float* __restrict__ X,
-                             int* err) {
+                             const int32_t* __restrict__ tok, int ld, int p0, int np, int d, int V,
+                             float* __restrict__ X, int* err) {
     const int m = blockIdx.x, b = m / np, p = m - b * np;
-    int t = tok[(size_t)b * ld + p];
+    int t = tok[(size_t)b * ld + p0 + p];
     if (t < 0 || t >= V) {
         if (threadIdx.x == 0 && err) atomicExch(err, 3);
         t = 0;
     }
     const float4* e = reinterpret_cast<const float4*>(table + (size_t)t * d);
-    const float4* q = pos_table ? reinterpret_cast<const float4*>(pos_table + (size_t)p * d) : nullptr;
+    const float4* q = pos_table ? reinterpret_cast<const float4*>(pos_table + (size_t)(p0 + p) * d) : nullptr;
     float4* x = reinterpret_cast<float4*>(X + (size_t)m * d);
     for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
         float4 v = e[i];
@@ -81,12 +81,13 @@ __global__ void __launch_bounds__(256) k_rownorm(const float* __restrict__ X, in
     }
 }
 
-// For row m = b*np + p: rotate q (in place, all heads) and k (NEOX half-split,
-// position p) and store k, v as fp16 at cache position p.  One CTA per row.
-__global__ void k_rope_kv(float* __restrict__ QKV, int ld, int np, int H, int Hkv, int hd, int n_ctx,
+// For row m = b*np + i at position p = p0 + i: rotate q (in place, all
+// heads) and k (NEOX half-split) and store k, v as fp16 at cache position p.
+// One CTA per row.
+__global__ void k_rope_kv(float* __restrict__ QKV, int ld, int p0, int np, int H, int Hkv, int hd, int n_ctx,
                           int row_heads, int head_off, const float* __restrict__ cs, const float* __restrict__ sn,
                           __half* __restrict__ kc, __half* __restrict__ vc) {
-    const int m = blockIdx.x, b = m / np, p = m - b * np;
+    const int m = blockIdx.x, b = m / np, p = p0 + (m - b * np);
     const int half = hd / 2, qd = H * hd, kd = Hkv * hd;
     float* row = QKV + (size_t)m * ld;
     for (int i = threadIdx.x; i < (H + Hkv) * half; i += blockDim.x) {
@@ -116,83 +117,105 @@ __global__ void k_rope_kv(float* __restrict__ QKV, int ld, int np, int H, int Hk
     }
 }
 
-// Causal attention for query position p of row b, head h (one warp): keys
-// 0..p from the fp16 cache, online softmax over chunks of 32 keys.
-__global__ void __launch_bounds__(128) k_prefill_attn(const float* __restrict__ QKV, int ld, int np, int H, int Hkv,
-                                                      int hd, int n_ctx, int row_heads, int head_off,
+// Causal attention for the query at position p = p0 + i of row b, head h
+// (one warp): keys 0..p from the fp16 cache, online softmax over chunks of 32
+// keys (lane j scores key j0 + j), DPL = head_dim / 32 dimensions per lane.
+template <int DPL>
+__global__ void __launch_bounds__(128) k_prefill_attn(const float* __restrict__ QKV, int ld, int p0, int np, int H,
+                                                      int Hkv, int n_ctx, int row_heads, int head_off,
                                                       const __half* __restrict__ kc, const __half* __restrict__ vc,
                                                       float* __restrict__ O, int ldo) {
+    constexpr int hd = 32 * DPL;
     const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int total = (gridDim.y) * np * H;  // rows x positions x heads
-    if (wid >= total) return;
-    const int h = wid % H, m = wid / H, b = m / np, p = m - b * np;
+    if (wid >= np * H) return;
+    const int b = blockIdx.y;
+    const int h = wid % H, i = wid / H, m = b * np + i, p = p0 + i;
     const int g = h / (H / Hkv);
     const float* q = QKV + (size_t)m * ld + h * hd;
     const __half* K = kc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
     const __half* Vv = vc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
-    const float scale = rsqrtf((float)hd);
-    const int dpl = hd / 32;  // dims per lane (2 or 4)
-    float qv[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int e = 0; e < dpl; ++e) qv[e] = q[lane * dpl + e] * scale;
+    const float scale = 1.0f / sqrtf((float)hd);
+    float qv[DPL], acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+        qv[e] = q[lane * DPL + e] * scale;
+        acc[e] = 0.f;
+    }
     float mrun = -INFINITY, lrun = 0.f;
     for (int j0 = 0; j0 <= p; j0 += 32) {
         const int n = min(32, p + 1 - j0);
-        // scores of the chunk: lane-split dot products, one key at a time
         float sj = -INFINITY;
         for (int j = 0; j < n; ++j) {
-            const __half* kr = K + (size_t)(j0 + j) * hd + lane * dpl;
+            const __half* kr = K + (size_t)(j0 + j) * hd + lane * DPL;
             float s = 0.f;
-            for (int e = 0; e < dpl; ++e) s = fmaf(qv[e], __half2float(kr[e]), s);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) s = fmaf(qv[e], __half2float(kr[e]), s);
+#pragma unroll
             for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             if (lane == j) sj = s;
         }
         float cm = sj;
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
         const float mnew = fmaxf(mrun, cm);
         const float corr = expf(mrun - mnew);
         const float pj = lane < n ? expf(sj - mnew) : 0.f;
         float ps = pj;
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
         lrun = lrun * corr + ps;
-        for (int e = 0; e < dpl; ++e) acc[e] *= corr;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] *= corr;
         for (int j = 0; j < n; ++j) {
             const float pb = __shfl_sync(0xffffffffu, pj, j);
-            const __half* vr = Vv + (size_t)(j0 + j) * hd + lane * dpl;
-            for (int e = 0; e < dpl; ++e) acc[e] = fmaf(pb, __half2float(vr[e]), acc[e]);
+            const __half* vr = Vv + (size_t)(j0 + j) * hd + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pb, __half2float(vr[e]), acc[e]);
         }
         mrun = mnew;
     }
-    for (int e = 0; e < dpl; ++e) O[(size_t)m * ldo + h * hd + lane * dpl + e] = acc[e] / lrun;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) O[(size_t)m * ldo + h * hd + lane * DPL + e] = acc[e] / lrun;
 }
 
 }  // namespace
 
-cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int np,
-                              int d, int V, float* X, int* err, cudaStream_t st) {
-    k_embed_rows<<<B * np, 256, 0, st>>>(table, pos_table, tok, ld, np, d, V, X, err);
+cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int p0,
+                              int np, int d, int V, float* X, int* err, cudaStream_t st) {
+    if (d % 4 || B < 1 || np < 1) return cudaErrorInvalidValue;
+    k_embed_rows<<<B * np, 256, 0, st>>>(table, pos_table, tok, ld, p0, np, d, V, X, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
                            cudaStream_t st) {
+    if (M < 1) return cudaErrorInvalidValue;
     k_rownorm<<<M, 256, 0, st>>>(X, d, ln, g, b, eps, H);
     return cudaGetLastError();
 }
 
-cudaError_t launch_rope_kv(float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
+cudaError_t launch_rope_kv(float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
                            int head_off, const float* cs, const float* sn, __half* kc, __half* vc, cudaStream_t st) {
-    k_rope_kv<<<B * np, 128, 0, st>>>(QKV, ld, np, H, Hkv, hd, n_ctx, row_heads, head_off, cs, sn, kc, vc);
+    if (hd % 2 || p0 < 0 || p0 + np > n_ctx) return cudaErrorInvalidValue;
+    k_rope_kv<<<B * np, 128, 0, st>>>(QKV, ld, p0, np, H, Hkv, hd, n_ctx, row_heads, head_off, cs, sn, kc, vc);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx,
+cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx,
                                 int row_heads, int head_off, const __half* kc, const __half* vc, float* O, int ldo,
                                 cudaStream_t st) {
-    if (hd % 32 || hd > 128 || H % Hkv) return cudaErrorInvalidValue;
-    const int warps = np * H;  // per row
-    dim3 grid((warps + 3) / 4, B);
-    k_prefill_attn<<<grid, 128, 0, st>>>(QKV, ld, np, H, Hkv, hd, n_ctx, row_heads, head_off, kc, vc, O, ldo);
+    if (H % Hkv || p0 < 0 || p0 + np > n_ctx) return cudaErrorInvalidValue;
+    const dim3 grid((np * H + 3) / 4, B);
+    switch (hd) {
+        case 64:
+            k_prefill_attn<2><<<grid, 128, 0, st>>>(QKV, ld, p0, np, H, Hkv, n_ctx, row_heads, head_off, kc, vc, O, ldo);
+            break;
+        case 128:
+            k_prefill_attn<4><<<grid, 128, 0, st>>>(QKV, ld, p0, np, H, Hkv, n_ctx, row_heads, head_off, kc, vc, O, ldo);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -107,6 +107,11 @@ struct sd_ctx {
     DevState* hs = nullptr;             // pinned host mirror
     bool force_pending = false;
 
+    // GEMM prefill of prompt positions 0..n-2 in chunks of pf_rows activation rows (all batch rows)
+    bool gemm_prefill = true;
+    int pf_chunk = 0;                   // positions per chunk
+    float *pf_x = nullptr, *pf_h = nullptr, *pf_qkv = nullptr, *pf_o = nullptr, *pf_u = nullptr;
+
     cudaGraphExec_t g_step = nullptr, g_body = nullptr, g_frame = nullptr, g_prompt_last = nullptr;
     int kernels_per_step = 0;
     int count_launch = 0;
@@ -355,6 +360,58 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     c->count_launch++;
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
     return SD_OK;
+}
+
+// Prompt positions [0, n) of the main stack as GEMMs over all batch rows, in
+// chunks of pf_chunk positions: embed, then per layer norm -> QKV GEMM ->
+// RoPE + fp16 KV store -> causal attention over the cache -> O GEMM (+resid)
+// -> norm -> FC / gate-up GEMM -> proj / down GEMM (+resid).  Leaves the KV
+// cache filled for positions < n and the device position at n.
+int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
+    DStack& s = c->main;
+    const int B = c->B, d = s.d, qd = s.H * s.hd, kd = s.Hkv * s.hd, qr = s.qkv_rows();
+    const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
+    auto ck = [&](cudaError_t e, const char* what) {
+        return e == cudaSuccess ? SD_OK : fail(c, SD_ERR_CUDA, "prefill %s: %s", what, cudaGetErrorString(e));
+    };
+    int rc;
+    for (int p0 = 0; p0 < n; p0 += c->pf_chunk) {
+        const int np = std::min(c->pf_chunk, n - p0), M = B * np;
+        if ((rc = ck(launch_embed_rows(qwen ? c->emb[0] : c->wte, c->wpe, c->prompt, c->cfg.max_ctx, B, p0, np, d,
+                                       c->cfg.vocab, c->pf_x, &c->ds->err, st), "embed")))
+            return rc;
+        for (int l = 0; l < s.n_layer; ++l) {
+            DLayer& L = s.L[l];
+            if ((rc = ck(launch_rownorm(c->pf_x, M, d, s.gpt2, L.n1g, L.n1b, s.eps, c->pf_h, st), "norm"))) return rc;
+            QGemmArgs g;
+            g.W = L.wqkv; g.M = M; g.x = c->pf_h; g.ldx = d; g.epi = EPI_LINEAR; g.bias = L.bqkv;
+            g.y = c->pf_qkv; g.ldy = qr;
+            if ((rc = ck(launch_qgemm(g, st), "qkv gemm"))) return rc;
+            if ((rc = ck(launch_rope_kv(c->pf_qkv, qr, B, p0, np, s.H, s.Hkv, s.hd, s.n_ctx, s.n_layer * s.Hkv,
+                                        l * s.Hkv, s.rope_cos, s.rope_sin, s.kc, s.vc, st), "rope/kv")))
+                return rc;
+            if ((rc = ck(launch_prefill_attn(c->pf_qkv, qr, B, p0, np, s.H, s.Hkv, s.hd, s.n_ctx, s.n_layer * s.Hkv,
+                                             l * s.Hkv, s.kc, s.vc, c->pf_o, qd, st), "attention")))
+                return rc;
+            QGemmArgs o;
+            o.W = L.wo; o.M = M; o.x = c->pf_o; o.ldx = qd; o.epi = EPI_LINEAR; o.bias = L.bo;
+            o.resid = c->pf_x; o.y = c->pf_x; o.ldy = d;
+            if ((rc = ck(launch_qgemm(o, st), "o gemm"))) return rc;
+            if ((rc = ck(launch_rownorm(c->pf_x, M, d, s.gpt2, L.n2g, L.n2b, s.eps, c->pf_h, st), "norm"))) return rc;
+            QGemmArgs f;
+            f.W = L.wfc; f.M = M; f.x = c->pf_h; f.ldx = d; f.epi = s.gpt2 ? EPI_GELU : EPI_SWIGLU; f.bias = L.bfc;
+            f.y = c->pf_u; f.ldy = s.ff;
+            if ((rc = ck(launch_qgemm(f, st), "fc gemm"))) return rc;
+            QGemmArgs q;
+            q.W = L.wproj; q.M = M; q.x = c->pf_u; q.ldx = s.ff; q.epi = EPI_LINEAR; q.bias = L.bproj;
+            q.resid = c->pf_x; q.y = c->pf_x; q.ldy = d;
+            if ((rc = ck(launch_qgemm(q, st), "proj gemm"))) return rc;
+            c->count_launch += 8;
+        }
+        c->count_launch += 1;
+        (void)kd;
+    }
+    return advance(c, &c->ds->pos, n, nullptr, 0, nullptr, 0, st);
 }
 
 enum class GraphKind { T3Step, T3Body, QwenFrame, QwenBody, QwenPromptLast };
@@ -711,6 +768,19 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     }
     if ((rc = dalloc(c, &c->logits, sizeof(float) * c->B * c->logits_ld))) return bail(rc);
     if ((rc = dalloc(c, &c->prompt, sizeof(int32_t) * c->B * m.max_ctx))) return bail(rc);
+    {
+        // GEMM prefill: SD_PREFILL=steps runs the prompt through the per-position step graphs instead
+        const char* e = getenv("SD_PREFILL");
+        c->gemm_prefill = !(e && strcmp(e, "steps") == 0);
+        const DStack& s = c->main;
+        c->pf_chunk = std::max(1, std::min(m.max_ctx, 512 / c->B));
+        const size_t R = (size_t)c->B * c->pf_chunk;
+        if ((rc = dalloc(c, &c->pf_x, sizeof(float) * R * s.d)) || (rc = dalloc(c, &c->pf_h, sizeof(float) * R * s.d)) ||
+            (rc = dalloc(c, &c->pf_qkv, sizeof(float) * R * s.qkv_rows())) ||
+            (rc = dalloc(c, &c->pf_o, sizeof(float) * R * s.H * s.hd)) ||
+            (rc = dalloc(c, &c->pf_u, sizeof(float) * R * s.ff)))
+            return bail(rc);
+    }
     if ((rc = dalloc(c, &c->ds, sizeof(DevState)))) return bail(rc);
     if (cudaHostAlloc(&c->hs, sizeof(DevState), cudaHostAllocDefault) != cudaSuccess)
         return bail(fail(c, SD_ERR_OOM, "pinned staging allocation failed"));
@@ -848,7 +918,11 @@ int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sa
     c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
     for (int b = 0; b < B; ++b) c->hs->tok[b] = tokens[(size_t)b * n + n - 1];  // read by the persistent step
     if ((rc = upload_inputs(c, qwen))) return rc;
-    for (int i = 0; i < n - 1; ++i) CK(cudaGraphLaunch(c->g_body, c->stream));
+    if (c->gemm_prefill && n > 1) {
+        if ((rc = enqueue_prefill_gemm(c, n - 1, c->stream))) return rc;
+    } else {
+        for (int i = 0; i < n - 1; ++i) CK(cudaGraphLaunch(c->g_body, c->stream));
+    }
     CK(cudaGraphLaunch(qwen ? c->g_prompt_last : c->g_step, c->stream));
     c->force_pending = false;
     rc = download_counters(c, qwen);   // synchronises: the staging mirror may change after this
@@ -1059,6 +1133,21 @@ int sd_qmat_gemv(const sd_qmat* m, const float* x_dev, int32_t nb, const float* 
     a.W = m->m; a.nb = nb; a.x = x_dev; a.x_stride = m->m.cols; a.pro = PRO_NONE;
     a.epi = EPI_LINEAR; a.bias = bias_dev; a.y = y_dev; a.y_stride = m->m.rows;
     CK(launch_gemv(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+    return SD_OK;
+}
+
+int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                 const float* resid_dev, float* y_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!m || !x_dev || !y_dev || M < 1 || epilogue < SD_EPI_LINEAR || epilogue > SD_EPI_SWIGLU)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm: bad argument");
+    if (epilogue == SD_EPI_SWIGLU && (bias_dev || m->m.rows % 2))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm: SwiGLU needs even rows and no bias");
+    QGemmArgs a;
+    a.W = m->m; a.M = M; a.x = x_dev; a.ldx = m->m.cols; a.epi = epilogue; a.bias = bias_dev;
+    a.resid = resid_dev; a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows;
+    CK(cudaSetDevice(m->device));
+    CK(launch_qgemm(a, reinterpret_cast<cudaStream_t>(stream)));
     return SD_OK;
 }
 

@@ -218,14 +218,15 @@ struct QGemmArgs {
 };
 cudaError_t launch_qgemm(const QGemmArgs& a, cudaStream_t st);
 
-// Prefill helpers (positions 0..np-1 of B rows at once).
-cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int np,
-                              int d, int V, float* X, int* err, cudaStream_t st);
+// Prefill helpers: positions p0..p0+np-1 of B rows at once, activation row
+// m = b*np + i for position p0 + i.
+cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int p0,
+                              int np, int d, int V, float* X, int* err, cudaStream_t st);
 cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
                            cudaStream_t st);
-cudaError_t launch_rope_kv(float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
+cudaError_t launch_rope_kv(float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
                            int head_off, const float* cs, const float* sn, __half* kc, __half* vc, cudaStream_t st);
-cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int np, int H, int Hkv, int hd, int n_ctx,
+cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx,
                                 int row_heads, int head_off, const __half* kc, const __half* vc, float* O, int ldo,
                                 cudaStream_t st);
 

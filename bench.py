@@ -42,6 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from synth import get_preset, prompt_tokens, uniform_draws  # noqa: E402
+from synth.presets import ARCH_QWEN_TTS  # noqa: E402
 from synth import presets as P  # noqa: E402
 
 METRIC = "decode tokens/s at batch 1 and achieved HBM GB/s vs ~8 TB/s roofline"
@@ -69,6 +70,18 @@ def step_bytes(m: P.ModelSpec, pos: int) -> int:
     small *= 4
     kv = m.batch * m.kv_bytes_per_position() * (pos + 1) + m.batch * m.kv_bytes_per_position()  # read + write
     return wq + small + kv
+
+
+def prefill_gemm_flops(m, P):
+    """2 * weights * rows for the quantised matmuls of positions 0..P-2 (every
+    layer, no head), plus the causal attention products (q.k and p.v)."""
+    if m.arch == ARCH_QWEN_TTS:
+        per_pos = m.talker_params() - m.vocab * m.d_model
+    else:
+        per_pos = m.quantised_params_per_step() - m.vocab * m.d_model
+    n = P - 1
+    att = 4 * m.n_layer * m.n_head * m.head_dim * (n * (n + 1) // 2)
+    return m.batch * (2 * per_pos * n + att)
 
 
 def mean_step_bytes(m, p0, n):
@@ -243,6 +256,19 @@ def run_gpu(args):
     e2e_s = max_over_ranks(dist, ws, t1 - t0, dev)
     e2e = ws * Ke * B / e2e_s
 
+    # prompt prefill: positions 0..P-2 as GEMMs, then the last position's step (CUDA events around sd_prefill)
+    pf_ms = []
+    for _ in range(3):
+        dec.reset()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        dec.prefill(prompt, s, draws[0])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        pf_ms.append(ev0.elapsed_time(ev1))
+    pf_ms = sorted(pf_ms)[1]
+    pf_flops = prefill_gemm_flops(m, run.prompt_len)
+
     # roofline of the decode step
     peaks, peak_kind = load_peaks()
     bytes_step = mean_step_bytes(m, run.prompt_len, K)
@@ -267,6 +293,11 @@ def run_gpu(args):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
                      "bytes_per_step": int(bytes_step),
                      "traffic": traffic},
+        "prefill": {"ms": round(pf_ms, 3), "positions": run.prompt_len, "rows": B,
+                    "gemm_gflop": round(pf_flops / 1e9, 2),
+                    "gemm_tflops": round(pf_flops / (pf_ms / 1e3) / 1e12, 2),
+                    "note": "sd_prefill end to end (median of 3): positions 0..P-2 through the tensor-core "
+                            "GEMMs, the last position through the step graph"},
         "gpu_launches": int(info.kernels_per_step * K),
         "clocks": clocks,
     }

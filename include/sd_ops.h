@@ -37,6 +37,28 @@ int sd_qmat_dequant(const sd_qmat* m, float* out_dev, void* stream);
 int sd_qmat_gemv(const sd_qmat* m, const float* x_dev, int32_t nb, const float* bias_dev, float* y_dev,
                  void* stream);
 
+/* Epilogues of sd_qmat_gemm. */
+enum { SD_EPI_LINEAR = 0, SD_EPI_GELU = 1, SD_EPI_SWIGLU = 2 };
+
+/* Tensor-core GEMM for prompt prefill and batched rows ("Chatterbox -> ggml
+ * Port: Development Journal", section 3.2: the prompt graph applies every
+ * layer to all prompt positions at once):
+ *   t[i][r] = sum_k W[r][k] x_dev[i][k] for i < M (x_dev [M][cols], fp32);
+ *   SD_EPI_LINEAR: y_dev[i][r] = t[i][r] (+ bias_dev[r]) (+ resid_dev[i][r]);
+ *   SD_EPI_GELU:   y_dev[i][r] = gelu_tanh(t[i][r] (+ bias_dev[r])) (+ resid_dev[i][r]);
+ *   SD_EPI_SWIGLU: rows are interleaved gate/up pairs (row 2j gate j, row
+ *     2j+1 up j), y_dev[i][j] = silu(t[i][2j]) * t[i][2j+1] (+ resid_dev[i][j]),
+ *     j < rows/2; bias_dev must be NULL; rows must be even.
+ * y_dev and resid_dev have leading dimension rows (rows/2 for SwiGLU); resid_dev
+ * may equal y_dev; bias_dev and resid_dev may be NULL.  The codes of a
+ * quantisation block enter the tensor cores exactly (fp16 integers), the
+ * fp32 activations as an fp16 high + low pair, and the block scale (and
+ * affine bias times the group's activation sum) is applied in fp32.
+ * Device pointers; enqueued on `stream`; returns SD_ERR_INVALID_ARG on a NULL
+ * pointer, M < 1 or a bad epilogue. */
+int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                 const float* resid_dev, float* y_dev, void* stream);
+
 /* Sample one token per row from logits_dev[rows][V] with draws u_dev[rows];
  * tokens to out_dev[rows].  Sampler semantics as in sd.h.  V <= 16384. */
 int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,

@@ -176,6 +176,34 @@ def test_llama_q4_both_step_paths(sd, step_path):
     _check_t3(sd, get_preset("llama_q4"), 4)
 
 
+@pytest.fixture(params=["gemm", "steps"])
+def prefill_path(request, monkeypatch):
+    """Run a test with the GEMM prefill and with the per-position step graphs."""
+    monkeypatch.setenv("SD_PREFILL", request.param)
+    return request.param
+
+
+def test_gpt2m_q4_both_prefill_paths(sd, prefill_path):
+    _check_t3(sd, get_preset("gpt2m_q4"), 3)
+
+
+def test_llama_gqa_prompt_spanning_chunks(sd, prefill_path):
+    """Two batch rows, 8 query / 2 KV heads, a 290-token prompt: the GEMM
+    prefill runs it as two chunks (256 positions, then 33)."""
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=2, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q4_0)
+    run = get_preset("llama_q4").with_model(**{f: getattr(spec, f) for f in
+                                               ("n_layer", "d_model", "n_head", "n_kv_head", "d_ff", "vocab",
+                                                "max_ctx", "quant")})
+    prompt = np.random.default_rng(5).integers(0, 1000, size=(2, 290)).astype(np.int32)
+    _check_t3(sd, run, 6, prompt=prompt)
+
+
+def test_one_token_prompt(sd, prefill_path):
+    run = get_preset("tiny")
+    _check_t3(sd, run, 3, prompt=np.array([[17]], np.int32))
+
+
 def test_persistent_kernel_is_used(sd, monkeypatch):
     monkeypatch.setenv("SD_PERSISTENT", "1")
     run = get_preset("tiny")
@@ -264,7 +292,7 @@ def _check_qwen(sd, spec, prompt, n_frames, sampler, free_run_frames=0):
     dec.close()
 
 
-def test_qwen_small(sd):
+def test_qwen_small(sd, prefill_path):
     spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
                        d_ff=1024, vocab=300, max_ctx=64, batch=2, quant=P.A8G64,
                        cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
