@@ -36,11 +36,13 @@ __global__ void k_embed_rows(const float* __restrict__ table, const float* __res
     }
 }
 
-// H[m] = norm(X[m]) * g (+ b): LayerNorm (biased variance) or RMSNorm, one CTA per row
-__global__ void __launch_bounds__(256) k_rownorm(const float* __restrict__ X, int d, int ln, const float* __restrict__ g,
-                                                 const float* __restrict__ bta, float eps, float* __restrict__ H) {
+// H[m] = norm(X[m]) * g (+ b): LayerNorm (biased variance) or RMSNorm, one CTA
+// per row; X rows ldx apart, H rows d apart.
+__global__ void __launch_bounds__(256) k_rownorm(const float* __restrict__ X, int ldx, int d, int ln,
+                                                 const float* __restrict__ g, const float* __restrict__ bta, float eps,
+                                                 float* __restrict__ H) {
     const int m = blockIdx.x, tid = threadIdx.x;
-    const float* x = X + (size_t)m * d;
+    const float* x = X + (size_t)m * ldx;
     __shared__ float red[32];
     __shared__ float stat[2];
     float s = 0.f;
@@ -188,10 +190,10 @@ cudaError_t launch_embed_rows(const float* table, const float* pos_table, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
-                           cudaStream_t st) {
-    if (M < 1) return cudaErrorInvalidValue;
-    k_rownorm<<<M, 256, 0, st>>>(X, d, ln, g, b, eps, H);
+cudaError_t launch_rownorm(const float* X, int ldx, int M, int d, int ln, const float* g, const float* b, float eps,
+                           float* H, cudaStream_t st) {
+    if (M < 1 || ldx < d) return cudaErrorInvalidValue;
+    k_rownorm<<<M, 256, 0, st>>>(X, ldx, d, ln, g, b, eps, H);
     return cudaGetLastError();
 }
 

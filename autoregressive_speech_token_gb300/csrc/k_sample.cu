@@ -1,4 +1,4 @@
-// On-device sampler kernel: one 1024-thread CTA per row around sample_block()
+// On-device sampler kernel: one 512-thread CTA per row around sample_block()
 // (sample_dev.cuh), logits staged in shared memory, token written to device
 // memory -- no host round trip.
 #include "sample_dev.cuh"
@@ -6,7 +6,7 @@
 namespace sd {
 namespace {
 
-constexpr int kST = 1024;
+constexpr int kST = 512;
 
 __global__ void __launch_bounds__(kST) k_sample(const SampleArgs a) {
     pdl_trigger();
@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(kST) k_sample(const SampleArgs a) {
 
 }  // namespace
 
-size_t sample_smem_bytes(int V) { return sample_smem_bytes_dev(V); }
+size_t sample_smem_bytes(int V) { return sample_smem_bytes_dev(V, kST); }
 
 cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t st) {
     if (a.V < 1 || a.V > sample_detail::kMaxV) return cudaErrorInvalidValue;

@@ -1,27 +1,33 @@
 // Persistent decode step for the GPT-2- and Llama-style T3 (rows B <= 2,
-// Q8_0/Q4_0 weights): one cooperative launch runs n decode steps, each phase
-// of each layer spread over every SM, phases separated by a grid barrier.
+// Q8_0/Q4_0 weights): one cooperative launch runs n decode steps.
 //
-// "Every Frame Is a Memory Read", section 3: a decode step is a memory read --
-// its time is bytes / bandwidth only if the weight stream never stalls.  With
-// one kernel per operation the stream stops at every dependency (a launch, a
-// tail, a cold start).  Here the weight stream is decoupled from the
-// dependency chain: at the start of each layer every CTA issues bulk L2
-// prefetches (cp.async.bulk.prefetch.L2) for all of its weight rows of the
-// *next* layer, so HBM keeps streaming while the current layer's phases wait
-// on each other; compute then reads its rows from L2.
+// "Every Frame Is a Memory Read", section 3: a decode step is a memory read,
+// and its time is bytes / bandwidth only if the weight stream never waits on
+// the dependency chain.  Two mechanisms keep the two apart here.
 //
-// Per step: embed -> for each layer [QKV rows (LayerNorm/RMSNorm prologue,
-// bias) | attention work items (split-KV, RoPE, fp16 KV append, last-item
-// log-sum-exp combine) | O rows (+bias +residual) | FC or gate/up rows
-// (+GELU / SwiGLU) | proj/down rows (+bias +residual)] -> head rows -> one
-// CTA per row samples the next token.  Row ranges are static per CTA.
+// Weight stream.  Every CTA owns fixed row ranges of every matrix.  A ring
+// buffer in shared memory receives, by bulk asynchronous copies
+// (cp.async.bulk with mbarrier completion), the CTA's rows of the matrices in
+// the order the step consumes them -- codes, scales, bias and norm gains of one
+// phase per record -- as far ahead as the ring holds (two to three layers).
+// Thread 0 issues records whenever space frees; compute never waits on HBM.
 //
-// Every grid barrier is a counter incremented once per CTA and waited on with
-// a clock64() budget: on expiry the CTA records an error, and every later
-// barrier of every CTA falls through, so the kernel always exits.  Buffers
-// written by other CTAs are read through L2 (ld.global.cg).
-#include "attn_dev.cuh"
+// Activation exchange.  A phase's outputs are published as 64-bit words
+// (epoch << 32 | float bits) written with one relaxed store each; a consumer
+// polls the words it needs until each carries the current epoch.  One L2
+// round trip both synchronises and delivers the data -- there is no grid
+// barrier.  Epochs are unique per (step, layer) over the life of the context,
+// so no buffer needs clearing.  Every poll is bounded: on expiry the CTA
+// records an error and the kernel returns.
+//
+// Per step (pos = position of the consumed token): embedding -> per layer
+// [QKV rows with the LayerNorm/RMSNorm prologue and bias | attention items:
+// (row, kv head, key split) with RoPE, the fp16 KV append and a partial
+// softmax | O rows: combine the partials, +bias +residual | FC or gate/up rows:
+// norm prologue, GELU or SwiGLU | proj/down rows: +bias +residual] -> head
+// rows with the final norm -> CTA b samples row b.  ("Chatterbox -> ggml
+// Port: Development Journal", section 3.2 for the layer order; sections
+// 3.12-3.13 for the cache layout [head][pos][dim] and the causal extent.)
 #include "k_gemv.cuh"
 #include "sample_dev.cuh"
 
@@ -32,23 +38,118 @@ using namespace gemv_detail;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kNMB = 16;         // records in flight at most
 constexpr int kErrTimeout = 6;
+constexpr int kMaxOwn = 64;      // residual-stream rows owned by one CTA
+constexpr int kMaxPart = 1024;   // per-slice GEMV partial sums (rows x batch rows x K slices)
+constexpr int kMaxHPG = 8;       // query heads per KV head
+constexpr int kKC = 128;         // cached keys staged per attention sub-chunk
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
+enum PhaseKind { PK_EMBED = 0, PK_QKV, PK_ATTN, PK_O, PK_FC, PK_PROJ, PK_HEAD, PK_SAMPLE };
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-    const char* c = reinterpret_cast<const char*>(p);
-    while (bytes) {
-        const unsigned n = bytes > 65536 ? 65536u : (unsigned)bytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
-        c += n;
-        bytes -= n;
+__device__ __forceinline__ unsigned long long gtime() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ flag-carrying words
+
+__device__ __forceinline__ void ll_store(unsigned long long* p, float v, unsigned e) {
+    const unsigned long long w = ((unsigned long long)e << 32) | (unsigned long long)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ll_load(const unsigned long long* p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+// Polls one word until it carries epoch e; false on timeout or a recorded error.
+__device__ __noinline__ bool ll_spin(const unsigned long long* p, unsigned e, unsigned long long* w, int* err,
+                                     long long budget) {
+    const long long t0 = clock64();
+    for (unsigned it = 1;; ++it) {
+        *w = ll_load(p);
+        if ((unsigned)(*w >> 32) == e) return true;
+        if ((it & 63u) == 0u) {
+            if (ld_volatile(err)) return false;
+            if (clock64() - t0 > budget) {
+                atomicCAS(err, 0, kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// dst[o * n_in + i] = value of word src[o * stride + i] (epoch e), o < n_out, i < n_in.
+// Per-thread result; the caller combines it with __syncthreads_and.
+__device__ bool ll_read(const unsigned long long* src, int n_out, int stride, int n_in, unsigned e, float* dst,
+                        int* err, long long budget) {
+    const int n = n_out * n_in;
+    bool ok = true;
+    for (int i0 = threadIdx.x; i0 < n && ok; i0 += 4 * kThreads) {
+        unsigned long long w[4];
+        const unsigned long long* p[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * kThreads;
+            p[j] = i < n ? src + (size_t)(i / n_in) * stride + (i % n_in) : nullptr;
+            w[j] = p[j] ? ll_load(p[j]) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!p[j] || !ok) continue;
+            if ((unsigned)(w[j] >> 32) != e) ok = ll_spin(p[j], e, &w[j], err, budget);
+            dst[i0 + j * kThreads] = __uint_as_float((unsigned)w[j]);
+        }
+    }
+    return ok;
+}
+
+// ------------------------------------------------------------------ weight records
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mb_init(uint32_t mb) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
+}
+
+__device__ __forceinline__ void mb_expect(uint32_t mb, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mb) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb) : "memory");
+}
+
+__device__ __forceinline__ bool mb_try(uint32_t mb, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for an mbarrier phase; honours the error flag unless `drain`.
+__device__ bool mb_wait(uint32_t mb, uint32_t parity, int* err, long long budget, bool drain) {
+    if (mb_try(mb, parity)) return true;
+    const long long t0 = clock64();
+    for (unsigned it = 1;; ++it) {
+        if (mb_try(mb, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (!drain && ld_volatile(err)) return false;
+            if (clock64() - t0 > budget) {
+                if (!drain) atomicCAS(err, 0, kErrTimeout);
+                return false;
+            }
+        }
     }
 }
 
@@ -57,505 +158,776 @@ __device__ __forceinline__ void row_range(int R, int i, int G, int& r0, int& r1)
     r1 = (int)((long long)R * (i + 1) / G);
 }
 
-__device__ __forceinline__ size_t qrow_bytes(const QMat& W) {
-    return W.kind == SD_Q4_0 ? (size_t)W.cols / 2 : (size_t)W.cols;
-}
-__device__ __forceinline__ size_t srow_bytes(const QMat& W) {
-    return W.kind == SD_A8G64 ? (size_t)(W.cols / 64) * 4 : (size_t)(W.cols / 32) * 2;
-}
+// One phase's record for this CTA: rows [r0, r1) of a matrix, with the scale
+// and bias windows widened to 16-byte boundaries, and the norm gains.
+struct Slice {
+    const uint8_t* q;
+    const uint8_t* s;
+    const float *bias, *g1, *g2;
+    int r0, r1, row_bytes, srow, s_lo, b_lo, K;
+    int o_sc, o_bias, o_g1, o_g2;  // offsets in the record (codes at 0)
+    int n_codes, n_sc, n_bias, n_g;
+    int bytes;                     // record size in the ring (128-byte multiple)
+};
 
-__device__ void prefetch_rows(const QMat& W, int r0, int r1) {
-    if (r1 <= r0) return;
-    const size_t qb = qrow_bytes(W), sb = srow_bytes(W);
-    prefetch_l2(W.q + (size_t)r0 * qb, (size_t)(r1 - r0) * qb);
-    prefetch_l2(reinterpret_cast<const char*>(W.s) + (size_t)r0 * sb, (size_t)(r1 - r0) * sb);
-}
-
-// Grid barrier: returns false once any CTA has recorded an error (then it
-// no longer waits).  `target` = (barriers passed so far + 1) * gridDim.x.
-__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned target, int* err, long long budget) {
-    __syncthreads();
-    __shared__ int s_ok;
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(bar, 1u);
-        int ok = ld_volatile(err) == 0;
-        if (ok) {
-            const long long t0 = clock64();
-            unsigned it = 0;
-            while (ld_acquire(bar) < target) {
-                if ((++it & 255u) == 0) {
-                    if (ld_volatile(err) != 0) { ok = 0; break; }
-                    if (clock64() - t0 > budget) {
-                        atomicCAS(err, 0, kErrTimeout);
-                        ok = 0;
-                        break;
-                    }
-                }
-            }
+// j: index of the slice within a step (4 per layer: QKV, O, FC, proj; then the head)
+__device__ Slice make_slice(const StepArgs& a, const StepLayer* tab, int j, int cta, int G) {
+    const int L = a.n_layer;
+    const int kind = j < 4 * L ? (j & 3) : 4;
+    const int l = j >> 2;
+    Slice s;
+    QMat W;
+    s.bias = nullptr; s.g1 = nullptr; s.g2 = nullptr;
+    if (kind == 0) {
+        W = tab[l].wqkv; s.bias = tab[l].bqkv; s.g1 = tab[l].n1g; s.g2 = tab[l].n1b;
+        row_range(W.rows, cta, G, s.r0, s.r1);
+    } else if (kind == 1) {
+        W = tab[l].wo; s.bias = tab[l].bo;
+        row_range(W.rows, cta, G, s.r0, s.r1);
+    } else if (kind == 2) {
+        W = tab[l].wfc; s.bias = tab[l].bfc; s.g1 = tab[l].n2g; s.g2 = tab[l].n2b;
+        if (a.gpt2) {
+            row_range(W.rows, cta, G, s.r0, s.r1);
+        } else {  // gate/up rows interleaved in pairs
+            row_range(W.rows / 2, cta, G, s.r0, s.r1);
+            s.r0 *= 2; s.r1 *= 2;
         }
-        s_ok = ok;
+    } else if (kind == 3) {
+        W = tab[l].wproj; s.bias = tab[l].bproj;
+        row_range(W.rows, cta, G, s.r0, s.r1);
+    } else {
+        W = a.head; s.g1 = a.nfg; s.g2 = a.nfb;
+        row_range(W.rows, cta, G, s.r0, s.r1);
     }
-    __syncthreads();
-    return s_ok != 0;
+    if (!a.gpt2) s.g2 = nullptr;  // RMSNorm: gain only
+    s.K = W.cols;
+    s.row_bytes = W.kind == SD_Q4_0 ? W.cols / 2 : W.cols;
+    s.srow = (W.cols / 32) * 2;
+    const int nr = s.r1 - s.r0;
+    s.n_codes = nr * s.row_bytes;
+    s.s_lo = (s.r0 * s.srow) & ~15;
+    s.n_sc = (((s.r1 * s.srow) + 15) & ~15) - s.s_lo;
+    s.o_sc = s.n_codes;
+    int off = s.o_sc + s.n_sc;
+    s.b_lo = s.r0 & ~3;
+    s.n_bias = s.bias ? ((((s.r1 + 3) & ~3) - s.b_lo) * 4) : 0;
+    s.o_bias = off;
+    off += s.n_bias;
+    s.n_g = s.g1 ? W.cols * 4 : 0;
+    s.o_g1 = off;
+    off += s.n_g;
+    s.o_g2 = off;
+    off += s.g2 ? s.n_g : 0;
+    s.bytes = (off + 127) & ~127;
+    s.q = W.q + (size_t)s.r0 * s.row_bytes;
+    s.s = reinterpret_cast<const uint8_t*>(W.s) + s.s_lo;
+    if (s.bias) s.bias += s.b_lo;
+    return s;
 }
 
-// Copy a norm's gain (and offset) into shared memory ahead of the barrier
-// that precedes its use: they are constants.
-__device__ __forceinline__ void preload_vec(const float* src, int n, float* dst) {
-    if (!src) return;
-    for (int i = threadIdx.x; i < (n >> 2); i += blockDim.x)
-        reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
-}
+// ------------------------------------------------------------------ compute helpers
 
-// Stage activation rows [NB][K] (global, written by other CTAs) into shared
-// memory, optionally normalised (LayerNorm with gain/offset, or RMSNorm) with
-// the gain/offset already in shared memory (s_g, s_b).
+// In-place LayerNorm (biased variance) or RMSNorm of x[b][0..K), b < NB.
 template <int NB>
-__device__ void stage_x(const float* x, int x_stride, int K, int pro, const float* s_g, const float* s_b, float eps,
-                        float* s_x, float* scr) {
-    const int K4 = K >> 2;
-    float4* xs4 = reinterpret_cast<float4*>(s_x);
-    for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
-        const int b = i / K4, k4 = i - b * K4;
-        xs4[i] = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * x_stride) + k4);
-    }
-    __syncthreads();
-    if (pro == PRO_NONE) return;
+__device__ void norm_rows(float* x, int K, bool ln, const float* g, const float* gb, float eps, float* scr) {
     float v[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         float sum = 0.f;
-        for (int k = threadIdx.x; k < K; k += blockDim.x) {
-            const float xv = s_x[b * K + k];
-            sum += (pro == PRO_LN) ? xv : xv * xv;
+        for (int k = threadIdx.x; k < K; k += kThreads) {
+            const float xv = x[b * K + k];
+            sum += ln ? xv : xv * xv;
         }
         v[b] = sum;
     }
     block_sum<NB>(v, scr);
     float mu[NB], rs[NB];
-    if (pro == PRO_LN) {
+    if (ln) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) mu[b] = v[b] / (float)K;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float sum = 0.f;
-            for (int k = threadIdx.x; k < K; k += blockDim.x) {
-                const float dx = s_x[b * K + k] - mu[b];
+            for (int k = threadIdx.x; k < K; k += kThreads) {
+                const float dx = x[b * K + k] - mu[b];
                 sum = fmaf(dx, dx, sum);
             }
             v[b] = sum;
         }
         block_sum<NB>(v, scr);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) rs[b] = 1.0f / sqrtf(v[b] / (float)K + eps);
     } else {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            mu[b] = 0.f;
-            rs[b] = 1.0f / sqrtf(v[b] / (float)K + eps);
-        }
+        for (int b = 0; b < NB; ++b) mu[b] = 0.f;
     }
-    const float4* g4 = reinterpret_cast<const float4*>(s_g);
-    const float4* b4 = reinterpret_cast<const float4*>(s_b);
-    for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
-        const int b = i / K4, k4 = i - b * K4;
-        const float4 gg = g4[k4];
-        float4 xx = xs4[i];
-        if (pro == PRO_LN) {
-            const float4 o = b4[k4];
-            xx.x = fmaf((xx.x - mu[b]) * rs[b], gg.x, o.x);
-            xx.y = fmaf((xx.y - mu[b]) * rs[b], gg.y, o.y);
-            xx.z = fmaf((xx.z - mu[b]) * rs[b], gg.z, o.z);
-            xx.w = fmaf((xx.w - mu[b]) * rs[b], gg.w, o.w);
-        } else {
-            xx.x = xx.x * rs[b] * gg.x;
-            xx.y = xx.y * rs[b] * gg.y;
-            xx.z = xx.z * rs[b] * gg.z;
-            xx.w = xx.w * rs[b] * gg.w;
-        }
-        xs4[i] = xx;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) rs[b] = 1.0f / sqrtf(v[b] / (float)K + eps);
+    for (int i = threadIdx.x; i < NB * K; i += kThreads) {
+        const int b = i / K, k = i - b * K;
+        const float xv = x[i];
+        x[i] = ln ? fmaf((xv - mu[b]) * rs[b], g[k], gb[k]) : xv * rs[b] * g[k];
     }
     __syncthreads();
 }
 
-template <int QK, int R>
-struct GemvPre {
-    uint4 w[R][Unit<QK>::kU];
-    float d[R][Unit<QK>::kU];
-};
-
-// Warp layout of a row tile: WK warps along K (1024 elements each), WR row
-// groups of R rows.
-struct GemvGeom {
-    int K, WK, WR, kw, rg, lane;
-    bool active;
-};
-__device__ __forceinline__ GemvGeom gemv_geom(int K) {
-    GemvGeom g;
-    g.K = K;
-    g.WK = (K + 1023) >> 10;
-    g.WR = kWarps / g.WK;
-    const int warp = threadIdx.x >> 5;
-    g.lane = threadIdx.x & 31;
-    g.kw = warp % g.WK;
-    g.rg = warp / g.WK;
-    g.active = g.rg < g.WR;
-    return g;
-}
-
-template <int QK, int R>
-__device__ __forceinline__ void gemv_load(GemvPre<QK, R>& p, const QMat& W, int base, int r1, const GemvGeom& g) {
-    constexpr int U = Unit<QK>::kU;
-    const int K = W.cols;
-    const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
-    const int spr = K >> 5;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-        const int r = base + g.rg * R + i;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = (QK == SD_Q4_0) ? (g.kw * 1024 + g.lane * 32) : (g.kw * 1024 + u * 512 + g.lane * 16);
-            const bool ok = g.active && r < r1 && e < K;
-            const int boff = (QK == SD_Q4_0) ? (e >> 1) : e;
-            p.w[i][u] = ok ? __ldcs(reinterpret_cast<const uint4*>(W.q + (size_t)r * row_bytes + boff))
-                           : make_uint4(0u, 0u, 0u, 0u);
-            p.d[i][u] = ok ? __half2float(__ldg(reinterpret_cast<const __half*>(W.s) + (size_t)r * spr + (e >> 5)))
-                           : 0.f;
-        }
-    }
-}
-
-// Constants of a phase, issued before the barrier that precedes it: the first
-// pass of weight rows into registers, this CTA's bias slice into s_bias.
-template <int QK, int R>
-__device__ __forceinline__ void gemv_preload(GemvPre<QK, R>& p, const QMat& W, int r0, int r1, const float* bias,
-                                             float* s_bias) {
-    gemv_load<QK, R>(p, W, r0, r1, gemv_geom(W.cols));
-    if (bias)
-        for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) s_bias[i] = __ldg(bias + r0 + i);
-}
-
-// Rows [r0, r1) of y = W x (+bias, activation, +resid), activations in shared
-// memory, first pass of weights already in registers (p), bias slice in
-// s_bias.  resid/out_own: this CTA's own rows of the residual stream (shared
-// memory), read and updated when non-null.  Partial sums of the WK warps meet
-// in shared memory in a fixed order.
-__device__ __forceinline__ void inner_stamp(unsigned long long* t, int k) {
-    if (t && blockIdx.x == 0 && threadIdx.x == 0) {
-        unsigned long long v;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
-        t[k] = v;
-    }
-}
-
-template <int QK, int NB, int R>
-__device__ void gemv_finish(GemvPre<QK, R>& p, const QMat& W, int r0, int r1, const float* s_x, int epi,
-                            const float* s_bias, float* own, int own_stride, float* y, int y_stride, float* s_tot,
-                            unsigned long long* tin = nullptr) {
+// y[i * NB + b] = sum_k W[r0 + i][k] x[b][k] for i < nr, with the codes and
+// scales of rows r0.. in shared memory.  Warp layout as the streaming GEMV: a
+// warp owns a 1024-element K slice (lane activations in registers) and visits
+// rows rg, rg + WR, ...; the WK slices of a row meet in s_part in fixed order.
+template <int QK, int NB>
+__device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr, const float* x, float* s_part,
+                         float* s_y) {
     constexpr int U = Unit<QK>::kU;
     constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;
-    const GemvGeom g = gemv_geom(W.cols);
-    const int K = W.cols;
-    float xr[NB][32];
+    const int WK = (K + 1023) >> 10, WR = kWarps / WK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kw = warp % WK, rg = warp / WK;
+    const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
+    const int spr = K >> 5;
+    if (rg < WR) {
+        float xr[NB][32];
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = (QK == SD_Q4_0) ? (g.kw * 1024 + g.lane * 32) : (g.kw * 1024 + u * 512 + g.lane * 16);
-            const bool in = g.active && e < K;
+            for (int u = 0; u < U; ++u) {
+                const int e = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
+                const bool in = e < K;
 #pragma unroll
-            for (int j = 0; j < EPU; j += 4) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * K + e + j]);
-                xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
-                xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
+                for (int j = 0; j < EPU; j += 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (in) v = *reinterpret_cast<const float4*>(&x[b * K + e + j]);
+                    xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
+                    xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
+                }
             }
-        }
-    inner_stamp(tin, 0);
-    for (int base = r0; base < r1; base += g.WR * R) {
-        if (base != r0) gemv_load<QK, R>(p, W, base, r1, g);
-        if (g.active) {
-            float acc[R][NB];
+        for (int i = rg; i < nr; i += WR) {
+            float acc[NB];
 #pragma unroll
-            for (int i = 0; i < R; ++i)
+            for (int b = 0; b < NB; ++b) acc[b] = 0.f;
 #pragma unroll
-                for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
-#pragma unroll
-            for (int i = 0; i < R; ++i)
-#pragma unroll
-                for (int u = 0; u < U; ++u)
+            for (int u = 0; u < U; ++u) {
+                const int e = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
+                if (e < K) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(codes + (size_t)i * row_bytes +
+                                                                     ((QK == SD_Q4_0) ? (e >> 1) : e));
+                    const float dq = __half2float(reinterpret_cast<const __half*>(sc)[(size_t)i * spr + (e >> 5)]);
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float dq = (QK == SD_Q4_0) ? dot_q4(p.w[i][u], &xr[b][0]) : dot_s8(p.w[i][u], &xr[b][u * EPU]);
-                        acc[i][b] = fmaf(p.d[i][u], dq, acc[i][b]);
+                        const float t = (QK == SD_Q4_0) ? dot_q4(w, &xr[b][0]) : dot_s8(w, &xr[b][u * EPU]);
+                        acc[b] = fmaf(dq, t, acc[b]);
                     }
-            inner_stamp(tin, 1);
+                }
+            }
 #pragma unroll
-            for (int i = 0; i < R; ++i)
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const float sv = warp_sum(acc[i][b]);
-                    if (g.lane == 0) s_tot[((g.rg * R + i) * NB + b) * g.WK + g.kw] = sv;
-                }
-            inner_stamp(tin, 2);
-        }
-        __syncthreads();
-        inner_stamp(tin, 3);
-        const int n_out = g.WR * R * NB;
-        for (int t = threadIdx.x; t < n_out; t += blockDim.x) {
-            const int b = t % NB;
-            const int i = (t / NB) % R;
-            const int gg = t / (NB * R);
-            const int r = base + gg * R + i;
-            if (r >= r1) continue;
-            float v = 0.f;
-            for (int k = 0; k < g.WK; ++k) v += s_tot[((gg * R + i) * NB + b) * g.WK + k];
-            if (epi == EPI_SWIGLU) {
-                if ((i & 1) == 0) {
-                    float up = 0.f;
-                    for (int k = 0; k < g.WK; ++k) up += s_tot[((gg * R + i + 1) * NB + b) * g.WK + k];
-                    y[(size_t)b * y_stride + (r >> 1)] = silu(v) * up;
-                }
-            } else {
-                if (s_bias) v += s_bias[r - r0];
-                if (epi == EPI_GELU) v = gelu_tanh(v);
-                if (own) {
-                    v += own[b * own_stride + (r - r0)];
-                    own[b * own_stride + (r - r0)] = v;
-                }
-                y[(size_t)b * y_stride + r] = v;
+            for (int b = 0; b < NB; ++b) {
+                const float v = warp_sum(acc[b]);
+                if (lane == 0) s_part[(i * NB + b) * WK + kw] = v;
             }
         }
-        inner_stamp(tin, 4);
-        __syncthreads();
-        inner_stamp(tin, 5);
     }
+    __syncthreads();
+    for (int t = threadIdx.x; t < nr * NB; t += kThreads) {
+        float v = 0.f;
+        for (int k = 0; k < WK; ++k) v += s_part[t * WK + k];
+        s_y[t] = v;
+    }
+    __syncthreads();
 }
 
-constexpr int kMaxBiasRows = 256;  // bias slice of one phase for one CTA
-constexpr int kMaxOwn = 128;       // residual-stream rows owned by one CTA
+// Attention splits for n = pos + 1 keys: at most max_split chunks of about
+// split_len keys, none empty.
+__device__ __forceinline__ void attn_split(const StepArgs& a, int n, int& S, int& chunk) {
+    S = (n + a.split_len - 1) / a.split_len;
+    if (S > a.max_split) S = a.max_split;
+    if (S < 1) S = 1;
+    chunk = (n + S - 1) / S;
+    S = (n + chunk - 1) / chunk;
+}
+
+// One attention item: row b, kv head g, keys [c0, c1) of n = pos + 1.  Writes
+// the unnormalised partial o (per query head of the group) with its running
+// max m and sum l.  sm: the activation region (>= attn_smem_floats).
+__device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, int chunk, int pos, unsigned e,
+                          float* sm, int* err) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hd = a.hd, half = hd >> 1, HPG = a.H / a.Hkv, n = pos + 1;
+    const int qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
+    const int c0 = c * chunk, c1 = min(n, c0 + chunk);
+    const bool last = c1 == n;
+    float* q = sm;                       // [HPG][hd]
+    float* kn = q + HPG * hd;            // [hd]
+    float* vn = kn + hd;                 // [hd]
+    float* o = vn + hd;                  // [HPG][hd]
+    float* sc = o + HPG * hd;            // [HPG][kKC] scores, then probabilities
+    float* mm = sc + HPG * kKC;          // [HPG] running max
+    float* ls = mm + kMaxHPG;            // [HPG] running sum
+    float* cr = ls + kMaxHPG;            // [HPG] rescale of this sub-chunk
+    float* op = cr + kMaxHPG;            // [kThreads] PV partials
+    __half* Ks = reinterpret_cast<__half*>(op + kThreads);  // [kKC][hd] (16-byte aligned: see attn_floats)
+    __half* Vs = Ks + kKC * hd;                               // [kKC][hd]
+    const size_t hb = ((size_t)(b * a.n_layer * a.Hkv + l * a.Hkv + g) * a.n_ctx) * hd;
+    const __half* Kg = a.kc + hb;
+    const __half* Vg = a.vc + hb;
+    const int u16 = hd / 8;              // 16-byte units per cached row
+
+    // cached rows [j0, j1) (the position being decoded comes from kn / vn)
+    auto stage = [&](int j0, int j1) {
+        const int nu = (j1 - j0) * u16;
+        for (int t = tid; t < 2 * nu; t += kThreads) {
+            const bool isv = t >= nu;
+            const int uu = isv ? t - nu : t;
+            if (j0 + uu / u16 == pos) continue;
+            const uint4 w = __ldcg(reinterpret_cast<const uint4*>((isv ? Vg : Kg) + (size_t)j0 * hd) + uu);
+            reinterpret_cast<uint4*>(isv ? Vs : Ks)[uu] = w;
+        }
+    };
+    stage(c0, min(c1, c0 + kKC));  // issued before the wait for this step's q
+
+    bool ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + (size_t)g * HPG * hd, 1, 0, HPG * hd, e, q, err,
+                      a.spin_budget);
+    if (last && ok) {
+        ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + qd + (size_t)g * hd, 1, 0, hd, e, kn, err, a.spin_budget);
+        if (ok) ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + qd + kd + (size_t)g * hd, 1, 0, hd, e, vn, err,
+                             a.spin_budget);
+    }
+    if (!__syncthreads_and(ok)) return false;
+    // RoPE (NEOX half split) at pos on q and the new k; q scaled by 1/sqrt(hd)
+    const float scale = 1.0f / sqrtf((float)hd);
+    for (int i = tid; i < (HPG + 1) * half; i += kThreads) {
+        const int h = i / half, dd = i - h * half;
+        if (h == HPG && !last) continue;
+        float* v = h < HPG ? q + h * hd : kn;
+        float x0 = v[dd], x1 = v[dd + half];
+        if (a.rope_cos) {
+            const float cs = a.rope_cos[(size_t)pos * half + dd], sn = a.rope_sin[(size_t)pos * half + dd];
+            const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+            x0 = y0;
+            x1 = y1;
+        }
+        if (h < HPG) {
+            x0 *= scale;
+            x1 *= scale;
+        }
+        v[dd] = x0;
+        v[dd + half] = x1;
+    }
+    for (int t = tid; t < HPG * hd; t += kThreads) o[t] = 0.f;
+    if (tid < HPG) {
+        mm[tid] = -INFINITY;
+        ls[tid] = 0.f;
+    }
+    __syncthreads();
+    if (last) {
+        // append the new position to the cache (fp16, round to nearest); the fence
+        // orders it before this item's published partial, which later steps' readers
+        // (through the chain of epochs) have observed before they read the cache
+        for (int dd = tid; dd < hd; dd += kThreads) {
+            a.kc[hb + (size_t)pos * hd + dd] = __float2half_rn(kn[dd]);
+            a.vc[hb + (size_t)pos * hd + dd] = __float2half_rn(vn[dd]);
+        }
+        __threadfence();
+    }
+    const int npair = HPG * hd, ng = kThreads / npair;  // PV: ng key groups per (head, dim)
+    for (int j0 = c0; j0 < c1; j0 += kKC) {
+        const int j1 = min(c1, j0 + kKC), nk = j1 - j0;
+        if (j0 != c0) {
+            __syncthreads();
+            stage(j0, j1);
+        }
+        if (pos >= j0 && pos < j1)
+            for (int dd = tid; dd < hd; dd += kThreads) {
+                Ks[(pos - j0) * hd + dd] = __float2half_rn(kn[dd]);
+                Vs[(pos - j0) * hd + dd] = __float2half_rn(vn[dd]);
+            }
+        __syncthreads();
+        // scores: a warp per key, lanes over dimensions
+        for (int jj = warp; jj < nk; jj += kWarps) {
+            for (int h = 0; h < HPG; ++h) {
+                float s = 0.f;
+                for (int dd = lane; dd < hd; dd += 32) s = fmaf(q[h * hd + dd], __half2float(Ks[jj * hd + dd]), s);
+                s = warp_sum(s);
+                if (lane == 0) sc[h * kKC + jj] = s;
+            }
+        }
+        __syncthreads();
+        // online softmax per head (warp h)
+        if (warp < HPG) {
+            const int h = warp;
+            float mx = -INFINITY;
+            for (int jj = lane; jj < nk; jj += 32) mx = fmaxf(mx, sc[h * kKC + jj]);
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            const float mnew = fmaxf(mm[h], mx);
+            float ps = 0.f;
+            for (int jj = lane; jj < nk; jj += 32) {
+                const float p = expf(sc[h * kKC + jj] - mnew);
+                sc[h * kKC + jj] = p;
+                ps += p;
+            }
+            ps = warp_sum(ps);
+            if (lane == 0) {
+                const float corr = expf(mm[h] - mnew);
+                cr[h] = corr;
+                ls[h] = ls[h] * corr + ps;
+                mm[h] = mnew;
+            }
+        }
+        __syncthreads();
+        // PV: thread (group kg, pair t) sums keys kg, kg + ng, ...
+        if (tid < ng * npair) {
+            const int kg = tid / npair, t = tid - kg * npair, h = t / hd, dd = t - h * hd;
+            float acc = 0.f;
+            for (int jj = kg; jj < nk; jj += ng) acc = fmaf(sc[h * kKC + jj], __half2float(Vs[jj * hd + dd]), acc);
+            op[tid] = acc;
+        }
+        __syncthreads();
+        for (int t = tid; t < npair; t += kThreads) {
+            float acc = 0.f;
+            for (int kg = 0; kg < ng; ++kg) acc += op[kg * npair + t];
+            o[t] = o[t] * cr[t / hd] + acc;
+        }
+    }
+    __syncthreads();
+    // publish (o[hd], m, l) per query head of the group
+    const int W = hd + 2;
+    for (int t = tid; t < HPG * W; t += kThreads) {
+        const int h = t / W, k = t - h * W;
+        const float v = k < hd ? o[h * hd + k] : (k == hd ? mm[h] : ls[h]);
+        unsigned long long* dst = a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k);
+        ll_store(dst, v, e);
+    }
+    __syncthreads();
+    return true;
+}
+
+// ------------------------------------------------------------------ the kernel
 
 template <int QK, int NB>
 __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
-    constexpr int R = (NB == 1) ? 4 : 2;
-    extern __shared__ __align__(16) unsigned char smraw[];
-    __shared__ float s_scr[33 * NB];
-    __shared__ float s_tot[kWarps * R * NB];
-    __shared__ __align__(16) float s_bias[kMaxBiasRows];
+    extern __shared__ __align__(128) unsigned char sm[];
+    unsigned char* ring = sm;
+    float* act = reinterpret_cast<float*>(sm + a.ring_bytes);
+    StepLayer* tab = reinterpret_cast<StepLayer*>(sm + a.ring_bytes + a.act_bytes);
+    __shared__ __align__(8) unsigned long long s_mb[kNMB];
+    __shared__ long long s_rec[kNMB];  // ring position (monotonic bytes) of record i % kNMB
+    __shared__ long long s_head;       // next free ring position (thread 0)
+    __shared__ long long s_ni;         // records issued (thread 0)
     __shared__ float s_own[NB * kMaxOwn];
-    __shared__ attn_detail::AttnScratch s_attn;
+    __shared__ float s_part[kMaxPart];
+    __shared__ float s_y[kMaxPart];
+    __shared__ float s_red[33 * NB + 8];
     __shared__ sample_detail::SampleScratch s_samp;
 
-    const int G = gridDim.x, cta = blockIdx.x;
-    const int d = a.d, qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
-    const int kmax = max(max(d, a.ff), qd);
-    // dynamic shared memory: [NB][kmax] staged activations, then [kmax] norm gain, [kmax] norm offset;
-    // the attention staging and the sampler reuse the same bytes in their own phases
-    float* s_x = reinterpret_cast<float*>(smraw);
-    float* s_g = s_x + NB * kmax;
-    float* s_b = s_g + kmax;
-    const bool swiglu = !a.gpt2;
-    const int pro = a.gpt2 ? PRO_LN : PRO_RMS;
-    unsigned nbar = 0;
-    // trace: 4 stamps per barrier interval -- staged, computed, preloaded, barrier passed
-    auto stamp = [&](int k) {
-        if (a.trace && cta == 0 && threadIdx.x == 0 && (int)nbar < a.trace_cap) {
-            unsigned long long t;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            a.trace[4 * nbar + k] = t;
-        }
-    };
-    auto sync = [&]() {
-        stamp(2);
-        const bool ok = grid_sync(a.bar, (nbar + 1) * (unsigned)G, a.err, a.spin_budget);
-        stamp(3);
-        ++nbar;
-        return ok;
-    };
-
-    // this CTA's static row ranges; o0..o1 (rows of the residual stream) serve embed, O and proj
-    int q0, q1, o0, o1, f0, f1, h0, h1;
-    row_range(qkv_rows, cta, G, q0, q1);
+    const int G = gridDim.x, cta = blockIdx.x, tid = threadIdx.x;
+    const int L = a.n_layer, d = a.d, qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
+    const int per_step = 4 * L + 1;
+    const long long total = (long long)a.n_steps * per_step;
+    const int RB = a.ring_bytes;
+    const long long budget = a.spin_budget;
+    const bool ln = a.gpt2 != 0;
+    int o0, o1;
     row_range(d, cta, G, o0, o1);
-    row_range(a.ff, cta, G, f0, f1);
-    if (swiglu) { f0 *= 2; f1 *= 2; }          // gate/up rows are interleaved in pairs
-    row_range(a.V, cta, G, h0, h1);
 
-    auto prefetch_layer = [&](int l) {
-        if (threadIdx.x != 0 || l >= a.n_layer || a.prefetch <= 0) return;
-        const StepLayer& L = a.layers[l];
-        prefetch_rows(L.wqkv, q0, q1);
-        prefetch_rows(L.wo, o0, o1);
-        prefetch_rows(L.wfc, f0, f1);
-        prefetch_rows(L.wproj, o0, o1);
-    };
-    GemvPre<QK, R> pre;
-    // constants of a layer's QKV phase (or of the head when l == n_layer)
-    auto preload_qkv = [&](int l) {
-        if (l < a.n_layer) {
-            const StepLayer& L = a.layers[l];
-            preload_vec(L.n1g, d, s_g);
-            preload_vec(L.n1b, d, s_b);
-            gemv_preload<QK, R>(pre, L.wqkv, q0, q1, L.bqkv, s_bias);
-        } else {
-            preload_vec(a.nfg, d, s_g);
-            preload_vec(a.nfb, d, s_b);
-            gemv_preload<QK, R>(pre, a.head, h0, h1, nullptr, s_bias);
-        }
-    };
-    if (threadIdx.x == 0 && a.trace) {
-        unsigned long long t;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        a.trace[4 * a.trace_cap] = t;  // launch start, in the slot after the barrier stamps
+    {
+        const int words = L * (int)(sizeof(StepLayer) / 4);
+        for (int i = tid; i < words; i += kThreads)
+            reinterpret_cast<int*>(tab)[i] = reinterpret_cast<const int*>(a.layers)[i];
     }
-    prefetch_layer(0);
-    prefetch_layer(1);
-    preload_qkv(0);
+    if (tid == 0) {
+        for (int k = 0; k < kNMB; ++k) mb_init(smem_u32(&s_mb[k]));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_head = 0;
+        s_ni = 0;
+    }
+    __syncthreads();
 
-    for (int s = 0; s < a.n_steps; ++s) {
-        const int pos = __ldcg(a.pos);
-        if (pos < 0 || pos >= a.n_ctx) {
-            if (threadIdx.x == 0) atomicCAS(a.err, 0, 1);
-            break;
-        }
-        // ---- embedding of this CTA's residual rows: x[b][r] = wte[tok][r] (+ wpe[pos][r])
-        for (int i = threadIdx.x; i < NB * (o1 - o0); i += blockDim.x) {
-            const int b = i / (o1 - o0), r = o0 + i % (o1 - o0);
-            int tok = __ldcg(a.tok + b);
-            if (tok < 0 || tok >= a.V) {
-                atomicCAS(a.err, 0, 3);
-                tok = 0;
+    const unsigned gen0 = *reinterpret_cast<const volatile unsigned*>(a.gen);
+    const int pos0 = ld_volatile(a.pos);
+    long long nc = 0;  // records consumed (uniform over the block)
+
+    // thread 0: issue the following records while the ring and the barriers have room
+    auto refill = [&]() {
+        if (tid != 0) return;
+        long long ni = s_ni, head = s_head;
+        bool fenced = false;
+        while (ni < total && ni - nc < kNMB) {
+            const Slice sl = make_slice(a, tab, (int)(ni % per_step), cta, G);
+            long long start = head;
+            if ((start % RB) + sl.bytes > RB) start += RB - (start % RB);
+            if (ni > nc && start + sl.bytes - s_rec[nc % kNMB] > RB) break;
+            if (!fenced) {  // the space was last read through the generic proxy
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                fenced = true;
             }
-            float v = __ldg(a.wte + (size_t)tok * d + r);
-            if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + r);
-            s_own[b * kMaxOwn + (r - o0)] = v;
-            a.x[(size_t)b * d + r] = v;
+            const uint32_t dst = smem_u32(ring + (start % RB));
+            const uint32_t mb = smem_u32(&s_mb[ni % kNMB]);
+            s_rec[ni % kNMB] = start;
+            mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) + (sl.g2 ? sl.n_g : 0)));
+            bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
+            bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
+            if (sl.bias) bulk_g2s(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb);
+            if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
+            if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
+            head = start + sl.bytes;
+            ++ni;
         }
-        if (!sync()) break;
+        s_ni = ni;
+        s_head = head;
+    };
+    // trace: CTA 0 sums, per phase kind, the wait for its inputs, the wait for
+    // its weight record and the rest (ns)
+    unsigned long long t_a = 0, t_b = 0, t_w = 0;
+    // waits for record nc (slice j of the step); returns its base in the ring
+    auto wait_rec = [&](const Slice& sl, bool& ok) -> const unsigned char* {
+        refill();
+        const unsigned long long tw0 = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
+        const uint32_t mb = smem_u32(&s_mb[nc % kNMB]);
+        ok = mb_wait(mb, (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
+        ok = __syncthreads_and(ok) != 0;
+        if (a.trace && cta == 0 && tid == 0) t_w += gtime() - tw0;
+        (void)sl;
+        return ring + (s_rec[nc % kNMB] % RB);
+    };
+    auto done_rec = [&]() {
+        __syncthreads();
+        ++nc;
+    };
+    auto tr_begin = [&]() { if (a.trace && cta == 0 && tid == 0) { t_a = gtime(); t_w = 0; } };
+    auto tr_waited = [&]() { if (a.trace && cta == 0 && tid == 0) t_b = gtime(); };
+    auto tr_end = [&](int kind) {
+        if (a.trace && cta == 0 && tid == 0) {
+            const unsigned long long t = gtime();
+            a.trace[3 * kind] += t_b - t_a;
+            a.trace[3 * kind + 1] += t_w;
+            a.trace[3 * kind + 2] += t - t_b - t_w;
+        }
+    };
 
-        bool ok = true;
-        for (int l = 0; l < a.n_layer && ok; ++l) {
-            const StepLayer& L = a.layers[l];
-            // ---- QKV (norm prologue, bias)
-            stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
-            stamp(0);
-            gemv_finish<QK, NB, R>(pre, L.wqkv, q0, q1, s_x, EPI_LINEAR, L.bqkv ? s_bias : nullptr, nullptr, 0,
-                                   a.qkv, qkv_rows, s_tot);
-            stamp(1);
-            const int items = NB * a.Hkv * a.nsplit;
-            if (threadIdx.x == 0 && a.prefetch > 0) {
-                // the cached K/V rows this CTA's attention items will read, and the next layer's weights
-                const int n = pos + 1, chunk = (n + a.nsplit - 1) / a.nsplit;
-                for (int it = cta; it < items; it += G) {
-                    const int split = it % a.nsplit, g = (it / a.nsplit) % a.Hkv, b = it / (a.nsplit * a.Hkv);
-                    const int c0 = split * chunk, c1 = min(n - 1, c0 + chunk);  // rows < pos are cached
-                    if (c1 > c0) {
-                        const size_t hb = ((size_t)(b * a.n_layer * a.Hkv + l * a.Hkv + g) * a.n_ctx) * a.hd;
-                        prefetch_l2(a.kc + hb + (size_t)c0 * a.hd, (size_t)(c1 - c0) * a.hd * 2);
-                        prefetch_l2(a.vc + hb + (size_t)c0 * a.hd, (size_t)(c1 - c0) * a.hd * 2);
+    refill();
+    bool ok = true;
+    for (int s = 0; s < a.n_steps && ok; ++s) {
+        const int pos = pos0 + s;
+        const unsigned eb = 1u + (gen0 + (unsigned)s) * (unsigned)(L + 1);  // epoch of layer 0 in this step
+        // ---- embedding (every CTA builds the whole input row; it owns rows o0..o1)
+        tr_begin();
+        {
+            int tk[NB];
+            bool okr = true;
+            if (s == 0) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) tk[b] = ld_volatile(a.tok + b);
+            } else {
+                if (tid < NB) {
+                    unsigned long long w = ll_load(a.ll_tok + tid);
+                    const unsigned et = eb - 1u;  // layer L of the previous step
+                    if ((unsigned)(w >> 32) != et) okr = ll_spin(a.ll_tok + tid, et, &w, a.err, budget);
+                    reinterpret_cast<int*>(s_red)[tid] = (int)(unsigned)w;
+                }
+                okr = __syncthreads_and(okr) != 0;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) tk[b] = reinterpret_cast<int*>(s_red)[b];
+                __syncthreads();
+            }
+            if (!okr) { ok = false; break; }
+            __threadfence();  // order this step's cache reads after the previous steps' appends
+            tr_waited();
+            for (int i = tid; i < NB * d; i += kThreads) {
+                const int b = i / d, k = i - b * d;
+                int t = tk[b];
+                if (t < 0 || t >= a.V) {
+                    atomicCAS(a.err, 0, 3);
+                    t = 0;
+                }
+                float v = __ldg(a.wte + (size_t)t * d + k);
+                if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + k);
+                act[i] = v;
+                if (k >= o0 && k < o1) s_own[b * kMaxOwn + (k - o0)] = v;
+            }
+            __syncthreads();
+            tr_end(PK_EMBED);
+        }
+
+        for (int l = 0; l < L && ok; ++l) {
+            const unsigned e = eb + (unsigned)l;
+            // ---- QKV rows (norm prologue, bias)
+            tr_begin();
+            if (l > 0) {
+                ok = __syncthreads_and(ll_read(a.ll_xb, NB, d, d, e - 1u, act, a.err, budget)) != 0;
+                if (!ok) break;
+            }
+            tr_waited();
+            {
+                const Slice sl = make_slice(a, tab, 4 * l, cta, G);
+                const unsigned char* rec = wait_rec(sl, ok);
+                if (!ok) break;
+                norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                const int nr = sl.r1 - sl.r0;
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+                const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
+                for (int t = tid; t < nr * NB; t += kThreads) {
+                    const int i = t / NB, b = t - i * NB;
+                    float v = s_y[t];
+                    if (sl.bias) v += bias[i];
+                    ll_store(a.ll_qkv + (size_t)b * qkv_rows + sl.r0 + i, v, e);
+                }
+                done_rec();
+            }
+            tr_end(PK_QKV);
+            // ---- attention items
+            tr_begin();
+            int S, chunk;
+            attn_split(a, pos + 1, S, chunk);
+            {
+                const int items = NB * a.Hkv * S;
+                tr_waited();
+                for (int it = cta; it < items && ok; it += G) {
+                    const int c = it % S, g = (it / S) % a.Hkv, b = it / (S * a.Hkv);
+                    ok = attn_item(a, l, b, g, c, S, chunk, pos, e, act, a.err);
+                }
+                if (!ok) break;
+            }
+            tr_end(PK_ATTN);
+            // ---- O rows: combine the partials, +bias +residual
+            tr_begin();
+            {
+                const int W = a.hd + 2;
+                float* pp = act + NB * qd;  // [NB*H][S][W]
+                ok = __syncthreads_and(ll_read(a.ll_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget)) != 0;
+                if (!ok) break;
+                tr_waited();
+                for (int t = tid; t < NB * qd; t += kThreads) {
+                    const int bh = t / a.hd, dd = t - bh * a.hd;
+                    const float* P = pp + (size_t)bh * S * W;
+                    float M = -INFINITY;
+                    for (int c = 0; c < S; ++c) M = fmaxf(M, P[c * W + a.hd]);
+                    float num = 0.f, den = 0.f;
+                    for (int c = 0; c < S; ++c) {
+                        const float w = expf(P[c * W + a.hd] - M);
+                        num = fmaf(w, P[c * W + dd], num);
+                        den = fmaf(w, P[c * W + a.hd + 1], den);
+                    }
+                    act[t] = num / den;  // act[b][h * hd + dd]
+                }
+                __syncthreads();
+                const Slice sl = make_slice(a, tab, 4 * l + 1, cta, G);
+                const unsigned char* rec = wait_rec(sl, ok);
+                if (!ok) break;
+                const int nr = sl.r1 - sl.r0;
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), qd, nr, act, s_part, s_y);
+                const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
+                for (int t = tid; t < nr * NB; t += kThreads) {
+                    const int i = t / NB, b = t - i * NB;
+                    float v = s_y[t];
+                    if (sl.bias) v += bias[i];
+                    v += s_own[b * kMaxOwn + i];
+                    s_own[b * kMaxOwn + i] = v;
+                    ll_store(a.ll_xa + (size_t)b * d + sl.r0 + i, v, e);
+                }
+                done_rec();
+            }
+            tr_end(PK_O);
+            // ---- FC / gate-up rows (norm prologue, GELU / SwiGLU)
+            tr_begin();
+            {
+                ok = __syncthreads_and(ll_read(a.ll_xa, NB, d, d, e, act, a.err, budget)) != 0;
+                if (!ok) break;
+                tr_waited();
+                const Slice sl = make_slice(a, tab, 4 * l + 2, cta, G);
+                const unsigned char* rec = wait_rec(sl, ok);
+                if (!ok) break;
+                norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                const int nr = sl.r1 - sl.r0;
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+                const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
+                if (ln) {
+                    for (int t = tid; t < nr * NB; t += kThreads) {
+                        const int i = t / NB, b = t - i * NB;
+                        float v = s_y[t];
+                        if (sl.bias) v += bias[i];
+                        ll_store(a.ll_u + (size_t)b * a.ff + sl.r0 + i, gelu_tanh(v), e);
+                    }
+                } else {
+                    for (int t = tid; t < (nr / 2) * NB; t += kThreads) {
+                        const int i = t / NB, b = t - i * NB;
+                        const float gt = s_y[(2 * i) * NB + b], up = s_y[(2 * i + 1) * NB + b];
+                        ll_store(a.ll_u + (size_t)b * a.ff + sl.r0 / 2 + i, silu(gt) * up, e);
                     }
                 }
+                done_rec();
             }
-            if (l + 1 < a.n_layer) prefetch_layer(l + 1);
-            else if (threadIdx.x == 0 && a.prefetch > 0) prefetch_rows(a.head, h0, h1);
-            if (!(ok = sync())) break;
-            // ---- attention items
+            tr_end(PK_FC);
+            // ---- proj / down rows (+bias +residual)
+            tr_begin();
             {
-                AttnArgs at;
-                at.q = a.qkv; at.q_stride = qkv_rows; at.knew = a.qkv + qd; at.vnew = a.qkv + qd + kd;
-                at.kc = a.kc; at.vc = a.vc; at.row_heads = a.n_layer * a.Hkv; at.head_off = l * a.Hkv;
-                at.n_head = a.H; at.n_kv = a.Hkv; at.hd = a.hd; at.n_ctx = a.n_ctx; at.nsplit = a.nsplit;
-                at.pos_ptr = a.pos; at.rope_cos = a.rope_cos; at.rope_sin = a.rope_sin; at.part = a.part;
-                at.counters = a.counters; at.out = a.o; at.out_stride = qd; at.err = a.err;
-                stamp(0);
-                for (int it = cta; it < items; it += G) {
-                    const int split = it % a.nsplit, g = (it / a.nsplit) % a.Hkv, b = it / (a.nsplit * a.Hkv);
-                    attn_detail::attn_item(at, split, g, b, reinterpret_cast<float*>(smraw), s_attn);
+                ok = __syncthreads_and(ll_read(a.ll_u, NB, a.ff, a.ff, e, act, a.err, budget)) != 0;
+                if (!ok) break;
+                tr_waited();
+                const Slice sl = make_slice(a, tab, 4 * l + 3, cta, G);
+                const unsigned char* rec = wait_rec(sl, ok);
+                if (!ok) break;
+                const int nr = sl.r1 - sl.r0;
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), a.ff, nr, act, s_part, s_y);
+                const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
+                for (int t = tid; t < nr * NB; t += kThreads) {
+                    const int i = t / NB, b = t - i * NB;
+                    float v = s_y[t];
+                    if (sl.bias) v += bias[i];
+                    v += s_own[b * kMaxOwn + i];
+                    s_own[b * kMaxOwn + i] = v;
+                    ll_store(a.ll_xb + (size_t)b * d + sl.r0 + i, v, e);
                 }
-                stamp(1);
+                done_rec();
             }
-            gemv_preload<QK, R>(pre, L.wo, o0, o1, L.bo, s_bias);
-            if (!(ok = sync())) break;
-            // ---- O projection (+bias +residual)
-            stage_x<NB>(a.o, qd, qd, PRO_NONE, nullptr, nullptr, 0.f, s_x, s_scr);
-            stamp(0);
-            gemv_finish<QK, NB, R>(pre, L.wo, o0, o1, s_x, EPI_LINEAR, L.bo ? s_bias : nullptr, s_own, kMaxOwn,
-                                   a.x, d, s_tot);
-            stamp(1);
-            preload_vec(L.n2g, d, s_g);
-            preload_vec(L.n2b, d, s_b);
-            gemv_preload<QK, R>(pre, L.wfc, f0, f1, L.bfc, s_bias);
-            if (!(ok = sync())) break;
-            // ---- FC / gate-up (norm prologue, GELU / SwiGLU)
-            stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
-            stamp(0);
-            gemv_finish<QK, NB, R>(pre, L.wfc, f0, f1, s_x, swiglu ? EPI_SWIGLU : EPI_GELU,
-                                   L.bfc ? s_bias : nullptr, nullptr, 0, a.u, a.ff, s_tot,
-                                   (a.trace && s == 0 && l == 1) ? a.trace + 4 * (size_t)a.trace_cap + 1 : nullptr);
-            stamp(1);
-            gemv_preload<QK, R>(pre, L.wproj, o0, o1, L.bproj, s_bias);
-            if (!(ok = sync())) break;
-            // ---- proj / down (+bias +residual)
-            stage_x<NB>(a.u, a.ff, a.ff, PRO_NONE, nullptr, nullptr, 0.f, s_x, s_scr);
-            stamp(0);
-            gemv_finish<QK, NB, R>(pre, L.wproj, o0, o1, s_x, EPI_LINEAR, L.bproj ? s_bias : nullptr, s_own,
-                                   kMaxOwn, a.x, d, s_tot);
-            stamp(1);
-            preload_qkv(l + 1);
-            if (!(ok = sync())) break;
+            tr_end(PK_PROJ);
         }
         if (!ok) break;
-        // ---- head (final norm prologue)
-        stage_x<NB>(a.x, d, d, pro, s_g, s_b, a.eps, s_x, s_scr);
-        gemv_finish<QK, NB, R>(pre, a.head, h0, h1, s_x, EPI_LINEAR, nullptr, nullptr, 0, a.logits, a.V, s_tot);
-        // the next step's first layers stream in while the sampler runs
-        if (s + 1 < a.n_steps) {
-            prefetch_layer(0);
-            prefetch_layer(1);
+        // ---- head rows (final norm prologue)
+        const unsigned eh = eb + (unsigned)L;
+        tr_begin();
+        {
+            ok = __syncthreads_and(ll_read(a.ll_xb, NB, d, d, eh - 1u, act, a.err, budget)) != 0;
+            if (!ok) break;
+            tr_waited();
+            const Slice sl = make_slice(a, tab, 4 * L, cta, G);
+            const unsigned char* rec = wait_rec(sl, ok);
+            if (!ok) break;
+            norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                          reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+            const int nr = sl.r1 - sl.r0;
+            gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+            for (int t = tid; t < nr * NB; t += kThreads) {
+                const int i = t / NB, b = t - i * NB;
+                const float v = s_y[t];
+                a.logits[(size_t)b * a.V + sl.r0 + i] = v;
+                ll_store(a.ll_logits + (size_t)b * a.V + sl.r0 + i, v, eh);
+            }
+            done_rec();
         }
-        if (!sync()) break;
+        tr_end(PK_HEAD);
         // ---- sampler: CTA b samples row b
         if (cta < NB) {
+            tr_begin();
+            float* z = act;
+            ok = __syncthreads_and(ll_read(a.ll_logits + (size_t)cta * a.V, 1, 0, a.V, eh, z, a.err, budget)) != 0;
+            if (!ok) break;
+            tr_waited();
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + cta : a.u1 + cta;
-            const int tok = sample_detail::sample_block(a.logits + (size_t)cta * a.V, a.V, *a.sp, up, smraw, s_samp,
-                                                        a.err);
-            if (threadIdx.x == 0) {
+            const int tok = sample_detail::sample_smem(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
+                                                       a.err);
+            if (tid == 0) {
                 a.tok[cta] = tok;
                 if (a.out_seq) a.out_seq[(size_t)s * NB + cta] = tok;
-                if (cta == 0) *a.pos = pos + 1;
+                ll_store(a.ll_tok + cta, __int_as_float(tok), eh);
             }
+            tr_end(PK_SAMPLE);
         }
-        if (s + 1 < a.n_steps) preload_qkv(0);
-        if (!sync()) break;
     }
+    // final counters (CTA 0; every other CTA read gen and pos at its start).  The
+    // generation advances even after an error, so that no later epoch can match
+    // a word this launch wrote.
+    if (cta == 0 && tid == 0) {
+        if (ok) *a.pos = pos0 + a.n_steps;
+        *a.gen = gen0 + (unsigned)a.n_steps;
+    }
+    // copies still in flight into this CTA's ring finish before it exits
+    __syncthreads();
+    if (tid == 0) {
+        const long long ni = s_ni;
+        for (long long i = nc; i < ni; ++i)
+            mb_wait(smem_u32(&s_mb[i % kNMB]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
+    }
+}
+
+// Bytes of the activation region: staged input rows, the attention item
+// workspace, the O-phase partials and the sampler's arrays.
+size_t act_region_bytes(const StepArgs& a) {
+    const int qd = a.H * a.hd, HPG = a.H / a.Hkv;
+    int kmax = a.d > a.ff ? a.d : a.ff;
+    if (qd > kmax) kmax = qd;
+    size_t need = sizeof(float) * (size_t)a.B * kmax;
+    const size_t o_phase = sizeof(float) * ((size_t)a.B * qd + (size_t)a.B * a.H * a.max_split * (a.hd + 2));
+    // attention floats before the fp16 staging: a multiple of 4 (16 bytes) for every hd in {64, 128}
+    const size_t attn_floats = (size_t)2 * HPG * a.hd + 2 * a.hd + HPG * kKC + 3 * kMaxHPG + kThreads;
+    const size_t attn = sizeof(float) * attn_floats + sizeof(__half) * 2 * kKC * a.hd;
+    const size_t smp = sample_smem_bytes_dev(a.V, kThreads);
+    if (o_phase > need) need = o_phase;
+    if (attn > need) need = attn;
+    if (smp > need) need = smp;
+    return (need + 127) & ~(size_t)127;
+}
+
+template <int QK, int NB>
+void* kernel_ptr() {
+    return reinterpret_cast<void*>(k_step<QK, NB>);
+}
+
+void* pick(const StepArgs& a) {
+    if (a.quant == SD_Q8_0) return a.B == 1 ? kernel_ptr<SD_Q8_0, 1>() : kernel_ptr<SD_Q8_0, 2>();
+    if (a.quant == SD_Q4_0) return a.B == 1 ? kernel_ptr<SD_Q4_0, 1>() : kernel_ptr<SD_Q4_0, 2>();
+    return nullptr;
 }
 
 }  // namespace step_detail
 
 size_t step_smem_bytes(const StepArgs& a) {
-    const int B = a.B;
-    int kmax = a.d > a.ff ? a.d : a.ff;
-    if (a.H * a.hd > kmax) kmax = a.H * a.hd;
-    size_t need = sizeof(float) * (size_t)(B + 2) * kmax;
-    AttnArgs at;
-    at.n_head = a.H; at.n_kv = a.Hkv; at.hd = a.hd; at.n_ctx = a.n_ctx; at.nsplit = a.nsplit;
-    const size_t att = attention_smem_bytes_dev(at);
-    const size_t smp = sample_smem_bytes_dev(a.V);
-    if (att > need) need = att;
-    if (smp > need) need = smp;
-    return need;
+    return (size_t)a.ring_bytes + (size_t)a.act_bytes + sizeof(StepLayer) * (size_t)a.n_layer;
+}
+
+// Fills ring_bytes / act_bytes / max_split of `a` (taken as the plan) and
+// returns the grid, or 0 when the configuration does not fit the kernel.
+int step_plan_grid(StepArgs& a, int sm_count) {
+    using namespace step_detail;
+    void* kern = pick(a);
+    if (!kern || a.B < 1 || a.B > 2 || a.n_layer < 1) return 0;
+    const int qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
+    const int HPG = a.Hkv > 0 ? a.H / a.Hkv : 0;
+    if (a.Hkv < 1 || a.H % a.Hkv || HPG > kMaxHPG || (a.hd != 64 && a.hd != 128) || HPG * a.hd > kThreads) return 0;
+    if (a.V > sample_detail::kMaxV || a.d % 32 || a.ff % 32 || qd % 32) return 0;
+    int G = sm_count < a.d ? sm_count : a.d;
+    if (G > qkv_rows || G > a.ff || G > a.V) return 0;
+    if ((a.d + G - 1) / G > kMaxOwn) return 0;
+    // partial-sum staging of every slice: rows per CTA x batch rows x K slices
+    auto fits = [&](int rows, int K) { return ((rows + G - 1) / G + 2) * a.B * ((K + 1023) / 1024) <= kMaxPart; };
+    if (!fits(qkv_rows, a.d) || !fits(a.d, qd) || !fits(a.gpt2 ? a.ff : 2 * a.ff, a.d) || !fits(a.d, a.ff) ||
+        !fits(a.V, a.d))
+        return 0;
+    a.max_split = G / (a.B * a.Hkv);
+    if (a.max_split > 8) a.max_split = 8;
+    if (a.max_split < 1) a.max_split = 1;
+    a.act_bytes = (int)act_region_bytes(a);
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return 0;
+    const int limit = 227 * 1024 - (int)fa.sharedSizeBytes - 1024;
+    const int ring = (limit - a.act_bytes - (int)(sizeof(StepLayer) * a.n_layer)) & ~127;
+    // the largest record: per slice, the rows one CTA owns (+2 for pair rounding)
+    // times the row's codes and scales, plus the bias and gain windows
+    auto rec = [&](int rows, int K, bool gains) {
+        const int nr = (rows + G - 1) / G + 2;
+        const int rowb = a.quant == SD_Q4_0 ? K / 2 : K;
+        return nr * (rowb + K / 16) + 32 + (nr + 8) * 4 + (gains ? 8 * a.d : 0) + 128;
+    };
+    int max_rec = rec(qkv_rows, a.d, true);
+    const int cand[4] = {rec(a.d, qd, false), rec(a.gpt2 ? a.ff : 2 * a.ff, a.d, true), rec(a.d, a.ff, false),
+                         rec(a.V, a.d, true)};
+    for (int i = 0; i < 4; ++i) max_rec = cand[i] > max_rec ? cand[i] : max_rec;
+    if (ring < 2 * max_rec) return 0;
+    a.ring_bytes = ring;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)step_smem_bytes(a)) !=
+        cudaSuccess)
+        return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, step_smem_bytes(a)) != cudaSuccess ||
+        per_sm < 1)
+        return 0;
+    return G;
 }
 
 cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st) {
     using namespace step_detail;
+    void* kern = pick(a);
+    if (!kern || grid < 1) return cudaErrorInvalidValue;
     const size_t smem = step_smem_bytes(a);
-    void (*kern)(const StepArgs) = nullptr;
-    if (a.quant == SD_Q8_0) kern = a.B == 1 ? k_step<SD_Q8_0, 1> : k_step<SD_Q8_0, 2>;
-    else if (a.quant == SD_Q4_0) kern = a.B == 1 ? k_step<SD_Q4_0, 1> : k_step<SD_Q4_0, 2>;
-    else return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -566,20 +938,8 @@ cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
-}
-
-int step_max_grid(const StepArgs& a, int sm_count) {
-    using namespace step_detail;
-    const size_t smem = step_smem_bytes(a);
-    void (*kern)(const StepArgs) = nullptr;
-    if (a.quant == SD_Q8_0) kern = a.B == 1 ? k_step<SD_Q8_0, 1> : k_step<SD_Q8_0, 2>;
-    else if (a.quant == SD_Q4_0) kern = a.B == 1 ? k_step<SD_Q4_0, 1> : k_step<SD_Q4_0, 2>;
-    else return 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess) return 0;
-    return per_sm >= 1 ? sm_count : 0;
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace sd

@@ -1,18 +1,25 @@
 // Block-level sampler (temperature -> top-k -> top-p -> index-order draw),
-// shared by the sampler kernel and the persistent step kernel.
+// shared by the sampler kernel and the persistent step kernels.
 // "Chatterbox -> ggml Port: Development Journal", section 3.2 (order) and the
 // defaults table of section 3.9; "Every Frame Is a Memory Read", section 5.6
 // (top-p over the top-k survivors, drawn in full-vocabulary index order).
 //
 //   greedy   argmax, ties to the lowest index;
 //   top-k    4-pass 8-bit radix select of the k-th largest order-preserving
-//            key (one warp finds each digit) -- every logit >= it survives;
-//   softmax  p_i = exp((z_i - max) / T) over the survivors, fp32, fixed order;
-//   top-p    survivors sorted by (p desc, index asc) with a bitonic sort of
-//            64-bit keys (logit key << 32 | ~index); the shortest prefix whose
-//            mass reaches top_p * Z is kept;
-//   draw     the smallest vocabulary index whose cumulative kept mass (index
-//            order, block prefix scan) exceeds u times the kept total.
+//            logit key (counts, per-warp histograms merged in fixed order) --
+//            every logit whose key is >= it survives;
+//   softmax  p_i = exp((z_i - max) / T) over the survivors (fp32), each
+//            mass also as a 2^-31 fixed-point integer so that every sum
+//            below is exact and independent of summation order;
+//   top-p    the survivors in (p desc, index asc) order are cut at the
+//            shortest prefix whose mass reaches top_p * Z: a second 4-pass
+//            radix select, on mass instead of counts, finds the key of the
+//            element where the cumulative mass crosses, and a prefix scan
+//            over its ties (index order) finds the element itself;
+//   draw     the smallest vocabulary index whose cumulative kept mass
+//            (index order) exceeds u times the kept total.
+// Shared memory: z[V] and p[V] (fp32), one 256-bin histogram per warp, and a
+// small fixed scratch.  No sort.
 #pragma once
 #include "sd_internal.cuh"
 
@@ -20,13 +27,14 @@ namespace sd {
 namespace sample_detail {
 
 constexpr int kMaxV = 16384;
-
 struct SampleScratch {
     float f[72];
     int i[40];
-    int hist[256];
-    uint32_t sel[3];  // prefix, mask, remaining
-    int cnt;
+    unsigned long long q[72];
+    unsigned hist[256];
+    unsigned long long mass[256];
+    uint32_t sel[4];  // key prefix, mask, remaining count; (top-p) tie index
+    unsigned long long rem;
 };
 
 static __device__ __forceinline__ uint32_t ord_key(float f) {
@@ -34,45 +42,48 @@ static __device__ __forceinline__ uint32_t ord_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-static __device__ __forceinline__ int pow2_ceil(int n) {
-    int c = 1;
-    while (c < n) c <<= 1;
-    return c;
+// p * 2^31 truncated to an integer, for p in [0, 1], by integer operations on
+// the float's fields (a float-to-64-bit-integer conversion is slow here).
+static __device__ __forceinline__ unsigned long long fixq(float p) {
+    const uint32_t u = __float_as_uint(p);
+    const int e = (int)(u >> 23) - 127;  // p = 1.m * 2^e
+    if (e < -31) return 0ull;            // below 2^-31 (and zero)
+    const uint32_t m = (u & 0x7FFFFFu) | 0x800000u;
+    const int sh = e + 8;                // p * 2^31 = m * 2^(e + 31 - 23)
+    return sh >= 0 ? (unsigned long long)m << sh : (unsigned long long)(m >> (-sh));
 }
 
-// exclusive scan of one float per thread (fixed order); returns the block total in *total
-static __device__ float block_exclusive_scan(float v, float* s_warp, float* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float inc = v;
+// byte offset of the per-warp histograms after z[V] and p[V]
+static __host__ __device__ __forceinline__ size_t sample_hist_offset(int V) { return ((size_t)8 * V + 15) & ~(size_t)15; }
+
+// exclusive scan of one u64 per thread in thread order; *total = block total
+static __device__ unsigned long long block_exclusive_scan_u64(unsigned long long v, unsigned long long* s,
+                                                              unsigned long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    unsigned long long inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, inc, o);
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += t;
     }
-    if (lane == 31) s_warp[warp] = inc;
+    if (lane == 31) s[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        float w = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0.f;
-        float wi = w;
+        const unsigned long long w = lane < nw ? s[lane] : 0ull;
+        unsigned long long wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_up_sync(0xffffffffu, wi, o);
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += t;
         }
-        s_warp[32 + lane] = wi - w;  // exclusive prefix of warp totals
-        if (lane == 31) s_warp[64] = wi;
+        s[32 + lane] = wi - w;
+        if (lane == 31) s[64] = wi;
     }
     __syncthreads();
-    const float r = s_warp[32 + warp] + inc - v;
-    *total = s_warp[64];
+    const unsigned long long r = s[32 + warp] + inc - v;
+    *total = s[64];
     __syncthreads();
     return r;
-}
-
-static __device__ float block_sum_f(float v, float* s_warp) {
-    float t;
-    block_exclusive_scan(v, s_warp, &t);
-    return t;
 }
 
 static __device__ int block_min_i(int v, int* s) {
@@ -92,227 +103,206 @@ static __device__ int block_min_i(int v, int* s) {
     return r;
 }
 
-static __device__ int block_max_i(int v, int* s) { return -block_min_i(-v, s); }
-
-// Samples one token from logits lg[0..V) with draw u (used by every thread of
-// the calling block; every thread gets the token).  Shared memory: `smraw`
-// holds sample_smem_bytes(V); `ss` the small scratch.  The block size is any
-// multiple of 32 up to 1024.
-static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
-                            unsigned char* smraw, SampleScratch& ss, int* err) {
-    const int tid = threadIdx.x, kST = blockDim.x;
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smraw);   // [pow2_ceil(V)]
-    float* z = reinterpret_cast<float*>(smraw + sizeof(unsigned long long) * pow2_ceil(V));  // [V] logits, then [V] p
-    float* s_f = ss.f;
-    int* s_i = ss.i;
-    int* s_hist = ss.hist;
-    uint32_t* s_sel = ss.sel;
-    int& s_cnt = ss.cnt;
-
-    // written by other CTAs in a persistent kernel: read through L2, all loads in flight at once
-    for (int i0 = 0; i0 < V; i0 += 16 * kST) {
-        float r[16];
+static __device__ float block_max_f(float v, float* s) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int i = i0 + j * kST + tid;
-            r[j] = i < V ? __ldcg(lg + i) : 0.f;
-        }
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float w = threadIdx.x < (blockDim.x >> 5) ? s[threadIdx.x] : -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int i = i0 + j * kST + tid;
-            if (i < V) z[i] = r[j];
-        }
+        for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+        if (threadIdx.x == 0) s[32] = w;
     }
     __syncthreads();
+    const float r = s[32];
+    __syncthreads();
+    return r;
+}
+
+// One digit of a radix select over the active elements, from the top:
+// finds the digit d (bits shift..shift+7 under the current prefix) at which
+// the cumulative weight of higher digits stays below the remaining rank and
+// reaches it within d.  Weights are per-digit totals in `w` (counts or fixed
+// masses).  Run by warp 0.
+template <typename T>
+static __device__ __forceinline__ void select_digit(const T* w, T rem, int shift, uint32_t* sel, T* rem_out) {
+    const int lane = threadIdx.x & 31;
+    T c[8], own = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        c[j] = w[255 - 8 * lane - j];
+        own += c[j];
+    }
+    T incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const T excl = incl - own;
+    const unsigned hit = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
+    if (hit && lane == __ffs(hit) - 1) {
+        T cum = excl;
+        int digit = 255 - 8 * lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (cum + c[j] >= rem) {
+                digit = 255 - 8 * lane - j;
+                break;
+            }
+            cum += c[j];
+        }
+        sel[0] |= (uint32_t)digit << shift;
+        sel[1] |= 255u << shift;
+        *rem_out = rem - cum;
+    }
+}
+
+// Samples one token from the logits already in shared memory (the first V
+// floats of `smraw`, which holds sample_smem_bytes_dev(V, blockDim.x) bytes) with draw
+// *u_ptr; every thread gets the token.  `ss` is the small scratch.  Block
+// size: any multiple of 32 up to 1024.
+static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
+                                  SampleScratch& ss, int* err) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    float* z = reinterpret_cast<float*>(smraw);   // [V] logits
+    float* pv = z + V;                            // [V] survivor masses (0 elsewhere)
+    // [nw][256] per-warp digit histograms: counts (top-k) or fixed-point masses (top-p)
+    unsigned long long* ph = reinterpret_cast<unsigned long long*>(smraw + sample_hist_offset(V));
+    unsigned* pc = reinterpret_cast<unsigned*>(ph);
+    (void)lane;
 
     int tok;
     if (sp.greedy || sp.top_k == 1 || sp.temperature <= 0.f) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        for (int i = tid; i < V; i += kST)
+        for (int i = tid; i < V; i += nt)
             if (z[i] > best) { best = z[i]; bi = i; }   // strided scan: first hit is the lowest index
-        // reduce (value desc, index asc)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-        }
-        if ((tid & 31) == 0) { s_f[tid >> 5] = best; s_i[tid >> 5] = bi; }
-        __syncthreads();
-        if (tid < 32) {
-            const bool have = tid < (kST >> 5);
-            best = have ? s_f[tid] : -INFINITY;
-            bi = have ? s_i[tid] : 0x7fffffff;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-            }
-            if (tid == 0) s_i[32] = bi;
-        }
-        __syncthreads();
-        tok = s_i[32];
+        const float mx = block_max_f(best, ss.f);
+        tok = block_min_i(best == mx ? bi : 0x7fffffff, ss.i);
     } else {
-        // ---- top-k threshold by radix select on order-preserving keys
+        float mloc = -INFINITY;
+        for (int i = tid; i < V; i += nt) mloc = fmaxf(mloc, z[i]);
+        const float mx = block_max_f(mloc, ss.f);
+
+        // ---- top-k: key of the k-th largest logit (counts, 4 x 8-bit digits)
         const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
-        if (tid == 0) { s_sel[0] = 0u; s_sel[1] = 0u; s_sel[2] = (uint32_t)k; }
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += kST) s_hist[i] = 0;
-            __syncthreads();
-            const uint32_t prefix = s_sel[0], mask = s_sel[1];
-            // lanes with equal digits add once (logits crowd into few high-order bins)
-            for (int i0 = 0; i0 < V; i0 += kST) {
-                const int i = i0 + tid;
-                const uint32_t key = i < V ? ord_key(z[i]) : 0u;
-                const bool in = i < V && (key & mask) == prefix;
-                const unsigned act = __ballot_sync(0xffffffffu, in);
-                if (in) {
-                    const uint32_t digit = (key >> shift) & 255u;
-                    const unsigned peers = __match_any_sync(act, digit);
-                    if ((tid & 31) == __ffs(peers) - 1) atomicAdd(&s_hist[digit], __popc(peers));
+        uint32_t thr = 0u;
+        if (k < V) {
+            if (tid == 0) { ss.sel[0] = 0u; ss.sel[1] = 0u; ss.sel[2] = (uint32_t)k; }
+            for (int shift = 24; shift >= 0; shift -= 8) {
+                // per-warp histograms: same-digit lanes collide only within their own warp
+                for (int i = tid; i < nw * 256; i += nt) pc[i] = 0u;
+                __syncthreads();
+                const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
+                for (int i = tid; i < V; i += nt) {
+                    const uint32_t key = ord_key(z[i]);
+                    if ((key & mask) == prefix) atomicAdd(&pc[warp * 256 + ((key >> shift) & 255u)], 1u);
                 }
+                __syncthreads();
+                for (int bn = tid; bn < 256; bn += nt) {
+                    unsigned t = 0u;
+                    for (int w = 0; w < nw; ++w) t += pc[w * 256 + bn];
+                    ss.hist[bn] = t;
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    uint32_t rem_out = 0;
+                    select_digit<uint32_t>(ss.hist, ss.sel[2], shift, ss.sel, &rem_out);
+                    const unsigned any = __ballot_sync(0xffffffffu, rem_out != 0u);
+                    if (any && lane == __ffs(any) - 1) ss.sel[2] = rem_out;
+                }
+                __syncthreads();
             }
-            __syncthreads();
-            if (tid < 32) {
-                // lane l owns bins 255-8l .. 248-8l (descending); find the digit whose
-                // cumulative count from the top reaches the remaining rank
-                const uint32_t rem = s_sel[2];
-                uint32_t c[8], own = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { c[j] = (uint32_t)s_hist[255 - 8 * tid - j]; own += c[j]; }
-                uint32_t incl = own;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += t;
-                }
-                const uint32_t excl = incl - own;
-                const unsigned hit = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
-                if (tid == __ffs(hit) - 1) {
-                    uint32_t cum = excl;
-                    int digit = 255 - 8 * tid;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (cum + c[j] >= rem) { digit = 255 - 8 * tid - j; break; }
-                        cum += c[j];
-                    }
-                    s_sel[0] = prefix | ((uint32_t)digit << shift);
-                    s_sel[1] = mask | (255u << shift);
-                    s_sel[2] = rem - cum;
-                }
-            }
-            __syncthreads();
+            thr = ss.sel[0];
         }
-        const uint32_t thr = s_sel[0];
 
-        // ---- max and softmax mass of the survivors
-        float mx = -INFINITY;
-        for (int i = tid; i < V; i += kST) mx = fmaxf(mx, z[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if ((tid & 31) == 0) s_f[tid >> 5] = mx;
-        __syncthreads();
-        mx = s_f[0];
-        for (int w = 1; w < (kST >> 5); ++w) mx = fmaxf(mx, s_f[w]);
-        __syncthreads();
+        // ---- survivor masses and their exact fixed-point total
         const float invT = 1.0f / sp.temperature;
-        float* pv = z + V;  // [V] probabilities of the survivors (0 elsewhere)
-        for (int i = tid; i < V; i += kST) pv[i] = ord_key(z[i]) >= thr ? expf((z[i] - mx) * invT) : 0.f;
-        __syncthreads();
-        auto pval = [&](int i) { return pv[i]; };
+        unsigned long long zloc = 0ull;
+        for (int i = tid; i < V; i += nt) {
+            const float p = ord_key(z[i]) >= thr ? expf((z[i] - mx) * invT) : 0.f;
+            pv[i] = p;
+            zloc += fixq(p);
+        }
+        unsigned long long Zq;
+        block_exclusive_scan_u64(zloc, ss.q, &Zq);
 
-        // ---- top-p: cut key over the (p desc, index asc) order
-        bool use_cut = false;
-        unsigned long long cut = 0ull;
+        // ---- top-p: crossing key by a mass radix select, then its ties in index order
+        bool cut = false;
+        uint32_t tkey = 0u;
+        int tidx = 0x7fffffff;
         if (sp.top_p < 1.0f) {
-            float zp = 0.f;
-            for (int i = tid; i < V; i += kST) zp += pv[i];
-            const float Z = block_sum_f(zp, s_f);
-            if (tid == 0) s_cnt = 0;
-            __syncthreads();
-            for (int i0 = 0; i0 < V; i0 += kST) {
-                const int i = i0 + tid;
-                const uint32_t key = i < V ? ord_key(z[i]) : 0u;
-                const bool keep = i < V && key >= thr;
-                const unsigned bal = __ballot_sync(0xffffffffu, keep);
-                int base = 0;
-                if ((tid & 31) == 0 && bal) base = atomicAdd(&s_cnt, __popc(bal));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                if (keep) {
-                    const int slot = base + __popc(bal & ((1u << (tid & 31)) - 1u));
-                    keys[slot] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+            const unsigned long long T = (unsigned long long)ceil((double)sp.top_p * (double)Zq);
+            if (tid == 0) { ss.sel[0] = 0u; ss.sel[1] = 0u; ss.rem = T > 0ull ? T : 1ull; }
+            for (int shift = 24; shift >= 0; shift -= 8) {
+                for (int i = tid; i < nw * 256; i += nt) ph[i] = 0ull;
+                __syncthreads();
+                const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
+                for (int i = tid; i < V; i += nt) {
+                    const float p = pv[i];
+                    const uint32_t key = ord_key(z[i]);
+                    if (p > 0.f && (key & mask) == prefix)
+                        atomicAdd(&ph[warp * 256 + ((key >> shift) & 255u)], fixq(p));
                 }
-            }
-            __syncthreads();
-            const int nk = s_cnt;
-            const int cap = pow2_ceil(nk < 2 ? 2 : nk);
-            for (int i = nk + tid; i < cap; i += kST) keys[i] = 0ull;
-            __syncthreads();
-            for (int size = 2; size <= cap; size <<= 1) {
-                for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                    for (int i = tid; i < (cap >> 1); i += kST) {
-                        const int lo = 2 * stride * (i / stride) + (i % stride);
-                        const int hi = lo + stride;
-                        const bool desc = (lo & size) == 0;
-                        const unsigned long long x = keys[lo], y = keys[hi];
-                        if (desc ? (x < y) : (x > y)) { keys[lo] = y; keys[hi] = x; }
-                    }
-                    __syncthreads();
+                __syncthreads();
+                for (int bn = tid; bn < 256; bn += nt) {
+                    unsigned long long t = 0ull;
+                    for (int w = 0; w < nw; ++w) t += ph[w * 256 + bn];
+                    ss.mass[bn] = t;
                 }
+                __syncthreads();
+                if (tid < 32) {
+                    unsigned long long rem_out = 0ull;
+                    select_digit<unsigned long long>(ss.mass, ss.rem, shift, ss.sel, &rem_out);
+                    const unsigned any = __ballot_sync(0xffffffffu, rem_out != 0ull);
+                    if (any && lane == __ffs(any) - 1) ss.rem = rem_out;
+                }
+                __syncthreads();
             }
-            // cumulative mass in sorted order: contiguous segment per thread
-            const int seg = (nk + kST - 1) / kST;
-            const int a0 = tid * seg, a1 = min(nk, a0 + seg);
-            float loc = 0.f;
-            for (int t = a0; t < a1; ++t) loc += pval((int)(0xFFFFFFFFu - (uint32_t)(keys[t] & 0xFFFFFFFFull)));
-            float tot;
-            float run = block_exclusive_scan(loc, s_f, &tot);
-            const float target = sp.top_p * Z;
+            tkey = ss.sel[0];
+            const unsigned long long rem = ss.rem;  // mass still needed from the elements with key == tkey
+            // ties of the crossing key in index order: contiguous segment per thread
+            const int seg = (V + nt - 1) / nt;
+            const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
+            unsigned long long loc = 0ull;
+            for (int i = a0; i < a1; ++i)
+                if (pv[i] > 0.f && ord_key(z[i]) == tkey) loc += fixq(pv[i]);
+            unsigned long long tot;
+            unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &tot);
             int c = 0x7fffffff;
-            for (int t = a0; t < a1; ++t) {
-                run += pval((int)(0xFFFFFFFFu - (uint32_t)(keys[t] & 0xFFFFFFFFull)));
-                if (run >= target) { c = t; break; }
+            for (int i = a0; i < a1; ++i) {
+                if (!(pv[i] > 0.f && ord_key(z[i]) == tkey)) continue;
+                run += fixq(pv[i]);
+                if (run >= rem) { c = i; break; }
             }
-            c = block_min_i(c, s_i);
-            if (c == 0x7fffffff) c = nk - 1;
-            cut = keys[c];
-            use_cut = true;
-            __syncthreads();
+            tidx = block_min_i(c, ss.i);
+            cut = true;
         }
 
-        // ---- draw in vocabulary order over the kept set
+        // ---- draw in vocabulary order over the kept set (exact fixed-point prefix sums)
         auto kept = [&](int i) {
+            if (!(pv[i] > 0.f)) return false;
+            if (!cut) return true;
             const uint32_t key = ord_key(z[i]);
-            if (key < thr) return false;
-            if (!use_cut) return true;
-            const unsigned long long ck = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
-            return ck >= cut;
+            return key > tkey || (key == tkey && i <= tidx);
         };
-        const int seg = (V + kST - 1) / kST;
-        const int v0 = tid * seg, v1 = min(V, v0 + seg);
-        float loc = 0.f;
+        const int seg = (V + nt - 1) / nt;
+        const int v0 = min(V, tid * seg), v1 = min(V, v0 + seg);
+        unsigned long long loc = 0ull;
         for (int i = v0; i < v1; ++i)
-            if (kept(i)) loc += pval(i);
-        float ZS;
-        float run = block_exclusive_scan(loc, s_f, &ZS);
-        const float target = (*u_ptr) * ZS;
+            if (kept(i)) loc += fixq(pv[i]);
+        unsigned long long ZS;
+        unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &ZS);
+        const unsigned long long target = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
         int cand = 0x7fffffff;
         for (int i = v0; i < v1; ++i) {
             if (!kept(i)) continue;
-            run += pval(i);
+            run += fixq(pv[i]);
             if (run > target) { cand = i; break; }
         }
-        cand = block_min_i(cand, s_i);
-        if (cand == 0x7fffffff) {
-            // u * ZS at or beyond the rounded total: the last kept index
-            int lk = -1;
-            for (int i = v0; i < v1; ++i)
-                if (kept(i)) lk = i;
-            cand = block_max_i(lk, s_i);
-        }
-        tok = cand;
+        tok = block_min_i(cand, ss.i);
     }
     if (tok < 0 || tok >= V) {
         if (tid == 0 && err) atomicExch(err, 2);
@@ -322,12 +312,34 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
     return tok;
 }
 
+// As sample_smem, loading the logits lg[0..V) first (through L2: they may
+// have been written by other CTAs of the same kernel).
+static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
+                                   unsigned char* smraw, SampleScratch& ss, int* err) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    float* z = reinterpret_cast<float*>(smraw);
+    for (int i0 = 0; i0 < V; i0 += 8 * nt) {
+        float r[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + j * nt + tid;
+            r[j] = i < V ? __ldcg(lg + i) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + j * nt + tid;
+            if (i < V) z[i] = r[j];
+        }
+    }
+    __syncthreads();
+    return sample_smem(V, sp, u_ptr, smraw, ss, err);
+}
+
 }  // namespace sample_detail
 
-inline size_t sample_smem_bytes_dev(int V) {
-    int c = 1;
-    while (c < V) c <<= 1;
-    return sizeof(unsigned long long) * (size_t)c + 2 * sizeof(float) * (size_t)V;
+// shared memory of sample_smem / sample_block for V logits and `threads` threads
+inline size_t sample_smem_bytes_dev(int V, int threads) {
+    return sample_detail::sample_hist_offset(V) + (size_t)(threads / 32) * 256 * sizeof(unsigned long long);
 }
 
 }  // namespace sd

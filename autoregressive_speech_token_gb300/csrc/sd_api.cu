@@ -101,6 +101,7 @@ struct sd_ctx {
     float* logits = nullptr;            // [B][V] or [B][16][Vmax]
     int logits_ld = 0, vmax = 0;
     float* ebuf = nullptr;              // [B][d] code-embedding staging (Qwen)
+    float* nrm = nullptr;               // [B][max width] normalised rows (B > 2)
     int32_t* prompt = nullptr;          // [B][max_ctx]
 
     DevState* ds = nullptr;             // device
@@ -121,7 +122,6 @@ struct sd_ctx {
     StepArgs step;
     std::string trace_path;             // SD_TRACE: per-phase timings of the persistent step
     StepLayer* step_layers = nullptr;   // device [n_layer]
-    unsigned* bar = nullptr;
     int step_grid = 0;
 };
 
@@ -217,9 +217,30 @@ int alloc_stack(sd_ctx* c, DStack& s) {
 
 // ------------------------------------------------------------------ enqueue helpers
 
+// y = W x for the context's rows: the streaming GEMV for 1-2 rows; for more
+// rows (G rollouts) the norm prologue as its own kernel and the tensor-core
+// GEMM with the same epilogue.
 int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
-    cudaError_t e = launch_gemv(a, c->sm_count, st);
-    c->count_launch++;
+    cudaError_t e;
+    if (a.nb <= 2) {
+        e = launch_gemv(a, c->sm_count, st);
+        c->count_launch++;
+    } else {
+        const float* x = a.x;
+        int ldx = a.x_stride;
+        if (a.pro != PRO_NONE) {
+            e = launch_rownorm(a.x, a.x_stride, a.nb, a.W.cols, a.pro == PRO_LN, a.ng, a.nbias, a.eps, c->nrm, st);
+            c->count_launch++;
+            if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "row norm launch: %s", cudaGetErrorString(e));
+            x = c->nrm;
+            ldx = a.W.cols;
+        }
+        QGemmArgs g;
+        g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
+        g.y = a.y; g.ldy = a.y_stride;
+        e = launch_qgemm(g, st);
+        c->count_launch++;
+    }
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
     return SD_OK;
 }
@@ -349,13 +370,13 @@ int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
     return SD_OK;
 }
 
-// One persistent step: zero the barrier counter, launch the cooperative kernel.
+// One cooperative launch of the persistent step kernel for n_steps steps.
 int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
     StepArgs a = c->step;
     a.n_steps = n_steps;
     a.u_seq = u_seq;
     a.out_seq = out_seq;
-    CK(cudaMemsetAsync(c->bar, 0, sizeof(unsigned), st));
+    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 24, st));
     cudaError_t e = launch_step(a, c->step_grid, st);
     c->count_launch++;
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
@@ -382,7 +403,7 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
             return rc;
         for (int l = 0; l < s.n_layer; ++l) {
             DLayer& L = s.L[l];
-            if ((rc = ck(launch_rownorm(c->pf_x, M, d, s.gpt2, L.n1g, L.n1b, s.eps, c->pf_h, st), "norm"))) return rc;
+            if ((rc = ck(launch_rownorm(c->pf_x, d, M, d, s.gpt2, L.n1g, L.n1b, s.eps, c->pf_h, st), "norm"))) return rc;
             QGemmArgs g;
             g.W = L.wqkv; g.M = M; g.x = c->pf_h; g.ldx = d; g.epi = EPI_LINEAR; g.bias = L.bqkv;
             g.y = c->pf_qkv; g.ldy = qr;
@@ -397,7 +418,7 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
             o.W = L.wo; o.M = M; o.x = c->pf_o; o.ldx = qd; o.epi = EPI_LINEAR; o.bias = L.bo;
             o.resid = c->pf_x; o.y = c->pf_x; o.ldy = d;
             if ((rc = ck(launch_qgemm(o, st), "o gemm"))) return rc;
-            if ((rc = ck(launch_rownorm(c->pf_x, M, d, s.gpt2, L.n2g, L.n2b, s.eps, c->pf_h, st), "norm"))) return rc;
+            if ((rc = ck(launch_rownorm(c->pf_x, d, M, d, s.gpt2, L.n2g, L.n2b, s.eps, c->pf_h, st), "norm"))) return rc;
             QGemmArgs f;
             f.W = L.wfc; f.M = M; f.x = c->pf_h; f.ldx = d; f.epi = s.gpt2 ? EPI_GELU : EPI_SWIGLU; f.bias = L.bfc;
             f.y = c->pf_u; f.ldy = s.ff;
@@ -584,8 +605,6 @@ int setup_persistent(sd_ctx* c) {
     const sd_model_config& m = c->cfg;
     c->persistent = false;
     if (!persistent_wanted() || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
-    if (m.d_model % 256 || m.d_ff % 256 || (m.n_head * m.head_dim) % 256 || m.d_model > 8192 || m.d_ff > 8192)
-        return SD_OK;
     DStack& s = c->main;
     std::vector<StepLayer> L(s.n_layer);
     for (int l = 0; l < s.n_layer; ++l) {
@@ -594,79 +613,60 @@ int setup_persistent(sd_ctx* c) {
         L[l].n2g = D.n2g; L[l].n2b = D.n2b; L[l].bfc = D.bfc; L[l].bproj = D.bproj;
         L[l].wqkv = D.wqkv; L[l].wo = D.wo; L[l].wfc = D.wfc; L[l].wproj = D.wproj;
     }
-    int rc;
-    if ((rc = dalloc(c, &c->step_layers, sizeof(StepLayer) * std::max(1, s.n_layer)))) return rc;
-    if (s.n_layer) CK(cudaMemcpy(c->step_layers, L.data(), sizeof(StepLayer) * s.n_layer, cudaMemcpyHostToDevice));
-    if ((rc = dalloc(c, &c->bar, 256))) return rc;
     StepArgs& a = c->step;
     a.gpt2 = s.gpt2 ? 1 : 0; a.n_layer = s.n_layer; a.d = s.d; a.H = s.H; a.Hkv = s.Hkv; a.hd = s.hd; a.ff = s.ff;
-    a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.nsplit = s.nsplit; a.quant = m.quant; a.eps = s.eps;
-    a.layers = c->step_layers; a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
+    a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.quant = m.quant; a.eps = s.eps;
+    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
     a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.kc = s.kc; a.vc = s.vc;
-    a.x = s.x; a.qkv = s.qkv; a.o = s.o; a.u = s.u; a.logits = c->logits; a.part = s.part; a.counters = s.counters;
+    a.logits = c->logits;
     a.pos = &c->ds->pos; a.tok = c->ds->tok; a.u1 = c->ds->u1; a.sp = &c->ds->samp[0]; a.err = &c->ds->err;
-    a.bar = c->bar;
+    if (const char* sl = getenv("SD_SPLIT_LEN")) a.split_len = std::max(16, atoi(sl));
+    c->step_grid = step_plan_grid(a, c->sm_count);
+    cudaGetLastError();
+    if (c->step_grid <= 0) return SD_OK;
+    int rc;
+    if ((rc = dalloc(c, &c->step_layers, sizeof(StepLayer) * s.n_layer))) return rc;
+    CK(cudaMemcpy(c->step_layers, L.data(), sizeof(StepLayer) * s.n_layer, cudaMemcpyHostToDevice));
+    a.layers = c->step_layers;
+    // exchange words start at epoch 0, which no step uses
+    const int B = c->B, qkv_rows = s.qkv_rows();
+    const size_t W = sizeof(unsigned long long);
+    if ((rc = dalloc(c, &a.ll_xa, W * B * s.d)) || (rc = dalloc(c, &a.ll_xb, W * B * s.d)) ||
+        (rc = dalloc(c, &a.ll_qkv, W * B * qkv_rows)) ||
+        (rc = dalloc(c, &a.ll_part, W * B * s.H * a.max_split * (s.hd + 2))) ||
+        (rc = dalloc(c, &a.ll_u, W * B * s.ff)) || (rc = dalloc(c, &a.ll_logits, W * B * m.vocab)) ||
+        (rc = dalloc(c, &a.ll_tok, W * B)) || (rc = dalloc(c, &a.gen, 256)))
+        return rc;
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
-    a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per barrier wait
-    if (step_smem_bytes(a) > 220 * 1024) return SD_OK;
-    c->step_grid = step_max_grid(a, c->sm_count);
-    cudaGetLastError();
-    // per-CTA slices must fit the kernel's fixed shared arrays (bias slice 256, residual rows 128)
-    if (c->step_grid > 0) {
-        const int G = c->step_grid;
-        const int widest = std::max(std::max(s.qkv_rows(), s.gpt2 ? s.ff : 2 * s.ff), std::max(m.vocab, s.d));
-        if ((widest + G - 1) / G + 2 > 256 || (s.d + G - 1) / G > 128) c->step_grid = 0;
-    }
-    c->persistent = c->step_grid > 0;
-    if (const char* pf = getenv("SD_PREFETCH")) a.prefetch = atoi(pf);
+    a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
-        a.trace_cap = (1 + 5 * s.n_layer + 2) * 512;  // up to 512 steps per launch
-        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * (4 * (size_t)a.trace_cap + 8)))) return rc;
+        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 24))) return rc;
     }
+    c->persistent = true;
     return SD_OK;
 }
 
-// Per-phase mean durations of the last persistent launch, appended to SD_TRACE:
-// for each phase kind the mean time from the previous barrier to the end of
-// staging, of compute, of the next phase's preloads, and through the barrier.
+// Per-phase times of CTA 0 over the last persistent launch, appended to
+// SD_TRACE: for each phase kind the mean wait for its inputs and the mean work.
 void write_trace(sd_ctx* c, int n_steps) {
     if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
-    const int L = c->step.n_layer, per = 1 + 5 * L + 2;
-    const int n = std::min(n_steps * per, c->step.trace_cap);
-    std::vector<unsigned long long> t(4 * (size_t)c->step.trace_cap + 8);
-    if (cudaMemcpy(t.data(), c->step.trace, sizeof(unsigned long long) * t.size(), cudaMemcpyDeviceToHost) !=
-        cudaSuccess)
-        return;
-    const char* names[8] = {"embed", "qkv", "attn", "o", "fc", "proj", "head", "sample"};
-    double acc[8][4] = {{0}}, cnt[8] = {0};
-    unsigned long long prev = t[4 * (size_t)c->step.trace_cap];
-    for (int i = 0; i < n; ++i) {
-        const int k = i % per;
-        const int kind = k == 0 ? 0 : (k <= 5 * L ? 1 + (k - 1) % 5 : (k == 5 * L + 1 ? 6 : 7));
-        const unsigned long long* e = &t[4 * (size_t)i];
-        const bool fine = e[0] >= prev && e[1] >= e[0] && e[2] >= e[1];
-        acc[kind][0] += fine ? (double)(e[0] - prev) : 0;
-        acc[kind][1] += fine ? (double)(e[1] - e[0]) : 0;
-        acc[kind][2] += fine ? (double)(e[2] - e[1]) : (double)(e[2] - prev);
-        acc[kind][3] += (double)(e[3] - e[2]);
-        cnt[kind] += 1;
-        prev = e[3];
-    }
+    unsigned long long t[24];
+    if (cudaMemcpy(t, c->step.trace, sizeof t, cudaMemcpyDeviceToHost) != cudaSuccess) return;
     FILE* f = fopen(c->trace_path.c_str(), "a");
     if (!f) return;
-    fprintf(f, "steps=%d us_per_step=%.2f prefetch=%d | phase: stage/compute/preload/barrier us\n", n / per,
-            (double)(t[4 * (size_t)(n - 1) + 3] - t[4 * (size_t)c->step.trace_cap]) / 1e3 / (n / per), c->step.prefetch);
+    const char* names[8] = {"embed", "qkv", "attn", "o", "fc", "proj", "head", "sample"};
+    const double per[8] = {1.0, (double)c->step.n_layer, (double)c->step.n_layer, (double)c->step.n_layer,
+                           (double)c->step.n_layer, (double)c->step.n_layer, 1.0, 1.0};
+    double tot = 0;
+    for (int k = 0; k < 24; ++k) tot += (double)t[k];
+    fprintf(f, "steps=%d grid=%d ring=%d act=%d max_split=%d | CTA 0 per step %.2f us | phase: input wait / "
+               "weight wait / rest us\n",
+            n_steps, c->step_grid, c->step.ring_bytes, c->step.act_bytes, c->step.max_split, tot / 1e3 / n_steps);
     for (int k = 0; k < 8; ++k)
-        if (cnt[k])
-            fprintf(f, "  %-6s %.3f %.3f %.3f %.3f\n", names[k], acc[k][0] / cnt[k] / 1e3, acc[k][1] / cnt[k] / 1e3,
-                    acc[k][2] / cnt[k] / 1e3, acc[k][3] / cnt[k] / 1e3);
-    // inner stamps of one FC phase (step 0, layer 1, CTA 0): registers, FMA, warp sums, sync, epilogue, sync
-    const unsigned long long* in = &t[4 * (size_t)c->step.trace_cap + 1];
-    fprintf(f, "  fc-inner:");
-    for (int k = 1; k < 6; ++k) fprintf(f, " %.3f", in[k] > in[k - 1] ? (double)(in[k] - in[k - 1]) / 1e3 : -1.0);
-    fprintf(f, "\n");
+        fprintf(f, "  %-6s %8.3f %8.3f %8.3f\n", names[k], (double)t[3 * k] / 1e3 / n_steps / per[k],
+                (double)t[3 * k + 1] / 1e3 / n_steps / per[k], (double)t[3 * k + 2] / 1e3 / n_steps / per[k]);
     fclose(f);
 }
 
@@ -731,8 +731,6 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     if (!cfg || !out) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_create: NULL argument");
     *out = nullptr;
     if (!validate_cfg(*cfg)) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_create: invalid model config");
-    if (cfg->batch > 2)
-        return fail(nullptr, SD_ERR_UNSUPPORTED, "sd_create: batch %d > 2 is not implemented by the GEMV path", cfg->batch);
     c = new sd_ctx();
     c->cfg = *cfg;
     c->device = device;
@@ -767,6 +765,8 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
         c->logits_ld = m.vocab;
     }
     if ((rc = dalloc(c, &c->logits, sizeof(float) * c->B * c->logits_ld))) return bail(rc);
+    if ((rc = dalloc(c, &c->nrm, sizeof(float) * c->B * std::max(m.d_model, m.arch == SD_ARCH_QWEN_TTS ? m.cp_d_model : 0))))
+        return bail(rc);
     if ((rc = dalloc(c, &c->prompt, sizeof(int32_t) * c->B * m.max_ctx))) return bail(rc);
     {
         // GEMM prefill: SD_PREFILL=steps runs the prompt through the per-position step graphs instead
@@ -833,7 +833,8 @@ int sd_load_weights(sd_ctx* c, const void* blob, size_t nbytes, int blob_on_devi
     size_t total = 0;
     int rc = load_all(c, b, nullptr, &total);
     if (!rc) {
-        cudaError_t e = cudaMalloc(&c->weights, total);
+        // + 256: the persistent step copies scale and bias windows widened to 16 bytes
+        cudaError_t e = cudaMalloc(&c->weights, total + 256);
         if (e != cudaSuccess) rc = fail(c, SD_ERR_OOM, "weight arena cudaMalloc(%zu) failed", total);
     }
     if (!rc) rc = load_all(c, b, c->weights, nullptr);

@@ -176,31 +176,42 @@ struct StepLayer {
     QMat wqkv, wo, wfc, wproj;
 };
 struct StepArgs {
-    int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, nsplit = 1, quant = 0;
+    int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, quant = 0;
     float eps = 1e-5f;
-    const StepLayer* layers = nullptr;  // device array [n_layer]
+    const StepLayer* layers = nullptr;   // device array [n_layer]
     QMat head;
     const float *nfg = nullptr, *nfb = nullptr, *wte = nullptr, *wpe = nullptr;
     const float *rope_cos = nullptr, *rope_sin = nullptr;
     __half *kc = nullptr, *vc = nullptr;
-    float *x = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr, *logits = nullptr, *part = nullptr;
-    int* counters = nullptr;
-    int* pos = nullptr;                  // incremented once per step
+    // flag-carrying exchange buffers: one 64-bit word per value, (epoch << 32) | float bits
+    unsigned long long *ll_xa = nullptr;    // [B][d]   residual stream after the O projection
+    unsigned long long *ll_xb = nullptr;    // [B][d]   residual stream after the down projection
+    unsigned long long *ll_qkv = nullptr;   // [B][qkv_rows]
+    unsigned long long *ll_part = nullptr;  // [B][H][max_split][hd + 2] attention partials (o, m, l)
+    unsigned long long *ll_u = nullptr;     // [B][ff]  FFN activations
+    unsigned long long *ll_logits = nullptr;// [B][V]
+    unsigned long long *ll_tok = nullptr;   // [B]      sampled token (as float bits)
+    unsigned* gen = nullptr;             // epoch generation: steps run by earlier launches
+    float* logits = nullptr;             // [B][V] plain copy of the last step's logits
+    int* pos = nullptr;                  // advanced by n_steps at the end
     int32_t* tok = nullptr;              // [B] input token, overwritten with the sampled one
     const float* u1 = nullptr;           // [B] draws when u_seq is null
     const float* u_seq = nullptr;        // [n_steps][B] draws, or null
     int32_t* out_seq = nullptr;          // [n_steps][B] sampled tokens, or null
     const SampParams* sp = nullptr;
     int* err = nullptr;
-    unsigned* bar = nullptr;             // grid-barrier counter, zero at launch
     int n_steps = 1;
-    long long spin_budget = 0;           // clock64 cycles per barrier wait
-    unsigned long long* trace = nullptr; // optional: %globaltimer stamps of CTA 0, 4 per barrier
-    int trace_cap = 0;                   // barriers covered by `trace`
-    int prefetch = 1;                    // layers of weights bulk-prefetched into L2 ahead (0: none)
+    long long spin_budget = 0;           // clock64 cycles per wait
+    int ring_bytes = 0;                  // shared-memory weight ring
+    int act_bytes = 0;                   // shared-memory activation / attention / sampler region
+    int max_split = 1;                   // attention splits per (row, kv head) at most
+    int split_len = 128;                 // cached positions per attention split (before the cap)
+    unsigned long long* trace = nullptr; // optional [24]: CTA 0 per phase kind: input wait, weight wait, rest (ns)
 };
 size_t step_smem_bytes(const StepArgs& a);
-int step_max_grid(const StepArgs& a, int sm_count);
+// grid size the persistent step runs with (0: the configuration does not fit)
+// fills a.ring_bytes, a.act_bytes and a.max_split as planned
+int step_plan_grid(StepArgs& a, int sm_count);
 cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
 
 // Tensor-core GEMM Y[M][N] = X[M][K] W[N][K]^T over a repacked weight, with
@@ -222,8 +233,8 @@ cudaError_t launch_qgemm(const QGemmArgs& a, cudaStream_t st);
 // m = b*np + i for position p0 + i.
 cudaError_t launch_embed_rows(const float* table, const float* pos_table, const int32_t* tok, int ld, int B, int p0,
                               int np, int d, int V, float* X, int* err, cudaStream_t st);
-cudaError_t launch_rownorm(const float* X, int M, int d, int ln, const float* g, const float* b, float eps, float* H,
-                           cudaStream_t st);
+cudaError_t launch_rownorm(const float* X, int ldx, int M, int d, int ln, const float* g, const float* b, float eps,
+                           float* H, cudaStream_t st);
 cudaError_t launch_rope_kv(float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx, int row_heads,
                            int head_off, const float* cs, const float* sn, __half* kc, __half* vc, cudaStream_t st);
 cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx,

@@ -204,9 +204,12 @@ def test_one_token_prompt(sd, prefill_path):
     _check_t3(sd, run, 3, prompt=np.array([[17]], np.int32))
 
 
-def test_persistent_kernel_is_used(sd, monkeypatch):
+@pytest.mark.parametrize("name", ["tiny", "gpt2m_q4", "gpt2m_q8", "llama_q4"])
+def test_persistent_kernel_is_used(sd, monkeypatch, name):
+    """The persistent step's plan accepts every GPT-2 / Llama workload (so the
+    persistent-path tests above do run the persistent kernel)."""
     monkeypatch.setenv("SD_PERSISTENT", "1")
-    run = get_preset("tiny")
+    run = get_preset(name)
     dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
     assert dec.info().persistent > 0 and dec.info().kernels_per_step == 1
     dec.close()
@@ -304,3 +307,30 @@ def test_qwen_small(sd, prefill_path):
 def test_qwen_full_size(sd):
     run = get_preset("qwen_a8")
     _check_qwen(sd, run.model, prompt_tokens(run), 2, run.sampler)
+
+
+def test_qwen_g16_small(sd, prefill_path):
+    """Sixteen rollout rows (the G=16 configuration's batch) through the
+    norm-kernel + tensor-core GEMM path that replaces the 1-2 row GEMV."""
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=16, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
+    prompt = np.random.default_rng(4).integers(0, 300, size=(16, 12)).astype(np.int32)
+    _check_qwen(sd, spec, prompt, 3, SamplerSpec(0.9, 50, 0.95, False))
+
+
+def test_qwen_g16_full_size(sd):
+    """The G=16 configuration's model at full size, one shared prompt (short,
+    so that the oracle finishes), one frame after the prompt frame."""
+    run = get_preset("qwen_a8_g16")
+    prompt = np.repeat(np.random.default_rng(6).integers(0, 3072, size=(1, 6)).astype(np.int32), 16, axis=0)
+    _check_qwen(sd, run.model, prompt, 1, run.sampler)
+
+
+def test_gpt2_four_rows(sd):
+    """Rows beyond two on the GPT-2 path (norm kernel + GEMM per matrix)."""
+    run = get_preset("tiny").with_model(batch=4)
+    prompt = np.random.default_rng(8).integers(0, 6561, size=(4, 20)).astype(np.int32)
+    _check_t3(sd, run, 10, prompt=prompt)
+
