@@ -65,7 +65,8 @@ def test_bad_configs_rejected_before_any_device_call(lib):
     cfg.quant = 9
     assert lib.sd_create(C.byref(cfg), 0, None, C.byref(h)) == -1
     cfg = sdm.ModelConfig.from_spec(get_preset("qwen_a8_g16").model)
-    assert lib.sd_create(C.byref(cfg), 0, None, C.byref(h)) == -7   # batch 16: not in the GEMV path yet
+    cfg.batch = 17                                                   # more rows than SD_MAX_ROWS
+    assert lib.sd_create(C.byref(cfg), 0, None, C.byref(h)) == -1
 
 
 def test_config_struct_matches_blob_echo():
