@@ -656,13 +656,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             }
             tr_waited();
             {
+                // sub-phase stamps of the QKV phase (CTA 0): slice, record wait, norm, matvec, publish
+                unsigned long long ts = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
+                auto sub = [&](int k) {
+                    if (a.trace && cta == 0 && tid == 0) {
+                        const unsigned long long t = gtime();
+                        a.trace[24 + k] += t - ts;
+                        ts = t;
+                    }
+                };
                 const Slice sl = make_slice(a, tab, 4 * l, cta, G);
+                sub(0);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
+                sub(1);
                 norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
                               reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                sub(2);
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+                sub(3);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
                 for (int t = tid; t < nr * NB; t += kThreads) {
                     const int i = t / NB, b = t - i * NB;
@@ -671,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     ll_store(a.ll_qkv + (size_t)b * qkv_rows + sl.r0 + i, v, e);
                 }
                 done_rec();
+                sub(4);
             }
             tr_end(PK_QKV);
             // ---- attention items

@@ -12,6 +12,7 @@
 // the device and covers only [0, pos] ("Every Frame Is a Memory Read",
 // section 5.3: attending over the whole fixed capacity is a loss).
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdarg>
 #include <cstddef>
@@ -112,6 +113,13 @@ struct sd_ctx {
     bool gemm_prefill = true;
     int pf_chunk = 0;                   // positions per chunk
     float *pf_x = nullptr, *pf_h = nullptr, *pf_qkv = nullptr, *pf_o = nullptr, *pf_u = nullptr;
+    // tensor-core (tcgen05) prefill: per layer the four matrices dequantised to fp16 hi/lo with their
+    // tensor maps, and the split activations ([rows][K] fp16 hi/lo, maps for K = d, q width, ffn width)
+    bool tc_prefill = false;
+    long long spin_budget = 0;                      // clock64 cycles a device wait may take (200 ms)
+    std::vector<std::array<CUtensorMap, 8>> tc_w;   // [layer]: qkv hi/lo, o hi/lo, fc hi/lo, proj hi/lo
+    __half *pf_xh = nullptr, *pf_xl = nullptr;
+    CUtensorMap tc_x[3][2];                         // [d | qd | ff][hi | lo]
 
     cudaGraphExec_t g_step = nullptr, g_body = nullptr, g_frame = nullptr, g_prompt_last = nullptr;
     int kernels_per_step = 0;
@@ -376,7 +384,7 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     a.n_steps = n_steps;
     a.u_seq = u_seq;
     a.out_seq = out_seq;
-    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 24, st));
+    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 32, st));
     cudaError_t e = launch_step(a, c->step_grid, st);
     c->count_launch++;
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
@@ -395,6 +403,19 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
     auto ck = [&](cudaError_t e, const char* what) {
         return e == cudaSuccess ? SD_OK : fail(c, SD_ERR_CUDA, "prefill %s: %s", what, cudaGetErrorString(e));
     };
+    // one GEMM: tcgen05 (split the activations, then the tensor-core kernel) or mma.sync
+    auto gemm = [&](const QGemmArgs& g, int l, int which, int kslot) -> cudaError_t {
+        if (!c->tc_prefill) return launch_qgemm(g, st);
+        cudaError_t e = launch_split_rows(g.x, g.ldx, g.M, g.W.cols, c->pf_xh, c->pf_xl, st);
+        if (e != cudaSuccess) return e;
+        TcGemmArgs t;
+        t.xh = c->tc_x[kslot][0]; t.xl = c->tc_x[kslot][1];
+        t.wh = c->tc_w[l][2 * which]; t.wl = c->tc_w[l][2 * which + 1];
+        t.M = g.M; t.N = g.W.rows; t.K = g.W.cols; t.epi = g.epi; t.bias = g.bias; t.resid = g.resid;
+        t.y = g.y; t.ldy = g.ldy; t.err = &c->ds->err; t.spin_budget = c->spin_budget;
+        c->count_launch++;
+        return launch_gemm_tc(t, st);
+    };
     int rc;
     for (int p0 = 0; p0 < n; p0 += c->pf_chunk) {
         const int np = std::min(c->pf_chunk, n - p0), M = B * np;
@@ -407,7 +428,7 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
             QGemmArgs g;
             g.W = L.wqkv; g.M = M; g.x = c->pf_h; g.ldx = d; g.epi = EPI_LINEAR; g.bias = L.bqkv;
             g.y = c->pf_qkv; g.ldy = qr;
-            if ((rc = ck(launch_qgemm(g, st), "qkv gemm"))) return rc;
+            if ((rc = ck(gemm(g, l, 0, 0), "qkv gemm"))) return rc;
             if ((rc = ck(launch_rope_kv(c->pf_qkv, qr, B, p0, np, s.H, s.Hkv, s.hd, s.n_ctx, s.n_layer * s.Hkv,
                                         l * s.Hkv, s.rope_cos, s.rope_sin, s.kc, s.vc, st), "rope/kv")))
                 return rc;
@@ -417,16 +438,16 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
             QGemmArgs o;
             o.W = L.wo; o.M = M; o.x = c->pf_o; o.ldx = qd; o.epi = EPI_LINEAR; o.bias = L.bo;
             o.resid = c->pf_x; o.y = c->pf_x; o.ldy = d;
-            if ((rc = ck(launch_qgemm(o, st), "o gemm"))) return rc;
+            if ((rc = ck(gemm(o, l, 1, 1), "o gemm"))) return rc;
             if ((rc = ck(launch_rownorm(c->pf_x, d, M, d, s.gpt2, L.n2g, L.n2b, s.eps, c->pf_h, st), "norm"))) return rc;
             QGemmArgs f;
             f.W = L.wfc; f.M = M; f.x = c->pf_h; f.ldx = d; f.epi = s.gpt2 ? EPI_GELU : EPI_SWIGLU; f.bias = L.bfc;
             f.y = c->pf_u; f.ldy = s.ff;
-            if ((rc = ck(launch_qgemm(f, st), "fc gemm"))) return rc;
+            if ((rc = ck(gemm(f, l, 2, 0), "fc gemm"))) return rc;
             QGemmArgs q;
             q.W = L.wproj; q.M = M; q.x = c->pf_u; q.ldx = s.ff; q.epi = EPI_LINEAR; q.bias = L.bproj;
             q.resid = c->pf_x; q.y = c->pf_x; q.ldy = d;
-            if ((rc = ck(launch_qgemm(q, st), "proj gemm"))) return rc;
+            if ((rc = ck(gemm(q, l, 3, 2), "proj gemm"))) return rc;
             c->count_launch += 8;
         }
         c->count_launch += 1;
@@ -595,6 +616,45 @@ constexpr size_t kStepH2D = offsetof(DevState, u) - offsetof(DevState, prompt_on
 constexpr size_t kStepD2H = offsetof(DevState, u1);
 // The persistent step is opt-in (SD_PERSISTENT=1) until it beats the
 // per-operation graph on the bench workload.
+// Tensor-core prefill: every main-stack matrix dequantised once into fp16 high
+// and low parts with its TMA tensor maps, and the split-activation buffers.
+// SD_PREFILL=mma keeps the mma.sync GEMM; a shape the kernel does not take
+// (a width not a multiple of 64) keeps it too.
+int setup_tc_prefill(sd_ctx* c) {
+    c->tc_prefill = false;
+    const char* env = getenv("SD_PREFILL");
+    if (!c->gemm_prefill || (env && strcmp(env, "mma") == 0)) return SD_OK;
+    DStack& s = c->main;
+    const int qd = s.H * s.hd;
+    if (s.d % 64 || qd % 64 || s.ff % 64) return SD_OK;
+    c->tc_w.assign(s.n_layer, std::array<CUtensorMap, 8>{});
+    int rc;
+    for (int l = 0; l < s.n_layer; ++l) {
+        const QMat* mats[4] = {&s.L[l].wqkv, &s.L[l].wo, &s.L[l].wfc, &s.L[l].wproj};
+        for (int w = 0; w < 4; ++w) {
+            const QMat& W = *mats[w];
+            const size_t n = (size_t)W.rows * W.cols;
+            __half* buf = nullptr;
+            if ((rc = dalloc(c, &buf, 2 * n * sizeof(__half)))) return rc;
+            CK(launch_dequant_split(W, buf, buf + n, c->stream));
+            if (!tc_map_fp16(&c->tc_w[l][2 * w], buf, W.rows, W.cols) ||
+                !tc_map_fp16(&c->tc_w[l][2 * w + 1], buf + n, W.rows, W.cols))
+                return fail(c, SD_ERR_CUDA, "tensor map for a prefill weight could not be encoded");
+        }
+    }
+    const int R = c->B * c->pf_chunk, kmax = std::max(std::max(s.d, qd), s.ff);
+    if ((rc = dalloc(c, &c->pf_xh, sizeof(__half) * (size_t)R * kmax)) ||
+        (rc = dalloc(c, &c->pf_xl, sizeof(__half) * (size_t)R * kmax)))
+        return rc;
+    const int ks[3] = {s.d, qd, s.ff};
+    for (int k = 0; k < 3; ++k)
+        if (!tc_map_fp16(&c->tc_x[k][0], c->pf_xh, R, ks[k]) || !tc_map_fp16(&c->tc_x[k][1], c->pf_xl, R, ks[k]))
+            return fail(c, SD_ERR_CUDA, "tensor map for the prefill activations could not be encoded");
+    CK(cudaStreamSynchronize(c->stream));
+    c->tc_prefill = true;
+    return SD_OK;
+}
+
 bool persistent_wanted() {
     const char* e = getenv("SD_PERSISTENT");
     return e && e[0] == '1';
@@ -642,7 +702,7 @@ int setup_persistent(sd_ctx* c) {
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
-        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 24))) return rc;
+        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 32))) return rc;
     }
     c->persistent = true;
     return SD_OK;
@@ -652,7 +712,7 @@ int setup_persistent(sd_ctx* c) {
 // SD_TRACE: for each phase kind the mean wait for its inputs and the mean work.
 void write_trace(sd_ctx* c, int n_steps) {
     if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
-    unsigned long long t[24];
+    unsigned long long t[32];
     if (cudaMemcpy(t, c->step.trace, sizeof t, cudaMemcpyDeviceToHost) != cudaSuccess) return;
     FILE* f = fopen(c->trace_path.c_str(), "a");
     if (!f) return;
@@ -667,6 +727,10 @@ void write_trace(sd_ctx* c, int n_steps) {
     for (int k = 0; k < 8; ++k)
         fprintf(f, "  %-6s %8.3f %8.3f %8.3f\n", names[k], (double)t[3 * k] / 1e3 / n_steps / per[k],
                 (double)t[3 * k + 1] / 1e3 / n_steps / per[k], (double)t[3 * k + 2] / 1e3 / n_steps / per[k]);
+    fprintf(f, "  qkv sub-phases us: slice %.3f record %.3f norm %.3f matvec %.3f publish %.3f\n",
+            (double)t[24] / 1e3 / n_steps / per[1], (double)t[25] / 1e3 / n_steps / per[1],
+            (double)t[26] / 1e3 / n_steps / per[1], (double)t[27] / 1e3 / n_steps / per[1],
+            (double)t[28] / 1e3 / n_steps / per[1]);
     fclose(f);
 }
 
@@ -739,6 +803,11 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     if (cudaSetDevice(device) != cudaSuccess) return bail(fail(c, SD_ERR_CUDA, "cudaSetDevice(%d) failed", device));
     if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return bail(fail(c, SD_ERR_CUDA, "device query failed"));
+    {
+        int clock_khz = 0;
+        cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, device);
+        c->spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;
+    }
     if (stream) {
         c->stream = reinterpret_cast<cudaStream_t>(stream);
     } else {
@@ -844,6 +913,7 @@ int sd_load_weights(sd_ctx* c, const void* blob, size_t nbytes, int blob_on_devi
     if (se != cudaSuccess) return fail(c, SD_ERR_CUDA, "weight repack: %s", cudaGetErrorString(se));
     c->weight_bytes = (int64_t)total;
     if ((rc = setup_persistent(c))) return rc;
+    if ((rc = setup_tc_prefill(c))) return rc;
     // graphs
     if (c->cfg.arch == SD_ARCH_QWEN_TTS) {
         if ((rc = capture(c, GraphKind::QwenFrame, &c->g_frame, &c->kernels_per_step))) return rc;
@@ -1038,6 +1108,7 @@ int sd_get_info(const sd_ctx* c, sd_info* out) {
     out->kernels_per_step = c->kernels_per_step;
     out->attn_splits = c->main.nsplit;
     out->persistent = c->persistent ? c->step_grid : 0;
+    out->prefill = !c->gemm_prefill ? 0 : (c->tc_prefill ? 2 : 1);
     out->weight_bytes = c->weight_bytes;
     out->kv_bytes = c->kv_bytes;
     out->step_h2d_bytes = (int64_t)kStepH2D;
@@ -1065,6 +1136,7 @@ struct sd_qmat {
     QMat m;
     void* buf = nullptr;
     int device = 0;
+    __half* split = nullptr;  // dequantised fp16 hi [rows][cols] then lo, made on first tensor-core use
 };
 
 int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int on_device, int device, sd_qmat** out) {
@@ -1114,6 +1186,7 @@ void sd_qmat_destroy(sd_qmat* m) {
     if (!m) return;
     cudaSetDevice(m->device);
     cudaFree(m->buf);
+    if (m->split) cudaFree(m->split);
     delete m;
 }
 
@@ -1149,6 +1222,47 @@ int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilog
     a.resid = resid_dev; a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows;
     CK(cudaSetDevice(m->device));
     CK(launch_qgemm(a, reinterpret_cast<cudaStream_t>(stream)));
+    return SD_OK;
+}
+
+int sd_qmat_gemm_tc(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                    const float* resid_dev, float* y_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!m || !x_dev || !y_dev || M < 1 || epilogue < SD_EPI_LINEAR || epilogue > SD_EPI_SWIGLU)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm_tc: bad argument");
+    if (epilogue == SD_EPI_SWIGLU && (bias_dev || m->m.rows % 2))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm_tc: SwiGLU needs even rows and no bias");
+    if (m->m.cols % 64) return fail(c, SD_ERR_UNSUPPORTED, "sd_qmat_gemm_tc: cols must be a multiple of 64");
+    CK(cudaSetDevice(m->device));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t wn = (size_t)m->m.rows * m->m.cols, xn = (size_t)M * m->m.cols;
+    if (!m->split) {
+        CK(cudaMalloc(&m->split, 2 * wn * sizeof(__half)));
+        CK(launch_dequant_split(m->m, m->split, m->split + wn, st));
+    }
+    __half* xs = nullptr;
+    int* err = nullptr;
+    CK(cudaMalloc(&xs, 2 * xn * sizeof(__half) + 256));
+    err = reinterpret_cast<int*>(reinterpret_cast<char*>(xs) + 2 * xn * sizeof(__half));
+    TcGemmArgs a;
+    bool ok = tc_map_fp16(&a.xh, xs, M, m->m.cols) && tc_map_fp16(&a.xl, xs + xn, M, m->m.cols) &&
+              tc_map_fp16(&a.wh, m->split, m->m.rows, m->m.cols) &&
+              tc_map_fp16(&a.wl, m->split + wn, m->m.rows, m->m.cols);
+    cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+    a.M = M; a.N = m->m.rows; a.K = m->m.cols; a.epi = epilogue; a.bias = bias_dev; a.resid = resid_dev;
+    a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows; a.err = err;
+    int clock_khz = 0;
+    cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, m->device);
+    a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, 4, st);
+    if (e == cudaSuccess) e = launch_split_rows(x_dev, m->m.cols, M, m->m.cols, xs, xs + xn, st);
+    if (e == cudaSuccess) e = launch_gemm_tc(a, st);
+    int herr = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(xs);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sd_qmat_gemm_tc: %s", cudaGetErrorString(e));
+    if (herr) return fail(c, SD_ERR_TIMEOUT, "sd_qmat_gemm_tc: a wait of the kernel timed out");
     return SD_OK;
 }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -206,7 +207,7 @@ struct StepArgs {
     int act_bytes = 0;                   // shared-memory activation / attention / sampler region
     int max_split = 1;                   // attention splits per (row, kv head) at most
     int split_len = 128;                 // cached positions per attention split (before the cap)
-    unsigned long long* trace = nullptr; // optional [24]: CTA 0 per phase kind: input wait, weight wait, rest (ns)
+    unsigned long long* trace = nullptr; // optional [32]: CTA 0 per phase kind: input wait, weight wait, rest (ns); [24..29) QKV sub-phases
 };
 size_t step_smem_bytes(const StepArgs& a);
 // grid size the persistent step runs with (0: the configuration does not fit)
@@ -228,6 +229,27 @@ struct QGemmArgs {
     int ldy = 0;
 };
 cudaError_t launch_qgemm(const QGemmArgs& a, cudaStream_t st);
+
+// Tensor-core (tcgen05) GEMM for prefill: fp16 hi/lo operands loaded by TMA
+// through 2-D tensor maps ([rows][K] fp16, K a multiple of 64), three MMAs per
+// K step, the QGemm epilogues.
+struct alignas(128) TcGemmArgs {
+    CUtensorMap xh, xl;          // activations [>= M][K]
+    CUtensorMap wh, wl;          // weights [N][K]
+    int M = 0, N = 0, K = 0;
+    int epi = EPI_LINEAR;
+    const float* bias = nullptr;
+    const float* resid = nullptr;
+    float* y = nullptr;
+    int ldy = 0;
+    int* err = nullptr;
+    long long spin_budget = 0;
+};
+bool tc_map_fp16(CUtensorMap* map, const void* base, int rows, int cols);
+size_t tc_smem_bytes();
+cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t st);
+cudaError_t launch_split_rows(const float* x, int ldx, int M, int K, __half* hi, __half* lo, cudaStream_t st);
+cudaError_t launch_dequant_split(const QMat& W, __half* hi, __half* lo, cudaStream_t st);
 
 // Prefill helpers: positions p0..p0+np-1 of B rows at once, activation row
 // m = b*np + i for position p0 + i.

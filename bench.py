@@ -296,8 +296,9 @@ def run_gpu(args):
         "prefill": {"ms": round(pf_ms, 3), "positions": run.prompt_len, "rows": B,
                     "gemm_gflop": round(pf_flops / 1e9, 2),
                     "gemm_tflops": round(pf_flops / (pf_ms / 1e3) / 1e12, 2),
-                    "note": "sd_prefill end to end (median of 3): positions 0..P-2 through the tensor-core "
-                            "GEMMs, the last position through the step graph"},
+                    "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill],
+                    "note": "sd_prefill end to end (median of 3): positions 0..P-2 as GEMMs over all rows, "
+                            "the last position through the step graph"},
         "gpu_launches": int(info.kernels_per_step * K),
         "clocks": clocks,
     }

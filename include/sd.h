@@ -154,7 +154,7 @@ typedef struct sd_info {
     int64_t step_h2d_bytes;    /* host->device bytes one sd_step copies (pinned staging) */
     int64_t step_d2h_bytes;    /* device->host bytes one sd_step copies back */
     int32_t persistent;        /* CTAs of the persistent step kernel (0: per-operation kernels) */
-    int32_t reserved;
+    int32_t prefill;           /* prompt path: 0 per-position step graphs, 1 mma.sync GEMMs, 2 tcgen05 GEMMs */
 } sd_info;
 int sd_get_info(const sd_ctx* ctx, sd_info* out);
 

@@ -59,6 +59,18 @@ enum { SD_EPI_LINEAR = 0, SD_EPI_GELU = 1, SD_EPI_SWIGLU = 2 };
 int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
                  const float* resid_dev, float* y_dev, void* stream);
 
+/* As sd_qmat_gemm, on the 5th-generation tensor cores (tcgen05 MMA with a
+ * tensor-memory accumulator, operands loaded by TMA), the form the prompt
+ * prefill uses.  The weights are dequantised once (kept with the matrix,
+ * device memory rows*cols*4 bytes, allocated on the first call) and, like the
+ * activations, split into fp16 high and low parts; three fp16 products per
+ * K step (hi*hi + hi*lo + lo*hi) accumulate in fp32.  cols must be a multiple
+ * of 64 (else SD_ERR_UNSUPPORTED).  Synchronises `stream` before returning;
+ * allocates and frees a scratch buffer of M*cols*4 bytes per call.  A kernel
+ * wait that runs out of its time budget returns SD_ERR_TIMEOUT. */
+int sd_qmat_gemm_tc(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                    const float* resid_dev, float* y_dev, void* stream);
+
 /* Sample one token per row from logits_dev[rows][V] with draws u_dev[rows];
  * tokens to out_dev[rows].  Sampler semantics as in sd.h.  V <= 16384. */
 int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,

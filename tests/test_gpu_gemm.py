@@ -41,7 +41,7 @@ def _silu(t):
     return t / (1.0 + np.exp(-t))
 
 
-def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed):
+def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed, tc=False):
     rng = np.random.default_rng(seed)
     w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
     canon, abias = _canon(kind, w)
@@ -55,7 +55,8 @@ def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed):
         xd = torch.from_numpy(x).cuda()
         bd = torch.from_numpy(bias).cuda() if bias is not None else None
         yd = torch.from_numpy(resid).cuda() if resid is not None else torch.empty(M, out_cols, device="cuda")
-        sd.sd_qmat_gemm(h, xd, M, epi, bd, yd if resid is not None else None, yd)
+        gemm = sd.sd_qmat_gemm_tc if tc else sd.sd_qmat_gemm
+        gemm(h, xd, M, epi, bd, yd if resid is not None else None, yd)
         torch.cuda.synchronize()
         y = yd.cpu().numpy().astype(np.float64)
     finally:
@@ -71,6 +72,10 @@ def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed):
         gsum = np.abs(x64).reshape(M, -1, 64).sum(2)
         mag = mag + 2 * gsum @ np.abs(abias.astype(np.float64)).T
     et = (2 * (cols // bk) + 64) * U * mag + 2.0 ** -25 * np.abs(deq).sum(1)
+    if tc:
+        # fp32 accumulation over K/16 steps of three products; the low fp16 parts of
+        # weights (|w - hi| < 2^-12 |w|) and activations may be subnormal: 2^-25 absolute each
+        et = (3 * (cols // 16) + 64) * U * mag + 2.0 ** -25 * (np.abs(deq).sum(1) + np.abs(x64).sum(1)[:, None])
     if bias is not None:
         t = t + bias
         et = et + 2 * U * np.abs(t)
@@ -138,3 +143,40 @@ def test_gemm_rejects_bad_arguments(sd):
                 sd.sd_qmat_gemm(h, *args)
     finally:
         sd.sd_qmat_destroy(h)
+
+
+TC_SHAPES = [(KQ8, (3072, 1024)), (KQ8, (130, 128)), (KQ4, (3072, 1024)), (KQ4, (1024, 4096)), (KQ4, (200, 64)),
+             (KA8, (4096, 2048)), (KA8, (2048, 6144)), (KA8, (130, 128))]
+
+
+@pytest.mark.parametrize("M", [1, 37, 150, 300])
+@pytest.mark.parametrize("kind,shape", TC_SHAPES)
+def test_gemm_tc_linear_bias(sd, kind, shape, M):
+    """The tcgen05 GEMM: ragged row counts (a partial 128-row tile), ragged
+    output counts (a partial 128-column tile), one K step (cols 64) up to 96."""
+    rows, cols = shape
+    _run(sd, kind, rows, cols, M, 0, True, False, rows + cols + M + kind + 7, tc=True)
+
+
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+def test_gemm_tc_epilogues(sd, kind):
+    cols = 1024 if kind != KA8 else 2048
+    _run(sd, kind, 4096, cols, 150, 1, True, False, 21 + kind, tc=True)
+    _run(sd, kind, 1024, cols, 150, 0, True, True, 22 + kind, tc=True)
+    _run(sd, kind, 8192 if kind != KA8 else 12288, cols, 200, 2, False, False, 23 + kind, tc=True)
+    _run(sd, kind, 66, 128, 16, 2, False, True, 24 + kind, tc=True)
+
+
+def test_gemm_tc_rejects_unaligned_k(sd):
+    w = (np.random.default_rng(0).standard_normal((64, 96)) * 0.02).astype(np.float32)
+    canon, _ = _canon(KQ8, w)
+    h = sd.sd_qmat_create(KQ8, canon, 64, 96)
+    try:
+        x = torch.zeros(4, 96, device="cuda")
+        y = torch.zeros(4, 64, device="cuda")
+        with pytest.raises(sd.SdError) as e:
+            sd.sd_qmat_gemm_tc(h, x, 4, 0, None, None, y)
+        assert e.value.code == -7
+    finally:
+        sd.sd_qmat_destroy(h)
+

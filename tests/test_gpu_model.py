@@ -176,11 +176,21 @@ def test_llama_q4_both_step_paths(sd, step_path):
     _check_t3(sd, get_preset("llama_q4"), 4)
 
 
-@pytest.fixture(params=["gemm", "steps"])
+@pytest.fixture(params=["tcgen05", "mma", "steps"])
 def prefill_path(request, monkeypatch):
-    """Run a test with the GEMM prefill and with the per-position step graphs."""
+    """Run a test with the tcgen05 GEMM prefill, the mma.sync GEMM prefill and
+    the per-position step graphs."""
     monkeypatch.setenv("SD_PREFILL", request.param)
     return request.param
+
+
+@pytest.mark.parametrize("name,want", [("gpt2m_q4", 2), ("llama_q4", 2), ("qwen_a8", 2), ("tiny", 2)])
+def test_prefill_uses_tensor_cores(sd, monkeypatch, name, want):
+    monkeypatch.delenv("SD_PREFILL", raising=False)
+    run = get_preset(name)
+    dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
+    assert dec.info().prefill == want
+    dec.close()
 
 
 def test_gpt2m_q4_both_prefill_paths(sd, prefill_path):
