@@ -31,7 +31,8 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// sum over the block of NB values; every thread gets the totals.
+// sum over the block of NB values; every thread gets the totals (fixed order:
+// warp sums, then warp 0 reduces the warp sums with shuffles).
 template <int NB>
 __device__ __forceinline__ void block_sum(float (&v)[NB], float* scratch) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -41,16 +42,26 @@ __device__ __forceinline__ void block_sum(float (&v)[NB], float* scratch) {
         if (lane == 0) scratch[warp * NB + b] = s;
     }
     __syncthreads();
-    if (threadIdx.x < NB) {
-        float s = 0.f;
-        for (int w = 0; w < nw; ++w) s += scratch[w * NB + threadIdx.x];
-        scratch[32 * NB + threadIdx.x] = s;
+    if (warp == 0) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float s = warp_sum(lane < nw ? scratch[lane * NB + b] : 0.f);
+            if (lane == 0) scratch[32 * NB + b] = s;
+        }
     }
     __syncthreads();
 #pragma unroll
     for (int b = 0; b < NB; ++b) v[b] = scratch[32 * NB + b];
     __syncthreads();
 }
+
+// Activation rows staged in shared memory carry 4 floats of padding after
+// every 32 elements: a lane's 32-element slice (its 16-byte weight unit) then
+// starts 36 floats after its neighbour's, so the eight 16-byte loads of a
+// quarter warp fall in distinct bank groups (unpadded, the 128-byte stride put
+// every lane of the warp on the same four banks).
+__device__ __forceinline__ int pidx(int k) { return k + ((k >> 5) << 2); }
+__host__ __device__ __forceinline__ int padded(int K) { return K + (K >> 3); }
 
 template <int QK>
 struct Unit {
@@ -147,7 +158,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
 
     __shared__ float s_scr[33 * NB];
     __shared__ float s_tot[8 * R * NB];
-    extern __shared__ float s_x[];  // [NB][K] transformed activations
+    extern __shared__ float s_x[];  // [NB][padded(K)] transformed activations (padded layout, pidx)
 
     // element index of the lane's unit u (units lie wholly inside or outside K)
     int ebase[U];
@@ -167,6 +178,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
     // ---------------------------------------------------------------- prologue
     // stage the activation rows in shared memory with 16-byte loads (one pass
     // over global memory), then normalise in place
+    const int KP = padded(K);  // padded row length in shared memory
     {
         const int K4 = K >> 2;
         const float4* xg = reinterpret_cast<const float4*>(a.x);
@@ -174,7 +186,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
 #pragma unroll 4
         for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
             const int b = i / K4, k4 = i - b * K4;
-            xs4[i] = xg[(size_t)b * (a.x_stride >> 2) + k4];
+            xs4[(b * KP >> 2) + k4 + (k4 >> 3)] = xg[(size_t)b * (a.x_stride >> 2) + k4];
         }
     }
     __syncthreads();
@@ -184,7 +196,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
         for (int b = 0; b < NB; ++b) {
             float s = 0.f;
             for (int k = threadIdx.x; k < K; k += blockDim.x) {
-                const float xv = s_x[b * K + k];
+                const float xv = s_x[b * KP + pidx(k)];
                 s += (a.pro == PRO_LN) ? xv : xv * xv;
             }
             v[b] = s;
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
             for (int b = 0; b < NB; ++b) {
                 float s = 0.f;
                 for (int k = threadIdx.x; k < K; k += blockDim.x) {
-                    const float dx = s_x[b * K + k] - mu[b];
+                    const float dx = s_x[b * KP + pidx(k)] - mu[b];
                     s = fmaf(dx, dx, s);
                 }
                 v[b] = s;
@@ -219,8 +231,9 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
         float4* xs4 = reinterpret_cast<float4*>(s_x);
         for (int i = threadIdx.x; i < NB * K4; i += blockDim.x) {
             const int b = i / K4, k4 = i - b * K4;
+            const int pi = (b * KP >> 2) + k4 + (k4 >> 3);
             const float4 g = g4[k4];
-            float4 x = xs4[i];
+            float4 x = xs4[pi];
             if (a.pro == PRO_LN) {
                 const float4 o = b4[k4];
                 x.x = fmaf((x.x - mu[b]) * rs[b], g.x, o.x);
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
                 x.z = x.z * rs[b] * g.z;
                 x.w = x.w * rs[b] * g.w;
             }
-            xs4[i] = x;
+            xs4[pi] = x;
         }
     }
     __syncthreads();
@@ -250,7 +263,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
 #pragma unroll
             for (int j = 0; j < EPU; j += 4) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * K + ebase[u] + j]);
+                if (in) v = *reinterpret_cast<const float4*>(&s_x[b * KP + pidx(ebase[u] + j)]);
                 xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
                 xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
                 s += (v.x + v.y) + (v.z + v.w);
@@ -348,7 +361,7 @@ cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
     while (WR > 1 && (a.W.rows + WR * R - 1) / (WR * R) < sm_count) WR >>= 1;
     const int tiles = (a.W.rows + WR * R - 1) / (WR * R);
     const int grid = tiles < 32 * sm_count ? tiles : 32 * sm_count;
-    const size_t smem = sizeof(float) * (size_t)NB * K;
+    const size_t smem = sizeof(float) * (size_t)NB * padded(K);
     if (smem > 32 * 1024) {  // with the static arrays the total passes the 48 KB default
         cudaError_t e = cudaFuncSetAttribute(k_gemv<QK, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
