@@ -10,11 +10,12 @@
 // (hi*hi + hi*lo + lo*hi, fp32 accumulation) give an error near 2^-22 of the
 // products, where one fp16 MMA would carry 2^-11.
 //
-// Tile: 128 rows x 128 outputs per CTA, K in steps of 64 (one 128-byte swizzled
-// row of fp16 per operand row), three stages of four operand tiles (X hi/lo,
-// W hi/lo) = 192 KB of shared memory.  Thread 0 issues the TMA loads and the
+// Tile: 128 rows x 64 outputs per CTA (more CTAs for the short prompt row
+// counts), K in steps of 64 (one 128-byte swizzled row of fp16 per operand
+// row), four stages of four operand tiles (X hi/lo 16 KB each, W hi/lo 8 KB
+// each) = 192 KB of shared memory.  Thread 0 issues the TMA loads and the
 // MMAs; the MMA completion (tcgen05.commit) frees a stage for the next load.
-// The accumulator (128 x 128 fp32) lives in tensor memory; after the last K
+// The accumulator (128 x 64 fp32) lives in tensor memory; after the last K
 // step each warp reads its 32 rows back (tcgen05.ld) for the epilogue.  Every
 // wait is bounded: on expiry the kernel records an error, waits (bounded) for
 // its own copies and MMAs, frees its tensor memory and returns.
@@ -25,9 +26,10 @@
 namespace sd {
 namespace tc_detail {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 3;
-constexpr int kTile = kBM * kBK * 2;          // 16 KB per operand tile
-constexpr int kStageBytes = 4 * kTile;        // X hi, X lo, W hi, W lo
+constexpr int kBM = 128, kBN = 64, kBK = 64, kStages = 4;
+constexpr int kTileX = kBM * kBK * 2;         // 16 KB per activation tile
+constexpr int kTileW = kBN * kBK * 2;         // 8 KB per weight tile
+constexpr int kStageBytes = 2 * kTileX + 2 * kTileW;  // X hi, X lo, W hi, W lo
 constexpr int kErrTimeout = 6;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -75,7 +77,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = N = 128.
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = 64.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 
 __device__ __forceinline__ void mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t acc) {
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ TcGe
     const int KT = a.K / kBK;
 
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(&s_tmem))
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "n"(kBN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -123,7 +126,10 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ TcGe
     const uint32_t tmem = s_tmem;
 
     if (tid == 0) {
-        auto stage_ptr = [&](int s, int which) { return smem_u32(sm + (size_t)s * kStageBytes + (size_t)which * kTile); };
+        auto stage_ptr = [&](int s, int which) {
+            const int off = which < 2 ? which * kTileX : 2 * kTileX + (which - 2) * kTileW;
+            return smem_u32(sm + (size_t)s * kStageBytes + off);
+        };
         auto issue = [&](int t) {
             const int s = t % kStages;
             const uint32_t mb = smem_u32(&s_full[s]);
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ TcGe
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kBN) : "memory");
 }
 
 // fp32 rows -> fp16 high and low parts: hi = fp16(x), lo = fp16(x - hi)
@@ -285,12 +291,12 @@ EncodeFn encoder() {
 }
 }  // namespace
 
-bool tc_map_fp16(CUtensorMap* map, const void* base, int rows, int cols) {
+bool tc_map_fp16(CUtensorMap* map, const void* base, int rows, int cols, bool weights) {
     EncodeFn enc = encoder();
     if (!enc || !base || rows < 1 || cols % tc_detail::kBK || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)tc_detail::kBK, (cuuint32_t)tc_detail::kBM};
+    const cuuint32_t box[2] = {(cuuint32_t)tc_detail::kBK, (cuuint32_t)(weights ? tc_detail::kBN : tc_detail::kBM)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -38,7 +38,7 @@ using namespace gemv_detail;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kNMB = 16;         // records in flight at most
+constexpr int kNMB = 16;         // records in flight at most (a power of two)
 constexpr int kErrTimeout = 6;
 constexpr int kMaxOwn = 64;      // residual-stream rows owned by one CTA
 constexpr int kMaxPart = 1024;   // per-slice GEMV partial sums (rows x batch rows x K slices)
@@ -68,13 +68,26 @@ __device__ __forceinline__ unsigned long long ll_load(const unsigned long long* 
     return w;
 }
 
-// Polls one word until it carries epoch e; false on timeout or a recorded error.
+// Every exchange word is written to kRep replicas (kRep x the buffer, the
+// buffer's size apart); CTA c polls replica c % kRep, so that one line is
+// polled by a quarter of the grid instead of all of it.
+constexpr int kRep = 4;
+
+__device__ __forceinline__ void ll_store_rep(unsigned long long* p, size_t stride, float v, unsigned e) {
+#pragma unroll
+    for (int r = 0; r < kRep; ++r) ll_store(p + r * stride, v, e);
+}
+
+// Polls one word until it carries epoch e; false on timeout or a recorded
+// error.  After a few polls it backs off (a short sleep between loads), which
+// frees L2 bandwidth for the producers' stores.
 __device__ __noinline__ bool ll_spin(const unsigned long long* p, unsigned e, unsigned long long* w, int* err,
                                      long long budget) {
     const long long t0 = clock64();
     for (unsigned it = 1;; ++it) {
         *w = ll_load(p);
         if ((unsigned)(*w >> 32) == e) return true;
+        if (it > 4u) __nanosleep(64);
         if ((it & 63u) == 0u) {
             if (ld_volatile(err)) return false;
             if (clock64() - t0 > budget) {
@@ -85,11 +98,13 @@ __device__ __noinline__ bool ll_spin(const unsigned long long* p, unsigned e, un
     }
 }
 
-// dst[o * n_in + i] = value of word src[o * stride + i] (epoch e), o < n_out, i < n_in.
+// dst[o * n_in + i] = value of word src[o * stride + i] (epoch e), o < n_out, i < n_in;
+// with `pad`, dst[o * padded(n_in) + pidx(i)] (the GEMV's bank-conflict-free layout).
 // Per-thread result; the caller combines it with __syncthreads_and.
 __device__ bool ll_read(const unsigned long long* src, int n_out, int stride, int n_in, unsigned e, float* dst,
-                        int* err, long long budget) {
+                        int* err, long long budget, bool pad = false) {
     const int n = n_out * n_in;
+    const int np = padded(n_in);
     bool ok = true;
     for (int i0 = threadIdx.x; i0 < n && ok; i0 += 4 * kThreads) {
         unsigned long long w[4];
@@ -104,7 +119,8 @@ __device__ bool ll_read(const unsigned long long* src, int n_out, int stride, in
         for (int j = 0; j < 4; ++j) {
             if (!p[j] || !ok) continue;
             if ((unsigned)(w[j] >> 32) != e) ok = ll_spin(p[j], e, &w[j], err, budget);
-            dst[i0 + j * kThreads] = __uint_as_float((unsigned)w[j]);
+            const int i = i0 + j * kThreads;
+            dst[pad ? (i / n_in) * np + pidx(i % n_in) : i] = __uint_as_float((unsigned)w[j]);
         }
     }
     return ok;
@@ -225,48 +241,128 @@ __device__ Slice make_slice(const StepArgs& a, const StepLayer* tab, int j, int 
     return s;
 }
 
+// Slice j of a step from the per-kind geometry computed once per launch
+// (rows, windows and record layout are the same in every layer; only the
+// pointers change).
+__device__ __forceinline__ Slice slice_at(const StepArgs& a, const StepLayer* tab, const Slice* geo, int j) {
+    const int L = a.n_layer;
+    const int kind = j < 4 * L ? (j & 3) : 4;
+    const int l = j >> 2;
+    Slice s = geo[kind];
+    const QMat* W;
+    const float *bias = nullptr, *g1 = nullptr, *g2 = nullptr;
+    if (kind == 0) { W = &tab[l].wqkv; bias = tab[l].bqkv; g1 = tab[l].n1g; g2 = tab[l].n1b; }
+    else if (kind == 1) { W = &tab[l].wo; bias = tab[l].bo; }
+    else if (kind == 2) { W = &tab[l].wfc; bias = tab[l].bfc; g1 = tab[l].n2g; g2 = tab[l].n2b; }
+    else if (kind == 3) { W = &tab[l].wproj; bias = tab[l].bproj; }
+    else { W = &a.head; g1 = a.nfg; g2 = a.nfb; }
+    s.q = W->q + (size_t)s.r0 * s.row_bytes;
+    s.s = reinterpret_cast<const uint8_t*>(W->s) + s.s_lo;
+    s.bias = (s.bias && bias) ? bias + s.b_lo : nullptr;
+    s.g1 = s.g1 ? g1 : nullptr;
+    s.g2 = s.g2 ? g2 : nullptr;
+    return s;
+}
+
 // ------------------------------------------------------------------ compute helpers
 
-// In-place LayerNorm (biased variance) or RMSNorm of x[b][0..K), b < NB.
+// In-place LayerNorm (biased variance) or RMSNorm of the padded rows
+// x[b][pidx(0..K)), b < NB.  Every warp computes the row statistics itself
+// (a full pass over the row in shared memory, conflict-free 16-byte loads,
+// xor-shuffle sums in a fixed order), so the only block barrier is the one that
+// publishes the normalised row.
 template <int NB>
-__device__ void norm_rows(float* x, int K, bool ln, const float* g, const float* gb, float eps, float* scr) {
-    float v[NB];
+__device__ void norm_rows(float* x, int K, bool ln, const float* g, const float* gb, float eps) {
+    const int KP = padded(K), lane = threadIdx.x & 31, K4 = K >> 2;
+    float mu[NB], rs[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-        float sum = 0.f;
-        for (int k = threadIdx.x; k < K; k += kThreads) {
-            const float xv = x[b * K + k];
-            sum += ln ? xv : xv * xv;
+        const float4* r4 = reinterpret_cast<const float4*>(x + b * KP);
+        float s0 = 0.f, s1 = 0.f;
+        for (int k4 = lane; k4 < K4; k4 += 32) {
+            const float4 v = r4[k4 + (k4 >> 3)];
+            if (ln) { s0 += v.x + v.y; s1 += v.z + v.w; }
+            else { s0 = fmaf(v.x, v.x, fmaf(v.y, v.y, s0)); s1 = fmaf(v.z, v.z, fmaf(v.w, v.w, s1)); }
         }
-        v[b] = sum;
-    }
-    block_sum<NB>(v, scr);
-    float mu[NB], rs[NB];
-    if (ln) {
+        float t = s0 + s1;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) mu[b] = v[b] / (float)K;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            float sum = 0.f;
-            for (int k = threadIdx.x; k < K; k += kThreads) {
-                const float dx = x[b * K + k] - mu[b];
-                sum = fmaf(dx, dx, sum);
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (ln) {
+            mu[b] = t / (float)K;
+            float q0 = 0.f, q1 = 0.f;
+            for (int k4 = lane; k4 < K4; k4 += 32) {
+                const float4 v = r4[k4 + (k4 >> 3)];
+                const float a0 = v.x - mu[b], a1 = v.y - mu[b], a2 = v.z - mu[b], a3 = v.w - mu[b];
+                q0 = fmaf(a0, a0, fmaf(a1, a1, q0));
+                q1 = fmaf(a2, a2, fmaf(a3, a3, q1));
             }
-            v[b] = sum;
+            float q = q0 + q1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+            rs[b] = 1.0f / sqrtf(q / (float)K + eps);
+        } else {
+            mu[b] = 0.f;
+            rs[b] = 1.0f / sqrtf(t / (float)K + eps);
         }
-        block_sum<NB>(v, scr);
-    } else {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) mu[b] = 0.f;
     }
-#pragma unroll
-    for (int b = 0; b < NB; ++b) rs[b] = 1.0f / sqrtf(v[b] / (float)K + eps);
-    for (int i = threadIdx.x; i < NB * K; i += kThreads) {
-        const int b = i / K, k = i - b * K;
-        const float xv = x[i];
-        x[i] = ln ? fmaf((xv - mu[b]) * rs[b], g[k], gb[k]) : xv * rs[b] * g[k];
+    // every warp holds the same statistics; all reads above precede the writes below
+    __syncthreads();
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    const float4* b4 = reinterpret_cast<const float4*>(gb);
+    for (int i = threadIdx.x; i < NB * K4; i += kThreads) {
+        const int b = i / K4, k4 = i - b * K4;
+        float4* p = reinterpret_cast<float4*>(x + b * KP) + k4 + (k4 >> 3);
+        float4 v = *p;
+        const float4 gg = g4[k4];
+        if (ln) {
+            const float4 oo = b4[k4];
+            v.x = fmaf((v.x - mu[b]) * rs[b], gg.x, oo.x);
+            v.y = fmaf((v.y - mu[b]) * rs[b], gg.y, oo.y);
+            v.z = fmaf((v.z - mu[b]) * rs[b], gg.z, oo.z);
+            v.w = fmaf((v.w - mu[b]) * rs[b], gg.w, oo.w);
+        } else {
+            v.x = v.x * rs[b] * gg.x;
+            v.y = v.y * rs[b] * gg.y;
+            v.z = v.z * rs[b] * gg.z;
+            v.w = v.w * rs[b] * gg.w;
+        }
+        *p = v;
     }
     __syncthreads();
+}
+
+// Partial dot products of one 16-byte weight unit with the lane's activations,
+// in four independent accumulators (a short dependency chain).
+__device__ __forceinline__ float dot4_q4(const uint4 w, const float* x) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = (wd[i] >> (8 * k)) & 0xFu;
+            const uint32_t hi = (wd[i] >> (8 * k + 4)) & 0xFu;
+            const float flo = __int_as_float(0x4B000000u | lo) - (kMagic + 8.0f);
+            const float fhi = __int_as_float(0x4B000000u | hi) - (kMagic + 8.0f);
+            s[k] = fmaf(flo, x[4 * i + k], s[k]);
+            s[k] = fmaf(fhi, x[16 + 4 * i + k], s[k]);
+        }
+    }
+    return (s[0] + s[1]) + (s[2] + s[3]);
+}
+
+__device__ __forceinline__ float dot4_s8(const uint4 w, const float* x) {
+    const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u = (wd[i] >> (8 * k)) & 0xFFu;
+            s[k] = fmaf(__int_as_float(0x4B000000u | u) - (kMagic + 128.0f), x[4 * i + k], s[k]);
+        }
+    }
+    return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 // y[i * NB + b] = sum_k W[r0 + i][k] x[b][k] for i < nr, with the codes and
@@ -283,6 +379,7 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
     const int kw = warp % WK, rg = warp / WK;
     const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
     const int spr = K >> 5;
+    const int KP = padded(K);  // x rows are in the padded layout
     if (rg < WR) {
         float xr[NB][32];
 #pragma unroll
@@ -294,7 +391,7 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
 #pragma unroll
                 for (int j = 0; j < EPU; j += 4) {
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (in) v = *reinterpret_cast<const float4*>(&x[b * K + e + j]);
+                    if (in) v = *reinterpret_cast<const float4*>(&x[b * KP + pidx(e + j)]);
                     xr[b][u * EPU + j] = v.x; xr[b][u * EPU + j + 1] = v.y;
                     xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
                 }
@@ -312,7 +409,7 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
                     const float dq = __half2float(reinterpret_cast<const __half*>(sc)[(size_t)i * spr + (e >> 5)]);
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float t = (QK == SD_Q4_0) ? dot_q4(w, &xr[b][0]) : dot_s8(w, &xr[b][u * EPU]);
+                        const float t = (QK == SD_Q4_0) ? dot4_q4(w, &xr[b][0]) : dot4_s8(w, &xr[b][u * EPU]);
                         acc[b] = fmaf(dq, t, acc[b]);
                     }
                 }
@@ -347,7 +444,7 @@ __device__ __forceinline__ void attn_split(const StepArgs& a, int n, int& S, int
 // the unnormalised partial o (per query head of the group) with its running
 // max m and sum l.  sm: the activation region (>= attn_smem_floats).
 __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, int chunk, int pos, unsigned e,
-                          float* sm, int* err) {
+                          float* sm, int* err, size_t rs_qkv, size_t rs_part) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hd = a.hd, half = hd >> 1, HPG = a.H / a.Hkv, n = pos + 1;
     const int qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
@@ -382,11 +479,11 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
     };
     stage(c0, min(c1, c0 + kKC));  // issued before the wait for this step's q
 
-    bool ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + (size_t)g * HPG * hd, 1, 0, HPG * hd, e, q, err,
-                      a.spin_budget);
+    const unsigned long long* src = a.ll_qkv + (size_t)(blockIdx.x & (kRep - 1)) * rs_qkv;
+    bool ok = ll_read(src + (size_t)b * qkv_rows + (size_t)g * HPG * hd, 1, 0, HPG * hd, e, q, err, a.spin_budget);
     if (last && ok) {
-        ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + qd + (size_t)g * hd, 1, 0, hd, e, kn, err, a.spin_budget);
-        if (ok) ok = ll_read(a.ll_qkv + (size_t)b * qkv_rows + qd + kd + (size_t)g * hd, 1, 0, hd, e, vn, err,
+        ok = ll_read(src + (size_t)b * qkv_rows + qd + (size_t)g * hd, 1, 0, hd, e, kn, err, a.spin_budget);
+        if (ok) ok = ll_read(src + (size_t)b * qkv_rows + qd + kd + (size_t)g * hd, 1, 0, hd, e, vn, err,
                              a.spin_budget);
     }
     if (!__syncthreads_and(ok)) return false;
@@ -493,7 +590,7 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         const int h = t / W, k = t - h * W;
         const float v = k < hd ? o[h * hd + k] : (k == hd ? mm[h] : ls[h]);
         unsigned long long* dst = a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k);
-        ll_store(dst, v, e);
+        ll_store_rep(dst, rs_part, v, e);
     }
     __syncthreads();
     return true;
@@ -509,18 +606,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
     StepLayer* tab = reinterpret_cast<StepLayer*>(sm + a.ring_bytes + a.act_bytes);
     __shared__ __align__(8) unsigned long long s_mb[kNMB];
     __shared__ long long s_rec[kNMB];  // ring position (monotonic bytes) of record i % kNMB
-    __shared__ long long s_head;       // next free ring position (thread 0)
-    __shared__ long long s_ni;         // records issued (thread 0)
+    __shared__ int s_off[kNMB];        // the same position within the ring
+    __shared__ long long s_head;       // next free ring position, monotonic (thread 0)
+    __shared__ int s_head_off;         // the same position within the ring
+    __shared__ int s_ni, s_pj;         // records issued; slice index of the next one within its step
     __shared__ float s_own[NB * kMaxOwn];
     __shared__ float s_part[kMaxPart];
     __shared__ float s_y[kMaxPart];
     __shared__ float s_red[33 * NB + 8];
     __shared__ sample_detail::SampleScratch s_samp;
+    __shared__ Slice s_geo[5];
 
     const int G = gridDim.x, cta = blockIdx.x, tid = threadIdx.x;
     const int L = a.n_layer, d = a.d, qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
     const int per_step = 4 * L + 1;
-    const long long total = (long long)a.n_steps * per_step;
+    const int total = a.n_steps * per_step;
     const int RB = a.ring_bytes;
     const long long budget = a.spin_budget;
     const bool ln = a.gpt2 != 0;
@@ -532,35 +632,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         for (int i = tid; i < words; i += kThreads)
             reinterpret_cast<int*>(tab)[i] = reinterpret_cast<const int*>(a.layers)[i];
     }
+    __syncthreads();
+    if (tid < 5) s_geo[tid] = make_slice(a, tab, tid < 4 ? tid : 4 * L, cta, G);
     if (tid == 0) {
         for (int k = 0; k < kNMB; ++k) mb_init(smem_u32(&s_mb[k]));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_head = 0;
+        s_head_off = 0;
         s_ni = 0;
+        s_pj = 0;
     }
     __syncthreads();
 
+    // replica strides (words) of the exchange buffers; this CTA reads replica `rep`
+    const size_t rs_x = (size_t)NB * d, rs_qkv = (size_t)NB * qkv_rows, rs_u = (size_t)NB * a.ff;
+    const size_t rs_part = (size_t)NB * a.H * a.max_split * (a.hd + 2), rs_lg = (size_t)NB * a.V, rs_tok = 32;
+    const int rep = cta & (kRep - 1);
     const unsigned gen0 = *reinterpret_cast<const volatile unsigned*>(a.gen);
     const int pos0 = ld_volatile(a.pos);
-    long long nc = 0;  // records consumed (uniform over the block)
+    int nc = 0;  // records consumed (uniform over the block)
 
-    // thread 0: issue the following records while the ring and the barriers have room
+    // thread 0: issue the following records while the ring and the barriers
+    // have room (ring positions tracked incrementally: no divisions)
     auto refill = [&]() {
         if (tid != 0) return;
-        long long ni = s_ni, head = s_head;
-        bool fenced = false;
+        const unsigned long long tr0 = (a.trace && cta == 0) ? gtime() : 0ull;
+        int ni = s_ni, pj = s_pj, hoff = s_head_off;
+        long long head = s_head;
         while (ni < total && ni - nc < kNMB) {
-            const Slice sl = make_slice(a, tab, (int)(ni % per_step), cta, G);
+            const Slice sl = slice_at(a, tab, s_geo, pj);
             long long start = head;
-            if ((start % RB) + sl.bytes > RB) start += RB - (start % RB);
-            if (ni > nc && start + sl.bytes - s_rec[nc % kNMB] > RB) break;
-            if (!fenced) {  // the space was last read through the generic proxy
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                fenced = true;
+            int off = hoff;
+            if (off + sl.bytes > RB) {
+                start += RB - off;
+                off = 0;
             }
-            const uint32_t dst = smem_u32(ring + (start % RB));
-            const uint32_t mb = smem_u32(&s_mb[ni % kNMB]);
-            s_rec[ni % kNMB] = start;
+            if (ni > nc && start + sl.bytes - s_rec[nc & (kNMB - 1)] > RB) break;
+            const uint32_t dst = smem_u32(ring + off);
+            const uint32_t mb = smem_u32(&s_mb[ni & (kNMB - 1)]);
+            s_rec[ni & (kNMB - 1)] = start;
+            s_off[ni & (kNMB - 1)] = off;
             mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) + (sl.g2 ? sl.n_g : 0)));
             bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
             bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
@@ -568,28 +679,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
             if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
             head = start + sl.bytes;
+            hoff = off + sl.bytes;
             ++ni;
+            if (++pj == per_step) pj = 0;
+        }
+        if (a.trace && cta == 0) {
+            a.trace[29] += gtime() - tr0;
+            a.trace[30] += (unsigned long long)(ni - s_ni);
+            a.trace[31] += 1ull;
         }
         s_ni = ni;
+        s_pj = pj;
         s_head = head;
+        s_head_off = hoff;
     };
     // trace: CTA 0 sums, per phase kind, the wait for its inputs, the wait for
     // its weight record and the rest (ns)
     unsigned long long t_a = 0, t_b = 0, t_w = 0;
     // waits for record nc (slice j of the step); returns its base in the ring
     auto wait_rec = [&](const Slice& sl, bool& ok) -> const unsigned char* {
-        refill();
+        if (tid == 0 && s_ni <= nc) refill();  // only when the record was not issued yet
         const unsigned long long tw0 = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
-        const uint32_t mb = smem_u32(&s_mb[nc % kNMB]);
+        const uint32_t mb = smem_u32(&s_mb[nc & (kNMB - 1)]);
         ok = mb_wait(mb, (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
         ok = __syncthreads_and(ok) != 0;
         if (a.trace && cta == 0 && tid == 0) t_w += gtime() - tw0;
         (void)sl;
-        return ring + (s_rec[nc % kNMB] % RB);
+        return ring + s_off[nc & (kNMB - 1)];
     };
+    // a record is consumed: its ring space is free, and thread 0 issues the
+    // following records now, while the other threads go on to the next
+    // phase's input wait
     auto done_rec = [&]() {
         __syncthreads();
         ++nc;
+        refill();
     };
     auto tr_begin = [&]() { if (a.trace && cta == 0 && tid == 0) { t_a = gtime(); t_w = 0; } };
     auto tr_waited = [&]() { if (a.trace && cta == 0 && tid == 0) t_b = gtime(); };
@@ -617,9 +741,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 for (int b = 0; b < NB; ++b) tk[b] = ld_volatile(a.tok + b);
             } else {
                 if (tid < NB) {
-                    unsigned long long w = ll_load(a.ll_tok + tid);
+                    const unsigned long long* tp = a.ll_tok + rep * rs_tok + tid;
+                    unsigned long long w = ll_load(tp);
                     const unsigned et = eb - 1u;  // layer L of the previous step
-                    if ((unsigned)(w >> 32) != et) okr = ll_spin(a.ll_tok + tid, et, &w, a.err, budget);
+                    if ((unsigned)(w >> 32) != et) okr = ll_spin(tp, et, &w, a.err, budget);
                     reinterpret_cast<int*>(s_red)[tid] = (int)(unsigned)w;
                 }
                 okr = __syncthreads_and(okr) != 0;
@@ -639,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 }
                 float v = __ldg(a.wte + (size_t)t * d + k);
                 if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + k);
-                act[i] = v;
+                act[b * padded(d) + pidx(k)] = v;
                 if (k >= o0 && k < o1) s_own[b * kMaxOwn + (k - o0)] = v;
             }
             __syncthreads();
@@ -651,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- QKV rows (norm prologue, bias)
             tr_begin();
             if (l > 0) {
-                ok = __syncthreads_and(ll_read(a.ll_xb, NB, d, d, e - 1u, act, a.err, budget)) != 0;
+                ok = __syncthreads_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, e - 1u, act, a.err, budget, true)) != 0;
                 if (!ok) break;
             }
             tr_waited();
@@ -665,13 +790,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                         ts = t;
                     }
                 };
-                const Slice sl = make_slice(a, tab, 4 * l, cta, G);
+                const Slice sl = slice_at(a, tab, s_geo, 4 * l);
                 sub(0);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
                 sub(1);
                 norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
                 sub(2);
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
@@ -681,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     const int i = t / NB, b = t - i * NB;
                     float v = s_y[t];
                     if (sl.bias) v += bias[i];
-                    ll_store(a.ll_qkv + (size_t)b * qkv_rows + sl.r0 + i, v, e);
+                    ll_store_rep(a.ll_qkv + (size_t)b * qkv_rows + sl.r0 + i, rs_qkv, v, e);
                 }
                 done_rec();
                 sub(4);
@@ -696,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 tr_waited();
                 for (int it = cta; it < items && ok; it += G) {
                     const int c = it % S, g = (it / S) % a.Hkv, b = it / (S * a.Hkv);
-                    ok = attn_item(a, l, b, g, c, S, chunk, pos, e, act, a.err);
+                    ok = attn_item(a, l, b, g, c, S, chunk, pos, e, act, a.err, rs_qkv, rs_part);
                 }
                 if (!ok) break;
             }
@@ -705,8 +830,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             tr_begin();
             {
                 const int W = a.hd + 2;
-                float* pp = act + NB * qd;  // [NB*H][S][W]
-                ok = __syncthreads_and(ll_read(a.ll_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget)) != 0;
+                float* pp = act + NB * padded(qd);  // [NB*H][S][W]
+                ok = __syncthreads_and(
+                         ll_read(a.ll_part + rep * rs_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget)) != 0;
                 if (!ok) break;
                 tr_waited();
                 for (int t = tid; t < NB * qd; t += kThreads) {
@@ -720,10 +846,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                         num = fmaf(w, P[c * W + dd], num);
                         den = fmaf(w, P[c * W + a.hd + 1], den);
                     }
-                    act[t] = num / den;  // act[b][h * hd + dd]
+                    act[(t / qd) * padded(qd) + pidx(t % qd)] = num / den;  // o[b][h * hd + dd], padded
                 }
                 __syncthreads();
-                const Slice sl = make_slice(a, tab, 4 * l + 1, cta, G);
+                const Slice sl = slice_at(a, tab, s_geo, 4 * l + 1);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
                 const int nr = sl.r1 - sl.r0;
@@ -735,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     if (sl.bias) v += bias[i];
                     v += s_own[b * kMaxOwn + i];
                     s_own[b * kMaxOwn + i] = v;
-                    ll_store(a.ll_xa + (size_t)b * d + sl.r0 + i, v, e);
+                    ll_store_rep(a.ll_xa + (size_t)b * d + sl.r0 + i, rs_x, v, e);
                 }
                 done_rec();
             }
@@ -743,14 +869,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- FC / gate-up rows (norm prologue, GELU / SwiGLU)
             tr_begin();
             {
-                ok = __syncthreads_and(ll_read(a.ll_xa, NB, d, d, e, act, a.err, budget)) != 0;
+                ok = __syncthreads_and(ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true)) != 0;
                 if (!ok) break;
                 tr_waited();
-                const Slice sl = make_slice(a, tab, 4 * l + 2, cta, G);
+                const Slice sl = slice_at(a, tab, s_geo, 4 * l + 2);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
                 norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
@@ -759,13 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                         const int i = t / NB, b = t - i * NB;
                         float v = s_y[t];
                         if (sl.bias) v += bias[i];
-                        ll_store(a.ll_u + (size_t)b * a.ff + sl.r0 + i, gelu_tanh(v), e);
+                        ll_store_rep(a.ll_u + (size_t)b * a.ff + sl.r0 + i, rs_u, gelu_tanh(v), e);
                     }
                 } else {
                     for (int t = tid; t < (nr / 2) * NB; t += kThreads) {
                         const int i = t / NB, b = t - i * NB;
                         const float gt = s_y[(2 * i) * NB + b], up = s_y[(2 * i + 1) * NB + b];
-                        ll_store(a.ll_u + (size_t)b * a.ff + sl.r0 / 2 + i, silu(gt) * up, e);
+                        ll_store_rep(a.ll_u + (size_t)b * a.ff + sl.r0 / 2 + i, rs_u, silu(gt) * up, e);
                     }
                 }
                 done_rec();
@@ -774,10 +900,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- proj / down rows (+bias +residual)
             tr_begin();
             {
-                ok = __syncthreads_and(ll_read(a.ll_u, NB, a.ff, a.ff, e, act, a.err, budget)) != 0;
+                ok = __syncthreads_and(ll_read(a.ll_u + rep * rs_u, NB, a.ff, a.ff, e, act, a.err, budget, true)) != 0;
                 if (!ok) break;
                 tr_waited();
-                const Slice sl = make_slice(a, tab, 4 * l + 3, cta, G);
+                const Slice sl = slice_at(a, tab, s_geo, 4 * l + 3);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
                 const int nr = sl.r1 - sl.r0;
@@ -789,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     if (sl.bias) v += bias[i];
                     v += s_own[b * kMaxOwn + i];
                     s_own[b * kMaxOwn + i] = v;
-                    ll_store(a.ll_xb + (size_t)b * d + sl.r0 + i, v, e);
+                    ll_store_rep(a.ll_xb + (size_t)b * d + sl.r0 + i, rs_x, v, e);
                 }
                 done_rec();
             }
@@ -800,21 +926,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         const unsigned eh = eb + (unsigned)L;
         tr_begin();
         {
-            ok = __syncthreads_and(ll_read(a.ll_xb, NB, d, d, eh - 1u, act, a.err, budget)) != 0;
+            ok = __syncthreads_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, eh - 1u, act, a.err, budget, true)) != 0;
             if (!ok) break;
             tr_waited();
-            const Slice sl = make_slice(a, tab, 4 * L, cta, G);
+            const Slice sl = slice_at(a, tab, s_geo, 4 * L);
             const unsigned char* rec = wait_rec(sl, ok);
             if (!ok) break;
             norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                          reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                          reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
             const int nr = sl.r1 - sl.r0;
             gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
             for (int t = tid; t < nr * NB; t += kThreads) {
                 const int i = t / NB, b = t - i * NB;
                 const float v = s_y[t];
                 a.logits[(size_t)b * a.V + sl.r0 + i] = v;
-                ll_store(a.ll_logits + (size_t)b * a.V + sl.r0 + i, v, eh);
+                ll_store_rep(a.ll_logits + (size_t)b * a.V + sl.r0 + i, rs_lg, v, eh);
             }
             done_rec();
         }
@@ -823,7 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         if (cta < NB) {
             tr_begin();
             float* z = act;
-            ok = __syncthreads_and(ll_read(a.ll_logits + (size_t)cta * a.V, 1, 0, a.V, eh, z, a.err, budget)) != 0;
+            ok = __syncthreads_and(
+                     ll_read(a.ll_logits + rep * rs_lg + (size_t)cta * a.V, 1, 0, a.V, eh, z, a.err, budget)) != 0;
             if (!ok) break;
             tr_waited();
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + cta : a.u1 + cta;
@@ -832,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             if (tid == 0) {
                 a.tok[cta] = tok;
                 if (a.out_seq) a.out_seq[(size_t)s * NB + cta] = tok;
-                ll_store(a.ll_tok + cta, __int_as_float(tok), eh);
+                ll_store_rep(a.ll_tok + cta, rs_tok, __int_as_float(tok), eh);
             }
             tr_end(PK_SAMPLE);
         }
@@ -847,9 +974,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
     // copies still in flight into this CTA's ring finish before it exits
     __syncthreads();
     if (tid == 0) {
-        const long long ni = s_ni;
-        for (long long i = nc; i < ni; ++i)
-            mb_wait(smem_u32(&s_mb[i % kNMB]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
+        const int ni = s_ni;
+        for (int i = nc; i < ni; ++i)
+            mb_wait(smem_u32(&s_mb[i & (kNMB - 1)]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
     }
 }
 
@@ -859,8 +986,8 @@ size_t act_region_bytes(const StepArgs& a) {
     const int qd = a.H * a.hd, HPG = a.H / a.Hkv;
     int kmax = a.d > a.ff ? a.d : a.ff;
     if (qd > kmax) kmax = qd;
-    size_t need = sizeof(float) * (size_t)a.B * kmax;
-    const size_t o_phase = sizeof(float) * ((size_t)a.B * qd + (size_t)a.B * a.H * a.max_split * (a.hd + 2));
+    size_t need = sizeof(float) * (size_t)a.B * padded(kmax);
+    const size_t o_phase = sizeof(float) * ((size_t)a.B * padded(qd) + (size_t)a.B * a.H * a.max_split * (a.hd + 2));
     // attention floats before the fp16 staging: a multiple of 4 (16 bytes) for every hd in {64, 128}
     const size_t attn_floats = (size_t)2 * HPG * a.hd + 2 * a.hd + HPG * kKC + 3 * kMaxHPG + kThreads;
     const size_t attn = sizeof(float) * attn_floats + sizeof(__half) * 2 * kKC * a.hd;

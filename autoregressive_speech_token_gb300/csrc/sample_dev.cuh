@@ -6,20 +6,23 @@
 //
 //   greedy   argmax, ties to the lowest index;
 //   top-k    4-pass 8-bit radix select of the k-th largest order-preserving
-//            logit key (counts, per-warp histograms merged in fixed order) --
+//            logit key (counts; equal digits of a warp combine by match_any
+//            into the warp's own histogram row, rows merged in fixed order) --
 //            every logit whose key is >= it survives;
-//   softmax  p_i = exp((z_i - max) / T) over the survivors (fp32), each
-//            mass also as a 2^-31 fixed-point integer so that every sum
-//            below is exact and independent of summation order;
+//   softmax  the survivors are compacted in index order with p_i =
+//            exp((z_i - max) / T) (fp32), each mass also as a 2^-31
+//            fixed-point integer so that every sum below is exact and
+//            independent of summation order;
 //   top-p    the survivors in (p desc, index asc) order are cut at the
 //            shortest prefix whose mass reaches top_p * Z: a second 4-pass
-//            radix select, on mass instead of counts, finds the key of the
-//            element where the cumulative mass crosses, and a prefix scan
-//            over its ties (index order) finds the element itself;
+//            radix select over the compacted survivors, on mass instead of
+//            counts, finds the key of the element where the cumulative mass
+//            crosses, and a prefix scan over its ties (index order) finds the
+//            element itself;
 //   draw     the smallest vocabulary index whose cumulative kept mass
 //            (index order) exceeds u times the kept total.
-// Shared memory: z[V] and p[V] (fp32), one 256-bin histogram per warp, and a
-// small fixed scratch.  No sort.
+// Shared memory: z[V], the compacted survivor indices and probabilities,
+// one 256-bin count histogram per warp, and a small fixed scratch.  No sort.
 #pragma once
 #include "sd_internal.cuh"
 
@@ -53,8 +56,8 @@ static __device__ __forceinline__ unsigned long long fixq(float p) {
     return sh >= 0 ? (unsigned long long)m << sh : (unsigned long long)(m >> (-sh));
 }
 
-// byte offset of the per-warp histograms after z[V] and p[V]
-static __host__ __device__ __forceinline__ size_t sample_hist_offset(int V) { return ((size_t)8 * V + 15) & ~(size_t)15; }
+// bytes of one [V] array of the sampler (z, survivor indices, survivor probabilities)
+static __host__ __device__ __forceinline__ size_t sample_array_bytes(int V) { return ((size_t)4 * V + 15) & ~(size_t)15; }
 
 // exclusive scan of one u64 per thread in thread order; *total = block total
 static __device__ unsigned long long block_exclusive_scan_u64(unsigned long long v, unsigned long long* s,
@@ -166,12 +169,11 @@ static __device__ __forceinline__ void select_digit(const T* w, T rem, int shift
 static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
                                   SampleScratch& ss, int* err) {
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-    float* z = reinterpret_cast<float*>(smraw);   // [V] logits
-    float* pv = z + V;                            // [V] survivor masses (0 elsewhere)
-    // [nw][256] per-warp digit histograms: counts (top-k) or fixed-point masses (top-p)
-    unsigned long long* ph = reinterpret_cast<unsigned long long*>(smraw + sample_hist_offset(V));
-    unsigned* pc = reinterpret_cast<unsigned*>(ph);
-    (void)lane;
+    const size_t arr = sample_array_bytes(V);
+    float* z = reinterpret_cast<float*>(smraw);               // [V] logits
+    int* ci = reinterpret_cast<int*>(smraw + arr);            // [V] survivor indices, ascending
+    float* cp = reinterpret_cast<float*>(smraw + 2 * arr);    // [V] survivor probabilities
+    unsigned* pc = reinterpret_cast<unsigned*>(smraw + 3 * arr);  // [nw][256] per-warp digit counts
 
     int tok;
     if (sp.greedy || sp.top_k == 1 || sp.temperature <= 0.f) {
@@ -186,19 +188,20 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
         for (int i = tid; i < V; i += nt) mloc = fmaxf(mloc, z[i]);
         const float mx = block_max_f(mloc, ss.f);
 
-        // ---- top-k: key of the k-th largest logit (counts, 4 x 8-bit digits)
+        // ---- top-k: key of the k-th largest logit (counts, 4 x 8-bit digits); each warp
+        // counts into its own histogram row, so equal digits collide only within a warp.
         const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
         uint32_t thr = 0u;
         if (k < V) {
             if (tid == 0) { ss.sel[0] = 0u; ss.sel[1] = 0u; ss.sel[2] = (uint32_t)k; }
             for (int shift = 24; shift >= 0; shift -= 8) {
-                // per-warp histograms: same-digit lanes collide only within their own warp
                 for (int i = tid; i < nw * 256; i += nt) pc[i] = 0u;
                 __syncthreads();
                 const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
+                unsigned* row = pc + warp * 256;
                 for (int i = tid; i < V; i += nt) {
                     const uint32_t key = ord_key(z[i]);
-                    if ((key & mask) == prefix) atomicAdd(&pc[warp * 256 + ((key >> shift) & 255u)], 1u);
+                    if ((key & mask) == prefix) atomicAdd(&row[(key >> shift) & 255u], 1u);
                 }
                 __syncthreads();
                 for (int bn = tid; bn < 256; bn += nt) {
@@ -218,40 +221,70 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
             thr = ss.sel[0];
         }
 
-        // ---- survivor masses and their exact fixed-point total
+        // ---- survivors compacted in index order (contiguous segment per thread), with their
+        // probabilities and the exact fixed-point total
         const float invT = 1.0f / sp.temperature;
-        unsigned long long zloc = 0ull;
-        for (int i = tid; i < V; i += nt) {
-            const float p = ord_key(z[i]) >= thr ? expf((z[i] - mx) * invT) : 0.f;
-            pv[i] = p;
-            zloc += fixq(p);
-        }
+        int ns;
         unsigned long long Zq;
-        block_exclusive_scan_u64(zloc, ss.q, &Zq);
+        {
+            const int seg = (V + nt - 1) / nt;
+            const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
+            int cnt = 0;
+            for (int i = a0; i < a1; ++i) cnt += ord_key(z[i]) >= thr;
+            unsigned long long tot;
+            int off = (int)block_exclusive_scan_u64((unsigned long long)cnt, ss.q, &tot);
+            ns = (int)tot;
+            unsigned long long zl = 0ull;
+            for (int i = a0; i < a1; ++i) {
+                if (ord_key(z[i]) < thr) continue;
+                const float p = expf((z[i] - mx) * invT);
+                ci[off] = i;
+                cp[off] = p;
+                zl += fixq(p);
+                ++off;
+            }
+            block_exclusive_scan_u64(zl, ss.q, &Zq);  // barrier: the compacted arrays are complete
+        }
 
-        // ---- top-p: crossing key by a mass radix select, then its ties in index order
+        // ---- top-p over the survivors: crossing key by a mass radix select, then its ties
         bool cut = false;
         uint32_t tkey = 0u;
         int tidx = 0x7fffffff;
         if (sp.top_p < 1.0f) {
-            const unsigned long long T = (unsigned long long)ceil((double)sp.top_p * (double)Zq);
-            if (tid == 0) { ss.sel[0] = 0u; ss.sel[1] = 0u; ss.rem = T > 0ull ? T : 1ull; }
+            if (tid == 0) {
+                const unsigned long long T = (unsigned long long)ceil((double)sp.top_p * (double)Zq);
+                ss.sel[0] = 0u; ss.sel[1] = 0u; ss.rem = T > 0ull ? T : 1ull;
+            }
+            unsigned* mh = pc;        // per-digit sums of the masses' high and low 16-bit halves
+            unsigned* ml = pc + 256;  // (32-bit shared atomics; exact: at most 2^14 * 2^16 each)
             for (int shift = 24; shift >= 0; shift -= 8) {
-                for (int i = tid; i < nw * 256; i += nt) ph[i] = 0ull;
+                for (int i = tid; i < 512; i += nt) pc[i] = 0u;
                 __syncthreads();
                 const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
-                for (int i = tid; i < V; i += nt) {
-                    const float p = pv[i];
-                    const uint32_t key = ord_key(z[i]);
-                    if (p > 0.f && (key & mask) == prefix)
-                        atomicAdd(&ph[warp * 256 + ((key >> shift) & 255u)], fixq(p));
+                for (int j0 = 0; j0 < ns; j0 += nt) {
+                    const int j = j0 + tid;
+                    const uint32_t key = j < ns ? ord_key(z[ci[j]]) : 0u;
+                    bool in = j < ns && (key & mask) == prefix;
+                    const uint32_t digit = (key >> shift) & 255u;
+                    const unsigned long long q = in ? fixq(cp[j]) : 0ull;
+                    // one full-warp reduction per distinct digit among the active lanes
+                    unsigned pend = __ballot_sync(0xffffffffu, in);
+                    while (pend) {
+                        const uint32_t dg = __shfl_sync(0xffffffffu, digit, __ffs(pend) - 1);
+                        const bool mine = in && digit == dg;
+                        const unsigned hi = __reduce_add_sync(0xffffffffu, mine ? (unsigned)(q >> 16) : 0u);
+                        const unsigned lo = __reduce_add_sync(0xffffffffu, mine ? (unsigned)(q & 0xFFFFu) : 0u);
+                        if (lane == __ffs(pend) - 1) {
+                            atomicAdd(&mh[dg], hi);
+                            atomicAdd(&ml[dg], lo);
+                        }
+                        pend &= ~__ballot_sync(0xffffffffu, mine);
+                        if (mine) in = false;
+                    }
                 }
                 __syncthreads();
-                for (int bn = tid; bn < 256; bn += nt) {
-                    unsigned long long t = 0ull;
-                    for (int w = 0; w < nw; ++w) t += ph[w * 256 + bn];
-                    ss.mass[bn] = t;
-                }
+                for (int bn = tid; bn < 256; bn += nt)
+                    ss.mass[bn] = ((unsigned long long)mh[bn] << 16) + (unsigned long long)ml[bn];
                 __syncthreads();
                 if (tid < 32) {
                     unsigned long long rem_out = 0ull;
@@ -263,44 +296,44 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
             }
             tkey = ss.sel[0];
             const unsigned long long rem = ss.rem;  // mass still needed from the elements with key == tkey
-            // ties of the crossing key in index order: contiguous segment per thread
-            const int seg = (V + nt - 1) / nt;
-            const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
+            const int seg = (ns + nt - 1) / nt;
+            const int b0 = min(ns, tid * seg), b1 = min(ns, b0 + seg);
             unsigned long long loc = 0ull;
-            for (int i = a0; i < a1; ++i)
-                if (pv[i] > 0.f && ord_key(z[i]) == tkey) loc += fixq(pv[i]);
+            for (int j = b0; j < b1; ++j)
+                if (ord_key(z[ci[j]]) == tkey) loc += fixq(cp[j]);
             unsigned long long tot;
             unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &tot);
             int c = 0x7fffffff;
-            for (int i = a0; i < a1; ++i) {
-                if (!(pv[i] > 0.f && ord_key(z[i]) == tkey)) continue;
-                run += fixq(pv[i]);
-                if (run >= rem) { c = i; break; }
+            for (int j = b0; j < b1; ++j) {
+                if (ord_key(z[ci[j]]) != tkey) continue;
+                run += fixq(cp[j]);
+                if (run >= rem) { c = ci[j]; break; }
             }
             tidx = block_min_i(c, ss.i);
             cut = true;
         }
 
-        // ---- draw in vocabulary order over the kept set (exact fixed-point prefix sums)
-        auto kept = [&](int i) {
-            if (!(pv[i] > 0.f)) return false;
+        // ---- draw in vocabulary order over the kept survivors (exact fixed-point prefix sums)
+        auto kept = [&](int j) {
             if (!cut) return true;
-            const uint32_t key = ord_key(z[i]);
-            return key > tkey || (key == tkey && i <= tidx);
+            const uint32_t key = ord_key(z[ci[j]]);
+            return key > tkey || (key == tkey && ci[j] <= tidx);
         };
-        const int seg = (V + nt - 1) / nt;
-        const int v0 = min(V, tid * seg), v1 = min(V, v0 + seg);
+        const int seg = (ns + nt - 1) / nt;
+        const int b0 = min(ns, tid * seg), b1 = min(ns, b0 + seg);
         unsigned long long loc = 0ull;
-        for (int i = v0; i < v1; ++i)
-            if (kept(i)) loc += fixq(pv[i]);
+        for (int j = b0; j < b1; ++j)
+            if (kept(j)) loc += fixq(cp[j]);
         unsigned long long ZS;
         unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &ZS);
-        const unsigned long long target = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
+        if (tid == 0) ss.rem = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
+        __syncthreads();
+        const unsigned long long target = ss.rem;
         int cand = 0x7fffffff;
-        for (int i = v0; i < v1; ++i) {
-            if (!kept(i)) continue;
-            run += fixq(pv[i]);
-            if (run > target) { cand = i; break; }
+        for (int j = b0; j < b1; ++j) {
+            if (!kept(j)) continue;
+            run += fixq(cp[j]);
+            if (run > target) { cand = ci[j]; break; }
         }
         tok = block_min_i(cand, ss.i);
     }
@@ -339,7 +372,7 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
 
 // shared memory of sample_smem / sample_block for V logits and `threads` threads
 inline size_t sample_smem_bytes_dev(int V, int threads) {
-    return sample_detail::sample_hist_offset(V) + (size_t)(threads / 32) * 256 * sizeof(unsigned long long);
+    return 3 * sample_detail::sample_array_bytes(V) + (size_t)(threads / 32) * 256 * sizeof(unsigned);
 }
 
 }  // namespace sd

@@ -637,8 +637,8 @@ int setup_tc_prefill(sd_ctx* c) {
             __half* buf = nullptr;
             if ((rc = dalloc(c, &buf, 2 * n * sizeof(__half)))) return rc;
             CK(launch_dequant_split(W, buf, buf + n, c->stream));
-            if (!tc_map_fp16(&c->tc_w[l][2 * w], buf, W.rows, W.cols) ||
-                !tc_map_fp16(&c->tc_w[l][2 * w + 1], buf + n, W.rows, W.cols))
+            if (!tc_map_fp16(&c->tc_w[l][2 * w], buf, W.rows, W.cols, true) ||
+                !tc_map_fp16(&c->tc_w[l][2 * w + 1], buf + n, W.rows, W.cols, true))
                 return fail(c, SD_ERR_CUDA, "tensor map for a prefill weight could not be encoded");
         }
     }
@@ -648,7 +648,8 @@ int setup_tc_prefill(sd_ctx* c) {
         return rc;
     const int ks[3] = {s.d, qd, s.ff};
     for (int k = 0; k < 3; ++k)
-        if (!tc_map_fp16(&c->tc_x[k][0], c->pf_xh, R, ks[k]) || !tc_map_fp16(&c->tc_x[k][1], c->pf_xl, R, ks[k]))
+        if (!tc_map_fp16(&c->tc_x[k][0], c->pf_xh, R, ks[k], false) ||
+            !tc_map_fp16(&c->tc_x[k][1], c->pf_xl, R, ks[k], false))
             return fail(c, SD_ERR_CUDA, "tensor map for the prefill activations could not be encoded");
     CK(cudaStreamSynchronize(c->stream));
     c->tc_prefill = true;
@@ -690,12 +691,12 @@ int setup_persistent(sd_ctx* c) {
     a.layers = c->step_layers;
     // exchange words start at epoch 0, which no step uses
     const int B = c->B, qkv_rows = s.qkv_rows();
-    const size_t W = sizeof(unsigned long long);
+    const size_t W = sizeof(unsigned long long) * 4;  // four replicas of every exchange buffer
     if ((rc = dalloc(c, &a.ll_xa, W * B * s.d)) || (rc = dalloc(c, &a.ll_xb, W * B * s.d)) ||
         (rc = dalloc(c, &a.ll_qkv, W * B * qkv_rows)) ||
         (rc = dalloc(c, &a.ll_part, W * B * s.H * a.max_split * (s.hd + 2))) ||
         (rc = dalloc(c, &a.ll_u, W * B * s.ff)) || (rc = dalloc(c, &a.ll_logits, W * B * m.vocab)) ||
-        (rc = dalloc(c, &a.ll_tok, W * B)) || (rc = dalloc(c, &a.gen, 256)))
+        (rc = dalloc(c, &a.ll_tok, W * 32)) || (rc = dalloc(c, &a.gen, 256)))
         return rc;
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
@@ -727,6 +728,9 @@ void write_trace(sd_ctx* c, int n_steps) {
     for (int k = 0; k < 8; ++k)
         fprintf(f, "  %-6s %8.3f %8.3f %8.3f\n", names[k], (double)t[3 * k] / 1e3 / n_steps / per[k],
                 (double)t[3 * k + 1] / 1e3 / n_steps / per[k], (double)t[3 * k + 2] / 1e3 / n_steps / per[k]);
+    fprintf(f, "  refill: %.3f us per call, %.2f records per call, %.1f calls per step\n",
+            t[31] ? (double)t[29] / 1e3 / (double)t[31] : 0.0, t[31] ? (double)t[30] / (double)t[31] : 0.0,
+            (double)t[31] / n_steps);
     fprintf(f, "  qkv sub-phases us: slice %.3f record %.3f norm %.3f matvec %.3f publish %.3f\n",
             (double)t[24] / 1e3 / n_steps / per[1], (double)t[25] / 1e3 / n_steps / per[1],
             (double)t[26] / 1e3 / n_steps / per[1], (double)t[27] / 1e3 / n_steps / per[1],
@@ -1245,9 +1249,9 @@ int sd_qmat_gemm_tc(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue,
     CK(cudaMalloc(&xs, 2 * xn * sizeof(__half) + 256));
     err = reinterpret_cast<int*>(reinterpret_cast<char*>(xs) + 2 * xn * sizeof(__half));
     TcGemmArgs a;
-    bool ok = tc_map_fp16(&a.xh, xs, M, m->m.cols) && tc_map_fp16(&a.xl, xs + xn, M, m->m.cols) &&
-              tc_map_fp16(&a.wh, m->split, m->m.rows, m->m.cols) &&
-              tc_map_fp16(&a.wl, m->split + wn, m->m.rows, m->m.cols);
+    bool ok = tc_map_fp16(&a.xh, xs, M, m->m.cols, false) && tc_map_fp16(&a.xl, xs + xn, M, m->m.cols, false) &&
+              tc_map_fp16(&a.wh, m->split, m->m.rows, m->m.cols, true) &&
+              tc_map_fp16(&a.wl, m->split + wn, m->m.rows, m->m.cols, true);
     cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
     a.M = M; a.N = m->m.rows; a.K = m->m.cols; a.epi = epilogue; a.bias = bias_dev; a.resid = resid_dev;
     a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows; a.err = err;

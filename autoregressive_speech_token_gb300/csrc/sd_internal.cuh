@@ -245,7 +245,8 @@ struct alignas(128) TcGemmArgs {
     int* err = nullptr;
     long long spin_budget = 0;
 };
-bool tc_map_fp16(CUtensorMap* map, const void* base, int rows, int cols);
+// 2-D fp16 tensor map [rows][cols] with the GEMM's box (weights: 64 rows, activations: 128 rows)
+bool tc_map_fp16(CUtensorMap* map, const void* base, int rows, int cols, bool weights);
 size_t tc_smem_bytes();
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t st);
 cudaError_t launch_split_rows(const float* x, int ldx, int M, int K, __half* hi, __half* lo, cudaStream_t st);

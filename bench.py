@@ -273,7 +273,7 @@ def run_gpu(args):
     peaks, peak_kind = load_peaks()
     bytes_step = mean_step_bytes(m, run.prompt_len, K)
     achieved = bytes_step / (ms / K / 1e3) / 1e9
-    traffic = load_traffic(args.config)
+    traffic = load_traffic(args.config, "persistent" if info.persistent else "graph")
     dec.close()
 
     line = {
@@ -288,7 +288,9 @@ def run_gpu(args):
                    "kernels_per_step": info.kernels_per_step, "attn_splits": info.attn_splits},
         "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": int(info.step_h2d_bytes),
                 "d2h_bytes_per_step": int(info.step_d2h_bytes), "steps": Ke},
-        "roofline": {"bound": "hbm", "kernel": f"decode step ({info.kernels_per_step} kernels, one CUDA graph)",
+        "roofline": {"bound": "hbm",
+                     "kernel": (f"decode step (persistent kernel, {info.persistent} CTAs, one launch per {K} steps)"
+                                if info.persistent else f"decode step ({info.kernels_per_step} kernels, one CUDA graph)"),
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
                      "bytes_per_step": int(bytes_step),
@@ -299,7 +301,7 @@ def run_gpu(args):
                     "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill],
                     "note": "sd_prefill end to end (median of 3): positions 0..P-2 as GEMMs over all rows, "
                             "the last position through the step graph"},
-        "gpu_launches": int(info.kernels_per_step * K),
+        "gpu_launches": 1 if info.persistent else int(info.kernels_per_step * K),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -310,12 +312,14 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def load_traffic(config):
-    """Per-step DRAM bytes from the committed ncu summary of this workload, if any."""
+def load_traffic(config, step_path):
+    """Per-step DRAM bytes from the committed ncu summary of this workload and
+    step path (graph or persistent kernel), if any."""
     path = os.path.join(ROOT, "profiles", f"traffic_{config}.json")
     try:
         with open(path) as f:
-            return json.load(f).get("dram_bytes_per_step")
+            d = json.load(f)
+        return d.get("dram_bytes_per_step") if d.get("path", "graph") == step_path else None
     except Exception:
         return None
 
