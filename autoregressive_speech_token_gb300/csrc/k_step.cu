@@ -29,6 +29,11 @@
 // Port: Development Journal", section 3.2 for the layer order; sections
 // 3.12-3.13 for the cache layout [head][pos][dim] and the causal extent.)
 #include "k_gemv.cuh"
+
+// The 512 compute threads synchronise on named barrier 1; warp 16 (the
+// weight-stream producer) runs its own loop and never joins them.
+#define SAMPLE_SYNC() asm volatile("bar.sync 1, 512;" ::: "memory")
+#define SAMPLE_NT 512
 #include "sample_dev.cuh"
 
 namespace sd {
@@ -36,8 +41,9 @@ namespace step_detail {
 
 using namespace gemv_detail;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;            // compute threads
 constexpr int kWarps = kThreads / 32;
+constexpr int kBlock = kThreads + 32;     // + the producer warp
 constexpr int kNMB = 16;         // records in flight at most (a power of two)
 constexpr int kErrTimeout = 6;
 constexpr int kMaxOwn = 64;      // residual-stream rows owned by one CTA
@@ -48,6 +54,18 @@ constexpr int kKC = 128;         // cached keys staged per attention sub-chunk
 enum PhaseKind { PK_EMBED = 0, PK_QKV, PK_ATTN, PK_O, PK_FC, PK_PROJ, PK_HEAD, PK_SAMPLE };
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+// barrier of the compute threads (named barrier 1)
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ int csync_and(int pred) {
+    int r;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.s32 p, %1, 0; bar.red.and.pred q, 1, 512, p; selp.s32 %0, 1, 0, q; }"
+        : "=r"(r)
+        : "r"(pred)
+        : "memory");
+    return r;
+}
 
 __device__ __forceinline__ unsigned long long gtime() {
     unsigned long long t;
@@ -306,7 +324,7 @@ __device__ void norm_rows(float* x, int K, bool ln, const float* g, const float*
         }
     }
     // every warp holds the same statistics; all reads above precede the writes below
-    __syncthreads();
+    csync();
     const float4* g4 = reinterpret_cast<const float4*>(g);
     const float4* b4 = reinterpret_cast<const float4*>(gb);
     for (int i = threadIdx.x; i < NB * K4; i += kThreads) {
@@ -328,7 +346,7 @@ __device__ void norm_rows(float* x, int K, bool ln, const float* g, const float*
         }
         *p = v;
     }
-    __syncthreads();
+    csync();
 }
 
 // Partial dot products of one 16-byte weight unit with the lane's activations,
@@ -421,13 +439,13 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
             }
         }
     }
-    __syncthreads();
+    csync();
     for (int t = threadIdx.x; t < nr * NB; t += kThreads) {
         float v = 0.f;
         for (int k = 0; k < WK; ++k) v += s_part[t * WK + k];
         s_y[t] = v;
     }
-    __syncthreads();
+    csync();
 }
 
 // Attention splits for n = pos + 1 keys: at most max_split chunks of about
@@ -466,17 +484,23 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
     const __half* Vg = a.vc + hb;
     const int u16 = hd / 8;              // 16-byte units per cached row
 
-    // cached rows [j0, j1) (the position being decoded comes from kn / vn)
+    // cached rows [j0, j1) (the position being decoded comes from kn / vn), as
+    // asynchronous 16-byte copies (cp.async, through L2): all in flight at once,
+    // completed by stage_wait()
     auto stage = [&](int j0, int j1) {
         const int nu = (j1 - j0) * u16;
         for (int t = tid; t < 2 * nu; t += kThreads) {
             const bool isv = t >= nu;
             const int uu = isv ? t - nu : t;
             if (j0 + uu / u16 == pos) continue;
-            const uint4 w = __ldcg(reinterpret_cast<const uint4*>((isv ? Vg : Kg) + (size_t)j0 * hd) + uu);
-            reinterpret_cast<uint4*>(isv ? Vs : Ks)[uu] = w;
+            const void* src = reinterpret_cast<const uint4*>((isv ? Vg : Kg) + (size_t)j0 * hd) + uu;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(reinterpret_cast<uint4*>(isv ? Vs : Ks) + uu)),
+                         "l"(src)
+                         : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
+    auto stage_wait = [&]() { asm volatile("cp.async.wait_all;" ::: "memory"); };
     stage(c0, min(c1, c0 + kKC));  // issued before the wait for this step's q
 
     const unsigned long long* src = a.ll_qkv + (size_t)(blockIdx.x & (kRep - 1)) * rs_qkv;
@@ -486,7 +510,7 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         if (ok) ok = ll_read(src + (size_t)b * qkv_rows + qd + kd + (size_t)g * hd, 1, 0, hd, e, vn, err,
                              a.spin_budget);
     }
-    if (!__syncthreads_and(ok)) return false;
+    if (!csync_and(ok)) return false;
     // RoPE (NEOX half split) at pos on q and the new k; q scaled by 1/sqrt(hd)
     const float scale = 1.0f / sqrtf((float)hd);
     for (int i = tid; i < (HPG + 1) * half; i += kThreads) {
@@ -512,7 +536,7 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         mm[tid] = -INFINITY;
         ls[tid] = 0.f;
     }
-    __syncthreads();
+    csync();
     if (last) {
         // append the new position to the cache (fp16, round to nearest); the fence
         // orders it before this item's published partial, which later steps' readers
@@ -527,25 +551,46 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
     for (int j0 = c0; j0 < c1; j0 += kKC) {
         const int j1 = min(c1, j0 + kKC), nk = j1 - j0;
         if (j0 != c0) {
-            __syncthreads();
+            csync();
             stage(j0, j1);
         }
+        stage_wait();
         if (pos >= j0 && pos < j1)
             for (int dd = tid; dd < hd; dd += kThreads) {
                 Ks[(pos - j0) * hd + dd] = __float2half_rn(kn[dd]);
                 Vs[(pos - j0) * hd + dd] = __float2half_rn(vn[dd]);
             }
-        __syncthreads();
-        // scores: a warp per key, lanes over dimensions
-        for (int jj = warp; jj < nk; jj += kWarps) {
-            for (int h = 0; h < HPG; ++h) {
-                float s = 0.f;
-                for (int dd = lane; dd < hd; dd += 32) s = fmaf(q[h * hd + dd], __half2float(Ks[jj * hd + dd]), s);
-                s = warp_sum(s);
-                if (lane == 0) sc[h * kKC + jj] = s;
+        csync();
+        // scores: a warp per key, lanes over dimensions; four keys at a time so that
+        // their shuffle reductions overlap
+        for (int h = 0; h < HPG; ++h) {
+            float qv[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) qv[t] = (lane + 32 * t < hd) ? q[h * hd + lane + 32 * t] : 0.f;
+            for (int jb = warp; jb < nk; jb += 4 * kWarps) {
+                float sv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int jj = jb + u * kWarps;
+                    float acc = 0.f;
+                    if (jj < nk) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            if (lane + 32 * t < hd) acc = fmaf(qv[t], __half2float(Ks[jj * hd + lane + 32 * t]), acc);
+                    }
+                    sv[u] = acc;
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) sv[u] += __shfl_xor_sync(0xffffffffu, sv[u], o2);
+                if (lane == 0)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (jb + u * kWarps < nk) sc[h * kKC + jb + u * kWarps] = sv[u];
             }
         }
-        __syncthreads();
+        csync();
         // online softmax per head (warp h)
         if (warp < HPG) {
             const int h = warp;
@@ -568,7 +613,7 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
                 mm[h] = mnew;
             }
         }
-        __syncthreads();
+        csync();
         // PV: thread (group kg, pair t) sums keys kg, kg + ng, ...
         if (tid < ng * npair) {
             const int kg = tid / npair, t = tid - kg * npair, h = t / hd, dd = t - h * hd;
@@ -576,14 +621,14 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
             for (int jj = kg; jj < nk; jj += ng) acc = fmaf(sc[h * kKC + jj], __half2float(Vs[jj * hd + dd]), acc);
             op[tid] = acc;
         }
-        __syncthreads();
+        csync();
         for (int t = tid; t < npair; t += kThreads) {
             float acc = 0.f;
             for (int kg = 0; kg < ng; ++kg) acc += op[kg * npair + t];
             o[t] = o[t] * cr[t / hd] + acc;
         }
     }
-    __syncthreads();
+    csync();
     // publish (o[hd], m, l) per query head of the group
     const int W = hd + 2;
     for (int t = tid; t < HPG * W; t += kThreads) {
@@ -592,14 +637,14 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         unsigned long long* dst = a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k);
         ll_store_rep(dst, rs_part, v, e);
     }
-    __syncthreads();
+    csync();
     return true;
 }
 
 // ------------------------------------------------------------------ the kernel
 
 template <int QK, int NB>
-__global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
+__global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
     unsigned char* ring = sm;
     float* act = reinterpret_cast<float*>(sm + a.ring_bytes);
@@ -607,9 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
     __shared__ __align__(8) unsigned long long s_mb[kNMB];
     __shared__ long long s_rec[kNMB];  // ring position (monotonic bytes) of record i % kNMB
     __shared__ int s_off[kNMB];        // the same position within the ring
-    __shared__ long long s_head;       // next free ring position, monotonic (thread 0)
-    __shared__ int s_head_off;         // the same position within the ring
-    __shared__ int s_ni, s_pj;         // records issued; slice index of the next one within its step
+    __shared__ int s_nc;               // records consumed (compute thread 0 -> producer)
+    __shared__ int s_done;             // compute threads finished (normally or on an error)
     __shared__ float s_own[NB * kMaxOwn];
     __shared__ float s_part[kMaxPart];
     __shared__ float s_y[kMaxPart];
@@ -629,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
 
     {
         const int words = L * (int)(sizeof(StepLayer) / 4);
-        for (int i = tid; i < words; i += kThreads)
+        for (int i = tid; i < words; i += kBlock)
             reinterpret_cast<int*>(tab)[i] = reinterpret_cast<const int*>(a.layers)[i];
     }
     __syncthreads();
@@ -637,83 +681,95 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
     if (tid == 0) {
         for (int k = 0; k < kNMB; ++k) mb_init(smem_u32(&s_mb[k]));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        s_head = 0;
-        s_head_off = 0;
-        s_ni = 0;
-        s_pj = 0;
+        s_nc = 0;
+        s_done = 0;
     }
     __syncthreads();
 
+    // ---- producer warp: streams this CTA's weight records into the ring, as
+    // far ahead as the ring and the barriers allow (positions tracked
+    // incrementally: no divisions), until every record of the launch is issued
+    if (tid >= kThreads) {
+        if (tid != kThreads) return;
+        int ni = 0, pj = 0, hoff = 0;
+        long long head = 0, idle0 = clock64();
+        bool ok = true;
+        while (ni < total) {
+            const int nc = ld_volatile(&s_nc);
+            if (ld_volatile(&s_done)) break;
+            bool issued = false;
+            if (ni - nc < kNMB) {
+                const Slice sl = slice_at(a, tab, s_geo, pj);
+                long long start = head;
+                int off = hoff;
+                if (off + sl.bytes > RB) {
+                    start += RB - off;
+                    off = 0;
+                }
+                if (!(ni > nc && start + sl.bytes - s_rec[nc & (kNMB - 1)] > RB)) {
+                    const uint32_t dst = smem_u32(ring + off);
+                    const uint32_t mb = smem_u32(&s_mb[ni & (kNMB - 1)]);
+                    s_rec[ni & (kNMB - 1)] = start;
+                    s_off[ni & (kNMB - 1)] = off;
+                    mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) +
+                                             (sl.g2 ? sl.n_g : 0)));
+                    bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
+                    bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
+                    if (sl.bias) bulk_g2s(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb);
+                    if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
+                    if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
+                    head = start + sl.bytes;
+                    hoff = off + sl.bytes;
+                    ++ni;
+                    if (++pj == per_step) pj = 0;
+                    issued = true;
+                    idle0 = clock64();
+                }
+            }
+            if (!issued) {
+                if (clock64() - idle0 > budget) {  // the consumers stopped advancing
+                    atomicCAS(a.err, 0, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        // copies still in flight into this CTA's ring finish before the CTA exits
+        const long long t0 = clock64();
+        while (!ld_volatile(&s_done) && ok && clock64() - t0 < budget) __nanosleep(256);
+        for (int i = ld_volatile(&s_nc); i < ni; ++i)
+            mb_wait(smem_u32(&s_mb[i & (kNMB - 1)]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
+        return;
+    }
+
+    // ---- compute threads
     // replica strides (words) of the exchange buffers; this CTA reads replica `rep`
     const size_t rs_x = (size_t)NB * d, rs_qkv = (size_t)NB * qkv_rows, rs_u = (size_t)NB * a.ff;
     const size_t rs_part = (size_t)NB * a.H * a.max_split * (a.hd + 2), rs_lg = (size_t)NB * a.V, rs_tok = 32;
     const int rep = cta & (kRep - 1);
     const unsigned gen0 = *reinterpret_cast<const volatile unsigned*>(a.gen);
     const int pos0 = ld_volatile(a.pos);
-    int nc = 0;  // records consumed (uniform over the block)
+    int nc = 0;  // records consumed (uniform over the compute threads)
 
-    // thread 0: issue the following records while the ring and the barriers
-    // have room (ring positions tracked incrementally: no divisions)
-    auto refill = [&]() {
-        if (tid != 0) return;
-        const unsigned long long tr0 = (a.trace && cta == 0) ? gtime() : 0ull;
-        int ni = s_ni, pj = s_pj, hoff = s_head_off;
-        long long head = s_head;
-        while (ni < total && ni - nc < kNMB) {
-            const Slice sl = slice_at(a, tab, s_geo, pj);
-            long long start = head;
-            int off = hoff;
-            if (off + sl.bytes > RB) {
-                start += RB - off;
-                off = 0;
-            }
-            if (ni > nc && start + sl.bytes - s_rec[nc & (kNMB - 1)] > RB) break;
-            const uint32_t dst = smem_u32(ring + off);
-            const uint32_t mb = smem_u32(&s_mb[ni & (kNMB - 1)]);
-            s_rec[ni & (kNMB - 1)] = start;
-            s_off[ni & (kNMB - 1)] = off;
-            mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) + (sl.g2 ? sl.n_g : 0)));
-            bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
-            bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
-            if (sl.bias) bulk_g2s(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb);
-            if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
-            if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
-            head = start + sl.bytes;
-            hoff = off + sl.bytes;
-            ++ni;
-            if (++pj == per_step) pj = 0;
-        }
-        if (a.trace && cta == 0) {
-            a.trace[29] += gtime() - tr0;
-            a.trace[30] += (unsigned long long)(ni - s_ni);
-            a.trace[31] += 1ull;
-        }
-        s_ni = ni;
-        s_pj = pj;
-        s_head = head;
-        s_head_off = hoff;
-    };
     // trace: CTA 0 sums, per phase kind, the wait for its inputs, the wait for
     // its weight record and the rest (ns)
     unsigned long long t_a = 0, t_b = 0, t_w = 0;
     // waits for record nc (slice j of the step); returns its base in the ring
     auto wait_rec = [&](const Slice& sl, bool& ok) -> const unsigned char* {
-        if (tid == 0 && s_ni <= nc) refill();  // only when the record was not issued yet
         const unsigned long long tw0 = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
         const uint32_t mb = smem_u32(&s_mb[nc & (kNMB - 1)]);
         ok = mb_wait(mb, (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
-        ok = __syncthreads_and(ok) != 0;
+        ok = csync_and(ok) != 0;
         if (a.trace && cta == 0 && tid == 0) t_w += gtime() - tw0;
         (void)sl;
         return ring + s_off[nc & (kNMB - 1)];
     };
-    // a record is consumed: its ring space is free, and thread 0 issues the
-    // following records now, while the other threads go on to the next
-    // phase's input wait
+    // a record is consumed: its ring space is free for the producer
     auto done_rec = [&]() {
-        __syncthreads();
+        csync();
         ++nc;
-        refill();
+        if (tid == 0) *reinterpret_cast<volatile int*>(&s_nc) = nc;
     };
     auto tr_begin = [&]() { if (a.trace && cta == 0 && tid == 0) { t_a = gtime(); t_w = 0; } };
     auto tr_waited = [&]() { if (a.trace && cta == 0 && tid == 0) t_b = gtime(); };
@@ -726,7 +782,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         }
     };
 
-    refill();
     bool ok = true;
     for (int s = 0; s < a.n_steps && ok; ++s) {
         const int pos = pos0 + s;
@@ -747,10 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     if ((unsigned)(w >> 32) != et) okr = ll_spin(tp, et, &w, a.err, budget);
                     reinterpret_cast<int*>(s_red)[tid] = (int)(unsigned)w;
                 }
-                okr = __syncthreads_and(okr) != 0;
+                okr = csync_and(okr) != 0;
 #pragma unroll
                 for (int b = 0; b < NB; ++b) tk[b] = reinterpret_cast<int*>(s_red)[b];
-                __syncthreads();
+                csync();
             }
             if (!okr) { ok = false; break; }
             __threadfence();  // order this step's cache reads after the previous steps' appends
@@ -767,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                 act[b * padded(d) + pidx(k)] = v;
                 if (k >= o0 && k < o1) s_own[b * kMaxOwn + (k - o0)] = v;
             }
-            __syncthreads();
+            csync();
             tr_end(PK_EMBED);
         }
 
@@ -776,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- QKV rows (norm prologue, bias)
             tr_begin();
             if (l > 0) {
-                ok = __syncthreads_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, e - 1u, act, a.err, budget, true)) != 0;
+                ok = csync_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, e - 1u, act, a.err, budget, true)) != 0;
                 if (!ok) break;
             }
             tr_waited();
@@ -831,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             {
                 const int W = a.hd + 2;
                 float* pp = act + NB * padded(qd);  // [NB*H][S][W]
-                ok = __syncthreads_and(
+                ok = csync_and(
                          ll_read(a.ll_part + rep * rs_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget)) != 0;
                 if (!ok) break;
                 tr_waited();
@@ -848,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
                     }
                     act[(t / qd) * padded(qd) + pidx(t % qd)] = num / den;  // o[b][h * hd + dd], padded
                 }
-                __syncthreads();
+                csync();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 1);
                 const unsigned char* rec = wait_rec(sl, ok);
                 if (!ok) break;
@@ -869,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- FC / gate-up rows (norm prologue, GELU / SwiGLU)
             tr_begin();
             {
-                ok = __syncthreads_and(ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true)) != 0;
+                ok = csync_and(ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true)) != 0;
                 if (!ok) break;
                 tr_waited();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 2);
@@ -900,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
             // ---- proj / down rows (+bias +residual)
             tr_begin();
             {
-                ok = __syncthreads_and(ll_read(a.ll_u + rep * rs_u, NB, a.ff, a.ff, e, act, a.err, budget, true)) != 0;
+                ok = csync_and(ll_read(a.ll_u + rep * rs_u, NB, a.ff, a.ff, e, act, a.err, budget, true)) != 0;
                 if (!ok) break;
                 tr_waited();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 3);
@@ -926,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         const unsigned eh = eb + (unsigned)L;
         tr_begin();
         {
-            ok = __syncthreads_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, eh - 1u, act, a.err, budget, true)) != 0;
+            ok = csync_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, eh - 1u, act, a.err, budget, true)) != 0;
             if (!ok) break;
             tr_waited();
             const Slice sl = slice_at(a, tab, s_geo, 4 * L);
@@ -949,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         if (cta < NB) {
             tr_begin();
             float* z = act;
-            ok = __syncthreads_and(
+            ok = csync_and(
                      ll_read(a.ll_logits + rep * rs_lg + (size_t)cta * a.V, 1, 0, a.V, eh, z, a.err, budget)) != 0;
             if (!ok) break;
             tr_waited();
@@ -971,12 +1026,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepArgs a) {
         if (ok) *a.pos = pos0 + a.n_steps;
         *a.gen = gen0 + (unsigned)a.n_steps;
     }
-    // copies still in flight into this CTA's ring finish before it exits
-    __syncthreads();
+    // the producer drains its copies in flight and exits once it sees this
+    csync();
     if (tid == 0) {
-        const int ni = s_ni;
-        for (int i = nc; i < ni; ++i)
-            mb_wait(smem_u32(&s_mb[i & (kNMB - 1)]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
+        *reinterpret_cast<volatile int*>(&s_nc) = nc;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&s_done) = 1;
     }
 }
 
@@ -1058,7 +1113,7 @@ int step_plan_grid(StepArgs& a, int sm_count) {
         cudaSuccess)
         return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, step_smem_bytes(a)) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlock, step_smem_bytes(a)) != cudaSuccess ||
         per_sm < 1)
         return 0;
     return G;
@@ -1071,7 +1126,7 @@ cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st) {
     const size_t smem = step_smem_bytes(a);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kBlock);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -26,6 +26,14 @@
 #pragma once
 #include "sd_internal.cuh"
 
+// The block barrier and thread count the sampler uses: the whole block by
+// default; a kernel whose block has threads outside the sampler (a producer
+// warp) defines both before including this header.
+#ifndef SAMPLE_SYNC
+#define SAMPLE_SYNC() __syncthreads()
+#define SAMPLE_NT ((int)blockDim.x)
+#endif
+
 namespace sd {
 namespace sample_detail {
 
@@ -62,7 +70,7 @@ static __host__ __device__ __forceinline__ size_t sample_array_bytes(int V) { re
 // exclusive scan of one u64 per thread in thread order; *total = block total
 static __device__ unsigned long long block_exclusive_scan_u64(unsigned long long v, unsigned long long* s,
                                                               unsigned long long* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = SAMPLE_NT >> 5;
     unsigned long long inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -70,7 +78,7 @@ static __device__ unsigned long long block_exclusive_scan_u64(unsigned long long
         if (lane >= o) inc += t;
     }
     if (lane == 31) s[warp] = inc;
-    __syncthreads();
+    SAMPLE_SYNC();
     if (warp == 0) {
         const unsigned long long w = lane < nw ? s[lane] : 0ull;
         unsigned long long wi = w;
@@ -82,10 +90,10 @@ static __device__ unsigned long long block_exclusive_scan_u64(unsigned long long
         s[32 + lane] = wi - w;
         if (lane == 31) s[64] = wi;
     }
-    __syncthreads();
+    SAMPLE_SYNC();
     const unsigned long long r = s[32 + warp] + inc - v;
     *total = s[64];
-    __syncthreads();
+    SAMPLE_SYNC();
     return r;
 }
 
@@ -93,16 +101,16 @@ static __device__ int block_min_i(int v, int* s) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
     if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = v;
-    __syncthreads();
+    SAMPLE_SYNC();
     if (threadIdx.x < 32) {
-        int w = threadIdx.x < (blockDim.x >> 5) ? s[threadIdx.x] : 0x7fffffff;
+        int w = threadIdx.x < (SAMPLE_NT >> 5) ? s[threadIdx.x] : 0x7fffffff;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) w = min(w, __shfl_xor_sync(0xffffffffu, w, o));
         if (threadIdx.x == 0) s[32] = w;
     }
-    __syncthreads();
+    SAMPLE_SYNC();
     const int r = s[32];
-    __syncthreads();
+    SAMPLE_SYNC();
     return r;
 }
 
@@ -110,16 +118,16 @@ static __device__ float block_max_f(float v, float* s) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = v;
-    __syncthreads();
+    SAMPLE_SYNC();
     if (threadIdx.x < 32) {
-        float w = threadIdx.x < (blockDim.x >> 5) ? s[threadIdx.x] : -INFINITY;
+        float w = threadIdx.x < (SAMPLE_NT >> 5) ? s[threadIdx.x] : -INFINITY;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
         if (threadIdx.x == 0) s[32] = w;
     }
-    __syncthreads();
+    SAMPLE_SYNC();
     const float r = s[32];
-    __syncthreads();
+    SAMPLE_SYNC();
     return r;
 }
 
@@ -163,12 +171,12 @@ static __device__ __forceinline__ void select_digit(const T* w, T rem, int shift
 }
 
 // Samples one token from the logits already in shared memory (the first V
-// floats of `smraw`, which holds sample_smem_bytes_dev(V, blockDim.x) bytes) with draw
+// floats of `smraw`, which holds sample_smem_bytes_dev(V, threads) bytes) with draw
 // *u_ptr; every thread gets the token.  `ss` is the small scratch.  Block
 // size: any multiple of 32 up to 1024.
 static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
                                   SampleScratch& ss, int* err) {
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int tid = threadIdx.x, nt = SAMPLE_NT, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const size_t arr = sample_array_bytes(V);
     float* z = reinterpret_cast<float*>(smraw);               // [V] logits
     int* ci = reinterpret_cast<int*>(smraw + arr);            // [V] survivor indices, ascending
@@ -195,28 +203,37 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
         if (k < V) {
             if (tid == 0) { ss.sel[0] = 0u; ss.sel[1] = 0u; ss.sel[2] = (uint32_t)k; }
             for (int shift = 24; shift >= 0; shift -= 8) {
-                for (int i = tid; i < nw * 256; i += nt) pc[i] = 0u;
-                __syncthreads();
+                // the first digit (sign and high exponent bits) is shared by most logits: each
+                // warp counts into its own row, rows merged in fixed order; later digits are
+                // spread, and one shared histogram takes few colliding atomics
+                const bool first = shift == 24;
+                if (first)
+                    for (int i = tid; i < nw * 256; i += nt) pc[i] = 0u;
+                else
+                    for (int i = tid; i < 256; i += nt) ss.hist[i] = 0u;
+                SAMPLE_SYNC();
                 const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
-                unsigned* row = pc + warp * 256;
+                unsigned* row = first ? pc + warp * 256 : ss.hist;
                 for (int i = tid; i < V; i += nt) {
                     const uint32_t key = ord_key(z[i]);
                     if ((key & mask) == prefix) atomicAdd(&row[(key >> shift) & 255u], 1u);
                 }
-                __syncthreads();
-                for (int bn = tid; bn < 256; bn += nt) {
-                    unsigned t = 0u;
-                    for (int w = 0; w < nw; ++w) t += pc[w * 256 + bn];
-                    ss.hist[bn] = t;
+                SAMPLE_SYNC();
+                if (first) {
+                    for (int bn = tid; bn < 256; bn += nt) {
+                        unsigned t = 0u;
+                        for (int w = 0; w < nw; ++w) t += pc[w * 256 + bn];
+                        ss.hist[bn] = t;
+                    }
+                    SAMPLE_SYNC();
                 }
-                __syncthreads();
                 if (tid < 32) {
                     uint32_t rem_out = 0;
                     select_digit<uint32_t>(ss.hist, ss.sel[2], shift, ss.sel, &rem_out);
                     const unsigned any = __ballot_sync(0xffffffffu, rem_out != 0u);
                     if (any && lane == __ffs(any) - 1) ss.sel[2] = rem_out;
                 }
-                __syncthreads();
+                SAMPLE_SYNC();
             }
             thr = ss.sel[0];
         }
@@ -259,7 +276,7 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
             unsigned* ml = pc + 256;  // (32-bit shared atomics; exact: at most 2^14 * 2^16 each)
             for (int shift = 24; shift >= 0; shift -= 8) {
                 for (int i = tid; i < 512; i += nt) pc[i] = 0u;
-                __syncthreads();
+                SAMPLE_SYNC();
                 const uint32_t prefix = ss.sel[0], mask = ss.sel[1];
                 for (int j0 = 0; j0 < ns; j0 += nt) {
                     const int j = j0 + tid;
@@ -267,7 +284,15 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
                     bool in = j < ns && (key & mask) == prefix;
                     const uint32_t digit = (key >> shift) & 255u;
                     const unsigned long long q = in ? fixq(cp[j]) : 0ull;
-                    // one full-warp reduction per distinct digit among the active lanes
+                    if (shift != 24) {
+                        // later digits are spread: direct atomics collide little
+                        if (in) {
+                            atomicAdd(&mh[digit], (unsigned)(q >> 16));
+                            atomicAdd(&ml[digit], (unsigned)(q & 0xFFFFu));
+                        }
+                        continue;
+                    }
+                    // first digit: one full-warp reduction per distinct digit among the active lanes
                     unsigned pend = __ballot_sync(0xffffffffu, in);
                     while (pend) {
                         const uint32_t dg = __shfl_sync(0xffffffffu, digit, __ffs(pend) - 1);
@@ -282,17 +307,17 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
                         if (mine) in = false;
                     }
                 }
-                __syncthreads();
+                SAMPLE_SYNC();
                 for (int bn = tid; bn < 256; bn += nt)
                     ss.mass[bn] = ((unsigned long long)mh[bn] << 16) + (unsigned long long)ml[bn];
-                __syncthreads();
+                SAMPLE_SYNC();
                 if (tid < 32) {
                     unsigned long long rem_out = 0ull;
                     select_digit<unsigned long long>(ss.mass, ss.rem, shift, ss.sel, &rem_out);
                     const unsigned any = __ballot_sync(0xffffffffu, rem_out != 0ull);
                     if (any && lane == __ffs(any) - 1) ss.rem = rem_out;
                 }
-                __syncthreads();
+                SAMPLE_SYNC();
             }
             tkey = ss.sel[0];
             const unsigned long long rem = ss.rem;  // mass still needed from the elements with key == tkey
@@ -327,7 +352,7 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
         unsigned long long ZS;
         unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &ZS);
         if (tid == 0) ss.rem = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
-        __syncthreads();
+        SAMPLE_SYNC();
         const unsigned long long target = ss.rem;
         int cand = 0x7fffffff;
         for (int j = b0; j < b1; ++j) {
@@ -341,7 +366,7 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
         if (tid == 0 && err) atomicExch(err, 2);
         tok = 0;
     }
-    __syncthreads();
+    SAMPLE_SYNC();
     return tok;
 }
 
@@ -349,7 +374,7 @@ static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr
 // have been written by other CTAs of the same kernel).
 static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
                                    unsigned char* smraw, SampleScratch& ss, int* err) {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = SAMPLE_NT;
     float* z = reinterpret_cast<float*>(smraw);
     for (int i0 = 0; i0 < V; i0 += 8 * nt) {
         float r[8];
@@ -364,7 +389,7 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
             if (i < V) z[i] = r[j];
         }
     }
-    __syncthreads();
+    SAMPLE_SYNC();
     return sample_smem(V, sp, u_ptr, smraw, ss, err);
 }
 

@@ -728,9 +728,6 @@ void write_trace(sd_ctx* c, int n_steps) {
     for (int k = 0; k < 8; ++k)
         fprintf(f, "  %-6s %8.3f %8.3f %8.3f\n", names[k], (double)t[3 * k] / 1e3 / n_steps / per[k],
                 (double)t[3 * k + 1] / 1e3 / n_steps / per[k], (double)t[3 * k + 2] / 1e3 / n_steps / per[k]);
-    fprintf(f, "  refill: %.3f us per call, %.2f records per call, %.1f calls per step\n",
-            t[31] ? (double)t[29] / 1e3 / (double)t[31] : 0.0, t[31] ? (double)t[30] / (double)t[31] : 0.0,
-            (double)t[31] / n_steps);
     fprintf(f, "  qkv sub-phases us: slice %.3f record %.3f norm %.3f matvec %.3f publish %.3f\n",
             (double)t[24] / 1e3 / n_steps / per[1], (double)t[25] / 1e3 / n_steps / per[1],
             (double)t[26] / 1e3 / n_steps / per[1], (double)t[27] / 1e3 / n_steps / per[1],
