@@ -284,13 +284,13 @@ __device__ __forceinline__ Slice slice_at(const StepArgs& a, const StepLayer* ta
 
 // ------------------------------------------------------------------ compute helpers
 
-// In-place LayerNorm (biased variance) or RMSNorm of the padded rows
-// x[b][pidx(0..K)), b < NB.  Every warp computes the row statistics itself
-// (a full pass over the row in shared memory, conflict-free 16-byte loads,
-// xor-shuffle sums in a fixed order), so the only block barrier is the one that
-// publishes the normalised row.
+// LayerNorm (biased variance) or RMSNorm of the padded rows x[b][pidx(0..K)),
+// b < NB, written to xn (same layout).  Every warp computes the row statistics
+// itself (a full pass over the row in shared memory, conflict-free 16-byte
+// loads, xor-shuffle sums in a fixed order); x is not overwritten, so the only
+// block barrier is the one that publishes xn.
 template <int NB>
-__device__ void norm_rows(float* x, int K, bool ln, const float* g, const float* gb, float eps) {
+__device__ void norm_to(const float* x, float* xn, int K, bool ln, const float* g, const float* gb, float eps) {
     const int KP = padded(K), lane = threadIdx.x & 31, K4 = K >> 2;
     float mu[NB], rs[NB];
 #pragma unroll
@@ -323,14 +323,12 @@ __device__ void norm_rows(float* x, int K, bool ln, const float* g, const float*
             rs[b] = 1.0f / sqrtf(t / (float)K + eps);
         }
     }
-    // every warp holds the same statistics; all reads above precede the writes below
-    csync();
     const float4* g4 = reinterpret_cast<const float4*>(g);
     const float4* b4 = reinterpret_cast<const float4*>(gb);
     for (int i = threadIdx.x; i < NB * K4; i += kThreads) {
         const int b = i / K4, k4 = i - b * K4;
-        float4* p = reinterpret_cast<float4*>(x + b * KP) + k4 + (k4 >> 3);
-        float4 v = *p;
+        const int pi = (b * KP >> 2) + k4 + (k4 >> 3);
+        float4 v = reinterpret_cast<const float4*>(x)[pi];
         const float4 gg = g4[k4];
         if (ln) {
             const float4 oo = b4[k4];
@@ -344,7 +342,7 @@ __device__ void norm_rows(float* x, int K, bool ln, const float* g, const float*
             v.z = v.z * rs[b] * gg.z;
             v.w = v.w * rs[b] * gg.w;
         }
-        *p = v;
+        reinterpret_cast<float4*>(xn)[pi] = v;
     }
     csync();
 }
@@ -538,14 +536,13 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
     }
     csync();
     if (last) {
-        // append the new position to the cache (fp16, round to nearest); the fence
-        // orders it before this item's published partial, which later steps' readers
-        // (through the chain of epochs) have observed before they read the cache
+        // append the new position to the cache (fp16, round to nearest); the fence after
+        // the partial is published orders it before every later word this CTA
+        // publishes, which the next step's readers observe before they read the cache
         for (int dd = tid; dd < hd; dd += kThreads) {
             a.kc[hb + (size_t)pos * hd + dd] = __float2half_rn(kn[dd]);
             a.vc[hb + (size_t)pos * hd + dd] = __float2half_rn(vn[dd]);
         }
-        __threadfence();
     }
     const int npair = HPG * hd, ng = kThreads / npair;  // PV: ng key groups per (head, dim)
     for (int j0 = c0; j0 < c1; j0 += kKC) {
@@ -622,21 +619,28 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
             op[tid] = acc;
         }
         csync();
+        // the last sub-chunk's update is the partial itself: publish (o[hd], m, l) per query
+        // head of the group as it is formed
+        const bool fin = j1 == c1;
+        const int W = hd + 2;
         for (int t = tid; t < npair; t += kThreads) {
             float acc = 0.f;
             for (int kg = 0; kg < ng; ++kg) acc += op[kg * npair + t];
-            o[t] = o[t] * cr[t / hd] + acc;
+            const float ov = o[t] * cr[t / hd] + acc;
+            o[t] = ov;
+            if (fin) {
+                const int h = t / hd, k = t - h * hd;
+                ll_store_rep(a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k), rs_part, ov,
+                             e);
+            }
+        }
+        if (fin && tid < 2 * HPG) {
+            const int h = tid >> 1, k = hd + (tid & 1);
+            ll_store_rep(a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k), rs_part,
+                         (tid & 1) ? ls[h] : mm[h], e);
         }
     }
-    csync();
-    // publish (o[hd], m, l) per query head of the group
-    const int W = hd + 2;
-    for (int t = tid; t < HPG * W; t += kThreads) {
-        const int h = t / W, k = t - h * W;
-        const float v = k < hd ? o[h * hd + k] : (k == hd ? mm[h] : ls[h]);
-        unsigned long long* dst = a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k);
-        ll_store_rep(dst, rs_part, v, e);
-    }
+    if (last) __threadfence();
     csync();
     return true;
 }
@@ -648,6 +652,8 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
     unsigned char* ring = sm;
     float* act = reinterpret_cast<float*>(sm + a.ring_bytes);
+    // normalised input rows [NB][padded(d)], after the largest staged input
+    float* xn = act + a.B * padded(a.d > a.ff ? (a.d > a.H * a.hd ? a.d : a.H * a.hd) : (a.ff > a.H * a.hd ? a.ff : a.H * a.hd));
     StepLayer* tab = reinterpret_cast<StepLayer*>(sm + a.ring_bytes + a.act_bytes);
     __shared__ __align__(8) unsigned long long s_mb[kNMB];
     __shared__ long long s_rec[kNMB];  // ring position (monotonic bytes) of record i % kNMB
@@ -755,16 +761,15 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     // trace: CTA 0 sums, per phase kind, the wait for its inputs, the wait for
     // its weight record and the rest (ns)
     unsigned long long t_a = 0, t_b = 0, t_w = 0;
-    // waits for record nc (slice j of the step); returns its base in the ring
-    auto wait_rec = [&](const Slice& sl, bool& ok) -> const unsigned char* {
+    // per-thread wait for record nc (normally complete long before); the caller
+    // joins it with the input wait in one barrier
+    auto rec_ready = [&]() -> bool {
         const unsigned long long tw0 = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
-        const uint32_t mb = smem_u32(&s_mb[nc & (kNMB - 1)]);
-        ok = mb_wait(mb, (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
-        ok = csync_and(ok) != 0;
+        const bool r = mb_wait(smem_u32(&s_mb[nc & (kNMB - 1)]), (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
         if (a.trace && cta == 0 && tid == 0) t_w += gtime() - tw0;
-        (void)sl;
-        return ring + s_off[nc & (kNMB - 1)];
+        return r;
     };
+    auto rec_base = [&]() -> const unsigned char* { return ring + s_off[nc & (kNMB - 1)]; };
     // a record is consumed: its ring space is free for the producer
     auto done_rec = [&]() {
         csync();
@@ -830,9 +835,10 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             const unsigned e = eb + (unsigned)l;
             // ---- QKV rows (norm prologue, bias)
             tr_begin();
-            if (l > 0) {
-                ok = csync_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, e - 1u, act, a.err, budget, true)) != 0;
-                if (!ok) break;
+            {
+                bool okr = l > 0 ? ll_read(a.ll_xb + rep * rs_x, NB, d, d, e - 1u, act, a.err, budget, true) : true;
+                okr = okr && rec_ready();
+                if (!(ok = csync_and(okr) != 0)) break;
             }
             tr_waited();
             {
@@ -847,14 +853,13 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                 };
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l);
                 sub(0);
-                const unsigned char* rec = wait_rec(sl, ok);
-                if (!ok) break;
+                const unsigned char* rec = rec_base();
                 sub(1);
-                norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+                norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
                 sub(2);
                 const int nr = sl.r1 - sl.r0;
-                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
                 sub(3);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
                 for (int t = tid; t < nr * NB; t += kThreads) {
@@ -886,9 +891,9 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             {
                 const int W = a.hd + 2;
                 float* pp = act + NB * padded(qd);  // [NB*H][S][W]
-                ok = csync_and(
-                         ll_read(a.ll_part + rep * rs_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget)) != 0;
-                if (!ok) break;
+                bool okr = ll_read(a.ll_part + rep * rs_part, NB * a.H, a.max_split * W, S * W, e, pp, a.err, budget);
+                okr = okr && rec_ready();
+                if (!(ok = csync_and(okr) != 0)) break;
                 tr_waited();
                 for (int t = tid; t < NB * qd; t += kThreads) {
                     const int bh = t / a.hd, dd = t - bh * a.hd;
@@ -905,8 +910,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                 }
                 csync();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 1);
-                const unsigned char* rec = wait_rec(sl, ok);
-                if (!ok) break;
+                const unsigned char* rec = rec_base();
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), qd, nr, act, s_part, s_y);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
@@ -924,16 +928,16 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             // ---- FC / gate-up rows (norm prologue, GELU / SwiGLU)
             tr_begin();
             {
-                ok = csync_and(ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true)) != 0;
-                if (!ok) break;
+                bool okr = ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true);
+                okr = okr && rec_ready();
+                if (!(ok = csync_and(okr) != 0)) break;
                 tr_waited();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 2);
-                const unsigned char* rec = wait_rec(sl, ok);
-                if (!ok) break;
-                norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                              reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+                const unsigned char* rec = rec_base();
+                norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
                 const int nr = sl.r1 - sl.r0;
-                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+                gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
                 if (ln) {
                     for (int t = tid; t < nr * NB; t += kThreads) {
@@ -955,12 +959,12 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             // ---- proj / down rows (+bias +residual)
             tr_begin();
             {
-                ok = csync_and(ll_read(a.ll_u + rep * rs_u, NB, a.ff, a.ff, e, act, a.err, budget, true)) != 0;
-                if (!ok) break;
+                bool okr = ll_read(a.ll_u + rep * rs_u, NB, a.ff, a.ff, e, act, a.err, budget, true);
+                okr = okr && rec_ready();
+                if (!(ok = csync_and(okr) != 0)) break;
                 tr_waited();
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 3);
-                const unsigned char* rec = wait_rec(sl, ok);
-                if (!ok) break;
+                const unsigned char* rec = rec_base();
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), a.ff, nr, act, s_part, s_y);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
@@ -981,16 +985,16 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
         const unsigned eh = eb + (unsigned)L;
         tr_begin();
         {
-            ok = csync_and(ll_read(a.ll_xb + rep * rs_x, NB, d, d, eh - 1u, act, a.err, budget, true)) != 0;
-            if (!ok) break;
+            bool okr = ll_read(a.ll_xb + rep * rs_x, NB, d, d, eh - 1u, act, a.err, budget, true);
+            okr = okr && rec_ready();
+            if (!(ok = csync_and(okr) != 0)) break;
             tr_waited();
             const Slice sl = slice_at(a, tab, s_geo, 4 * L);
-            const unsigned char* rec = wait_rec(sl, ok);
-            if (!ok) break;
-            norm_rows<NB>(act, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                          reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+            const unsigned char* rec = rec_base();
+            norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                        reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
             const int nr = sl.r1 - sl.r0;
-            gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, act, s_part, s_y);
+            gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
             for (int t = tid; t < nr * NB; t += kThreads) {
                 const int i = t / NB, b = t - i * NB;
                 const float v = s_y[t];
@@ -1041,7 +1045,7 @@ size_t act_region_bytes(const StepArgs& a) {
     const int qd = a.H * a.hd, HPG = a.H / a.Hkv;
     int kmax = a.d > a.ff ? a.d : a.ff;
     if (qd > kmax) kmax = qd;
-    size_t need = sizeof(float) * (size_t)a.B * padded(kmax);
+    size_t need = sizeof(float) * ((size_t)a.B * padded(kmax) + (size_t)a.B * padded(a.d));
     const size_t o_phase = sizeof(float) * ((size_t)a.B * padded(qd) + (size_t)a.B * a.H * a.max_split * (a.hd + 2));
     // attention floats before the fp16 staging: a multiple of 4 (16 bytes) for every hd in {64, 128}
     const size_t attn_floats = (size_t)2 * HPG * a.hd + 2 * a.hd + HPG * kKC + 3 * kMaxHPG + kThreads;

@@ -656,9 +656,12 @@ int setup_tc_prefill(sd_ctx* c) {
     return SD_OK;
 }
 
+// The persistent step kernel is the default for the GPT-2/Llama T3 with
+// Q8_0/Q4_0 weights and up to two rows (faster than the per-operation graph on
+// GB300); SD_PERSISTENT=0 selects the graph.
 bool persistent_wanted() {
     const char* e = getenv("SD_PERSISTENT");
-    return e && e[0] == '1';
+    return !(e && e[0] == '0');
 }
 
 // Persistent step plan for GPT-2/Llama with Q8_0/Q4_0 weights and B <= 2.
