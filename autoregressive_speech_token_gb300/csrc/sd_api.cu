@@ -657,18 +657,20 @@ int setup_tc_prefill(sd_ctx* c) {
 }
 
 // The persistent step kernel is the default for the GPT-2/Llama T3 with
-// Q8_0/Q4_0 weights and up to two rows (faster than the per-operation graph on
-// GB300); SD_PERSISTENT=0 selects the graph.
-bool persistent_wanted() {
+// Q8_0/Q4_0 weights and one row (faster than the per-operation graph on
+// GB300); SD_PERSISTENT=1 also selects it for two rows, SD_PERSISTENT=0 never.
+bool persistent_wanted(int rows) {
     const char* e = getenv("SD_PERSISTENT");
-    return !(e && e[0] == '0');
+    if (e && e[0] == '0') return false;
+    if (e && e[0] == '1') return true;
+    return rows == 1;
 }
 
 // Persistent step plan for GPT-2/Llama with Q8_0/Q4_0 weights and B <= 2.
 int setup_persistent(sd_ctx* c) {
     const sd_model_config& m = c->cfg;
     c->persistent = false;
-    if (!persistent_wanted() || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
+    if (!persistent_wanted(c->B) || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
     DStack& s = c->main;
     std::vector<StepLayer> L(s.n_layer);
     for (int l = 0; l < s.n_layer; ++l) {

@@ -53,6 +53,11 @@ def workload_text(run) -> str:
     m = run.model
     s = run.sampler
     samp = "greedy" if s.greedy else f"T {s.temperature}, top-k {s.top_k}, top-p {s.top_p}"
+    if m.arch == P.ARCH_QWEN_TTS:
+        return (f"{run.name}: Talker {m.n_layer}x{m.d_model} ({m.n_head}/{m.n_kv_head} heads x {m.head_dim}, "
+                f"FFN {m.d_ff}, codebook-0 vocab {m.vocab}) + code predictor {m.cp_layer}x{m.cp_d_model} "
+                f"({m.n_codebooks - 1} passes per frame, vocab {m.cp_vocab}), {P.QUANT_NAMES[m.quant]} weights, "
+                f"fp16 KV; prompt {run.prompt_len} + {run.n_steps} frames ({samp}), {m.batch} rows")
     return (f"{run.name}: {m.n_layer}x{m.d_model} {'GPT-2' if m.arch == P.ARCH_GPT2 else 'Llama'} T3, "
             f"{m.n_head}x{m.head_dim} heads, FFN {m.d_ff}, vocab {m.vocab}, {P.QUANT_NAMES[m.quant]} weights, "
             f"fp16 KV; prompt {run.prompt_len} + {run.n_steps} decode steps ({samp}), batch {m.batch}")
@@ -69,6 +74,11 @@ def step_bytes(m: P.ModelSpec, pos: int) -> int:
         small = m.n_layer * 2 * d + d + d
     small *= 4
     kv = m.batch * m.kv_bytes_per_position() * (pos + 1) + m.batch * m.kv_bytes_per_position()  # read + write
+    if m.arch == P.ARCH_QWEN_TTS:
+        # code predictor: positions 0..15 of each frame read their prefix (the cache restarts per frame)
+        cp_pos = 2 * m.cp_layer * m.cp_n_kv_head * m.cp_head_dim * 2
+        kv += m.batch * cp_pos * sum(j + 1 for j in range(m.n_codebooks))
+        small += 4 * m.batch * m.n_codebooks * m.d_model                   # code-embedding rows
     return wq + small + kv
 
 
@@ -198,6 +208,8 @@ def run_gpu(args):
 
     run = get_preset(args.config)
     m = run.model
+    if m.arch == P.ARCH_QWEN_TTS:
+        return run_gpu_frames(args, run, torch, sdpkg, build_model_blob, ws, rank, local, dist, dev)
     K, W = args.steps, args.warmup
     if run.prompt_len + max(K, W) > m.max_ctx:
         raise SystemExit(f"steps must keep prompt + steps <= {m.max_ctx}")
@@ -312,6 +324,91 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_gpu_frames(args, run, torch, sdpkg, build_model_blob, ws, rank, local, dist, dev):
+    """Talker + code predictor: a step is one frame (sd_frame: the Talker step,
+    15 code-predictor passes and 16 samples per row); frames are host-driven
+    calls, so the device-timed and end-to-end numbers both include the per-frame
+    host round trip."""
+    m = run.model
+    K, W = args.steps, args.warmup
+    if run.prompt_len + max(K, W) > m.max_ctx:
+        raise SystemExit(f"frames must keep prompt + frames <= {m.max_ctx}")
+    blob, _ = build_model_blob(m, seed=run.weight_seed)
+    stream = torch.cuda.current_stream(dev)
+    dec = sdpkg.Decoder(m, blob, device=local, stream=stream.cuda_stream)
+    del blob
+    info = dec.info()
+    prompt = prompt_tokens(run)
+    s = sdpkg.Sampler.from_spec(run.sampler)
+    B = m.batch
+    draws = uniform_draws(run.draw_seed, max(K, W) + 1, B, m.n_codebooks)
+    dec.reset()
+    codes = dec.prefill(prompt, s, draws[0])
+    for i in range(W):
+        codes = dec.frame(codes, s, s, draws[1 + i])
+    dec.reset()
+    codes = dec.prefill(prompt, s, draws[0])
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        ev0.record(stream)
+        for i in range(K):
+            codes = dec.frame(codes, s, s, draws[1 + i])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+    barrier(dist, ws)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(dist, ws, ms, dev)
+    e2e_s = max_over_ranks(dist, ws, t1 - t0, dev)
+    pf_ms = []
+    for _ in range(3):
+        dec.reset()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        dec.prefill(prompt, s, draws[0])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        pf_ms.append(ev0.elapsed_time(ev1))
+    pf_ms = sorted(pf_ms)[1]
+    pf_flops = prefill_gemm_flops(m, run.prompt_len)
+    dec.close()
+    peaks, peak_kind = load_peaks()
+    bytes_frame = mean_step_bytes(m, run.prompt_len, K)
+    achieved = bytes_frame / (ms / K / 1e3) / 1e9
+    unit = "row-frames/s" if B > 1 else "frames/s"
+    line = {
+        "metric": METRIC, "value": round(ws * K * B / (ms_max / 1e3), 2), "unit": unit, "n_gpus": ws, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights, uniform prompt IDs, Philox draws)",
+        "config": {"workload": workload_text(run), "batch": B, "prompt_len": run.prompt_len,
+                   "positions": [run.prompt_len, run.prompt_len + K - 1], "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2: {bytes_frame / 1e6:.1f} MB streamed per frame vs "
+                         f"{L2_BYTES / 2 ** 20:.0f} MiB L2",
+                   "kernels_per_step": info.kernels_per_step},
+        "e2e": {"value": round(ws * K * B / e2e_s, 2), "unit": unit,
+                "h2d_bytes_per_step": int(info.step_h2d_bytes), "d2h_bytes_per_step": int(info.step_d2h_bytes),
+                "steps": K},
+        "roofline": {"bound": "hbm", "kernel": f"frame ({info.kernels_per_step} kernels, one CUDA graph)",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+                     "bytes_per_step": int(bytes_frame), "traffic": None},
+        "prefill": {"ms": round(pf_ms, 3), "positions": run.prompt_len, "rows": B,
+                    "gemm_gflop": round(pf_flops / 1e9, 2),
+                    "gemm_tflops": round(pf_flops / (pf_ms / 1e3) / 1e12, 2),
+                    "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill]},
+        "gpu_launches": int(info.kernels_per_step * K),
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 def load_traffic(config, step_path):
     """Per-step DRAM bytes from the committed ncu summary of this workload and
     step path (graph or persistent kernel), if any."""
@@ -395,7 +492,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=250)
     ap.add_argument("--warmup", type=int, default=25)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", default="gpt2m_q4", choices=["gpt2m_q4", "gpt2m_q8", "llama_q4", "tiny"])
+    ap.add_argument("--config", default="gpt2m_q4",
+                    choices=["gpt2m_q4", "gpt2m_q8", "llama_q4", "tiny", "qwen_a8", "qwen_a8_g16"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
