@@ -232,24 +232,42 @@ def run_gpu(args):
     dec.decode_n(W, s, u_dev, out_dev)
     torch.cuda.synchronize()
 
-    # timed: K steps from position prompt_len
-    dec.reset()
-    dec.prefill(prompt, s, draws[0])
+    # timed: K steps from position prompt_len, repeated; the median repetition is the result
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist, ws)
-    torch.cuda.synchronize()
+    reps = []
     with ClockSampler(local) as clk:
-        torch.cuda.nvtx.range_push("timed")
+        for r in range(args.repeats):
+            dec.reset()
+            dec.prefill(prompt, s, draws[0])
+            barrier(dist, ws)
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("timed")
+            ev0.record(stream)
+            dec.decode_n(K, s, u_dev, out_dev)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
+            barrier(dist, ws)
+            reps.append(max_over_ranks(dist, ws, ev0.elapsed_time(ev1), dev))
+    clocks = clk.summary()
+    ms_max = sorted(reps)[len(reps) // 2]
+    ms = ms_max
+    value = ws * K * B / (ms_max / 1e3)
+
+    # per-step time at the start and at the end of the run's position range (10 steps each)
+    at_pos = {}
+    nfix = min(10, K)
+    for p0 in sorted({run.prompt_len, run.prompt_len + K - nfix}):
+        dec.reset()
+        dec.prefill(prompt, s, draws[0])
+        if p0 > run.prompt_len:
+            dec.decode_n(p0 - run.prompt_len, s, u_dev, out_dev)
+        torch.cuda.synchronize()
         ev0.record(stream)
-        dec.decode_n(K, s, u_dev, out_dev)
+        dec.decode_n(nfix, s, u_dev, out_dev)
         ev1.record(stream)
         torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    barrier(dist, ws)
-    ms = ev0.elapsed_time(ev1)
-    clocks = clk.summary()
-    ms_max = max_over_ranks(dist, ws, ms, dev)
-    value = ws * K * B / (ms_max / 1e3)
+        at_pos[f"pos_{p0}"] = round(ev0.elapsed_time(ev1) / nfix * 1e3, 1)
 
     # end to end through sd_step with host buffers
     dec.reset()
@@ -313,11 +331,14 @@ def run_gpu(args):
                     "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill],
                     "note": "sd_prefill end to end (median of 3): positions 0..P-2 as GEMMs over all rows, "
                             "the last position through the step graph"},
+        "repetitions": {"n": len(reps), "ms_per_step": [round(x / K, 5) for x in reps],
+                        "spread_ms_per_step": round((max(reps) - min(reps)) / K, 5)},
+        "us_per_step_at": at_pos,
         "gpu_launches": 1 if info.persistent else int(info.kernels_per_step * K),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(run, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(run, seconds=args.cpu_seconds, single_core_steps=2)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -423,7 +444,7 @@ def load_traffic(config, step_path):
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
-def cpu_baseline(run, seconds: float = 15.0):
+def cpu_baseline(run, seconds: float = 15.0, single_core_steps: int = 0):
     """The oracle as it stands on the host cores: prompt processed untimed,
     then decode steps timed until about `seconds` of CPU work."""
     import oracle
@@ -451,10 +472,26 @@ def cpu_baseline(run, seconds: float = 15.0):
         if time.perf_counter() - t0 > seconds and n >= 3:
             break
     dt = time.perf_counter() - t0
+    threads = model.threads
+    # the same oracle on one core, a few further steps (same arithmetic, bitwise the same results)
+    single = None
+    if single_core_steps > 0 and n + single_core_steps < run.n_steps:
+        oracle.lib().orc_set_threads(1)
+        t1 = time.perf_counter()
+        for i in range(single_core_steps):
+            for b in range(m.batch):
+                z = model.token_forward(b, tok[b], m.vocab)
+                tok[b] = oracle.sample(z, u=float(draws[n + 1 + i][b]), **sa)[0]
+        single = round(single_core_steps * m.batch / (time.perf_counter() - t1), 3)
+        oracle.lib().orc_set_threads(threads)
     model.close()
-    return {"value": round(n * m.batch / dt, 3), "unit": "tokens/s", "cores": model.threads, "kind": "oracle",
-            "sample": f"{n} decode steps at positions {run.prompt_len}..{run.prompt_len + n - 1} after an untimed "
-                      f"{run.prompt_len}-token prompt, batch {m.batch}, {model.threads} OpenMP threads"}
+    out = {"value": round(n * m.batch / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"{n} decode steps at positions {run.prompt_len}..{run.prompt_len + n - 1} after an untimed "
+                     f"{run.prompt_len}-token prompt, batch {m.batch}, {threads} OpenMP threads"}
+    if single is not None:
+        out["single_core"] = {"value": single, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{single_core_steps} further decode steps on one thread"}
+    return out
 
 
 def run_reference(args):
@@ -495,6 +532,7 @@ def main(argv=None):
     ap.add_argument("--config", default="gpt2m_q4",
                     choices=["gpt2m_q4", "gpt2m_q8", "llama_q4", "tiny", "qwen_a8", "qwen_a8_g16"])
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--repeats", type=int, default=5, help="timed repetitions (the median is reported)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
