@@ -103,6 +103,9 @@ struct sd_ctx {
     int logits_ld = 0, vmax = 0;
     float* ebuf = nullptr;              // [B][d] code-embedding staging (Qwen)
     float* nrm = nullptr;               // [B][max width] normalised rows (B > 2)
+    float* g16_ws = nullptr;            // skinny GEMM partial sums (B > 2)
+    int* g16_cnt = nullptr;             // skinny GEMM column-tile counters (zero between launches)
+    bool rows_gemm_mma = false;         // SD_ROWS_GEMM=mma: the 64x64 mma.sync GEMM for > 2 rows instead
     int32_t* prompt = nullptr;          // [B][max_ctx]
 
     DevState* ds = nullptr;             // device
@@ -226,8 +229,8 @@ int alloc_stack(sd_ctx* c, DStack& s) {
 // ------------------------------------------------------------------ enqueue helpers
 
 // y = W x for the context's rows: the streaming GEMV for 1-2 rows; for more
-// rows (G rollouts) the norm prologue as its own kernel and the tensor-core
-// GEMM with the same epilogue.
+// rows (G rollouts, at most 16) the norm prologue as its own kernel and the
+// skinny split-K tensor-core GEMM with the same epilogue.
 int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
     cudaError_t e;
     if (a.nb <= 2) {
@@ -243,10 +246,17 @@ int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
             x = c->nrm;
             ldx = a.W.cols;
         }
-        QGemmArgs g;
-        g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
-        g.y = a.y; g.ldy = a.y_stride;
-        e = launch_qgemm(g, st);
+        if (c->rows_gemm_mma) {
+            QGemmArgs g;
+            g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
+            g.y = a.y; g.ldy = a.y_stride;
+            e = launch_qgemm(g, st);
+        } else {
+            Gemm16Args g;
+            g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
+            g.y = a.y; g.ldy = a.y_stride; g.ws = c->g16_ws; g.cnt = c->g16_cnt;
+            e = launch_gemm16(g, c->sm_count, st);
+        }
         c->count_launch++;
     }
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
@@ -843,6 +853,33 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     if ((rc = dalloc(c, &c->nrm, sizeof(float) * c->B * std::max(m.d_model, m.arch == SD_ARCH_QWEN_TTS ? m.cp_d_model : 0))))
         return bail(rc);
     if ((rc = dalloc(c, &c->prompt, sizeof(int32_t) * c->B * m.max_ctx))) return bail(rc);
+    if (c->B > 2) {
+        const char* rg = getenv("SD_ROWS_GEMM");
+        c->rows_gemm_mma = rg && strcmp(rg, "mma") == 0;
+        // skinny GEMM workspace: the largest partial-sum array and tile count over every matrix
+        std::vector<std::pair<int, int>> nk;  // (rows, cols)
+        auto stack_mats = [&](int d, int H, int Hkv, int hd, int ff, bool gpt2) {
+            nk.push_back({(H + 2 * Hkv) * hd, d});
+            nk.push_back({d, H * hd});
+            nk.push_back({gpt2 ? ff : 2 * ff, d});
+            nk.push_back({d, ff});
+        };
+        stack_mats(m.d_model, m.n_head, m.n_kv_head, m.head_dim, m.d_ff, m.arch == SD_ARCH_GPT2);
+        nk.push_back({m.vocab, m.d_model});
+        if (m.arch == SD_ARCH_QWEN_TTS) {
+            stack_mats(m.cp_d_model, m.cp_n_head, m.cp_n_kv_head, m.cp_head_dim, m.cp_d_ff, false);
+            nk.push_back({m.cp_d_model, m.d_model});
+            nk.push_back({m.cp_vocab, m.cp_d_model});
+        }
+        size_t wsf = 0;
+        int tiles = 0;
+        for (const auto& p : nk) {
+            wsf = std::max(wsf, gemm16_ws_floats(p.first, p.second, c->sm_count));
+            tiles = std::max(tiles, gemm16_tiles(p.first));
+        }
+        if ((rc = dalloc(c, &c->g16_ws, sizeof(float) * wsf)) || (rc = dalloc(c, &c->g16_cnt, sizeof(int) * tiles)))
+            return bail(rc);
+    }
     {
         // GEMM prefill: SD_PREFILL=steps runs the prompt through the per-position step graphs instead
         const char* e = getenv("SD_PREFILL");
@@ -1143,6 +1180,8 @@ struct sd_qmat {
     void* buf = nullptr;
     int device = 0;
     __half* split = nullptr;  // dequantised fp16 hi [rows][cols] then lo, made on first tensor-core use
+    float* g16_ws = nullptr;  // skinny GEMM partial sums, made on first use
+    int* g16_cnt = nullptr;   // skinny GEMM column-tile counters (zero between launches)
 };
 
 int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int on_device, int device, sd_qmat** out) {
@@ -1193,6 +1232,8 @@ void sd_qmat_destroy(sd_qmat* m) {
     cudaSetDevice(m->device);
     cudaFree(m->buf);
     if (m->split) cudaFree(m->split);
+    if (m->g16_ws) cudaFree(m->g16_ws);
+    if (m->g16_cnt) cudaFree(m->g16_cnt);
     delete m;
 }
 
@@ -1228,6 +1269,30 @@ int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilog
     a.resid = resid_dev; a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows;
     CK(cudaSetDevice(m->device));
     CK(launch_qgemm(a, reinterpret_cast<cudaStream_t>(stream)));
+    return SD_OK;
+}
+
+int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                   const float* resid_dev, float* y_dev, void* stream) {
+    sd_ctx* c = nullptr;
+    if (!m || !x_dev || !y_dev || M < 1 || M > 16 || epilogue < SD_EPI_LINEAR || epilogue > SD_EPI_SWIGLU ||
+        reinterpret_cast<uintptr_t>(x_dev) % 16)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm16: bad argument");
+    if (epilogue == SD_EPI_SWIGLU && (bias_dev || m->m.rows % 2))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_gemm16: SwiGLU needs even rows and no bias");
+    CK(cudaSetDevice(m->device));
+    int sms = 0;
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, m->device));
+    if (!m->g16_ws) {
+        CK(cudaMalloc(&m->g16_ws, sizeof(float) * gemm16_ws_floats(m->m.rows, m->m.cols, sms)));
+        CK(cudaMalloc(&m->g16_cnt, sizeof(int) * gemm16_tiles(m->m.rows)));
+        CK(cudaMemset(m->g16_cnt, 0, sizeof(int) * gemm16_tiles(m->m.rows)));
+    }
+    Gemm16Args a;
+    a.W = m->m; a.M = M; a.x = x_dev; a.ldx = m->m.cols; a.epi = epilogue; a.bias = bias_dev;
+    a.resid = resid_dev; a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows;
+    a.ws = m->g16_ws; a.cnt = m->g16_cnt;
+    CK(launch_gemm16(a, sms, reinterpret_cast<cudaStream_t>(stream)));
     return SD_OK;
 }
 

@@ -230,6 +230,29 @@ struct QGemmArgs {
 };
 cudaError_t launch_qgemm(const QGemmArgs& a, cudaStream_t st);
 
+// Skinny split-K tensor-core GEMM for M <= 16 rows (the same operation and
+// epilogues as QGemm).  x must be 16-byte aligned with ldx a multiple of 4.
+// ws holds gemm16_ws_floats(N, K) floats of partial sums; cnt holds
+// gemm16_tiles(N) ints, zero before the launch and zero again after it (one
+// launch at a time may use a given cnt).
+struct Gemm16Args {
+    QMat W;
+    int M = 0;
+    const float* x = nullptr;      // [M][ldx]
+    int ldx = 0;
+    int epi = EPI_LINEAR;
+    const float* bias = nullptr;
+    const float* resid = nullptr;  // may alias y
+    float* y = nullptr;
+    int ldy = 0;
+    float* ws = nullptr;
+    int* cnt = nullptr;
+    int k_per = 0;                 // set by the launcher
+};
+size_t gemm16_ws_floats(int N, int K, int sm_count);
+int gemm16_tiles(int N);
+cudaError_t launch_gemm16(Gemm16Args a, int sm_count, cudaStream_t st);
+
 // Tensor-core (tcgen05) GEMM for prefill: fp16 hi/lo operands loaded by TMA
 // through 2-D tensor maps ([rows][K] fp16, K a multiple of 64), three MMAs per
 // K step, the QGemm epilogues.

@@ -27,7 +27,7 @@ MAX_CODEBOOKS = 16
 # every symbol the headers declare
 EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes",
            "sd_decode_n", "sd_get_logits", "sd_reset", "sd_destroy", "sd_last_error", "sd_get_info",
-           "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm_tc", "sd_sample_rows",
+           "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm16", "sd_qmat_gemm_tc", "sd_sample_rows",
            "sd_attend_rows", "sd_attend_rows_static"]
 
 
@@ -96,6 +96,7 @@ def load_library(path: str | None = None):
         "sd_qmat_dequant": ([vp, vp, vp], C.c_int),
         "sd_qmat_gemv": ([vp, vp, i32, vp, vp, vp], C.c_int),
         "sd_qmat_gemm": ([vp, vp, i32, i32, vp, vp, vp, vp], C.c_int),
+        "sd_qmat_gemm16": ([vp, vp, i32, i32, vp, vp, vp, vp], C.c_int),
         "sd_qmat_gemm_tc": ([vp, vp, i32, i32, vp, vp, vp, vp], C.c_int),
         "sd_sample_rows": ([vp, i32, i32, C.POINTER(Sampler), vp, vp, vp], C.c_int),
         "sd_attend_rows": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp], C.c_int),
@@ -256,6 +257,11 @@ EPI_LINEAR, EPI_GELU, EPI_SWIGLU = 0, 1, 2
 def sd_qmat_gemm(m: int, x_dev, M: int, epilogue: int, bias_dev, resid_dev, y_dev, stream=None) -> None:
     _check(load_library().sd_qmat_gemm(m, _ptr(x_dev), M, epilogue, _ptr(bias_dev), _ptr(resid_dev), _ptr(y_dev),
                                        stream), None)
+
+
+def sd_qmat_gemm16(m: int, x_dev, M: int, epilogue: int, bias_dev, resid_dev, y_dev, stream=None) -> None:
+    _check(load_library().sd_qmat_gemm16(m, _ptr(x_dev), M, epilogue, _ptr(bias_dev), _ptr(resid_dev),
+                                         _ptr(y_dev), stream), None)
 
 
 def sd_qmat_gemm_tc(m: int, x_dev, M: int, epilogue: int, bias_dev, resid_dev, y_dev, stream=None) -> None:

@@ -71,6 +71,20 @@ int sd_qmat_gemm(const sd_qmat* m, const float* x_dev, int32_t M, int32_t epilog
 int sd_qmat_gemm_tc(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
                     const float* resid_dev, float* y_dev, void* stream);
 
+/* As sd_qmat_gemm for 1 <= M <= 16 rows (the G rollouts of "Every Frame Is a
+ * Memory Read", section 8, which share one read of the weights per step):
+ * the form the decode step uses for more than two rows.  The weights stream
+ * once from memory straight into the tensor cores (mma.sync m16n8k16, the same
+ * exact-code / fp16 hi+lo / fp32-scale arithmetic); K is split over CTAs and
+ * the partial sums are added in a fixed order, so results are reproducible.
+ * x_dev must be 16-byte aligned.  A workspace of partial sums and column-tile
+ * counters is kept with the matrix (allocated on the first call, at most
+ * 16 * rows * cols / 32 floats).  Calls on one matrix must not run
+ * concurrently on different streams.  Returns SD_ERR_INVALID_ARG on a NULL
+ * pointer, M outside [1, 16], a bad epilogue or a misaligned x_dev. */
+int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, const float* bias_dev,
+                   const float* resid_dev, float* y_dev, void* stream);
+
 /* Sample one token per row from logits_dev[rows][V] with draws u_dev[rows];
  * tokens to out_dev[rows].  Sampler semantics as in sd.h.  V <= 16384. */
 int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,

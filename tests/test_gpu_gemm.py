@@ -41,7 +41,7 @@ def _silu(t):
     return t / (1.0 + np.exp(-t))
 
 
-def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed, tc=False):
+def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed, tc=False, g16=False):
     rng = np.random.default_rng(seed)
     w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
     canon, abias = _canon(kind, w)
@@ -55,10 +55,17 @@ def _run(sd, kind, rows, cols, M, epi, with_bias, with_resid, seed, tc=False):
         xd = torch.from_numpy(x).cuda()
         bd = torch.from_numpy(bias).cuda() if bias is not None else None
         yd = torch.from_numpy(resid).cuda() if resid is not None else torch.empty(M, out_cols, device="cuda")
-        gemm = sd.sd_qmat_gemm_tc if tc else sd.sd_qmat_gemm
+        gemm = sd.sd_qmat_gemm_tc if tc else (sd.sd_qmat_gemm16 if g16 else sd.sd_qmat_gemm)
+        y0 = yd.clone()
         gemm(h, xd, M, epi, bd, yd if resid is not None else None, yd)
         torch.cuda.synchronize()
         y = yd.cpu().numpy().astype(np.float64)
+        if g16:
+            # the split-K partial sums are added in a fixed order: a second call gives the same bits
+            yd.copy_(y0)
+            gemm(h, xd, M, epi, bd, yd if resid is not None else None, yd)
+            torch.cuda.synchronize()
+            assert np.array_equal(yd.cpu().numpy().astype(np.float64), y)
     finally:
         sd.sd_qmat_destroy(h)
     deq = oracle.dequant(kind, canon, rows, cols).astype(np.float64)
@@ -180,3 +187,45 @@ def test_gemm_tc_rejects_unaligned_k(sd):
     finally:
         sd.sd_qmat_destroy(h)
 
+
+
+G16_SHAPES = [(KQ8, (3072, 1024)), (KQ8, (200, 96)), (KQ8, (64, 32)), (KQ8, (1024, 4096)),
+              (KQ4, (3072, 1024)), (KQ4, (200, 96)), (KQ4, (1024, 4096)), (KQ4, (130, 1088)),
+              (KA8, (4096, 2048)), (KA8, (2048, 6144)), (KA8, (1024, 3072)), (KA8, (130, 128)), (KA8, (3072, 1024))]
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("kind,shape", G16_SHAPES)
+def test_gemm16_linear_bias(sd, kind, shape, M):
+    """The skinny split-K GEMM: row counts up to 16 (one or both MMA row halves),
+    ragged column tiles (200, 130 rows), K ranges that are and are not multiples
+    of 64, one split (K = 32) up to many."""
+    rows, cols = shape
+    _run(sd, kind, rows, cols, M, 0, True, False, rows + cols + M + kind + 31, g16=True)
+
+
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+@pytest.mark.parametrize("M", [5, 16])
+def test_gemm16_epilogues(sd, kind, M):
+    cols = 1024 if kind != KA8 else 2048
+    _run(sd, kind, 4096, cols, M, 1, True, False, 41 + M + kind, g16=True)
+    _run(sd, kind, 1024, cols, M, 0, True, True, 42 + M + kind, g16=True)
+    _run(sd, kind, 8192 if kind != KA8 else 12288, cols, M, 2, False, False, 43 + M + kind, g16=True)
+    _run(sd, kind, 66, 128, M, 2, False, True, 44 + M + kind, g16=True)
+
+
+def test_gemm16_rejects_bad_arguments(sd):
+    w = (np.random.default_rng(0).standard_normal((64, 64)) * 0.02).astype(np.float32)
+    canon, _ = _canon(KQ8, w)
+    h = sd.sd_qmat_create(KQ8, canon, 64, 64)
+    try:
+        x = torch.zeros(20, 64, device="cuda")
+        y = torch.zeros(20, 64, device="cuda")
+        b = torch.zeros(64, device="cuda")
+        xm = torch.zeros(4 * 64 + 1, device="cuda")[1:]       # not 16-byte aligned
+        for args in [(x, 17, 0, None, None, y), (x, 0, 0, None, None, y), (x, 4, 3, None, None, y),
+                     (x, 4, 2, b, None, y), (xm, 4, 0, None, None, y)]:
+            with pytest.raises(sd.SdError):
+                sd.sd_qmat_gemm16(h, *args)
+    finally:
+        sd.sd_qmat_destroy(h)
