@@ -285,64 +285,93 @@ __device__ __forceinline__ Slice slice_at(const StepArgs& a, const StepLayer* ta
 // ------------------------------------------------------------------ compute helpers
 
 // LayerNorm (biased variance) or RMSNorm of the padded rows x[b][pidx(0..K)),
-// b < NB, written to xn (same layout).  Every warp computes the row statistics
-// itself (a full pass over the row in shared memory, conflict-free 16-byte
-// loads, xor-shuffle sums in a fixed order); x is not overwritten, so the only
-// block barrier is the one that publishes xn.
+// b < NB, written to xn (same layout).  Each thread holds at most two float4
+// of a row in registers (K <= 4096), so the row is read from shared memory
+// once; the sums go through warp shuffles and a 16-entry table per row in
+// `red` (>= 2 * NB * 16 floats, 16-byte aligned) in a fixed order.  LayerNorm
+// is two-pass: the mean first, then the squared deviations of the held values.
 template <int NB>
-__device__ void norm_to(const float* x, float* xn, int K, bool ln, const float* g, const float* gb, float eps) {
-    const int KP = padded(K), lane = threadIdx.x & 31, K4 = K >> 2;
-    float mu[NB], rs[NB];
+__device__ void norm_to(const float* x, float* xn, int K, bool ln, const float* g, const float* gb, float eps,
+                        float* red) {
+    constexpr int V = 2;
+    const int KP = padded(K), K4 = K >> 2, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float4 v[NB][V];
+    auto table_sum = [&](const float* t) {
+        const float4* r4 = reinterpret_cast<const float4*>(t);
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps / 4; ++w) {
+            const float4 q = r4[w];
+            tot += (q.x + q.y) + (q.z + q.w);
+        }
+        return tot;
+    };
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-        const float4* r4 = reinterpret_cast<const float4*>(x + b * KP);
-        float s0 = 0.f, s1 = 0.f;
-        for (int k4 = lane; k4 < K4; k4 += 32) {
-            const float4 v = r4[k4 + (k4 >> 3)];
-            if (ln) { s0 += v.x + v.y; s1 += v.z + v.w; }
-            else { s0 = fmaf(v.x, v.x, fmaf(v.y, v.y, s0)); s1 = fmaf(v.z, v.z, fmaf(v.w, v.w, s1)); }
-        }
-        float t = s0 + s1;
+        float s = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (ln) {
-            mu[b] = t / (float)K;
-            float q0 = 0.f, q1 = 0.f;
-            for (int k4 = lane; k4 < K4; k4 += 32) {
-                const float4 v = r4[k4 + (k4 >> 3)];
-                const float a0 = v.x - mu[b], a1 = v.y - mu[b], a2 = v.z - mu[b], a3 = v.w - mu[b];
-                q0 = fmaf(a0, a0, fmaf(a1, a1, q0));
-                q1 = fmaf(a2, a2, fmaf(a3, a3, q1));
+        for (int j = 0; j < V; ++j) {
+            const int k4 = tid + j * kThreads;
+            v[b][j] = k4 < K4 ? reinterpret_cast<const float4*>(x + b * KP)[k4 + (k4 >> 3)]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 q = v[b][j];
+            if (ln) s += (q.x + q.y) + (q.z + q.w);
+            else s += fmaf(q.x, q.x, q.y * q.y) + fmaf(q.z, q.z, q.w * q.w);
+        }
+        s = warp_sum(s);
+        if (lane == 0) red[b * kWarps + warp] = s;
+    }
+    csync();
+    float mu[NB], ms[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float tot = table_sum(red + b * kWarps);
+        mu[b] = ln ? tot / (float)K : 0.f;
+        ms[b] = tot / (float)K;
+    }
+    if (ln) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float q = 0.f;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                if (tid + j * kThreads >= K4) continue;
+                const float a0 = v[b][j].x - mu[b], a1 = v[b][j].y - mu[b];
+                const float a2 = v[b][j].z - mu[b], a3 = v[b][j].w - mu[b];
+                q += fmaf(a0, a0, a1 * a1) + fmaf(a2, a2, a3 * a3);
             }
-            float q = q0 + q1;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-            rs[b] = 1.0f / sqrtf(q / (float)K + eps);
-        } else {
-            mu[b] = 0.f;
-            rs[b] = 1.0f / sqrtf(t / (float)K + eps);
+            q = warp_sum(q);
+            if (lane == 0) red[(NB + b) * kWarps + warp] = q;
         }
+        csync();
+#pragma unroll
+        for (int b = 0; b < NB; ++b) ms[b] = table_sum(red + (NB + b) * kWarps) / (float)K;
     }
     const float4* g4 = reinterpret_cast<const float4*>(g);
     const float4* b4 = reinterpret_cast<const float4*>(gb);
-    for (int i = threadIdx.x; i < NB * K4; i += kThreads) {
-        const int b = i / K4, k4 = i - b * K4;
-        const int pi = (b * KP >> 2) + k4 + (k4 >> 3);
-        float4 v = reinterpret_cast<const float4*>(x)[pi];
-        const float4 gg = g4[k4];
-        if (ln) {
-            const float4 oo = b4[k4];
-            v.x = fmaf((v.x - mu[b]) * rs[b], gg.x, oo.x);
-            v.y = fmaf((v.y - mu[b]) * rs[b], gg.y, oo.y);
-            v.z = fmaf((v.z - mu[b]) * rs[b], gg.z, oo.z);
-            v.w = fmaf((v.w - mu[b]) * rs[b], gg.w, oo.w);
-        } else {
-            v.x = v.x * rs[b] * gg.x;
-            v.y = v.y * rs[b] * gg.y;
-            v.z = v.z * rs[b] * gg.z;
-            v.w = v.w * rs[b] * gg.w;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float rs = 1.0f / sqrtf(ms[b] + eps);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k4 = tid + j * kThreads;
+            if (k4 >= K4) continue;
+            const float4 gg = g4[k4];
+            float4 o = v[b][j];
+            if (ln) {
+                const float4 oo = b4[k4];
+                o.x = fmaf((o.x - mu[b]) * rs, gg.x, oo.x);
+                o.y = fmaf((o.y - mu[b]) * rs, gg.y, oo.y);
+                o.z = fmaf((o.z - mu[b]) * rs, gg.z, oo.z);
+                o.w = fmaf((o.w - mu[b]) * rs, gg.w, oo.w);
+            } else {
+                o.x = o.x * rs * gg.x;
+                o.y = o.y * rs * gg.y;
+                o.z = o.z * rs * gg.z;
+                o.w = o.w * rs * gg.w;
+            }
+            reinterpret_cast<float4*>(xn + b * KP)[k4 + (k4 >> 3)] = o;
         }
-        reinterpret_cast<float4*>(xn)[pi] = v;
     }
     csync();
 }
@@ -384,7 +413,10 @@ __device__ __forceinline__ float dot4_s8(const uint4 w, const float* x) {
 // y[i * NB + b] = sum_k W[r0 + i][k] x[b][k] for i < nr, with the codes and
 // scales of rows r0.. in shared memory.  Warp layout as the streaming GEMV: a
 // warp owns a 1024-element K slice (lane activations in registers) and visits
-// rows rg, rg + WR, ...; the WK slices of a row meet in s_part in fixed order.
+// rows rg, rg + WR, ... two at a time (independent chains); only warps that
+// own a row load the activations.  With one K slice (K <= 1024) lane 0 writes
+// the row sums directly; otherwise the WK slices of a row meet in s_part in
+// fixed order.
 template <int QK, int NB>
 __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr, const float* x, float* s_part,
                          float* s_y) {
@@ -396,7 +428,7 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
     const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
     const int spr = K >> 5;
     const int KP = padded(K);  // x rows are in the padded layout
-    if (rg < WR) {
+    if (rg < WR && rg < nr) {
         float xr[NB][32];
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -412,38 +444,70 @@ __device__ void gemv_rec(const uint8_t* codes, const uint8_t* sc, int K, int nr,
                     xr[b][u * EPU + j + 2] = v.z; xr[b][u * EPU + j + 3] = v.w;
                 }
             }
-        for (int i = rg; i < nr; i += WR) {
-            float acc[NB];
+        for (int i = rg; i < nr; i += 2 * WR) {
+            const int i2 = i + WR;
+            const bool two = i2 < nr;  // warp-uniform
+            float acc0[NB], acc1[NB];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+            for (int b = 0; b < NB; ++b) {
+                acc0[b] = 0.f;
+                acc1[b] = 0.f;
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
                 if (e < K) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(codes + (size_t)i * row_bytes +
-                                                                     ((QK == SD_Q4_0) ? (e >> 1) : e));
-                    const float dq = __half2float(reinterpret_cast<const __half*>(sc)[(size_t)i * spr + (e >> 5)]);
+                    const int off = (QK == SD_Q4_0) ? (e >> 1) : e;
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(codes + (size_t)i * row_bytes + off);
+                    const float d0 = __half2float(reinterpret_cast<const __half*>(sc)[(size_t)i * spr + (e >> 5)]);
+                    uint4 w1 = make_uint4(0u, 0u, 0u, 0u);
+                    float d1 = 0.f;
+                    if (two) {
+                        w1 = *reinterpret_cast<const uint4*>(codes + (size_t)i2 * row_bytes + off);
+                        d1 = __half2float(reinterpret_cast<const __half*>(sc)[(size_t)i2 * spr + (e >> 5)]);
+                    }
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float t = (QK == SD_Q4_0) ? dot4_q4(w, &xr[b][0]) : dot4_s8(w, &xr[b][u * EPU]);
-                        acc[b] = fmaf(dq, t, acc[b]);
+                        const float t0 = (QK == SD_Q4_0) ? dot4_q4(w0, &xr[b][0]) : dot4_s8(w0, &xr[b][u * EPU]);
+                        acc0[b] = fmaf(d0, t0, acc0[b]);
+                        if (two) {
+                            const float t1 =
+                                (QK == SD_Q4_0) ? dot4_q4(w1, &xr[b][0]) : dot4_s8(w1, &xr[b][u * EPU]);
+                            acc1[b] = fmaf(d1, t1, acc1[b]);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float v = warp_sum(acc[b]);
-                if (lane == 0) s_part[(i * NB + b) * WK + kw] = v;
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    acc0[b] += __shfl_xor_sync(0xffffffffu, acc0[b], o);
+                    acc1[b] += __shfl_xor_sync(0xffffffffu, acc1[b], o);
+                }
+            if (lane == 0) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    if (WK == 1) {
+                        s_y[i * NB + b] = acc0[b];
+                        if (two) s_y[i2 * NB + b] = acc1[b];
+                    } else {
+                        s_part[(i * NB + b) * WK + kw] = acc0[b];
+                        if (two) s_part[(i2 * NB + b) * WK + kw] = acc1[b];
+                    }
+                }
             }
         }
     }
     csync();
-    for (int t = threadIdx.x; t < nr * NB; t += kThreads) {
-        float v = 0.f;
-        for (int k = 0; k < WK; ++k) v += s_part[t * WK + k];
-        s_y[t] = v;
+    if (WK > 1) {
+        for (int t = threadIdx.x; t < nr * NB; t += kThreads) {
+            float v = 0.f;
+            for (int k = 0; k < WK; ++k) v += s_part[t * WK + k];
+            s_y[t] = v;
+        }
+        csync();
     }
-    csync();
 }
 
 // Attention splits for n = pos + 1 keys: at most max_split chunks of about
@@ -456,27 +520,119 @@ __device__ __forceinline__ void attn_split(const StepArgs& a, int n, int& S, int
     S = (n + chunk - 1) / chunk;
 }
 
+// One warp's share of an attention sub-chunk: keys 0..cnt-1 of the staged
+// rows Kw (pitch HD + 8 halves) and Vw (pitch HD), lane = key for the scores,
+// lanes over dimensions for p V; the running (o, m, l) of query head h is
+// updated in place in st + h * (HD + 2).  Loops have fixed trip counts so
+// loads and shuffles pipeline; staged rows past cnt are never multiplied (they
+// may hold any bits, and 0 * inf is not 0).
+template <int HD>
+__device__ __forceinline__ void attn_warp(const float* q, const __half* Kw, const __half* Vw, float* st, int HPG,
+                                          int cnt) {
+    constexpr int DPL = HD / 32, W = HD + 2;
+    const int lane = threadIdx.x & 31;
+    const bool valid = lane < cnt;
+    const __half* kr = Kw + lane * (HD + 8);  // rows >= cnt are staging space: read, then masked
+    for (int h = 0; h < HPG; ++h) {
+        float* r = st + h * W;
+        const float4* q4 = reinterpret_cast<const float4*>(q + h * HD);
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int d8 = 0; d8 < HD; d8 += 8) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(kr + d8);
+            const float4 qa = q4[d8 >> 2], qb = q4[(d8 >> 2) + 1];
+            const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
+            const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
+            const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
+            const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
+            s0 = fmaf(qa.x, k0.x, s0);
+            s1 = fmaf(qa.y, k0.y, s1);
+            s2 = fmaf(qa.z, k1.x, s2);
+            s3 = fmaf(qa.w, k1.y, s3);
+            s0 = fmaf(qb.x, k2.x, s0);
+            s1 = fmaf(qb.y, k2.y, s1);
+            s2 = fmaf(qb.z, k3.x, s2);
+            s3 = fmaf(qb.w, k3.y, s3);
+        }
+        const float sc = valid ? (s0 + s1) + (s2 + s3) : -INFINITY;
+        float mx = sc;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        const float mold = r[HD];
+        const float mnew = fmaxf(mold, mx);
+        const float p = valid ? expf(sc - mnew) : 0.f;
+        const float corr = expf(mold - mnew);
+        const float ps = warp_sum(p);
+        float ov[DPL];
+#pragma unroll
+        for (int dd = 0; dd < DPL; ++dd) ov[dd] = 0.f;
+        const __half* vr = Vw + lane * DPL;
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, p, jj);
+            if (jj >= cnt) continue;  // rows past the warp's keys hold stale staging data (warp-uniform)
+            if (DPL == 2) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2*>(vr + jj * HD));
+                ov[0] = fmaf(pj, v.x, ov[0]);
+                ov[1] = fmaf(pj, v.y, ov[1]);
+            } else {
+                const uint2 vv = *reinterpret_cast<const uint2*>(vr + jj * HD);
+                const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
+                const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
+                ov[0] = fmaf(pj, v0.x, ov[0]);
+                ov[1] = fmaf(pj, v0.y, ov[1]);
+                ov[DPL - 2] = fmaf(pj, v1.x, ov[DPL - 2]);
+                ov[DPL - 1] = fmaf(pj, v1.y, ov[DPL - 1]);
+            }
+        }
+        float* ro = r + lane * DPL;
+#pragma unroll
+        for (int dd = 0; dd < DPL; ++dd) ro[dd] = fmaf(ro[dd], corr, ov[dd]);
+        __syncwarp();
+        if (lane == 0) {
+            r[HD] = mnew;
+            r[HD + 1] = fmaf(r[HD + 1], corr, ps);
+        }
+        __syncwarp();
+    }
+}
+
 // One attention item: row b, kv head g, keys [c0, c1) of n = pos + 1.  Writes
 // the unnormalised partial o (per query head of the group) with its running
-// max m and sum l.  sm: the activation region (>= attn_smem_floats).
+// max m and sum l.  sm: the activation region (>= the attention floats of
+// act_region_bytes).
+//
+// Keys are staged kKC at a time (cp.async, issued before the wait for q).
+// Four warps own 32 keys each, lane = key: a lane forms its key's score with
+// the whole head dimension (no shuffles; staged key rows are (hd + 8) halves
+// apart so that the lanes' rows fall in distinct banks), the warp keeps an
+// online softmax (m, l) and accumulates p V with lanes over dimensions.  The
+// four warp partials are combined in shared memory and published.
 __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, int chunk, int pos, unsigned e,
-                          float* sm, int* err, size_t rs_qkv, size_t rs_part) {
+                          float* sm, int* err, size_t rs_qkv, size_t rs_part, unsigned long long* tr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // cycle stamps of the sub-steps (traced CTA, thread 0): tr[k] += cycles since the previous stamp
+    long long tc = (tr && tid == 0) ? clock64() : 0;
+    auto stamp = [&](int k) {
+        if (tr && tid == 0) {
+            const long long t = clock64();
+            tr[k] += (unsigned long long)(t - tc);
+            tc = t;
+        }
+    };
+    constexpr int kAW = kKC / 32;        // warps that own keys
     const int hd = a.hd, half = hd >> 1, HPG = a.H / a.Hkv, n = pos + 1;
     const int qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
     const int c0 = c * chunk, c1 = min(n, c0 + chunk);
     const bool last = c1 == n;
+    const int KP = hd + 8;               // staged key row pitch (halves)
+    const int W = hd + 2;                // partial record: o[hd], m, l
     float* q = sm;                       // [HPG][hd]
     float* kn = q + HPG * hd;            // [hd]
     float* vn = kn + hd;                 // [hd]
-    float* o = vn + hd;                  // [HPG][hd]
-    float* sc = o + HPG * hd;            // [HPG][kKC] scores, then probabilities
-    float* mm = sc + HPG * kKC;          // [HPG] running max
-    float* ls = mm + kMaxHPG;            // [HPG] running sum
-    float* cr = ls + kMaxHPG;            // [HPG] rescale of this sub-chunk
-    float* op = cr + kMaxHPG;            // [kThreads] PV partials
-    __half* Ks = reinterpret_cast<__half*>(op + kThreads);  // [kKC][hd] (16-byte aligned: see attn_floats)
-    __half* Vs = Ks + kKC * hd;                               // [kKC][hd]
+    float* wp = vn + hd;                 // [kAW][HPG][W] warp partials
+    __half* Ks = reinterpret_cast<__half*>(wp + kAW * HPG * W);  // [kKC][KP] (16-byte aligned: see act_region_bytes)
+    __half* Vs = Ks + kKC * KP;                                   // [kKC][hd]
     const size_t hb = ((size_t)(b * a.n_layer * a.Hkv + l * a.Hkv + g) * a.n_ctx) * hd;
     const __half* Kg = a.kc + hb;
     const __half* Vg = a.vc + hb;
@@ -489,12 +645,11 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         const int nu = (j1 - j0) * u16;
         for (int t = tid; t < 2 * nu; t += kThreads) {
             const bool isv = t >= nu;
-            const int uu = isv ? t - nu : t;
-            if (j0 + uu / u16 == pos) continue;
-            const void* src = reinterpret_cast<const uint4*>((isv ? Vg : Kg) + (size_t)j0 * hd) + uu;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(reinterpret_cast<uint4*>(isv ? Vs : Ks) + uu)),
-                         "l"(src)
-                         : "memory");
+            const int uu = isv ? t - nu : t, r = uu / u16, un = uu - r * u16;
+            if (j0 + r == pos) continue;
+            const __half* src = (isv ? Vg : Kg) + (size_t)(j0 + r) * hd + un * 8;
+            __half* dst = isv ? Vs + r * hd + un * 8 : Ks + r * KP + un * 8;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -509,6 +664,7 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
                              a.spin_budget);
     }
     if (!csync_and(ok)) return false;
+    stamp(0);
     // RoPE (NEOX half split) at pos on q and the new k; q scaled by 1/sqrt(hd)
     const float scale = 1.0f / sqrtf((float)hd);
     for (int i = tid; i < (HPG + 1) * half; i += kThreads) {
@@ -529,11 +685,6 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
         v[dd] = x0;
         v[dd + half] = x1;
     }
-    for (int t = tid; t < HPG * hd; t += kThreads) o[t] = 0.f;
-    if (tid < HPG) {
-        mm[tid] = -INFINITY;
-        ls[tid] = 0.f;
-    }
     csync();
     if (last) {
         // append the new position to the cache (fp16, round to nearest); the fence after
@@ -544,104 +695,62 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
             a.vc[hb + (size_t)pos * hd + dd] = __float2half_rn(vn[dd]);
         }
     }
-    const int npair = HPG * hd, ng = kThreads / npair;  // PV: ng key groups per (head, dim)
+    const int DPL = hd >> 5;  // value dimensions per lane (2 or 4)
+    // the warps' running state (o, m, l) per query head lives in their partial slots
+    if (warp < kAW)
+        for (int h = 0; h < HPG; ++h) {
+            float* r = wp + (warp * HPG + h) * W;
+            for (int dd = lane; dd < hd; dd += 32) r[dd] = 0.f;
+            if (lane == 0) {
+                r[hd] = -INFINITY;
+                r[hd + 1] = 0.f;
+            }
+        }
     for (int j0 = c0; j0 < c1; j0 += kKC) {
         const int j1 = min(c1, j0 + kKC), nk = j1 - j0;
         if (j0 != c0) {
             csync();
             stage(j0, j1);
         }
+        stamp(1);
         stage_wait();
         if (pos >= j0 && pos < j1)
             for (int dd = tid; dd < hd; dd += kThreads) {
-                Ks[(pos - j0) * hd + dd] = __float2half_rn(kn[dd]);
+                Ks[(pos - j0) * KP + dd] = __float2half_rn(kn[dd]);
                 Vs[(pos - j0) * hd + dd] = __float2half_rn(vn[dd]);
             }
         csync();
-        // scores: a warp per key, lanes over dimensions; four keys at a time so that
-        // their shuffle reductions overlap
-        for (int h = 0; h < HPG; ++h) {
-            float qv[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) qv[t] = (lane + 32 * t < hd) ? q[h * hd + lane + 32 * t] : 0.f;
-            for (int jb = warp; jb < nk; jb += 4 * kWarps) {
-                float sv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int jj = jb + u * kWarps;
-                    float acc = 0.f;
-                    if (jj < nk) {
-#pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            if (lane + 32 * t < hd) acc = fmaf(qv[t], __half2float(Ks[jj * hd + lane + 32 * t]), acc);
-                    }
-                    sv[u] = acc;
-                }
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) sv[u] += __shfl_xor_sync(0xffffffffu, sv[u], o2);
-                if (lane == 0)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (jb + u * kWarps < nk) sc[h * kKC + jb + u * kWarps] = sv[u];
-            }
+        stamp(2);
+        if (warp < kAW && warp * 32 < nk) {
+            if (hd == 64) attn_warp<64>(q, Ks + warp * 32 * KP, Vs + warp * 32 * hd, wp + warp * HPG * W, HPG,
+                                        min(32, nk - warp * 32));
+            else attn_warp<128>(q, Ks + warp * 32 * KP, Vs + warp * 32 * hd, wp + warp * HPG * W, HPG,
+                                min(32, nk - warp * 32));
         }
-        csync();
-        // online softmax per head (warp h)
-        if (warp < HPG) {
-            const int h = warp;
-            float mx = -INFINITY;
-            for (int jj = lane; jj < nk; jj += 32) mx = fmaxf(mx, sc[h * kKC + jj]);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-            const float mnew = fmaxf(mm[h], mx);
-            float ps = 0.f;
-            for (int jj = lane; jj < nk; jj += 32) {
-                const float p = expf(sc[h * kKC + jj] - mnew);
-                sc[h * kKC + jj] = p;
-                ps += p;
-            }
-            ps = warp_sum(ps);
-            if (lane == 0) {
-                const float corr = expf(mm[h] - mnew);
-                cr[h] = corr;
-                ls[h] = ls[h] * corr + ps;
-                mm[h] = mnew;
-            }
-        }
-        csync();
-        // PV: thread (group kg, pair t) sums keys kg, kg + ng, ...
-        if (tid < ng * npair) {
-            const int kg = tid / npair, t = tid - kg * npair, h = t / hd, dd = t - h * hd;
-            float acc = 0.f;
-            for (int jj = kg; jj < nk; jj += ng) acc = fmaf(sc[h * kKC + jj], __half2float(Vs[jj * hd + dd]), acc);
-            op[tid] = acc;
-        }
-        csync();
-        // the last sub-chunk's update is the partial itself: publish (o[hd], m, l) per query
-        // head of the group as it is formed
-        const bool fin = j1 == c1;
-        const int W = hd + 2;
-        for (int t = tid; t < npair; t += kThreads) {
-            float acc = 0.f;
-            for (int kg = 0; kg < ng; ++kg) acc += op[kg * npair + t];
-            const float ov = o[t] * cr[t / hd] + acc;
-            o[t] = ov;
-            if (fin) {
-                const int h = t / hd, k = t - h * hd;
-                ll_store_rep(a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k), rs_part, ov,
-                             e);
-            }
-        }
-        if (fin && tid < 2 * HPG) {
-            const int h = tid >> 1, k = hd + (tid & 1);
-            ll_store_rep(a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k), rs_part,
-                         (tid & 1) ? ls[h] : mm[h], e);
-        }
+        stamp(3);
     }
+    csync();
+    stamp(4);
+    for (int t = tid; t < HPG * (hd + 2); t += kThreads) {
+        const int h = t / (hd + 2), k = t - h * (hd + 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAW; ++w) M = fmaxf(M, wp[(w * HPG + h) * W + hd]);
+        float v = M;
+        if (k != hd) {
+            v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kAW; ++w) {
+                const float mw = wp[(w * HPG + h) * W + hd];
+                if (mw != -INFINITY) v = fmaf(expf(mw - M), wp[(w * HPG + h) * W + k], v);
+            }
+        }
+        ll_store_rep(a.ll_part + (((size_t)(b * a.H + g * HPG + h) * a.max_split + c) * W + k), rs_part, v, e);
+    }
+    stamp(5);
     if (last) __threadfence();
     csync();
+    stamp(6);
     return true;
 }
 
@@ -661,9 +770,10 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     __shared__ int s_nc;               // records consumed (compute thread 0 -> producer)
     __shared__ int s_done;             // compute threads finished (normally or on an error)
     __shared__ float s_own[NB * kMaxOwn];
+    __shared__ unsigned long long s_trc[16];  // traced CTA: sub-step cycle sums (thread 0), flushed at the end
     __shared__ float s_part[kMaxPart];
     __shared__ float s_y[kMaxPart];
-    __shared__ float s_red[33 * NB + 8];
+    __shared__ __align__(16) float s_red[33 * NB + 8];
     __shared__ sample_detail::SampleScratch s_samp;
     __shared__ Slice s_geo[5];
 
@@ -690,6 +800,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
         s_nc = 0;
         s_done = 0;
     }
+    if (tid < 16) s_trc[tid] = 0ull;
     __syncthreads();
 
     // ---- producer warp: streams this CTA's weight records into the ring, as
@@ -776,6 +887,15 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
         ++nc;
         if (tid == 0) *reinterpret_cast<volatile int*>(&s_nc) = nc;
     };
+    // publish stamps (trace_pub): latest and earliest CTA per (step, layer, phase)
+    auto tr_pub = [&](int s_, int l_, int ph) {
+        if (a.trace_pub && tid == 0 && s_ < kTraceSteps) {
+            const unsigned long long t = gtime();
+            const size_t i = ((size_t)s_ * L + l_) * kTracePhases + ph;
+            atomicMax(a.trace_pub + i, t);
+            atomicMin(a.trace_pub + (size_t)kTraceSteps * L * kTracePhases + i, t);
+        }
+    };
     auto tr_begin = [&]() { if (a.trace && cta == 0 && tid == 0) { t_a = gtime(); t_w = 0; } };
     auto tr_waited = [&]() { if (a.trace && cta == 0 && tid == 0) t_b = gtime(); };
     auto tr_end = [&](int kind) {
@@ -841,6 +961,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                 if (!(ok = csync_and(okr) != 0)) break;
             }
             tr_waited();
+            tr_pub(s, l, 0);
             {
                 // sub-phase stamps of the QKV phase (CTA 0): slice, record wait, norm, matvec, publish
                 unsigned long long ts = (a.trace && cta == 0 && tid == 0) ? gtime() : 0ull;
@@ -856,7 +977,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                 const unsigned char* rec = rec_base();
                 sub(1);
                 norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
                 sub(2);
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
@@ -868,6 +989,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                     if (sl.bias) v += bias[i];
                     ll_store_rep(a.ll_qkv + (size_t)b * qkv_rows + sl.r0 + i, rs_qkv, v, e);
                 }
+                tr_pub(s, l, 1);
                 done_rec();
                 sub(4);
             }
@@ -881,7 +1003,9 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                 tr_waited();
                 for (int it = cta; it < items && ok; it += G) {
                     const int c = it % S, g = (it / S) % a.Hkv, b = it / (S * a.Hkv);
-                    ok = attn_item(a, l, b, g, c, S, chunk, pos, e, act, a.err, rs_qkv, rs_part);
+                    ok = attn_item(a, l, b, g, c, S, chunk, pos, e, act, a.err, rs_qkv, rs_part,
+                                   (a.trace && cta == 0) ? s_trc + 8 : nullptr);
+                    tr_pub(s, l, 2);
                 }
                 if (!ok) break;
             }
@@ -922,22 +1046,34 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                     s_own[b * kMaxOwn + i] = v;
                     ll_store_rep(a.ll_xa + (size_t)b * d + sl.r0 + i, rs_x, v, e);
                 }
+                tr_pub(s, l, 3);
                 done_rec();
             }
             tr_end(PK_O);
             // ---- FC / gate-up rows (norm prologue, GELU / SwiGLU)
             tr_begin();
             {
+                long long tc = (a.trace && cta == 0 && tid == 0) ? clock64() : 0;
+                auto stamp = [&](int k) {
+                    if (a.trace && cta == 0 && tid == 0) {
+                        const long long t = clock64();
+                        s_trc[k] += (unsigned long long)(t - tc);
+                        tc = t;
+                    }
+                };
                 bool okr = ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true);
                 okr = okr && rec_ready();
                 if (!(ok = csync_and(okr) != 0)) break;
                 tr_waited();
+                stamp(0);
                 const Slice sl = slice_at(a, tab, s_geo, 4 * l + 2);
                 const unsigned char* rec = rec_base();
                 norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                stamp(1);
                 const int nr = sl.r1 - sl.r0;
                 gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
+                stamp(2);
                 const float* bias = reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.r0 - sl.b_lo);
                 if (ln) {
                     for (int t = tid; t < nr * NB; t += kThreads) {
@@ -953,7 +1089,10 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                         ll_store_rep(a.ll_u + (size_t)b * a.ff + sl.r0 / 2 + i, rs_u, silu(gt) * up, e);
                     }
                 }
+                tr_pub(s, l, 4);
+                stamp(3);
                 done_rec();
+                stamp(4);
             }
             tr_end(PK_FC);
             // ---- proj / down rows (+bias +residual)
@@ -976,6 +1115,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                     s_own[b * kMaxOwn + i] = v;
                     ll_store_rep(a.ll_xb + (size_t)b * d + sl.r0 + i, rs_x, v, e);
                 }
+                tr_pub(s, l, 5);
                 done_rec();
             }
             tr_end(PK_PROJ);
@@ -992,7 +1132,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             const Slice sl = slice_at(a, tab, s_geo, 4 * L);
             const unsigned char* rec = rec_base();
             norm_to<NB>(act, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                        reinterpret_cast<const float*>(rec + sl.o_g2), a.eps);
+                        reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
             const int nr = sl.r1 - sl.r0;
             gemv_rec<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, s_part, s_y);
             for (int t = tid; t < nr * NB; t += kThreads) {
@@ -1032,6 +1172,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     }
     // the producer drains its copies in flight and exits once it sees this
     csync();
+    if (a.trace && cta == 0 && tid < 16) a.trace[32 + tid] += s_trc[tid];
     if (tid == 0) {
         *reinterpret_cast<volatile int*>(&s_nc) = nc;
         __threadfence_block();
@@ -1047,9 +1188,10 @@ size_t act_region_bytes(const StepArgs& a) {
     if (qd > kmax) kmax = qd;
     size_t need = sizeof(float) * ((size_t)a.B * padded(kmax) + (size_t)a.B * padded(a.d));
     const size_t o_phase = sizeof(float) * ((size_t)a.B * padded(qd) + (size_t)a.B * a.H * a.max_split * (a.hd + 2));
-    // attention floats before the fp16 staging: a multiple of 4 (16 bytes) for every hd in {64, 128}
-    const size_t attn_floats = (size_t)2 * HPG * a.hd + 2 * a.hd + HPG * kKC + 3 * kMaxHPG + kThreads;
-    const size_t attn = sizeof(float) * attn_floats + sizeof(__half) * 2 * kKC * a.hd;
+    // attention: q, the new k and v, the warp partials (a multiple of 4 floats, so the fp16
+    // staging after them is 16-byte aligned), then keys at a pitch of hd + 8 halves and values
+    const size_t attn_floats = (size_t)HPG * a.hd + 2 * a.hd + (size_t)(kKC / 32) * HPG * (a.hd + 2);
+    const size_t attn = sizeof(float) * attn_floats + sizeof(__half) * (size_t)kKC * (2 * a.hd + 8);
     const size_t smp = sample_smem_bytes_dev(a.V, kThreads);
     if (o_phase > need) need = o_phase;
     if (attn > need) need = attn;

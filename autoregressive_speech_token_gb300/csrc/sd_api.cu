@@ -394,7 +394,12 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     a.n_steps = n_steps;
     a.u_seq = u_seq;
     a.out_seq = out_seq;
-    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 32, st));
+    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 64, st));
+    if (a.trace_pub) {
+        const size_t half = (size_t)kTraceSteps * a.n_layer * kTracePhases;
+        CK(cudaMemsetAsync(a.trace_pub, 0, sizeof(unsigned long long) * half, st));
+        CK(cudaMemsetAsync(a.trace_pub + half, 0xFF, sizeof(unsigned long long) * half, st));
+    }
     cudaError_t e = launch_step(a, c->step_grid, st);
     c->count_launch++;
     if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
@@ -718,7 +723,9 @@ int setup_persistent(sd_ctx* c) {
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
-        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 32))) return rc;
+        if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 64))) return rc;
+        if ((rc = dalloc(c, &a.trace_pub, sizeof(unsigned long long) * 2 * kTraceSteps * a.n_layer * kTracePhases)))
+            return rc;
     }
     c->persistent = true;
     return SD_OK;
@@ -728,7 +735,7 @@ int setup_persistent(sd_ctx* c) {
 // SD_TRACE: for each phase kind the mean wait for its inputs and the mean work.
 void write_trace(sd_ctx* c, int n_steps) {
     if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
-    unsigned long long t[32];
+    unsigned long long t[64];
     if (cudaMemcpy(t, c->step.trace, sizeof t, cudaMemcpyDeviceToHost) != cudaSuccess) return;
     FILE* f = fopen(c->trace_path.c_str(), "a");
     if (!f) return;
@@ -747,6 +754,46 @@ void write_trace(sd_ctx* c, int n_steps) {
             (double)t[24] / 1e3 / n_steps / per[1], (double)t[25] / 1e3 / n_steps / per[1],
             (double)t[26] / 1e3 / n_steps / per[1], (double)t[27] / 1e3 / n_steps / per[1],
             (double)t[28] / 1e3 / n_steps / per[1]);
+    {
+        // cycle stamps of CTA 0: FC phase sub-steps and attention item sub-steps, per layer
+        const double nl = (double)n_steps * c->step.n_layer;
+        fprintf(f, "  fc cycles/layer: inputs %.0f norm %.0f matvec %.0f publish %.0f release %.0f\n", t[32] / nl,
+                t[33] / nl, t[34] / nl, t[35] / nl, t[36] / nl);
+        fprintf(f, "  attn cycles/layer: qkv-wait %.0f rope+append %.0f stage-wait %.0f warps %.0f partials %.0f "
+                   "combine+publish %.0f fence %.0f\n",
+                t[40] / nl, t[41] / nl, t[42] / nl, t[43] / nl, t[44] / nl, t[45] / nl, t[46] / nl);
+    }
+    if (c->step.trace_pub) {
+        // critical path: per phase, the latest publish minus the previous phase's latest publish,
+        // and the spread between the earliest and the latest CTA (layers >= 1 of the first steps)
+        const int L = c->step.n_layer, ns = std::min(n_steps, kTraceSteps);
+        const size_t half = (size_t)kTraceSteps * L * kTracePhases;
+        std::vector<unsigned long long> tp(2 * half);
+        if (L > 1 && cudaMemcpy(tp.data(), c->step.trace_pub, tp.size() * 8, cudaMemcpyDeviceToHost) == cudaSuccess) {
+            const char* pn[kTracePhases] = {"input", "qkv", "attn", "o", "fc", "proj"};
+            double dl[kTracePhases] = {}, sp[kTracePhases] = {};
+            int cnt = 0;
+            for (int st = 0; st < ns; ++st)
+                for (int l = 1; l < L; ++l) {
+                    const unsigned long long* mx = tp.data() + ((size_t)st * L + l) * kTracePhases;
+                    const unsigned long long* mn = mx + half;
+                    const unsigned long long* prev = tp.data() + ((size_t)st * L + l - 1) * kTracePhases;
+                    for (int ph = 0; ph < kTracePhases; ++ph) {
+                        const unsigned long long ref = ph == 0 ? prev[kTracePhases - 1] : mx[ph - 1];
+                        dl[ph] += (double)(long long)(mx[ph] - ref);
+                        sp[ph] += (double)(long long)(mx[ph] - mn[ph]);
+                    }
+                    ++cnt;
+                }
+            fprintf(f, "  critical path per layer (us): phase: latest publish - previous latest | latest - earliest\n");
+            double tot = 0;
+            for (int ph = 0; ph < kTracePhases; ++ph) {
+                fprintf(f, "    %-6s %8.3f %8.3f\n", pn[ph], dl[ph] / 1e3 / cnt, sp[ph] / 1e3 / cnt);
+                tot += dl[ph] / 1e3 / cnt;
+            }
+            fprintf(f, "    layer  %8.3f\n", tot);
+        }
+    }
     fclose(f);
 }
 

@@ -207,12 +207,16 @@ struct StepArgs {
     int act_bytes = 0;                   // shared-memory activation / attention / sampler region
     int max_split = 1;                   // attention splits per (row, kv head) at most
     int split_len = 128;                 // cached positions per attention split (before the cap)
-    unsigned long long* trace = nullptr; // optional [32]: CTA 0 per phase kind: input wait, weight wait, rest (ns); [24..29) QKV sub-phases
+    unsigned long long* trace = nullptr; // optional [64]: CTA 0 per phase kind: input wait, weight wait, rest (ns); [24..29) QKV sub-phases (ns); [32..37) FC and [40..48) attention sub-steps (cycles)
+    // optional publish stamps of the first kTraceSteps steps: [2][kTraceSteps][n_layer][kTracePhases]
+    // (latest over CTAs, then earliest over CTAs) of the global time at which a CTA published a phase
+    unsigned long long* trace_pub = nullptr;
 };
 size_t step_smem_bytes(const StepArgs& a);
 // grid size the persistent step runs with (0: the configuration does not fit)
 // fills a.ring_bytes, a.act_bytes and a.max_split as planned
 int step_plan_grid(StepArgs& a, int sm_count);
+constexpr int kTraceSteps = 64, kTracePhases = 6;  // phases: layer input, QKV, attention, O, FC, proj
 cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
 
 // Tensor-core GEMM Y[M][N] = X[M][K] W[N][K]^T over a repacked weight, with
