@@ -124,9 +124,12 @@ __device__ __forceinline__ float gelu_tanh(float t) {
 
 __device__ __forceinline__ float silu(float t) { return t / (1.0f + expf(-t)); }
 
+// Loads tile tt's weight units and their block scales (affine: scale and
+// bias as one half2) into registers; issued a tile ahead, so neither the
+// codes nor the scales are waited for inside the dot products.
 template <int QK, int R, int U>
-__device__ __forceinline__ void load_tile(uint4 (&w)[R][U], const uint8_t* q, int tt, int WR, int rg, int rows,
-                                          int row_bytes, const int (&ebase)[U], int K) {
+__device__ __forceinline__ void load_tile(uint4 (&w)[R][U], uint32_t (&sc)[R][U], const GemvArgs& a, int tt, int WR,
+                                          int rg, int rows, int row_bytes, int spr, const int (&ebase)[U], int K) {
     const int r0 = tt * WR * R + rg * R;
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -135,9 +138,14 @@ __device__ __forceinline__ void load_tile(uint4 (&w)[R][U], const uint8_t* q, in
         for (int u = 0; u < U; ++u) {
             if (r < rows && ebase[u] < K) {
                 const int boff = (QK == SD_Q4_0) ? (ebase[u] >> 1) : ebase[u];
-                w[i][u] = ld_stream(q + (size_t)r * row_bytes + boff);
+                w[i][u] = ld_stream(a.W.q + (size_t)r * row_bytes + boff);
+                if (QK == SD_A8G64)
+                    sc[i][u] = __ldg(reinterpret_cast<const unsigned int*>(a.W.s) + (size_t)r * spr + (ebase[u] >> 6));
+                else
+                    sc[i][u] = __ldg(reinterpret_cast<const unsigned short*>(a.W.s) + (size_t)r * spr + (ebase[u] >> 5));
             } else {
                 w[i][u] = make_uint4(0u, 0u, 0u, 0u);
+                sc[i][u] = 0u;
             }
         }
     }
@@ -170,9 +178,10 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
     // issue the first tile's weight loads before the prologue: they do not
     // depend on the activations.
     uint4 w[R][U];
+    uint32_t scw[R][U];
     int t = blockIdx.x;
     pdl_trigger();
-    if (t < tiles) load_tile<QK, R, U>(w, a.W.q, t, WR, rg, rows, row_bytes, ebase, K);
+    if (t < tiles) load_tile<QK, R, U>(w, scw, a, t, WR, rg, rows, row_bytes, spr, ebase, K);
     pdl_wait();  // activations come from the previous kernel
 
     // ---------------------------------------------------------------- prologue
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
             for (int u = 0; u < U; ++u) {
                 if (ebase[u] >= K) continue;
                 if (QK == SD_A8G64) {
-                    const __half2 sb = reinterpret_cast<const __half2*>(a.W.s)[(size_t)r * spr + (ebase[u] >> 6)];
+                    const __half2 sb = *reinterpret_cast<const __half2*>(&scw[i][u]);
                     const float sc = __low2float(sb), bi = __high2float(sb);
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
                         acc[i][b] = fmaf(sc, dq, fmaf(bi, xsum[b][u], acc[i][b]));
                     }
                 } else {
-                    const float d = __half2float(reinterpret_cast<const __half*>(a.W.s)[(size_t)r * spr + (ebase[u] >> 5)]);
+                    const float d = __half2float(__ushort_as_half((unsigned short)scw[i][u]));
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
                         const float dq = (QK == SD_Q4_0) ? dot_q4(w[i][u], &xr[b][0]) : dot_s8(w[i][u], &xr[b][u * EPU]);
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
         }
         // prefetch the next tile while reducing this one
         const int tn = t + gridDim.x;
-        if (tn < tiles) load_tile<QK, R, U>(w, a.W.q, tn, WR, rg, rows, row_bytes, ebase, K);
+        if (tn < tiles) load_tile<QK, R, U>(w, scw, a, tn, WR, rg, rows, row_bytes, spr, ebase, K);
 
 #pragma unroll
         for (int i = 0; i < R; ++i)
@@ -360,13 +369,26 @@ cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
     // fewer rows per CTA when the matrix is short, so that every SM gets work
     while (WR > 1 && (a.W.rows + WR * R - 1) / (WR * R) < sm_count) WR >>= 1;
     const int tiles = (a.W.rows + WR * R - 1) / (WR * R);
-    const int grid = tiles < 32 * sm_count ? tiles : 32 * sm_count;
     const size_t smem = sizeof(float) * (size_t)NB * padded(K);
     if (smem > 32 * 1024) {  // with the static arrays the total passes the 48 KB default
         cudaError_t e = cudaFuncSetAttribute(k_gemv<QK, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_k(k_gemv<QK, NB, R>, dim3(grid), dim3(32 * WK * WR), smem, st, a);
+    // one wave of resident CTAs that loop over the tiles (the next tile's loads are in flight
+    // while a tile is reduced, and the activation prologue is paid once per CTA); the
+    // occupancy of each (K slices, row groups) shape is asked once
+    const int threads = 32 * WK * WR;
+    static int occ_cache[9][4] = {};  // [WK][WR index] -> resident CTAs per SM
+    int& occ = occ_cache[WK][WR >= 8 ? 3 : WR >= 4 ? 2 : WR >= 2 ? 1 : 0];
+    if (occ == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemv<QK, NB, R>, threads, smem) != cudaSuccess || n < 1)
+            n = 1;
+        occ = n;
+    }
+    const int wave = occ * sm_count;
+    const int grid = tiles < wave ? tiles : wave;
+    return launch_k(k_gemv<QK, NB, R>, dim3(grid), dim3(threads), smem, st, a);
 }
 
 inline cudaError_t check_gemv(const GemvArgs& a) {
