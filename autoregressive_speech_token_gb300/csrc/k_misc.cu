@@ -177,14 +177,21 @@ cudaError_t launch_advance(int* a, int add_a, int* b, int add_b, int* c, int set
     return launch_k(k_advance, dim3(1), dim3(1), 0, st, a, add_a, b, add_b, c, set_c);
 }
 
-// Programmatic dependent launch is off unless SD_PDL=1: on the step graph it
-// measured slower (1.09 ms vs 0.86 ms per GPT-2-Medium Q4_0 step).
+// Programmatic dependent launch: SD_PDL=1 / SD_PDL=0 force it on / off;
+// otherwise the graph being captured decides (set_pdl_default).  Measured on
+// GB300: the Talker + code-predictor frame gains (3.98 vs 4.35 ms per frame at
+// one row, 9.86 vs 10.17 ms at sixteen), the GPT-2-Medium Q4_0 step graph
+// loses (0.875 vs 0.809 ms).
+namespace {
+thread_local bool t_pdl_default = false;
+}
+void set_pdl_default(bool on) { t_pdl_default = on; }
 bool use_pdl() {
-    static const bool on = [] {
+    static const int env = [] {
         const char* e = getenv("SD_PDL");
-        return e && e[0] == '1';
+        return e && e[0] ? (e[0] == '1' ? 1 : 0) : -1;
     }();
-    return on;
+    return env >= 0 ? env == 1 : t_pdl_default;
 }
 
 }  // namespace sd

@@ -504,7 +504,11 @@ int capture(sd_ctx* c, GraphKind k, cudaGraphExec_t* out, int* n_kernels) {
     cudaGraph_t g = nullptr;
     c->count_launch = 0;
     CK(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+    // programmatic dependent launch inside the Talker + code-predictor graphs (many short
+    // kernels whose weight loads can start before their predecessor ends)
+    set_pdl_default(c->cfg.arch == SD_ARCH_QWEN_TTS);
     int rc = enqueue_graph(c, k, c->cap);
+    set_pdl_default(false);
     cudaError_t e = cudaStreamEndCapture(c->cap, &g);
     if (rc) {
         if (g) cudaGraphDestroy(g);

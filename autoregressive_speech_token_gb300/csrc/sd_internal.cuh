@@ -19,6 +19,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Launch with the programmatic-serialization attribute (set when use_pdl()).
 bool use_pdl();
+void set_pdl_default(bool on);  // this thread's default when SD_PDL is unset
 template <typename Kern, typename... Args>
 cudaError_t launch_k(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};
