@@ -290,9 +290,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm16(const Gemm16Args a) {
     const int outs = a.epi == EPI_SWIGLU ? ncols / 2 : ncols;
     for (int i = tid; i < M * outs; i += kThreads) {
         const int m = i / outs, jj = i - m * outs;
+        // the splits' partials in split order; loads issued eight at a time (independent L2
+        // round trips), the additions stay in order so the result does not depend on the grouping
         auto sum = [&](int n) {
+            const int S = (int)gridDim.y;
+            const float* p = a.ws + (size_t)m * N + n;
+            const size_t stride = (size_t)16 * N;
             float v = 0.f;
-            for (int sp = 0; sp < (int)gridDim.y; ++sp) v += __ldcg(a.ws + ((size_t)sp * 16 + m) * N + n);
+            for (int s0 = 0; s0 < S; s0 += 8) {
+                float pv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) pv[j] = s0 + j < S ? __ldcg(p + (size_t)(s0 + j) * stride) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < S) v += pv[j];
+            }
             return v;
         };
         float v;
@@ -324,7 +336,10 @@ Plan plan(int N, int K, int sm_count) {
     const int want = std::max(1, (2 * std::max(sm_count, 1) + p.tiles - 1) / p.tiles);
     int kp = (K + want - 1) / want;
     kp = ((kp + gran - 1) / gran) * gran;
-    p.k_per = std::min(std::max(kp, gran), kMaxKPer);
+    // at least 256 codes per CTA row range: below that the staging and the split reduction
+    // cost more than the extra CTAs gain (small code-predictor matrices)
+    const int kmin = std::min(K, 256) / gran * gran;
+    p.k_per = std::min(std::max(kp, std::max(kmin, gran)), kMaxKPer);
     p.splits = (K + p.k_per - 1) / p.k_per;
     return p;
 }
