@@ -1225,6 +1225,7 @@ int step_plan_grid(StepArgs& a, int sm_count) {
     const int qd = a.H * a.hd, kd = a.Hkv * a.hd, qkv_rows = qd + 2 * kd;
     const int HPG = a.Hkv > 0 ? a.H / a.Hkv : 0;
     if (a.Hkv < 1 || a.H % a.Hkv || HPG > kMaxHPG || (a.hd != 64 && a.hd != 128) || HPG * a.hd > kThreads) return 0;
+    if (a.d > 8 * kThreads) return 0;  // norm_to holds at most two float4 of a row per thread
     if (a.V > sample_detail::kMaxV || a.d % 32 || a.ff % 32 || qd % 32) return 0;
     int G = sm_count < a.d ? sm_count : a.d;
     if (G > qkv_rows || G > a.ff || G > a.V) return 0;
