@@ -13,6 +13,7 @@ this package.  It shares no code with the CUDA library.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 import subprocess
@@ -40,6 +41,38 @@ def build(force: bool = False) -> str:
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def build_mutant(n: int) -> str:
+    """The oracle compiled with planted mistake n (ORC_MUTANT, listed in
+    sd_oracle.c) into oracle/_build/liboracle_m<n>.so, for the tests that check
+    that the pins reject each mistake."""
+    path = os.path.join(_HERE, "_build", f"liboracle_m{n}.so")
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    if os.path.exists(path) and os.path.getmtime(path) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "sd_oracle.h"))):
+        return path
+    tmp = path + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall", "-Wextra", f"-DORC_MUTANT={int(n)}",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every oracle call to the library at `path` (a planted-mistake
+    build) inside the block."""
+    global _lib
+    prev = lib()
+    L = C.CDLL(path)
+    _declare(L)
+    _lib = L
+    try:
+        yield
+    finally:
+        _lib = prev
 
 
 def lib():

@@ -31,6 +31,23 @@
 #endif
 
 enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
+
+/* Planted mistakes for the pin tests (tests/test_oracle_mutants.py): a build
+ * with -DORC_MUTANT=n carries mistake n, and the pins must reject it.  Normal
+ * builds leave ORC_MUTANT at 0 and none of these branches exist.
+ *   1 fp16 rounding truncates          2 Q4_0 nibble halves swapped
+ *   3 Q8_0 codes read unsigned         4 affine group bias dropped
+ *   5 linear layer bias dropped        6 LayerNorm unbiased variance
+ *   7 RMSNorm gain dropped             8 GELU with erf instead of tanh form
+ *   9 RoPE rotates the wrong way      10 attention scores unscaled
+ *  11 attention misses the newest key 12 sampler drops top-k ties
+ *  13 top-p cut one element late      14 draw in probability order
+ *  15 temperature multiplies          16 attention residual dropped
+ *  17 SwiGLU gate and up swapped      18 query heads interleaved over KV heads
+ *  19 RoPE skipped on keys                                                  */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
 enum { A_GPT2 = 1, A_LLAMA = 2, A_QWEN = 3 };
 
 /* ------------------------------------------------------------------ fp16 */
@@ -59,7 +76,11 @@ uint16_t orc_float_to_half(float f) {
     int e;
     frexp(a, &e);                                       /* a = f * 2^e, f in [0.5, 1) */
     e -= 1;                                             /* a in [2^e, 2^(e+1)) */
+#if ORC_MUTANT == 1
+    double m = floor(ldexp(a, 10 - e));
+#else
     double m = rint(ldexp(a, 10 - e));                  /* in [1024, 2048] */
+#endif
     if (m == 2048.0) { m = 1024.0; e += 1; }
     if (e + 15 >= 31) return sign | 0x7c00;
     return sign | (uint16_t)(((e + 15) << 10) | ((int)m - 1024));
@@ -73,7 +94,11 @@ static void dequant_row(int kind, const uint8_t* data, int64_t r, int64_t cols, 
         for (int64_t b = 0; b < cols / 32; ++b) {
             const uint8_t* blk = row + b * 34;
             float d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+#if ORC_MUTANT == 3
+            for (int j = 0; j < 32; ++j) out[b * 32 + j] = d * (float)blk[2 + j];
+#else
             for (int j = 0; j < 32; ++j) out[b * 32 + j] = d * (float)(int8_t)blk[2 + j];
+#endif
         }
     } else if (kind == K_Q4_0) {
         const uint8_t* row = data + r * (cols / 32) * 18;
@@ -82,7 +107,11 @@ static void dequant_row(int kind, const uint8_t* data, int64_t r, int64_t cols, 
             float d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
             for (int j = 0; j < 32; ++j) {
                 int byte = blk[2 + (j % 16)];
+#if ORC_MUTANT == 2
+                int nib = j < 16 ? (byte >> 4) : (byte & 0xf);
+#else
                 int nib = j < 16 ? (byte & 0xf) : (byte >> 4);
+#endif
                 out[b * 32 + j] = d * (float)(nib - 8);
             }
         }
@@ -103,7 +132,11 @@ static void qmat_row(const qmat* W, int64_t r, float* out) {
         const uint16_t* s = W->scale + r * (W->cols / 64);
         const uint16_t* b = W->bias + r * (W->cols / 64);
         for (int64_t k = 0; k < W->cols; ++k)
+#if ORC_MUTANT == 4
+            out[k] = orc_half_to_float(s[k / 64]) * (float)q[k] + 0.0f * orc_half_to_float(b[k / 64]);
+#else
             out[k] = fmaf(orc_half_to_float(s[k / 64]), (float)q[k], orc_half_to_float(b[k / 64]));
+#endif
     } else if (W->kind == K_F32) {
         memcpy(out, (const float*)W->data + r * W->cols, (size_t)W->cols * sizeof(float));
     } else {
@@ -156,7 +189,11 @@ static void linear_q(const qmat* W, const float* x, const float* bias, float* y)
             qmat_row(W, r, w);
             double acc = 0.0;
             for (int64_t k = 0; k < cols; ++k) acc += (double)w[k] * (double)x[k];
+#if ORC_MUTANT != 5
             if (bias) acc += (double)bias[r];
+#else
+            (void)bias;
+#endif
             y[r] = (float)acc;
         }
         free(w);
@@ -178,7 +215,11 @@ void orc_layernorm(const float* x, int n, const float* g, const float* b, float 
     for (int i = 0; i < n; ++i) mu += x[i];
     mu /= n;
     for (int i = 0; i < n; ++i) var += ((double)x[i] - mu) * ((double)x[i] - mu);
+#if ORC_MUTANT == 6
+    var /= (n - 1);
+#else
     var /= n;                                       /* biased variance */
+#endif
     double r = 1.0 / sqrt(var + (double)eps);
     for (int i = 0; i < n; ++i) out[i] = (float)(((double)x[i] - mu) * r * (double)g[i] + (double)b[i]);
 }
@@ -188,12 +229,21 @@ void orc_rmsnorm(const float* x, int n, const float* g, float eps, float* out) {
     for (int i = 0; i < n; ++i) ms += (double)x[i] * (double)x[i];
     ms /= n;
     double r = 1.0 / sqrt(ms + (double)eps);
+#if ORC_MUTANT == 7
+    (void)g;
+    for (int i = 0; i < n; ++i) out[i] = (float)((double)x[i] * r);
+#else
     for (int i = 0; i < n; ++i) out[i] = (float)((double)x[i] * r * (double)g[i]);
+#endif
 }
 
 float orc_gelu_tanh(float t) {
     double x = t;
+#if ORC_MUTANT == 8
+    return (float)(0.5 * x * (1.0 + erf(x / sqrt(2.0))));
+#else
     return (float)(0.5 * x * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (x + 0.044715 * x * x * x))));
+#endif
 }
 
 float orc_silu(float t) {
@@ -206,7 +256,11 @@ void orc_rope(float* x, int hd, int pos, float theta) {
     for (int i = 0; i < half; ++i) {
         double freq = pow((double)theta, -2.0 * i / hd);
         double phi = (double)pos * freq;
+#if ORC_MUTANT == 9
+        double c = cos(phi), s = -sin(phi);
+#else
         double c = cos(phi), s = sin(phi);
+#endif
         double a = x[i], b = x[i + half];
         x[i] = (float)(a * c - b * s);
         x[i + half] = (float)(a * s + b * c);
@@ -215,7 +269,11 @@ void orc_rope(float* x, int hd, int pos, float theta) {
 
 void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int hd, float* out) {
     double* s = (double*)malloc((size_t)n * sizeof(double));
+#if ORC_MUTANT == 10
+    double scale = 1.0;
+#else
     double scale = 1.0 / sqrt((double)hd);
+#endif
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
         double acc = 0.0;
@@ -255,7 +313,11 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         if (margin) *margin = V > 1 ? (double)z[best] - second : INFINITY;
         return best;
     }
+#if ORC_MUTANT == 15
+    double inv_t = (double)temperature;
+#else
     double inv_t = 1.0 / (double)temperature;
+#endif
     zi* s = (zi*)malloc((size_t)V * sizeof(zi));
     for (int32_t i = 0; i < V; ++i) { s[i].z = (double)z[i] * inv_t; s[i].i = i; }
     qsort(s, (size_t)V, sizeof(zi), cmp_desc);
@@ -264,7 +326,12 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     double thr = s[k - 1].z;
     double gap_k = k < V ? s[k - 1].z - s[k].z : INFINITY;
     int32_t n_keep = 0;
+#if ORC_MUTANT == 12
+    (void)thr;
+    n_keep = k;
+#else
     while (n_keep < V && s[n_keep].z >= thr) ++n_keep;
+#endif
     /* softmax over the survivors (s is already in (p desc, index asc) order) */
     double zmax = s[0].z, Z = 0.0;
     double* p = (double*)malloc((size_t)V * sizeof(double));  /* indexed by vocabulary id */
@@ -283,7 +350,11 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         for (int32_t t = 0; t < n_keep; ++t) {
             prev = cum;
             cum += p[s[t].i] / Z;
+#if ORC_MUTANT == 13
+            if (cum >= (double)top_p) { cut = t + 1 < n_keep ? t + 1 : t; break; }
+#else
             if (cum >= (double)top_p) { cut = t; break; }
+#endif
         }
         gap_p = fabs(cum - (double)top_p);
         if (cut > 0 && fabs((double)top_p - prev) < gap_p) gap_p = fabs((double)top_p - prev);
@@ -299,7 +370,12 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     for (int32_t i = 0; i < V; ++i) if (in_s[i]) zs += p[i];
     double target = u * zs, c = 0.0, c_lo = 0.0;
     int32_t tok = -1, last = -1;
+#if ORC_MUTANT == 14
+    for (int32_t t = 0; t < V; ++t) {
+        const int32_t i = s[t].i;
+#else
     for (int32_t i = 0; i < V; ++i) {
+#endif
         if (!in_s[i]) continue;
         last = i;
         c_lo = c;
@@ -541,7 +617,9 @@ static int stack_forward(ostack* s, int row, float* x) {
         float *q = s->qkv, *k = s->qkv + qd, *v = s->qkv + qd + kd;
         if (!s->gpt2) {
             for (int h = 0; h < H; ++h) orc_rope(q + h * hd, hd, pos, s->theta);
+#if ORC_MUTANT != 19
             for (int h = 0; h < Hk; ++h) orc_rope(k + h * hd, hd, pos, s->theta);
+#endif
         }
         size_t layer_base = ((size_t)row * s->n_layer + l) * Hk;
         for (int g = 0; g < Hk; ++g) {
@@ -552,12 +630,24 @@ static int stack_forward(ostack* s, int row, float* x) {
             }
         }
         for (int h = 0; h < H; ++h) {
+#if ORC_MUTANT == 18
+            int g = h % Hk;
+#else
             int g = h / (H / Hk);                   /* contiguous query-head groups */
+#endif
             size_t base = (layer_base + g) * s->max_ctx * hd;
+#if ORC_MUTANT == 11
+            orc_attend(q + h * hd, s->kc + base, s->vc + base, pos > 0 ? pos : 1, hd, s->o + h * hd);
+#else
             orc_attend(q + h * hd, s->kc + base, s->vc + base, pos + 1, hd, s->o + h * hd);
+#endif
         }
         linear_q(&L->wo, s->o, s->gpt2 ? L->bo : NULL, s->y);
+#if ORC_MUTANT == 16
+        for (int i = 0; i < d; ++i) x[i] = s->y[i];
+#else
         for (int i = 0; i < d; ++i) x[i] = (float)((double)x[i] + (double)s->y[i]);
+#endif
         /* MLP block */
         if (s->gpt2) {
             orc_layernorm(x, d, L->n2g, L->n2b, s->eps, s->h);
@@ -567,7 +657,11 @@ static int stack_forward(ostack* s, int row, float* x) {
             orc_rmsnorm(x, d, L->n2g, s->eps, s->h);
             linear_q(&L->wfc, s->h, NULL, s->t);    /* rows [0, ff) gate, [ff, 2ff) up */
             for (int i = 0; i < s->ff; ++i)
+#if ORC_MUTANT == 17
+                s->u[i] = (float)((double)orc_silu(s->t[s->ff + i]) * (double)s->t[i]);
+#else
                 s->u[i] = (float)((double)orc_silu(s->t[i]) * (double)s->t[s->ff + i]);
+#endif
         }
         linear_q(&L->wproj, s->u, s->gpt2 ? L->bproj : NULL, s->y);
         for (int i = 0; i < d; ++i) x[i] = (float)((double)x[i] + (double)s->y[i]);

@@ -1,0 +1,61 @@
+"""Planted mistakes: each pin must reject a plausible error in the oracle.
+
+The oracle is built once per mistake with ORC_MUTANT=n (the list is in
+oracle/sd_oracle.c: a dropped term, a wrong sign, a swapped operand or index,
+a wrong order), every oracle call is routed to that build, and the pins that
+cover the mistake's place are run: at least one of them must fail.  A pin set
+that still passes would let that mistake through, and the CUDA path's parity
+against the oracle would prove nothing there.  Everything runs on the CPU.
+"""
+
+import pytest
+
+import oracle
+from tests import test_oracle_model as om
+from tests import test_oracle_ops as oo
+
+KQ8, KQ4, KA8 = 1, 2, 3
+
+MUTANTS = {
+    1: ("fp16 rounding truncates", [oo.test_fp16_conversions_match_numpy]),
+    2: ("Q4_0 nibble halves swapped", [oo.test_q4_0_hand_block]),
+    3: ("Q8_0 codes read unsigned", [oo.test_q8_0_hand_block]),
+    4: ("affine group bias dropped", [oo.test_a8g64_hand_group]),
+    5: ("linear layer bias dropped", [lambda: oo.test_linear_against_float64_dot(KQ8)]),
+    6: ("LayerNorm unbiased variance", [oo.test_layernorm_invariants_and_torch]),
+    7: ("RMSNorm gain dropped", [oo.test_rmsnorm_invariants_and_torch]),
+    8: ("GELU with erf instead of the tanh form", [oo.test_activations_against_torch]),
+    9: ("RoPE rotates the wrong way", [oo.test_rope_identity_norms_and_complex_form]),
+    10: ("attention scores unscaled", [oo.test_attention_closed_forms_and_sdpa]),
+    11: ("attention misses the newest key", [om.test_tiny_gpt2_incremental_equals_full_recompute]),
+    12: ("sampler drops top-k ties", [oo.test_sampler_adversarial_ties_and_boundaries]),
+    13: ("top-p cut one element late", [oo.test_sampler_bruteforce_random_logits]),
+    14: ("draw in probability order", [oo.test_sampler_bruteforce_random_logits]),
+    15: ("temperature multiplies", [oo.test_sampler_bruteforce_random_logits]),
+    16: ("attention residual dropped", [om.test_tiny_gpt2_incremental_equals_full_recompute]),
+    17: ("SwiGLU gate and up swapped", [om.test_llama_gqa_rows_match_full_recompute]),
+    18: ("query heads interleaved over KV heads", [om.test_llama_gqa_rows_match_full_recompute]),
+    19: ("RoPE skipped on keys", [om.test_llama_gqa_rows_match_full_recompute]),
+}
+
+
+@pytest.mark.parametrize("n", sorted(MUTANTS))
+def test_planted_mistake_is_rejected(n):
+    what, pins = MUTANTS[n]
+    path = oracle.build_mutant(n)
+    caught = []
+    with oracle.using_library(path):
+        for pin in pins:
+            try:
+                pin()
+            except AssertionError as e:
+                caught.append(repr(e)[:120])
+    assert caught, f"planted mistake {n} ({what}) passed every pin that covers it"
+
+
+def test_unmutated_build_passes_the_same_pins():
+    """The pins used above pass on the oracle itself (so a failure above is the
+    planted mistake, not a pin that always fails)."""
+    for n in (2, 6, 10, 12, 13):
+        for pin in MUTANTS[n][1]:
+            pin()
