@@ -695,7 +695,6 @@ __device__ bool attn_item(const StepArgs& a, int l, int b, int g, int c, int S, 
             a.vc[hb + (size_t)pos * hd + dd] = __float2half_rn(vn[dd]);
         }
     }
-    const int DPL = hd >> 5;  // value dimensions per lane (2 or 4)
     // the warps' running state (o, m, l) per query head lives in their partial slots
     if (warp < kAW)
         for (int h = 0; h < HPG; ++h) {
