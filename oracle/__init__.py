@@ -99,6 +99,9 @@ def _declare(L):
     L.orc_sample.argtypes = [f32p, C.c_int32, C.c_float, C.c_int32, C.c_float, C.c_int32, C.c_double,
                              C.POINTER(C.c_double)]
     L.orc_sample.restype = C.c_int32
+    L.orc_sample_ladder.argtypes = [f32p, f32p, C.c_int32, C.c_float, u8p, C.c_float, C.c_float, C.c_float,
+                                    C.c_float, C.c_int32, C.c_double, C.POINTER(C.c_double)]
+    L.orc_sample_ladder.restype = C.c_int32
     L.orc_open.argtypes = [u8p, C.c_uint64, C.POINTER(C.c_void_p)]
     L.orc_close.argtypes = [C.c_void_p]; L.orc_close.restype = None
     L.orc_reset.argtypes = [C.c_void_p]; L.orc_reset.restype = None
@@ -198,6 +201,21 @@ def sample(z, temperature=1.0, top_k=1, top_p=1.0, greedy=True, u=0.0):
     m = C.c_double()
     tok = lib().orc_sample(_p(z, C.c_float), z.size, float(temperature), int(top_k), float(top_p),
                            int(bool(greedy)), float(u), C.byref(m))
+    return int(tok), float(m.value)
+
+
+def sample_ladder(z_cond, z_uncond=None, cfg_weight=0.0, seen=None, rep_penalty=1.0, temperature=1.0, min_p=0.0,
+                  top_p=1.0, top_k=0, u=0.0):
+    """The multilingual T3's sampler ladder (CFG combine, repetition penalty,
+    temperature, min_p, top-p, top-k, draw in vocabulary order).  Returns
+    (token, margin)."""
+    zc = _f32(z_cond)
+    zu = _f32(z_uncond) if z_uncond is not None else None
+    sn = np.ascontiguousarray(seen, np.uint8) if seen is not None else None
+    m = C.c_double()
+    tok = lib().orc_sample_ladder(_p(zc, C.c_float), _p(zu, C.c_float), zc.size, float(cfg_weight),
+                                  _p(sn, C.c_uint8), float(rep_penalty), float(temperature), float(min_p),
+                                  float(top_p), int(top_k), float(u), C.byref(m))
     return int(tok), float(m.value)
 
 

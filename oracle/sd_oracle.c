@@ -44,7 +44,8 @@ enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
  *  13 top-p cut one element late      14 draw in probability order
  *  15 temperature multiplies          16 attention residual dropped
  *  17 SwiGLU gate and up swapped      18 query heads interleaved over KV heads
- *  19 RoPE skipped on keys                                                  */
+ *  19 RoPE skipped on keys         20 repetition penalty backwards
+ *  21 ladder: top-k before top-p                                            */
 #ifndef ORC_MUTANT
 #define ORC_MUTANT 0
 #endif
@@ -394,6 +395,111 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     if (m_u <= pp_flip / zs && gap_p < m) m = gap_p;
     if (margin) *margin = m;
     free(s); free(p); free(in_s);
+    return tok;
+}
+
+/* Sampler ladder of the multilingual T3 ("Chatterbox -> ggml Port:
+ * Development Journal", the multilingual port's sampling path: CFG combine,
+ * repetition penalty, temperature, min_p, top-p, top-k, multinomial).  Each
+ * stage acts on the survivors of the previous one:
+ *   z_i = c_i + w (c_i - u_i)                 (c conditional, u unconditional logits)
+ *   seen i: z_i / penalty if z_i > 0, else z_i * penalty   (journal: the HF rule)
+ *   z_i / T, p_i proportional to exp(z_i)
+ *   min_p:  keep p_i >= min_p * max_j p_j
+ *   top-p:  the shortest (p desc, index asc) prefix of the survivors whose
+ *           renormalised mass reaches top_p
+ *   top-k:  keep the survivors whose value is >= the k-th largest survivor's
+ *   draw:   the smallest vocabulary index whose cumulative kept mass exceeds u
+ *           times the kept total. */
+int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V, float cfg_weight,
+                          const uint8_t* seen, float rep_penalty, float temperature, float min_p, float top_p,
+                          int32_t top_k, double u, double* margin) {
+    if (V <= 0) return -1;
+    double* z = (double*)malloc((size_t)V * sizeof(double));
+    for (int32_t i = 0; i < V; ++i) {
+        double c = z_cond[i];
+        if (z_uncond && cfg_weight != 0.0f) c = c + (double)cfg_weight * (c - (double)z_uncond[i]);
+        z[i] = c;
+    }
+    if (seen && rep_penalty != 1.0f)
+        for (int32_t i = 0; i < V; ++i)
+            if (seen[i]) {
+#if ORC_MUTANT == 20
+                z[i] = z[i] > 0.0 ? z[i] * (double)rep_penalty : z[i] / (double)rep_penalty;
+#else
+                z[i] = z[i] > 0.0 ? z[i] / (double)rep_penalty : z[i] * (double)rep_penalty;
+#endif
+            }
+    if (temperature <= 0.0f) {
+        int32_t best = 0;
+        for (int32_t i = 1; i < V; ++i) if (z[i] > z[best]) best = i;
+        double second = -INFINITY;
+        for (int32_t i = 0; i < V; ++i) if (i != best && z[i] > second) second = z[i];
+        if (margin) *margin = V > 1 ? z[best] - second : INFINITY;
+        free(z);
+        return best;
+    }
+    for (int32_t i = 0; i < V; ++i) z[i] /= (double)temperature;
+    double mx = -INFINITY;
+    for (int32_t i = 0; i < V; ++i) if (z[i] > mx) mx = z[i];
+    double* p = (double*)malloc((size_t)V * sizeof(double));
+    char* keep = (char*)malloc((size_t)V);
+    for (int32_t i = 0; i < V; ++i) { p[i] = exp(z[i] - mx); keep[i] = 1; }
+    /* min_p: relative to the largest probability, which is exp(0) = 1 here (the
+     * largest always survives: min_p above 1 acts as 1) */
+    if (min_p > 0.0f) {
+        const double mp = min_p < 1.0f ? (double)min_p : 1.0;
+        for (int32_t i = 0; i < V; ++i) if (p[i] < mp) keep[i] = 0;
+    }
+    /* survivors in (p desc, index asc) order: z desc, index asc */
+    zi* s = (zi*)malloc((size_t)V * sizeof(zi));
+    int32_t ns = 0;
+    for (int32_t i = 0; i < V; ++i) if (keep[i]) { s[ns].z = z[i]; s[ns].i = i; ++ns; }
+    qsort(s, (size_t)ns, sizeof(zi), cmp_desc);
+#if ORC_MUTANT == 21
+    /* top-k before top-p (the order of the first port) */
+    {
+        int32_t k = top_k < 1 || top_k > ns ? ns : top_k;
+        int32_t n_keep = 0;
+        while (n_keep < ns && s[n_keep].z >= s[k - 1].z) ++n_keep;
+        for (int32_t t = n_keep; t < ns; ++t) keep[s[t].i] = 0;
+        ns = n_keep;
+    }
+#endif
+    if (top_p < 1.0f) {
+        double mass = 0.0;
+        for (int32_t t = 0; t < ns; ++t) mass += p[s[t].i];
+        double cum = 0.0;
+        int32_t cut = ns - 1;
+        for (int32_t t = 0; t < ns; ++t) {
+            cum += p[s[t].i] / mass;
+            if (cum >= (double)top_p) { cut = t; break; }
+        }
+        for (int32_t t = cut + 1; t < ns; ++t) keep[s[t].i] = 0;
+        ns = cut + 1;
+    }
+#if ORC_MUTANT != 21
+    {
+        int32_t k = top_k < 1 || top_k > ns ? ns : top_k;
+        int32_t n_keep = 0;
+        while (n_keep < ns && s[n_keep].z >= s[k - 1].z) ++n_keep;   /* ties at the k-th value kept */
+        for (int32_t t = n_keep; t < ns; ++t) keep[s[t].i] = 0;
+    }
+#endif
+    double zs = 0.0;
+    for (int32_t i = 0; i < V; ++i) if (keep[i]) zs += p[i];
+    double target = u * zs, c = 0.0, c_lo = 0.0;
+    int32_t tok = -1, last = -1;
+    for (int32_t i = 0; i < V; ++i) {
+        if (!keep[i]) continue;
+        last = i;
+        c_lo = c;
+        c += p[i];
+        if (c > target) { tok = i; break; }
+    }
+    if (tok < 0) { tok = last; c_lo = c - p[last]; }
+    if (margin) *margin = fmin(target - c_lo, c - target) / zs;
+    free(z); free(p); free(keep); free(s);
     return tok;
 }
 

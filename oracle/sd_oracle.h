@@ -49,6 +49,16 @@ void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int
 int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
                    int32_t greedy, double u, double* margin);
 
+/* Sampler ladder of the multilingual T3: classifier-free-guidance combine ->
+ * repetition penalty -> temperature -> min_p -> top-p -> top-k -> draw in
+ * vocabulary order with u.  z_uncond may be NULL (no combine); seen may be
+ * NULL (no penalty); top_k < 1 or > V keeps every survivor; temperature <= 0
+ * returns the argmax of the combined, penalised logits.  margin (may be NULL)
+ * receives the draw's distance to the chosen token's CDF edges. */
+int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V, float cfg_weight,
+                          const uint8_t* seen, float rep_penalty, float temperature, float min_p, float top_p,
+                          int32_t top_k, double u, double* margin);
+
 /* Model.  The blob must outlive the model. */
 int  orc_open(const uint8_t* blob, uint64_t nbytes, orc_model** out);
 void orc_close(orc_model* m);

@@ -11,6 +11,7 @@ against the oracle would prove nothing there.  Everything runs on the CPU.
 import pytest
 
 import oracle
+from tests import test_oracle_ladder as ol
 from tests import test_oracle_model as om
 from tests import test_oracle_ops as oo
 
@@ -36,6 +37,8 @@ MUTANTS = {
     17: ("SwiGLU gate and up swapped", [om.test_llama_gqa_rows_match_full_recompute]),
     18: ("query heads interleaved over KV heads", [om.test_llama_gqa_rows_match_full_recompute]),
     19: ("RoPE skipped on keys", [om.test_llama_gqa_rows_match_full_recompute]),
+    20: ("repetition penalty backwards", [ol.test_repetition_penalty_divides_positive_and_multiplies_negative_logits]),
+    21: ("ladder: top-k before top-p", [ol.test_top_p_acts_before_top_k]),
 }
 
 
