@@ -1,0 +1,216 @@
+// Sampler ladder of the multilingual T3 as an op-level kernel: classifier-
+// free-guidance combine -> repetition penalty -> temperature -> min_p ->
+// top-p -> top-k -> draw in vocabulary order ("Chatterbox -> ggml Port:
+// Development Journal", the multilingual port's sampling path; the penalty
+// divides positive logits and multiplies negative ones, as the journal's fix
+// table records).  One CTA per row, every quantity in double precision (the
+// ladder is not on the decode step's critical path):
+//   z_i = c_i + w (c_i - u_i); seen i: z_i / penalty (z_i > 0) or z_i * penalty;
+//   z_i / T; p_i = exp(z_i - max z)
+//   min_p: keep p_i >= min(min_p, 1) (the largest probability is 1 here)
+//   the survivors sorted by (z desc, index asc) with a bitonic sort in shared
+//   memory; top-p: the shortest prefix whose renormalised mass reaches top_p;
+//   top-k: the prefix entries whose value is >= the k-th (ties kept)
+//   draw: the smallest vocabulary index whose cumulative kept mass exceeds u
+//   times the kept total.
+#include "sd_internal.cuh"
+
+namespace sd {
+namespace ladder_detail {
+
+constexpr int kT = 1024, kW = kT / 32;
+
+__device__ __forceinline__ bool before(double ka, int ia, double kb, int ib) {
+    return ka > kb || (ka == kb && ia < ib);
+}
+
+__device__ double block_max_d(double v, double* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    double r = red[0];
+    for (int w = 1; w < kW; ++w) r = fmax(r, red[w]);
+    __syncthreads();
+    return r;
+}
+
+__device__ int block_min_i(int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = red[0];
+    for (int w = 1; w < kW; ++w) r = min(r, red[w]);
+    __syncthreads();
+    return r;
+}
+
+__device__ int block_max_i(int v, int* red) { return -block_min_i(-v, red); }
+
+// exclusive scan of one double per thread in thread order (fixed order); *total = the sum
+__device__ double block_excl_scan_d(double v, double* red, double* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) red[warp] = inc;
+    __syncthreads();
+    double before_w = 0.0, tot = 0.0;
+    for (int w = 0; w < kW; ++w) {
+        if (w == warp) before_w = tot;
+        tot += red[w];
+    }
+    __syncthreads();
+    *total = tot;
+    return before_w + inc - v;
+}
+
+__global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const float* zu, int V, int NP, float w,
+                                                      float pen, float T, float min_p, float top_p, int top_k,
+                                                      const uint8_t* seen, const float* u, int32_t* out) {
+    extern __shared__ __align__(16) unsigned char lsm[];
+    double* key = reinterpret_cast<double*>(lsm);   // [NP] sort keys
+    double* zv = key + NP;                           // [V] ladder logits in vocabulary order
+    int* idx = reinterpret_cast<int*>(zv + V);       // [NP] vocabulary index of each key
+    uint8_t* flag = reinterpret_cast<uint8_t*>(idx + NP);  // [V] kept after every stage
+    __shared__ double dred[kW];
+    __shared__ int ired[kW];
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const float* c = zc + (size_t)row * V;
+    const float* un = zu ? zu + (size_t)row * V : nullptr;
+    const uint8_t* sn = seen ? seen + (size_t)row * V : nullptr;
+
+    // ---- combine, penalty
+    for (int i = tid; i < V; i += kT) {
+        double z = c[i];
+        if (un && w != 0.0f) z = z + (double)w * (z - (double)un[i]);
+        if (sn && pen != 1.0f && sn[i]) z = z > 0.0 ? z / (double)pen : z * (double)pen;
+        zv[i] = z;
+    }
+    __syncthreads();
+    if (T <= 0.0f) {  // argmax, lowest index on ties
+        double best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = tid; i < V; i += kT)
+            if (zv[i] > best) { best = zv[i]; bi = i; }
+        const double mx = block_max_d(best, dred);
+        const int tok = block_min_i(best == mx ? bi : 0x7fffffff, ired);
+        if (tid == 0) out[row] = tok;
+        return;
+    }
+    // ---- temperature, max
+    double lm = -INFINITY;
+    for (int i = tid; i < V; i += kT) {
+        zv[i] /= (double)T;
+        lm = fmax(lm, zv[i]);
+    }
+    const double m = block_max_d(lm, dred);  // its barrier also publishes zv
+    const double mp = min_p < 1.0f ? (double)min_p : 1.0;
+    // ---- min_p survivors as sort keys (the rest sort last as -inf)
+    for (int j = tid; j < NP; j += kT) {
+        double k = -INFINITY;
+        if (j < V && (min_p <= 0.0f || exp(zv[j] - m) >= mp)) k = zv[j];
+        key[j] = k;
+        idx[j] = j;
+    }
+    __syncthreads();
+    // ---- bitonic sort: (z desc, index asc)
+    for (int k = 2; k <= NP; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < NP; i += kT) {
+                const int l = i ^ j;
+                if (l <= i) continue;
+                const bool up = (i & k) == 0;  // this pair's block sorts in the "before" order
+                const bool swap = up ? before(key[l], idx[l], key[i], idx[i]) : before(key[i], idx[i], key[l], idx[l]);
+                if (swap) {
+                    const double tk = key[i]; key[i] = key[l]; key[l] = tk;
+                    const int ti = idx[i]; idx[i] = idx[l]; idx[l] = ti;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // survivors: the prefix of finite keys
+    int ns = 0;
+    {
+        int last = -1;
+        for (int t = tid; t < NP; t += kT)
+            if (key[t] != -INFINITY) last = max(last, t);
+        ns = block_max_i(last, ired) + 1;
+    }
+    // ---- top-p over the survivors: contiguous segments per thread, prefix of masses
+    const int seg = (NP + kT - 1) / kT, t0 = min(NP, tid * seg), t1 = min(NP, t0 + seg);
+    if (top_p < 1.0f) {
+        double loc = 0.0;
+        for (int t = t0; t < t1; ++t)
+            if (t < ns) loc += exp(key[t] - m);
+        double mass;
+        double run = block_excl_scan_d(loc, dred, &mass);
+        int cut = 0x7fffffff;
+        for (int t = t0; t < t1 && t < ns; ++t) {
+            run += exp(key[t] - m);
+            if (run / mass >= (double)top_p) { cut = t; break; }
+        }
+        cut = block_min_i(cut, ired);
+        if (cut < ns) ns = cut + 1;
+    }
+    // ---- top-k over those: the prefix entries whose value is >= the k-th
+    if (top_k >= 1 && top_k < ns) {
+        const double thr = key[top_k - 1];
+        int last = -1;
+        for (int t = tid; t < ns; t += kT)
+            if (key[t] >= thr) last = max(last, t);
+        ns = block_max_i(last, ired) + 1;
+    }
+    // ---- kept flags in vocabulary order
+    for (int i = tid; i < V; i += kT) flag[i] = 0;
+    __syncthreads();
+    for (int t = tid; t < ns; t += kT) flag[idx[t]] = 1;
+    __syncthreads();
+    // ---- draw in vocabulary order
+    const int vseg = (V + kT - 1) / kT, v0 = min(V, tid * vseg), v1 = min(V, v0 + vseg);
+    double loc = 0.0;
+    for (int i = v0; i < v1; ++i)
+        if (flag[i]) loc += exp(zv[i] - m);
+    double zs;
+    double run = block_excl_scan_d(loc, dred, &zs);
+    const double target = (double)u[row] * zs;
+    int cand = 0x7fffffff, lastk = -1;
+    for (int i = v0; i < v1; ++i) {
+        if (!flag[i]) continue;
+        lastk = i;
+        run += exp(zv[i] - m);
+        if (run > target) { cand = i; break; }
+    }
+    int tok = block_min_i(cand, ired);
+    const int lastv = block_max_i(lastk, ired);
+    if (tok == 0x7fffffff) tok = lastv;  // u * total rounded onto the last edge
+    if (tid == 0) out[row] = tok;
+}
+
+}  // namespace ladder_detail
+
+size_t sample_ladder_smem_bytes(int V) {
+    int NP = 1;
+    while (NP < V) NP <<= 1;
+    return (size_t)NP * 8 + (size_t)V * 8 + (size_t)NP * 4 + (((size_t)V + 15) & ~(size_t)15);
+}
+
+cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int V, const LadderParams& p,
+                                 const uint8_t* seen, const float* u, int32_t* out, cudaStream_t st) {
+    using namespace ladder_detail;
+    int NP = 1;
+    while (NP < V) NP <<= 1;
+    const size_t smem = sample_ladder_smem_bytes(V);
+    cudaError_t e = cudaFuncSetAttribute(k_sample_ladder, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_sample_ladder<<<rows, kT, smem, st>>>(zc, zu, V, NP, p.cfg_weight, p.rep_penalty, p.temperature, p.min_p,
+                                            p.top_p, p.top_k, seen, u, out);
+    return cudaGetLastError();
+}
+
+}  // namespace sd

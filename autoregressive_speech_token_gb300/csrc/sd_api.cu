@@ -1416,6 +1416,25 @@ int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sa
     return SD_OK;
 }
 
+int sd_sample_rows_ladder(const float* logits_cond_dev, const float* logits_uncond_dev, int32_t rows, int32_t V,
+                          const sd_sampler_ladder* s, const uint8_t* seen_dev, const float* u_dev, int32_t* out_dev,
+                          void* stream) {
+    sd_ctx* c = nullptr;
+    if (!logits_cond_dev || !s || !u_dev || !out_dev || rows < 1 || rows > 65535 || V < 1 || V > 8192)
+        return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows_ladder: bad argument");
+    if (!(s->repetition_penalty > 0.f) || !(s->min_p >= 0.f) || !(s->top_p > 0.f && s->top_p <= 1.f) ||
+        !(s->temperature == s->temperature) || !(s->cfg_weight == s->cfg_weight))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows_ladder: sampler out of range");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    LadderParams p;
+    p.cfg_weight = s->cfg_weight; p.rep_penalty = s->repetition_penalty; p.temperature = s->temperature;
+    p.min_p = s->min_p; p.top_p = s->top_p; p.top_k = s->top_k;
+    cudaError_t e = launch_sample_ladder(logits_cond_dev, logits_uncond_dev, rows, V, p, seen_dev, u_dev, out_dev, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "sd_sample_rows_ladder: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
 int sd_attend_rows(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_dev, int32_t B, int32_t H, int32_t Hkv,
                    int32_t hd, int32_t n_ctx, int32_t n, int32_t nsplit, float* out_dev, void* stream) {
     sd_ctx* c = nullptr;

@@ -127,6 +127,16 @@ cudaError_t launch_gemv_a8(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t st);
 size_t attention_smem_bytes(const AttnArgs& a);
 cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t st);
+
+// Sampler ladder (op level): CFG combine -> repetition penalty -> temperature
+// -> min_p -> top-p -> top-k -> draw, one CTA per row, V <= 8192.
+struct LadderParams {
+    float cfg_weight = 0.f, rep_penalty = 1.f, temperature = 1.f, min_p = 0.f, top_p = 1.f;
+    int top_k = 0;
+};
+size_t sample_ladder_smem_bytes(int V);
+cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int V, const LadderParams& p,
+                                 const uint8_t* seen, const float* u, int32_t* out, cudaStream_t st);
 size_t sample_smem_bytes(int V);
 
 cudaError_t launch_repack(int kind, const uint8_t* canon, int rows, int cols, int swiglu_ff, uint8_t* q,

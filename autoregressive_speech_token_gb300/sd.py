@@ -27,7 +27,7 @@ MAX_CODEBOOKS = 16
 # every symbol the headers declare
 EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes",
            "sd_decode_n", "sd_get_logits", "sd_reset", "sd_destroy", "sd_last_error", "sd_get_info",
-           "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm16", "sd_qmat_gemm_tc", "sd_sample_rows",
+           "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm16", "sd_qmat_gemm_tc", "sd_sample_rows", "sd_sample_rows_ladder",
            "sd_attend_rows", "sd_attend_rows_static"]
 
 
@@ -55,6 +55,12 @@ class Sampler(C.Structure):
     @classmethod
     def from_spec(cls, s) -> "Sampler":
         return cls(float(s.temperature), int(s.top_k), float(s.top_p), int(bool(s.greedy)))
+
+
+class SamplerLadder(C.Structure):
+    """sd_sampler_ladder: CFG weight, repetition penalty, temperature, min_p, top_p, top_k."""
+    _fields_ = [("cfg_weight", C.c_float), ("repetition_penalty", C.c_float), ("temperature", C.c_float),
+                ("min_p", C.c_float), ("top_p", C.c_float), ("top_k", C.c_int32)]
 
 
 class Info(C.Structure):
@@ -99,6 +105,7 @@ def load_library(path: str | None = None):
         "sd_qmat_gemm16": ([vp, vp, i32, i32, vp, vp, vp, vp], C.c_int),
         "sd_qmat_gemm_tc": ([vp, vp, i32, i32, vp, vp, vp, vp], C.c_int),
         "sd_sample_rows": ([vp, i32, i32, C.POINTER(Sampler), vp, vp, vp], C.c_int),
+        "sd_sample_rows_ladder": ([vp, vp, i32, i32, C.POINTER(SamplerLadder), vp, vp, vp, vp], C.c_int),
         "sd_attend_rows": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp], C.c_int),
         "sd_attend_rows_static": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp], C.c_int),
     }
@@ -267,6 +274,13 @@ def sd_qmat_gemm16(m: int, x_dev, M: int, epilogue: int, bias_dev, resid_dev, y_
 def sd_qmat_gemm_tc(m: int, x_dev, M: int, epilogue: int, bias_dev, resid_dev, y_dev, stream=None) -> None:
     _check(load_library().sd_qmat_gemm_tc(m, _ptr(x_dev), M, epilogue, _ptr(bias_dev), _ptr(resid_dev),
                                           _ptr(y_dev), stream), None)
+
+
+def sd_sample_rows_ladder(logits_cond_dev, logits_uncond_dev, rows: int, V: int, sampler: SamplerLadder, seen_dev,
+                          u_dev, out_dev, stream=None) -> None:
+    _check(load_library().sd_sample_rows_ladder(_ptr(logits_cond_dev), _ptr(logits_uncond_dev), rows, V,
+                                                C.byref(sampler), _ptr(seen_dev), _ptr(u_dev), _ptr(out_dev),
+                                                stream), None)
 
 
 def sd_sample_rows(logits_dev, rows: int, V: int, sampler: Sampler, u_dev, out_dev, stream=None) -> None:

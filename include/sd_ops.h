@@ -90,6 +90,36 @@ int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, 
 int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,
                    const float* u_dev, int32_t* out_dev, void* stream);
 
+/* Parameters of the sampler ladder (sd_sample_rows_ladder). */
+typedef struct sd_sampler_ladder {
+    float cfg_weight;          /* guidance weight w: z = c + w (c - u); 0 = conditional logits only */
+    float repetition_penalty;  /* > 0; 1 = off */
+    float temperature;         /* <= 0: argmax of the combined, penalised logits */
+    float min_p;               /* keep p >= min_p * max p; 0 = off (values above 1 act as 1) */
+    float top_p;               /* (0, 1]; 1 = off */
+    int32_t top_k;             /* < 1 or >= the survivors: off */
+} sd_sampler_ladder;
+
+/* Sampler ladder of the multilingual T3 ("Chatterbox -> ggml Port: Development
+ * Journal", the multilingual port's sampling path): classifier-free-guidance
+ * combine -> repetition penalty -> temperature -> min_p -> top-p -> top-k ->
+ * draw in vocabulary order.  Per row b:
+ *   z_i = c_i + w (c_i - u_i)      (c = logits_cond_dev[b], u = logits_uncond_dev[b]; w ignored when NULL)
+ *   seen_dev[b][i] != 0: z_i / penalty if z_i > 0, else z_i * penalty   (seen_dev may be NULL)
+ *   z_i / T; p_i proportional to exp(z_i); min_p keeps p_i >= min_p * max p;
+ *   top-p keeps the shortest (p desc, index asc) prefix of those whose
+ *   renormalised mass reaches top_p; top-k keeps the ones whose value is >= the
+ *   k-th largest remaining (ties kept); the token is the smallest vocabulary
+ *   index whose cumulative kept mass exceeds u_dev[b] times the kept total.
+ * Layouts: logits [rows][V] fp32, seen [rows][V] bytes, u [rows], out [rows] int32;
+ * device pointers; 1 <= V <= 8192.  Double-precision arithmetic, one CTA per row.
+ * This entry is an op-level form of the ladder: the decode step's own sampler
+ * is temperature -> top-k -> top-p (sd.h).  Synchronises `stream`; returns
+ * SD_ERR_INVALID_ARG on a NULL required pointer or a parameter out of range. */
+int sd_sample_rows_ladder(const float* logits_cond_dev, const float* logits_uncond_dev, int32_t rows, int32_t V,
+                          const sd_sampler_ladder* sampler, const uint8_t* seen_dev, const float* u_dev,
+                          int32_t* out_dev, void* stream);
+
 /* Decode attention for one query per head against n cached positions
  * (journal section 3.13 flash attention over a cache laid out
  * [head][pos][dim]): out[b][h] = softmax(q[b][h] . K[b][g][0:n] / sqrt(hd))
