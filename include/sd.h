@@ -46,7 +46,7 @@ extern "C" {
 #define SD_ERR_OOM (-4)          /* device or pinned allocation failed */
 #define SD_ERR_CUDA (-5)         /* a CUDA runtime call failed */
 #define SD_ERR_TIMEOUT (-6)      /* a device-side bounded wait expired */
-#define SD_ERR_UNSUPPORTED (-7)  /* valid request this build does not implement */
+#define SD_ERR_UNSUPPORTED (-7)  /* valid request the library does not implement */
 #define SD_ERR_BLOB (-8)         /* weight blob malformed or not matching the config */
 #define SD_ERR_DEVICE (-9)       /* a kernel flagged an out-of-range index and skipped it */
 
