@@ -633,6 +633,9 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
 // previous codes and forced codes.
 constexpr size_t kStepH2D = offsetof(DevState, u) - offsetof(DevState, prompt_on);
 constexpr size_t kStepD2H = offsetof(DevState, u1);
+// sd_frame uploads the inputs through the forced codes and reads the codes back as well
+constexpr size_t kFrameH2D = offsetof(DevState, codes) - offsetof(DevState, prompt_on);
+constexpr size_t kFrameD2H = kStepD2H + sizeof(DevState::codes);
 // The persistent step is opt-in (SD_PERSISTENT=1) until it beats the
 // per-operation graph on the bench workload.
 // Tensor-core prefill: every main-stack matrix dequantised once into fp16 high
@@ -1205,8 +1208,9 @@ int sd_get_info(const sd_ctx* c, sd_info* out) {
     out->prefill = !c->gemm_prefill ? 0 : (c->tc_prefill ? 2 : 1);
     out->weight_bytes = c->weight_bytes;
     out->kv_bytes = c->kv_bytes;
-    out->step_h2d_bytes = (int64_t)kStepH2D;
-    out->step_d2h_bytes = (int64_t)kStepD2H;
+    const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
+    out->step_h2d_bytes = (int64_t)(qwen ? kFrameH2D : kStepH2D);
+    out->step_d2h_bytes = (int64_t)(qwen ? kFrameD2H : kStepD2H);
     return SD_OK;
 }
 

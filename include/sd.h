@@ -151,8 +151,8 @@ typedef struct sd_info {
     int32_t attn_splits;       /* split-KV chunks per (row, kv head) */
     int64_t weight_bytes;      /* repacked weight bytes resident on the device */
     int64_t kv_bytes;          /* KV cache bytes allocated */
-    int64_t step_h2d_bytes;    /* host->device bytes one sd_step copies (pinned staging) */
-    int64_t step_d2h_bytes;    /* device->host bytes one sd_step copies back */
+    int64_t step_h2d_bytes;    /* host->device bytes one sd_step (Talker+CP: one sd_frame) copies (pinned staging) */
+    int64_t step_d2h_bytes;    /* device->host bytes one sd_step (Talker+CP: one sd_frame) copies back */
     int32_t persistent;        /* CTAs of the persistent step kernel (0: per-operation kernels) */
     int32_t prefill;           /* prompt path: 0 per-position step graphs, 1 mma.sync GEMMs, 2 tcgen05 GEMMs */
 } sd_info;
