@@ -10,7 +10,8 @@
 // (cp.async.bulk with mbarrier completion), the CTA's rows of the matrices in
 // the order the step consumes them -- codes, scales, bias and norm gains of one
 // phase per record -- as far ahead as the ring holds (two to three layers).
-// Thread 0 issues records whenever space frees; compute never waits on HBM.
+// A producer warp (one lane) issues records whenever space frees and never
+// joins the compute barriers; compute never waits on HBM.
 //
 // Activation exchange.  A phase's outputs are published as 64-bit words
 // (epoch << 32 | float bits) written with one relaxed store each; a consumer

@@ -636,8 +636,6 @@ constexpr size_t kStepD2H = offsetof(DevState, u1);
 // sd_frame uploads the inputs through the forced codes and reads the codes back as well
 constexpr size_t kFrameH2D = offsetof(DevState, codes) - offsetof(DevState, prompt_on);
 constexpr size_t kFrameD2H = kStepD2H + sizeof(DevState::codes);
-// The persistent step is opt-in (SD_PERSISTENT=1) until it beats the
-// per-operation graph on the bench workload.
 // Tensor-core prefill: every main-stack matrix dequantised once into fp16 high
 // and low parts with its TMA tensor maps, and the split-activation buffers.
 // SD_PREFILL=mma keeps the mma.sync GEMM; a shape the kernel does not take
