@@ -134,6 +134,9 @@ struct sd_ctx {
     std::string trace_path;             // SD_TRACE: per-phase timings of the persistent step
     StepLayer* step_layers = nullptr;   // device [n_layer]
     int step_grid = 0;
+    // cluster persistent step kernel (k_cstep.cu): preferred over the flat one where its plan fits
+    bool cpersistent = false;
+    CStepArgs cstep;
 };
 
 namespace {
@@ -388,8 +391,27 @@ int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
     return SD_OK;
 }
 
+// One launch of the cluster step kernel for n_steps steps.
+int enqueue_cstep(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
+    CStepArgs a = c->cstep;
+    a.n_steps = n_steps;
+    a.u_seq = u_seq;
+    a.out_seq = out_seq;
+    if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * kCTraceSub, st));
+    if (a.trace_pub) {
+        const size_t half = (size_t)kTraceSteps * a.n_layer * kCTracePhases;
+        CK(cudaMemsetAsync(a.trace_pub, 0, sizeof(unsigned long long) * half, st));
+        CK(cudaMemsetAsync(a.trace_pub + half, 0xFF, sizeof(unsigned long long) * half, st));
+    }
+    cudaError_t e = launch_cstep(a, st);
+    c->count_launch++;
+    if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "cluster step launch: %s", cudaGetErrorString(e));
+    return SD_OK;
+}
+
 // One cooperative launch of the persistent step kernel for n_steps steps.
 int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
+    if (c->cpersistent) return enqueue_cstep(c, n_steps, u_seq, out_seq, st);
     StepArgs a = c->step;
     a.n_steps = n_steps;
     a.u_seq = u_seq;
@@ -676,21 +698,125 @@ int setup_tc_prefill(sd_ctx* c) {
     return SD_OK;
 }
 
-// The persistent step kernel is the default for the GPT-2/Llama T3 with
-// Q8_0/Q4_0 weights and one row (faster than the per-operation graph on
-// GB300); SD_PERSISTENT=1 also selects it for two rows, SD_PERSISTENT=0 never.
-bool persistent_wanted(int rows) {
+// Which persistent step kernel runs the decode steps of a GPT-2/Llama T3 with
+// Q8_0/Q4_0 weights: 0 none (the per-operation graph), 1 the cluster kernel
+// where its plan fits and the flat one otherwise, 2 the flat kernel only, 3
+// the cluster kernel only.  Default: 1 for one row, 0 for two.
+// SD_PERSISTENT = 0 | 1 | flat | cluster overrides.
+int persistent_mode(int rows) {
     const char* e = getenv("SD_PERSISTENT");
-    if (e && e[0] == '0') return false;
-    if (e && e[0] == '1') return true;
-    return rows == 1;
+    if (e && !strcmp(e, "flat")) return 2;
+    if (e && !strcmp(e, "cluster")) return 3;
+    if (e && e[0] == '0') return 0;
+    if (e && e[0] == '1') return 1;
+    return rows == 1 ? 1 : 0;
+}
+
+// Cluster step plan, repacked matrices (cluster-major QKV rows, Wo and the
+// down projection as column slabs) and exchange buffers.  Leaves
+// c->cpersistent false when the plan does not fit.
+int setup_cstep(sd_ctx* c) {
+    const sd_model_config& m = c->cfg;
+    DStack& s = c->main;
+    CStepArgs& a = c->cstep;
+    a = CStepArgs();
+    a.gpt2 = s.gpt2 ? 1 : 0; a.n_layer = s.n_layer; a.d = s.d; a.H = s.H; a.Hkv = s.Hkv; a.hd = s.hd; a.ff = s.ff;
+    a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.quant = m.quant; a.eps = s.eps;
+    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
+    a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.kc = s.kc; a.vc = s.vc;
+    a.logits = c->logits;
+    a.pos = &c->ds->pos; a.tok = c->ds->tok; a.u1 = c->ds->u1; a.sp = &c->ds->samp[0]; a.err = &c->ds->err;
+    const int grid = cstep_plan(a, c->sm_count);
+    cudaGetLastError();
+    if (grid <= 0) return SD_OK;
+    int rc;
+    // q, k, v rows of each cluster's heads, contiguous
+    const int qd = s.H * s.hd, kd = s.Hkv * s.hd, R = s.qkv_rows();
+    std::vector<int> perm(R);
+    for (int cl = 0; cl < a.ncl; ++cl)
+        for (int i = 0; i < a.rpc; ++i) {
+            const int qn = a.hpc * s.hd, kn = a.kpc * s.hd;
+            int src;
+            if (i < qn) src = cl * qn + i;
+            else if (i < qn + kn) src = qd + cl * kn + (i - qn);
+            else src = qd + kd + cl * kn + (i - qn - kn);
+            perm[cl * a.rpc + i] = src;
+        }
+    int* dperm = nullptr;
+    if ((rc = dalloc(c, &dperm, sizeof(int) * R))) return rc;
+    CK(cudaMemcpy(dperm, perm.data(), sizeof(int) * R, cudaMemcpyHostToDevice));
+    auto slab = [&](const QMat& W, int width, const int* pm, QMat* out) -> int {
+        const size_t qb = (size_t)W.rows * (W.kind == SD_Q4_0 ? W.cols / 2 : W.cols);
+        const size_t sb = (size_t)W.rows * (W.cols / 32) * sizeof(__half);
+        uint8_t* q = nullptr;
+        __half* sc = nullptr;
+        int r;
+        // + 256: the step's bulk copies read scale windows widened to 16 bytes
+        if ((r = dalloc(c, &q, qb)) || (r = dalloc(c, &sc, sb + 256))) return r;
+        cudaError_t e = launch_slab_gather(W, width, pm, q, sc, c->stream);
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "slab gather: %s", cudaGetErrorString(e));
+        out->kind = W.kind;
+        out->rows = W.rows * (W.cols / width);
+        out->cols = width;
+        out->q = q;
+        out->s = sc;
+        return SD_OK;
+    };
+    std::vector<StepLayer> L(s.n_layer);
+    std::vector<float> bh(R), bp(R);
+    for (int l = 0; l < s.n_layer; ++l) {
+        const DLayer& D = s.L[l];
+        StepLayer& t = L[l];
+        t.n1g = D.n1g; t.n1b = D.n1b; t.bo = D.bo; t.n2g = D.n2g; t.n2b = D.n2b; t.bfc = D.bfc; t.bproj = D.bproj;
+        t.wfc = D.wfc;
+        if ((rc = slab(D.wqkv, D.wqkv.cols, dperm, &t.wqkv)) || (rc = slab(D.wo, a.ko, nullptr, &t.wo)) ||
+            (rc = slab(D.wproj, a.upc, nullptr, &t.wproj)))
+            return rc;
+        if (D.bqkv) {
+            CK(cudaMemcpy(bh.data(), D.bqkv, sizeof(float) * R, cudaMemcpyDeviceToHost));
+            for (int i = 0; i < R; ++i) bp[i] = bh[perm[i]];
+            float* db = nullptr;
+            if ((rc = dalloc(c, &db, sizeof(float) * R + 256))) return rc;  // bias windows widened to 16 bytes
+            CK(cudaMemcpy(db, bp.data(), sizeof(float) * R, cudaMemcpyHostToDevice));
+            t.bqkv = db;
+        }
+    }
+    StepLayer* dl = nullptr;
+    if ((rc = dalloc(c, &dl, sizeof(StepLayer) * s.n_layer))) return rc;
+    CK(cudaMemcpy(dl, L.data(), sizeof(StepLayer) * s.n_layer, cudaMemcpyHostToDevice));
+    a.layers = dl;
+    const size_t w8 = sizeof(unsigned long long);
+    if ((rc = dalloc(c, &a.ll_po, w8 * a.ncl * c->B * s.d)) || (rc = dalloc(c, &a.ll_pp, w8 * a.ncl * c->B * s.d)) ||
+        (rc = dalloc(c, &a.ll_logits, w8 * c->B * m.vocab)) || (rc = dalloc(c, &a.ll_tok, w8 * 8 * 32)) ||
+        (rc = dalloc(c, &a.gen, 256)))
+        return rc;
+    int clock_khz = 0;
+    cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
+    a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
+    if (const char* tp = getenv("SD_TRACE")) {
+        c->trace_path = tp;
+        if ((rc = dalloc(c, &a.trace_pub, sizeof(unsigned long long) * 2 * kTraceSteps * a.n_layer * kCTracePhases)) ||
+            (rc = dalloc(c, &a.trace, sizeof(unsigned long long) * kCTraceSub)))
+            return rc;
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    c->step_grid = grid;
+    c->cpersistent = true;
+    c->persistent = true;
+    return SD_OK;
 }
 
 // Persistent step plan for GPT-2/Llama with Q8_0/Q4_0 weights and B <= 2.
 int setup_persistent(sd_ctx* c) {
     const sd_model_config& m = c->cfg;
     c->persistent = false;
-    if (!persistent_wanted(c->B) || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
+    c->cpersistent = false;
+    const int mode = persistent_mode(c->B);
+    if (!mode || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
+    if (mode == 1 || mode == 3) {
+        int rc0 = setup_cstep(c);
+        if (rc0 || c->cpersistent || mode == 3) return rc0;
+    }
     DStack& s = c->main;
     std::vector<StepLayer> L(s.n_layer);
     for (int l = 0; l < s.n_layer; ++l) {
@@ -738,7 +864,59 @@ int setup_persistent(sd_ctx* c) {
 
 // Per-phase times of CTA 0 over the last persistent launch, appended to
 // SD_TRACE: for each phase kind the mean wait for its inputs and the mean work.
+void write_ctrace(sd_ctx* c, int n_steps) {
+    const CStepArgs& a = c->cstep;
+    if (c->trace_path.empty() || !a.trace_pub || n_steps < 1 || a.n_layer < 2) return;
+    const int L = a.n_layer, ns = std::min(n_steps, kTraceSteps);
+    const size_t half = (size_t)kTraceSteps * L * kCTracePhases;
+    std::vector<unsigned long long> tp(2 * half);
+    if (cudaMemcpy(tp.data(), a.trace_pub, tp.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return;
+    FILE* f = fopen(c->trace_path.c_str(), "a");
+    if (!f) return;
+    const char* pn[kCTracePhases] = {"x-ready", "qkv", "attn", "o-pub", "x'-sent", "fc", "proj-pub", "x''-sent"};
+    double dl[kCTracePhases] = {}, sp[kCTracePhases] = {};
+    int cnt = 0;
+    for (int st = 0; st < ns; ++st)
+        for (int l = 1; l < L; ++l) {
+            const unsigned long long* mx = tp.data() + ((size_t)st * L + l) * kCTracePhases;
+            const unsigned long long* mn = mx + half;
+            const unsigned long long* prev = tp.data() + ((size_t)st * L + l - 1) * kCTracePhases;
+            for (int ph = 0; ph < kCTracePhases; ++ph) {
+                const unsigned long long ref = ph == 0 ? prev[kCTracePhases - 1] : mx[ph - 1];
+                dl[ph] += (double)(long long)(mx[ph] - ref);
+                sp[ph] += (double)(long long)(mx[ph] - mn[ph]);
+            }
+            ++cnt;
+        }
+    fprintf(f, "cluster step: steps=%d clusters=%d x %d ring=%d act=%d kkc=%d\n", n_steps, a.ncl, a.cs, a.ring_bytes,
+            a.act_bytes, a.kkc);
+    fprintf(f, "  critical path per layer (us): phase: latest stamp - previous latest | latest - earliest\n");
+    double tot = 0;
+    for (int ph = 0; ph < kCTracePhases; ++ph) {
+        fprintf(f, "    %-9s %8.3f %8.3f\n", pn[ph], dl[ph] / 1e3 / cnt, sp[ph] / 1e3 / cnt);
+        tot += dl[ph] / 1e3 / cnt;
+    }
+    fprintf(f, "    layer     %8.3f\n", tot);
+    unsigned long long t[kCTraceSub];
+    if (a.trace && cudaMemcpy(t, a.trace, sizeof t, cudaMemcpyDeviceToHost) == cudaSuccess) {
+        // CTA 0's cycles per sub-step (per layer, or per step for the last four)
+        const char* nm[28] = {"wait x''", "rec qkv", "norm1", "gemv qkv", "send qkv", "wait qkv", "rope/append",
+                              "attn keys", "attn comb+send", "wait part", "combine", "rec o", "gemv o", "pub o",
+                              "reduce o", "wait x'", "rec fc", "norm2", "gemv fc", "send u", "wait u", "rec proj",
+                              "gemv proj", "pub proj", "reduce proj", "head*", "sample*", "embed*"};
+        const double nl = (double)n_steps * L;
+        fprintf(f, "  CTA 0 cycles per layer (* per step):\n   ");
+        for (int k = 0; k < 28; ++k) {
+            fprintf(f, " %s %.0f |", nm[k], (double)t[k] / (k >= 25 ? (double)n_steps : nl));
+            if (k % 7 == 6) fprintf(f, "\n   ");
+        }
+        fprintf(f, "\n");
+    }
+    fclose(f);
+}
+
 void write_trace(sd_ctx* c, int n_steps) {
+    if (c->cpersistent) return write_ctrace(c, n_steps);
     if (c->trace_path.empty() || !c->step.trace || n_steps < 1) return;
     unsigned long long t[64];
     if (cudaMemcpy(t, c->step.trace, sizeof t, cudaMemcpyDeviceToHost) != cudaSuccess) return;
@@ -1203,6 +1381,8 @@ int sd_get_info(const sd_ctx* c, sd_info* out) {
     out->kernels_per_step = c->kernels_per_step;
     out->attn_splits = c->main.nsplit;
     out->persistent = c->persistent ? c->step_grid : 0;
+    out->persistent_clusters = c->cpersistent ? c->cstep.ncl : 0;
+    out->cluster_size = c->cpersistent ? c->cstep.cs : 0;
     out->prefill = !c->gemm_prefill ? 0 : (c->tc_prefill ? 2 : 1);
     out->weight_bytes = c->weight_bytes;
     out->kv_bytes = c->kv_bytes;

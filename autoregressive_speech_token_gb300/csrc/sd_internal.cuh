@@ -230,6 +230,62 @@ int step_plan_grid(StepArgs& a, int sm_count);
 constexpr int kTraceSteps = 64, kTracePhases = 6;  // phases: layer input, QKV, attention, O, FC, proj
 cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
 
+// Cluster persistent decode step (k_cstep.cu).  The grid is `ncl` thread-block
+// clusters of `cs` CTAs; cluster c owns KV heads [c*kpc, (c+1)*kpc) with their
+// query heads, FFN activations [c*upc, (c+1)*upc) and, through split-K
+// partials, a share of every residual row.  The layer table holds repacked
+// matrices: wqkv with each cluster's q, k, v rows contiguous ([ncl][rpc][d],
+// bqkv permuted alike), wo as column slabs [ncl][d][ko], wproj as column slabs
+// [ncl][d][upc]; wfc and the head keep the row-major layout.
+struct CStepArgs {
+    int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, quant = 0;
+    float eps = 1e-5f;
+    int ncl = 0, cs = 0;                 // clusters, CTAs per cluster
+    int hpc = 0, kpc = 0;                // query heads, KV heads per cluster
+    int rpc = 0, ko = 0, upc = 0;        // QKV rows, O slab width, FFN activations per cluster
+    const StepLayer* layers = nullptr;   // device array [n_layer] (repacked matrices)
+    QMat head;
+    const float *nfg = nullptr, *nfb = nullptr, *wte = nullptr, *wpe = nullptr;
+    const float *rope_cos = nullptr, *rope_sin = nullptr;
+    __half *kc = nullptr, *vc = nullptr;
+    // exchange words (epoch << 32 | float bits)
+    unsigned long long *ll_po = nullptr;     // [ncl][B][d] O-projection partials
+    unsigned long long *ll_pp = nullptr;     // [ncl][B][d] down-projection partials
+    unsigned long long *ll_logits = nullptr; // [B][V]
+    unsigned long long *ll_tok = nullptr;    // [8][32] sampled tokens (8 replicas, one line each)
+    unsigned* gen = nullptr;
+    float* logits = nullptr;
+    int* pos = nullptr;
+    int32_t* tok = nullptr;
+    const float* u1 = nullptr;
+    const float* u_seq = nullptr;
+    int32_t* out_seq = nullptr;
+    const SampParams* sp = nullptr;
+    int* err = nullptr;
+    int n_steps = 1;
+    long long spin_budget = 0;
+    int ring_bytes = 0, act_bytes = 0;
+    int kkc = 128;                       // cached keys staged per (row, KV head) item at once
+    // byte offsets in the activation region
+    int o_x = 0, o_xn = 0, o_u = 0, o_qkv = 0, o_part = 0, o_y = 0, o_wp = 0, o_stage = 0;
+    // optional publish stamps [2][kTraceSteps][n_layer][kCTracePhases] (latest, then earliest CTA)
+    unsigned long long* trace_pub = nullptr;
+    // optional [kCTraceSub]: CTA 0's clock64 cycles per sub-step, summed over the launch
+    unsigned long long* trace = nullptr;
+};
+constexpr int kCTraceSub = 32;
+constexpr int kCTracePhases = 8;  // x ready, QKV sent, attention sent, O published, x' sent, u sent, proj published, x'' sent
+size_t cstep_smem_bytes(const CStepArgs& a);
+// Chooses ncl / cs and fills the layout fields of `a`; returns the grid size,
+// or 0 when the configuration does not fit the kernel.
+int cstep_plan(CStepArgs& a, int sm_count);
+cudaError_t launch_cstep(const CStepArgs& a, cudaStream_t st);
+// Column-slab / row-permuted copy of a Q8_0 or Q4_0 matrix for the cluster
+// step: out row (s*R + i) holds columns [s*W, (s+1)*W) of source row perm[i]
+// (perm null: i), for s < K / W.
+cudaError_t launch_slab_gather(const QMat& src, int W, const int* perm, uint8_t* q_out, __half* s_out,
+                               cudaStream_t st);
+
 // Tensor-core GEMM Y[M][N] = X[M][K] W[N][K]^T over a repacked weight, with
 // the GEMV epilogues (bias, GELU, interleaved SwiGLU -> Y[M][N/2], residual).
 struct QGemmArgs {

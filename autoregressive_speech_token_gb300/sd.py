@@ -67,7 +67,7 @@ class Info(C.Structure):
     _fields_ = [("pos", C.c_int32), ("sm_count", C.c_int32), ("kernels_per_step", C.c_int32),
                 ("attn_splits", C.c_int32), ("weight_bytes", C.c_int64), ("kv_bytes", C.c_int64),
                 ("step_h2d_bytes", C.c_int64), ("step_d2h_bytes", C.c_int64), ("persistent", C.c_int32),
-                ("prefill", C.c_int32)]
+                ("prefill", C.c_int32), ("persistent_clusters", C.c_int32), ("cluster_size", C.c_int32)]
 
 
 _lib = None

@@ -155,6 +155,8 @@ typedef struct sd_info {
     int64_t step_d2h_bytes;    /* device->host bytes one sd_step (Talker+CP: one sd_frame) copies back */
     int32_t persistent;        /* CTAs of the persistent step kernel (0: per-operation kernels) */
     int32_t prefill;           /* prompt path: 0 per-position step graphs, 1 mma.sync GEMMs, 2 tcgen05 GEMMs */
+    int32_t persistent_clusters; /* thread-block clusters of the persistent step (0: the flat kernel or none) */
+    int32_t cluster_size;      /* CTAs per cluster of the persistent step (0: the flat kernel or none) */
 } sd_info;
 int sd_get_info(const sd_ctx* ctx, sd_info* out);
 

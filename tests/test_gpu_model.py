@@ -181,10 +181,11 @@ def test_bench_configuration_gpt2m_q4(sd):
     assert _rel(z_last, ref.logits[n]) <= REL_L2
 
 
-@pytest.fixture(params=["graph", "persistent"])
+@pytest.fixture(params=["graph", "flat", "cluster"])
 def step_path(request, monkeypatch):
-    """Run a test on the per-operation graph and on the persistent step kernel."""
-    monkeypatch.setenv("SD_PERSISTENT", "1" if request.param == "persistent" else "0")
+    """Run a test on the per-operation graph, the flat persistent step kernel and
+    the cluster persistent step kernel."""
+    monkeypatch.setenv("SD_PERSISTENT", {"graph": "0", "flat": "flat", "cluster": "cluster"}[request.param])
     return request.param
 
 
@@ -235,13 +236,29 @@ def test_one_token_prompt(sd, prefill_path):
 
 
 @pytest.mark.parametrize("name", ["tiny", "gpt2m_q4", "gpt2m_q8", "llama_q4"])
-def test_persistent_kernel_is_used(sd, monkeypatch, name):
-    """The persistent step's plan accepts every GPT-2 / Llama workload (so the
-    persistent-path tests above do run the persistent kernel)."""
-    monkeypatch.setenv("SD_PERSISTENT", "1")
+@pytest.mark.parametrize("kind", ["flat", "cluster"])
+def test_persistent_kernel_is_used(sd, monkeypatch, name, kind):
+    """Both persistent step kernels' plans accept every GPT-2 / Llama workload
+    (so the persistent-path tests above do run the kernel they name)."""
+    monkeypatch.setenv("SD_PERSISTENT", kind)
     run = get_preset(name)
     dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
-    assert dec.info().persistent > 0 and dec.info().kernels_per_step == 1
+    info = dec.info()
+    assert info.persistent > 0 and info.kernels_per_step == 1
+    if kind == "cluster":
+        assert info.persistent_clusters > 0 and info.cluster_size > 1
+        assert info.persistent == info.persistent_clusters * info.cluster_size
+        print(f"[{name}] cluster step: {info.persistent_clusters} clusters x {info.cluster_size} CTAs")
+    else:
+        assert info.persistent_clusters == 0
+    dec.close()
+
+
+def test_default_one_row_path_is_the_cluster_step(sd, monkeypatch):
+    monkeypatch.delenv("SD_PERSISTENT", raising=False)
+    run = get_preset("gpt2m_q4")
+    dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
+    assert dec.info().persistent_clusters > 0
     dec.close()
 
 
