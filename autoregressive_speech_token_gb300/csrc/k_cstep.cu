@@ -32,9 +32,15 @@
 //   cluster's column slab of the down projection for its rows -- exchange 2
 //   as exchange 1.
 //
-// Weights reach each CTA through the producer warp's bulk-copy ring, as in
-// the flat persistent step; every wait (exchange word, mbarrier, ring) is
-// bounded, and on expiry the kernel records an error and returns.
+// Every matvec is a run of mma.sync m16n8k16 over 16-row tiles of exact fp16
+// codes against the activations split into fp16 hi and lo parts (see the
+// tensor-core matvec below): the decode step's arithmetic is issue-bound on
+// CUDA cores at this grid size, and the tensor cores take a 16 x 16 block of
+// weights per instruction.  Weights reach each CTA through a ring of bulk
+// asynchronous copies in shared memory, issued by thread 0 whenever it is
+// about to wait anyway, as far ahead as the ring holds; every wait (exchange
+// word, mbarrier, ring) is bounded, and on expiry the kernel records an error,
+// finishes the step on whatever data it has and returns.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -56,7 +62,9 @@ using namespace stepdev;
 constexpr int kNMB = 16;      // weight records in flight at most (a power of two)
 constexpr int kTokRep = 8;    // replicas of the sampled-token word
 
-enum XB { XB_QKV = 0, XB_PART = 1, XB_X = 2, XB_U = 3 };
+// exchange barriers: q/k/v rows, attention partials, residual rows after the O projection (x')
+// and after the down projection (x''), FFN activations -- one phase per layer each
+enum XB { XB_QKV = 0, XB_PART = 1, XB_X0 = 2, XB_X1 = 3, XB_U = 4 };
 
 // ------------------------------------------------------------------ cluster primitives
 
@@ -70,7 +78,7 @@ __device__ __forceinline__ uint32_t cluster_index() {
     asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
 }
-// every thread of every CTA of the cluster (the producer warp included)
+// every thread of every CTA of the cluster
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -89,6 +97,20 @@ __device__ __forceinline__ void st_async(uint32_t raddr, float v, uint32_t rmb) 
 // write that happens before it -- the KV-cache append among them
 __device__ __forceinline__ void mb_arrive_remote(uint32_t rmb) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rmb) : "memory");
+}
+// non-blocking test of an mbarrier phase (this CTA's view)
+__device__ __forceinline__ bool mb_test(uint32_t mb, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// one arrival on this CTA's mbarrier (release at CTA scope)
+__device__ __forceinline__ void mb_arrive_local(uint32_t mb) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mb) : "memory");
 }
 __device__ __forceinline__ void mb_init_n(uint32_t mb, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mb), "r"(n) : "memory");
@@ -123,19 +145,35 @@ __device__ bool xb_wait(uint32_t mb, uint32_t parity, int* err, long long budget
     }
 }
 
+// ------------------------------------------------------------------ fragment-major weights
+
+// The cluster step's matrices are stored 16 rows (a tile) by 32 columns (a
+// block) at a time, in the order the tensor-core matvec consumes them: per
+// (tile, block), the 32 lanes' code words for rows g and g + 8 of the tile
+// (lane 4g + t) -- Q4_0: the word of code bytes 4t..4t+3 of each row, Q8_0:
+// the two words of code bytes 8t..8t+7 -- then, after all (tile, block)
+// pairs of the matrix, the tiles' fp16 block scales [tile][block][16 rows].
+// A warp's loads of one (tile, block) are then 256 (Q4_0) or 512 (Q8_0)
+// contiguous bytes, free of bank conflicts, and a range of whole tiles is one
+// contiguous copy.  Rows past the matrix end are zero codes with zero scales.
+template <int QK>
+struct Frag {
+    static constexpr int W = (QK == SD_Q4_0) ? 1 : 2;  // code words per lane per row and block
+    static constexpr int TB = 256 * W;                 // code bytes of one (tile, block)
+};
+__host__ __device__ __forceinline__ int frag_tb(int quant) { return quant == SD_Q4_0 ? 256 : 512; }
+
 // ------------------------------------------------------------------ weight records
 
-// One phase's record for this CTA: code rows [r0, r1) of a matrix (scale
-// window widened to 16 bytes), bias rows [br0, br0 + r1 - r0) (window widened
-// likewise), and the norm gains.
+// One phase's record for this CTA: tiles [t0, t0 + nt) of a fragment-major
+// matrix (codes, then scales), the bias of rows [br0, br0 + nr) (window widened
+// to 16 bytes), and the norm gains (padded layout).  Pointers are per layer.
 struct CSlice {
-    const uint8_t* q;
-    const uint8_t* s;
-    const float *bias, *g1, *g2;
-    int r0, r1, br0, row_bytes, srow, s_lo, b_lo, K;
+    int t0, nt, nr, br0, KB;
     int o_sc, o_bias, o_g1, o_g2;
-    int n_codes, n_sc, n_bias, n_g;
+    int n_codes, n_sc, n_bias, n_g, b_lo;
     int bytes;
+    int has_bias, has_g1, has_g2;
 };
 
 // matrix, bias and gains of slice kind k (0 QKV, 1 O, 2 FC, 3 proj, 4 head) of layer l
@@ -150,205 +188,352 @@ __device__ __forceinline__ void kind_ptrs(const CStepArgs& a, const StepLayer* t
     if (!a.gpt2) g2 = nullptr;  // RMSNorm: gain only
 }
 
+// tiles [t0, t1) of N tiles for part i of G (in whole tiles)
+__host__ __device__ __forceinline__ void tile_range(int N, int i, int G, int& t0, int& t1) {
+    t0 = N * i / G;
+    t1 = N * (i + 1) / G;
+}
+
 __device__ CSlice make_cslice(const CStepArgs& a, const StepLayer* tab, int kind, int cl, int rank) {
     const int G = a.ncl * a.cs, gi = cl * a.cs + rank;
     const QMat* W;
     const float *bias, *g1, *g2;
     kind_ptrs(a, tab, kind, 0, W, bias, g1, g2);
     CSlice s;
-    int r0, r1, br0;
+    int t0, t1;
     if (kind == 0) {
-        row_range(a.rpc, rank, a.cs, r0, r1);
-        r0 += cl * a.rpc; r1 += cl * a.rpc; br0 = r0;
+        const int N = a.rpc / 16;
+        tile_range(N, rank, a.cs, t0, t1);
+        t0 += cl * N; t1 += cl * N;
+        s.br0 = 16 * t0;
+        s.nr = 16 * (t1 - t0);
     } else if (kind == 1 || kind == 3) {
-        row_range(a.d, rank, a.cs, r0, r1);
-        br0 = r0;
-        r0 += cl * a.d; r1 += cl * a.d;
+        const int N = a.d / 16;
+        tile_range(N, rank, a.cs, t0, t1);
+        s.br0 = 16 * t0;  // residual rows of this rank
+        s.nr = 16 * (t1 - t0);
+        t0 += cl * N; t1 += cl * N;
     } else if (kind == 2) {
-        row_range(a.upc, rank, a.cs, r0, r1);
-        r0 += cl * a.upc; r1 += cl * a.upc;
-        if (!a.gpt2) { r0 *= 2; r1 *= 2; }  // gate/up rows interleaved in pairs
-        br0 = r0;
+        const int N = (a.gpt2 ? a.upc : 2 * a.upc) / 16;  // gate/up rows interleaved in pairs
+        tile_range(N, rank, a.cs, t0, t1);
+        t0 += cl * N; t1 += cl * N;
+        s.br0 = 16 * t0;
+        s.nr = 16 * (t1 - t0);
     } else {
-        row_range(a.V, gi, G, r0, r1);
-        br0 = r0;
+        tile_range((a.V + 15) / 16, gi, G, t0, t1);
+        s.br0 = 16 * t0;
+        s.nr = min(16 * t1, a.V) - 16 * t0;
     }
-    s.r0 = r0; s.r1 = r1; s.br0 = br0;
-    s.K = W->cols;
-    s.row_bytes = W->kind == SD_Q4_0 ? W->cols / 2 : W->cols;
-    s.srow = (W->cols / 32) * 2;
-    const int nr = r1 - r0;
-    s.n_codes = nr * s.row_bytes;
-    s.s_lo = (r0 * s.srow) & ~15;
-    s.n_sc = (((r1 * s.srow) + 15) & ~15) - s.s_lo;
-    s.o_sc = (s.n_codes + 15) & ~15;
+    s.t0 = t0;
+    s.nt = t1 - t0;
+    s.KB = W->cols / 32;
+    s.n_codes = s.nt * s.KB * frag_tb(W->kind);
+    s.n_sc = s.nt * s.KB * 32;
+    s.o_sc = s.n_codes;
     int off = s.o_sc + s.n_sc;
-    s.b_lo = br0 & ~3;
-    s.n_bias = bias ? ((((br0 + nr + 3) & ~3) - s.b_lo) * 4) : 0;
+    s.b_lo = s.br0 & ~3;
+    s.n_bias = bias ? ((((s.br0 + s.nr + 3) & ~3) - s.b_lo) * 4) : 0;
     s.o_bias = off;
     off += s.n_bias;
-    s.n_g = g1 ? a.d * 4 : 0;
+    s.n_g = g1 ? padded(a.d) * 4 : 0;  // gains are stored in the padded activation layout
     s.o_g1 = off;
     off += s.n_g;
     s.o_g2 = off;
     off += g2 ? s.n_g : 0;
     s.bytes = (off + 127) & ~127;
-    s.q = nullptr; s.s = nullptr;
-    s.bias = bias; s.g1 = g1; s.g2 = g2;  // presence only; pointers per layer in cslice_at
+    s.has_bias = bias != nullptr;
+    s.has_g1 = g1 != nullptr;
+    s.has_g2 = g2 != nullptr;
     return s;
 }
 
-// slice j of a step (4 per layer, then the head): the per-kind geometry with
-// this layer's pointers
-__device__ __forceinline__ CSlice cslice_at(const CStepArgs& a, const StepLayer* tab, const CSlice* geo, int j) {
-    const int L = a.n_layer;
-    const int kind = j < 4 * L ? (j & 3) : 4;
-    const int l = j >> 2;
-    CSlice s = geo[kind];
-    const QMat* W;
-    const float *bias, *g1, *g2;
-    kind_ptrs(a, tab, kind, l < L ? l : 0, W, bias, g1, g2);
-    s.q = W->q + (size_t)s.r0 * s.row_bytes;
-    s.s = reinterpret_cast<const uint8_t*>(W->s) + s.s_lo;
-    s.bias = (s.bias && bias) ? bias + s.b_lo : nullptr;
-    s.g1 = s.g1 ? g1 : nullptr;
-    s.g2 = s.g2 ? g2 : nullptr;
-    return s;
+// ------------------------------------------------------------------ tensor-core matvec over a record
+
+// The record's rows are the M = 16 side of mma.sync m16n8k16: the codes are
+// small integers, exact in fp16 (byte v placed under the exponent of 1024 is
+// the half 1024 + v; one half2 subtraction removes the offset), and the fp32
+// activations enter as B columns 2b (hi = fp16(x)) and 2b + 1 (lo = fp16(x -
+// hi)), so x = hi + lo to 22 bits and every product is exact in fp32.  A
+// block's two 16-wide k-steps accumulate in fp32 and are scaled by the rows'
+// block scales.  Inside a block the MMA k index is permuted -- the same
+// permutation for codes and activations, so the dot product is unchanged --
+// so that a lane's codes of a row are one word per step: step s of a block
+// takes elements 16s + 4t + j (Q4_0: low nibbles of code bytes 4t..4t+3 for
+// s = 0, high nibbles for s = 1) or 8t + 4s + j (Q8_0: code bytes 8t..8t+7),
+// j = 0..3, which sit at k = 2t, 2t+1 (j = 0, 1) and 2t+8, 2t+9 (j = 2, 3).
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ------------------------------------------------------------------ matvec over a record
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
 
-// y[i * NB + b] = sum_k W[i][k] x[b][k] for the record's rows i < nr (codes
-// row-major, fp16 block scales [nr][K/32] at sc); x rows are in the padded
-// layout with row stride xs.  A row is split over LPR lanes (LPR = the row's
-// 16-byte units, rounded up to a power of two, at most 32), each lane keeping
-// the activations of its units in registers; a warp visits RPW = 32 / LPR rows
-// at once, two row groups per iteration.  The LPR lane sums meet by xor
-// shuffles (a fixed order).
+// the four codes of word w (elements j = 0..3) of step s -> halves for
+// k = 2t, 2t+1 (lo) and 2t+8, 2t+9 (hi)
+template <int QK>
+__device__ __forceinline__ void code_pair(uint32_t w, int s, uint32_t& lo, uint32_t& hi) {
+    uint32_t off;
+    if constexpr (QK == SD_Q4_0) {
+        w = (s ? (w >> 4) : w) & 0x0F0F0F0Fu;
+        off = 0x64086408u;  // 1024 + 8
+    } else {
+        w ^= 0x80808080u;   // signed byte v -> v + 128
+        off = 0x64806480u;  // 1024 + 128
+    }
+    lo = hsub2_u(__byte_perm(w, 0x64646464u, 0x4140), off);
+    hi = hsub2_u(__byte_perm(w, 0x64646464u, 0x4342), off);
+}
+
+// Half index of element e (of a K-long activation row) in the B-fragment
+// buffer [block][step][column][lane t][4 halves j]; batch row b's hi part is
+// column 2b, its lo part column 2b + 1.
 template <int QK, int NB>
-__device__ void cgemv(const uint8_t* codes, const uint8_t* sc, int K, int nr, const float* x, int xs, float* y) {
-    constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;
-    constexpr int MAXU = (QK == SD_Q4_0) ? 1 : 2;
-    const int UPR = K / EPU;
-    const int LPR = UPR >= 32 ? 32 : ((UPR & (UPR - 1)) ? 32 : UPR);
-    const int RPW = 32 / LPR;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane % LPR, rl = lane / LPR;
-    const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K, spr = K >> 5;
-    const int step = kWarps * RPW;
-    const __half* sh = reinterpret_cast<const __half*>(sc);
-    if (warp * RPW < nr) {
-        float xr[NB][MAXU * EPU];
+__device__ __forceinline__ int bf_index(int e, int col) {
+    const int kb = e >> 5, r = e & 31, j = r & 3;
+    int s, t;
+    if (QK == SD_Q4_0) { s = r >> 4; t = (r >> 2) & 3; }
+    else { t = r >> 3; s = (r >> 2) & 1; }
+    return ((((kb * 2 + s) * 2 * NB + col) * 4 + t) << 2) + j;
+}
+
+template <int QK, int NB>
+__device__ __forceinline__ void bf_put(__half* bf, int e, int b, float x) {
+    const __half h = __float2half_rn(x);
+    bf[bf_index<QK, NB>(e, 2 * b)] = h;
+    bf[bf_index<QK, NB>(e, 2 * b + 1)] = __float2half_rn(x - __half2float(h));
+}
+
+// B fragments of activation rows src[b][pidx(k)] (row stride ss), k < K, as
+// they are.  Ends with a CTA barrier.
+template <int QK, int NB>
+__device__ void bf_plain(const float* src, int ss, int K, __half* bf) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
+    for (int b = 0; b < NB; ++b)
+        for (int e = threadIdx.x; e < K; e += kThreads) bf_put<QK, NB>(bf, e, b, src[b * ss + pidx(e)]);
+    csync();
+}
+
+// B fragments of the LayerNorm (biased variance) or RMSNorm of x[b][pidx(k)],
+// k < K <= 2 * kThreads, with gains g1 and offsets g2 in the padded layout.
+// One pass: the sums of (x - c) and (x - c)^2 with the shift c = x[0] (the
+// shifted-data variance, exact in real arithmetic and free of the cancellation
+// of the plain one-pass form when |mean| >> deviation), per warp by shuffles,
+// then across the warps through `red` (>= 4 * NB * kWarps floats, each warp
+// reducing the table again by shuffles in a fixed order).  Ends with a CTA
+// barrier.
+template <int QK, int NB>
+__device__ void bf_norm(const float* x, int xs, int K, bool ln, const float* g1, const float* g2, float eps,
+                        float* red, __half* bf) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float v[NB][2], c[NB];
 #pragma unroll
-            for (int j = 0; j < MAXU; ++j) {
-                const int u = sub + j * LPR;
+    for (int b = 0; b < NB; ++b) {
+        c[b] = ln ? x[b * xs] : 0.f;
+        float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-                for (int t = 0; t < EPU; t += 4) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (u < UPR) v = *reinterpret_cast<const float4*>(&x[b * xs + pidx(u * EPU + t)]);
-                    xr[b][j * EPU + t] = v.x; xr[b][j * EPU + t + 1] = v.y;
-                    xr[b][j * EPU + t + 2] = v.z; xr[b][j * EPU + t + 3] = v.w;
-                }
-            }
-        for (int i0 = warp * RPW; i0 < nr; i0 += 2 * step) {
-            const int i1 = i0 + rl, i2 = i0 + step + rl;
-            const bool v1 = i1 < nr, v2 = i2 < nr;
-            float a1[NB], a2[NB];
+        for (int j = 0; j < 2; ++j) {
+            const int e = tid + j * kThreads;
+            v[b][j] = e < K ? x[b * xs + pidx(e)] : 0.f;
+            const float dv = e < K ? v[b][j] - c[b] : 0.f;
+            s1 += dv;
+            s2 = fmaf(dv, dv, s2);
+        }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) { a1[b] = 0.f; a2[b] = 0.f; }
+        for (int o = 16; o > 0; o >>= 1) {
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        }
+        if (lane == 0) {
+            red[(2 * b) * kWarps + warp] = s1;
+            red[(2 * b + 1) * kWarps + warp] = s2;
+        }
+    }
+    csync();
+    const float inv = 1.0f / (float)K;
 #pragma unroll
-            for (int j = 0; j < MAXU; ++j) {
-                const int u = sub + j * LPR;
-                if (u < UPR) {
-                    const int e = u * EPU, off = (QK == SD_Q4_0) ? (e >> 1) : e;
-                    uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1;
-                    float d1 = 0.f, d2 = 0.f;
-                    if (v1) {
-                        w1 = *reinterpret_cast<const uint4*>(codes + (size_t)i1 * row_bytes + off);
-                        d1 = __half2float(sh[(size_t)i1 * spr + (e >> 5)]);
-                    }
-                    if (v2) {
-                        w2 = *reinterpret_cast<const uint4*>(codes + (size_t)i2 * row_bytes + off);
-                        d2 = __half2float(sh[(size_t)i2 * spr + (e >> 5)]);
-                    }
+    for (int b = 0; b < NB; ++b) {
+        float s1 = lane < kWarps ? red[(2 * b) * kWarps + lane] : 0.f;
+        float s2 = lane < kWarps ? red[(2 * b + 1) * kWarps + lane] : 0.f;
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const float t1 = (QK == SD_Q4_0) ? dot4_q4(w1, &xr[b][0]) : dot4_s8(w1, &xr[b][j * EPU]);
-                        a1[b] = fmaf(d1, t1, a1[b]);
-                        if (v2) {
-                            const float t2 =
-                                (QK == SD_Q4_0) ? dot4_q4(w2, &xr[b][0]) : dot4_s8(w2, &xr[b][j * EPU]);
-                            a2[b] = fmaf(d2, t2, a2[b]);
-                        }
-                    }
-                }
-            }
-            for (int o = 1; o < LPR; o <<= 1)
+        for (int o = 16; o > 0; o >>= 1) {  // lanes past the table hold zeros; every lane gets the totals
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        }
+        const float m1 = s1 * inv;  // mean of x - c
+        const float var = ln ? fmaxf(s2 * inv - m1 * m1, 0.f) : s2 * inv;
+        const float mu = ln ? c[b] + m1 : 0.f;
+        const float r = 1.0f / sqrtf(var + eps);
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    a1[b] += __shfl_xor_sync(0xffffffffu, a1[b], o);
-                    a2[b] += __shfl_xor_sync(0xffffffffu, a2[b], o);
-                }
-            if (sub == 0) {
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (v1) y[i1 * NB + b] = a1[b];
-                    if (v2) y[i2 * NB + b] = a2[b];
-                }
-            }
+        for (int j = 0; j < 2; ++j) {
+            const int e = tid + j * kThreads;
+            if (e >= K) continue;
+            const float gg = g1[pidx(e)];
+            const float y = ln ? fmaf((v[b][j] - mu) * r, gg, g2[pidx(e)]) : v[b][j] * r * gg;
+            bf_put<QK, NB>(bf, e, b, y);
         }
     }
     csync();
 }
 
+// sum_k W[i][k] x[b][k] for the record's rows i < nr (tiles of fragment-major
+// codes and scales), x given as B fragments.  Units of (tile, k-slice) go to
+// the warps -- KS slices per tile, as many as leave no warp idle -- and each
+// unit's partial sums go to red[unit][16][NB]; after a CTA barrier the slices
+// are added in order and emit(i, b, y) (PAIRS: emit(i, b, y_2i, y_2i+1) for
+// row pairs) runs once per output.  The codes are read straight from the
+// record in shared memory.
+template <int QK, int NB, bool PAIRS, typename Emit>
+__device__ __forceinline__ void mma_rows(const uint8_t* codes, const uint8_t* sc, int K, int nt, int nr,
+                                         const __half* bf, float* red, Emit&& emit) {
+    constexpr int W = Frag<QK>::W;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int KB = K >> 5;
+    int KS = kWarps / nt;
+    if (KS < 1) KS = 1;
+    if (KS > KB) KS = KB;
+    const int units = nt * KS;
+    const __half* sh = reinterpret_cast<const __half*>(sc);
+    const uint2* bfv = reinterpret_cast<const uint2*>(bf);
+    for (int u = warp; u < units; u += kWarps) {
+        const int rt = u / KS, s = u - rt * KS;
+        const int kb0 = KB * s / KS, kb1 = KB * (s + 1) / KS;
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 2
+        for (int kb = kb0; kb < kb1; ++kb) {
+            const int tb = rt * KB + kb;
+            uint32_t w0[W], w1[W];
+            if constexpr (W == 1) {
+                const uint2 aw = reinterpret_cast<const uint2*>(codes)[tb * 32 + lane];
+                w0[0] = aw.x;
+                w1[0] = aw.y;
+            } else {
+                const uint4 aw = reinterpret_cast<const uint4*>(codes)[tb * 32 + lane];
+                w0[0] = aw.x; w0[W - 1] = aw.y;
+                w1[0] = aw.z; w1[W - 1] = aw.w;
+            }
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int st = 0; st < 2; ++st) {
+                uint32_t a0, a1, a2, a3;
+                code_pair<QK>(w0[W == 1 ? 0 : st], st, a0, a2);
+                code_pair<QK>(w1[W == 1 ? 0 : st], st, a1, a3);
+                uint2 bb = make_uint2(0u, 0u);
+                if (g < 2 * NB) bb = bfv[((kb * 2 + st) * 2 * NB + g) * 4 + t];
+                mma16816(c, a0, a1, a2, a3, bb.x, bb.y);
+            }
+            const float d0 = __half2float(sh[tb * 16 + g]), d1 = __half2float(sh[tb * 16 + g + 8]);
+            acc0 = fmaf(d0, c[0] + c[1], acc0);
+            acc1 = fmaf(d1, c[2] + c[3], acc1);
+        }
+        if (t < NB) {
+            red[(u * 16 + g) * NB + t] = acc0;
+            red[(u * 16 + g + 8) * NB + t] = acc1;
+        }
+    }
+    csync();
+    if (PAIRS) {
+        for (int i = tid; i < (nr >> 1) * NB; i += kThreads) {
+            const int k = NB == 1 ? i : i / NB, b = i - k * NB;
+            const int r0 = 2 * k, rt = r0 >> 4, rr = r0 & 15;
+            float v0 = 0.f, v1 = 0.f;
+            for (int s = 0; s < KS; ++s) {
+                v0 += red[((rt * KS + s) * 16 + rr) * NB + b];
+                v1 += red[((rt * KS + s) * 16 + rr + 1) * NB + b];
+            }
+            emit(k, b, v0, v1);
+        }
+    } else {
+        for (int i = tid; i < nr * NB; i += kThreads) {
+            const int row = NB == 1 ? i : i / NB, b = i - row * NB;
+            const int rt = row >> 4, rr = row & 15;
+            float v = 0.f;
+            for (int s = 0; s < KS; ++s) v += red[((rt * KS + s) * 16 + rr) * NB + b];
+            emit(row, b, v, 0.f);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ attention over the rank's keys
 
-// One warp's online-softmax pass over keys [0, nk) of a staged sub-chunk
-// (K and V rows of HD halves): LPK = HD / 8 lanes per key, each holding 8
-// dimensions; KPP = 32 / LPK keys per warp pass.  (m: running max, uniform
-// over the warp; l and o: per key slot, summed over the slots at the end.)
+// One warp's pass over keys [j0, j0 + 32) of a staged sub-chunk of nk keys
+// (rows of HD halves): lane = key.  A lane forms its key's score over the
+// whole head dimension, reading the row's 16-byte chunks in an order rotated
+// by the lane so that a quarter warp touches distinct bank groups; the warp
+// keeps an online softmax (m, l: uniform over the warp; o: DPL dimensions per
+// lane) and accumulates p V with lanes over dimensions.
 template <int HD>
-__device__ __forceinline__ void attn_keys(const float (&q)[8], const __half* Ks, const __half* Vs, int nk, float& m,
-                                          float& l, float (&o)[8]) {
-    constexpr int LPK = HD / 8, KPP = 32 / LPK;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ks = lane / LPK, dg = lane % LPK;
-    for (int j0 = warp * KPP; j0 < nk; j0 += kWarps * KPP) {
-        const int j = j0 + ks;
-        const bool valid = j < nk;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-        if (valid) {
-            kv = *reinterpret_cast<const uint4*>(Ks + (size_t)j * HD + dg * 8);
-            vv = *reinterpret_cast<const uint4*>(Vs + (size_t)j * HD + dg * 8);
+__device__ __forceinline__ void attn_lk(const float* q, const __half* Ks, const __half* Vs, int j0, int nk, float& m,
+                                        float& l, float (&o)[HD / 32]) {
+    constexpr int CH = HD / 8, DPL = HD / 32;
+    const int lane = threadIdx.x & 31;
+    const int j = j0 + lane;
+    const bool valid = j < nk;
+    float s = -INFINITY;
+    if (valid) {
+        const __half* kr = Ks + (size_t)j * HD;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int cc = (c + lane) & (CH - 1);
+            const uint4 kv = *reinterpret_cast<const uint4*>(kr + cc * 8);
+            const float4 qa = *reinterpret_cast<const float4*>(q + cc * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(q + cc * 8 + 4);
+            const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
+            const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
+            const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
+            const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
+            s0 = fmaf(qa.x, k0.x, s0);
+            s1 = fmaf(qa.y, k0.y, s1);
+            s2 = fmaf(qa.z, k1.x, s2);
+            s3 = fmaf(qa.w, k1.y, s3);
+            s0 = fmaf(qb.x, k2.x, s0);
+            s1 = fmaf(qb.y, k2.y, s1);
+            s2 = fmaf(qb.z, k3.x, s2);
+            s3 = fmaf(qb.w, k3.y, s3);
         }
-        const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
-        const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
-        const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
-        const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
-        float s = fmaf(q[0], k0.x, q[1] * k0.y) + fmaf(q[2], k1.x, q[3] * k1.y);
-        s += fmaf(q[4], k2.x, q[5] * k2.y) + fmaf(q[6], k3.x, q[7] * k3.y);
-#pragma unroll
-        for (int w = 1; w < LPK; w <<= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-        s = valid ? s : -INFINITY;
-        float pm = s;
-#pragma unroll
-        for (int w = LPK; w < 32; w <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, w));
-        const float mn = fmaxf(m, pm);  // finite: key j0 (slot 0) is valid
-        const float corr = expf(m - mn);
-        const float p = valid ? expf(s - mn) : 0.f;
-        l = fmaf(l, corr, p);
-        const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
-        const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
-        const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(&vv.z));
-        const float2 v3 = __half22float2(*reinterpret_cast<const __half2*>(&vv.w));
-        o[0] = fmaf(o[0], corr, p * v0.x); o[1] = fmaf(o[1], corr, p * v0.y);
-        o[2] = fmaf(o[2], corr, p * v1.x); o[3] = fmaf(o[3], corr, p * v1.y);
-        o[4] = fmaf(o[4], corr, p * v2.x); o[5] = fmaf(o[5], corr, p * v2.y);
-        o[6] = fmaf(o[6], corr, p * v3.x); o[7] = fmaf(o[7], corr, p * v3.y);
-        m = mn;
+        s = (s0 + s1) + (s2 + s3);
     }
+    float mx = s;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+    const float mn = fmaxf(m, mx);  // finite: key j0 (lane 0) is valid
+    const float corr = expf(m - mn);
+    const float p = valid ? expf(s - mn) : 0.f;
+    l = fmaf(l, corr, warp_sum(p));
+    float ov[DPL];
+#pragma unroll
+    for (int dd = 0; dd < DPL; ++dd) ov[dd] = 0.f;
+    const int cnt = min(32, nk - j0);
+    const __half* vr = Vs + (size_t)j0 * HD + lane * DPL;
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        if (jj >= cnt) continue;  // warp-uniform
+        if (DPL == 2) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(vr + (size_t)jj * HD));
+            ov[0] = fmaf(pj, v.x, ov[0]);
+            ov[1] = fmaf(pj, v.y, ov[1]);
+        } else {
+            const uint2 vv = *reinterpret_cast<const uint2*>(vr + (size_t)jj * HD);
+            const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
+            const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
+            ov[0] = fmaf(pj, v0.x, ov[0]);
+            ov[1] = fmaf(pj, v0.y, ov[1]);
+            ov[DPL - 2] = fmaf(pj, v1.x, ov[DPL - 2]);
+            ov[DPL - 1] = fmaf(pj, v1.y, ov[DPL - 1]);
+        }
+    }
+#pragma unroll
+    for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(o[dd], corr, ov[dd]);
+    m = mn;
 }
 
 // ------------------------------------------------------------------ cross-cluster reduction
@@ -359,23 +544,25 @@ __device__ __forceinline__ void attn_keys(const float (&q)[8], const __half* Ks,
 // take clusters j, j + TPR, ... in increasing order and meet by xor shuffles
 // -- then bias and the residual are added and the row is sent to every rank of
 // the cluster (st.async into x, completing on its mbarrier mb_x).  All loads of
-// a lane are issued before the first is waited for.  False on a timeout.
+// a lane are issued before the first is waited for.  A wait that expires
+// leaves the error word set and the sum undefined (the step is then abandoned).
 template <int NB>
-__device__ bool reduce_bcast(const unsigned long long* P, int ncl, int d, int xr0, int nr, unsigned e,
+__device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr0, int nr, unsigned e,
                              const float* bias, const float* xs, int PD, uint32_t a_x, uint32_t mb_x, int cs, int* err,
                              long long budget) {
-    int TPR = 1;
-    while (TPR < 8 && 2 * TPR <= ncl && 2 * TPR * nr * NB <= kThreads) TPR <<= 1;
+    int lt = 0;  // TPR = 1 << lt
+    while (lt < 3 && (2 << lt) <= ncl && (2 << lt) * nr * NB <= kThreads) ++lt;
+    const int TPR = 1 << lt;
     const int total = nr * NB * TPR;
     bool ok = true;
     for (int base = 0; base < total; base += kThreads) {
         const int t = base + (int)threadIdx.x;
         const bool valid = t < total;
-        const int ib = t / TPR, j = t - ib * TPR;
+        const int ib = t >> lt, j = t & (TPR - 1);
         const int i = ib / NB, b = ib - i * NB;
         float acc = 0.f;
-        if (valid && ok) {
-            for (int c0 = j; c0 < ncl && ok; c0 += 4 * TPR) {
+        if (valid) {
+            for (int c0 = j; c0 < ncl; c0 += 4 * TPR) {
                 unsigned long long w[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -385,8 +572,8 @@ __device__ bool reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c = c0 + q * TPR;
-                    if (c >= ncl || !ok) continue;
-                    if ((unsigned)(w[q] >> 32) != e)
+                    if (c >= ncl) continue;
+                    if (ok && (unsigned)(w[q] >> 32) != e)
                         ok = ll_spin(P + ((size_t)c * NB + b) * d + xr0 + i, e, &w[q], err, budget);
                     acc += __uint_as_float((unsigned)w[q]);
                 }
@@ -394,183 +581,196 @@ __device__ bool reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
         }
         for (int o = 1; o < TPR; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         float v = 0.f;
-        if (valid && ok) {
+        if (valid) {
             if (bias) acc += bias[i];
             v = xs[b * PD + pidx(xr0 + i)] + acc;
         }
         __syncwarp();  // every lane of the group has read the old row before one of them overwrites it
-        if (valid && ok) {
+        if (valid) {
             const uint32_t addr = a_x + 4u * (uint32_t)(b * PD + pidx(xr0 + i));
             for (int dst = j; dst < cs; dst += TPR) st_async(mapa(addr, dst), v, mapa(mb_x, dst));
         }
     }
-    return ok;
 }
 
 // ------------------------------------------------------------------ the kernel
 
-struct Geo {
-    int cl, rank, gi, G;
-    int xr0, xr1, qr0, qr1, fr0, fr1, hr0, hr1;
-};
+constexpr int kCBlock = kThreads;  // 16 warps, no producer warp: a thread may hold 128 registers
 
 template <int QK, int NB>
-__global__ void __launch_bounds__(kBlock, 1) k_cstep(const CStepArgs a) {
+__global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
     unsigned char* ring = sm;
     unsigned char* actb = sm + a.ring_bytes;
-    float* xs = reinterpret_cast<float*>(actb + a.o_x);     // [NB][padded(d)] residual rows
-    float* xn = reinterpret_cast<float*>(actb + a.o_xn);    // [NB][padded(kin)] matvec input
-    float* ub = reinterpret_cast<float*>(actb + a.o_u);     // [NB][padded(upc)] cluster FFN activations
-    float* qkv = reinterpret_cast<float*>(actb + a.o_qkv);  // [NB][rpc] cluster q, k, v rows
+    float* xs = reinterpret_cast<float*>(actb + a.o_x);       // [NB][padded(d)] residual rows
+    float* ub = reinterpret_cast<float*>(actb + a.o_u);       // [NB][padded(upc)] cluster FFN activations
+    float* qkv = reinterpret_cast<float*>(actb + a.o_qkv);    // [NB][rpc] cluster q, k, v rows
     float* part = reinterpret_cast<float*>(actb + a.o_part);  // [cs][NB * hpc][hd + 4] rank partials
-    float* ys = reinterpret_cast<float*>(actb + a.o_y);     // [rows][NB] matvec output
-    float* wp = reinterpret_cast<float*>(actb + a.o_wp);    // [16][hd + 4] warp partials
+    float* wq = reinterpret_cast<float*>(actb + a.o_wq);      // [16][hd] each warp's rotated query
+    float* wp = reinterpret_cast<float*>(actb + a.o_wp);      // [16][hd + 4] warp partials
+    __half* bf = reinterpret_cast<__half*>(actb + a.o_bf);    // B fragments of the current matvec input
+    float* red = reinterpret_cast<float*>(actb + a.o_red);    // matvec partial sums
     __half* stg = reinterpret_cast<__half*>(actb + a.o_stage);  // K then V [NB * kpc][kkc][hd]
     StepLayer* tab = reinterpret_cast<StepLayer*>(sm + a.ring_bytes + a.act_bytes);
-    __shared__ __align__(8) unsigned long long s_mb[kNMB];
-    __shared__ __align__(8) unsigned long long s_xb[4];
+    __shared__ __align__(8) unsigned long long s_mb[kNMB];     // record landed
+    __shared__ __align__(8) unsigned long long s_empty[kNMB];  // record consumed by every warp
+    __shared__ __align__(8) unsigned long long s_xb[5];        // exchange phases received
+    __shared__ __align__(8) unsigned long long s_kv;           // KV staging landed
     __shared__ long long s_rec[kNMB];
     __shared__ int s_off[kNMB];
-    __shared__ int s_nc, s_done;
-    __shared__ __align__(16) float s_red[64];
     __shared__ int s_tok[2];
+    __shared__ __align__(16) float s_red[4 * 2 * kWarps];
     __shared__ sample_detail::SampleScratch s_samp;
     __shared__ CSlice s_geo[5];
     __shared__ unsigned long long s_trc[kCTraceSub];
 
-    const int tid = threadIdx.x;
-    Geo g;
-    g.cl = (int)cluster_index();
-    g.rank = (int)cluster_rank();
-    g.G = a.ncl * a.cs;
-    g.gi = g.cl * a.cs + g.rank;
-    row_range(a.d, g.rank, a.cs, g.xr0, g.xr1);
-    row_range(a.rpc, g.rank, a.cs, g.qr0, g.qr1);
-    row_range(a.upc, g.rank, a.cs, g.fr0, g.fr1);
-    row_range(a.V, g.gi, g.G, g.hr0, g.hr1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cl = (int)cluster_index(), rank = (int)cluster_rank();
+    const int gi = cl * a.cs + rank;
     const int L = a.n_layer, d = a.d, hd = a.hd, cs = a.cs;
     const int per_step = 4 * L + 1, total = a.n_steps * per_step;
     const int RB = a.ring_bytes;
     const long long budget = a.spin_budget;
     const bool ln = a.gpt2 != 0;
-    const int PD = padded(d), PU = padded(a.upc), PO = padded(a.ko);
+    const int PD = padded(d), PU = padded(a.upc);
     const int W2 = hd + 4;  // partial record stride
+    const int lhd = 31 - __clz(hd);
+    // attention roles, fixed for the launch: (row, query head) pair pr of this warp and its index
+    // wi among the WG warps of the pair; b_, qh_, gl_: its batch row, query head and KV head
+    const int hpg = a.hpc / a.kpc, nph = NB * a.hpc;
+    const int WG = nph >= kWarps ? 1 : kWarps / nph;
+    const int pr = warp / WG, wi = warp - pr * WG;
+    const int b_ = pr < nph ? pr / a.hpc : 0;
+    const int qh_ = pr < nph ? pr - b_ * a.hpc : 0;
+    const int gl_ = qh_ / hpg;
+    // combine-and-send entries of this thread: (pair, component) = (cp_p, cp_k) for u = tid
+    const int cp_p = tid / (hd + 2), cp_k = tid - cp_p * (hd + 2);
     // bytes each exchange phase delivers to this CTA
     auto xb_bytes_of = [&](int k) -> uint32_t {
         return k == XB_QKV ? (uint32_t)(4 * NB * a.rpc)
              : k == XB_PART ? (uint32_t)(4 * cs * NB * a.hpc * (hd + 2))
-             : k == XB_X ? (uint32_t)(4 * NB * d) : (uint32_t)(4 * NB * a.upc);
+             : k == XB_U ? (uint32_t)(4 * NB * a.upc) : (uint32_t)(4 * NB * d);
     };
 
     {
         const int words = L * (int)(sizeof(StepLayer) / 4);
-        for (int i = tid; i < words; i += kBlock)
+        for (int i = tid; i < words; i += kCBlock)
             reinterpret_cast<int*>(tab)[i] = reinterpret_cast<const int*>(a.layers)[i];
     }
     __syncthreads();
-    if (tid < 5) s_geo[tid] = make_cslice(a, tab, tid, g.cl, g.rank);
+    if (tid < 5) s_geo[tid] = make_cslice(a, tab, tid, cl, rank);
     if (tid < kCTraceSub) s_trc[tid] = 0ull;
     if (tid == 0) {
-        for (int k = 0; k < kNMB; ++k) mb_init(smem_u32(&s_mb[k]));
+        for (int k = 0; k < kNMB; ++k) {
+            mb_init(smem_u32(&s_mb[k]));
+            mb_init_n(smem_u32(&s_empty[k]), kWarps);
+        }
         // the partial exchange also counts one release arrival per rank (see the attention phase)
-        for (int k = 0; k < 4; ++k) mb_init_n(smem_u32(&s_xb[k]), k == XB_PART ? 1 + a.cs : 1);
+        for (int k = 0; k < 5; ++k) mb_init_n(smem_u32(&s_xb[k]), k == XB_PART ? 1 + a.cs : 1);
+        mb_init(smem_u32(&s_kv));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        s_nc = 0;
-        s_done = 0;
     }
     __syncthreads();
     if (tid == 0)
-        for (int k = 0; k < 4; ++k) mb_arm(smem_u32(&s_xb[k]), xb_bytes_of(k));
+        for (int k = 0; k < 5; ++k) mb_arm(smem_u32(&s_xb[k]), xb_bytes_of(k));
     // every CTA's exchange barriers are initialised and armed before any rank sends
     cluster_sync_all();
+    // this rank's rows: residual rows (O / proj), cluster q/k/v rows, FFN activations
+    const int xr0 = s_geo[1].br0, nx = s_geo[1].nr;
+    const int qr0 = s_geo[0].br0 - cl * a.rpc;
+    const int fr0 = (s_geo[2].br0 - cl * (ln ? a.upc : 2 * a.upc)) >> (ln ? 0 : 1);
 
-    // ---- producer warp: streams this CTA's weight records into the ring
-    if (tid >= kThreads) {
-        if (tid == kThreads) {
-            int ni = 0, pj = 0, hoff = 0;
-            long long head = 0, idle0 = clock64();
-            bool ok = true;
-            while (ni < total) {
-                const int nc = ld_volatile(&s_nc);
-                if (ld_volatile(&s_done)) break;
-                bool issued = false;
-                if (ni - nc < kNMB) {
-                    const CSlice sl = cslice_at(a, tab, s_geo, pj);
-                    long long start = head;
-                    int off = hoff;
-                    if (off + sl.bytes > RB) {
-                        start += RB - off;
-                        off = 0;
-                    }
-                    if (!(ni > nc && start + sl.bytes - s_rec[nc & (kNMB - 1)] > RB)) {
-                        const uint32_t dst = smem_u32(ring + off);
-                        const uint32_t mb = smem_u32(&s_mb[ni & (kNMB - 1)]);
-                        s_rec[ni & (kNMB - 1)] = start;
-                        s_off[ni & (kNMB - 1)] = off;
-                        mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) +
-                                                 (sl.g2 ? sl.n_g : 0)));
-                        bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
-                        bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
-                        if (sl.bias) bulk_g2s(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb);
-                        if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
-                        if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
-                        head = start + sl.bytes;
-                        hoff = off + sl.bytes;
-                        ++ni;
-                        if (++pj == per_step) pj = 0;
-                        issued = true;
-                        idle0 = clock64();
-                    }
-                }
-                if (!issued) {
-                    if (clock64() - idle0 > budget) {
-                        atomicCAS(a.err, 0, kErrTimeout);
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(128);
-                }
-            }
-            const long long t0 = clock64();
-            while (!ld_volatile(&s_done) && ok && clock64() - t0 < budget) __nanosleep(256);
-            for (int i = ld_volatile(&s_nc); i < ni; ++i)
-                mb_wait(smem_u32(&s_mb[i & (kNMB - 1)]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
-        }
-        __syncwarp();
-        cluster_sync_all();
-        if (ld_volatile(a.err)) __nanosleep(20000);  // stores in flight from other ranks land first
-        return;
-    }
-
-    // ---- compute threads
     const unsigned gen0 = *reinterpret_cast<const volatile unsigned*>(a.gen);
     const int pos0 = ld_volatile(a.pos);
-    int nc = 0;
-    unsigned ph_qkv = 0u, ph_part = 0u, ph_x = 0u, ph_u = 0u;  // completed phases of each exchange barrier
-    // this CTA's exchange barriers and receive buffers (shared-window addresses; mapa() gives rank r's)
+    int nc = 0;  // records this warp has consumed (the same sequence in every warp)
+    // completed phases of the exchange barriers and of the KV staging barrier
+    unsigned ph_qkv = 0u, ph_part = 0u, ph_x0 = 0u, ph_x1 = 0u, ph_u = 0u, ph_kv = 0u;
     const uint32_t mb_qkv = smem_u32(&s_xb[XB_QKV]), mb_part = smem_u32(&s_xb[XB_PART]);
-    const uint32_t mb_x = smem_u32(&s_xb[XB_X]), mb_u = smem_u32(&s_xb[XB_U]);
+    const uint32_t mb_x0 = smem_u32(&s_xb[XB_X0]), mb_x1 = smem_u32(&s_xb[XB_X1]), mb_u = smem_u32(&s_xb[XB_U]);
+    const uint32_t mb_kv = smem_u32(&s_kv);
     const uint32_t a_x = smem_u32(xs), a_qkv = smem_u32(qkv), a_part = smem_u32(part), a_u = smem_u32(ub);
 
-    auto rec_ready = [&]() -> bool {
-        return mb_wait(smem_u32(&s_mb[nc & (kNMB - 1)]), (uint32_t)((nc / kNMB) & 1), a.err, budget, false);
+    // ---- weight ring, run by thread 0: records issued (p_ni), records every warp has consumed
+    // (p_nc), the next record's slice index within a step (p_pj), the ring head (p_head, p_hoff)
+    int p_ni = 0, p_nc = 0, p_pj = 0, p_hoff = 0;
+    long long p_head = 0;
+    // issues records while they fit: at most kNMB in flight, and a record never overwrites the
+    // oldest record a warp still reads; with nothing in flight any record fits
+    auto pump = [&]() {
+        while (p_nc < p_ni && mb_test(smem_u32(&s_empty[p_nc & (kNMB - 1)]), (uint32_t)((p_nc / kNMB) & 1)))
+            ++p_nc;
+        while (p_ni < total && p_ni - p_nc < kNMB) {
+            const int kind = p_pj < 4 * L ? (p_pj & 3) : 4;
+            const CSlice& G0 = s_geo[kind];
+            const int bytes = G0.bytes;
+            long long start = p_head;
+            int off = p_hoff;
+            if (off + bytes > RB) {
+                start += RB - off;
+                off = 0;
+            }
+            if (p_ni > p_nc && start + bytes - s_rec[p_nc & (kNMB - 1)] > RB) break;
+            const int l = p_pj >> 2;
+            const QMat* Wm;
+            const float *bias, *g1, *g2;
+            kind_ptrs(a, tab, kind, l < L ? l : 0, Wm, bias, g1, g2);
+            const uint32_t dst = smem_u32(ring + off);
+            const uint32_t mb = smem_u32(&s_mb[p_ni & (kNMB - 1)]);
+            s_rec[p_ni & (kNMB - 1)] = start;
+            s_off[p_ni & (kNMB - 1)] = off;
+            const int nb_ = G0.has_bias ? G0.n_bias : 0, ng = G0.has_g1 ? G0.n_g : 0, ng2 = G0.has_g2 ? G0.n_g : 0;
+            const size_t tbase = (size_t)G0.t0 * G0.KB;
+            const size_t sc_off = (size_t)((Wm->rows + 15) / 16) * G0.KB * frag_tb(Wm->kind);
+            mb_expect(mb, (uint32_t)(G0.n_codes + G0.n_sc + nb_ + ng + ng2));
+            bulk_g2s(dst, Wm->q + tbase * frag_tb(Wm->kind), (uint32_t)G0.n_codes, mb);
+            bulk_g2s(dst + G0.o_sc, Wm->q + sc_off + tbase * 32, (uint32_t)G0.n_sc, mb);
+            if (nb_) bulk_g2s(dst + G0.o_bias, bias + G0.b_lo, (uint32_t)nb_, mb);
+            if (ng) bulk_g2s(dst + G0.o_g1, g1, (uint32_t)ng, mb);
+            if (ng2) bulk_g2s(dst + G0.o_g2, g2, (uint32_t)ng2, mb);
+            p_head = start + bytes;
+            p_hoff = off + bytes;
+            ++p_ni;
+            if (++p_pj == per_step) p_pj = 0;
+        }
+    };
+    // waits for record nc to land (thread 0 keeps the ring topped up meanwhile, so the record is
+    // issued as soon as it fits); false on an expired wait or a recorded error
+    auto rec_wait = [&]() -> bool {
+        const uint32_t mb = smem_u32(&s_mb[nc & (kNMB - 1)]), par = (uint32_t)((nc / kNMB) & 1);
+        if (tid == 0) pump();
+        if (mb_try(mb, par)) return true;
+        const long long t0 = clock64();
+        for (unsigned it = 1;; ++it) {
+            if (tid == 0) pump();
+            if (mb_try(mb, par)) return true;
+            if ((it & 15u) == 0u) {
+                if (ld_volatile(a.err)) return false;
+                if (clock64() - t0 > budget) {
+                    atomicCAS(a.err, 0, kErrTimeout);
+                    return false;
+                }
+            }
+        }
     };
     auto rec_base = [&]() -> const unsigned char* { return ring + s_off[nc & (kNMB - 1)]; };
-    auto done_rec = [&]() {
-        csync();
+    // this warp is done with record nc
+    auto rec_done = [&]() {
+        __syncwarp();
+        if (lane == 0) mb_arrive_local(smem_u32(&s_empty[nc & (kNMB - 1)]));
         ++nc;
-        if (tid == 0) *reinterpret_cast<volatile int*>(&s_nc) = nc;
     };
-    // waits for the next phase of an exchange barrier (every compute thread), re-arms it
+    // waits for the next phase of an exchange barrier; thread 0 re-arms it at once.  (Every barrier
+    // is re-armed before this CTA's next CTA-wide barrier, and no rank sends the next phase's data
+    // before this CTA has passed that barrier.)
     auto xwait = [&](uint32_t mb, unsigned& ph, uint32_t bytes) -> bool {
-        bool ok = xb_wait(mb, ph & 1u, a.err, budget);
+        if (tid == 0) pump();
+        const bool ok = xb_wait(mb, ph & 1u, a.err, budget);
         if (ok && tid == 0) mb_arm(mb, bytes);
         ++ph;
-        return csync_and(ok) != 0;
+        return ok;
     };
     // CTA 0, thread 0: cycles since the previous stamp, added to sub-step k
-    const bool trc = a.trace && g.gi == 0 && tid == 0;
+    const bool trc = a.trace && gi == 0 && tid == 0;
     long long tc0 = trc ? clock64() : 0;
     auto stamp = [&](int k) {
         if (trc) {
@@ -587,47 +787,59 @@ __global__ void __launch_bounds__(kBlock, 1) k_cstep(const CStepArgs a) {
             atomicMin(a.trace_pub + (size_t)kTraceSteps * L * kCTracePhases + i, t);
         }
     };
-
-    // KV staging of layer l (cp.async, through L2): item it = b * kpc + gg, keys [c0, min(c1, c0 + kkc))
-    // except the position being decoded (it comes from this step's k, v)
-    auto stage = [&](int l, int pos, int c0, int c1) {
-        const int u16 = hd / 8, j1 = min(c1, c0 + a.kkc), nk = j1 - c0;
-        const int items = NB * a.kpc, per = nk * u16;
-        __half* Ks = stg;
-        __half* Vs = stg + (size_t)items * a.kkc * hd;
-        for (int t = tid; t < 2 * items * per; t += kThreads) {
-            const bool isv = t >= items * per;
-            const int tt = isv ? t - items * per : t;
-            const int it = tt / per, rem = tt - it * per, r = rem / u16, un = rem - r * u16;
-            if (c0 + r == pos) continue;
-            const int b = it / a.kpc, gg = g.cl * a.kpc + (it - b * a.kpc);
-            const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd;
-            const __half* src = (isv ? a.vc : a.kc) + hb + (size_t)(c0 + r) * hd + un * 8;
-            __half* dst = (isv ? Vs : Ks) + ((size_t)it * a.kkc + r) * hd + un * 8;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+    // KV staging of keys [j0, j1) of layer l for every (row, KV head) item of the cluster, without
+    // the position being decoded (its key comes from this step): two bulk copies per item (thread 0)
+    int kv_issued = 0;
+    auto kv_fetch = [&](int l, int pos, int j0, int j1) {
+        ++kv_issued;
+        // the staging was last read by generic loads; the cache was appended by generic stores
+        asm volatile("fence.proxy.async.shared::cta;\n\tfence.proxy.async.global;" ::: "memory");
+        const int jc = min(j1, pos);
+        const int nk = jc > j0 ? jc - j0 : 0, items = NB * a.kpc;
+        const uint32_t bytes = (uint32_t)(nk * hd * 2);
+        mb_expect(mb_kv, 2u * (uint32_t)items * bytes);
+        if (nk > 0)
+            for (int it = 0; it < items; ++it) {
+                const int b = it / a.kpc, gg = cl * a.kpc + (it - b * a.kpc);
+                const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd + (size_t)j0 * hd;
+                bulk_g2s(smem_u32(stg + (size_t)it * a.kkc * hd), a.kc + hb, bytes, mb_kv);
+                bulk_g2s(smem_u32(stg + ((size_t)items + it) * a.kkc * hd), a.vc + hb, bytes, mb_kv);
+            }
     };
+    // matvec operands of the current record
+    auto rec_codes = [&](const unsigned char* rec) { return reinterpret_cast<const uint8_t*>(rec); };
 
+    if (tid == 0) pump();
     bool ok = true;
-    for (int s = 0; s < a.n_steps && ok; ++s) {
+    for (int s = 0; s < a.n_steps; ++s) {
         const int pos = pos0 + s, n = pos + 1;
         const unsigned eb = 1u + (gen0 + (unsigned)s) * (unsigned)(L + 1);
-        int c0, c1;
-        row_range(n, g.rank, cs, c0, c1);
+        const int c0 = n * rank / cs, c1 = n * (rank + 1) / cs;  // this rank's keys
+        const bool last = c1 == n;             // this rank holds the position being decoded
+        const bool one_pass = c1 - c0 <= a.kkc;  // the rank's keys fit the staging at once
         stamp(26);
-        stage(0, pos, c0, c1);
+        if (tid == 0) kv_fetch(0, pos, c0, one_pass ? c1 : c0 + a.kkc);
+        // RoPE angles at pos for the pairs (i, i + hd/2) of this lane, i = lane, lane + 32
+        float rcs[2] = {1.f, 1.f}, rsn[2] = {0.f, 0.f};
+        if (a.rope_cos)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int i = lane + 32 * t;
+                if (i < hd / 2) {
+                    rcs[t] = __ldg(a.rope_cos + (size_t)pos * (hd / 2) + i);
+                    rsn[t] = __ldg(a.rope_sin + (size_t)pos * (hd / 2) + i);
+                }
+            }
         // ---- embedding: every CTA builds the whole input row
         {
-            bool okr = true;
             if (tid < NB) {
                 int t;
                 if (s == 0) {
                     t = ld_volatile(a.tok + tid);
                 } else {
-                    const unsigned long long* tp = a.ll_tok + (g.gi % kTokRep) * 32 + tid;
+                    const unsigned long long* tp = a.ll_tok + (gi % kTokRep) * 32 + tid;
                     unsigned long long w = ll_load(tp);
-                    if ((unsigned)(w >> 32) != eb - 1u) okr = ll_spin(tp, eb - 1u, &w, a.err, budget);
+                    if ((unsigned)(w >> 32) != eb - 1u && !ll_spin(tp, eb - 1u, &w, a.err, budget)) w = 0ull;
                     t = (int)(unsigned)w;
                 }
                 if (t < 0 || t >= a.V) {
@@ -636,193 +848,168 @@ __global__ void __launch_bounds__(kBlock, 1) k_cstep(const CStepArgs a) {
                 }
                 s_tok[tid] = t;
             }
-            if (!csync_and(okr)) { ok = false; break; }
-            for (int i = tid; i < NB * d; i += kThreads) {
-                const int b = i / d, k = i - b * d;
-                float v = __ldg(a.wte + (size_t)s_tok[b] * d + k);
-                if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + k);
-                xs[b * PD + pidx(k)] = v;
+            csync();
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float* te = a.wte + (size_t)s_tok[b] * d;
+                for (int k = tid; k < d; k += kThreads) {
+                    float v = __ldg(te + k);
+                    if (a.wpe) v += __ldg(a.wpe + (size_t)pos * d + k);
+                    xs[b * PD + pidx(k)] = v;
+                }
             }
             csync();
             stamp(27);
         }
-        for (int l = 0; l < L && ok; ++l) {
+        for (int l = 0; l < L; ++l) {
             const unsigned e = eb + (unsigned)l;
+            const int qd = a.hpc * hd, kd = a.kpc * hd;
             // ---- norm and this rank's q, k, v rows -> every rank of the cluster
             {
-                bool okr = l > 0 ? xwait(mb_x, ph_x, xb_bytes_of(XB_X)) : true;
+                if (l > 0) xwait(mb_x1, ph_x1, xb_bytes_of(XB_X1));
                 stamp(0);
-                if (okr) okr = csync_and(rec_ready()) != 0;
-                if (!okr) { ok = false; break; }
+                rec_wait();
                 stamp(1);
                 tr_pub(s, l, 0);
-                const CSlice sl = cslice_at(a, tab, s_geo, 4 * l);
+                const CSlice& sl = s_geo[0];
                 const unsigned char* rec = rec_base();
-                norm_to<NB>(xs, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
+                bf_norm<QK, NB>(xs, PD, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                                reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red, bf);
                 stamp(2);
-                const int nr = sl.r1 - sl.r0;
-                cgemv<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, PD, ys);
-                stamp(3);
-                const float* bias = sl.bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo)
-                                            : nullptr;
-                for (int t = tid; t < nr * NB * cs; t += kThreads) {
-                    const int dst = t % cs, ib = t / cs, i = ib / NB, b = ib - i * NB;
-                    float v = ys[i * NB + b];
-                    if (bias) v += bias[i];
-                    st_async(mapa(a_qkv + 4u * (uint32_t)(b * a.rpc + g.qr0 + i), dst), v,
-                             mapa(mb_qkv, dst));
-                }
+                const float* bias =
+                    sl.has_bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo) : nullptr;
+                mma_rows<QK, NB, false>(rec_codes(rec), rec + sl.o_sc, d, sl.nt, sl.nr, bf, red,
+                                        [&](int i, int b, float v, float) {
+                                            if (bias) v += bias[i];
+                                            const uint32_t addr = a_qkv + 4u * (uint32_t)(b * a.rpc + qr0 + i);
+                                            for (int dst = 0; dst < cs; ++dst)
+                                                st_async(mapa(addr, dst), v, mapa(mb_qkv, dst));
+                                        });
+                rec_done();
                 tr_pub(s, l, 1);
-                done_rec();
-                stamp(4);
+                stamp(3);
             }
             // ---- attention over this rank's keys [c0, c1)
             {
-                if (!xwait(mb_qkv, ph_qkv, xb_bytes_of(XB_QKV))) { ok = false; break; }
-                stamp(5);
-                const int qd = a.hpc * hd, kd = a.kpc * hd, half = hd >> 1, hpg = a.hpc / a.kpc;
-                const float scale = 1.0f / sqrtf((float)hd);
-                const bool last = c1 == n;  // this rank holds the position being decoded
-                // RoPE (NEOX half split) at pos on q and k; q scaled by 1/sqrt(hd)
-                for (int i = tid; i < NB * (a.hpc + a.kpc) * half; i += kThreads) {
-                    const int b = i / ((a.hpc + a.kpc) * half), r = i - b * (a.hpc + a.kpc) * half;
-                    const int h = r / half, dd = r - h * half;
-                    float* v = qkv + b * a.rpc + h * hd;  // q heads, then k heads (contiguous)
-                    float x0 = v[dd], x1 = v[dd + half];
-                    if (a.rope_cos) {
-                        const float c = a.rope_cos[(size_t)pos * half + dd], sn = a.rope_sin[(size_t)pos * half + dd];
-                        const float y0 = x0 * c - x1 * sn, y1 = x0 * sn + x1 * c;
-                        x0 = y0;
-                        x1 = y1;
-                    }
-                    if (h < a.hpc) {
-                        x0 *= scale;
-                        x1 *= scale;
-                    }
-                    v[dd] = x0;
-                    v[dd + half] = x1;
-                }
-                csync();
+                xwait(mb_qkv, ph_qkv, xb_bytes_of(XB_QKV));
+                stamp(4);
+                const int half = hd >> 1;
                 const int items = NB * a.kpc;
                 __half* Ks = stg;
                 __half* Vs = stg + (size_t)items * a.kkc * hd;
-                if (last) {
-                    // append the new position to the cache (fp16, round to nearest) and to the staging
-                    for (int i = tid; i < items * hd; i += kThreads) {
-                        const int it = i / hd, dd = i - it * hd, b = it / a.kpc, gl = it - b * a.kpc;
-                        const int gg = g.cl * a.kpc + gl;
-                        const __half kh = __float2half_rn(qkv[b * a.rpc + qd + gl * hd + dd]);
-                        const __half vh = __float2half_rn(qkv[b * a.rpc + qd + kd + gl * hd + dd]);
-                        const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd + (size_t)pos * hd + dd;
-                        a.kc[hb] = kh;
-                        a.vc[hb] = vh;
-                        if (pos - c0 < a.kkc) {
-                            Ks[((size_t)it * a.kkc + (pos - c0)) * hd + dd] = kh;
-                            Vs[((size_t)it * a.kkc + (pos - c0)) * hd + dd] = vh;
-                        }
+                const float scale = 1.0f / sqrtf((float)hd);
+                float m = -INFINITY, lsum = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                const int b = b_, gl = gl_, qh = qh_;
+                if (pr < nph) {
+                    // this warp's query: RoPE at pos (NEOX half split), scaled by 1/sqrt(hd)
+                    float* q = wq + warp * hd;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int i = lane + 32 * t;
+                        if (i >= half) continue;
+                        const float x0 = qkv[b * a.rpc + qh * hd + i], x1 = qkv[b * a.rpc + qh * hd + i + half];
+                        q[i] = (x0 * rcs[t] - x1 * rsn[t]) * scale;
+                        q[i + half] = (x0 * rsn[t] + x1 * rcs[t]) * scale;
                     }
                 }
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                csync();
-                stamp(6);
-                const int warp = tid >> 5, lane = tid & 31;
-                bool first_staged = true;  // the staging holds each item's first sub-chunk
-                for (int it = 0; it < items; ++it) {
-                    const int b = it / a.kpc, gl = it - b * a.kpc;
-                    for (int h = 0; h < hpg; ++h) {
-                        const int qh = gl * hpg + h;  // query head within the cluster
-                        const int LPK = hd / 8, dg = lane % LPK;
-                        float q[8];
+                // the position being decoded: its rotated key and its value, fp16, into the cache
+                // (one warp per item) and into the staging slot of every warp that reads it
+                auto put_new = [&](int jloc, bool to_cache) {
+                    const int it = b * a.kpc + gl, gg = cl * a.kpc + gl;
+                    const float* kk = qkv + b * a.rpc + qd + gl * hd;
+                    const float* vv = qkv + b * a.rpc + qd + kd + gl * hd;
+                    const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd + (size_t)pos * hd;
+                    __half* ks = Ks + ((size_t)it * a.kkc + jloc) * hd;
+                    __half* vs = Vs + ((size_t)it * a.kkc + jloc) * hd;
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) q[t] = qkv[b * a.rpc + qh * hd + dg * 8 + t];
-                        float m = -INFINITY, lsum = 0.f, o[8];
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) o[t] = 0.f;
-                        for (int j0 = c0; j0 < c1; j0 += a.kkc) {
-                            const int j1 = min(c1, j0 + a.kkc);
-                            if (!(j0 == c0 && first_staged)) {
-                                // a later sub-chunk (or the first one again after it was replaced)
-                                csync();
-                                const int u16 = hd / 8, per = (j1 - j0) * u16;
-                                for (int t = tid; t < 2 * per; t += kThreads) {
-                                    const bool isv = t >= per;
-                                    const int tt = isv ? t - per : t, r = tt / u16, un = tt - r * u16;
-                                    __half* dst = (isv ? Vs : Ks) + ((size_t)it * a.kkc + r) * hd + un * 8;
-                                    if (j0 + r == pos) {
-                                        const float* srcf = qkv + b * a.rpc + qd + (isv ? kd : 0) + gl * hd + un * 8;
-#pragma unroll
-                                        for (int w = 0; w < 8; ++w) dst[w] = __float2half_rn(srcf[w]);
-                                        continue;
-                                    }
-                                    const int gg = g.cl * a.kpc + gl;
-                                    const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd;
-                                    const __half* src = (isv ? a.vc : a.kc) + hb + (size_t)(j0 + r) * hd + un * 8;
-                                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                                                 "l"(src)
-                                                 : "memory");
-                                }
-                                asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-                                csync();
-                                first_staged = false;
+                    for (int t = 0; t < 2; ++t) {
+                        const int i = lane + 32 * t;
+                        if (i >= half) continue;
+                        const __half k0 = __float2half_rn(kk[i] * rcs[t] - kk[i + half] * rsn[t]);
+                        const __half k1 = __float2half_rn(kk[i] * rsn[t] + kk[i + half] * rcs[t]);
+                        const __half v0 = __float2half_rn(vv[i]), v1 = __float2half_rn(vv[i + half]);
+                        ks[i] = k0; ks[i + half] = k1; vs[i] = v0; vs[i + half] = v1;
+                        if (to_cache) {
+                            a.kc[hb + i] = k0; a.kc[hb + i + half] = k1;
+                            a.vc[hb + i] = v0; a.vc[hb + i + half] = v1;
+                        }
+                    }
+                };
+                __syncwarp();
+                for (int j0s = c0; j0s < c1; j0s += a.kkc) {
+                    const int j1s = min(c1, j0s + a.kkc), nk = j1s - j0s;
+                    if (j0s != c0) {
+                        // a later sub-chunk: every warp is done with the staging first
+                        csync();
+                        if (tid == 0) kv_fetch(l, pos, j0s, j1s);
+                    }
+                    xb_wait(mb_kv, ph_kv & 1u, a.err, budget);
+                    ++ph_kv;
+                    if (pr < nph) {
+                        const float* q = wq + warp * hd;
+                        const __half* Ki = Ks + (size_t)(b * a.kpc + gl) * a.kkc * hd;
+                        const __half* Vi = Vs + (size_t)(b * a.kpc + gl) * a.kkc * hd;
+                        for (int j0 = wi * 32; j0 < nk; j0 += WG * 32) {
+                            if (last && j1s == c1 && j0 + 32 >= nk) {
+                                // this pass holds the position being decoded (local index nk - 1)
+                                put_new(nk - 1, qh % hpg == 0);
+                                asm volatile("fence.proxy.async.global;" ::: "memory");
+                                __syncwarp();
                             }
                             if (hd == 64)
-                                attn_keys<64>(q, Ks + (size_t)it * a.kkc * hd, Vs + (size_t)it * a.kkc * hd, j1 - j0,
-                                              m, lsum, o);
+                                attn_lk<64>(q, Ki, Vi, j0, nk, m, lsum, *reinterpret_cast<float(*)[2]>(o));
                             else
-                                attn_keys<128>(q, Ks + (size_t)it * a.kkc * hd, Vs + (size_t)it * a.kkc * hd, j1 - j0,
-                                               m, lsum, o);
+                                attn_lk<128>(q, Ki, Vi, j0, nk, m, lsum, o);
                         }
-                        stamp(7);
-                        // sum the key slots of the warp, then the warps (in warp order)
-                        for (int w = LPK; w < 32; w <<= 1) {
-                            lsum += __shfl_xor_sync(0xffffffffu, lsum, w);
-#pragma unroll
-                            for (int t = 0; t < 8; ++t) o[t] += __shfl_xor_sync(0xffffffffu, o[t], w);
-                        }
-                        if (lane < LPK) {
-#pragma unroll
-                            for (int t = 0; t < 8; ++t) wp[warp * W2 + dg * 8 + t] = o[t];
-                            if (lane == 0) {
-                                wp[warp * W2 + hd] = m;
-                                wp[warp * W2 + hd + 1] = lsum;
-                            }
-                        }
-                        csync();
-                        const int bh = b * a.hpc + qh;
-                        for (int t = tid; t < (hd + 2) * cs; t += kThreads) {
-                            const int dst = t / (hd + 2), k = t - dst * (hd + 2);
-                            float M = -INFINITY;
-#pragma unroll 4
-                            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wp[w * W2 + hd]);
-                            float v = M;
-                            if (k != hd) {
-                                v = 0.f;
-                                for (int w = 0; w < kWarps; ++w) {
-                                    const float mw = wp[w * W2 + hd];
-                                    if (mw != -INFINITY) v = fmaf(expf(mw - M), wp[w * W2 + k], v);
-                                }
-                            }
-                            st_async(mapa(a_part + 4u * (uint32_t)((g.rank * NB * a.hpc + bh) * W2 + k), dst), v,
-                                     mapa(mb_part, dst));
-                        }
-                        csync();
                     }
                 }
-                // one release arrival per rank: a reader of this KV head's cache in a later step
-                // (another rank of this cluster) acquires the append through this barrier
+                stamp(5);
+                // warp partials -> the warps of a pair combined in warp order -> every rank
+                {
+                    const int DPL = hd / 32;
+#pragma unroll
+                    for (int dd = 0; dd < 4; ++dd)
+                        if (dd < DPL) wp[warp * W2 + lane * DPL + dd] = o[dd];
+                    if (lane == 0) {
+                        wp[warp * W2 + hd] = m;
+                        wp[warp * W2 + hd + 1] = lsum;
+                    }
+                }
+                csync();
+                // only the first ceil(keys / 32) warps of a pair hold keys (the last sub-chunk decides)
+                const int nkl = c1 - c0 - ((c1 - c0 - 1) / a.kkc) * a.kkc;
+                const int wa = c1 > c0 ? min(WG, (max(nkl, min(c1 - c0, a.kkc)) + 31) / 32) : 0;
+                for (int u = tid; u < nph * (hd + 2); u += kThreads) {
+                    const int p = u == tid ? cp_p : u / (hd + 2), k = u == tid ? cp_k : u - p * (hd + 2);
+                    const float* P = wp + (size_t)p * WG * W2;
+                    float M = -INFINITY;
+                    for (int w = 0; w < wa; ++w) M = fmaxf(M, P[w * W2 + hd]);
+                    float v = M;
+                    if (k != hd) {
+                        v = 0.f;
+                        for (int w = 0; w < wa; ++w) {
+                            const float mw = P[w * W2 + hd];
+                            if (mw != -INFINITY) v = fmaf(expf(mw - M), P[w * W2 + k], v);
+                        }
+                    }
+                    const uint32_t addr = a_part + 4u * (uint32_t)((rank * NB * a.hpc + p) * W2 + k);
+                    for (int dst = 0; dst < cs; ++dst) st_async(mapa(addr, dst), v, mapa(mb_part, dst));
+                }
+                // one release arrival per rank, after this CTA's barrier: a reader of this KV head's
+                // cache in a later step (another rank of this cluster) acquires the append through it
+                csync();
                 if (tid < cs) mb_arrive_remote(mapa(mb_part, tid));
+                // the staging is free: the next layer's keys (off the critical path, after the sends)
+                if (tid == 0 && l + 1 < L) kv_fetch(l + 1, pos, c0, one_pass ? c1 : c0 + a.kkc);
                 tr_pub(s, l, 2);
-                stamp(8);
-                // the staging is free: the next layer's keys
-                if (l + 1 < L) stage(l + 1, pos, c0, c1);
+                stamp(6);
             }
             // ---- combine the ranks' partials; O slab for this rank's rows -> global partial words
             {
-                if (!xwait(mb_part, ph_part, xb_bytes_of(XB_PART))) { ok = false; break; }
-                stamp(9);
+                xwait(mb_part, ph_part, xb_bytes_of(XB_PART));
+                stamp(7);
                 for (int t = tid; t < NB * a.hpc * hd; t += kThreads) {
-                    const int bh = t / hd, dd = t - bh * hd;
+                    const int bh = t >> lhd, dd = t & (hd - 1);
                     float M = -INFINITY;
                     for (int r = 0; r < cs; ++r) M = fmaxf(M, part[(r * NB * a.hpc + bh) * W2 + hd]);
                     float num = 0.f, den = 0.f;
@@ -833,138 +1020,125 @@ __global__ void __launch_bounds__(kBlock, 1) k_cstep(const CStepArgs a) {
                         num = fmaf(w, P[dd], num);
                         den = fmaf(w, P[hd + 1], den);
                     }
-                    const int b = bh / a.hpc, qh = bh - b * a.hpc;
-                    xn[b * PO + pidx(qh * hd + dd)] = num / den;
+                    const int bb = NB == 1 ? 0 : bh / a.hpc, qh = bh - bb * a.hpc;
+                    bf_put<QK, NB>(bf, qh * hd + dd, bb, num / den);
                 }
                 csync();
-                stamp(10);
-                if (!csync_and(rec_ready())) { ok = false; break; }
-                stamp(11);
-                const CSlice sl = cslice_at(a, tab, s_geo, 4 * l + 1);
+                stamp(8);
+                rec_wait();
+                stamp(9);
+                const CSlice& sl = s_geo[1];
                 const unsigned char* rec = rec_base();
-                const int nr = sl.r1 - sl.r0;
-                cgemv<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), a.ko, nr, xn, PO, ys);
-                stamp(12);
-                for (int t = tid; t < nr * NB; t += kThreads) {
-                    const int i = t / NB, b = t - i * NB;
-                    ll_store(a.ll_po + ((size_t)g.cl * NB + b) * d + g.xr0 + i, ys[t], e);
-                }
+                unsigned long long* P = a.ll_po + (size_t)cl * NB * d;
+                mma_rows<QK, NB, false>(rec_codes(rec), rec + sl.o_sc, a.ko, sl.nt, sl.nr, bf, red,
+                                        [&](int i, int bb, float v, float) {
+                                            ll_store(P + (size_t)bb * d + xr0 + i, v, e);
+                                        });
                 tr_pub(s, l, 3);
-                stamp(13);
-                // ---- exchange 1: rows [xr0, xr1) of every cluster's partial, summed in cluster order
-                const float* bias = sl.bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo)
-                                            : nullptr;
-                const bool okr = reduce_bcast<NB>(a.ll_po, a.ncl, d, g.xr0, nr, e, bias, xs, PD, a_x, mb_x, cs, a.err,
-                                                  budget);
-                if (!csync_and(okr)) { ok = false; break; }
+                stamp(10);
+                // ---- exchange 1: rows [xr0, xr0 + nx) of every cluster's partial, summed in cluster order
+                const float* bias =
+                    sl.has_bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo) : nullptr;
+                reduce_bcast<NB>(a.ll_po, a.ncl, d, xr0, nx, e, bias, xs, PD, a_x, mb_x0, cs, a.err, budget);
+                rec_done();
                 tr_pub(s, l, 4);
-                done_rec();
-                stamp(14);
+                stamp(11);
             }
             // ---- norm and this rank's FC / gate-up rows -> cluster FFN activations
             {
-                bool okr = xwait(mb_x, ph_x, xb_bytes_of(XB_X));
-                stamp(15);
-                if (okr) okr = csync_and(rec_ready()) != 0;
-                if (!okr) { ok = false; break; }
-                stamp(16);
-                const CSlice sl = cslice_at(a, tab, s_geo, 4 * l + 2);
+                xwait(mb_x0, ph_x0, xb_bytes_of(XB_X0));
+                stamp(12);
+                rec_wait();
+                stamp(13);
+                const CSlice& sl = s_geo[2];
                 const unsigned char* rec = rec_base();
-                norm_to<NB>(xs, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
-                stamp(17);
-                const int nr = sl.r1 - sl.r0;
-                cgemv<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, PD, ys);
-                stamp(18);
-                const float* bias = sl.bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo)
-                                            : nullptr;
-                const int nu = ln ? nr : nr / 2;
-                for (int t = tid; t < nu * NB * cs; t += kThreads) {
-                    const int dst = t % cs, ib = t / cs, i = ib / NB, b = ib - i * NB;
-                    float v;
-                    if (ln) {
-                        v = ys[i * NB + b];
-                        if (bias) v += bias[i];
-                        v = gelu_tanh(v);
-                    } else {
-                        v = silu(ys[(2 * i) * NB + b]) * ys[(2 * i + 1) * NB + b];
-                    }
-                    st_async(mapa(a_u + 4u * (uint32_t)(b * PU + pidx(g.fr0 + i)), dst), v, mapa(mb_u, dst));
-                }
+                bf_norm<QK, NB>(xs, PD, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                                reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red, bf);
+                stamp(14);
+                const float* bias =
+                    sl.has_bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo) : nullptr;
+                auto send_u = [&](int i, int bb, float v) {
+                    const uint32_t addr = a_u + 4u * (uint32_t)(bb * PU + pidx(fr0 + i));
+                    for (int dst = 0; dst < cs; ++dst) st_async(mapa(addr, dst), v, mapa(mb_u, dst));
+                };
+                if (ln)
+                    mma_rows<QK, NB, false>(rec_codes(rec), rec + sl.o_sc, d, sl.nt, sl.nr, bf, red,
+                                            [&](int i, int bb, float v, float) {
+                                                if (bias) v += bias[i];
+                                                send_u(i, bb, gelu_tanh(v));
+                                            });
+                else
+                    mma_rows<QK, NB, true>(rec_codes(rec), rec + sl.o_sc, d, sl.nt, sl.nr, bf, red,
+                                           [&](int k, int bb, float gt, float up) { send_u(k, bb, silu(gt) * up); });
+                rec_done();
                 tr_pub(s, l, 5);
-                done_rec();
-                stamp(19);
+                stamp(15);
             }
             // ---- down-projection slab for this rank's rows -> exchange 2
             {
-                bool okr = xwait(mb_u, ph_u, xb_bytes_of(XB_U));
-                stamp(20);
-                if (okr) okr = csync_and(rec_ready()) != 0;
-                if (!okr) { ok = false; break; }
-                stamp(21);
-                const CSlice sl = cslice_at(a, tab, s_geo, 4 * l + 3);
+                xwait(mb_u, ph_u, xb_bytes_of(XB_U));
+                stamp(16);
+                rec_wait();
+                stamp(17);
+                bf_plain<QK, NB>(ub, PU, a.upc, bf);
+                const CSlice& sl = s_geo[3];
                 const unsigned char* rec = rec_base();
-                const int nr = sl.r1 - sl.r0;
-                cgemv<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), a.upc, nr, ub, PU, ys);
-                stamp(22);
-                for (int t = tid; t < nr * NB; t += kThreads) {
-                    const int i = t / NB, b = t - i * NB;
-                    ll_store(a.ll_pp + ((size_t)g.cl * NB + b) * d + g.xr0 + i, ys[t], e);
-                }
+                unsigned long long* P = a.ll_pp + (size_t)cl * NB * d;
+                mma_rows<QK, NB, false>(rec_codes(rec), rec + sl.o_sc, a.upc, sl.nt, sl.nr, bf, red,
+                                        [&](int i, int bb, float v, float) {
+                                            ll_store(P + (size_t)bb * d + xr0 + i, v, e);
+                                        });
                 tr_pub(s, l, 6);
-                stamp(23);
-                const float* bias = sl.bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo)
-                                            : nullptr;
-                okr = reduce_bcast<NB>(a.ll_pp, a.ncl, d, g.xr0, nr, e, bias, xs, PD, a_x, mb_x, cs, a.err, budget);
-                if (!csync_and(okr)) { ok = false; break; }
+                stamp(18);
+                const float* bias =
+                    sl.has_bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo) : nullptr;
+                reduce_bcast<NB>(a.ll_pp, a.ncl, d, xr0, nx, e, bias, xs, PD, a_x, mb_x1, cs, a.err, budget);
+                rec_done();
                 tr_pub(s, l, 7);
-                done_rec();
-                stamp(24);
+                stamp(19);
             }
         }
-        if (!ok) break;
         // ---- head rows (final norm)
         const unsigned eh = eb + (unsigned)L;
         {
-            bool okr = xwait(mb_x, ph_x, xb_bytes_of(XB_X));
-            if (okr) okr = csync_and(rec_ready()) != 0;
-            if (!okr) { ok = false; break; }
-            const CSlice sl = cslice_at(a, tab, s_geo, 4 * L);
+            xwait(mb_x1, ph_x1, xb_bytes_of(XB_X1));
+            rec_wait();
+            const CSlice& sl = s_geo[4];
             const unsigned char* rec = rec_base();
-            norm_to<NB>(xs, xn, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
-                        reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red);
-            const int nr = sl.r1 - sl.r0;
-            cgemv<QK, NB>(rec, rec + sl.o_sc + (sl.r0 * sl.srow - sl.s_lo), d, nr, xn, PD, ys);
-            for (int t = tid; t < nr * NB; t += kThreads) {
-                const int i = t / NB, b = t - i * NB;
-                a.logits[(size_t)b * a.V + sl.r0 + i] = ys[t];
-                ll_store(a.ll_logits + (size_t)b * a.V + sl.r0 + i, ys[t], eh);
-            }
-            done_rec();
-            stamp(25);
+            bf_norm<QK, NB>(xs, PD, d, ln, reinterpret_cast<const float*>(rec + sl.o_g1),
+                            reinterpret_cast<const float*>(rec + sl.o_g2), a.eps, s_red, bf);
+            const int hr0 = sl.br0;
+            mma_rows<QK, NB, false>(rec_codes(rec), rec + sl.o_sc, d, sl.nt, sl.nr, bf, red,
+                                    [&](int i, int bb, float v, float) {
+                                        a.logits[(size_t)bb * a.V + hr0 + i] = v;
+                                        ll_store(a.ll_logits + (size_t)bb * a.V + hr0 + i, v, eh);
+                                    });
+            rec_done();
+            stamp(20);
         }
-        // ---- sampler: CTA b samples row b
-        if (g.gi < NB) {
-            float* z = reinterpret_cast<float*>(stg);
-            const int b = g.gi;
-            bool okr = true;
-            for (int i0 = tid; i0 < a.V && okr; i0 += 4 * kThreads) {
+        // ---- sampler: CTA b samples row b (its shared memory overlays the activation region: every
+        // buffer there is idle until the next step, and no rank sends into it before this token)
+        if (gi < NB) {
+            float* z = reinterpret_cast<float*>(actb);
+            csync();  // the head's partial sums are read
+            const int b = gi;
+            for (int i0 = tid; i0 < a.V; i0 += 4 * kThreads) {
                 unsigned long long w[4];
-                const unsigned long long* p[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int i = i0 + j * kThreads;
-                    p[j] = i < a.V ? a.ll_logits + (size_t)b * a.V + i : nullptr;
-                    w[j] = p[j] ? ll_load(p[j]) : 0ull;
+                    w[j] = i < a.V ? ll_load(a.ll_logits + (size_t)b * a.V + i) : 0ull;
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (!p[j] || !okr) continue;
-                    if ((unsigned)(w[j] >> 32) != eh) okr = ll_spin(p[j], eh, &w[j], a.err, budget);
-                    z[i0 + j * kThreads] = __uint_as_float((unsigned)w[j]);
+                    const int i = i0 + j * kThreads;
+                    if (i >= a.V) continue;
+                    if ((unsigned)(w[j] >> 32) != eh)
+                        ll_spin(a.ll_logits + (size_t)b * a.V + i, eh, &w[j], a.err, budget);
+                    z[i] = __uint_as_float((unsigned)w[j]);
                 }
             }
-            if (!csync_and(okr)) { ok = false; break; }
+            csync();
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + b : a.u1 + b;
             const int tk = sample_detail::sample_smem(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
                                                       a.err);
@@ -974,24 +1148,27 @@ __global__ void __launch_bounds__(kBlock, 1) k_cstep(const CStepArgs a) {
 #pragma unroll
                 for (int r = 0; r < kTokRep; ++r) ll_store(a.ll_tok + r * 32 + b, __int_as_float(tk), eh);
             }
-            csync();
         }
+        // the step ends uniformly: on a recorded error every thread leaves here
+        ok = csync_and(ld_volatile(a.err) == 0) != 0;
+        stamp(21);
+        if (!ok) break;
     }
-    if (g.gi == 0 && tid == 0) {
+    if (gi == 0 && tid == 0) {
         if (ok) *a.pos = pos0 + a.n_steps;
         *a.gen = gen0 + (unsigned)a.n_steps;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    csync();
-    if (a.trace && g.gi == 0 && tid < kCTraceSub) a.trace[tid] += s_trc[tid];
+    // copies still in flight into this CTA's shared memory land before the CTA exits
     if (tid == 0) {
-        *reinterpret_cast<volatile int*>(&s_nc) = nc;
-        __threadfence_block();
-        *reinterpret_cast<volatile int*>(&s_done) = 1;
+        for (int i = p_nc; i < p_ni; ++i)
+            mb_wait(smem_u32(&s_mb[i & (kNMB - 1)]), (uint32_t)((i / kNMB) & 1), a.err, budget, true);
+        if (kv_issued > (int)ph_kv) mb_wait(mb_kv, ph_kv & 1u, a.err, budget, true);
     }
+    csync();
+    if (a.trace && gi == 0 && tid < kCTraceSub) a.trace[tid] += s_trc[tid];
     // no CTA of the cluster leaves while another may still send into its shared memory
     cluster_sync_all();
-    if (ld_volatile(a.err)) __nanosleep(20000);
+    if (!ok) __nanosleep(20000);
 }
 
 template <int QK, int NB>
@@ -1005,30 +1182,49 @@ void* pick(const CStepArgs& a) {
     return nullptr;
 }
 
-// ------------------------------------------------------------------ slab gather (set-up)
+// ------------------------------------------------------------------ fragment-major repack (set-up)
 
-__global__ void k_slab_gather(const uint8_t* q, const __half* s, int R, int K, int W, int q4, const int* perm,
-                              uint8_t* qo, __half* so) {
-    const int rb = q4 ? K / 2 : K, wb = q4 ? W / 2 : W;  // code bytes per source row / per slab row
-    const int ns = K / W;
-    const long long chunks = (long long)R * rb / 16;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < chunks;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int i = (int)(t / (rb / 16)), cb = (int)(t % (rb / 16)) * 16;  // out row i, byte cb of the full row
-        const int sl = cb / wb, ib = cb - sl * wb;
-        const int src = perm ? perm[i] : i;
-        *reinterpret_cast<uint4*>(qo + ((size_t)sl * R + i) * wb + ib) =
-            *reinterpret_cast<const uint4*>(q + (size_t)src * rb + cb);
+// out = the fragment-major copy (see Frag) of column slab s of rows perm[i]
+// (or i) of a row-major Q8_0 / Q4_0 matrix, for s < K / Wd; rows past R are
+// zero.  Slabs follow each other; the scales of all slabs come after all codes.
+__global__ void k_frag_pack(const uint8_t* q, const __half* sc, int R, int K, int Wd, int q4, const int* perm,
+                            uint8_t* out) {
+    const int rb = q4 ? K / 2 : K;           // code bytes per source row
+    const int blk = q4 ? 16 : 32;            // code bytes per block
+    const int W = q4 ? 1 : 2, TB = 256 * W;  // words per lane per row, bytes per (tile, block)
+    const int NT = (R + 15) / 16, KB = Wd / 32, NS = K / Wd;
+    const long long lanes = (long long)NS * NT * KB * 32;
+    const size_t sc_base = (size_t)NS * NT * KB * TB;
+    for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < lanes;
+         x += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(x & 31);
+        const long long tbk = x >> 5;                       // (slab, tile, block)
+        const int kb = (int)(tbk % KB), tile = (int)((tbk / KB) % NT), sl = (int)(tbk / ((long long)KB * NT));
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t* o = reinterpret_cast<uint32_t*>(out + (size_t)tbk * TB) + lane * 2 * W;
+        for (int h = 0; h < 2; ++h) {
+            const int row = tile * 16 + g + 8 * h;
+            for (int w = 0; w < W; ++w) {
+                uint32_t v = 0u;
+                if (row < R) {
+                    const int src = perm ? perm[row] : row;
+                    const size_t off = (size_t)src * rb + (size_t)sl * (Wd / 32) * blk + (size_t)kb * blk +
+                                       (size_t)(4 * W) * t + 4 * w;
+                    v = *reinterpret_cast<const uint32_t*>(q + off);
+                }
+                o[h * W + w] = v;
+            }
+        }
+        if (lane < 16) {
+            const int row = tile * 16 + lane;
+            __half hv = __float2half(0.f);
+            if (row < R) {
+                const int src = perm ? perm[row] : row;
+                hv = sc[(size_t)src * (K / 32) + (size_t)sl * KB + kb];
+            }
+            reinterpret_cast<__half*>(out + sc_base)[(size_t)tbk * 16 + lane] = hv;
+        }
     }
-    const int spr = K / 32, sps = W / 32;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < (long long)R * spr;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int i = (int)(t / spr), j = (int)(t % spr);
-        const int sl = j / sps, jj = j - sl * sps;
-        const int src = perm ? perm[i] : i;
-        so[((size_t)sl * R + i) * sps + jj] = s[(size_t)src * spr + j];
-    }
-    (void)ns;
 }
 
 }  // namespace cstep_detail
@@ -1037,25 +1233,29 @@ size_t cstep_smem_bytes(const CStepArgs& a) {
     return (size_t)a.ring_bytes + (size_t)a.act_bytes + sizeof(StepLayer) * (size_t)a.n_layer;
 }
 
-// Activation-region layout for the plan in `a` (B, d, upc, ko, rpc, hpc, kpc, cs, hd, kkc); returns its bytes.
-static size_t cstep_layout(CStepArgs& a, int yrows) {
+// Activation-region layout for the plan in `a`; returns its bytes.  maxnt: the
+// most tiles of one record (the matvec partial sums hold max(16, maxnt) units).
+static size_t cstep_layout(CStepArgs& a, int maxnt) {
     using gemv_detail::padded;
     const int B = a.B;
     auto al = [](size_t v) { return (v + 127) & ~(size_t)127; };
     size_t off = 0;
-    const int kin = a.d > a.ko ? a.d : a.ko;
+    int kin = a.d > a.ko ? a.d : a.ko;
+    if (a.upc > kin) kin = a.upc;
     a.o_x = (int)off; off = al(off + 4 * (size_t)B * padded(a.d));
-    a.o_xn = (int)off; off = al(off + 4 * (size_t)B * padded(kin));
     a.o_u = (int)off; off = al(off + 4 * (size_t)B * padded(a.upc));
     a.o_qkv = (int)off; off = al(off + 4 * (size_t)B * a.rpc);
     a.o_part = (int)off; off = al(off + 4 * (size_t)a.cs * B * a.hpc * (a.hd + 4));
-    a.o_y = (int)off; off = al(off + 4 * (size_t)yrows * B);
+    a.o_wq = (int)off; off = al(off + 4 * (size_t)stepdev::kWarps * a.hd);
     a.o_wp = (int)off; off = al(off + 4 * (size_t)stepdev::kWarps * (a.hd + 4));
+    a.o_bf = (int)off; off = al(off + 2 * 2 * 2 * (size_t)B * kin);  // hi and lo halves per element and row
+    a.o_red = (int)off; off = al(off + 4 * (size_t)(maxnt > 16 ? maxnt : 16) * 16 * B);
     a.o_stage = (int)off;
-    const size_t stage = 2 * sizeof(__half) * (size_t)B * a.kpc * a.kkc * a.hd;
+    off = al(off + 2 * sizeof(__half) * (size_t)B * a.kpc * a.kkc * a.hd);
+    // the sampler overlays the whole region: while a CTA samples, every buffer above is idle and no
+    // rank sends into it (the next step's exchanges need the token this sample produces)
     const size_t smp = sample_smem_bytes_dev(a.V, stepdev::kThreads);
-    off = al(off + (stage > smp ? stage : smp));
-    return off;
+    return off > smp ? off : al(smp);
 }
 
 int cstep_plan(CStepArgs& a, int sm_count) {
@@ -1063,9 +1263,7 @@ int cstep_plan(CStepArgs& a, int sm_count) {
     void* kern = pick(a);
     if (!kern || a.B < 1 || a.B > 2 || a.n_layer < 1 || a.Hkv < 1 || a.H % a.Hkv) return 0;
     if ((a.hd != 64 && a.hd != 128) || a.d % 32 || a.ff % 32 || a.V > sample_detail::kMaxV) return 0;
-    if (a.d > 8 * stepdev::kThreads) return 0;  // norm_to holds at most two float4 of a row per thread
-    const int maxk = a.quant == SD_Q4_0 ? 1024 : 1024;  // one (Q4_0) or two (Q8_0) 16-byte units per lane
-    if (a.d > maxk) return 0;
+    if (a.d > 2 * stepdev::kThreads) return 0;  // the norm holds at most two elements of a row per thread
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return 0;
@@ -1076,7 +1274,7 @@ int cstep_plan(CStepArgs& a, int sm_count) {
     // candidates: ncl divides Hkv, cs any size from 16 down to 2 (the part's GPCs do not all
     // hold the same number of clusters of a size); the most CTAs that can be resident wins,
     // then the most clusters (fewer heads per cluster)
-    std::vector<std::pair<int, int>> cand;  // (ncl, cs), best first: the most CTAs, then the most clusters
+    std::vector<std::pair<int, int>> cand;
     for (int ncl = a.Hkv; ncl >= 1; --ncl)
         if (a.Hkv % ncl == 0)
             for (int cs = 16; cs >= 2; --cs)
@@ -1085,77 +1283,73 @@ int cstep_plan(CStepArgs& a, int sm_count) {
         const int gx = x.first * x.second, gy = y.first * y.second;
         return gx != gy ? gx > gy : x.first > y.first;
     });
+    const int tb = frag_tb(a.quant);
     for (const auto& nc : cand) {
         if (best) break;
-        {
-            const int ncl = nc.first, cs = nc.second;
-            CStepArgs t = a;
-            t.ncl = ncl; t.cs = cs;
-            t.kpc = a.Hkv / ncl; t.hpc = a.H / ncl;
-            t.rpc = (t.hpc + 2 * t.kpc) * a.hd;
-            t.ko = t.hpc * a.hd;
-            t.upc = a.ff / ncl;
-            if (a.ff % ncl || t.upc % 32 || t.ko > maxk || t.upc > maxk) continue;
-            if (ncl * cs > a.V || cs > a.d || t.upc < cs || t.rpc < cs) continue;
-            // keys per rank staged at once: the whole share of a full context where it fits
-            const int G = ncl * cs;
-            auto cdiv = [](int x, int y) { return (x + y - 1) / y; };
-            const int urows = a.gpt2 ? cdiv(t.upc, cs) : 2 * cdiv(t.upc, cs);
-            int yrows = cdiv(t.rpc, cs) + 1;
-            yrows = std::max(yrows, cdiv(a.d, cs) + 1);
-            yrows = std::max(yrows, urows + 2);
-            yrows = std::max(yrows, cdiv(a.V, G) + 1);
-            t.kkc = std::min(256, std::max(32, ((cdiv(a.n_ctx, cs) + 31) / 32) * 32));
-            int act = (int)cstep_layout(t, yrows);
-            while (t.kkc > 32 && act > limit / 2) {
-                t.kkc -= 32;
-                act = (int)cstep_layout(t, yrows);
-            }
-            t.act_bytes = act;
-            const int ring = (limit - act - (int)(sizeof(StepLayer) * a.n_layer)) & ~127;
-            // the largest record: rows x (codes + scales) + bias and gain windows
-            auto rec = [&](int rows, int K, bool gains) {
-                const int rowb = a.quant == SD_Q4_0 ? K / 2 : K;
-                return rows * (rowb + K / 16) + 64 + (rows + 8) * 4 + (gains ? 8 * a.d : 0) + 256;
-            };
-            // records in step order: QKV, O, FC, proj per layer, then the head; the ring holds
-            // any two consecutive ones of a layer, so the next record streams in while one is in
-            // use (the head record, once per step, may have to wait for the ring to drain)
-            const int rq = rec(cdiv(t.rpc, cs), a.d, true), ro = rec(cdiv(a.d, cs), t.ko, false);
-            const int rf = rec(urows, a.d, true), rp = rec(cdiv(a.d, cs), t.upc, false);
-            const int rh = rec(cdiv(a.V, G), a.d, true);
-            const int need = std::max({rq + ro, ro + rf, rf + rp, rp + rq, rh});
-            if (dbg)
-                fprintf(stderr, "cstep plan: ncl %d cs %d act %d ring %d records %d %d %d %d %d kkc %d\n", ncl, cs,
-                        act, ring, rq, ro, rf, rp, rh, t.kkc);
-            if (ring < need) continue;
-            t.ring_bytes = ring;
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cstep_smem_bytes(t)) !=
-                cudaSuccess)
-                continue;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(G);
-            cfg.blockDim = dim3(stepdev::kBlock);
-            cfg.dynamicSmemBytes = cstep_smem_bytes(t);
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = cs;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int nclu = 0;
-            const cudaError_t oe = cudaOccupancyMaxActiveClusters(&nclu, kern, &cfg);
-            if (dbg) fprintf(stderr, "cstep plan: ncl %d cs %d: %d clusters fit (%s)\n", ncl, cs, nclu, cudaGetErrorString(oe));
-            if (oe != cudaSuccess || nclu < ncl) {
-                cudaGetLastError();
-                continue;
-            }
-            if (G > best || (G == best && ncl > pick_a.ncl)) {
-                best = G;
-                pick_a = t;
-            }
+        const int ncl = nc.first, cs = nc.second, G = ncl * cs;
+        CStepArgs t = a;
+        t.ncl = ncl; t.cs = cs;
+        t.kpc = a.Hkv / ncl; t.hpc = a.H / ncl;
+        t.rpc = (t.hpc + 2 * t.kpc) * a.hd;
+        t.ko = t.hpc * a.hd;
+        t.upc = a.ff / ncl;
+        if (a.ff % ncl || t.upc % 32) continue;
+        // every rank needs at least one tile of every matrix; the norm and B fragments cover a row
+        const int nq = t.rpc / 16, nd = a.d / 16, nf = (a.gpt2 ? t.upc : 2 * t.upc) / 16, nh = (a.V + 15) / 16;
+        if (nq < cs || nd < cs || nf < cs || nh < G || t.ko > 2 * stepdev::kThreads || t.upc > 2 * stepdev::kThreads)
+            continue;
+        if (a.B * t.hpc > stepdev::kWarps) continue;
+        auto cdiv = [](int x, int y) { return (x + y - 1) / y; };
+        const int tq = cdiv(nq, cs), td = cdiv(nd, cs), tf = cdiv(nf, cs), th = cdiv(nh, G);
+        const int maxnt = std::max({tq, td, tf, th});
+        // keys per rank staged at once: the whole share of a full context where it fits
+        t.kkc = std::min(256, std::max(32, ((cdiv(a.n_ctx, cs) + 31) / 32) * 32));
+        int act = (int)cstep_layout(t, maxnt);
+        while (t.kkc > 32 && act > limit / 2) {
+            t.kkc -= 32;
+            act = (int)cstep_layout(t, maxnt);
         }
+        t.act_bytes = act;
+        const int ring = (limit - act - (int)(sizeof(StepLayer) * a.n_layer)) & ~127;
+        // record bytes: tiles x blocks x (codes + scales) + bias and gain windows
+        auto rec = [&](int tiles, int K, bool gains) {
+            return tiles * (K / 32) * (tb + 32) + (16 * tiles + 8) * 4 + (gains ? 2 * 4 * gemv_detail::padded(a.d) : 0) +
+                   128;
+        };
+        // records in step order: QKV, O, FC, proj per layer, then the head; the ring holds any
+        // two consecutive ones of a layer, so the next record streams in while one is in use
+        // (the head record, once per step, may have to wait for the ring to drain)
+        const int rq = rec(tq, a.d, true), ro = rec(td, t.ko, false), rf = rec(tf, a.d, true);
+        const int rp = rec(td, t.upc, false), rh = rec(th, a.d, true);
+        const int need = std::max({rq + ro, ro + rf, rf + rp, rp + rq, rh});
+        if (dbg)
+            fprintf(stderr, "cstep plan: ncl %d cs %d act %d ring %d records %d %d %d %d %d kkc %d\n", ncl, cs, act,
+                    ring, rq, ro, rf, rp, rh, t.kkc);
+        if (ring < need) continue;
+        t.ring_bytes = ring;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cstep_smem_bytes(t)) !=
+            cudaSuccess)
+            continue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(G);
+        cfg.blockDim = dim3(cstep_detail::kCBlock);
+        cfg.dynamicSmemBytes = cstep_smem_bytes(t);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nclu = 0;
+        const cudaError_t oe = cudaOccupancyMaxActiveClusters(&nclu, kern, &cfg);
+        if (dbg) fprintf(stderr, "cstep plan: ncl %d cs %d: %d clusters fit (%s)\n", ncl, cs, nclu, cudaGetErrorString(oe));
+        if (oe != cudaSuccess || nclu < ncl) {
+            cudaGetLastError();
+            continue;
+        }
+        best = G;
+        pick_a = t;
     }
     if (!best) return 0;
     a = pick_a;
@@ -1171,7 +1365,7 @@ cudaError_t launch_cstep(const CStepArgs& a, cudaStream_t st) {
     if (!kern || a.ncl < 1 || a.cs < 1) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.ncl * a.cs);
-    cfg.blockDim = dim3(stepdev::kBlock);
+    cfg.blockDim = dim3(cstep_detail::kCBlock);
     cfg.dynamicSmemBytes = cstep_smem_bytes(a);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1185,13 +1379,16 @@ cudaError_t launch_cstep(const CStepArgs& a, cudaStream_t st) {
     return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
-cudaError_t launch_slab_gather(const QMat& src, int W, const int* perm, uint8_t* q_out, __half* s_out,
-                               cudaStream_t st) {
-    if ((src.kind != SD_Q4_0 && src.kind != SD_Q8_0) || W < 32 || W % 32 || src.cols % W) return cudaErrorInvalidValue;
-    const int q4 = src.kind == SD_Q4_0;
-    if ((q4 ? W / 2 : W) % 16) return cudaErrorInvalidValue;
-    cstep_detail::k_slab_gather<<<1024, 256, 0, st>>>(src.q, reinterpret_cast<const __half*>(src.s), src.rows,
-                                                      src.cols, W, q4, perm, q_out, s_out);
+size_t frag_bytes(int quant, int rows, int cols, int slab_cols) {
+    const int nt = (rows + 15) / 16, ns = cols / slab_cols, kb = slab_cols / 32;
+    return (size_t)ns * nt * kb * (cstep_detail::frag_tb(quant) + 32);
+}
+
+cudaError_t launch_frag_pack(const QMat& src, int slab_cols, const int* perm, uint8_t* out, cudaStream_t st) {
+    if ((src.kind != SD_Q4_0 && src.kind != SD_Q8_0) || slab_cols < 32 || slab_cols % 32 || src.cols % slab_cols)
+        return cudaErrorInvalidValue;
+    cstep_detail::k_frag_pack<<<1024, 256, 0, st>>>(src.q, reinterpret_cast<const __half*>(src.s), src.rows, src.cols,
+                                                    slab_cols, src.kind == SD_Q4_0, perm, out);
     return cudaGetLastError();
 }
 

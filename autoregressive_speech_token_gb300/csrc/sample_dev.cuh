@@ -174,7 +174,7 @@ static __device__ __forceinline__ void select_digit(const T* w, T rem, int shift
 // floats of `smraw`, which holds sample_smem_bytes_dev(V, threads) bytes) with draw
 // *u_ptr; every thread gets the token.  `ss` is the small scratch.  Block
 // size: any multiple of 32 up to 1024.
-static __device__ int sample_smem(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
+static __device__ __noinline__ int sample_smem(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
                                   SampleScratch& ss, int* err) {
     const int tid = threadIdx.x, nt = SAMPLE_NT, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const size_t arr = sample_array_bytes(V);

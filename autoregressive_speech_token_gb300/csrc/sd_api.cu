@@ -745,32 +745,49 @@ int setup_cstep(sd_ctx* c) {
     int* dperm = nullptr;
     if ((rc = dalloc(c, &dperm, sizeof(int) * R))) return rc;
     CK(cudaMemcpy(dperm, perm.data(), sizeof(int) * R, cudaMemcpyHostToDevice));
-    auto slab = [&](const QMat& W, int width, const int* pm, QMat* out) -> int {
-        const size_t qb = (size_t)W.rows * (W.kind == SD_Q4_0 ? W.cols / 2 : W.cols);
-        const size_t sb = (size_t)W.rows * (W.cols / 32) * sizeof(__half);
+    // fragment-major copy of a matrix: column slabs of `width` columns, rows permuted by pm
+    auto frag = [&](const QMat& W, int width, const int* pm, QMat* out) -> int {
         uint8_t* q = nullptr;
-        __half* sc = nullptr;
         int r;
-        // + 256: the step's bulk copies read scale windows widened to 16 bytes
-        if ((r = dalloc(c, &q, qb)) || (r = dalloc(c, &sc, sb + 256))) return r;
-        cudaError_t e = launch_slab_gather(W, width, pm, q, sc, c->stream);
-        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "slab gather: %s", cudaGetErrorString(e));
+        if ((r = dalloc(c, &q, frag_bytes(W.kind, W.rows, W.cols, width)))) return r;
+        cudaError_t e = launch_frag_pack(W, width, pm, q, c->stream);
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "fragment repack: %s", cudaGetErrorString(e));
         out->kind = W.kind;
-        out->rows = W.rows * (W.cols / width);
+        out->rows = (W.cols / width) * ((W.rows + 15) / 16) * 16;
         out->cols = width;
         out->q = q;
-        out->s = sc;
+        out->s = nullptr;
         return SD_OK;
     };
+    // a norm gain or offset vector [d] in the padded activation layout (four zero floats after
+    // every 32), as the kernel's matvec lanes read it next to their activations
+    std::vector<float> hv(s.d), hpad((size_t)s.d + (s.d >> 3));
+    auto padv = [&](const float* src, const float** out) -> int {
+        *out = nullptr;
+        if (!src) return SD_OK;
+        CK(cudaMemcpy(hv.data(), src, sizeof(float) * s.d, cudaMemcpyDeviceToHost));
+        std::fill(hpad.begin(), hpad.end(), 0.f);
+        for (int k = 0; k < s.d; ++k) hpad[k + ((k >> 5) << 2)] = hv[k];
+        float* dv = nullptr;
+        int r;
+        if ((r = dalloc(c, &dv, sizeof(float) * hpad.size()))) return r;
+        CK(cudaMemcpy(dv, hpad.data(), sizeof(float) * hpad.size(), cudaMemcpyHostToDevice));
+        *out = dv;
+        return SD_OK;
+    };
+    if ((rc = padv(s.nfg, &a.nfg)) || (rc = padv(s.nfb, &a.nfb))) return rc;
+    if ((rc = frag(c->head, c->head.cols, nullptr, &a.head))) return rc;
     std::vector<StepLayer> L(s.n_layer);
     std::vector<float> bh(R), bp(R);
     for (int l = 0; l < s.n_layer; ++l) {
         const DLayer& D = s.L[l];
         StepLayer& t = L[l];
-        t.n1g = D.n1g; t.n1b = D.n1b; t.bo = D.bo; t.n2g = D.n2g; t.n2b = D.n2b; t.bfc = D.bfc; t.bproj = D.bproj;
-        t.wfc = D.wfc;
-        if ((rc = slab(D.wqkv, D.wqkv.cols, dperm, &t.wqkv)) || (rc = slab(D.wo, a.ko, nullptr, &t.wo)) ||
-            (rc = slab(D.wproj, a.upc, nullptr, &t.wproj)))
+        t.bo = D.bo; t.bfc = D.bfc; t.bproj = D.bproj;
+        if ((rc = padv(D.n1g, &t.n1g)) || (rc = padv(D.n1b, &t.n1b)) || (rc = padv(D.n2g, &t.n2g)) ||
+            (rc = padv(D.n2b, &t.n2b)))
+            return rc;
+        if ((rc = frag(D.wqkv, D.wqkv.cols, dperm, &t.wqkv)) || (rc = frag(D.wo, a.ko, nullptr, &t.wo)) ||
+            (rc = frag(D.wfc, D.wfc.cols, nullptr, &t.wfc)) || (rc = frag(D.wproj, a.upc, nullptr, &t.wproj)))
             return rc;
         if (D.bqkv) {
             CK(cudaMemcpy(bh.data(), D.bqkv, sizeof(float) * R, cudaMemcpyDeviceToHost));
@@ -900,14 +917,15 @@ void write_ctrace(sd_ctx* c, int n_steps) {
     unsigned long long t[kCTraceSub];
     if (a.trace && cudaMemcpy(t, a.trace, sizeof t, cudaMemcpyDeviceToHost) == cudaSuccess) {
         // CTA 0's cycles per sub-step (per layer, or per step for the last four)
-        const char* nm[28] = {"wait x''", "rec qkv", "norm1", "gemv qkv", "send qkv", "wait qkv", "rope/append",
-                              "attn keys", "attn comb+send", "wait part", "combine", "rec o", "gemv o", "pub o",
-                              "reduce o", "wait x'", "rec fc", "norm2", "gemv fc", "send u", "wait u", "rec proj",
-                              "gemv proj", "pub proj", "reduce proj", "head*", "sample*", "embed*"};
+        const char* nm[28] = {"wait x''", "rec qkv", "norm1", "mma qkv+send", "wait qkv", "attn keys",
+                              "comb+send", "wait part", "combine", "rec o", "mma o+pub", "reduce o", "wait x'",
+                              "rec fc", "norm2", "mma fc+send", "wait u", "rec proj", "mma proj+pub", "reduce proj",
+                              "head*", "sample+end*", "", "", "", "", "start*", "embed*"};
         const double nl = (double)n_steps * L;
         fprintf(f, "  CTA 0 cycles per layer (* per step):\n   ");
         for (int k = 0; k < 28; ++k) {
-            fprintf(f, " %s %.0f |", nm[k], (double)t[k] / (k >= 25 ? (double)n_steps : nl));
+            if (!nm[k][0]) continue;
+            fprintf(f, " %s %.0f |", nm[k], (double)t[k] / (k >= 20 ? (double)n_steps : nl));
             if (k % 7 == 6) fprintf(f, "\n   ");
         }
         fprintf(f, "\n");

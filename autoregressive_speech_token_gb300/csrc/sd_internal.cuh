@@ -233,10 +233,12 @@ cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
 // Cluster persistent decode step (k_cstep.cu).  The grid is `ncl` thread-block
 // clusters of `cs` CTAs; cluster c owns KV heads [c*kpc, (c+1)*kpc) with their
 // query heads, FFN activations [c*upc, (c+1)*upc) and, through split-K
-// partials, a share of every residual row.  The layer table holds repacked
-// matrices: wqkv with each cluster's q, k, v rows contiguous ([ncl][rpc][d],
-// bqkv permuted alike), wo as column slabs [ncl][d][ko], wproj as column slabs
-// [ncl][d][upc]; wfc and the head keep the row-major layout.
+// partials, a share of every residual row.  Every matrix of the layer table
+// and the head are fragment-major copies (launch_frag_pack): wqkv with each
+// cluster's q, k, v rows contiguous (bqkv permuted alike), wo as ncl column
+// slabs of ko columns, wproj as ncl column slabs of upc columns, wfc and the
+// head as they are.  Norm gains and offsets are in the padded activation
+// layout (four zero floats after every 32).
 struct CStepArgs {
     int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, quant = 0;
     float eps = 1e-5f;
@@ -267,7 +269,7 @@ struct CStepArgs {
     int ring_bytes = 0, act_bytes = 0;
     int kkc = 128;                       // cached keys staged per (row, KV head) item at once
     // byte offsets in the activation region
-    int o_x = 0, o_xn = 0, o_u = 0, o_qkv = 0, o_part = 0, o_y = 0, o_wp = 0, o_stage = 0;
+    int o_x = 0, o_u = 0, o_qkv = 0, o_part = 0, o_wq = 0, o_wp = 0, o_bf = 0, o_red = 0, o_stage = 0;
     // optional publish stamps [2][kTraceSteps][n_layer][kCTracePhases] (latest, then earliest CTA)
     unsigned long long* trace_pub = nullptr;
     // optional [kCTraceSub]: CTA 0's clock64 cycles per sub-step, summed over the launch
@@ -280,11 +282,13 @@ size_t cstep_smem_bytes(const CStepArgs& a);
 // or 0 when the configuration does not fit the kernel.
 int cstep_plan(CStepArgs& a, int sm_count);
 cudaError_t launch_cstep(const CStepArgs& a, cudaStream_t st);
-// Column-slab / row-permuted copy of a Q8_0 or Q4_0 matrix for the cluster
-// step: out row (s*R + i) holds columns [s*W, (s+1)*W) of source row perm[i]
-// (perm null: i), for s < K / W.
-cudaError_t launch_slab_gather(const QMat& src, int W, const int* perm, uint8_t* q_out, __half* s_out,
-                               cudaStream_t st);
+// Fragment-major copy of a Q8_0 or Q4_0 matrix for the cluster step (k_cstep.cu):
+// column slabs of slab_cols columns, rows perm[i] (or i) of the source, padded
+// to whole 16-row tiles; frag_bytes() is its size.  The cluster step's layer
+// table holds such copies as QMat {kind, rows = slabs * tiles * 16, cols =
+// slab_cols, q = the copy, s = unused}.
+size_t frag_bytes(int quant, int rows, int cols, int slab_cols);
+cudaError_t launch_frag_pack(const QMat& src, int slab_cols, const int* perm, uint8_t* out, cudaStream_t st);
 
 // Tensor-core GEMM Y[M][N] = X[M][K] W[N][K]^T over a repacked weight, with
 // the GEMV epilogues (bias, GELU, interleaved SwiGLU -> Y[M][N/2], residual).
