@@ -15,7 +15,9 @@
 //   CTA normalises the full residual row; rank r computes its share of the
 //   cluster's q, k, v rows and sends them to every rank of the cluster
 //   (distributed shared memory, st.async completing on an mbarrier); rank r
-//   attends over its share of the cached keys and sends its partial softmax
+//   attends over its blocks of 32 cached positions (block j belongs to rank
+//   j % cs, so a position is appended and later read by the same CTA and the
+//   cache needs no cross-CTA ordering) and sends its partial softmax
 //   state (o, m, l) to every rank; every rank combines the partials and
 //   multiplies the head outputs by the cluster's column slab of Wo, for its
 //   own residual rows -- a split-K partial of the O projection.
@@ -93,11 +95,6 @@ __device__ __forceinline__ void st_async(uint32_t raddr, float v, uint32_t rmb) 
                  "r"(__float_as_uint(v)), "r"(rmb)
                  : "memory");
 }
-// one arrival on a cluster CTA's mbarrier, releasing (at cluster scope) every
-// write that happens before it -- the KV-cache append among them
-__device__ __forceinline__ void mb_arrive_remote(uint32_t rmb) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rmb) : "memory");
-}
 // non-blocking test of an mbarrier phase (this CTA's view)
 __device__ __forceinline__ bool mb_test(uint32_t mb, uint32_t parity) {
     uint32_t ok;
@@ -122,14 +119,15 @@ __device__ __forceinline__ void mb_arm(uint32_t mb, uint32_t bytes) {
 __device__ __forceinline__ bool mb_try_cl(uint32_t mb, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
         "selp.u32 %0, 1, 0, p; }"
         : "=r"(ok)
         : "r"(mb), "r"(parity)
         : "memory");
     return ok != 0;
 }
-// bounded wait for an exchange phase (cluster-scope acquire of the data)
+// bounded wait for a phase of this CTA's mbarrier: bytes written by st.async or bulk copies that
+// completed the phase are visible to the waiting thread once it returns true
 __device__ bool xb_wait(uint32_t mb, uint32_t parity, int* err, long long budget) {
     if (mb_try_cl(mb, parity)) return true;
     const long long t0 = clock64();
@@ -439,25 +437,35 @@ __device__ __forceinline__ void mma_rows(const uint8_t* codes, const uint8_t* sc
         }
     }
     csync();
-    if (PAIRS) {
-        for (int i = tid; i < (nr >> 1) * NB; i += kThreads) {
-            const int k = NB == 1 ? i : i / NB, b = i - k * NB;
-            const int r0 = 2 * k, rt = r0 >> 4, rr = r0 & 15;
-            float v0 = 0.f, v1 = 0.f;
-            for (int s = 0; s < KS; ++s) {
-                v0 += red[((rt * KS + s) * 16 + rr) * NB + b];
-                v1 += red[((rt * KS + s) * 16 + rr + 1) * NB + b];
-            }
-            emit(k, b, v0, v1);
+    // the KS slices of an output meet by xor shuffles: lane s of a group of KSP (a power of two
+    // >= KS) lanes loads slice s (a fixed order); the group then holds the sum
+    int lk = 0;
+    while ((1 << lk) < KS) ++lk;
+    const int KSP = 1 << lk;
+    const int outs = PAIRS ? (nr >> 1) * NB : nr * NB;
+    for (int base = 0; base < outs * KSP; base += kThreads) {
+        const int x = base + tid, o = x >> lk, s = x & (KSP - 1);
+        const bool live = o < outs;
+        int row, b;
+        if (PAIRS) {
+            const int k = NB == 1 ? o : o / NB;
+            b = o - k * NB;
+            row = 2 * k;
+        } else {
+            row = NB == 1 ? o : o / NB;
+            b = o - row * NB;
         }
-    } else {
-        for (int i = tid; i < nr * NB; i += kThreads) {
-            const int row = NB == 1 ? i : i / NB, b = i - row * NB;
-            const int rt = row >> 4, rr = row & 15;
-            float v = 0.f;
-            for (int s = 0; s < KS; ++s) v += red[((rt * KS + s) * 16 + rr) * NB + b];
-            emit(row, b, v, 0.f);
+        const int rt = row >> 4, rr = row & 15;
+        float v0 = 0.f, v1 = 0.f;
+        if (live && s < KS) {
+            v0 = red[((rt * KS + s) * 16 + rr) * NB + b];
+            if (PAIRS) v1 = red[((rt * KS + s) * 16 + rr + 1) * NB + b];
         }
+        for (int m = 1; m < KSP; m <<= 1) {
+            v0 += __shfl_xor_sync(0xffffffffu, v0, m);
+            if (PAIRS) v1 += __shfl_xor_sync(0xffffffffu, v1, m);
+        }
+        if (live && s == 0) emit(PAIRS ? row >> 1 : row, b, v0, v1);
     }
 }
 
@@ -563,20 +571,39 @@ __device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
         float acc = 0.f;
         if (valid) {
             for (int c0 = j; c0 < ncl; c0 += 4 * TPR) {
+                // the (up to) four words are polled together until all carry epoch e, so the
+                // wait ends one load after the last of them lands
+                const unsigned long long* pw[4];
                 unsigned long long w[4];
+                unsigned pend = 0u;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c = c0 + q * TPR;
-                    w[q] = c < ncl ? ll_load(P + ((size_t)c * NB + b) * d + xr0 + i) : 0ull;
+                    pw[q] = P + ((size_t)(c < ncl ? c : 0) * NB + b) * d + xr0 + i;
+                    w[q] = 0ull;
+                    if (c < ncl) pend |= 1u << q;
+                }
+                const long long t0 = clock64();
+                for (unsigned it = 0; pend && ok; ++it) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (pend & (1u << q)) w[q] = ll_load(pw[q]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if ((pend & (1u << q)) && (unsigned)(w[q] >> 32) == e) pend &= ~(1u << q);
+                    if (!pend) break;
+                    if (it > 2u) __nanosleep(32);
+                    if ((it & 31u) == 31u) {
+                        if (ld_volatile(err)) ok = false;
+                        else if (clock64() - t0 > budget) {
+                            atomicCAS(err, 0, kErrTimeout);
+                            ok = false;
+                        }
+                    }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int c = c0 + q * TPR;
-                    if (c >= ncl) continue;
-                    if (ok && (unsigned)(w[q] >> 32) != e)
-                        ok = ll_spin(P + ((size_t)c * NB + b) * d + xr0 + i, e, &w[q], err, budget);
-                    acc += __uint_as_float((unsigned)w[q]);
-                }
+                for (int q = 0; q < 4; ++q)
+                    if (c0 + q * TPR < ncl) acc += __uint_as_float((unsigned)w[q]);
             }
         }
         for (int o = 1; o < TPR; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -665,8 +692,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             mb_init(smem_u32(&s_mb[k]));
             mb_init_n(smem_u32(&s_empty[k]), kWarps);
         }
-        // the partial exchange also counts one release arrival per rank (see the attention phase)
-        for (int k = 0; k < 5; ++k) mb_init_n(smem_u32(&s_xb[k]), k == XB_PART ? 1 + a.cs : 1);
+        for (int k = 0; k < 5; ++k) mb_init_n(smem_u32(&s_xb[k]), 1);
         mb_init(smem_u32(&s_kv));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -737,8 +763,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
     // issued as soon as it fits); false on an expired wait or a recorded error
     auto rec_wait = [&]() -> bool {
         const uint32_t mb = smem_u32(&s_mb[nc & (kNMB - 1)]), par = (uint32_t)((nc / kNMB) & 1);
-        if (tid == 0) pump();
-        if (mb_try(mb, par)) return true;
+        if (mb_test(mb, par)) return true;  // landed (thread 0 refills the ring when it has to wait)
         const long long t0 = clock64();
         for (unsigned it = 1;; ++it) {
             if (tid == 0) pump();
@@ -763,7 +788,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
     // is re-armed before this CTA's next CTA-wide barrier, and no rank sends the next phase's data
     // before this CTA has passed that barrier.)
     auto xwait = [&](uint32_t mb, unsigned& ph, uint32_t bytes) -> bool {
-        if (tid == 0) pump();
+        if (tid == 0 && !mb_test(mb, ph & 1u)) pump();  // idle time: refill the weight ring
         const bool ok = xb_wait(mb, ph & 1u, a.err, budget);
         if (ok && tid == 0) mb_arm(mb, bytes);
         ++ph;
@@ -785,26 +810,38 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             const size_t i = ((size_t)s_ * L + l_) * kCTracePhases + phs;
             atomicMax(a.trace_pub + i, t);
             atomicMin(a.trace_pub + (size_t)kTraceSteps * L * kCTracePhases + i, t);
+            if (a.trace_cta && s_ < kCtaSteps) a.trace_cta[i * (a.ncl * a.cs) + gi] = t;
         }
     };
-    // KV staging of keys [j0, j1) of layer l for every (row, KV head) item of the cluster, without
-    // the position being decoded (its key comes from this step): two bulk copies per item (thread 0)
+    // KV staging: the cached keys are owned in blocks of 32 positions, block j by rank j % cs, so the
+    // rank that appends a position is the only one that ever reads it back (no cross-CTA ordering of
+    // the cache is needed).  Staging fill: this rank's blocks q0..q1-1 (block j = rank + q * cs) of
+    // layer l for every (row, KV head) item, without the position being decoded (its key comes
+    // from this step): two bulk copies per item and block (thread 0)
     int kv_issued = 0;
-    auto kv_fetch = [&](int l, int pos, int j0, int j1) {
+    const int SB = a.kkc / 32;  // blocks per staging fill
+    auto kv_fetch = [&](int l, int pos, int q0, int q1) {
         ++kv_issued;
         // the staging was last read by generic loads; the cache was appended by generic stores
         asm volatile("fence.proxy.async.shared::cta;\n\tfence.proxy.async.global;" ::: "memory");
-        const int jc = min(j1, pos);
-        const int nk = jc > j0 ? jc - j0 : 0, items = NB * a.kpc;
-        const uint32_t bytes = (uint32_t)(nk * hd * 2);
-        mb_expect(mb_kv, 2u * (uint32_t)items * bytes);
-        if (nk > 0)
+        const int items = NB * a.kpc;
+        uint32_t total = 0u;
+        for (int q = q0; q < q1; ++q) {
+            const int j = rank + q * cs, nrow = min(32, pos - 32 * j);
+            if (nrow > 0) total += (uint32_t)(nrow * hd * 2);
+        }
+        mb_expect(mb_kv, 2u * (uint32_t)items * total);
+        for (int q = q0; q < q1; ++q) {
+            const int j = rank + q * cs, nrow = min(32, pos - 32 * j);
+            if (nrow <= 0) continue;
             for (int it = 0; it < items; ++it) {
                 const int b = it / a.kpc, gg = cl * a.kpc + (it - b * a.kpc);
-                const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd + (size_t)j0 * hd;
-                bulk_g2s(smem_u32(stg + (size_t)it * a.kkc * hd), a.kc + hb, bytes, mb_kv);
-                bulk_g2s(smem_u32(stg + ((size_t)items + it) * a.kkc * hd), a.vc + hb, bytes, mb_kv);
+                const size_t hb = ((size_t)(b * L + l) * a.Hkv + gg) * a.n_ctx * hd + (size_t)(32 * j) * hd;
+                const size_t so = ((size_t)it * a.kkc + (q - q0) * 32) * hd;
+                bulk_g2s(smem_u32(stg + so), a.kc + hb, (uint32_t)(nrow * hd * 2), mb_kv);
+                bulk_g2s(smem_u32(stg + (size_t)items * a.kkc * hd + so), a.vc + hb, (uint32_t)(nrow * hd * 2), mb_kv);
             }
+        }
     };
     // matvec operands of the current record
     auto rec_codes = [&](const unsigned char* rec) { return reinterpret_cast<const uint8_t*>(rec); };
@@ -814,11 +851,11 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
     for (int s = 0; s < a.n_steps; ++s) {
         const int pos = pos0 + s, n = pos + 1;
         const unsigned eb = 1u + (gen0 + (unsigned)s) * (unsigned)(L + 1);
-        const int c0 = n * rank / cs, c1 = n * (rank + 1) / cs;  // this rank's keys
-        const bool last = c1 == n;             // this rank holds the position being decoded
-        const bool one_pass = c1 - c0 <= a.kkc;  // the rank's keys fit the staging at once
+        const int nb = (n + 31) >> 5;                                      // key blocks
+        const int nbr = nb > rank ? (nb - rank + cs - 1) / cs : 0;          // this rank's blocks
+        const int jl = nb - 1;                                              // the block of pos
         stamp(26);
-        if (tid == 0) kv_fetch(0, pos, c0, one_pass ? c1 : c0 + a.kkc);
+        if (tid == 0) kv_fetch(0, pos, 0, min(nbr, SB));
         // RoPE angles at pos for the pairs (i, i + hd/2) of this lane, i = lane, lane + 32
         float rcs[2] = {1.f, 1.f}, rsn[2] = {0.f, 0.f};
         if (a.rope_cos)
@@ -889,7 +926,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                 tr_pub(s, l, 1);
                 stamp(3);
             }
-            // ---- attention over this rank's keys [c0, c1)
+            // ---- attention over this rank's key blocks
             {
                 xwait(mb_qkv, ph_qkv, xb_bytes_of(XB_QKV));
                 stamp(4);
@@ -936,32 +973,35 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                     }
                 };
                 __syncwarp();
-                for (int j0s = c0; j0s < c1; j0s += a.kkc) {
-                    const int j1s = min(c1, j0s + a.kkc), nk = j1s - j0s;
-                    if (j0s != c0) {
-                        // a later sub-chunk: every warp is done with the staging first
+                stamp(22);
+                for (int q0 = 0;; q0 += SB) {
+                    const int q1 = min(nbr, q0 + SB);
+                    if (q0 != 0) {
+                        // a later staging fill: every warp is done with the staging first
                         csync();
-                        if (tid == 0) kv_fetch(l, pos, j0s, j1s);
+                        if (tid == 0) kv_fetch(l, pos, q0, q1);
                     }
                     xb_wait(mb_kv, ph_kv & 1u, a.err, budget);
                     ++ph_kv;
+                    stamp(23);
                     if (pr < nph) {
                         const float* q = wq + warp * hd;
-                        const __half* Ki = Ks + (size_t)(b * a.kpc + gl) * a.kkc * hd;
-                        const __half* Vi = Vs + (size_t)(b * a.kpc + gl) * a.kkc * hd;
-                        for (int j0 = wi * 32; j0 < nk; j0 += WG * 32) {
-                            if (last && j1s == c1 && j0 + 32 >= nk) {
-                                // this pass holds the position being decoded (local index nk - 1)
-                                put_new(nk - 1, qh % hpg == 0);
+                        for (int qq = wi; q0 + qq < q1; qq += WG) {
+                            const int j = rank + (q0 + qq) * cs, nk = min(32, n - 32 * j);
+                            const size_t so = ((size_t)(b * a.kpc + gl) * a.kkc + qq * 32) * hd;
+                            if (j == jl) {
+                                // this block holds the position being decoded (row nk - 1)
+                                put_new(qq * 32 + nk - 1, qh % hpg == 0);
                                 asm volatile("fence.proxy.async.global;" ::: "memory");
                                 __syncwarp();
                             }
                             if (hd == 64)
-                                attn_lk<64>(q, Ki, Vi, j0, nk, m, lsum, *reinterpret_cast<float(*)[2]>(o));
+                                attn_lk<64>(q, Ks + so, Vs + so, 0, nk, m, lsum, *reinterpret_cast<float(*)[2]>(o));
                             else
-                                attn_lk<128>(q, Ki, Vi, j0, nk, m, lsum, o);
+                                attn_lk<128>(q, Ks + so, Vs + so, 0, nk, m, lsum, o);
                         }
                     }
+                    if (q1 >= nbr) break;
                 }
                 stamp(5);
                 // warp partials -> the warps of a pair combined in warp order -> every rank
@@ -976,9 +1016,9 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                     }
                 }
                 csync();
-                // only the first ceil(keys / 32) warps of a pair hold keys (the last sub-chunk decides)
-                const int nkl = c1 - c0 - ((c1 - c0 - 1) / a.kkc) * a.kkc;
-                const int wa = c1 > c0 ? min(WG, (max(nkl, min(c1 - c0, a.kkc)) + 31) / 32) : 0;
+                stamp(24);
+                // only the first min(WG, blocks per fill) warps of a pair hold keys
+                const int wa = min(WG, min(nbr, SB));
                 for (int u = tid; u < nph * (hd + 2); u += kThreads) {
                     const int p = u == tid ? cp_p : u / (hd + 2), k = u == tid ? cp_k : u - p * (hd + 2);
                     const float* P = wp + (size_t)p * WG * W2;
@@ -995,12 +1035,9 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                     const uint32_t addr = a_part + 4u * (uint32_t)((rank * NB * a.hpc + p) * W2 + k);
                     for (int dst = 0; dst < cs; ++dst) st_async(mapa(addr, dst), v, mapa(mb_part, dst));
                 }
-                // one release arrival per rank, after this CTA's barrier: a reader of this KV head's
-                // cache in a later step (another rank of this cluster) acquires the append through it
-                csync();
-                if (tid < cs) mb_arrive_remote(mapa(mb_part, tid));
+                stamp(25);
                 // the staging is free: the next layer's keys (off the critical path, after the sends)
-                if (tid == 0 && l + 1 < L) kv_fetch(l + 1, pos, c0, one_pass ? c1 : c0 + a.kkc);
+                if (tid == 0 && l + 1 < L) kv_fetch(l + 1, pos, 0, min(nbr, SB));
                 tr_pub(s, l, 2);
                 stamp(6);
             }

@@ -813,7 +813,8 @@ int setup_cstep(sd_ctx* c) {
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
         if ((rc = dalloc(c, &a.trace_pub, sizeof(unsigned long long) * 2 * kTraceSteps * a.n_layer * kCTracePhases)) ||
-            (rc = dalloc(c, &a.trace, sizeof(unsigned long long) * kCTraceSub)))
+            (rc = dalloc(c, &a.trace, sizeof(unsigned long long) * kCTraceSub)) ||
+            (rc = dalloc(c, &a.trace_cta, sizeof(unsigned long long) * kCtaSteps * a.n_layer * kCTracePhases * grid)))
             return rc;
     }
     CK(cudaStreamSynchronize(c->stream));
@@ -914,18 +915,33 @@ void write_ctrace(sd_ctx* c, int n_steps) {
         tot += dl[ph] / 1e3 / cnt;
     }
     fprintf(f, "    layer     %8.3f\n", tot);
+    if (a.trace_cta) {
+        // every CTA's stamps of the first steps, raw, beside the trace: int32 grid, layers, phases,
+        // steps, then [steps][layers][phases][grid] uint64 global-timer ns
+        const int G = a.ncl * a.cs, ns2 = std::min(n_steps, kCtaSteps);
+        std::vector<unsigned long long> tc((size_t)kCtaSteps * L * kCTracePhases * G);
+        if (cudaMemcpy(tc.data(), a.trace_cta, tc.size() * 8, cudaMemcpyDeviceToHost) == cudaSuccess) {
+            FILE* fb = fopen((c->trace_path + ".cta.bin").c_str(), "wb");
+            if (fb) {
+                const int32_t hdr[4] = {G, L, kCTracePhases, ns2};
+                fwrite(hdr, sizeof hdr, 1, fb);
+                fwrite(tc.data(), 8, (size_t)ns2 * L * kCTracePhases * G, fb);
+                fclose(fb);
+            }
+        }
+    }
     unsigned long long t[kCTraceSub];
     if (a.trace && cudaMemcpy(t, a.trace, sizeof t, cudaMemcpyDeviceToHost) == cudaSuccess) {
         // CTA 0's cycles per sub-step (per layer, or per step for the last four)
         const char* nm[28] = {"wait x''", "rec qkv", "norm1", "mma qkv+send", "wait qkv", "attn keys",
                               "comb+send", "wait part", "combine", "rec o", "mma o+pub", "reduce o", "wait x'",
                               "rec fc", "norm2", "mma fc+send", "wait u", "rec proj", "mma proj+pub", "reduce proj",
-                              "head*", "sample+end*", "", "", "", "", "start*", "embed*"};
+                              "head*", "sample+end*", "(q prep)", "(kv wait)", "(wp+bar)", "(send+bar)", "start*", "embed*"};
         const double nl = (double)n_steps * L;
         fprintf(f, "  CTA 0 cycles per layer (* per step):\n   ");
         for (int k = 0; k < 28; ++k) {
             if (!nm[k][0]) continue;
-            fprintf(f, " %s %.0f |", nm[k], (double)t[k] / (k >= 20 ? (double)n_steps : nl));
+            fprintf(f, " %s %.0f |", nm[k], (double)t[k] / ((k >= 20 && k <= 21) || k >= 26 ? (double)n_steps : nl));
             if (k % 7 == 6) fprintf(f, "\n   ");
         }
         fprintf(f, "\n");

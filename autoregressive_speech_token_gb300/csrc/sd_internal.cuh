@@ -269,12 +269,15 @@ struct CStepArgs {
     int ring_bytes = 0, act_bytes = 0;
     int kkc = 128;                       // cached keys staged per (row, KV head) item at once
     // byte offsets in the activation region
-    int o_x = 0, o_u = 0, o_qkv = 0, o_part = 0, o_wq = 0, o_wp = 0, o_bf = 0, o_red = 0, o_stage = 0;
+    int o_x = 0, o_u = 0, o_qkv = 0, o_part = 0, o_wq = 0, o_wp = 0, o_bf = 0, o_red = 0, o_yv = 0, o_stage = 0;
     // optional publish stamps [2][kTraceSteps][n_layer][kCTracePhases] (latest, then earliest CTA)
     unsigned long long* trace_pub = nullptr;
     // optional [kCTraceSub]: CTA 0's clock64 cycles per sub-step, summed over the launch
     unsigned long long* trace = nullptr;
+    // optional [kCtaSteps][n_layer][kCTracePhases][grid]: every CTA's publish stamps of the first steps
+    unsigned long long* trace_cta = nullptr;
 };
+constexpr int kCtaSteps = 4;
 constexpr int kCTraceSub = 32;
 constexpr int kCTracePhases = 8;  // x ready, QKV sent, attention sent, O published, x' sent, u sent, proj published, x'' sent
 size_t cstep_smem_bytes(const CStepArgs& a);
