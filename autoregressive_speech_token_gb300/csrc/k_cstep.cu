@@ -1159,25 +1159,41 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             float* z = reinterpret_cast<float*>(actb);
             csync();  // the head's partial sums are read
             const int b = gi;
-            for (int i0 = tid; i0 < a.V; i0 += 4 * kThreads) {
-                unsigned long long w[4];
+            // every word of the row is loaded (16 per thread at a time), then the ones not yet carrying
+            // epoch eh are polled again together
+            for (int i0 = tid; i0 < a.V; i0 += 16 * kThreads) {
+                unsigned long long w[16];
+                unsigned pend = 0u;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     const int i = i0 + j * kThreads;
                     w[j] = i < a.V ? ll_load(a.ll_logits + (size_t)b * a.V + i) : 0ull;
+                    if (i < a.V && (unsigned)(w[j] >> 32) != eh) pend |= 1u << j;
+                }
+                const long long t0 = clock64();
+                for (unsigned it = 0; pend; ++it) {
+                    if (it > 2u) __nanosleep(32);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (pend & (1u << j)) {
+                            w[j] = ll_load(a.ll_logits + (size_t)b * a.V + i0 + j * kThreads);
+                            if ((unsigned)(w[j] >> 32) == eh) pend &= ~(1u << j);
+                        }
+                    if ((it & 31u) == 31u && (ld_volatile(a.err) || clock64() - t0 > budget)) {
+                        atomicCAS(a.err, 0, kErrTimeout);
+                        break;
+                    }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     const int i = i0 + j * kThreads;
-                    if (i >= a.V) continue;
-                    if ((unsigned)(w[j] >> 32) != eh)
-                        ll_spin(a.ll_logits + (size_t)b * a.V + i, eh, &w[j], a.err, budget);
-                    z[i] = __uint_as_float((unsigned)w[j]);
+                    if (i < a.V) z[i] = __uint_as_float((unsigned)w[j]);
                 }
             }
             csync();
+            stamp(28);
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + b : a.u1 + b;
-            const int tk = sample_detail::sample_smem(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
+            const int tk = sample_detail::sample_fast(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
                                                       a.err);
             if (tid == 0) {
                 a.tok[b] = tk;
@@ -1185,6 +1201,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
 #pragma unroll
                 for (int r = 0; r < kTokRep; ++r) ll_store(a.ll_tok + r * 32 + b, __int_as_float(tk), eh);
             }
+            stamp(29);
         }
         // the step ends uniformly: on a recorded error every thread leaves here
         ok = csync_and(ld_volatile(a.err) == 0) != 0;

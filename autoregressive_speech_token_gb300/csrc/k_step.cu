@@ -922,7 +922,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             if (!ok) break;
             tr_waited();
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + cta : a.u1 + cta;
-            const int tok = sample_detail::sample_smem(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
+            const int tok = sample_detail::sample_fast(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
                                                        a.err);
             if (tid == 0) {
                 a.tok[cta] = tok;

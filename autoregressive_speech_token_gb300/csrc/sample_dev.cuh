@@ -370,6 +370,223 @@ static __device__ __noinline__ int sample_smem(int V, const SampParams sp, const
     return tok;
 }
 
+// ---------------------------------------------------------------- fast path
+//
+// The same sampler (the same survivors, fixed-point masses, cut and draw as
+// sample_smem, so the same token) located through value histograms instead of
+// radix passes.  The logits are binned linearly between their minimum and
+// maximum (kFB bins, bin 0 holding the largest): the bin of a value is a
+// monotone function of it, so equal values share a bin and every value of a
+// bin is at least every value of a later bin.  One count histogram and one
+// prefix over the bins find the bin holding the k-th largest logit; the exact
+// k-th largest key is then selected among that bin's members.  The top-p cut
+// is found the same way on a histogram of fixed-point masses: the bin where the
+// cumulative mass (from the top) reaches top_p * Z, then, among its members in
+// (key desc, index asc) order, the element where it does.  A bin with more than
+// kFC members (a degenerate distribution) falls back to sample_smem.
+constexpr int kFB = 2048, kFC = 1024;
+
+// shared memory after z[V]: the survivors' masses q[V] (u32), the count and mass histograms, the candidates
+static __host__ __device__ __forceinline__ size_t sample_fast_extra_bytes(int V) {
+    return sample_array_bytes(V) + (size_t)kFB * 4 + (size_t)kFB * 8 + (size_t)kFC * (4 + 4 + 4) + 64;
+}
+
+static __device__ __forceinline__ int vbin(float z, float mx, float sc) {
+    const float f = (mx - z) * sc;  // >= 0, non-decreasing as z decreases
+    return f >= (float)(kFB - 1) ? kFB - 1 : (int)f;
+}
+
+static __device__ float block_min_f(float v, float* s) {
+    return -block_max_f(-v, s);
+}
+
+// Inclusive scan over the threads of one value per thread (thread order); the
+// exclusive prefix is returned, the block total in *total.
+static __device__ __forceinline__ unsigned block_excl_scan_u32(unsigned v, unsigned long long* s, unsigned* total) {
+    unsigned long long tot;
+    const unsigned long long r = block_exclusive_scan_u64(v, s, &tot);
+    *total = (unsigned)tot;
+    return (unsigned)r;
+}
+
+static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
+                                               SampleScratch& ss, int* err) {
+    const int tid = threadIdx.x, nt = SAMPLE_NT;
+    if (sp.greedy || sp.top_k == 1 || sp.temperature <= 0.f || nt * 4 != kFB)
+        return sample_smem(V, sp, u_ptr, smraw, ss, err);
+    const size_t arr = sample_array_bytes(V);
+    const float* z = reinterpret_cast<const float*>(smraw);
+    // each survivor's mass p * 2^31 (truncated, <= 2^31: fits 32 bits), computed once; 0 for the others
+    unsigned* qv = reinterpret_cast<unsigned*>(smraw + arr);               // [V]
+    unsigned* cnt = reinterpret_cast<unsigned*>(smraw + 2 * arr);          // [kFB]
+    // per-bin masses, as sums of their high and low 16-bit halves (32-bit shared atomics; exact:
+    // at most 2^14 terms of at most 2^16 each), combined into mass[] before the prefix
+    unsigned long long* mass = reinterpret_cast<unsigned long long*>(cnt + kFB);  // [kFB]
+    unsigned* mh = reinterpret_cast<unsigned*>(mass);                      // [kFB], in mass[]'s space
+    unsigned* ml = mh + kFB;                                               // [kFB]
+    uint32_t* ckey = reinterpret_cast<uint32_t*>(mass + kFB);              // [kFC]
+    int* cidx = reinterpret_cast<int*>(ckey + kFC);                        // [kFC]
+    unsigned* cq = reinterpret_cast<unsigned*>(cidx + kFC);                // [kFC]
+
+    float mloc = -INFINITY, nloc = INFINITY;
+    for (int i = tid; i < V; i += nt) {
+        mloc = fmaxf(mloc, z[i]);
+        nloc = fminf(nloc, z[i]);
+    }
+    const float mx = block_max_f(mloc, ss.f), mn = block_min_f(nloc, ss.f);
+    // (capped: a range near the smallest normal would make the scale infinite, and 0 * inf is not 0)
+    const float sc = mx > mn ? fminf((float)(kFB - 1) / (mx - mn), 1e30f) : 0.f;
+    const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
+    const float invT = 1.0f / sp.temperature;
+    for (int b = tid; b < kFB; b += nt) {
+        cnt[b] = 0u;
+        mh[b] = 0u;
+        ml[b] = 0u;
+    }
+    if (tid == 0) { ss.i[0] = 0; ss.i[1] = 0; }
+    SAMPLE_SYNC();
+
+    // ---- top-k threshold key
+    uint32_t thr = 0u;
+    if (k < V) {
+        for (int i = tid; i < V; i += nt) atomicAdd(&cnt[vbin(z[i], mx, sc)], 1u);
+        SAMPLE_SYNC();
+        const uint4 c4 = reinterpret_cast<const uint4*>(cnt)[tid];  // bins 4 tid .. 4 tid + 3
+        unsigned tot;
+        unsigned cum = block_excl_scan_u32(c4.x + c4.y + c4.z + c4.w, ss.q, &tot);
+        const unsigned cb[4] = {c4.x, c4.y, c4.z, c4.w};
+        for (int j = 0; j < 4; ++j) {
+            if (cum < (unsigned)k && cum + cb[j] >= (unsigned)k) {
+                ss.i[2] = 4 * tid + j;          // the bin of the k-th largest
+                ss.i[3] = k - (int)cum;         // its rank inside the bin (1 = the bin's largest)
+                ss.i[4] = (int)cb[j];
+            }
+            cum += cb[j];
+        }
+        SAMPLE_SYNC();
+        const int bk = ss.i[2], rk = ss.i[3], nbk = ss.i[4];
+        if (nbk > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
+        for (int i = tid; i < V; i += nt)
+            if (vbin(z[i], mx, sc) == bk) ckey[atomicAdd(&ss.i[0], 1)] = ord_key(z[i]);
+        SAMPLE_SYNC();
+        for (int c = tid; c < nbk; c += nt) {
+            const uint32_t key = ckey[c];
+            int gt = 0, ge = 0;
+            for (int j = 0; j < nbk; ++j) {
+                gt += ckey[j] > key;
+                ge += ckey[j] >= key;
+            }
+            if (gt < rk && rk <= ge) ss.sel[0] = key;  // every writer writes the same key
+        }
+        SAMPLE_SYNC();
+        thr = ss.sel[0];
+    }
+
+    // ---- survivors' fixed-point masses: the total, and (for top-p) per bin
+    const bool topp = sp.top_p < 1.0f;
+    unsigned long long zl = 0ull;
+    for (int i = tid; i < V; i += nt) {
+        if (ord_key(z[i]) < thr) {
+            qv[i] = 0u;
+            continue;
+        }
+        const unsigned q = (unsigned)fixq(expf((z[i] - mx) * invT));
+        qv[i] = q;
+        zl += q;
+        if (topp) {
+            const int bn = vbin(z[i], mx, sc);
+            atomicAdd(&mh[bn], (unsigned)(q >> 16));
+            atomicAdd(&ml[bn], (unsigned)(q & 0xFFFFu));
+        }
+    }
+    unsigned long long Zq;
+    block_exclusive_scan_u64(zl, ss.q, &Zq);  // barrier: the mass histograms are complete
+
+    // ---- top-p cut: (tkey, tidx) of the element where the (key desc, index asc) cumulative mass
+    // reaches T = ceil(top_p * Z)
+    bool cut = false;
+    uint32_t tkey = 0u;
+    int tidx = 0x7fffffff;
+    if (topp) {
+        const unsigned long long T0 = (unsigned long long)ceil((double)sp.top_p * (double)Zq);
+        const unsigned long long T = T0 > 0ull ? T0 : 1ull;
+        const uint4 h4 = reinterpret_cast<const uint4*>(mh)[tid], l4 = reinterpret_cast<const uint4*>(ml)[tid];
+        const unsigned long long mb[4] = {((unsigned long long)h4.x << 16) + l4.x, ((unsigned long long)h4.y << 16) + l4.y,
+                                          ((unsigned long long)h4.z << 16) + l4.z, ((unsigned long long)h4.w << 16) + l4.w};
+        unsigned long long tot;
+        unsigned long long cum = block_exclusive_scan_u64(mb[0] + mb[1] + mb[2] + mb[3], ss.q, &tot);
+        if (tid == 0) ss.i[0] = 0;
+        for (int j = 0; j < 4; ++j) {
+            if (cum < T && cum + mb[j] >= T) {
+                ss.i[5] = 4 * tid + j;  // the bin where the cumulative mass reaches T
+                ss.rem = T - cum;       // mass still needed inside it
+            }
+            cum += mb[j];
+        }
+        SAMPLE_SYNC();
+        const int bp = ss.i[5];
+        const unsigned long long remT = ss.rem;
+        for (int i = tid; i < V; i += nt) {
+            const uint32_t key = ord_key(z[i]);
+            if (key < thr || vbin(z[i], mx, sc) != bp) continue;
+            const int c = atomicAdd(&ss.i[0], 1);
+            if (c < kFC) {
+                ckey[c] = key;
+                cidx[c] = i;
+                cq[c] = qv[i];
+            }
+        }
+        SAMPLE_SYNC();
+        const int np = ss.i[0];
+        if (np > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
+        for (int c = tid; c < np; c += nt) {
+            const uint32_t key = ckey[c];
+            const int idx = cidx[c];
+            unsigned long long pre = 0ull;  // mass before this element in (key desc, index asc) order
+            for (int j = 0; j < np; ++j)
+                if (ckey[j] > key || (ckey[j] == key && cidx[j] < idx)) pre += cq[j];
+            if (pre < remT && pre + (unsigned long long)cq[c] >= remT) {
+                ss.sel[1] = key;
+                ss.sel[2] = (uint32_t)idx;
+            }
+        }
+        SAMPLE_SYNC();
+        tkey = ss.sel[1];
+        tidx = (int)ss.sel[2];
+        cut = true;
+    }
+
+    // ---- draw in vocabulary order over the kept elements (exact fixed-point prefix sums)
+    auto kept = [&](int i) {
+        if (!cut) return true;  // qv is 0 for the elements under the top-k threshold
+        const uint32_t key = ord_key(z[i]);
+        return key > tkey || (key == tkey && i <= tidx);
+    };
+    const int seg = (V + nt - 1) / nt;
+    const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
+    unsigned long long loc = 0ull;
+    for (int i = a0; i < a1; ++i)
+        if (kept(i)) loc += qv[i];
+    unsigned long long ZS;
+    unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &ZS);
+    if (tid == 0) ss.rem = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
+    SAMPLE_SYNC();
+    const unsigned long long target = ss.rem;
+    int cand = 0x7fffffff;
+    for (int i = a0; i < a1; ++i) {
+        if (!kept(i) || qv[i] == 0u) continue;
+        run += qv[i];
+        if (run > target) { cand = i; break; }
+    }
+    int tok = block_min_i(cand, ss.i);
+    if (tok < 0 || tok >= V) {
+        if (tid == 0 && err) atomicExch(err, 2);
+        tok = 0;
+    }
+    SAMPLE_SYNC();
+    return tok;
+}
+
 // As sample_smem, loading the logits lg[0..V) first (through L2: they may
 // have been written by other CTAs of the same kernel).
 static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
@@ -390,14 +607,16 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
         }
     }
     SAMPLE_SYNC();
-    return sample_smem(V, sp, u_ptr, smraw, ss, err);
+    return sample_fast(V, sp, u_ptr, smraw, ss, err);
 }
 
 }  // namespace sample_detail
 
-// shared memory of sample_smem / sample_block for V logits and `threads` threads
+// shared memory of sample_fast / sample_smem / sample_block for V logits and `threads` threads
 inline size_t sample_smem_bytes_dev(int V, int threads) {
-    return 3 * sample_detail::sample_array_bytes(V) + (size_t)(threads / 32) * 256 * sizeof(unsigned);
+    const size_t radix = 3 * sample_detail::sample_array_bytes(V) + (size_t)(threads / 32) * 256 * sizeof(unsigned);
+    const size_t fast = sample_detail::sample_array_bytes(V) + sample_detail::sample_fast_extra_bytes(V);
+    return radix > fast ? radix : fast;
 }
 
 }  // namespace sd

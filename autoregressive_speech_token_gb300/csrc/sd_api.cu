@@ -701,7 +701,8 @@ int setup_tc_prefill(sd_ctx* c) {
 // Which persistent step kernel runs the decode steps of a GPT-2/Llama T3 with
 // Q8_0/Q4_0 weights: 0 none (the per-operation graph), 1 the cluster kernel
 // where its plan fits and the flat one otherwise, 2 the flat kernel only, 3
-// the cluster kernel only.  Default: 1 for one row, 0 for two.
+// the cluster kernel only.  Default: 1 for one row; 3 for two rows (where the
+// flat kernel is slower than the graph, so the graph is the fallback).
 // SD_PERSISTENT = 0 | 1 | flat | cluster overrides.
 int persistent_mode(int rows) {
     const char* e = getenv("SD_PERSISTENT");
@@ -709,7 +710,7 @@ int persistent_mode(int rows) {
     if (e && !strcmp(e, "cluster")) return 3;
     if (e && e[0] == '0') return 0;
     if (e && e[0] == '1') return 1;
-    return rows == 1 ? 1 : 0;
+    return rows == 1 ? 1 : 3;
 }
 
 // Cluster step plan, repacked matrices (cluster-major QKV rows, Wo and the
@@ -933,13 +934,14 @@ void write_ctrace(sd_ctx* c, int n_steps) {
     unsigned long long t[kCTraceSub];
     if (a.trace && cudaMemcpy(t, a.trace, sizeof t, cudaMemcpyDeviceToHost) == cudaSuccess) {
         // CTA 0's cycles per sub-step (per layer, or per step for the last four)
-        const char* nm[28] = {"wait x''", "rec qkv", "norm1", "mma qkv+send", "wait qkv", "attn keys",
+        const char* nm[30] = {"wait x''", "rec qkv", "norm1", "mma qkv+send", "wait qkv", "attn keys",
                               "comb+send", "wait part", "combine", "rec o", "mma o+pub", "reduce o", "wait x'",
                               "rec fc", "norm2", "mma fc+send", "wait u", "rec proj", "mma proj+pub", "reduce proj",
-                              "head*", "sample+end*", "(q prep)", "(kv wait)", "(wp+bar)", "(send+bar)", "start*", "embed*"};
+                              "head*", "end*", "(q prep)", "(kv wait)", "(wp+bar)", "(send+bar)", "start*", "embed*", "gather*",
+                              "sample*"};
         const double nl = (double)n_steps * L;
         fprintf(f, "  CTA 0 cycles per layer (* per step):\n   ");
-        for (int k = 0; k < 28; ++k) {
+        for (int k = 0; k < 30; ++k) {
             if (!nm[k][0]) continue;
             fprintf(f, " %s %.0f |", nm[k], (double)t[k] / ((k >= 20 && k <= 21) || k >= 26 ? (double)n_steps : nl));
             if (k % 7 == 6) fprintf(f, "\n   ");

@@ -278,7 +278,7 @@ struct CStepArgs {
     unsigned long long* trace_cta = nullptr;
 };
 constexpr int kCtaSteps = 4;
-constexpr int kCTraceSub = 32;
+constexpr int kCTraceSub = 32;  // sub-steps 28, 29: the sampler CTA's logits gather and sampling
 constexpr int kCTracePhases = 8;  // x ready, QKV sent, attention sent, O published, x' sent, u sent, proj published, x'' sent
 size_t cstep_smem_bytes(const CStepArgs& a);
 // Chooses ncl / cs and fills the layout fields of `a`; returns the grid size,

@@ -254,9 +254,11 @@ def test_persistent_kernel_is_used(sd, monkeypatch, name, kind):
     dec.close()
 
 
-def test_default_one_row_path_is_the_cluster_step(sd, monkeypatch):
+@pytest.mark.parametrize("name", ["gpt2m_q4", "llama_q4"])
+def test_default_step_path_is_the_cluster_step(sd, monkeypatch, name):
+    """One row (GPT-2-Medium) and two rows (Llama) decode on the cluster step by default."""
     monkeypatch.delenv("SD_PERSISTENT", raising=False)
-    run = get_preset("gpt2m_q4")
+    run = get_preset(name)
     dec = sd.Decoder(run.model, _blob(run.model), stream=_stream())
     assert dec.info().persistent_clusters > 0
     dec.close()
