@@ -107,6 +107,7 @@ def _declare(L):
     L.orc_reset.argtypes = [C.c_void_p]; L.orc_reset.restype = None
     L.orc_set_threads.argtypes = [C.c_int]
     L.orc_pos.argtypes = [C.c_void_p, C.c_int]
+    L.orc_copy_row.argtypes = [C.c_void_p, C.c_int, C.c_int]
     L.orc_token_forward.argtypes = [C.c_void_p, C.c_int, C.c_int32, f32p]
     L.orc_talker_forward.argtypes = [C.c_void_p, C.c_int, f32p, f32p, f32p]
     L.orc_talker_embed.argtypes = [C.c_void_p, C.c_int32, f32p]
@@ -279,6 +280,11 @@ class Model:
     def cp_reset(self, row: int):
         lib().orc_cp_reset(self._h, row)
 
+    def copy_row(self, dst: int, src: int):
+        """Row dst continues from row src's state (same inputs so far)."""
+        if lib().orc_copy_row(self._h, dst, src):
+            raise ValueError("bad row")
+
     def code_embed(self, j: int, code: int, d: int):
         e = np.empty(d, np.float32)
         if lib().orc_code_embed(self._h, j, int(code), _p(e, C.c_float)):
@@ -353,12 +359,23 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
     B = prompt.shape[0]
     d, V0, Vc, ncb = spec.d_model, spec.vocab, spec.cp_vocab, spec.n_codebooks
     ta, ca = _sampler_args(talker_sampler), _sampler_args(cp_sampler)
-    traces = []
+    # every row's prompt first; a row whose prompt equals an earlier row's takes a
+    # copy of that row's state right after its prompt (the rows are independent)
+    prompt_end = []
     for b in range(B):
-        tr = Trace()
+        same = [a for a in range(b) if np.array_equal(prompt[a], prompt[b])]
+        if same:
+            model.copy_row(b, same[0])
+            prompt_end.append(prompt_end[same[0]])
+            continue
         z0 = h = None
         for tok in prompt[b]:
             z0, h = model.talker_forward(b, model.talker_embed(int(tok), d), V0, d)
+        prompt_end.append((z0, h))
+    traces = []
+    for b in range(B):
+        tr = Trace()
+        z0, h = prompt_end[b]
         for f in range(n_frames + 1):
             codes, zs, ms = [], [z0], []
             c0, m0 = sample(z0, u=float(draws[f][b][0]), **ta)

@@ -45,7 +45,9 @@ enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
  *  15 temperature multiplies          16 attention residual dropped
  *  17 SwiGLU gate and up swapped      18 query heads interleaved over KV heads
  *  19 RoPE skipped on keys         20 repetition penalty backwards
- *  21 ladder: top-k before top-p                                            */
+ *  21 ladder: top-k before top-p     22 margin ignores membership flips
+ *  23 margin taken as if T were 1    24 top-p bound counts t before itself
+ *  25 mass factor 1+r instead of its square root                           */
 #ifndef ORC_MUTANT
 #define ORC_MUTANT 0
 #endif
@@ -132,12 +134,15 @@ static void qmat_row(const qmat* W, int64_t r, float* out) {
         const uint8_t* q = W->data + r * W->cols;
         const uint16_t* s = W->scale + r * (W->cols / 64);
         const uint16_t* b = W->bias + r * (W->cols / 64);
-        for (int64_t k = 0; k < W->cols; ++k)
+        for (int64_t g = 0; g < W->cols / 64; ++g) {
+            const float sc = orc_half_to_float(s[g]), bi = orc_half_to_float(b[g]);
+            for (int64_t k = g * 64; k < (g + 1) * 64; ++k)
 #if ORC_MUTANT == 4
-            out[k] = orc_half_to_float(s[k / 64]) * (float)q[k] + 0.0f * orc_half_to_float(b[k / 64]);
+                out[k] = sc * (float)q[k] + 0.0f * bi;
 #else
-            out[k] = fmaf(orc_half_to_float(s[k / 64]), (float)q[k], orc_half_to_float(b[k / 64]));
+                out[k] = fmaf(sc, (float)q[k], bi);
 #endif
+        }
     } else if (W->kind == K_F32) {
         memcpy(out, (const float*)W->data + r * W->cols, (size_t)W->cols * sizeof(float));
     } else {
@@ -303,6 +308,179 @@ static int cmp_desc(const void* a, const void* b) {
     return (x->i > y->i) - (x->i < y->i);           /* ties: lower index first */
 }
 
+/* ------------------------------------------------------------------ decision margin
+ *
+ * The pages define no margin for a sampled decision.  Here it is the size of the
+ * smallest change of the decision's inputs that can change the chosen token,
+ * in one unit r:
+ *   - the draw u moved by r (u is a normalised position on the kept mass);
+ *   - every unnormalised probability multiplied by its own factor within
+ *     [(1+r)^-1/2, (1+r)^1/2], i.e. every scaled logit z/T moved by at most
+ *     log1p(r)/2 (a logit error d at temperature T is r = expm1(2d/T)).
+ * Every selection stage (top-k, top-p, min_p) keeps a prefix of its input in
+ * (scaled logit desc, index asc) order, so after all stages an element's
+ * membership can flip under a change of size r only if it lies between the
+ * prefix that surely stays and the prefix that possibly stays; both are
+ * bounded stage by stage below.  Two facts bound the token's CDF edges:
+ * changing every mass by a factor within [1/a, a] (a^2 = 1+r) moves a
+ * normalised edge by at most r/4; adding or removing mass F moves it by at most
+ * F over the remaining total.  So the token cannot change while
+ *   r < its distance to the CDF edges between kept entries (u moved), and
+ *   r/4 + (1+r)F/(zs - (1+r)F) < its distance to its interval's ends
+ * (F = mass of the entries whose membership can flip, zs = kept mass).  The
+ * margin is the largest such r, found by bisection: the condition is monotone
+ * in r.  It never exceeds the smallest change that flips the token, and it is
+ * the draw's distance itself when no membership flip can move the token's
+ * edges that far. */
+
+enum { SEL_TOPK = 1, SEL_TOPP = 2, SEL_MINP = 3 };
+typedef struct { int kind; int32_t k; double p; } sel_stage;
+
+/* positions t with zz[t] > x, and with zz[t] >= x (zz descending) */
+static int32_t n_above(const double* zz, int32_t V, double x) {
+    int32_t lo = 0, hi = V;
+    while (lo < hi) { int32_t mid = lo + (hi - lo) / 2; if (zz[mid] > x) lo = mid + 1; else hi = mid; }
+    return lo;
+}
+static int32_t n_at_or_above(const double* zz, int32_t V, double x) {
+    int32_t lo = 0, hi = V;
+    while (lo < hi) { int32_t mid = lo + (hi - lo) / 2; if (zz[mid] >= x) lo = mid + 1; else hi = mid; }
+    return lo;
+}
+
+/* Lengths *nq <= *np of the sorted prefixes that surely / possibly survive all
+ * stages under every change of size r.  zz: scaled logits sorted descending
+ * (ties: lower index first); cw[t] = sum of exp(zz[i] - zz[0]) over i < t. */
+static void kept_bounds(const double* zz, const double* cw, int32_t V, const sel_stage* st, int n_st, double r,
+                        int32_t* nq_out, int32_t* np_out) {
+    const double L = log1p(r);            /* largest change of a difference of two scaled logits */
+#if ORC_MUTANT == 25
+    const double a = 1.0 + r;
+#else
+    const double a = sqrt(1.0 + r);       /* largest factor on one mass */
+#endif
+    int32_t np = V, nq = V;                /* before the first stage every entry is present */
+    for (int s = 0; s < n_st; ++s) {
+        int32_t np2 = 0, nq2 = 0;
+        if (st[s].kind == SEL_TOPK) {
+            /* kept iff fewer than k present entries lie strictly above.  t can stay
+             * if fewer than k surely-present entries surely lie above it; t surely
+             * stays if fewer than k possibly-present others can lie above it. */
+            const int32_t k = st[s].k;
+            while (np2 < np) {
+                int32_t above = n_above(zz, V, zz[np2] + L);
+                if (above > nq) above = nq;
+                if (above >= k) break;
+                ++np2;
+            }
+            while (nq2 < nq) {
+                int32_t above = n_at_or_above(zz, V, zz[nq2] - L);
+                if (above > np) above = np;
+                if (above - 1 >= k) break;     /* less t itself */
+                ++nq2;
+            }
+        } else if (st[s].kind == SEL_TOPP) {
+            /* kept iff the mass of the present entries ordered before t, over the
+             * present total, is below p.  Least that share can be: only the
+             * surely-present entries surely above t count before it, shrunk, and
+             * every possibly-present entry not surely above t counts after it,
+             * grown.  Most: every possibly-present entry that can be above t counts
+             * before it, grown, and only t and the surely-present entries surely
+             * below it count after it, shrunk. */
+            const double p = st[s].p;
+            while (np2 < np) {
+                const int32_t t = np2;
+                const int32_t m = n_above(zz, V, zz[t] + L);
+                const int32_t mq = m < nq ? m : nq;
+                const double B = cw[mq] / a, R = (cw[np] - cw[m]) * a;
+                if (B / (B + R) >= p) break;
+                ++np2;
+            }
+            while (nq2 < nq) {
+                const int32_t t = nq2;
+                const int32_t j = n_at_or_above(zz, V, zz[t] - L);
+                const int32_t jp = j < np ? j : np;
+                const double w_t = cw[t + 1] - cw[t];
+#if ORC_MUTANT == 24
+                const double B = cw[jp] * a;
+#else
+                const double B = (cw[jp] - w_t) * a;
+#endif
+                const double R = (w_t + (j < nq ? cw[nq] - cw[j] : 0.0)) / a;
+                if (B / (B + R) >= p) break;
+                ++nq2;
+            }
+        } else {
+            /* min_p, the first stage: kept iff its probability is at least p times
+             * the largest, i.e. zz[t] - zz[0] >= log p; the largest moves too */
+            const double lp = log(st[s].p);
+            while (np2 < np && zz[np2] - zz[0] + L >= lp) ++np2;
+            while (nq2 < nq && zz[nq2] - zz[0] - L >= lp) ++nq2;
+        }
+        np = np2;
+        nq = nq2 < np2 ? nq2 : np2;
+    }
+    *nq_out = nq;
+    *np_out = np;
+}
+
+/* can membership flips under a change of size r move the token's edges by m_edge? */
+static int flips_reach(const double* zz, const double* cw, int32_t V, const sel_stage* st, int n_st, double zs,
+                       double m_edge, double r) {
+    int32_t nq, np;
+    kept_bounds(zz, cw, V, st, n_st, r, &nq, &np);
+    const double F = cw[np] - cw[nq];
+    if (!(F > 0.0)) return 0;
+    const double rest = zs - (1.0 + r) * F;
+    if (rest <= 0.0) return 1;
+    return r / 4.0 + (1.0 + r) * F / rest >= m_edge;
+}
+
+/* The margin of a sampled draw.  s: every entry's scaled logit in (desc, index
+ * asc) order; kept[i]: entry i survived every stage; the draw chose `tok`,
+ * whose interval on the kept mass zs is [c_lo, c) and holds target = u zs. */
+static double draw_margin(const zi* s, int32_t V, const sel_stage* st, int n_st, const char* kept, int32_t tok,
+                          double target, double c_lo, double c, double zs) {
+    int32_t first = -1, last = -1;
+    for (int32_t i = 0; i < V; ++i) if (kept[i]) { if (first < 0) first = i; last = i; }
+    double lo_d = target - c_lo, hi_d = c - target;
+    if (lo_d < 0.0) lo_d = 0.0;
+    if (hi_d < 0.0) hi_d = 0.0;
+    /* distance to the interval's ends, and to the edges shared with another kept
+     * entry (the ends of [0, 1) are not reachable by moving u) */
+    const double m_edge = fmin(lo_d, hi_d) / zs;
+    const double m_move = fmin(tok != first ? lo_d : INFINITY, tok != last ? hi_d : INFINITY) / zs;
+#if ORC_MUTANT == 22
+    (void)st; (void)n_st; (void)s; (void)m_edge; (void)flips_reach;
+    return m_move;
+#else
+    double* zz = (double*)malloc((size_t)V * sizeof(double));
+    double* cw = (double*)malloc((size_t)(V + 1) * sizeof(double));
+    cw[0] = 0.0;
+    for (int32_t t = 0; t < V; ++t) {
+        zz[t] = s[t].z;
+        cw[t + 1] = cw[t] + exp(s[t].z - s[0].z);
+    }
+    double m;
+    double hi = m_move < 1e6 ? m_move : 1e6;
+    if (!flips_reach(zz, cw, V, st, n_st, zs, m_edge, hi)) {
+        m = m_move;
+    } else if (flips_reach(zz, cw, V, st, n_st, zs, m_edge, 0.0)) {
+        m = 0.0;
+    } else {
+        double lo = 0.0;
+        for (int it = 0; it < 200; ++it) {
+            const double mid = 0.5 * (lo + hi);
+            if (flips_reach(zz, cw, V, st, n_st, zs, m_edge, mid)) hi = mid; else lo = mid;
+        }
+        m = lo;
+    }
+    free(zz);
+    free(cw);
+    return m;
+#endif
+}
+
 int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
                    int32_t greedy, double u, double* margin) {
     if (V <= 0) return -1;
@@ -325,7 +503,6 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     /* top-k: keep every value >= the k-th largest (ties at the threshold kept) */
     int32_t k = top_k < 1 || top_k > V ? V : top_k;
     double thr = s[k - 1].z;
-    double gap_k = k < V ? s[k - 1].z - s[k].z : INFINITY;
     int32_t n_keep = 0;
 #if ORC_MUTANT == 12
     (void)thr;
@@ -340,16 +517,11 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
     for (int32_t t = 0; t < n_keep; ++t) p[s[t].i] = exp(s[t].z - zmax);
     for (int32_t t = 0; t < n_keep; ++t) in_s[s[t].i] = 1;
     for (int32_t i = 0; i < V; ++i) if (in_s[i]) Z += p[i];
-    /* the elements whose top-k membership a small perturbation could flip */
-    double pk_flip = 0.0;
-    if (k < V) pk_flip = exp((k < n_keep ? s[k].z : s[k - 1].z) - zmax);
     /* top-p: the shortest (p desc, index asc) prefix whose cumulative mass >= top_p */
-    double gap_p = INFINITY, pp_flip = 0.0;
     if (top_p < 1.0f) {
-        double cum = 0.0, prev = 0.0;
+        double cum = 0.0;
         int32_t cut = n_keep - 1;
         for (int32_t t = 0; t < n_keep; ++t) {
-            prev = cum;
             cum += p[s[t].i] / Z;
 #if ORC_MUTANT == 13
             if (cum >= (double)top_p) { cut = t + 1 < n_keep ? t + 1 : t; break; }
@@ -357,13 +529,6 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
             if (cum >= (double)top_p) { cut = t; break; }
 #endif
         }
-        gap_p = fabs(cum - (double)top_p);
-        if (cut > 0 && fabs((double)top_p - prev) < gap_p) gap_p = fabs((double)top_p - prev);
-        /* the last kept and the first dropped element swap places when their
-         * logits cross: that gap bounds the cut too */
-        if (cut + 1 < n_keep && s[cut].z - s[cut + 1].z < gap_p) gap_p = s[cut].z - s[cut + 1].z;
-        pp_flip = p[s[cut].i];
-        if (cut + 1 < n_keep && p[s[cut + 1].i] > pp_flip) pp_flip = p[s[cut + 1].i];
         for (int32_t t = cut + 1; t < n_keep; ++t) in_s[s[t].i] = 0;
     }
     /* draw in vocabulary order */
@@ -384,16 +549,16 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         if (c > target) { tok = i; break; }
     }
     if (tok < 0) { tok = last; c_lo = c - p[last]; }
-    /* Decision margin: the distance of the draw to the chosen token's CDF edges
-     * (normalised).  A top-k or top-p membership flip of element e moves the
-     * normalised draw position by at most p_e / zs, so a near-tie at those
-     * boundaries only matters when the draw lies within that distance of an edge;
-     * then the boundary gap bounds the margin too. */
-    double m_u = fmin(target - c_lo, c - target) / zs;
-    double m = m_u;
-    if (m_u <= pk_flip / zs && gap_k < m) m = gap_k;
-    if (m_u <= pp_flip / zs && gap_p < m) m = gap_p;
-    if (margin) *margin = m;
+    if (margin) {
+        sel_stage st[2];
+        int n_st = 0;
+        st[n_st].kind = SEL_TOPK; st[n_st].k = k; st[n_st].p = 0.0; ++n_st;
+        if (top_p < 1.0f) { st[n_st].kind = SEL_TOPP; st[n_st].k = 0; st[n_st].p = (double)top_p; ++n_st; }
+#if ORC_MUTANT == 23
+        for (int32_t t = 0; t < V; ++t) s[t].z = (double)z[s[t].i];   /* margin taken as if T were 1 */
+#endif
+        *margin = draw_margin(s, V, st, n_st, in_s, tok, target, c_lo, c, zs);
+    }
     free(s); free(p); free(in_s);
     return tok;
 }
@@ -498,7 +663,19 @@ int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V,
         if (c > target) { tok = i; break; }
     }
     if (tok < 0) { tok = last; c_lo = c - p[last]; }
-    if (margin) *margin = fmin(target - c_lo, c - target) / zs;
+    if (margin) {
+        /* every entry in (desc, index asc) order, and the stages as applied */
+        zi* a = (zi*)malloc((size_t)V * sizeof(zi));
+        for (int32_t i = 0; i < V; ++i) { a[i].z = z[i]; a[i].i = i; }
+        qsort(a, (size_t)V, sizeof(zi), cmp_desc);
+        sel_stage st[3];
+        int n_st = 0;
+        if (min_p > 0.0f) { st[n_st].kind = SEL_MINP; st[n_st].k = 0; st[n_st].p = min_p < 1.0f ? (double)min_p : 1.0; ++n_st; }
+        if (top_p < 1.0f) { st[n_st].kind = SEL_TOPP; st[n_st].k = 0; st[n_st].p = (double)top_p; ++n_st; }
+        st[n_st].kind = SEL_TOPK; st[n_st].k = top_k < 1 ? V : top_k; st[n_st].p = 0.0; ++n_st;
+        *margin = draw_margin(a, V, st, n_st, keep, tok, target, c_lo, c, zs);
+        free(a);
+    }
     free(z); free(p); free(keep); free(s);
     return tok;
 }
@@ -705,6 +882,16 @@ void orc_reset(orc_model* m) {
 }
 
 int orc_pos(const orc_model* m, int row) { return m->s.pos[row]; }
+
+int orc_copy_row(orc_model* m, int dst, int src) {
+    ostack* s = &m->s;
+    if (dst < 0 || src < 0 || dst >= s->batch || src >= s->batch) return -1;
+    const size_t per_row = (size_t)s->n_layer * s->n_kv * s->max_ctx * s->hd;
+    memcpy(s->kc + (size_t)dst * per_row, s->kc + (size_t)src * per_row, per_row * sizeof(uint16_t));
+    memcpy(s->vc + (size_t)dst * per_row, s->vc + (size_t)src * per_row, per_row * sizeof(uint16_t));
+    s->pos[dst] = s->pos[src];
+    return 0;
+}
 
 /* ------------------------------------------------------------------ one transformer position */
 

@@ -45,7 +45,13 @@ void orc_rope(float* x, int hd, int pos, float theta);
 void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int hd, float* out);
 
 /* Sampler: temperature -> top-k -> top-p -> draw in vocabulary order with u.
- * margin (may be NULL) receives the decision margin. */
+ * margin (may be NULL) receives the decision margin.  Greedy (or top_k 1, or
+ * temperature <= 0): the gap between the two largest logits.  A sampled draw:
+ * the largest r such that neither moving u by less than r nor multiplying
+ * every unnormalised probability by factors within [(1+r)^-1/2, (1+r)^1/2]
+ * can change the token (a lower bound of the true value, found by bisection;
+ * it equals the draw's distance to the token's CDF edges when no membership
+ * flip at the top-k / top-p boundaries can move those edges that far). */
 int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
                    int32_t greedy, double u, double* margin);
 
@@ -54,7 +60,8 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
  * vocabulary order with u.  z_uncond may be NULL (no combine); seen may be
  * NULL (no penalty); top_k < 1 or > V keeps every survivor; temperature <= 0
  * returns the argmax of the combined, penalised logits.  margin (may be NULL)
- * receives the draw's distance to the chosen token's CDF edges. */
+ * receives the decision margin as orc_sample defines it, over the combined,
+ * penalised and scaled logits and the min_p, top-p and top-k stages. */
 int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V, float cfg_weight,
                           const uint8_t* seen, float rep_penalty, float temperature, float min_p, float top_p,
                           int32_t top_k, double u, double* margin);
@@ -65,6 +72,9 @@ void orc_close(orc_model* m);
 void orc_reset(orc_model* m);
 int  orc_set_threads(int n);
 int  orc_pos(const orc_model* m, int row);
+/* Row dst takes a copy of row src's (Talker / T3) cache and position: the state
+ * that row src's inputs so far produced, for a row that received the same inputs. */
+int  orc_copy_row(orc_model* m, int dst, int src);
 
 /* GPT-2 / Llama: process token `tok` at row `row`'s next position; logits may be NULL. */
 int orc_token_forward(orc_model* m, int row, int32_t tok, float* logits);

@@ -52,6 +52,16 @@ def config_words(m) -> bytes:
     return raw + b"\0" * (4 * CONFIG_FIELDS - len(raw))
 
 
+def with_batch(blob: np.ndarray, batch: int) -> np.ndarray:
+    """A copy of ``blob`` whose header names ``batch`` rows (the tensors do not
+    depend on the batch)."""
+    magic, _ver, _n, _toff = struct.unpack_from("<4I", blob, 0)
+    assert magic == MAGIC
+    out = np.array(blob, dtype=np.uint8, copy=True)
+    struct.pack_into("<i", out, 16 + 4 * 9, int(batch))
+    return out
+
+
 def _payload(kind: int, data) -> bytes:
     if kind == KIND_A8G64:
         q, s, b = data

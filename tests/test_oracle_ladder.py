@@ -11,6 +11,7 @@ import math
 import numpy as np
 
 import oracle
+from tests import test_oracle_ops as oo
 
 F32 = np.float32
 
@@ -126,3 +127,43 @@ def test_top_p_acts_before_top_k():
     z = np.log(np.array([0.4, 0.3, 0.2, 0.1])).astype(F32)
     assert oracle.sample_ladder(z, temperature=1.0, top_p=0.5, top_k=2, u=0.9)[0] == 1
     _check(z, None, 0, None, 1, 1.0, 0.0, 0.5, 2)
+
+
+def _ladder(T, min_p, top_p, k):
+    return lambda z, u: oracle.sample_ladder(z, temperature=T, min_p=min_p, top_p=top_p, top_k=k, u=u)
+
+
+def test_ladder_margin_bruteforce_changes_below_it_keep_the_token():
+    """The ladder's margin means what the plain sampler's does (over the final
+    scaled logits): moving u, or the scaled logits, by less than it keeps the
+    token, and it never exceeds the draw's distance to its CDF edges."""
+    rng = np.random.default_rng(24)
+    for trial in range(16):
+        z = (rng.standard_normal(16) * rng.choice([1.0, 2.0, 3.0])).astype(F32)
+        if trial % 2:
+            for i in rng.choice(16, size=4, replace=False):
+                z[(i + 1) % 16] = z[i] - F32(rng.choice([1e-3, 1e-2]))
+        T = float(F32(rng.choice([0.7, 1.0, 1.2])))
+        min_p = float(F32(rng.choice([0.0, 0.02, 0.1, 0.3])))
+        top_p = float(F32(rng.choice([1.0, 0.6, 0.9])))
+        k = int(rng.choice([0, 3, 6]))
+        probs = _ladder_probs(z, None, 0.0, None, 1.0, T, min_p, top_p, k)
+        for u in rng.random(3):
+            tok, M = oo._assert_margin_sound(_ladder(T, min_p, top_p, k), z, T, float(u))
+            assert M <= oo._draw_distance(probs, tok, float(u)) * (1 + 1e-12) + 1e-15
+
+
+def test_ladder_margin_at_a_min_p_boundary():
+    # probabilities relative to the largest: 1 (id 4), 0.5 (id 9), 0.1 e^0.01 (id 2),
+    # the rest below 0.1 / e: min_p = 0.1 keeps three, and id 2 drops once a change
+    # of expm1(0.01) lets its ratio to the largest fall under min_p
+    z = np.full(16, -4.0, F32) - 0.05 * np.arange(16, dtype=F32)
+    z[4], z[9], z[2] = 0.0, math.log(0.5), math.log(0.1) + 0.01
+    u = 0.03                                            # inside id 2's interval (first in vocabulary order)
+    tok, M = oo._assert_margin_sound(_ladder(1.0, 0.1, 1.0, 0), z, 1.0, u)
+    assert tok == 2
+    delta = float(z[2]) - float(z[4]) - math.log(float(F32(0.1)))
+    assert abs(M - math.expm1(delta)) <= 1e-9 * M, (M, math.expm1(delta))
+    d = np.ones(16)
+    d[2] = -1.0
+    assert oo._flip_within(_ladder(1.0, 0.1, 1.0, 0), z, 1.0, u, tok, M, d)

@@ -101,6 +101,31 @@ def test_qwen_frames_match_full_recompute():
             assert _rel(tr.logits[f][j], ref[f][j]) < TOL, (f, j)
 
 
+def test_qwen_rows_sharing_a_prompt_match_full_recompute():
+    """Rows whose prompt equals an earlier row's start from a copy of that row's
+    cache (run_qwen's shortcut for G rollouts of one prompt); every row's frames
+    still match an independent full recompute of its own tokens."""
+    import dataclasses
+    m = dataclasses.replace(_small_qwen(), batch=3)
+    blob, _ = build_model_blob(m)
+    model = oracle.Model(blob)
+    rng = np.random.default_rng(7)
+    prompt = rng.integers(0, m.vocab, size=(3, 7)).astype(np.int32)
+    prompt[2] = prompt[0]
+    nf = 2
+    draws = uniform_draws(5, nf + 1, 3, 16)
+    s = SamplerSpec(temperature=0.9, top_k=50, top_p=0.95, greedy=False)
+    trs = oracle.run_qwen(model, m, prompt, draws, nf, s, s)
+    for b in range(3):
+        ref = torch_ref.qwen_frame_logits(blob, m, prompt[b], trs[b].tokens)
+        for f in range(nf + 1):
+            for j in range(16):
+                # 5 x TOL: over three frames an fp16 cache rounding may tip between the two
+                # computations; a wrong or missing copy errs by the logits' own size
+                assert _rel(trs[b].logits[f][j], ref[f][j]) < 5 * TOL, (b, f, j)
+    assert np.array_equal(trs[0].logits[0][0], trs[2].logits[0][0])
+
+
 def test_zero_layer_model_is_head_of_norm_of_embedding():
     m = P.ModelSpec(arch=P.ARCH_GPT2, n_layer=0, d_model=128, n_head=2, n_kv_head=2, head_dim=64,
                     d_ff=256, vocab=200, max_ctx=16, batch=1, quant=P.Q8_0)

@@ -39,6 +39,13 @@ MUTANTS = {
     19: ("RoPE skipped on keys", [om.test_llama_gqa_rows_match_full_recompute]),
     20: ("repetition penalty backwards", [ol.test_repetition_penalty_divides_positive_and_multiplies_negative_logits]),
     21: ("ladder: top-k before top-p", [ol.test_top_p_acts_before_top_k]),
+    22: ("margin ignores membership flips", [oo.test_sampler_margin_at_a_top_k_boundary,
+                                             oo.test_sampler_margin_bruteforce_changes_below_it_keep_the_token]),
+    23: ("margin taken as if T were 1", [oo.test_sampler_margin_at_a_top_k_boundary]),
+    24: ("top-p bound counts an entry before itself", [oo.test_sampler_margin_is_the_draw_distance_when_no_flip_reaches,
+                                                       oo.test_sampler_margin_at_a_top_p_cut_that_can_shrink]),
+    25: ("mass factor 1+r instead of its square root", [oo.test_sampler_margin_at_a_top_p_cut_that_can_shrink,
+                                                         oo.test_sampler_margin_at_a_top_p_cut_that_can_grow]),
 }
 
 
@@ -59,6 +66,6 @@ def test_planted_mistake_is_rejected(n):
 def test_unmutated_build_passes_the_same_pins():
     """The pins used above pass on the oracle itself (so a failure above is the
     planted mistake, not a pin that always fails)."""
-    for n in (2, 6, 10, 12, 13):
+    for n in (2, 6, 10, 12, 13, 22, 24, 25):
         for pin in MUTANTS[n][1]:
             pin()

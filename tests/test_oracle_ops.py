@@ -14,6 +14,7 @@ import oracle
 from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64
 
 KQ8, KQ4, KA8 = 1, 2, 3
+F32 = np.float32
 
 
 # ----------------------------------------------------------------------------- fp16
@@ -343,3 +344,197 @@ def test_sampler_margin_greedy():
     z = np.array([0.0, 1.5, 1.25, -2.0], np.float32)
     tok, m = oracle.sample(z, 1.0, 1, 1.0, True, 0.0)
     assert tok == 1 and m == 0.25
+
+
+# ----------------------------------------------------------------------------- sampled decision margin
+#
+# The margin of a sampled draw is read as the smallest change that can change
+# the token, in one unit r: u moved by r, or every unnormalised probability
+# multiplied by its own factor within [(1+r)^-1/2, (1+r)^1/2] (every scaled
+# logit moved by at most log1p(r)/2).  The pins below check it against brute
+# force on 16-entry vocabularies: changes below the margin never change the
+# token; where a CDF edge is nearest the margin is the enumerated distance to
+# it; where a top-k or top-p membership flip is nearest, it is the size at which
+# the flip first becomes possible, and a change just above it does flip the token.
+
+def _draw_distance(probs, tok, u):
+    """Distance of u to the token's interval edges on the enumerated CDF (vocabulary
+    order), counting only edges shared with another kept entry."""
+    kept = np.nonzero(probs > 0)[0]
+    cdf = np.concatenate([[0.0], np.cumsum(probs)])
+    lo, hi = cdf[tok], cdf[tok + 1]
+    return min(u - lo if tok != kept[0] else math.inf, hi - u if tok != kept[-1] else math.inf)
+
+
+def _directions(z, T):
+    """Sign patterns of a change of the scaled logits: prefix/suffix splits of the
+    (scaled logit desc, index asc) order and of the vocabulary order, one entry
+    against all others, every ordered pair, and random signs."""
+    V = len(z)
+    order = sorted(range(V), key=lambda i: (-float(z[i]) / T, i))
+    dirs = []
+    for j in range(1, V):
+        top = -np.ones(V)
+        top[order[:j]] = 1.0
+        voc = np.where(np.arange(V) < j, 1.0, -1.0)
+        dirs += [top, -top, voc, -voc]
+    for a in range(V):
+        e = -np.ones(V)
+        e[a] = 1.0
+        dirs += [e, -e]
+        for b in range(V):
+            if a != b:
+                d = np.zeros(V)
+                d[a], d[b] = 1.0, -1.0
+                dirs.append(d)
+    dirs += list(np.random.default_rng(V).choice([-1.0, 1.0], size=(24, V)))
+    return dirs
+
+
+def _changed(z, T, d, r):
+    """Logits after moving every scaled logit by d * log1p(r) / 2 (rounded to fp32),
+    and the size of the change that the rounding actually made."""
+    z64 = np.asarray(z, np.float64)
+    zp = (z64 + T * d * math.log1p(r) / 2).astype(np.float32)
+    dev = float(np.max(np.abs(zp.astype(np.float64) - z64))) / T
+    return zp, math.expm1(2 * dev)
+
+
+def _assert_margin_sound(draw, z, T, u, frac=0.999):
+    """draw(z, u) -> (token, margin).  Moving u, or the scaled logits in any of the
+    directions above, by less than the margin keeps the token."""
+    tok, M = draw(z, u)
+    assert M >= 0.0
+    if math.isinf(M):
+        for uu in np.linspace(0.0, 0.999, 41):
+            assert draw(z, float(uu))[0] == tok
+        return tok, M
+    for f in (0.25, 0.5, 0.9, frac):
+        for uu in (u - f * M, u + f * M):
+            if 0.0 <= uu < 1.0:
+                assert draw(z, uu)[0] == tok, ("u moved", u, uu, M)
+    if M > 0.0:
+        for d in _directions(z, T):
+            zp, r = _changed(z, T, d, frac * M)
+            if r < M:
+                assert draw(zp, u)[0] == tok, ("logits moved", z, T, u, M, r, d)
+    return tok, M
+
+
+def _plain(T, k, p):
+    return lambda z, u: oracle.sample(z, T, k, p, False, u)
+
+
+def test_sampler_margin_bruteforce_changes_below_it_keep_the_token():
+    rng = np.random.default_rng(21)
+    n_bound = 0
+    for trial in range(40):
+        z = (rng.standard_normal(16) * rng.choice([0.5, 1.0, 2.0, 4.0])).astype(np.float32)
+        if trial % 2:   # near-ties: pairs a small gap apart make boundary flips cheap
+            for i in rng.choice(16, size=4, replace=False):
+                z[(i + 1) % 16] = z[i] - F32(rng.choice([1e-3, 1e-2, 5e-2]))
+        T = float(F32(rng.choice([0.5, 0.8, 1.3])))      # the values the oracle sees (fp32)
+        k = int(rng.choice([2, 3, 5, 8, 16]))
+        p = float(F32(rng.choice([1.0, 0.5, 0.7, 0.9, 0.95])))
+        for u in rng.random(4):
+            tok, M = _assert_margin_sound(_plain(T, k, p), z, T, float(u))
+            probs = _enumerated_probs(z, T, k, p)
+            dist = _draw_distance(probs, tok, float(u))
+            assert M <= dist * (1 + 1e-12) + 1e-15           # never beyond the draw's own edges
+            n_bound += M < dist * (1 - 1e-9)
+    assert n_bound > 0     # some cases were decided by a membership flip, not the draw
+
+
+
+def test_sampler_margin_is_the_draw_distance_when_no_flip_reaches():
+    rng = np.random.default_rng(23)
+    # no selection at all: only the draw decides
+    for _ in range(6):
+        z = (rng.standard_normal(16) * 1.5).astype(np.float32)
+        T = float(F32(rng.choice([0.6, 1.0, 1.7])))
+        probs = _enumerated_probs(z, T, 16, 1.0)
+        for u in np.linspace(0.0, 0.999, 97):
+            tok, M = oracle.sample(z, T, 16, 1.0, False, float(u))
+            d = _draw_distance(probs, tok, float(u))
+            assert (math.isinf(M) and math.isinf(d)) or abs(M - d) <= 1e-12, (u, tok, M, d)
+    # a top-k boundary 4 apart and a top-p cut far from top_p: no flip within reach
+    w = np.array([0.03, 0.0002, 0.0003, 0.3, 0.0004, 0.0005, 0.0006, 0.5, 0.0007, 0.0008, 0.0009, 0.15,
+                  0.001, 0.0011, 0.0012, 0.0013])
+    z = np.log(w).astype(np.float32)
+    for k, p in [(16, float(F32(0.9))), (4, 1.0), (3, float(F32(0.9)))]:
+        probs = _enumerated_probs(z, 1.0, k, p)
+        for u in np.linspace(0.0, 0.999, 61):
+            tok, M = oracle.sample(z, 1.0, k, p, False, float(u))
+            d = _draw_distance(probs, tok, float(u))
+            assert (math.isinf(M) and math.isinf(d)) or abs(M - d) <= 1e-12, (k, p, u, tok, M, d)
+
+
+def _flip_within(draw, z, T, u, tok, M, d):
+    """A change of 1.01 x the margin in direction d changes the token."""
+    zp, r = _changed(z, T, d, 1.01 * M)
+    assert r < 1.02 * M
+    return draw(zp, u)[0] != tok
+
+
+def test_sampler_margin_at_a_top_k_boundary():
+    # scaled logits 2, 1.5, 1.0 | 0.98, rest <= -4 at T = 0.5: k = 3 keeps the first
+    # three; the third and fourth are 0.02 apart, so they swap once a change of
+    # expm1(0.02) is allowed; the draw sits inside the third's interval, which
+    # then leaves the kept set
+    z = np.array([-2.0 - 0.1 * i for i in range(16)], np.float32)
+    z[5], z[9], z[2], z[12] = 1.0, 0.75, 0.5, 0.49
+    T, k, p, u = 0.5, 3, 1.0, 0.09
+    tok, M = _assert_margin_sound(_plain(T, k, p), z, T, u)
+    assert tok == 2
+    gap = (float(z[2]) - float(z[12])) / T
+    assert abs(M - math.expm1(gap)) <= 1e-12 * M, (M, math.expm1(gap))
+    d = np.zeros(16)
+    d[2], d[12] = -1.0, 1.0
+    assert _flip_within(_plain(T, k, p), z, T, u, tok, M, d)
+
+
+def _cut_case():
+    # probabilities 0.5 (id 7), 0.3 (id 3), 0.15 (id 11), 0.03 (id 0), 12 small ones
+    w = np.zeros(16)
+    w[7], w[3], w[11], w[0] = 0.5, 0.3, 0.15, 0.03
+    small = [i for i in range(16) if w[i] == 0]
+    w[small] = 0.02 * np.arange(1, 13) / 78.0
+    z = np.log(w).astype(np.float32)
+    q = np.exp(z.astype(np.float64) - float(np.max(z)))
+    return z, q / q.sum()
+
+
+def test_sampler_margin_at_a_top_p_cut_that_can_shrink():
+    # top_p just above the mass of the first two: the third (id 11) is kept, and
+    # a change that grows the first two against the rest by a factor 1 + r drops
+    # it once prev (1+r) / (prev (1+r) + 1 - prev) reaches top_p
+    z, q = _cut_case()
+    top_p = 0.801
+    tp = float(F32(top_p))
+    prev = q[7] + q[3]
+    r_prev = (tp - prev) / (prev * (1 - tp))
+    u = 0.92                                       # inside id 11's interval
+    tok, M = _assert_margin_sound(_plain(1.0, 16, top_p), z, 1.0, u)
+    assert tok == 11
+    assert abs(M - r_prev) <= 1e-9 * r_prev, (M, r_prev)
+    d = -np.ones(16)
+    d[[7, 3]] = 1.0
+    assert _flip_within(_plain(1.0, 16, top_p), z, 1.0, u, tok, M, d)
+
+
+def test_sampler_margin_at_a_top_p_cut_that_can_grow():
+    # top_p just below the mass of the first three: the fourth (id 0, first in
+    # vocabulary order) joins once cum / (cum + (1+r)(1 - cum)) falls below top_p,
+    # which moves every edge of the kept CDF up past a draw close above one
+    z, q = _cut_case()
+    cum = q[7] + q[3] + q[11]
+    top_p = float(F32(cum - 2e-4))
+    r_cum = (cum - top_p) / (top_p * (1 - cum))
+    kept = q[3] + q[7] + q[11]
+    u = q[3] / kept + 0.01                         # 0.01 above the edge between id 3 and id 7
+    tok, M = _assert_margin_sound(_plain(1.0, 16, top_p), z, 1.0, u)
+    assert tok == 7
+    assert abs(M - r_cum) <= 1e-9 * r_cum, (M, r_cum)
+    d = np.ones(16)
+    d[[7, 3, 11]] = -1.0
+    assert _flip_within(_plain(1.0, 16, top_p), z, 1.0, u, tok, M, d)

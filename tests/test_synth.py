@@ -129,3 +129,14 @@ def test_affine_blob_kind():
     assert t["t0.wqkv"][0] == KIND_A8G64
     kind, rows, cols, off, nb = t["cp.proj"]
     assert nb == rows * cols + 2 * 2 * rows * cols // 64
+
+
+def test_with_batch_equals_a_blob_built_for_that_batch():
+    import dataclasses
+    from synth import get_preset
+    from synth.blob import with_batch
+    from synth.weights import build_model_blob
+    run = get_preset("tiny")
+    a = build_model_blob(run.model)[0]
+    b = build_model_blob(dataclasses.replace(run.model, batch=3))[0]
+    assert np.array_equal(with_batch(a, 3), b)
