@@ -97,6 +97,9 @@ int sd_attend_rows_static(const float* q_dev, const uint16_t* k_dev, const uint1
     e = cudaMemsetAsync(counters, 0, sizeof(int) * (size_t)B * Hkv, st);
     if (e == cudaSuccess) e = sd::launch_attention(a, B, st);
     if (e != cudaSuccess) return err(SD_ERR_CUDA, "launch", e);
+    // Stream-ordered: no synchronisation here (sd_attend_rows synchronises).  The
+    // kernel may still be running; its errors surface at the caller's next
+    // synchronisation of `stream`.
     return SD_OK;
 }
 

@@ -1076,7 +1076,9 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                 // ---- exchange 1: rows [xr0, xr0 + nx) of every cluster's partial, summed in cluster order
                 const float* bias =
                     sl.has_bias ? reinterpret_cast<const float*>(rec + sl.o_bias) + (sl.br0 - sl.b_lo) : nullptr;
-                reduce_bcast<NB>(a.ll_po, a.ncl, d, xr0, nx, e, bias, xs, PD, a_x, mb_x0, cs, a.err, budget);
+                const bool stall = a.test_budget > 0 && s == 0 && l == 0 && gi == 0;  // test hook
+                reduce_bcast<NB>(a.ll_po, a.ncl, d, xr0, nx, stall ? e + 0x40000000u : e, bias, xs, PD, a_x, mb_x0,
+                                 cs, a.err, stall ? a.test_budget : budget);
                 rec_done();
                 tr_pub(s, l, 4);
                 stamp(11);

@@ -830,7 +830,9 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                         tc = t;
                     }
                 };
-                bool okr = ll_read(a.ll_xa + rep * rs_x, NB, d, d, e, act, a.err, budget, true);
+                const bool stall = a.test_budget > 0 && s == 0 && l == 0 && cta == 0;  // test hook
+                bool okr = ll_read(a.ll_xa + rep * rs_x, NB, d, d, stall ? e + 0x40000000u : e, act, a.err,
+                                   stall ? a.test_budget : budget, true);
                 okr = okr && rec_ready();
                 if (!(ok = csync_and(okr) != 0)) break;
                 tr_waited();

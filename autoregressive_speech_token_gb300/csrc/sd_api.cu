@@ -136,6 +136,7 @@ struct sd_ctx {
     int step_grid = 0;
     // cluster persistent step kernel (k_cstep.cu): preferred over the flat one where its plan fits
     bool cpersistent = false;
+    long long test_stall = 0;           // test hook (SD_TEST_STALL_US): cycles for one wait of the next persistent launch
     CStepArgs cstep;
 };
 
@@ -395,6 +396,8 @@ int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
 int enqueue_cstep(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
     CStepArgs a = c->cstep;
     a.n_steps = n_steps;
+    a.test_budget = c->test_stall;
+    c->test_stall = 0;
     a.u_seq = u_seq;
     a.out_seq = out_seq;
     if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * kCTraceSub, st));
@@ -414,6 +417,8 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     if (c->cpersistent) return enqueue_cstep(c, n_steps, u_seq, out_seq, st);
     StepArgs a = c->step;
     a.n_steps = n_steps;
+    a.test_budget = c->test_stall;
+    c->test_stall = 0;
     a.u_seq = u_seq;
     a.out_seq = out_seq;
     if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 64, st));
@@ -811,6 +816,9 @@ int setup_cstep(sd_ctx* c) {
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
+    // test hook: the first persistent launch lets one exchange-word wait run out after this many us
+    if (const char* ts = getenv("SD_TEST_STALL_US"))
+        c->test_stall = (long long)(clock_khz > 0 ? clock_khz : 2000000) * std::max(1, atoi(ts)) / 1000;
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
         if ((rc = dalloc(c, &a.trace_pub, sizeof(unsigned long long) * 2 * kTraceSteps * a.n_layer * kCTracePhases)) ||
@@ -871,6 +879,9 @@ int setup_persistent(sd_ctx* c) {
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
+    // test hook: the first persistent launch lets one exchange-word wait run out after this many us
+    if (const char* ts = getenv("SD_TEST_STALL_US"))
+        c->test_stall = (long long)(clock_khz > 0 ? clock_khz : 2000000) * std::max(1, atoi(ts)) / 1000;
     if (const char* tp = getenv("SD_TRACE")) {
         c->trace_path = tp;
         if ((rc = dalloc(c, &a.trace, sizeof(unsigned long long) * 64))) return rc;
@@ -1043,11 +1054,21 @@ int download_counters(sd_ctx* c, bool codes) {
     return check_device_err(c);
 }
 
+// SD_OK, or the error code of an sd_sampler the decode sampler does not take
+int sampler_check(const sd_sampler* s) {
+    if (!(s->temperature >= 0.f) || s->top_k < 1 || !(s->top_p > 0.f && s->top_p <= 1.f)) return SD_ERR_INVALID_ARG;
+    if (!(s->rep_penalty >= 0.f)) return SD_ERR_INVALID_ARG;
+    if (s->rep_penalty != 0.f && s->rep_penalty != 1.f) return SD_ERR_UNSUPPORTED;
+    return SD_OK;
+}
+
 int set_sampler(sd_ctx* c, int which, const sd_sampler* s) {
     if (!s) return fail(c, SD_ERR_INVALID_ARG, "sampler is NULL");
-    if (!(s->temperature >= 0.f) || s->top_k < 1 || !(s->top_p > 0.f && s->top_p <= 1.f))
-        return fail(c, SD_ERR_INVALID_ARG, "sampler out of range (T=%g k=%d p=%g)", s->temperature, s->top_k,
-                    s->top_p);
+    if (const int rc = sampler_check(s))
+        return fail(c, rc, "sampler %s (T=%g k=%d p=%g penalty=%g)",
+                    rc == SD_ERR_UNSUPPORTED ? "asks for a repetition penalty, which the decode step does not apply"
+                                             : "out of range",
+                    s->temperature, s->top_k, s->top_p, s->rep_penalty);
     c->hs->samp[which].temperature = s->temperature;
     c->hs->samp[which].top_k = s->top_k;
     c->hs->samp[which].top_p = s->top_p;
@@ -1611,8 +1632,7 @@ int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sa
     sd_ctx* c = nullptr;
     if (!logits_dev || !s || !u_dev || !out_dev || rows < 1 || rows > 65535 || V < 1 || V > 16384)
         return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows: bad argument");
-    if (!(s->temperature >= 0.f) || s->top_k < 1 || !(s->top_p > 0.f && s->top_p <= 1.f))
-        return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows: sampler out of range");
+    if (const int rc = sampler_check(s)) return fail(c, rc, "sd_sample_rows: sampler out of range or unsupported");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     SampParams* sp = nullptr;
     int* err = nullptr;

@@ -214,6 +214,9 @@ struct StepArgs {
     int* err = nullptr;
     int n_steps = 1;
     long long spin_budget = 0;           // clock64 cycles per wait
+    // test hook (0: off): in the launch's first step, CTA 0's first-layer wait for the O
+    // projection's output words looks for an epoch no producer writes, for this many cycles
+    long long test_budget = 0;
     int ring_bytes = 0;                  // shared-memory weight ring
     int act_bytes = 0;                   // shared-memory activation / attention / sampler region
     int max_split = 1;                   // attention splits per (row, kv head) at most
@@ -266,6 +269,9 @@ struct CStepArgs {
     int* err = nullptr;
     int n_steps = 1;
     long long spin_budget = 0;
+    // test hook (0: off): in the launch's first step, cluster 0 rank 0's first-layer wait for
+    // the O-projection partials looks for an epoch no producer writes, for this many cycles
+    long long test_budget = 0;
     int ring_bytes = 0, act_bytes = 0;
     int kkc = 128;                       // cached keys staged per (row, KV head) item at once
     // byte offsets in the activation region

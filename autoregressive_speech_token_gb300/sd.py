@@ -50,11 +50,13 @@ class ModelConfig(C.Structure):
 
 
 class Sampler(C.Structure):
-    _fields_ = [("temperature", C.c_float), ("top_k", C.c_int32), ("top_p", C.c_float), ("greedy", C.c_int32)]
+    """sd_sampler; rep_penalty 0 (the default) or 1 applies no penalty."""
+    _fields_ = [("temperature", C.c_float), ("top_k", C.c_int32), ("top_p", C.c_float), ("greedy", C.c_int32),
+                ("rep_penalty", C.c_float)]
 
     @classmethod
     def from_spec(cls, s) -> "Sampler":
-        return cls(float(s.temperature), int(s.top_k), float(s.top_p), int(bool(s.greedy)))
+        return cls(float(s.temperature), int(s.top_k), float(s.top_p), int(bool(s.greedy)), 1.0)
 
 
 class SamplerLadder(C.Structure):

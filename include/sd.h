@@ -75,29 +75,43 @@ typedef struct sd_model_config {
  * in (probability desc, index asc) order, whose mass reaches top_p; draw the
  * smallest vocabulary index whose cumulative kept mass (index order) exceeds
  * u times the kept total.  Valid: temperature >= 0, top_k >= 1,
- * 0 < top_p <= 1. */
+ * 0 < top_p <= 1.  rep_penalty is the repetition penalty of the multilingual
+ * sampling path (journal section 3.19, "Sampling path"): 1, or 0 (read as 1),
+ * applies none; the decode step does not implement the penalty, so any other
+ * positive value returns SD_ERR_UNSUPPORTED and a negative or NaN value
+ * SD_ERR_INVALID_ARG (the whole ladder runs standalone in
+ * sd_sample_rows_ladder, sd_ops.h). */
 typedef struct sd_sampler {
     float temperature;
     int32_t top_k;
     float top_p;
     int32_t greedy;
+    float rep_penalty;
 } sd_sampler;
 
 typedef struct sd_ctx sd_ctx;
 
-/* Create a context on CUDA device `device`.  `stream` is a cudaStream_t or
- * NULL.  Allocates the KV cache ([row][layer][kv_head][pos][dim] fp16),
- * activations and pinned staging; weights come later. */
+/* Create a context on CUDA device `device` (journal section 3.2: the prompt
+ * graph and the step graph share one KV cache, allocated here; section 3.13:
+ * laid out [row][layer][kv_head][pos][dim] fp16, the order the attention reads).
+ * `stream` is a cudaStream_t or NULL.  Allocates the cache, activations and
+ * pinned staging; weights come later.  Errors: SD_ERR_INVALID_ARG (bad
+ * config), SD_ERR_UNSUPPORTED (a shape the kernels do not take), SD_ERR_OOM,
+ * SD_ERR_CUDA; *out is NULL then. */
 int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out);
 
 /* Load the weight blob (the flat format written by the seeded generator:
- * header + config echo + tensor table + canonical tensors).  `blob` is host
- * memory, or device memory when blob_on_device != 0.  The tensors are
- * repacked into the library's device layout; the blob may be freed after the
- * call.  The config echo must equal the context's config. */
+ * header + config echo + tensor table + canonical tensors; the block formats
+ * of journal Tier A item A3 and section 3.23, and the blog's section 3 for
+ * affine groups).  `blob` is host memory, or device memory when
+ * blob_on_device != 0.  The tensors are repacked into the library's device
+ * layout; the blob may be freed after the call.  The config echo must equal
+ * the context's config (else SD_ERR_BLOB). */
 int sd_load_weights(sd_ctx* ctx, const void* blob, size_t nbytes, int blob_on_device);
 
-/* Process a prompt of n tokens per row (tokens [batch][n], host) at positions
+/* The prompt graph (journal section 3.2; "Every Frame Is a Memory Read",
+ * section 1 for the Talker's prompt frame).
+ * Process a prompt of n tokens per row (tokens [batch][n], host) at positions
  * 0..n-1 and sample the first generated token of each row with draw u[row].
  * GPT-2/Llama: out_tok[batch].  Qwen Talker+CP: u and out_tok are
  * [batch][16]: the codes of frame 0 (code 0 from the Talker's last prompt
@@ -106,44 +120,56 @@ int sd_load_weights(sd_ctx* ctx, const void* blob, size_t nbytes, int blob_on_de
 int sd_prefill(sd_ctx* ctx, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
                int32_t* out_tok);
 
-/* One decode step (GPT-2/Llama): consume tok[row] at the current position,
- * sample the next token with draw u[row] into out_tok[row], advance. */
+/* One decode step (GPT-2/Llama; the step graph of journal section 3.2, two
+ * rows in one step per section 3.21): consume tok[row] at the current
+ * position, sample the next token with draw u[row] into out_tok[row],
+ * advance.  Errors: SD_ERR_STATE before sd_prefill, SD_ERR_CTX_FULL at
+ * max_ctx, SD_ERR_TIMEOUT / SD_ERR_DEVICE from the kernels (sd_reset
+ * recovers). */
 int sd_step(sd_ctx* ctx, const int32_t* tok, const sd_sampler* sampler, const float* u, int32_t* out_tok);
 
-/* One frame (Qwen Talker+CP): the Talker consumes the sum of the 16 code
+/* One frame (Qwen Talker+CP; "Every Frame Is a Memory Read", section 1 and
+ * section 5.2, the code-predictor frame): the Talker consumes the sum of the 16 code
  * embeddings of codes_in[row][0..15] (the previous frame), samples code 0 with
  * `talker`; the code predictor then samples codes 1..15 with `cp`.  Draws
  * u[row][j] feed code j.  Output codes_out[row][16]. */
 int sd_frame(sd_ctx* ctx, const int32_t* codes_in, const sd_sampler* talker, const sd_sampler* cp,
              const float* u, int32_t* codes_out);
 
-/* Teacher forcing for the next sd_prefill/sd_frame of a Qwen context: within
+/* Teacher forcing (a test aid for the parity of "Every Frame Is a Memory
+ * Read", section 1's frame) for the next sd_prefill/sd_frame of a Qwen context: within
  * the frame the code fed to the next code-predictor pass is codes[row][j]
  * instead of the sampled one (the sampled codes are still returned).  NULL
  * clears it.  Applies to one call only. */
 int sd_set_forced_codes(sd_ctx* ctx, const int32_t* codes);
 
-/* n_steps decode steps with device-side token feedback (GPT-2/Llama): step i
+/* n_steps decode steps with device-side token feedback (GPT-2/Llama; "Every
+ * Frame Is a Memory Read", section 3: no host round trip in the loop): step i
  * samples with u_dev[i][row] and writes out_dev[i][row]; its input is the
  * previous step's token (the last sd_prefill/sd_step output for i = 0).  No
  * host round trip between steps. */
 int sd_decode_n(sd_ctx* ctx, int32_t n_steps, const sd_sampler* sampler, const float* u_dev, int32_t* out_dev);
 
-/* Copy the last step's logits to host: [batch][vocab] (GPT-2/Llama) or
+/* The head's output of journal section 3.2's step graph, for parity checks.
+ * Copy the last step's logits to host: [batch][vocab] (GPT-2/Llama) or
  * [batch][16][max(vocab, cp_vocab)] (Qwen, pass j in slot j).  n_floats must
  * be at least that size. */
 int sd_get_logits(sd_ctx* ctx, float* host_out, size_t n_floats);
 
-/* Back to position 0; weights are kept, cache contents become undefined. */
+/* Back to position 0 (journal section 3.2: a new utterance reuses the graphs
+ * and the cache); weights are kept, cache contents become undefined.  Clears
+ * a recorded kernel error. */
 int sd_reset(sd_ctx* ctx);
 
+/* Free the context and everything it allocated (NULL is ignored). */
 void sd_destroy(sd_ctx* ctx);
 
 /* Last error message of the context (never NULL); with ctx == NULL the last
  * error of a failed sd_create or of an op-level call on this thread. */
 const char* sd_last_error(const sd_ctx* ctx);
 
-/* Introspection for benchmarks and tests. */
+/* Introspection for benchmarks and tests ("Every Frame Is a Memory Read",
+ * section 3: bytes per step against the bandwidth). */
 typedef struct sd_info {
     int32_t pos;               /* current position (Talker position for Qwen) */
     int32_t sm_count;          /* streaming multiprocessors of the device */

@@ -136,19 +136,27 @@ int sd_attend_rows(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_
  * latency budget (cudaMalloc can synchronise the whole device) or a host
  * framework that owns all device memory through its own pool.  This entry has
  * no counterpart in the pages; it exists for those callers.  Arguments,
- * layouts and results are those of sd_attend_rows.
+ * layouts and the values written to out_dev are those of sd_attend_rows.
  *
- * Instead of allocating, the split-KV partial results go to one fixed array of
- * 1048576 floats (4 MiB) that every device loading the library keeps until the
- * process exits.  A call needs B * H * nsplit * (hd + 4) floats of it; larger
- * requests return SD_ERR_INVALID_ARG.  The call allocates nothing: no
- * cudaMalloc, cudaFree or allocating library routine.  The first call on each
- * device (with that device current) looks up the array's device address; make
- * that first call before any stream capture.  All calls share the one array:
- * calls that overlap on the GPU (different streams, or different threads on
- * the same device) race on it and must be serialised by the caller.  Every
- * record of the array that a call reads is written earlier in the same call,
- * so nothing needs clearing between calls. */
+ * Unlike sd_attend_rows, the call is stream-ordered: it queues a counter clear
+ * (cudaMemsetAsync) and the attention kernel on `stream` and returns without
+ * waiting.  out_dev is ready, and the inputs may be released, only after the
+ * caller synchronises the stream (or orders later work after it); an error
+ * raised by the kernel appears at that synchronisation, not in this call's
+ * return value, which reports only argument and launch errors.
+ *
+ * Instead of allocating, the split-KV partial results and one counter per
+ * (row, kv head) go to one fixed array of 1048576 floats (4 MiB) that every
+ * device loading the library keeps until the process exits.  A call needs
+ * B * H * nsplit * (hd + 4) + B * Hkv floats of it; a larger request returns
+ * SD_ERR_INVALID_ARG.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.  The first call on each device (with that device
+ * current) looks up the array's device address; make that first call before
+ * any stream capture.  All calls share the one array: calls that overlap on
+ * the GPU (different streams, or different threads on the same device) race on
+ * it and must be serialised by the caller.  Every partial record a call reads
+ * is written earlier in the same call; the counters, which must start at zero,
+ * are cleared by the call itself on `stream` before the kernel runs. */
 int sd_attend_rows_static(const float* q_dev, const uint16_t* k_dev, const uint16_t* v_dev, int32_t B, int32_t H,
                           int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n, int32_t nsplit, float* out_dev,
                           void* stream);

@@ -354,6 +354,12 @@ def test_errors_and_context_limit(sd):
     with pytest.raises(sd.SdError) as e:
         dec.prefill(np.array([[1, 2]], np.int32), sd.Sampler(0.5, 0, 0.9, 0), u)
     assert e.value.code == -1                                        # top_k < 1
+    with pytest.raises(sd.SdError) as e:
+        dec.prefill(np.array([[1, 2]], np.int32), sd.Sampler(0.8, 50, 0.9, 0, 1.3), u)
+    assert e.value.code == -7                                        # a repetition penalty: SD_ERR_UNSUPPORTED
+    with pytest.raises(sd.SdError) as e:
+        dec.prefill(np.array([[1, 2]], np.int32), sd.Sampler(0.8, 50, 0.9, 0, -1.0), u)
+    assert e.value.code == -1                                        # a negative penalty
     t = dec.prefill(np.arange(38, dtype=np.int32)[None], s, u)
     first = int(t[0])
     t = dec.step(t, s, u)
@@ -363,6 +369,44 @@ def test_errors_and_context_limit(sd):
     assert e.value.code == -3                                        # SD_ERR_CTX_FULL
     dec.reset()                                                      # recovers after the error
     assert int(dec.prefill(np.arange(38, dtype=np.int32)[None], s, u)[0]) == first
+    dec.close()
+
+
+@pytest.mark.parametrize("kind", ["flat", "cluster"])
+def test_expired_exchange_wait_reports_timeout_and_recovers(sd, monkeypatch, kind):
+    """A wait on an exchange word that runs out.  A test hook (SD_TEST_STALL_US)
+    makes the first persistent launch's CTA 0 wait, for 1 ms, for an epoch that
+    no CTA writes; every other wait keeps its budget, sees the recorded error and
+    ends, and each CTA waits for its bulk copies in flight before it returns (no
+    mbarrier or copy wait is made to expire).  The call reports SD_ERR_TIMEOUT;
+    after sd_reset the same context decodes with oracle-equal logits and tokens."""
+    monkeypatch.setenv("SD_PERSISTENT", kind)
+    monkeypatch.setenv("SD_TEST_STALL_US", "1000")
+    run = get_preset("tiny").with_model(quant=P.Q4_0)
+    run = dataclasses.replace(run, sampler=SamplerSpec(0.8, 1000, 0.95, False))
+    spec = run.model
+    blob = _blob(spec)
+    prompt = prompt_tokens(run)
+    n = 4
+    draws = uniform_draws(run.draw_seed, n + 1, 1)[..., 0]
+    s = sd.Sampler.from_spec(run.sampler)
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    info = dec.info()
+    assert info.persistent > 0 and (info.persistent_clusters > 0) == (kind == "cluster")
+    with pytest.raises(sd.SdError) as e:
+        t = dec.prefill(prompt, s, draws[0])
+        dec.step(t, s, draws[1])
+    assert e.value.code == -6, e.value                              # SD_ERR_TIMEOUT
+    dec.reset()
+    ref = oracle.run_t3(oracle.Model(blob, THREADS), spec, prompt, draws, n, run.sampler)[0]
+    got = dec.prefill(prompt, s, draws[0])
+    for i in range(n + 1):
+        z = dec.logits()[0]
+        assert _rel(z, ref.logits[i]) <= REL_L2, i
+        if ref.margins[i] >= MARGIN:
+            assert int(got[0]) == ref.tokens[i], i
+        if i < n:
+            got = dec.step(np.array([ref.tokens[i]], np.int32), s, draws[i + 1])
     dec.close()
 
 

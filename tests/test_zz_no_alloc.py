@@ -56,3 +56,72 @@ def test_static_scratch_rejects_oversized_requests(sd):
     with pytest.raises(sd.SdError) as e:
         sd.sd_attend_rows_static(q, k, v, 16, 32, 32, 128, 64, 64, 64, out)
     assert e.value.code == -1 and "scratch" in str(e.value)
+
+
+def test_static_scratch_at_its_capacity_edges(sd):
+    """need = B * Hkv * (H / Hkv * nsplit * (hd + 4) + 1) floats always has an odd
+    factor above 1, so neither 2^20 nor 2^20 + 1 (= 17 * 61681) is a reachable
+    size: the closest requests on each side are checked instead."""
+    # 13 * 79 * 15 * 68 + 13 * 79 = 1048567 floats: 9 under the capacity -- accepted and correct
+    B, H, Hkv, hd, n_ctx, n, nsplit = 13, 79, 79, 64, 64, 60, 15
+    assert B * H * nsplit * (hd + 4) + B * Hkv == (1 << 20) - 9
+    q, k, v, vmax = _inputs(5, B, H, Hkv, hd, n_ctx)
+    ref = torch.empty(B, H, hd, dtype=torch.float32, device="cuda")
+    out = torch.full((B, H, hd), float("nan"), dtype=torch.float32, device="cuda")
+    sd.sd_attend_rows(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, ref)
+    sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out)
+    torch.cuda.synchronize()
+    assert (out - ref).abs().max().item() <= TOL * vmax
+    # 8 * 107 * 18 * 68 + 8 * 107 = 1048600 floats: 24 over -- rejected before any work
+    B, H, Hkv, nsplit = 8, 107, 107, 18
+    assert B * H * nsplit * (hd + 4) + B * Hkv == (1 << 20) + 24
+    q, k, v, _ = _inputs(6, B, H, Hkv, hd, n_ctx)
+    out = torch.empty(B, H, hd, dtype=torch.float32, device="cuda")
+    with pytest.raises(sd.SdError) as e:
+        sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out)
+    assert e.value.code == -1 and "scratch" in str(e.value)
+
+
+def test_static_call_allocates_nothing(sd):
+    """After one warm-up call, a call captured into a CUDA graph in global capture
+    mode (where any cudaMalloc or cudaFree, from any thread, breaks the capture)
+    records only its memset and kernel, and replaying the graph gives the
+    allocating entry's result; the device's free memory is unchanged by a loop of
+    calls."""
+    B, H, Hkv, hd, n_ctx, n, nsplit = 2, 16, 8, 128, 512, 333, 8
+    q, k, v, vmax = _inputs(7, B, H, Hkv, hd, n_ctx)
+    ref = torch.empty(B, H, hd, dtype=torch.float32, device="cuda")
+    out = torch.full((B, H, hd), float("nan"), dtype=torch.float32, device="cuda")
+    sd.sd_attend_rows(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, ref)
+    sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out)   # warm-up: address lookup
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(50):
+        sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    out.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="global"):
+        sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out,
+                                 torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert (out - ref).abs().max().item() <= TOL * vmax
+
+
+def test_static_entry_matches_the_oracle(sd):
+    """The static entry against the oracle's attention (plain loops, fp64 sums) at
+    one shape, per (row, head): no device path in between."""
+    import oracle
+    B, H, Hkv, hd, n_ctx, n, nsplit = 2, 8, 2, 64, 300, 277, 6
+    q, k, v, vmax = _inputs(8, B, H, Hkv, hd, n_ctx)
+    out = torch.empty(B, H, hd, dtype=torch.float32, device="cuda")
+    sd.sd_attend_rows_static(q, k, v, B, H, Hkv, hd, n_ctx, n, nsplit, out)
+    torch.cuda.synchronize()
+    qh, kh, vh, got = q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(), out.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            g = h // (H // Hkv)
+            want = oracle.attend(qh[b, h], kh[b, g, :n], vh[b, g, :n])
+            assert np.abs(got[b, h] - want).max() <= TOL * vmax, (b, h)
