@@ -62,6 +62,7 @@ using namespace gemv_detail;
 using namespace stepdev;
 
 constexpr int kNMB = 16;      // weight records in flight at most (a power of two)
+constexpr int kRB = 8;        // exchange words one thread of a reduction loads at once
 constexpr int kTokRep = 8;    // replicas of the sampled-token word
 
 // exchange barriers: q/k/v rows, attention partials, residual rows after the O projection (x')
@@ -551,8 +552,9 @@ __device__ __forceinline__ void attn_lk(const float* q, const __half* Ks, const 
 // (epoch-tagged words) are summed in a fixed order -- TPR lanes of a group
 // take clusters j, j + TPR, ... in increasing order and meet by xor shuffles
 // -- then bias and the residual are added and the row is sent to every rank of
-// the cluster (st.async into x, completing on its mbarrier mb_x).  All loads of
-// a lane are issued before the first is waited for.  A wait that expires
+// the cluster (st.async into x, completing on its mbarrier mb_x).  A lane
+// issues up to kRB loads before it waits for the first (all of them when
+// ncl <= kRB * TPR: one L2 round trip per reduction).  A wait that expires
 // leaves the error word set and the sum undefined (the step is then abandoned).
 template <int NB>
 __device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr0, int nr, unsigned e,
@@ -570,14 +572,15 @@ __device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
         const int i = ib / NB, b = ib - i * NB;
         float acc = 0.f;
         if (valid) {
-            for (int c0 = j; c0 < ncl; c0 += 4 * TPR) {
-                // the (up to) four words are polled together until all carry epoch e, so the
-                // wait ends one load after the last of them lands
-                const unsigned long long* pw[4];
-                unsigned long long w[4];
+            for (int c0 = j; c0 < ncl; c0 += kRB * TPR) {
+                // the (up to) kRB words are loaded together and polled until all carry epoch e,
+                // so the wait ends one load after the last of them lands; they are added in
+                // cluster order
+                const unsigned long long* pw[kRB];
+                unsigned long long w[kRB];
                 unsigned pend = 0u;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < kRB; ++q) {
                     const int c = c0 + q * TPR;
                     pw[q] = P + ((size_t)(c < ncl ? c : 0) * NB + b) * d + xr0 + i;
                     w[q] = 0ull;
@@ -586,10 +589,10 @@ __device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
                 const long long t0 = clock64();
                 for (unsigned it = 0; pend && ok; ++it) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < kRB; ++q)
                         if (pend & (1u << q)) w[q] = ll_load(pw[q]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < kRB; ++q)
                         if ((pend & (1u << q)) && (unsigned)(w[q] >> 32) == e) pend &= ~(1u << q);
                     if (!pend) break;
                     if (it > 2u) __nanosleep(32);
@@ -602,7 +605,7 @@ __device__ void reduce_bcast(const unsigned long long* P, int ncl, int d, int xr
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < kRB; ++q)
                     if (c0 + q * TPR < ncl) acc += __uint_as_float((unsigned)w[q]);
             }
         }

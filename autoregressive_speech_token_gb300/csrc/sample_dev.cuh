@@ -373,17 +373,22 @@ static __device__ __noinline__ int sample_smem(int V, const SampParams sp, const
 // ---------------------------------------------------------------- fast path
 //
 // The same sampler (the same survivors, fixed-point masses, cut and draw as
-// sample_smem, so the same token) located through value histograms instead of
-// radix passes.  The logits are binned linearly between their minimum and
-// maximum (kFB bins, bin 0 holding the largest): the bin of a value is a
-// monotone function of it, so equal values share a bin and every value of a
-// bin is at least every value of a later bin.  One count histogram and one
-// prefix over the bins find the bin holding the k-th largest logit; the exact
-// k-th largest key is then selected among that bin's members.  The top-p cut
-// is found the same way on a histogram of fixed-point masses: the bin where the
-// cumulative mass (from the top) reaches top_p * Z, then, among its members in
-// (key desc, index asc) order, the element where it does.  A bin with more than
-// kFC members (a degenerate distribution) falls back to sample_smem.
+// sample_smem) located through value histograms instead of radix passes.  The
+// logits are binned linearly between their minimum and maximum (kFB bins, bin
+// 0 holding the largest): the bin of a value is a monotone function of it, so
+// equal values share a bin and every value of a bin is at least every value of
+// a later bin.  One count histogram and one prefix over the bins find the bin
+// holding the k-th largest logit; the exact k-th largest key is then selected
+// among that bin's members.  The top-p cut is found the same way on a histogram
+// of fixed-point masses: the bin where the cumulative mass (from the top)
+// reaches T = ceil(top_p * Z), then, among its members in (key desc, index asc)
+// order, the element where it does.  The draw target is floor(u * ZS).  Both
+// products are formed exactly in integers (a float times a 64-bit integer, a
+// 128-bit product), the same on every thread.  Every block-wide reduction or
+// scan takes one barrier: the warps leave their partials in shared memory and
+// each warp then folds all of them itself.  A bin with more than kFC members (a
+// degenerate distribution) falls back to sample_smem.  The caller must pass a
+// barrier before it reuses the sampler's shared memory.
 constexpr int kFB = 2048, kFC = 1024;
 
 // shared memory after z[V]: the survivors' masses q[V] (u32), the count and mass histograms, the candidates
@@ -400,51 +405,104 @@ static __device__ float block_min_f(float v, float* s) {
     return -block_max_f(-v, s);
 }
 
-// Inclusive scan over the threads of one value per thread (thread order); the
-// exclusive prefix is returned, the block total in *total.
-static __device__ __forceinline__ unsigned block_excl_scan_u32(unsigned v, unsigned long long* s, unsigned* total) {
-    unsigned long long tot;
-    const unsigned long long r = block_exclusive_scan_u64(v, s, &tot);
-    *total = (unsigned)tot;
-    return (unsigned)r;
+static __device__ __forceinline__ unsigned warp_incl_scan_u32(unsigned v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+static __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// ceil(p * n) (up) or floor(p * n) for a float p in [0, 1] and an integer n, exactly:
+// p = m * 2^-sh with a 24-bit m, and m * n is formed in 128 bits
+static __device__ __forceinline__ unsigned long long mul_frac(float p, unsigned long long n, bool up) {
+    if (!(p > 0.f) || n == 0ull) return 0ull;
+    if (p >= 1.0f) return n;
+    const uint32_t u = __float_as_uint(p);
+    const int ex = (int)(u >> 23);  // p > 0: the sign bit is clear
+    const unsigned long long m = ex ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);
+    const int sh = ex ? 150 - ex : 149;  // p = m * 2^-sh, sh >= 24 for p < 1
+    const unsigned long long lo = m * n, hi = __umul64hi(m, n);
+    unsigned long long q;
+    bool rem;
+    if (sh >= 128) {
+        q = 0ull;
+        rem = true;
+    } else if (sh >= 64) {
+        q = hi >> (sh - 64);
+        rem = lo != 0ull || (sh > 64 && (hi & ((1ull << (sh - 64)) - 1ull)) != 0ull);
+    } else {
+        q = (hi << (64 - sh)) | (lo >> sh);
+        rem = (lo & ((1ull << sh) - 1ull)) != 0ull;
+    }
+    return q + ((up && rem) ? 1ull : 0ull);
 }
 
 static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
                                                SampleScratch& ss, int* err) {
-    const int tid = threadIdx.x, nt = SAMPLE_NT;
+    const int tid = threadIdx.x, nt = SAMPLE_NT, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     if (sp.greedy || sp.top_k == 1 || sp.temperature <= 0.f || nt * 4 != kFB)
         return sample_smem(V, sp, u_ptr, smraw, ss, err);
     const size_t arr = sample_array_bytes(V);
     const float* z = reinterpret_cast<const float*>(smraw);
-    // each survivor's mass p * 2^31 (truncated, <= 2^31: fits 32 bits), computed once; 0 for the others
+    // each survivor's mass p * 2^31 (truncated, <= 2^31: fits 32 bits); 0 for the others
     unsigned* qv = reinterpret_cast<unsigned*>(smraw + arr);               // [V]
     unsigned* cnt = reinterpret_cast<unsigned*>(smraw + 2 * arr);          // [kFB]
-    // per-bin masses, as sums of their high and low 16-bit halves (32-bit shared atomics; exact:
-    // at most 2^14 terms of at most 2^16 each), combined into mass[] before the prefix
-    unsigned long long* mass = reinterpret_cast<unsigned long long*>(cnt + kFB);  // [kFB]
-    unsigned* mh = reinterpret_cast<unsigned*>(mass);                      // [kFB], in mass[]'s space
+    // per-bin masses as sums of their high and low 16-bit halves (32-bit shared atomics; exact:
+    // at most 2^14 terms of at most 2^16 each)
+    unsigned* mh = cnt + kFB;                                              // [kFB]
     unsigned* ml = mh + kFB;                                               // [kFB]
-    uint32_t* ckey = reinterpret_cast<uint32_t*>(mass + kFB);              // [kFC]
+    uint32_t* ckey = ml + kFB;                                             // [kFC]
     int* cidx = reinterpret_cast<int*>(ckey + kFC);                        // [kFC]
     unsigned* cq = reinterpret_cast<unsigned*>(cidx + kFC);                // [kFC]
 
+    // ---- the range of the logits; the histograms cleared on the way
     float mloc = -INFINITY, nloc = INFINITY;
     for (int i = tid; i < V; i += nt) {
-        mloc = fmaxf(mloc, z[i]);
-        nloc = fminf(nloc, z[i]);
+        const float v = z[i];
+        mloc = fmaxf(mloc, v);
+        nloc = fminf(nloc, v);
     }
-    const float mx = block_max_f(mloc, ss.f), mn = block_min_f(nloc, ss.f);
-    // (capped: a range near the smallest normal would make the scale infinite, and 0 * inf is not 0)
-    const float sc = mx > mn ? fminf((float)(kFB - 1) / (mx - mn), 1e30f) : 0.f;
-    const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
-    const float invT = 1.0f / sp.temperature;
     for (int b = tid; b < kFB; b += nt) {
         cnt[b] = 0u;
         mh[b] = 0u;
         ml[b] = 0u;
     }
-    if (tid == 0) { ss.i[0] = 0; ss.i[1] = 0; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+        nloc = fminf(nloc, __shfl_xor_sync(0xffffffffu, nloc, o));
+    }
+    if (lane == 0) {
+        ss.f[warp] = mloc;
+        ss.f[32 + warp] = nloc;
+    }
+    if (tid == 0) {
+        ss.i[0] = 0;
+        ss.i[1] = 0;
+    }
     SAMPLE_SYNC();
+    float mx = ss.f[0], mn = ss.f[32];
+    for (int w = 1; w < nw; ++w) {
+        mx = fmaxf(mx, ss.f[w]);
+        mn = fminf(mn, ss.f[32 + w]);
+    }
+    // (capped: a range near the smallest normal would make the scale infinite, and 0 * inf is not 0)
+    const float sc = mx > mn ? fminf((float)(kFB - 1) / (mx - mn), 1e30f) : 0.f;
+    const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
+    const float invT = 1.0f / sp.temperature;
 
     // ---- top-k threshold key
     uint32_t thr = 0u;
@@ -452,13 +510,18 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         for (int i = tid; i < V; i += nt) atomicAdd(&cnt[vbin(z[i], mx, sc)], 1u);
         SAMPLE_SYNC();
         const uint4 c4 = reinterpret_cast<const uint4*>(cnt)[tid];  // bins 4 tid .. 4 tid + 3
-        unsigned tot;
-        unsigned cum = block_excl_scan_u32(c4.x + c4.y + c4.z + c4.w, ss.q, &tot);
+        const unsigned own = c4.x + c4.y + c4.z + c4.w;
+        const unsigned inc = warp_incl_scan_u32(own);
+        if (lane == 31) ss.i[8 + warp] = (int)inc;
+        SAMPLE_SYNC();
+        unsigned cum = inc - own;
+        for (int w = 0; w < warp; ++w) cum += (unsigned)ss.i[8 + w];
         const unsigned cb[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (cum < (unsigned)k && cum + cb[j] >= (unsigned)k) {
-                ss.i[2] = 4 * tid + j;          // the bin of the k-th largest
-                ss.i[3] = k - (int)cum;         // its rank inside the bin (1 = the bin's largest)
+                ss.i[2] = 4 * tid + j;   // the bin of the k-th largest
+                ss.i[3] = k - (int)cum;  // its rank inside the bin (1 = the bin's largest)
                 ss.i[4] = (int)cb[j];
             }
             cum += cb[j];
@@ -486,21 +549,25 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     const bool topp = sp.top_p < 1.0f;
     unsigned long long zl = 0ull;
     for (int i = tid; i < V; i += nt) {
-        if (ord_key(z[i]) < thr) {
-            qv[i] = 0u;
-            continue;
+        const float v = z[i];
+        unsigned q = 0u;
+        if (ord_key(v) >= thr) {
+            q = (unsigned)fixq(expf((v - mx) * invT));
+            if (topp && q) {
+                const int bn = vbin(v, mx, sc);
+                atomicAdd(&mh[bn], q >> 16);
+                atomicAdd(&ml[bn], q & 0xFFFFu);
+            }
         }
-        const unsigned q = (unsigned)fixq(expf((z[i] - mx) * invT));
         qv[i] = q;
         zl += q;
-        if (topp) {
-            const int bn = vbin(z[i], mx, sc);
-            atomicAdd(&mh[bn], (unsigned)(q >> 16));
-            atomicAdd(&ml[bn], (unsigned)(q & 0xFFFFu));
-        }
     }
-    unsigned long long Zq;
-    block_exclusive_scan_u64(zl, ss.q, &Zq);  // barrier: the mass histograms are complete
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zl += __shfl_xor_sync(0xffffffffu, zl, o);
+    if (lane == 0) ss.q[warp] = zl;
+    SAMPLE_SYNC();  // also: the mass histograms and qv are complete
+    unsigned long long Zq = 0ull;
+    for (int w = 0; w < nw; ++w) Zq += ss.q[w];
 
     // ---- top-p cut: (tkey, tidx) of the element where the (key desc, index asc) cumulative mass
     // reaches T = ceil(top_p * Z)
@@ -508,14 +575,18 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     uint32_t tkey = 0u;
     int tidx = 0x7fffffff;
     if (topp) {
-        const unsigned long long T0 = (unsigned long long)ceil((double)sp.top_p * (double)Zq);
-        const unsigned long long T = T0 > 0ull ? T0 : 1ull;
+        unsigned long long T = mul_frac(sp.top_p, Zq, true);
+        if (T == 0ull) T = 1ull;
         const uint4 h4 = reinterpret_cast<const uint4*>(mh)[tid], l4 = reinterpret_cast<const uint4*>(ml)[tid];
         const unsigned long long mb[4] = {((unsigned long long)h4.x << 16) + l4.x, ((unsigned long long)h4.y << 16) + l4.y,
                                           ((unsigned long long)h4.z << 16) + l4.z, ((unsigned long long)h4.w << 16) + l4.w};
-        unsigned long long tot;
-        unsigned long long cum = block_exclusive_scan_u64(mb[0] + mb[1] + mb[2] + mb[3], ss.q, &tot);
-        if (tid == 0) ss.i[0] = 0;
+        const unsigned long long own = mb[0] + mb[1] + mb[2] + mb[3];
+        const unsigned long long inc = warp_incl_scan_u64(own);
+        if (lane == 31) ss.q[16 + warp] = inc;
+        SAMPLE_SYNC();
+        unsigned long long cum = inc - own;
+        for (int w = 0; w < warp; ++w) cum += ss.q[16 + w];
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (cum < T && cum + mb[j] >= T) {
                 ss.i[5] = 4 * tid + j;  // the bin where the cumulative mass reaches T
@@ -526,18 +597,20 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         SAMPLE_SYNC();
         const int bp = ss.i[5];
         const unsigned long long remT = ss.rem;
+        // its members that carry mass (a survivor without mass cannot be where the mass crosses,
+        // nor change anything before it)
         for (int i = tid; i < V; i += nt) {
-            const uint32_t key = ord_key(z[i]);
-            if (key < thr || vbin(z[i], mx, sc) != bp) continue;
-            const int c = atomicAdd(&ss.i[0], 1);
+            const unsigned q = qv[i];
+            if (q == 0u || vbin(z[i], mx, sc) != bp) continue;
+            const int c = atomicAdd(&ss.i[1], 1);
             if (c < kFC) {
-                ckey[c] = key;
+                ckey[c] = ord_key(z[i]);
                 cidx[c] = i;
-                cq[c] = qv[i];
+                cq[c] = q;
             }
         }
         SAMPLE_SYNC();
-        const int np = ss.i[0];
+        const int np = ss.i[1];
         if (np > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
         for (int c = tid; c < np; c += nt) {
             const uint32_t key = ckey[c];
@@ -556,7 +629,8 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         cut = true;
     }
 
-    // ---- draw in vocabulary order over the kept elements (exact fixed-point prefix sums)
+    // ---- draw in vocabulary order over the kept elements (exact fixed-point prefix sums; each
+    // thread takes one contiguous segment)
     auto kept = [&](int i) {
         if (!cut) return true;  // qv is 0 for the elements under the top-k threshold
         const uint32_t key = ord_key(z[i]);
@@ -565,25 +639,37 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     const int seg = (V + nt - 1) / nt;
     const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
     unsigned long long loc = 0ull;
-    for (int i = a0; i < a1; ++i)
-        if (kept(i)) loc += qv[i];
-    unsigned long long ZS;
-    unsigned long long run = block_exclusive_scan_u64(loc, ss.q, &ZS);
-    if (tid == 0) ss.rem = (unsigned long long)floor((double)(*u_ptr) * (double)ZS);
+    for (int i = a0; i < a1; ++i) {
+        const unsigned q = qv[i];
+        if (q && kept(i)) loc += q;
+    }
+    const unsigned long long inc = warp_incl_scan_u64(loc);
+    if (lane == 31) ss.q[32 + warp] = inc;
     SAMPLE_SYNC();
-    const unsigned long long target = ss.rem;
+    unsigned long long run = inc - loc, ZS = 0ull;
+    for (int w = 0; w < nw; ++w) {
+        const unsigned long long t = ss.q[32 + w];
+        ZS += t;
+        if (w < warp) run += t;
+    }
+    const unsigned long long target = mul_frac(*u_ptr, ZS, false);
     int cand = 0x7fffffff;
     for (int i = a0; i < a1; ++i) {
-        if (!kept(i) || qv[i] == 0u) continue;
-        run += qv[i];
+        const unsigned q = qv[i];
+        if (q == 0u || !kept(i)) continue;
+        run += q;
         if (run > target) { cand = i; break; }
     }
-    int tok = block_min_i(cand, ss.i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    if (lane == 0) ss.hist[warp] = (unsigned)cand;
+    SAMPLE_SYNC();
+    int tok = 0x7fffffff;
+    for (int w = 0; w < nw; ++w) tok = min(tok, (int)ss.hist[w]);
     if (tok < 0 || tok >= V) {
         if (tid == 0 && err) atomicExch(err, 2);
         tok = 0;
     }
-    SAMPLE_SYNC();
     return tok;
 }
 

@@ -393,11 +393,21 @@ int enqueue_cp_frame(sd_ctx* c, cudaStream_t st) {
 }
 
 // One launch of the cluster step kernel for n_steps steps.
+// Test hook: the first persistent launch made outside a stream capture takes the stall budget
+// (a captured graph would replay it on every step).
+void take_test_stall(sd_ctx* c, cudaStream_t st, long long* budget) {
+    *budget = 0;
+    if (!c->test_stall) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+    *budget = c->test_stall;
+    c->test_stall = 0;
+}
+
 int enqueue_cstep(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_seq, cudaStream_t st) {
     CStepArgs a = c->cstep;
     a.n_steps = n_steps;
-    a.test_budget = c->test_stall;
-    c->test_stall = 0;
+    take_test_stall(c, st, &a.test_budget);
     a.u_seq = u_seq;
     a.out_seq = out_seq;
     if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * kCTraceSub, st));
@@ -417,8 +427,7 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     if (c->cpersistent) return enqueue_cstep(c, n_steps, u_seq, out_seq, st);
     StepArgs a = c->step;
     a.n_steps = n_steps;
-    a.test_budget = c->test_stall;
-    c->test_stall = 0;
+    take_test_stall(c, st, &a.test_budget);
     a.u_seq = u_seq;
     a.out_seq = out_seq;
     if (a.trace) CK(cudaMemsetAsync(a.trace, 0, sizeof(unsigned long long) * 64, st));

@@ -206,18 +206,18 @@ def sample(z, temperature=1.0, top_k=1, top_p=1.0, greedy=True, u=0.0):
 
 
 def sample_ladder(z_cond, z_uncond=None, cfg_weight=0.0, seen=None, rep_penalty=1.0, temperature=1.0, min_p=0.0,
-                  top_p=1.0, top_k=0, u=0.0):
+                  top_p=1.0, top_k=0, u=0.0, with_draw=False):
     """The multilingual T3's sampler ladder (CFG combine, repetition penalty,
     temperature, min_p, top-p, top-k, draw in vocabulary order).  Returns
-    (token, margin)."""
+    (token, margin), or (token, margin, draw distance) with with_draw."""
     zc = _f32(z_cond)
     zu = _f32(z_uncond) if z_uncond is not None else None
     sn = np.ascontiguousarray(seen, np.uint8) if seen is not None else None
-    m = C.c_double()
+    m, dd = C.c_double(), C.c_double()
     tok = lib().orc_sample_ladder(_p(zc, C.c_float), _p(zu, C.c_float), zc.size, float(cfg_weight),
                                   _p(sn, C.c_uint8), float(rep_penalty), float(temperature), float(min_p),
-                                  float(top_p), int(top_k), float(u), C.byref(m))
-    return int(tok), float(m.value)
+                                  float(top_p), int(top_k), float(u), C.byref(m), C.byref(dd))
+    return (int(tok), float(m.value), float(dd.value)) if with_draw else (int(tok), float(m.value))
 
 
 # ----------------------------------------------------------------------------- model-level

@@ -578,8 +578,9 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
  *           times the kept total. */
 int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V, float cfg_weight,
                           const uint8_t* seen, float rep_penalty, float temperature, float min_p, float top_p,
-                          int32_t top_k, double u, double* margin) {
+                          int32_t top_k, double u, double* margin, double* draw_dist) {
     if (V <= 0) return -1;
+    if (draw_dist) *draw_dist = INFINITY;
     double* z = (double*)malloc((size_t)V * sizeof(double));
     for (int32_t i = 0; i < V; ++i) {
         double c = z_cond[i];
@@ -663,6 +664,7 @@ int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V,
         if (c > target) { tok = i; break; }
     }
     if (tok < 0) { tok = last; c_lo = c - p[last]; }
+    if (draw_dist) *draw_dist = fmax(0.0, fmin(target - c_lo, c - target)) / zs;
     if (margin) {
         /* every entry in (desc, index asc) order, and the stages as applied */
         zi* a = (zi*)malloc((size_t)V * sizeof(zi));

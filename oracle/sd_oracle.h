@@ -61,10 +61,12 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
  * NULL (no penalty); top_k < 1 or > V keeps every survivor; temperature <= 0
  * returns the argmax of the combined, penalised logits.  margin (may be NULL)
  * receives the decision margin as orc_sample defines it, over the combined,
- * penalised and scaled logits and the min_p, top-p and top-k stages. */
+ * penalised and scaled logits and the min_p, top-p and top-k stages;
+ * draw_dist (may be NULL) the draw's distance alone: u to the nearer end of the
+ * chosen token's interval on the kept mass (normalised; infinite for argmax). */
 int32_t orc_sample_ladder(const float* z_cond, const float* z_uncond, int32_t V, float cfg_weight,
                           const uint8_t* seen, float rep_penalty, float temperature, float min_p, float top_p,
-                          int32_t top_k, double u, double* margin);
+                          int32_t top_k, double u, double* margin, double* draw_dist);
 
 /* Model.  The blob must outlive the model. */
 int  orc_open(const uint8_t* blob, uint64_t nbytes, orc_model** out);
