@@ -384,7 +384,7 @@ __device__ void bf_norm(const float* x, int xs, int K, bool ln, const float* g1,
 
 // sum_k W[i][k] x[b][k] for the record's rows i < nr (tiles of fragment-major
 // codes and scales), x given as B fragments.  Units of (tile, k-slice) go to
-// the warps -- KS slices per tile, as many as leave no warp idle -- and each
+// the warps -- KS slices per tile, as many as leave no warp idle, at most four -- and each
 // unit's partial sums go to red[unit][16][NB]; after a CTA barrier the slices
 // are added in order and emit(i, b, y) (PAIRS: emit(i, b, y_2i, y_2i+1) for
 // row pairs) runs once per output.  The codes are read straight from the
@@ -397,6 +397,7 @@ __device__ __forceinline__ void mma_rows(const uint8_t* codes, const uint8_t* sc
     const int KB = K >> 5;
     int KS = kWarps / nt;
     if (KS < 1) KS = 1;
+    if (KS > 4) KS = 4;  // measured: past four slices the extra reduction costs more than the shorter runs save
     if (KS > KB) KS = KB;
     const int units = nt * KS;
     const __half* sh = reinterpret_cast<const __half*>(sc);
@@ -798,7 +799,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
         return ok;
     };
     // CTA 0, thread 0: cycles since the previous stamp, added to sub-step k
-    const bool trc = a.trace && gi == 0 && tid == 0;
+    const bool trc = a.trace && gi == a.trace_gi && tid == 0;
     long long tc0 = trc ? clock64() : 0;
     auto stamp = [&](int k) {
         if (trc) {
@@ -1020,20 +1021,29 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                 }
                 csync();
                 stamp(24);
-                // only the first min(WG, blocks per fill) warps of a pair hold keys
+                // only the first min(WG, blocks per fill) warps of a pair hold keys.  One warp per pair
+                // folds their maxima (lane w: warp w of the pair) into M and the weights exp(m_w - M),
+                // kept in wq (idle once every warp has attended); then each component is one
+                // weighted sum over the warps, and the pair's M
                 const int wa = min(WG, min(nbr, SB));
+                float* ew = wq;  // [nph][17]: the weights, then M
+                if (warp < nph) {
+                    const float* P = wp + (size_t)warp * WG * W2;
+                    const float mw = lane < wa ? P[lane * W2 + hd] : -INFINITY;
+                    float M = mw;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                    if (lane < wa) ew[warp * 17 + lane] = mw != -INFINITY ? expf(mw - M) : 0.f;
+                    if (lane == 0) ew[warp * 17 + 16] = M;
+                }
+                csync();
                 for (int u = tid; u < nph * (hd + 2); u += kThreads) {
                     const int p = u == tid ? cp_p : u / (hd + 2), k = u == tid ? cp_k : u - p * (hd + 2);
                     const float* P = wp + (size_t)p * WG * W2;
-                    float M = -INFINITY;
-                    for (int w = 0; w < wa; ++w) M = fmaxf(M, P[w * W2 + hd]);
-                    float v = M;
+                    float v = ew[p * 17 + 16];
                     if (k != hd) {
                         v = 0.f;
-                        for (int w = 0; w < wa; ++w) {
-                            const float mw = P[w * W2 + hd];
-                            if (mw != -INFINITY) v = fmaf(expf(mw - M), P[w * W2 + k], v);
-                        }
+                        for (int w = 0; w < wa; ++w) v = fmaf(ew[p * 17 + w], P[w * W2 + k], v);
                     }
                     const uint32_t addr = a_part + 4u * (uint32_t)((rank * NB * a.hpc + p) * W2 + k);
                     for (int dst = 0; dst < cs; ++dst) st_async(mapa(addr, dst), v, mapa(mb_part, dst));
@@ -1048,20 +1058,30 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             {
                 xwait(mb_part, ph_part, xb_bytes_of(XB_PART));
                 stamp(7);
-                for (int t = tid; t < NB * a.hpc * hd; t += kThreads) {
+                // per (batch row, head): one warp (lane r: rank r) folds the ranks' maxima and
+                // denominators into the weights exp(m_r - M) / sum_r exp(m_r - M) l_r, kept in red
+                // (idle until the O matvec); then each output element is one weighted sum over ranks
+                const int nbh = NB * a.hpc;
+                float* cw = red;  // [nbh][16]
+                if (warp < nbh) {
+                    const float* P = part + (size_t)(lane * nbh + warp) * W2;
+                    const float mr = lane < cs ? P[hd] : -INFINITY;
+                    float M = mr;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                    const float w = (lane < cs && mr != -INFINITY) ? expf(mr - M) : 0.f;
+                    float den = lane < cs ? w * P[hd + 1] : 0.f;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+                    if (lane < cs) cw[warp * 16 + lane] = w / den;
+                }
+                csync();
+                for (int t = tid; t < nbh * hd; t += kThreads) {
                     const int bh = t >> lhd, dd = t & (hd - 1);
-                    float M = -INFINITY;
-                    for (int r = 0; r < cs; ++r) M = fmaxf(M, part[(r * NB * a.hpc + bh) * W2 + hd]);
-                    float num = 0.f, den = 0.f;
-                    for (int r = 0; r < cs; ++r) {
-                        const float* P = part + (r * NB * a.hpc + bh) * W2;
-                        if (P[hd] == -INFINITY) continue;
-                        const float w = expf(P[hd] - M);
-                        num = fmaf(w, P[dd], num);
-                        den = fmaf(w, P[hd + 1], den);
-                    }
+                    float v = 0.f;
+                    for (int r = 0; r < cs; ++r) v = fmaf(cw[bh * 16 + r], part[(r * nbh + bh) * W2 + dd], v);
                     const int bb = NB == 1 ? 0 : bh / a.hpc, qh = bh - bb * a.hpc;
-                    bf_put<QK, NB>(bf, qh * hd + dd, bb, num / den);
+                    bf_put<QK, NB>(bf, qh * hd + dd, bb, v);
                 }
                 csync();
                 stamp(8);
@@ -1224,7 +1244,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
         if (kv_issued > (int)ph_kv) mb_wait(mb_kv, ph_kv & 1u, a.err, budget, true);
     }
     csync();
-    if (a.trace && gi == 0 && tid < kCTraceSub) a.trace[tid] += s_trc[tid];
+    if (a.trace && gi == a.trace_gi && tid < kCTraceSub) a.trace[tid] += s_trc[tid];
     // no CTA of the cluster leaves while another may still send into its shared memory
     cluster_sync_all();
     if (!ok) __nanosleep(20000);

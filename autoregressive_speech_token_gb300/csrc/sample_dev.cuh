@@ -450,6 +450,64 @@ static __device__ __forceinline__ unsigned long long mul_frac(float p, unsigned 
     return q + ((up && rem) ? 1ull : 0ull);
 }
 
+// f(i, z[i]) for this thread's elements i = tid, tid + nt, ... < V, the loads issued four at a time
+template <typename F>
+static __device__ __forceinline__ void for_strided(const float* z, int V, F&& f) {
+    const int tid = threadIdx.x, nt = SAMPLE_NT;
+    for (int i0 = tid; i0 < V; i0 += 4 * nt) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nt;
+            v[j] = i < V ? z[i] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nt;
+            if (i < V) f(i, v[j]);
+        }
+    }
+}
+
+// as for_strided, with qv[i] loaded beside z[i]
+template <typename F>
+static __device__ __forceinline__ void for_strided_q(const float* z, const unsigned* qv, int V, F&& f) {
+    const int tid = threadIdx.x, nt = SAMPLE_NT;
+    for (int i0 = tid; i0 < V; i0 += 4 * nt) {
+        float v[4];
+        unsigned q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nt;
+            v[j] = i < V ? z[i] : 0.f;
+            q[j] = i < V ? qv[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nt;
+            if (i < V) f(i, v[j], q[j]);
+        }
+    }
+}
+
+// f(i, z[i], qv[i]) for i in [a0, a1) in order, the loads issued eight at a time; f returns false to stop
+template <typename F>
+static __device__ __forceinline__ void for_segment(const float* z, const unsigned* qv, int a0, int a1, F&& f) {
+    for (int b = a0; b < a1; b += 8) {
+        float v[8];
+        unsigned q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = b + j;
+            v[j] = i < a1 ? z[i] : 0.f;
+            q[j] = i < a1 ? qv[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (b + j < a1 && !f(b + j, v[j], q[j])) return;
+    }
+}
+
 static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
                                                SampleScratch& ss, int* err) {
     const int tid = threadIdx.x, nt = SAMPLE_NT, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
@@ -470,11 +528,10 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
 
     // ---- the range of the logits; the histograms cleared on the way
     float mloc = -INFINITY, nloc = INFINITY;
-    for (int i = tid; i < V; i += nt) {
-        const float v = z[i];
+    for_strided(z, V, [&](int, float v) {
         mloc = fmaxf(mloc, v);
         nloc = fminf(nloc, v);
-    }
+    });
     for (int b = tid; b < kFB; b += nt) {
         cnt[b] = 0u;
         mh[b] = 0u;
@@ -507,7 +564,7 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     // ---- top-k threshold key
     uint32_t thr = 0u;
     if (k < V) {
-        for (int i = tid; i < V; i += nt) atomicAdd(&cnt[vbin(z[i], mx, sc)], 1u);
+        for_strided(z, V, [&](int, float v) { atomicAdd(&cnt[vbin(v, mx, sc)], 1u); });
         SAMPLE_SYNC();
         const uint4 c4 = reinterpret_cast<const uint4*>(cnt)[tid];  // bins 4 tid .. 4 tid + 3
         const unsigned own = c4.x + c4.y + c4.z + c4.w;
@@ -529,8 +586,9 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         SAMPLE_SYNC();
         const int bk = ss.i[2], rk = ss.i[3], nbk = ss.i[4];
         if (nbk > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
-        for (int i = tid; i < V; i += nt)
-            if (vbin(z[i], mx, sc) == bk) ckey[atomicAdd(&ss.i[0], 1)] = ord_key(z[i]);
+        for_strided(z, V, [&](int, float v) {
+            if (vbin(v, mx, sc) == bk) ckey[atomicAdd(&ss.i[0], 1)] = ord_key(v);
+        });
         SAMPLE_SYNC();
         for (int c = tid; c < nbk; c += nt) {
             const uint32_t key = ckey[c];
@@ -548,8 +606,7 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     // ---- survivors' fixed-point masses: the total, and (for top-p) per bin
     const bool topp = sp.top_p < 1.0f;
     unsigned long long zl = 0ull;
-    for (int i = tid; i < V; i += nt) {
-        const float v = z[i];
+    for_strided(z, V, [&](int i, float v) {
         unsigned q = 0u;
         if (ord_key(v) >= thr) {
             q = (unsigned)fixq(expf((v - mx) * invT));
@@ -561,7 +618,7 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         }
         qv[i] = q;
         zl += q;
-    }
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zl += __shfl_xor_sync(0xffffffffu, zl, o);
     if (lane == 0) ss.q[warp] = zl;
@@ -599,16 +656,15 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
         const unsigned long long remT = ss.rem;
         // its members that carry mass (a survivor without mass cannot be where the mass crosses,
         // nor change anything before it)
-        for (int i = tid; i < V; i += nt) {
-            const unsigned q = qv[i];
-            if (q == 0u || vbin(z[i], mx, sc) != bp) continue;
+        for_strided_q(z, qv, V, [&](int i, float v, unsigned q) {
+            if (q == 0u || vbin(v, mx, sc) != bp) return;
             const int c = atomicAdd(&ss.i[1], 1);
             if (c < kFC) {
-                ckey[c] = ord_key(z[i]);
+                ckey[c] = ord_key(v);
                 cidx[c] = i;
                 cq[c] = q;
             }
-        }
+        });
         SAMPLE_SYNC();
         const int np = ss.i[1];
         if (np > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
@@ -631,18 +687,18 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
 
     // ---- draw in vocabulary order over the kept elements (exact fixed-point prefix sums; each
     // thread takes one contiguous segment)
-    auto kept = [&](int i) {
+    auto kept = [&](int i, float v) {
         if (!cut) return true;  // qv is 0 for the elements under the top-k threshold
-        const uint32_t key = ord_key(z[i]);
+        const uint32_t key = ord_key(v);
         return key > tkey || (key == tkey && i <= tidx);
     };
     const int seg = (V + nt - 1) / nt;
     const int a0 = min(V, tid * seg), a1 = min(V, a0 + seg);
     unsigned long long loc = 0ull;
-    for (int i = a0; i < a1; ++i) {
-        const unsigned q = qv[i];
-        if (q && kept(i)) loc += q;
-    }
+    for_segment(z, qv, a0, a1, [&](int i, float v, unsigned q) {
+        if (q && kept(i, v)) loc += q;
+        return true;
+    });
     const unsigned long long inc = warp_incl_scan_u64(loc);
     if (lane == 31) ss.q[32 + warp] = inc;
     SAMPLE_SYNC();
@@ -654,12 +710,15 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     }
     const unsigned long long target = mul_frac(*u_ptr, ZS, false);
     int cand = 0x7fffffff;
-    for (int i = a0; i < a1; ++i) {
-        const unsigned q = qv[i];
-        if (q == 0u || !kept(i)) continue;
+    for_segment(z, qv, a0, a1, [&](int i, float v, unsigned q) {
+        if (q == 0u || !kept(i, v)) return true;
         run += q;
-        if (run > target) { cand = i; break; }
-    }
+        if (run > target) {
+            cand = i;
+            return false;
+        }
+        return true;
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
     if (lane == 0) ss.hist[warp] = (unsigned)cand;

@@ -834,6 +834,7 @@ int setup_cstep(sd_ctx* c) {
             (rc = dalloc(c, &a.trace, sizeof(unsigned long long) * kCTraceSub)) ||
             (rc = dalloc(c, &a.trace_cta, sizeof(unsigned long long) * kCtaSteps * a.n_layer * kCTracePhases * grid)))
             return rc;
+        if (const char* tg = getenv("SD_TRACE_CTA")) a.trace_gi = std::min(std::max(0, atoi(tg)), grid - 1);
     }
     CK(cudaStreamSynchronize(c->stream));
     c->step_grid = grid;
@@ -960,7 +961,7 @@ void write_ctrace(sd_ctx* c, int n_steps) {
                               "head*", "end*", "(q prep)", "(kv wait)", "(wp+bar)", "(send+bar)", "start*", "embed*", "gather*",
                               "sample*"};
         const double nl = (double)n_steps * L;
-        fprintf(f, "  CTA 0 cycles per layer (* per step):\n   ");
+        fprintf(f, "  CTA %d cycles per layer (* per step):\n   ", a.trace_gi);
         for (int k = 0; k < 30; ++k) {
             if (!nm[k][0]) continue;
             fprintf(f, " %s %.0f |", nm[k], (double)t[k] / ((k >= 20 && k <= 21) || k >= 26 ? (double)n_steps : nl));

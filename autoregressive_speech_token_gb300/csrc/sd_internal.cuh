@@ -282,6 +282,7 @@ struct CStepArgs {
     unsigned long long* trace = nullptr;
     // optional [kCtaSteps][n_layer][kCTracePhases][grid]: every CTA's publish stamps of the first steps
     unsigned long long* trace_cta = nullptr;
+    int trace_gi = 0;                    // the CTA whose sub-steps `trace` accumulates
 };
 constexpr int kCtaSteps = 4;
 constexpr int kCTraceSub = 32;  // sub-steps 28, 29: the sampler CTA's logits gather and sampling
