@@ -303,7 +303,8 @@ def run_gpu(args):
     peaks, peak_kind = load_peaks()
     bytes_step = mean_step_bytes(m, run.prompt_len, K)
     achieved = bytes_step / (ms / K / 1e3) / 1e9
-    traffic = load_traffic(args.config, "persistent" if info.persistent else "graph")
+    step_path = "cluster" if info.persistent_clusters else ("persistent" if info.persistent else "graph")
+    traffic = load_traffic(args.config, step_path)
     dec.close()
 
     line = {
@@ -319,7 +320,9 @@ def run_gpu(args):
         "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": int(info.step_h2d_bytes),
                 "d2h_bytes_per_step": int(info.step_d2h_bytes), "steps": Ke},
         "roofline": {"bound": "hbm",
-                     "kernel": (f"decode step (persistent kernel, {info.persistent} CTAs, one launch per {K} steps)"
+                     "kernel": (f"decode step (cluster persistent kernel k_cstep, {info.persistent_clusters} clusters "
+                                f"x {info.cluster_size} CTAs, one launch per {K} steps)" if info.persistent_clusters
+                                else f"decode step (persistent kernel, {info.persistent} CTAs, one launch per {K} steps)"
                                 if info.persistent else f"decode step ({info.kernels_per_step} kernels, one CUDA graph)"),
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
