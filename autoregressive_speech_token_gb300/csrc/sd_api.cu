@@ -105,6 +105,7 @@ struct sd_ctx {
     float* nrm = nullptr;               // [B][max width] normalised rows (B > 2)
     float* g16_ws = nullptr;            // skinny GEMM partial sums (B > 2)
     int* g16_cnt = nullptr;             // skinny GEMM column-tile counters (zero between launches)
+    bool rows_gemm_tc = false;          // 3-16 rows, affine weights: the tcgen05 skinny GEMM (SD_ROWS_GEMM unset)
     bool rows_gemm_mma = false;         // SD_ROWS_GEMM=mma: the 64x64 mma.sync GEMM for > 2 rows instead
     int32_t* prompt = nullptr;          // [B][max_ctx]
 
@@ -259,7 +260,8 @@ int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
             Gemm16Args g;
             g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
             g.y = a.y; g.ldy = a.y_stride; g.ws = c->g16_ws; g.cnt = c->g16_cnt;
-            e = launch_gemm16(g, c->sm_count, st);
+            e = (c->rows_gemm_tc && gemm16_tc_supported(a.W)) ? launch_gemm16_tc(g, c->sm_count, &c->ds->err, st)
+                                                               : launch_gemm16(g, c->sm_count, st);
         }
         c->count_launch++;
     }
@@ -1153,6 +1155,7 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     if (c->B > 2) {
         const char* rg = getenv("SD_ROWS_GEMM");
         c->rows_gemm_mma = rg && strcmp(rg, "mma") == 0;
+        c->rows_gemm_tc = !rg;  // SD_ROWS_GEMM=skinny: the mma.sync skinny GEMM for every format
         // skinny GEMM workspace: the largest partial-sum array and tile count over every matrix
         std::vector<std::pair<int, int>> nk;  // (rows, cols)
         auto stack_mats = [&](int d, int H, int Hkv, int hd, int ff, bool gpt2) {
@@ -1172,6 +1175,8 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
         int tiles = 0;
         for (const auto& p : nk) {
             wsf = std::max(wsf, gemm16_ws_floats(p.first, p.second, c->sm_count));
+            if (m.quant == SD_A8G64 && p.second % 64 == 0)
+                wsf = std::max(wsf, gemm16_tc_ws_floats(p.first, p.second, c->sm_count));
             tiles = std::max(tiles, gemm16_tiles(p.first));
         }
         if ((rc = dalloc(c, &c->g16_ws, sizeof(float) * wsf)) || (rc = dalloc(c, &c->g16_cnt, sizeof(int) * tiles)))
@@ -1583,8 +1588,11 @@ int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, 
     CK(cudaSetDevice(m->device));
     int sms = 0;
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, m->device));
+    const bool tc = gemm16_tc_supported(m->m) && !getenv("SD_ROWS_GEMM");
     if (!m->g16_ws) {
-        CK(cudaMalloc(&m->g16_ws, sizeof(float) * gemm16_ws_floats(m->m.rows, m->m.cols, sms)));
+        size_t wsf = gemm16_ws_floats(m->m.rows, m->m.cols, sms);
+        if (gemm16_tc_supported(m->m)) wsf = std::max(wsf, gemm16_tc_ws_floats(m->m.rows, m->m.cols, sms));
+        CK(cudaMalloc(&m->g16_ws, sizeof(float) * wsf));
         CK(cudaMalloc(&m->g16_cnt, sizeof(int) * gemm16_tiles(m->m.rows)));
         CK(cudaMemset(m->g16_cnt, 0, sizeof(int) * gemm16_tiles(m->m.rows)));
     }
@@ -1592,7 +1600,8 @@ int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, 
     a.W = m->m; a.M = M; a.x = x_dev; a.ldx = m->m.cols; a.epi = epilogue; a.bias = bias_dev;
     a.resid = resid_dev; a.y = y_dev; a.ldy = epilogue == SD_EPI_SWIGLU ? m->m.rows / 2 : m->m.rows;
     a.ws = m->g16_ws; a.cnt = m->g16_cnt;
-    CK(launch_gemm16(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+    CK(tc ? launch_gemm16_tc(a, sms, nullptr, reinterpret_cast<cudaStream_t>(stream))
+          : launch_gemm16(a, sms, reinterpret_cast<cudaStream_t>(stream)));
     return SD_OK;
 }
 

@@ -338,6 +338,18 @@ size_t gemm16_ws_floats(int N, int K, int sm_count);
 int gemm16_tiles(int N);
 cudaError_t launch_gemm16(Gemm16Args a, int sm_count, cudaStream_t st);
 
+// The same product on tcgen05 for 8-bit affine-group weights (k_gemm16_tc.cu): the
+// codes' 2-D tensor map, the skinny-GEMM arguments, the wait budget and error word.
+struct alignas(128) Gemm16TcArgs {
+    CUtensorMap wq;
+    Gemm16Args g;
+    long long budget = 0;
+    int* err = nullptr;
+};
+bool gemm16_tc_supported(const QMat& W);
+size_t gemm16_tc_ws_floats(int N, int K, int sm_count);
+cudaError_t launch_gemm16_tc(Gemm16Args g, int sm_count, int* err, cudaStream_t st);
+
 // Tensor-core (tcgen05) GEMM for prefill: fp16 hi/lo operands loaded by TMA
 // through 2-D tensor maps ([rows][K] fp16, K a multiple of 64), three MMAs per
 // K step, the QGemm epilogues.

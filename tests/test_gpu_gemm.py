@@ -194,9 +194,20 @@ G16_SHAPES = [(KQ8, (3072, 1024)), (KQ8, (200, 96)), (KQ8, (64, 32)), (KQ8, (102
               (KA8, (4096, 2048)), (KA8, (2048, 6144)), (KA8, (1024, 3072)), (KA8, (130, 128)), (KA8, (3072, 1024))]
 
 
+@pytest.fixture(params=["tc", "skinny"])
+def g16_path(request, monkeypatch):
+    """8-bit affine weights run on the tcgen05 skinny GEMM by default; SD_ROWS_GEMM=skinny
+    selects the mma.sync one (the other formats always take it)."""
+    if request.param == "skinny":
+        monkeypatch.setenv("SD_ROWS_GEMM", "skinny")
+    else:
+        monkeypatch.delenv("SD_ROWS_GEMM", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
 @pytest.mark.parametrize("kind,shape", G16_SHAPES)
-def test_gemm16_linear_bias(sd, kind, shape, M):
+def test_gemm16_linear_bias(sd, kind, shape, M, g16_path):
     """The skinny split-K GEMM: row counts up to 16 (one or both MMA row halves),
     ragged column tiles (200, 130 rows), K ranges that are and are not multiples
     of 64, one split (K = 32) up to many."""
@@ -206,7 +217,7 @@ def test_gemm16_linear_bias(sd, kind, shape, M):
 
 @pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
 @pytest.mark.parametrize("M", [5, 16])
-def test_gemm16_epilogues(sd, kind, M):
+def test_gemm16_epilogues(sd, kind, M, g16_path):
     cols = 1024 if kind != KA8 else 2048
     _run(sd, kind, 4096, cols, M, 1, True, False, 41 + M + kind, g16=True)
     _run(sd, kind, 1024, cols, M, 0, True, True, 42 + M + kind, g16=True)
