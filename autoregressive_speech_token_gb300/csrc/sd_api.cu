@@ -105,7 +105,7 @@ struct sd_ctx {
     float* nrm = nullptr;               // [B][max width] normalised rows (B > 2)
     float* g16_ws = nullptr;            // skinny GEMM partial sums (B > 2)
     int* g16_cnt = nullptr;             // skinny GEMM column-tile counters (zero between launches)
-    bool rows_gemm_tc = false;          // 3-16 rows, affine weights: the tcgen05 skinny GEMM (SD_ROWS_GEMM unset)
+    bool rows_gemm_tc = false;          // SD_ROWS_GEMM=tc: 3-16 rows with affine weights on the tcgen05 skinny GEMM
     bool rows_gemm_mma = false;         // SD_ROWS_GEMM=mma: the 64x64 mma.sync GEMM for > 2 rows instead
     int32_t* prompt = nullptr;          // [B][max_ctx]
 
@@ -1155,7 +1155,7 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     if (c->B > 2) {
         const char* rg = getenv("SD_ROWS_GEMM");
         c->rows_gemm_mma = rg && strcmp(rg, "mma") == 0;
-        c->rows_gemm_tc = !rg;  // SD_ROWS_GEMM=skinny: the mma.sync skinny GEMM for every format
+        c->rows_gemm_tc = rg && strcmp(rg, "tc") == 0;  // default: the mma.sync skinny GEMM (faster, measured)
         // skinny GEMM workspace: the largest partial-sum array and tile count over every matrix
         std::vector<std::pair<int, int>> nk;  // (rows, cols)
         auto stack_mats = [&](int d, int H, int Hkv, int hd, int ff, bool gpt2) {
@@ -1588,7 +1588,8 @@ int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, 
     CK(cudaSetDevice(m->device));
     int sms = 0;
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, m->device));
-    const bool tc = gemm16_tc_supported(m->m) && !getenv("SD_ROWS_GEMM");
+    const char* rg = getenv("SD_ROWS_GEMM");
+    const bool tc = gemm16_tc_supported(m->m) && rg && strcmp(rg, "tc") == 0;
     if (!m->g16_ws) {
         size_t wsf = gemm16_ws_floats(m->m.rows, m->m.cols, sms);
         if (gemm16_tc_supported(m->m)) wsf = std::max(wsf, gemm16_tc_ws_floats(m->m.rows, m->m.cols, sms));

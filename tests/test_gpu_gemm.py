@@ -196,10 +196,10 @@ G16_SHAPES = [(KQ8, (3072, 1024)), (KQ8, (200, 96)), (KQ8, (64, 32)), (KQ8, (102
 
 @pytest.fixture(params=["tc", "skinny"])
 def g16_path(request, monkeypatch):
-    """8-bit affine weights run on the tcgen05 skinny GEMM by default; SD_ROWS_GEMM=skinny
-    selects the mma.sync one (the other formats always take it)."""
-    if request.param == "skinny":
-        monkeypatch.setenv("SD_ROWS_GEMM", "skinny")
+    """The mma.sync skinny GEMM (default), and with SD_ROWS_GEMM=tc the tcgen05 one for
+    8-bit affine weights (the other formats always take the mma.sync kernel)."""
+    if request.param == "tc":
+        monkeypatch.setenv("SD_ROWS_GEMM", "tc")
     else:
         monkeypatch.delenv("SD_ROWS_GEMM", raising=False)
     return request.param

@@ -477,7 +477,17 @@ def test_qwen_full_size(sd):
     _check_qwen(sd, run.model, prompt_tokens(run), 16, run.sampler, "qwen_a8")
 
 
-def test_qwen_g16_small(sd, prefill_path):
+@pytest.fixture(params=["skinny", "tc"])
+def rows_gemm(request, monkeypatch):
+    """The 3-16 row GEMM: mma.sync skinny (default) or tcgen05 (SD_ROWS_GEMM=tc)."""
+    if request.param == "tc":
+        monkeypatch.setenv("SD_ROWS_GEMM", "tc")
+    else:
+        monkeypatch.delenv("SD_ROWS_GEMM", raising=False)
+    return request.param
+
+
+def test_qwen_g16_small(sd, prefill_path, rows_gemm):
     """Sixteen rollout rows (the G=16 configuration's batch) through the
     norm-kernel + tensor-core GEMM path that replaces the 1-2 row GEMV."""
     spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
