@@ -1354,10 +1354,13 @@ int cstep_plan(CStepArgs& a, int sm_count) {
     // hold the same number of clusters of a size); the most CTAs that can be resident wins,
     // then the most clusters (fewer heads per cluster)
     std::vector<std::pair<int, int>> cand;
+    // SD_CLUSTERS / SD_CLUSTER_SIZE restrict the candidates (measurement of other shapes)
+    const int want_ncl = getenv("SD_CLUSTERS") ? atoi(getenv("SD_CLUSTERS")) : 0;
+    const int want_cs = getenv("SD_CLUSTER_SIZE") ? atoi(getenv("SD_CLUSTER_SIZE")) : 0;
     for (int ncl = a.Hkv; ncl >= 1; --ncl)
-        if (a.Hkv % ncl == 0)
+        if (a.Hkv % ncl == 0 && (!want_ncl || ncl == want_ncl))
             for (int cs = 16; cs >= 2; --cs)
-                if (ncl * cs <= sm_count) cand.push_back({ncl, cs});
+                if (ncl * cs <= sm_count && (!want_cs || cs == want_cs)) cand.push_back({ncl, cs});
     std::stable_sort(cand.begin(), cand.end(), [](const std::pair<int, int>& x, const std::pair<int, int>& y) {
         const int gx = x.first * x.second, gy = y.first * y.second;
         return gx != gy ? gx > gy : x.first > y.first;

@@ -23,9 +23,9 @@
 //   - all threads turn a landed group into fp16 codes in the 128-byte swizzled
 //     K-major layout the MMA reads (16-byte chunk c of row r at chunk c ^ (r & 7)
 //     of its 128-byte row, 8-row atoms 1024 bytes apart: the layout a TMA load
-//     with 128-byte swizzle writes), double buffered;
+//     with 128-byte swizzle writes), in a ring of kAStages buffers;
 //   - thread 0 issues the group's eight MMAs and commits them to an mbarrier
-//     that frees the buffer two groups later.
+//     that frees the buffer kAStages groups later.
 // The activations of the K range (fp16 hi/lo in the same layout), their group
 // sums and the rows' scales and biases are staged once.  Partial sums go to a
 // workspace [split][16][N]; the last CTA of each column tile adds the splits in
@@ -48,6 +48,7 @@ constexpr int kRows = 128;            // weight rows per CTA (the MMA's M)
 constexpr int kG = 64;                // affine group width = one 128-byte swizzled row of fp16
 constexpr int kMaxGroups = 16;        // K range per CTA <= 1024
 constexpr int kRaw = 6;               // raw code groups in flight
+constexpr int kAStages = 4;           // converted groups the MMAs may still be reading
 constexpr int kThreads = 128;
 constexpr int kTmemCols = 256;        // 16 columns per group, 16 groups
 constexpr int kErrTimeout = 6;
@@ -59,7 +60,7 @@ constexpr int kXBytes = 16 * kG * 2;          // 2 KB: 16 activation rows of a g
 // shared memory: [x hi | x lo] per group, two A buffers, the raw ring, then scales / biases / sums
 constexpr size_t kOffX = 0;
 constexpr size_t kOffA = kOffX + (size_t)kMaxGroups * 2 * kXBytes;
-constexpr size_t kOffRaw = kOffA + 2 * (size_t)kABytes;
+constexpr size_t kOffRaw = kOffA + (size_t)kAStages * kABytes;
 constexpr size_t kOffSc = kOffRaw + (size_t)kRaw * kRawBytes;
 constexpr size_t kOffBi = kOffSc + (size_t)kMaxGroups * kRows * 4;
 constexpr size_t kOffXs = kOffBi + (size_t)kMaxGroups * kRows * 4;
@@ -146,7 +147,7 @@ __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 __global__ void __launch_bounds__(kThreads, 1) k_gemm16_tc(const __grid_constant__ Gemm16TcArgs a) {
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    __shared__ __align__(8) unsigned long long s_full[kRaw], s_done[2];
+    __shared__ __align__(8) unsigned long long s_full[kRaw], s_done[kAStages];
     __shared__ uint32_t s_tmem;
     __shared__ int s_ok, s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,8 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm16_tc(const __grid_constant
     }
     if (tid == 0) {
         for (int s = 0; s < kRaw; ++s) mb_init(smem_u32(&s_full[s]));
-        mb_init(smem_u32(&s_done[0]));
-        mb_init(smem_u32(&s_done[1]));
+        for (int s = 0; s < kAStages; ++s) mb_init(smem_u32(&s_done[s]));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ok = 1;
     }
@@ -239,10 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm16_tc(const __grid_constant
     bool ok = true;
     int qstop = ng;  // groups whose MMAs were issued
     for (int q = 0; q < ng && ok; ++q) {
-        const int slot = q % kRaw, st = q & 1;
-        // the raw group has landed, and the MMAs that read this A buffer two groups ago are done
+        const int slot = q % kRaw, st = q % kAStages;
+        // the raw group has landed, and the MMAs that read this A buffer kAStages groups ago are done
         bool w = mb_wait(smem_u32(&s_full[slot]), (uint32_t)((q / kRaw) & 1), a.budget);
-        if (w && q >= 2) w = mb_wait(smem_u32(&s_done[st]), (uint32_t)(((q - 2) >> 1) & 1), a.budget);
+        if (w && q >= kAStages)
+            w = mb_wait(smem_u32(&s_done[st]), (uint32_t)(((q - kAStages) / kAStages) & 1), a.budget);
         if (!__syncthreads_and(w)) {
             ok = false;
             qstop = q;
@@ -279,14 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm16_tc(const __grid_constant
     }
     // the last group's commit covers every MMA before it
     if (tid == 0) {
-        const bool w = ok && mb_wait(smem_u32(&s_done[(ng - 1) & 1]), (uint32_t)(((ng - 1) >> 1) & 1), a.budget);
+        const bool w =
+            ok && mb_wait(smem_u32(&s_done[(ng - 1) % kAStages]), (uint32_t)(((ng - 1) / kAStages) & 1), a.budget);
         if (!w) {
             s_ok = 0;
             if (a.err) atomicCAS(a.err, 0, kErrTimeout);
             // bounded drain of this CTA's copies and MMAs still in flight
             for (int q = qstop; q < issued; ++q)
                 mb_wait(smem_u32(&s_full[q % kRaw]), (uint32_t)((q / kRaw) & 1), a.budget);
-            if (qstop > 0) mb_wait(smem_u32(&s_done[(qstop - 1) & 1]), (uint32_t)(((qstop - 1) >> 1) & 1), a.budget);
+            if (qstop > 0)
+                mb_wait(smem_u32(&s_done[(qstop - 1) % kAStages]), (uint32_t)(((qstop - 1) / kAStages) & 1), a.budget);
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
