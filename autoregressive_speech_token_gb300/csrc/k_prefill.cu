@@ -119,66 +119,119 @@ __global__ void k_rope_kv(float* __restrict__ QKV, int ld, int p0, int np, int H
     }
 }
 
-// Causal attention for the query at position p = p0 + i of row b, head h
-// (one warp): keys 0..p from the fp16 cache, online softmax over chunks of 32
-// keys (lane j scores key j0 + j), DPL = head_dim / 32 dimensions per lane.
+// Causal attention over the prompt chunk: queries at positions p0 .. p0 + np - 1
+// of row b, head h, against keys 0..p of the fp16 cache (the chunk's own keys
+// were appended by k_rope_kv).  A CTA takes kQC queries of one (row, head);
+// each of its four warps takes every fourth query.  The keys and values of a
+// block of kKB positions are staged once in shared memory for all kQC queries
+// (key rows at a pitch of hd + 8 halves, so lane j reading row j is free of
+// bank conflicts); lane j scores key j of a 32-key sub-block with a full dot
+// product (no shuffles per key), the sub-block updates an online softmax, and
+// p.V accumulates with lanes over dimensions (DPL = head_dim / 32 per lane).
+constexpr int kQC = 16, kKB = 64;
+
 template <int DPL>
 __global__ void __launch_bounds__(128) k_prefill_attn(const float* __restrict__ QKV, int ld, int p0, int np, int H,
                                                       int Hkv, int n_ctx, int row_heads, int head_off,
                                                       const __half* __restrict__ kc, const __half* __restrict__ vc,
                                                       float* __restrict__ O, int ldo) {
-    constexpr int hd = 32 * DPL;
-    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (wid >= np * H) return;
-    const int b = blockIdx.y;
-    const int h = wid % H, i = wid / H, m = b * np + i, p = p0 + i;
+    constexpr int hd = 32 * DPL, KP = hd + 8, NQ = kQC / 4;
+    __shared__ __align__(16) __half Ks[kKB * KP];
+    __shared__ __align__(16) __half Vs[kKB * hd];
+    __shared__ __align__(16) float Qs[kQC * hd];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = blockIdx.x * kQC, h = blockIdx.y, b = blockIdx.z;
     const int g = h / (H / Hkv);
-    const float* q = QKV + (size_t)m * ld + h * hd;
+    const int nq = min(kQC, np - c0);            // queries of this CTA
+    const int p_last = p0 + c0 + nq - 1;         // the chunk's last position
     const __half* K = kc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
     const __half* Vv = vc + ((size_t)(b * row_heads + head_off + g) * n_ctx) * hd;
     const float scale = 1.0f / sqrtf((float)hd);
-    float qv[DPL], acc[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-        qv[e] = q[lane * DPL + e] * scale;
-        acc[e] = 0.f;
+    for (int i = threadIdx.x; i < nq * hd; i += blockDim.x) {
+        const int qi = i / hd, e = i - qi * hd;
+        Qs[qi * hd + e] = QKV[(size_t)(b * np + c0 + qi) * ld + h * hd + e] * scale;
     }
-    float mrun = -INFINITY, lrun = 0.f;
-    for (int j0 = 0; j0 <= p; j0 += 32) {
-        const int n = min(32, p + 1 - j0);
-        float sj = -INFINITY;
-        for (int j = 0; j < n; ++j) {
-            const __half* kr = K + (size_t)(j0 + j) * hd + lane * DPL;
-            float s = 0.f;
+    float m[NQ], l[NQ], acc[NQ][DPL];
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) s = fmaf(qv[e], __half2float(kr[e]), s);
+    for (int t = 0; t < NQ; ++t) {
+        m[t] = -INFINITY;
+        l[t] = 0.f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == j) sj = s;
+        for (int e = 0; e < DPL; ++e) acc[t][e] = 0.f;
+    }
+    for (int kb0 = 0; kb0 <= p_last; kb0 += kKB) {
+        const int nk = min(kKB, p_last + 1 - kb0);
+        __syncthreads();  // every warp is done with the previous block (and Qs is written)
+        for (int i = threadIdx.x; i < nk * (hd / 8); i += blockDim.x) {
+            const int j = i / (hd / 8), c = i - j * (hd / 8);
+            *reinterpret_cast<uint4*>(Ks + j * KP + 8 * c) = *reinterpret_cast<const uint4*>(K + (size_t)(kb0 + j) * hd + 8 * c);
+            *reinterpret_cast<uint4*>(Vs + j * hd + 8 * c) = *reinterpret_cast<const uint4*>(Vv + (size_t)(kb0 + j) * hd + 8 * c);
         }
-        float cm = sj;
+        __syncthreads();
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-        const float mnew = fmaxf(mrun, cm);
-        const float corr = expf(mrun - mnew);
-        const float pj = lane < n ? expf(sj - mnew) : 0.f;
-        float ps = pj;
+        for (int t = 0; t < NQ; ++t) {
+            const int qi = warp + 4 * t;
+            if (qi >= nq) continue;
+            const int p = p0 + c0 + qi;
+            const float* q = Qs + qi * hd;
+            for (int sb = 0; sb < nk && kb0 + sb <= p; sb += 32) {
+                const int j = sb + lane;                 // key kb0 + j of the block
+                const bool valid = j < nk && kb0 + j <= p;
+                float s = -INFINITY;
+                if (valid) {
+                    float d = 0.f;
+                    const __half* kr = Ks + j * KP;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        lrun = lrun * corr + ps;
+                    for (int c = 0; c < hd / 8; ++c) {
+                        const uint4 kw = *reinterpret_cast<const uint4*>(kr + 8 * c);
+                        const __half2* k2 = reinterpret_cast<const __half2*>(&kw);
+                        const float4 qa = *reinterpret_cast<const float4*>(q + 8 * c);
+                        const float4 qb = *reinterpret_cast<const float4*>(q + 8 * c + 4);
+                        const float2 f0 = __half22float2(k2[0]), f1 = __half22float2(k2[1]);
+                        const float2 f2 = __half22float2(k2[2]), f3 = __half22float2(k2[3]);
+                        d = fmaf(qa.x, f0.x, d); d = fmaf(qa.y, f0.y, d);
+                        d = fmaf(qa.z, f1.x, d); d = fmaf(qa.w, f1.y, d);
+                        d = fmaf(qb.x, f2.x, d); d = fmaf(qb.y, f2.y, d);
+                        d = fmaf(qb.z, f3.x, d); d = fmaf(qb.w, f3.y, d);
+                    }
+                    s = d;
+                }
+                float cm = s;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] *= corr;
-        for (int j = 0; j < n; ++j) {
-            const float pb = __shfl_sync(0xffffffffu, pj, j);
-            const __half* vr = Vv + (size_t)(j0 + j) * hd + lane * DPL;
+                for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+                const float mnew = fmaxf(m[t], cm);
+                const float corr = expf(m[t] - mnew);
+                const float pj = valid ? expf(s - mnew) : 0.f;
+                float ps = pj;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pb, __half2float(vr[e]), acc[e]);
+                for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                l[t] = l[t] * corr + ps;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[t][e] *= corr;
+                const int nv = min(32, min(nk - sb, p + 1 - (kb0 + sb)));  // valid keys of the sub-block
+                for (int jj = 0; jj < nv; ++jj) {
+                    const float pb = __shfl_sync(0xffffffffu, pj, jj);
+                    const __half* vr = Vs + (sb + jj) * hd + lane * DPL;
+                    if constexpr (DPL == 2) {
+                        const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(vr));
+                        acc[t][0] = fmaf(pb, v2.x, acc[t][0]);
+                        acc[t][1] = fmaf(pb, v2.y, acc[t][1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) acc[t][e] = fmaf(pb, __half2float(vr[e]), acc[t][e]);
+                    }
+                }
+                m[t] = mnew;
+            }
         }
-        mrun = mnew;
     }
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) O[(size_t)m * ldo + h * hd + lane * DPL + e] = acc[e] / lrun;
+    for (int t = 0; t < NQ; ++t) {
+        const int qi = warp + 4 * t;
+        if (qi >= nq) continue;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) O[(size_t)(b * np + c0 + qi) * ldo + h * hd + lane * DPL + e] = acc[t][e] / l[t];
+    }
 }
 
 }  // namespace
@@ -207,8 +260,8 @@ cudaError_t launch_rope_kv(float* QKV, int ld, int B, int p0, int np, int H, int
 cudaError_t launch_prefill_attn(const float* QKV, int ld, int B, int p0, int np, int H, int Hkv, int hd, int n_ctx,
                                 int row_heads, int head_off, const __half* kc, const __half* vc, float* O, int ldo,
                                 cudaStream_t st) {
-    if (H % Hkv || p0 < 0 || p0 + np > n_ctx) return cudaErrorInvalidValue;
-    const dim3 grid((np * H + 3) / 4, B);
+    if (H % Hkv || p0 < 0 || p0 + np > n_ctx || np < 1) return cudaErrorInvalidValue;
+    const dim3 grid((np + kQC - 1) / kQC, H, B);
     switch (hd) {
         case 64:
             k_prefill_attn<2><<<grid, 128, 0, st>>>(QKV, ld, p0, np, H, Hkv, n_ctx, row_heads, head_off, kc, vc, O, ldo);
