@@ -8,8 +8,9 @@
 //   z_i = c_i + w (c_i - u_i); seen i: z_i / penalty (z_i > 0) or z_i * penalty;
 //   z_i / T; p_i = exp(z_i - max z)
 //   min_p: keep p_i >= min(min_p, 1) (the largest probability is 1 here)
-//   the survivors sorted by (z desc, index asc) with a bitonic sort in shared
-//   memory; top-p: the shortest prefix whose renormalised mass reaches top_p;
+//   the survivors sorted by (z desc, index asc) with a bitonic sort of their
+//   indices in shared memory (each comparison reads the two values); top-p: the
+//   shortest prefix whose renormalised mass reaches top_p;
 //   top-k: the prefix entries whose value is >= the k-th (ties kept)
 //   draw: the smallest vocabulary index whose cumulative kept mass exceeds u
 //   times the kept total.
@@ -73,9 +74,8 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
                                                       float pen, float T, float min_p, float top_p, int top_k,
                                                       const uint8_t* seen, const float* u, int32_t* out) {
     extern __shared__ __align__(16) unsigned char lsm[];
-    double* key = reinterpret_cast<double*>(lsm);   // [NP] sort keys
-    double* zv = key + NP;                           // [V] ladder logits in vocabulary order
-    int* idx = reinterpret_cast<int*>(zv + V);       // [NP] vocabulary index of each key
+    double* zv = reinterpret_cast<double*>(lsm);     // [V] ladder logits in vocabulary order (-inf: cut by min_p)
+    int* idx = reinterpret_cast<int*>(zv + V);       // [NP] vocabulary index at each sorted position
     uint8_t* flag = reinterpret_cast<uint8_t*>(idx + NP);  // [V] kept after every stage
     __shared__ double dred[kW];
     __shared__ int ired[kW];
@@ -110,14 +110,13 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     }
     const double m = block_max_d(lm, dred);  // its barrier also publishes zv
     const double mp = min_p < 1.0f ? (double)min_p : 1.0;
-    // ---- min_p survivors as sort keys (the rest sort last as -inf)
+    // ---- min_p: the entries it cuts sort last as -inf (as do the positions past V)
     for (int j = tid; j < NP; j += kT) {
-        double k = -INFINITY;
-        if (j < V && (min_p <= 0.0f || exp(zv[j] - m) >= mp)) k = zv[j];
-        key[j] = k;
+        if (j < V && min_p > 0.0f && !(exp(zv[j] - m) >= mp)) zv[j] = -INFINITY;
         idx[j] = j;
     }
     __syncthreads();
+    auto key = [&](int t) -> double { return idx[t] < V ? zv[idx[t]] : -INFINITY; };
     // ---- bitonic sort: (z desc, index asc)
     for (int k = 2; k <= NP; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -125,9 +124,9 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
                 const int l = i ^ j;
                 if (l <= i) continue;
                 const bool up = (i & k) == 0;  // this pair's block sorts in the "before" order
-                const bool swap = up ? before(key[l], idx[l], key[i], idx[i]) : before(key[i], idx[i], key[l], idx[l]);
+                const double ki = key(i), kl = key(l);
+                const bool swap = up ? before(kl, idx[l], ki, idx[i]) : before(ki, idx[i], kl, idx[l]);
                 if (swap) {
-                    const double tk = key[i]; key[i] = key[l]; key[l] = tk;
                     const int ti = idx[i]; idx[i] = idx[l]; idx[l] = ti;
                 }
             }
@@ -139,7 +138,7 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     {
         int last = -1;
         for (int t = tid; t < NP; t += kT)
-            if (key[t] != -INFINITY) last = max(last, t);
+            if (key(t) != -INFINITY) last = max(last, t);
         ns = block_max_i(last, ired) + 1;
     }
     // ---- top-p over the survivors: contiguous segments per thread, prefix of masses
@@ -147,12 +146,12 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     if (top_p < 1.0f) {
         double loc = 0.0;
         for (int t = t0; t < t1; ++t)
-            if (t < ns) loc += exp(key[t] - m);
+            if (t < ns) loc += exp(key(t) - m);
         double mass;
         double run = block_excl_scan_d(loc, dred, &mass);
         int cut = 0x7fffffff;
         for (int t = t0; t < t1 && t < ns; ++t) {
-            run += exp(key[t] - m);
+            run += exp(key(t) - m);
             if (run / mass >= (double)top_p) { cut = t; break; }
         }
         cut = block_min_i(cut, ired);
@@ -160,10 +159,10 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     }
     // ---- top-k over those: the prefix entries whose value is >= the k-th
     if (top_k >= 1 && top_k < ns) {
-        const double thr = key[top_k - 1];
+        const double thr = key(top_k - 1);
         int last = -1;
         for (int t = tid; t < ns; t += kT)
-            if (key[t] >= thr) last = max(last, t);
+            if (key(t) >= thr) last = max(last, t);
         ns = block_max_i(last, ired) + 1;
     }
     // ---- kept flags in vocabulary order
@@ -192,12 +191,52 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     if (tid == 0) out[row] = tok;
 }
 
+// The decode step's ladder (one token for a conditional / unconditional row
+// pair): before it, the token this step consumed joins the history mask (the
+// tokens fed forward since the prompt; none in the prompt's own step) and row
+// 0's draw goes to the ladder's input slot; after it, the token goes to both
+// rows and to the step's output sequence.
+__global__ void k_ladder_prep(const float* u1, const float* const* u_seq, const int* step_idx, int rows, float* u,
+                              const int* prompt_on, const int32_t* tok, int V, uint8_t* seen) {
+    if (threadIdx.x != 0) return;
+    *u = *u_seq ? (*u_seq)[(size_t)(*step_idx) * rows] : u1[0];
+    const int t = tok[0];
+    if (!*prompt_on && t >= 0 && t < V) seen[t] = 1;
+}
+
+__global__ void k_ladder_commit(const int32_t* t_in, int32_t* tok, int rows, int V, int32_t* const* out_seq,
+                                const int* step_idx, int* err) {
+    if (threadIdx.x != 0) return;
+    int t = *t_in;
+    if (t < 0 || t >= V) {
+        atomicCAS(err, 0, 2);
+        t = 0;
+    }
+    for (int b = 0; b < rows; ++b) {
+        tok[b] = t;
+        if (*out_seq) (*out_seq)[(size_t)(*step_idx) * rows + b] = t;
+    }
+}
+
 }  // namespace ladder_detail
+
+cudaError_t launch_ladder_step(const float* logits, int ld, int rows, int V, const LadderParams& p, uint8_t* seen,
+                               const int* prompt_on, const float* u1, const float* const* u_seq, const int* step_idx,
+                               float* u_slot, int32_t* t_slot, int32_t* tok, int32_t* const* out_seq, int* err,
+                               cudaStream_t st) {
+    using namespace ladder_detail;
+    k_ladder_prep<<<1, 32, 0, st>>>(u1, u_seq, step_idx, rows, u_slot, prompt_on, tok, V, seen);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_sample_ladder(logits, logits + ld, 1, V, p, seen, u_slot, t_slot, st);
+    if (e != cudaSuccess) return e;
+    k_ladder_commit<<<1, 32, 0, st>>>(t_slot, tok, rows, V, out_seq, step_idx, err);
+    return cudaGetLastError();
+}
 
 size_t sample_ladder_smem_bytes(int V) {
     int NP = 1;
     while (NP < V) NP <<= 1;
-    return (size_t)NP * 8 + (size_t)V * 8 + (size_t)NP * 4 + (((size_t)V + 15) & ~(size_t)15);
+    return (size_t)V * 8 + (size_t)NP * 4 + (((size_t)V + 15) & ~(size_t)15);
 }
 
 cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int V, const LadderParams& p,

@@ -137,6 +137,11 @@ struct sd_ctx {
     int step_grid = 0;
     // cluster persistent step kernel (k_cstep.cu): preferred over the flat one where its plan fits
     bool cpersistent = false;
+    bool ladder_on = false;             // sd_set_ladder: one token per step for a cond / uncond row pair
+    LadderParams ladder;
+    uint8_t* seen = nullptr;            // [vocab] tokens generated since sd_prefill (ladder mode)
+    float* lad_u = nullptr;             // the ladder's draw slot
+    int32_t* lad_t = nullptr;           // the ladder's token slot
     long long test_stall = 0;           // test hook (SD_TEST_STALL_US): cycles for one wait of the next persistent launch
     CStepArgs cstep;
 };
@@ -513,7 +518,7 @@ enum class GraphKind { T3Step, T3Body, QwenFrame, QwenBody, QwenPromptLast };
 
 int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
     int rc;
-    if (k == GraphKind::T3Step && c->persistent) return enqueue_persistent(c, 1, nullptr, nullptr, st);
+    if (k == GraphKind::T3Step && c->persistent && !c->ladder_on) return enqueue_persistent(c, 1, nullptr, nullptr, st);
     const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
     if (k == GraphKind::QwenFrame) {
         EmbedSumArgs es;
@@ -533,7 +538,15 @@ int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
     if (k == GraphKind::T3Body || k == GraphKind::QwenBody)
         return advance(c, &c->ds->pos, 1, nullptr, 0, nullptr, 0, st);
     if ((rc = enqueue_head(c, c->main, c->head, 0, st))) return rc;
-    if ((rc = enqueue_sample(c, 0, 0, c->cfg.vocab, !qwen, st))) return rc;
+    if (c->ladder_on && !qwen) {
+        cudaError_t e = launch_ladder_step(c->logits, c->logits_ld, c->B, c->cfg.vocab, c->ladder, c->seen,
+                                           &c->ds->prompt_on, c->ds->u1, &c->ds->u_seq, &c->ds->step_idx, c->lad_u,
+                                           c->lad_t, c->ds->tok, &c->ds->out_seq, &c->ds->err, st);
+        c->count_launch += 3;
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "ladder launch: %s", cudaGetErrorString(e));
+    } else if ((rc = enqueue_sample(c, 0, 0, c->cfg.vocab, !qwen, st))) {
+        return rc;
+    }
     if (qwen && (rc = enqueue_cp_frame(c, st))) return rc;
     return advance(c, &c->ds->pos, 1, &c->ds->step_idx, 1, nullptr, 0, st);
 }
@@ -1289,6 +1302,35 @@ int sd_reset(sd_ctx* c) {
     return SD_OK;
 }
 
+int sd_set_ladder(sd_ctx* c, const sd_sampler_ladder* s) {
+    if (!c) return fail(nullptr, SD_ERR_INVALID_ARG, "sd_set_ladder: NULL context");
+    if (c->cfg.arch == SD_ARCH_QWEN_TTS || c->B != 2)
+        return fail(c, SD_ERR_UNSUPPORTED, "the ladder needs a GPT-2/Llama context with a conditional and an unconditional row");
+    if (c->phase != Phase::Loaded || c->host_pos != 0) return fail(c, SD_ERR_STATE, "sd_set_ladder needs a loaded, reset context");
+    if (c->cfg.vocab > 16384) return fail(c, SD_ERR_UNSUPPORTED, "the ladder takes at most 16384 logits");
+    if (s && (!(s->repetition_penalty > 0.f) || !(s->min_p >= 0.f) || !(s->top_p > 0.f && s->top_p <= 1.f) ||
+              !(s->temperature == s->temperature) || !(s->cfg_weight == s->cfg_weight)))
+        return fail(c, SD_ERR_INVALID_ARG, "sd_set_ladder: ladder out of range");
+    CK(cudaSetDevice(c->device));
+    int rc;
+    if (s && !c->seen) {
+        if ((rc = dalloc(c, &c->seen, (size_t)((c->cfg.vocab + 15) & ~15))) || (rc = dalloc(c, &c->lad_u, 16)) ||
+            (rc = dalloc(c, &c->lad_t, 16)))
+            return rc;
+    }
+    c->ladder_on = s != nullptr;
+    if (s) {
+        c->ladder.cfg_weight = s->cfg_weight; c->ladder.rep_penalty = s->repetition_penalty;
+        c->ladder.temperature = s->temperature; c->ladder.min_p = s->min_p; c->ladder.top_p = s->top_p;
+        c->ladder.top_k = s->top_k;
+    }
+    // the step graph takes the ladder (or the per-row sampler again)
+    CK(cudaStreamSynchronize(c->stream));
+    if (c->g_step) cudaGraphExecDestroy(c->g_step);
+    c->g_step = nullptr;
+    return capture(c, GraphKind::T3Step, &c->g_step, &c->kernels_per_step);
+}
+
 int sd_set_forced_codes(sd_ctx* c, const int32_t* codes) {
     if (!c) return fail(nullptr, SD_ERR_INVALID_ARG, "NULL context");
     if (c->cfg.arch != SD_ARCH_QWEN_TTS) return fail(c, SD_ERR_UNSUPPORTED, "forced codes need a Talker+CP model");
@@ -1334,6 +1376,7 @@ int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sa
     c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
     for (int b = 0; b < B; ++b) c->hs->tok[b] = tokens[(size_t)b * n + n - 1];  // read by the persistent step
     if ((rc = upload_inputs(c, qwen))) return rc;
+    if (c->ladder_on) CK(cudaMemsetAsync(c->seen, 0, (size_t)c->cfg.vocab, c->stream));
     if (c->gemm_prefill && n > 1) {
         if ((rc = enqueue_prefill_gemm(c, n - 1, c->stream))) return rc;
     } else {
@@ -1389,7 +1432,7 @@ int sd_decode_n(sd_ctx* c, int32_t n_steps, const sd_sampler* sampler, const flo
     c->hs->prompt_on = 0; c->hs->u_seq = u_dev; c->hs->out_seq = out_dev;
     if ((rc = upload_inputs(c, false))) return rc;
     CK(cudaMemsetAsync(&c->ds->step_idx, 0, sizeof(int32_t), c->stream));
-    if (c->persistent) {
+    if (c->persistent && !c->ladder_on) {
         if (n_steps > 0 && (rc = enqueue_persistent(c, n_steps, u_dev, out_dev, c->stream))) return rc;
     } else {
         for (int i = 0; i < n_steps; ++i) CK(cudaGraphLaunch(c->g_step, c->stream));
@@ -1398,7 +1441,7 @@ int sd_decode_n(sd_ctx* c, int32_t n_steps, const sd_sampler* sampler, const flo
     // later per-step calls upload null sequence pointers
     c->hs->u_seq = nullptr; c->hs->out_seq = nullptr;
     if (rc) return rc;
-    if (c->persistent) write_trace(c, n_steps);
+    if (c->persistent && !c->ladder_on) write_trace(c, n_steps);
     c->host_pos += n_steps;
     return SD_OK;
 }
@@ -1678,7 +1721,7 @@ int sd_sample_rows_ladder(const float* logits_cond_dev, const float* logits_unco
                           const sd_sampler_ladder* s, const uint8_t* seen_dev, const float* u_dev, int32_t* out_dev,
                           void* stream) {
     sd_ctx* c = nullptr;
-    if (!logits_cond_dev || !s || !u_dev || !out_dev || rows < 1 || rows > 65535 || V < 1 || V > 8192)
+    if (!logits_cond_dev || !s || !u_dev || !out_dev || rows < 1 || rows > 65535 || V < 1 || V > 16384)
         return fail(c, SD_ERR_INVALID_ARG, "sd_sample_rows_ladder: bad argument");
     if (!(s->repetition_penalty > 0.f) || !(s->min_p >= 0.f) || !(s->top_p > 0.f && s->top_p <= 1.f) ||
         !(s->temperature == s->temperature) || !(s->cfg_weight == s->cfg_weight))

@@ -25,7 +25,7 @@ ERRORS = {-1: "SD_ERR_INVALID_ARG", -2: "SD_ERR_STATE", -3: "SD_ERR_CTX_FULL", -
 MAX_CODEBOOKS = 16
 
 # every symbol the headers declare
-EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes",
+EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes", "sd_set_ladder",
            "sd_decode_n", "sd_get_logits", "sd_reset", "sd_destroy", "sd_last_error", "sd_get_info",
            "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm16", "sd_qmat_gemm_tc", "sd_sample_rows", "sd_sample_rows_ladder",
            "sd_attend_rows", "sd_attend_rows_static"]
@@ -64,6 +64,10 @@ class SamplerLadder(C.Structure):
     _fields_ = [("cfg_weight", C.c_float), ("repetition_penalty", C.c_float), ("temperature", C.c_float),
                 ("min_p", C.c_float), ("top_p", C.c_float), ("top_k", C.c_int32)]
 
+    @classmethod
+    def from_spec(cls, spec) -> "SamplerLadder":
+        return cls(spec.cfg_weight, spec.rep_penalty, spec.temperature, spec.min_p, spec.top_p, spec.top_k)
+
 
 class Info(C.Structure):
     _fields_ = [("pos", C.c_int32), ("sm_count", C.c_int32), ("kernels_per_step", C.c_int32),
@@ -93,6 +97,7 @@ def load_library(path: str | None = None):
         "sd_step": ([vp, i32p, C.POINTER(Sampler), f32p, i32p], C.c_int),
         "sd_frame": ([vp, i32p, C.POINTER(Sampler), C.POINTER(Sampler), f32p, i32p], C.c_int),
         "sd_set_forced_codes": ([vp, i32p], C.c_int),
+        "sd_set_ladder": ([vp, C.POINTER(SamplerLadder)], C.c_int),
         "sd_decode_n": ([vp, i32, C.POINTER(Sampler), vp, vp], C.c_int),
         "sd_get_logits": ([vp, f32p, C.c_size_t], C.c_int),
         "sd_reset": ([vp], C.c_int),
@@ -201,6 +206,12 @@ def sd_set_forced_codes(ctx: int, codes) -> None:
     full = np.zeros((B, MAX_CODEBOOKS), np.int32)
     full[:, :ncb] = c
     _check(L.sd_set_forced_codes(ctx, _p(full, C.c_int32)), ctx)
+
+
+def sd_set_ladder(ctx: int, ladder) -> None:
+    """sd_set_ladder: a SamplerLadder (one token per step for the cond / uncond row pair), or None."""
+    L = load_library()
+    _check(L.sd_set_ladder(ctx, C.byref(ladder) if ladder is not None else None), ctx)
 
 
 def sd_decode_n(ctx: int, n_steps: int, sampler: Sampler, u_dev, out_dev) -> None:
@@ -343,6 +354,9 @@ class Decoder:
 
     def force(self, codes):
         sd_set_forced_codes(self.ctx, codes)
+
+    def set_ladder(self, ladder):
+        sd_set_ladder(self.ctx, ladder)
 
     def decode_n(self, n, sampler, u_dev, out_dev):
         sd_decode_n(self.ctx, n, sampler, u_dev, out_dev)

@@ -89,6 +89,19 @@ typedef struct sd_sampler {
     float rep_penalty;
 } sd_sampler;
 
+/* Parameters of the multilingual T3's sampler ladder ("Chatterbox -> ggml Port:
+ * Development Journal", section 3.19, "Sampling path"): classifier-free-guidance
+ * combine -> repetition penalty -> temperature -> min_p -> top-p -> top-k -> draw
+ * in vocabulary order (sd_set_ladder here, sd_sample_rows_ladder in sd_ops.h). */
+typedef struct sd_sampler_ladder {
+    float cfg_weight;          /* guidance weight w: z = c + w (c - u); 0 = conditional logits only */
+    float repetition_penalty;  /* > 0; 1 = off */
+    float temperature;         /* <= 0: argmax of the combined, penalised logits */
+    float min_p;               /* keep p >= min_p * max p; 0 = off (values above 1 act as 1) */
+    float top_p;               /* (0, 1]; 1 = off */
+    int32_t top_k;             /* < 1 or >= the survivors: off */
+} sd_sampler_ladder;
+
 typedef struct sd_ctx sd_ctx;
 
 /* Create a context on CUDA device `device` (journal section 3.2: the prompt
@@ -135,6 +148,21 @@ int sd_step(sd_ctx* ctx, const int32_t* tok, const sd_sampler* sampler, const fl
  * u[row][j] feed code j.  Output codes_out[row][16]. */
 int sd_frame(sd_ctx* ctx, const int32_t* codes_in, const sd_sampler* talker, const sd_sampler* cp,
              const float* u, int32_t* codes_out);
+
+/* The multilingual T3's guided decode (journal section 3.19, "Sampling path",
+ * and section 3.21: the conditional and the unconditional sequence decoded as
+ * two rows of one step).  For a GPT-2/Llama context of batch 2 -- row 0 the
+ * conditional, row 1 the unconditional sequence -- a non-NULL ladder makes
+ * every sd_prefill / sd_step / sd_decode_n step draw ONE token: the ladder above
+ * on row 0's and row 1's logits, the repetition penalty over the tokens drawn
+ * since the last sd_prefill (a device-side mask), with row 0's draw; the token
+ * is returned for, and fed to, both rows.  The sampler argument of those calls
+ * is then only checked.  The steps run on the per-operation step graph (the
+ * persistent kernels do not implement the ladder).  NULL restores per-row
+ * sampling.  Needs a loaded or reset context (position 0) and vocab <= 16384;
+ * SD_ERR_UNSUPPORTED for other models or batch sizes, SD_ERR_INVALID_ARG for
+ * a ladder out of range. */
+int sd_set_ladder(sd_ctx* ctx, const sd_sampler_ladder* ladder);
 
 /* Teacher forcing (a test aid for the parity of "Every Frame Is a Memory
  * Read", section 1's frame) for the next sd_prefill/sd_frame of a Qwen context: within

@@ -90,15 +90,7 @@ int sd_qmat_gemm16(sd_qmat* m, const float* x_dev, int32_t M, int32_t epilogue, 
 int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sampler* sampler,
                    const float* u_dev, int32_t* out_dev, void* stream);
 
-/* Parameters of the sampler ladder (sd_sample_rows_ladder). */
-typedef struct sd_sampler_ladder {
-    float cfg_weight;          /* guidance weight w: z = c + w (c - u); 0 = conditional logits only */
-    float repetition_penalty;  /* > 0; 1 = off */
-    float temperature;         /* <= 0: argmax of the combined, penalised logits */
-    float min_p;               /* keep p >= min_p * max p; 0 = off (values above 1 act as 1) */
-    float top_p;               /* (0, 1]; 1 = off */
-    int32_t top_k;             /* < 1 or >= the survivors: off */
-} sd_sampler_ladder;
+/* (sd_sampler_ladder, the ladder's parameters, is declared in sd.h.) */
 
 /* Sampler ladder of the multilingual T3 ("Chatterbox -> ggml Port: Development
  * Journal", the multilingual port's sampling path): classifier-free-guidance
@@ -112,7 +104,7 @@ typedef struct sd_sampler_ladder {
  *   k-th largest remaining (ties kept); the token is the smallest vocabulary
  *   index whose cumulative kept mass exceeds u_dev[b] times the kept total.
  * Layouts: logits [rows][V] fp32, seen [rows][V] bytes, u [rows], out [rows] int32;
- * device pointers; 1 <= V <= 8192.  Double-precision arithmetic, one CTA per row.
+ * device pointers; 1 <= V <= 16384.  Double-precision arithmetic, one CTA per row.
  * This entry is an op-level form of the ladder: the decode step's own sampler
  * is temperature -> top-k -> top-p (sd.h).  Synchronises `stream`; returns
  * SD_ERR_INVALID_ARG on a NULL required pointer or a parameter out of range. */

@@ -343,6 +343,45 @@ def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: i
     return traces
 
 
+def run_t3_cfg(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: int, ladder,
+               forced=None) -> Trace:
+    """The multilingual T3 with classifier-free guidance: row 0 reads the
+    conditional prompt, row 1 the unconditional one (same length), and both rows
+    are fed the one token that the sampler ladder picks from the two rows' logits
+    ("Multilingual (Llama-520M) variant", sampling path: the cond and uncond
+    forwards are combined at the logit level).
+
+    prompt [2][P]; draws [n_steps+1] (draw 0 samples the prefill's token);
+    ladder holds cfg_weight, rep_penalty, temperature, min_p, top_p, top_k.  The
+    repetition penalty's history is the tokens fed forward since the prompt (the
+    prompt's own tokens are not in it): step i's ladder sees the tokens fed at
+    steps 1..i.  With teacher forcing, forced[i-1] is fed at step i instead of
+    the sampled token (and joins the history).  Returns one Trace whose logits
+    are (conditional, unconditional) pairs."""
+    V = spec.vocab
+    assert prompt.shape[0] == 2
+    zs = []
+    for b in range(2):
+        z = None
+        for i, tok in enumerate(prompt[b]):
+            z = model.token_forward(b, int(tok), V, want_logits=(i == prompt.shape[1] - 1))
+        zs.append(z)
+    seen = np.zeros(V, np.uint8)
+    tr = Trace()
+    for i in range(n_steps + 1):
+        tok, margin = sample_ladder(zs[0], zs[1], ladder.cfg_weight, seen, ladder.rep_penalty,
+                                    ladder.temperature, ladder.min_p, ladder.top_p, ladder.top_k,
+                                    u=float(draws[i]))
+        tr.tokens.append(tok)
+        tr.margins.append(margin)
+        tr.logits.append((zs[0], zs[1]))
+        if i < n_steps:
+            feed = tok if forced is None else int(forced[i])
+            seen[feed] = 1
+            zs = [model.token_forward(b, feed, V) for b in range(2)]
+    return tr
+
+
 def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames: int, talker_sampler,
              cp_sampler, keep_logits=True, forced=None) -> list:
     """Talker + code predictor: prompt then frames per row.

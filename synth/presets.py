@@ -132,6 +132,24 @@ QWEN_SAMPLED = SamplerSpec(temperature=0.9, top_k=50, top_p=0.95, greedy=False)
 
 
 @dataclass(frozen=True)
+class LadderSpec:
+    """The multilingual T3's sampler ladder settings (CFG combine, repetition
+    penalty, temperature, min_p, top-p, top-k)."""
+    cfg_weight: float = 0.5
+    rep_penalty: float = 2.0
+    temperature: float = 0.8
+    min_p: float = 0.05
+    top_p: float = 1.0
+    top_k: int = 1000
+
+
+# The multilingual variant's sampling path names the stages but prints no
+# values: a representative setting (guidance 0.5, penalty 2, T 0.8, min_p 0.05,
+# top-p off, top-k 1000).
+MTL_LADDER = LadderSpec()
+
+
+@dataclass(frozen=True)
 class RunSpec:
     name: str
     model: ModelSpec

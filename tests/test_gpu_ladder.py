@@ -1,7 +1,7 @@
 """Parity of the device sampler ladder (sd_sample_rows_ladder) with the
 oracle's ladder on the same logits: CFG combine, repetition penalty,
 temperature, min_p, top-p, top-k and the index-order draw, over vocabulary
-sizes from 16 to 8192, random histories and draws, the greedy path, ties at
+sizes from 16 to 16384, random histories and draws, the greedy path, ties at
 the thresholds, and argument checks.  Both sides compute in double precision,
 so tokens must agree except where the draw lies within 1e-9 of a CDF edge."""
 
@@ -63,7 +63,7 @@ COMBOS = [(0.0, 1.0, 1.0, 0.0, 1.0, 0), (0.5, 1.3, 0.8, 0.05, 0.9, 8), (1.0, 1.0
           (-0.5, 2.0, 1.2, 0.2, 0.7, 3), (0.0, 1.0, 0.7, 0.3, 1.0, 0), (2.0, 1.5, 1.0, 0.01, 0.8, 1000)]
 
 
-@pytest.mark.parametrize("V", [16, 2048, 3072, 6563, 8192])
+@pytest.mark.parametrize("V", [16, 2048, 3072, 6563, 8192, 8194, 16384])
 def test_ladder_matches_oracle(sd, V):
     rng = np.random.default_rng(V)
     rows = 4
@@ -102,9 +102,9 @@ def test_ladder_rejects_bad_arguments(sd):
     u = torch.zeros(2, device="cuda")
     out = torch.zeros(2, dtype=torch.int32, device="cuda")
     st = torch.cuda.current_stream().cuda_stream
-    big = torch.zeros(1, 8193, device="cuda")
+    big = torch.zeros(1, 16385, device="cuda")
     with pytest.raises(sd.SdError):
-        sd.sd_sample_rows_ladder(big, None, 1, 8193, sd.SamplerLadder(0, 1, 1, 0, 1, 0), None, u, out, st)
+        sd.sd_sample_rows_ladder(big, None, 1, 16385, sd.SamplerLadder(0, 1, 1, 0, 1, 0), None, u, out, st)
     for bad in [sd.SamplerLadder(0, 1, 1, 0, 0.0, 0), sd.SamplerLadder(0, 0.0, 1, 0, 1, 0),
                 sd.SamplerLadder(0, 1, 1, -0.5, 1, 0)]:
         with pytest.raises(sd.SdError):

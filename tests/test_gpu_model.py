@@ -94,8 +94,8 @@ class _Tally:
         self.total = self.strict = self.derived = 0
         self.strict_bad, self.derived_bad = [], []
 
-    def add(self, where, got, want, margin, z_dev, z_ref):
-        d = _logit_error(z_dev, z_ref)
+    def add(self, where, got, want, margin, z_dev, z_ref, d=None):
+        d = _logit_error(z_dev, z_ref) if d is None else d
         self.total += 1
         if margin >= MARGIN:
             self.strict += 1
@@ -237,6 +237,127 @@ def test_bench_configuration_gpt2m_q4(sd):
         tally.add((i, 0), toks[i], ref.tokens[i], ref.margins[i], zs[i], ref.logits[i])
     print(f"[{name}] worst logits rel L2 {worst:.2e}")
     tally.check()
+
+
+def _check_cfg(sd, spec, prompt, n_steps, lad, name, draw_seed=3):
+    """The multilingual T3 with guidance through sd_set_ladder: row 0 conditional,
+    row 1 unconditional, one token per step fed to both rows, teacher-forced with
+    the oracle's tokens.  Per step: both rows' logits within REL_L2 of the
+    oracle's; the device ladder picks what the oracle's ladder picks on the
+    device's own logits (same history, margin >= SAMPLER_MARGIN); the token
+    against the oracle's under _Tally's rules, d being the largest change of the
+    ladder's tempered input that the two rows' logit errors allow
+    (guidance mixes them with weights 1+w and w, the penalty scales by at most
+    its factor)."""
+    blob = _blob(spec)
+    draws = uniform_draws(draw_seed, n_steps + 1, 2)[..., 0]
+    ref = oracle.run_t3_cfg(oracle.Model(blob, THREADS), spec, prompt, draws[:, 0], n_steps, lad)
+    dec = sd.Decoder(spec, blob, stream=_stream())
+    dec.set_ladder(sd.SamplerLadder.from_spec(lad))
+    s = sd.Sampler.from_spec(P.T3_SAMPLED)     # per-row sampler: not used while the ladder is set
+    got = dec.prefill(prompt, s, draws[0])
+    as_sampler = SamplerSpec(temperature=lad.temperature, top_k=lad.top_k, top_p=lad.top_p,
+                             greedy=lad.temperature <= 0)
+    tally = _Tally(name, as_sampler)
+    w = abs(lad.cfg_weight)
+    seen = np.zeros(spec.vocab, np.uint8)
+    worst = 0.0
+    for i in range(n_steps + 1):
+        z = dec.logits()
+        assert int(got[0]) == int(got[1]), (i, got)
+        for b in range(2):
+            r = _rel(z[b], ref.logits[i][b])
+            worst = max(worst, r)
+            assert r <= REL_L2, (i, b, r)
+        tg, mg = oracle.sample_ladder(z[0], z[1], lad.cfg_weight, seen, lad.rep_penalty, lad.temperature,
+                                      lad.min_p, lad.top_p, lad.top_k, u=float(draws[i][0]))
+        if mg >= SAMPLER_MARGIN:
+            assert int(got[0]) == tg, ("ladder", i, int(got[0]), tg, mg)
+        d = max(lad.rep_penalty, 1.0) * ((1 + w) * _logit_error(z[0], ref.logits[i][0]) +
+                                         w * _logit_error(z[1], ref.logits[i][1]))
+        tally.add(i, int(got[0]), ref.tokens[i], ref.margins[i], None, None, d=d)
+        if i < n_steps:
+            t = ref.tokens[i]
+            seen[t] = 1
+            got = dec.step(np.array([t, t], np.int32), s, draws[i + 1])
+    dec.close()
+    print(f"[{name}] worst logits rel L2 {worst:.2e}")
+    tally.check()
+
+
+def test_cfg_ladder_small_llama(sd):
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=3, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q4_0)
+    prompt = np.random.default_rng(4).integers(0, 1000, size=(2, 40)).astype(np.int32)
+    _check_cfg(sd, spec, prompt, 80, P.MTL_LADDER, "cfg ladder llama-small q4")
+    greedy = dataclasses.replace(P.MTL_LADDER, temperature=0.0, top_k=1)
+    _check_cfg(sd, spec, prompt, 40, greedy, "cfg ladder llama-small q4 greedy")
+
+
+def test_cfg_ladder_llama_q4(sd):
+    """The multilingual T3's shape (Llama-style, Q4_0, two rows: conditional and
+    unconditional, 200-token prompts) with the ladder, 100 steps."""
+    run = get_preset("llama_q4")
+    _check_cfg(sd, run.model, prompt_tokens(run), 100, P.MTL_LADDER, "cfg ladder llama_q4")
+
+
+def test_cfg_ladder_decode_n_equals_step_chain(sd):
+    """decode_n with the ladder (device-side feedback and history) gives the
+    step chain's tokens and final logits bit for bit."""
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=2, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q8_0)
+    blob = _blob(spec)
+    prompt = np.random.default_rng(6).integers(0, 1000, size=(2, 24)).astype(np.int32)
+    n = 30
+    draws = uniform_draws(8, n + 1, 2)[..., 0]
+    s = sd.Sampler.from_spec(P.T3_SAMPLED)
+    a = sd.Decoder(spec, blob, stream=_stream())
+    a.set_ladder(sd.SamplerLadder.from_spec(P.MTL_LADDER))
+    t = a.prefill(prompt, s, draws[0])
+    chain = [int(t[0])]
+    for i in range(n):
+        t = a.step(np.array([chain[-1]] * 2, np.int32), s, draws[i + 1])
+        assert int(t[0]) == int(t[1])
+        chain.append(int(t[0]))
+    za = a.logits()
+    a.reset()
+    t = a.prefill(prompt, s, draws[0])
+    assert int(t[0]) == chain[0]
+    out = torch.zeros(n, 2, dtype=torch.int32, device="cuda")
+    a.decode_n(n, s, torch.from_numpy(np.ascontiguousarray(draws[1:])).cuda(), out)
+    o = out.cpu().numpy()
+    assert [int(x) for x in o[:, 0]] == chain[1:]
+    assert np.array_equal(o[:, 0], o[:, 1])
+    assert np.array_equal(a.logits().view(np.uint32), za.view(np.uint32))
+    # the ladder off again: the per-row sampler, rows independent
+    a.reset()
+    a.set_ladder(None)
+    t = a.prefill(prompt, s, draws[0])
+    z = a.logits()
+    for b in range(2):
+        tg, mg = oracle.sample(z[b], u=float(draws[0][b]), temperature=0.8, top_k=1000, top_p=0.95, greedy=False)
+        if mg >= SAMPLER_MARGIN:
+            assert int(t[b]) == tg, (b, int(t[b]), tg, mg)
+    a.close()
+
+
+def test_set_ladder_rejects(sd):
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=1, d_model=256, n_head=4, n_kv_head=4, head_dim=64,
+                       d_ff=512, vocab=300, max_ctx=40, batch=1, quant=P.Q8_0)
+    dec = sd.Decoder(spec, _blob(spec), stream=_stream())
+    with pytest.raises(sd.SdError):
+        dec.set_ladder(sd.SamplerLadder.from_spec(P.MTL_LADDER))     # one row
+    dec.close()
+    spec2 = dataclasses.replace(spec, batch=2)
+    dec = sd.Decoder(spec2, _blob(spec2), stream=_stream())
+    for bad in (dict(rep_penalty=0.0), dict(top_p=0.0), dict(top_p=1.5), dict(min_p=-0.1)):
+        with pytest.raises(sd.SdError):
+            dec.set_ladder(sd.SamplerLadder.from_spec(dataclasses.replace(P.MTL_LADDER, **bad)))
+    s = sd.Sampler.from_spec(P.T3_SAMPLED)
+    dec.prefill(np.zeros((2, 4), np.int32), s, np.zeros(2, np.float32))
+    with pytest.raises(sd.SdError):
+        dec.set_ladder(sd.SamplerLadder.from_spec(P.MTL_LADDER))     # not reset
+    dec.close()
 
 
 @pytest.fixture(params=["graph", "flat", "cluster"])

@@ -3,6 +3,8 @@ independent full causal recompute in torch float64 (tests/torch_ref.py), on
 small GPT-2, Llama (with grouped KV heads) and Talker + code-predictor models,
 plus closed-form special cases."""
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -84,6 +86,54 @@ def test_llama_gqa_rows_match_full_recompute():
         ref = torch_ref.t3_logits(blob, m, list(prompt[b]) + trs[b].tokens[:n])
         for i in range(n + 1):
             assert _rel(trs[b].logits[i], ref[11 + i]) < TOL, (b, i)
+
+
+def _cfg_run(ladder, n=10, seed=5):
+    m = _small_llama()
+    blob, _ = build_model_blob(m)
+    rng = np.random.default_rng(seed)
+    prompt = rng.integers(0, m.vocab, size=(2, 12)).astype(np.int32)
+    draws = uniform_draws(3, n + 1, 1)[:, 0, 0]
+    return m, blob, prompt, draws, oracle.run_t3_cfg(oracle.Model(blob), m, prompt, draws, n, ladder)
+
+
+def test_cfg_rows_both_consume_the_ladder_token():
+    """Both rows are fed the one picked token: each row's logits equal a full
+    recompute of its own prompt followed by the picked tokens."""
+    n = 10
+    m, blob, prompt, draws, tr = _cfg_run(P.LadderSpec(), n)
+    for b in range(2):
+        ref = torch_ref.t3_logits(blob, m, list(prompt[b]) + tr.tokens[:n])
+        for i in range(n + 1):
+            assert _rel(tr.logits[i][b], ref[11 + i]) < TOL, (b, i)
+
+
+def test_cfg_run_with_neutral_stages_is_the_plain_run_of_a_row():
+    """Guidance weight 0 with no penalty, min_p or top-p samples the conditional
+    row like the plain sampler; weight -1 samples the unconditional row."""
+    n = 10
+    for w, row in ((0.0, 0), (-1.0, 1)):
+        lad = P.LadderSpec(cfg_weight=w, rep_penalty=1.0, temperature=0.8, min_p=0.0, top_p=1.0, top_k=50)
+        m, blob, prompt, draws, tr = _cfg_run(lad, n)
+        d2 = np.stack([draws, draws], axis=1)
+        plain = oracle.run_t3(oracle.Model(blob), m, prompt, d2, n,
+                              SamplerSpec(temperature=0.8, top_k=50, top_p=1.0, greedy=False))[row]
+        assert tr.tokens == plain.tokens, (w, tr.tokens, plain.tokens)
+
+
+def test_cfg_history_holds_the_fed_tokens_only():
+    """Greedy with a huge repetition penalty: the first token is the plain
+    argmax of the combined logits (the prompt is not in the history), and no
+    fed token is picked again; without the penalty the same model repeats."""
+    n = 24
+    big = P.LadderSpec(cfg_weight=0.5, rep_penalty=1e6, temperature=0.0, min_p=0.0, top_p=1.0, top_k=1)
+    m, blob, prompt, draws, tr = _cfg_run(big, n)
+    zc, zu = (np.asarray(z, np.float64) for z in tr.logits[0])
+    assert tr.tokens[0] == int(np.argmax(zc + 0.5 * (zc - zu)))
+    assert len(set(tr.tokens)) == n + 1, tr.tokens
+    none = dataclasses.replace(big, rep_penalty=1.0)
+    _, _, _, _, tr0 = _cfg_run(none, n)
+    assert len(set(tr0.tokens)) < n + 1, tr0.tokens
 
 
 def test_qwen_frames_match_full_recompute():
