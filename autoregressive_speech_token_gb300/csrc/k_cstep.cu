@@ -662,6 +662,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
     const int per_step = 4 * L + 1, total = a.n_steps * per_step;
     const int RB = a.ring_bytes;
     const long long budget = a.spin_budget;
+    const uint64_t wpol = l2_policy(a.w_evict_first != 0);
     const bool ln = a.gpt2 != 0;
     const int PD = padded(d), PU = padded(a.upc);
     const int W2 = hd + 4;  // partial record stride
@@ -752,11 +753,11 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             const size_t tbase = (size_t)G0.t0 * G0.KB;
             const size_t sc_off = (size_t)((Wm->rows + 15) / 16) * G0.KB * frag_tb(Wm->kind);
             mb_expect(mb, (uint32_t)(G0.n_codes + G0.n_sc + nb_ + ng + ng2));
-            bulk_g2s(dst, Wm->q + tbase * frag_tb(Wm->kind), (uint32_t)G0.n_codes, mb);
-            bulk_g2s(dst + G0.o_sc, Wm->q + sc_off + tbase * 32, (uint32_t)G0.n_sc, mb);
-            if (nb_) bulk_g2s(dst + G0.o_bias, bias + G0.b_lo, (uint32_t)nb_, mb);
-            if (ng) bulk_g2s(dst + G0.o_g1, g1, (uint32_t)ng, mb);
-            if (ng2) bulk_g2s(dst + G0.o_g2, g2, (uint32_t)ng2, mb);
+            bulk_g2s_pol(dst, Wm->q + tbase * frag_tb(Wm->kind), (uint32_t)G0.n_codes, mb, wpol);
+            bulk_g2s_pol(dst + G0.o_sc, Wm->q + sc_off + tbase * 32, (uint32_t)G0.n_sc, mb, wpol);
+            if (nb_) bulk_g2s_pol(dst + G0.o_bias, bias + G0.b_lo, (uint32_t)nb_, mb, wpol);
+            if (ng) bulk_g2s_pol(dst + G0.o_g1, g1, (uint32_t)ng, mb, wpol);
+            if (ng2) bulk_g2s_pol(dst + G0.o_g2, g2, (uint32_t)ng2, mb, wpol);
             p_head = start + bytes;
             p_hoff = off + bytes;
             ++p_ni;
@@ -1218,7 +1219,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
             csync();
             stamp(28);
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + b : a.u1 + b;
-            const int tk = sample_detail::sample_fast(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
+            const int tk = sample_detail::sample_reg(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
                                                       a.err);
             if (tid == 0) {
                 a.tok[b] = tk;

@@ -552,6 +552,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
     const int total = a.n_steps * per_step;
     const int RB = a.ring_bytes;
     const long long budget = a.spin_budget;
+    const uint64_t wpol = l2_policy(a.w_evict_first != 0);
     const bool ln = a.gpt2 != 0;
     int o0, o1;
     row_range(d, cta, G, o0, o1);
@@ -599,11 +600,11 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
                     s_off[ni & (kNMB - 1)] = off;
                     mb_expect(mb, (uint32_t)(sl.n_codes + sl.n_sc + sl.n_bias + (sl.g1 ? sl.n_g : 0) +
                                              (sl.g2 ? sl.n_g : 0)));
-                    bulk_g2s(dst, sl.q, (uint32_t)sl.n_codes, mb);
-                    bulk_g2s(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb);
-                    if (sl.bias) bulk_g2s(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb);
-                    if (sl.g1) bulk_g2s(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb);
-                    if (sl.g2) bulk_g2s(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb);
+                    bulk_g2s_pol(dst, sl.q, (uint32_t)sl.n_codes, mb, wpol);
+                    bulk_g2s_pol(dst + sl.o_sc, sl.s, (uint32_t)sl.n_sc, mb, wpol);
+                    if (sl.bias) bulk_g2s_pol(dst + sl.o_bias, sl.bias, (uint32_t)sl.n_bias, mb, wpol);
+                    if (sl.g1) bulk_g2s_pol(dst + sl.o_g1, sl.g1, (uint32_t)sl.n_g, mb, wpol);
+                    if (sl.g2) bulk_g2s_pol(dst + sl.o_g2, sl.g2, (uint32_t)sl.n_g, mb, wpol);
                     head = start + sl.bytes;
                     hoff = off + sl.bytes;
                     ++ni;
@@ -924,7 +925,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             if (!ok) break;
             tr_waited();
             const float* up = a.u_seq ? a.u_seq + (size_t)s * NB + cta : a.u1 + cta;
-            const int tok = sample_detail::sample_fast(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
+            const int tok = sample_detail::sample_reg(a.V, *a.sp, up, reinterpret_cast<unsigned char*>(z), s_samp,
                                                        a.err);
             if (tid == 0) {
                 a.tok[cta] = tok;

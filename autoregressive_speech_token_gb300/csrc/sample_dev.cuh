@@ -732,7 +732,292 @@ static __device__ __noinline__ int sample_fast(int V, const SampParams sp, const
     return tok;
 }
 
-// As sample_smem, loading the logits lg[0..V) first (through L2: they may
+constexpr int kRS = 17;   // elements per thread held in registers (V <= 17 * SAMPLE_NT)
+
+static __device__ __forceinline__ int lower_bound_u64(const unsigned long long* a, int n, unsigned long long t) {
+    int lo = 0, hi = n;  // first index in [0, n) with a[i] >= t, or n
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] >= t) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+// The path every kernel takes first for a sampled row (512 threads, V <= 17 * 512): the same
+// survivors, cut and draw as sample_fast, with each thread's logits and fixed-point masses held
+// in registers over a contiguous segment of the vocabulary (odd segment length: the loads hit
+// 32 distinct banks).  One pass builds the count and mass histograms over the value bins
+// together (masses of every element; the bins above the k-th largest hold survivors only), one
+// scan gives each bin's inclusive mass prefix, and one pass collects the members of the k-th
+// bin and of the bins where the top-p cut can fall (the cut's T = ceil(top_p * Z) is bracketed
+// by Z's bounds before the k-th bin is resolved).  Warp 0 then resolves the threshold key, Z,
+// T and the cut element; the draw scans the kept masses in vocabulary order.  Eight barriers.
+static __device__ __noinline__ int sample_reg(int V, const SampParams sp, const float* u_ptr, unsigned char* smraw,
+                                              SampleScratch& ss, int* err) {
+    const int tid = threadIdx.x, nt = SAMPLE_NT, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    int S = (V + nt - 1) / nt;
+    S |= 1;  // odd: lane stride S hits 32 distinct banks
+    if (sp.greedy || sp.top_k == 1 || sp.temperature <= 0.f || nt * 4 != kFB || S > kRS)
+        return sample_fast(V, sp, u_ptr, smraw, ss, err);
+    const size_t arr = sample_array_bytes(V);
+    const float* z = reinterpret_cast<const float*>(smraw);
+    unsigned* cnt = reinterpret_cast<unsigned*>(smraw + arr);             // [kFB]
+    unsigned* mh = cnt + kFB;                                              // [kFB]
+    unsigned* ml = mh + kFB;                                               // [kFB]
+    unsigned long long* pre = reinterpret_cast<unsigned long long*>(mh);   // [kFB] after the scan
+    uint32_t* ckey = ml + kFB;                                             // [kFC]
+    unsigned* cbi = ckey + kFC;                                            // [kFC] bin << 14 | index
+    unsigned* cq = cbi + kFC;                                              // [kFC]
+    const int a0 = tid * S;
+
+    // ---- P1: this thread's logits into registers; range; histograms cleared
+    float v[kRS];
+    float mloc = -INFINITY, nloc = INFINITY;
+#pragma unroll
+    for (int j = 0; j < kRS; ++j) {
+        const int i = a0 + j;
+        v[j] = (j < S && i < V) ? z[i] : 0.f;
+        if (j < S && i < V) {
+            mloc = fmaxf(mloc, v[j]);
+            nloc = fminf(nloc, v[j]);
+        }
+    }
+    for (int b = tid; b < kFB; b += nt) {
+        cnt[b] = 0u;
+        mh[b] = 0u;
+        ml[b] = 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+        nloc = fminf(nloc, __shfl_xor_sync(0xffffffffu, nloc, o));
+    }
+    if (lane == 0) {
+        ss.f[warp] = mloc;
+        ss.f[32 + warp] = nloc;
+    }
+    if (tid == 0) {
+        ss.i[0] = 0;
+        ss.i[2] = 0;
+        ss.i[3] = 1;
+        ss.i[6] = -1;
+        ss.q[40] = 0ull;
+    }
+    SAMPLE_SYNC();
+    float mx = ss.f[0], mn = ss.f[32];
+    for (int w = 1; w < nw; ++w) {
+        mx = fmaxf(mx, ss.f[w]);
+        mn = fminf(mn, ss.f[32 + w]);
+    }
+    const float sc = mx > mn ? fminf((float)(kFB - 1) / (mx - mn), 1e30f) : 0.f;
+    const int k = (sp.top_k < 1 || sp.top_k > V) ? V : sp.top_k;
+    const bool topk = k < V, topp = sp.top_p < 1.0f;
+    const float invT = 1.0f / sp.temperature;
+
+    // ---- P2: masses of every element; count and mass histograms over the bins
+    unsigned q[kRS];
+#pragma unroll
+    for (int j = 0; j < kRS; ++j) {
+        q[j] = 0u;
+        if (j < S && a0 + j < V) {
+            q[j] = (unsigned)fixq(expf((v[j] - mx) * invT));
+            const int bn = vbin(v[j], mx, sc);
+            atomicAdd(&cnt[bn], 1u);
+            if (q[j]) {
+                atomicAdd(&mh[bn], q[j] >> 16);
+                atomicAdd(&ml[bn], q[j] & 0xFFFFu);
+            }
+        }
+    }
+    SAMPLE_SYNC();
+
+    // ---- P3: scans of counts and masses over the bins (4 bins per thread)
+    const uint4 c4 = reinterpret_cast<const uint4*>(cnt)[tid];
+    const uint4 h4 = reinterpret_cast<const uint4*>(mh)[tid], l4 = reinterpret_cast<const uint4*>(ml)[tid];
+    const unsigned cb[4] = {c4.x, c4.y, c4.z, c4.w};
+    const unsigned long long mb[4] = {((unsigned long long)h4.x << 16) + l4.x, ((unsigned long long)h4.y << 16) + l4.y,
+                                      ((unsigned long long)h4.z << 16) + l4.z, ((unsigned long long)h4.w << 16) + l4.w};
+    const unsigned ownc = cb[0] + cb[1] + cb[2] + cb[3];
+    const unsigned long long ownm = mb[0] + mb[1] + mb[2] + mb[3];
+    const unsigned incc = warp_incl_scan_u32(ownc);
+    const unsigned long long incm = warp_incl_scan_u64(ownm);
+    if (lane == 31) {
+        ss.i[8 + warp] = (int)incc;
+        ss.q[16 + warp] = incm;
+    }
+    SAMPLE_SYNC();
+
+    // ---- P4: inclusive mass prefix per bin; the bin of the k-th largest
+    {
+        unsigned cc = incc - ownc;
+        unsigned long long cm = incm - ownm;
+        for (int w = 0; w < warp; ++w) {
+            cc += (unsigned)ss.i[8 + w];
+            cm += ss.q[16 + w];
+        }
+        unsigned long long pr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (topk && cc < (unsigned)k && cc + cb[j] >= (unsigned)k) {
+                ss.i[2] = 4 * tid + j;   // the bin of the k-th largest
+                ss.i[3] = k - (int)cc;   // its rank inside the bin (1 = the bin's largest)
+                ss.i[4] = (int)cb[j];
+                ss.q[40] = cm;           // the mass of the bins before it
+            }
+            cc += cb[j];
+            cm += mb[j];
+            pr[j] = cm;
+        }
+        reinterpret_cast<ulonglong2*>(pre)[2 * tid] = make_ulonglong2(pr[0], pr[1]);
+        reinterpret_cast<ulonglong2*>(pre)[2 * tid + 1] = make_ulonglong2(pr[2], pr[3]);
+    }
+    SAMPLE_SYNC();
+
+    // ---- P5: the members of the k-th bin and of the bins where the top-p cut can fall
+    unsigned long long Ztot = 0ull;
+    for (int w = 0; w < nw; ++w) Ztot += ss.q[16 + w];
+    const int bk = topk ? ss.i[2] : kFB;               // kFB: no top-k bin
+    const unsigned long long mAbove = topk ? ss.q[40] : Ztot;
+    int blo = kFB, bhi = -1;
+    if (topp) {
+        const unsigned long long zhi = topk ? pre[bk] : Ztot;  // Z lies in [mAbove, zhi]
+        unsigned long long tlo = mul_frac(sp.top_p, mAbove, true), thi = mul_frac(sp.top_p, zhi, true);
+        if (tlo == 0ull) tlo = 1ull;
+        if (thi == 0ull) thi = 1ull;
+        const int lim = topk ? bk : kFB;
+        blo = lower_bound_u64(pre, lim, tlo);
+        bhi = lower_bound_u64(pre, lim, thi);
+        if (bhi >= lim) bhi = lim - 1;
+    }
+#pragma unroll
+    for (int j = 0; j < kRS; ++j) {
+        const int i = a0 + j;
+        if (j < S && i < V) {
+            const int bn = vbin(v[j], mx, sc);
+            if (bn == bk || (bn >= blo && bn <= bhi)) {
+                const int c = atomicAdd(&ss.i[0], 1);
+                if (c < kFC) {
+                    ckey[c] = ord_key(v[j]);
+                    cbi[c] = ((unsigned)bn << 14) | (unsigned)i;
+                    cq[c] = q[j];
+                }
+            }
+        }
+    }
+    SAMPLE_SYNC();
+    const int nm = ss.i[0];
+    if (nm > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
+
+    // ---- P6 (warp 0): the top-k threshold key and the top-p cut element
+    if (warp == 0) {
+        const int rk = topk ? ss.i[3] : 0;
+        // survivors of the k-th bin: fewer than rk of its members above them
+        uint32_t thr = 0u;
+        unsigned long long sk = 0ull;
+        if (topk) {
+            for (int c = lane; c < nm; c += 32) {
+                if ((int)(cbi[c] >> 14) != bk) continue;
+                const uint32_t key = ckey[c];
+                int gt = 0, ge = 0;
+                for (int j = 0; j < nm; ++j) {
+                    if ((int)(cbi[j] >> 14) != bk) continue;
+                    gt += ckey[j] > key;
+                    ge += ckey[j] >= key;
+                }
+                if (gt < rk) sk += cq[c];
+                if (gt < rk && rk <= ge) ss.sel[0] = key;  // every writer writes the same key
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            __syncwarp();
+            thr = ss.sel[0];
+        }
+        const unsigned long long Zq = topk ? mAbove + sk : Ztot;
+        if (lane == 0) {
+            ss.sel[0] = thr;
+            ss.i[5] = 0;  // no cut
+        }
+        __syncwarp();
+        if (topp) {
+            unsigned long long T = mul_frac(sp.top_p, Zq, true);
+            if (T == 0ull) T = 1ull;
+            // the bin where the cumulative (bins in order) mass reaches T, and the mass needed inside it
+            int bp;
+            unsigned long long before;
+            if (topk && T > mAbove) {
+                bp = bk;
+                before = mAbove;
+            } else {
+                bp = lower_bound_u64(pre, topk ? bk : kFB, T);
+                before = bp > 0 ? pre[bp - 1] : 0ull;
+            }
+            const unsigned long long rem = T - before;
+            for (int c = lane; c < nm; c += 32) {
+                if ((int)(cbi[c] >> 14) != bp) continue;
+                const uint32_t key = ckey[c];
+                if (key < thr) continue;
+                const int idx = (int)(cbi[c] & 0x3FFFu);
+                unsigned long long p0 = 0ull;  // mass before this element in (key desc, index asc) order
+                for (int j = 0; j < nm; ++j) {
+                    if ((int)(cbi[j] >> 14) != bp || ckey[j] < thr) continue;
+                    const int jx = (int)(cbi[j] & 0x3FFFu);
+                    if (ckey[j] > key || (ckey[j] == key && jx < idx)) p0 += cq[j];
+                }
+                if (p0 < rem && p0 + (unsigned long long)cq[c] >= rem) {
+                    ss.sel[1] = key;
+                    ss.sel[2] = (uint32_t)idx;
+                    ss.i[5] = 1;
+                }
+            }
+        }
+    }
+    SAMPLE_SYNC();
+    const uint32_t thr = ss.sel[0];
+    const bool cut = ss.i[5] != 0;
+    const uint32_t tkey = ss.sel[1];
+    const int tidx = (int)ss.sel[2];
+
+    // ---- P7: kept mass of this thread's segment, scanned in thread (= vocabulary) order
+    unsigned long long loc = 0ull;
+#pragma unroll
+    for (int j = 0; j < kRS; ++j) {
+        const int i = a0 + j;
+        if (j < S && i < V && q[j]) {
+            const uint32_t key = ord_key(v[j]);
+            if (!(key >= thr && (!cut || key > tkey || (key == tkey && i <= tidx)))) q[j] = 0u;  // not kept
+        }
+        loc += q[j];
+    }
+    const unsigned long long inc = warp_incl_scan_u64(loc);
+    if (lane == 31) ss.q[32 + warp] = inc;
+    SAMPLE_SYNC();
+    unsigned long long run = inc - loc, ZS = 0ull;
+    for (int w = 0; w < nw; ++w) {
+        const unsigned long long t = ss.q[32 + w];
+        ZS += t;
+        if (w < warp) run += t;
+    }
+    const unsigned long long target = mul_frac(*u_ptr, ZS, false);
+    if (run <= target && target < run + loc) {
+#pragma unroll
+        for (int j = 0; j < kRS; ++j) {
+            run += q[j];
+            if (run > target) {
+                ss.i[6] = a0 + j;
+                break;
+            }
+        }
+    }
+    SAMPLE_SYNC();
+    int tok = ss.i[6];
+    if (tok < 0 || tok >= V) {
+        if (tid == 0 && err) atomicExch(err, 2);
+        tok = 0;
+    }
+    return tok;
+}
+
+// As sample_reg, loading the logits lg[0..V) first (through L2: they may
 // have been written by other CTAs of the same kernel).
 static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
                                    unsigned char* smraw, SampleScratch& ss, int* err) {
@@ -752,7 +1037,7 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
         }
     }
     SAMPLE_SYNC();
-    return sample_fast(V, sp, u_ptr, smraw, ss, err);
+    return sample_reg(V, sp, u_ptr, smraw, ss, err);
 }
 
 }  // namespace sample_detail

@@ -840,6 +840,8 @@ int setup_cstep(sd_ctx* c) {
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
+    // SD_L2_WEIGHTS=normal: weight copies without the evict-first policy (for measurement)
+    if (const char* lw = getenv("SD_L2_WEIGHTS")) a.w_evict_first = strcmp(lw, "normal") != 0;
     // test hook: the first persistent launch lets one exchange-word wait run out after this many us
     if (const char* ts = getenv("SD_TEST_STALL_US"))
         c->test_stall = (long long)(clock_khz > 0 ? clock_khz : 2000000) * std::max(1, atoi(ts)) / 1000;
@@ -904,6 +906,8 @@ int setup_persistent(sd_ctx* c) {
     int clock_khz = 0;
     cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, c->device);
     a.spin_budget = (long long)(clock_khz > 0 ? clock_khz : 2000000) * 200;  // 200 ms per wait
+    // SD_L2_WEIGHTS=normal: weight copies without the evict-first policy (for measurement)
+    if (const char* lw = getenv("SD_L2_WEIGHTS")) a.w_evict_first = strcmp(lw, "normal") != 0;
     // test hook: the first persistent launch lets one exchange-word wait run out after this many us
     if (const char* ts = getenv("SD_TEST_STALL_US"))
         c->test_stall = (long long)(clock_khz > 0 ? clock_khz : 2000000) * std::max(1, atoi(ts)) / 1000;

@@ -222,6 +222,7 @@ struct StepArgs {
     int* err = nullptr;
     int n_steps = 1;
     long long spin_budget = 0;           // clock64 cycles per wait
+    int w_evict_first = 1;               // weight copies with the L2 evict-first policy
     // test hook (0: off): in the launch's first step, CTA 0's first-layer wait for the O
     // projection's output words looks for an epoch no producer writes, for this many cycles
     long long test_budget = 0;
@@ -277,6 +278,7 @@ struct CStepArgs {
     int* err = nullptr;
     int n_steps = 1;
     long long spin_budget = 0;
+    int w_evict_first = 1;               // weight copies with the L2 evict-first policy
     // test hook (0: off): in the launch's first step, cluster 0 rank 0's first-layer wait for
     // the O-projection partials looks for an epoch no producer writes, for this many cycles
     long long test_budget = 0;

@@ -90,6 +90,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(mb) : "memory");
 }
 
+// L2 policies for bulk copies: evict-first for data read once per step (the weight stream,
+// more bytes per step than L2 holds), so that the step's code, KV cache and exchange words stay
+// resident while the weights stream through; evict-normal otherwise.
+__device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
+    uint64_t p;
+    if (evict_first)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes, uint32_t mb, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ bool mb_try(uint32_t mb, uint32_t parity) {
     uint32_t ok;
     asm volatile(

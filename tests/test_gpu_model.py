@@ -239,16 +239,26 @@ def test_bench_configuration_gpt2m_q4(sd):
     tally.check()
 
 
+def _ladder_input(zc, zu, lad, seen):
+    """The ladder's input to its temperature stage, in float64: the guided
+    combination of the two rows, then the repetition penalty on the history (a
+    measure of how far the two sides' inputs to the sampling stages differ)."""
+    zc, zu = np.asarray(zc, np.float64), np.asarray(zu, np.float64)
+    z = zc + lad.cfg_weight * (zc - zu)
+    pen = seen.astype(bool)
+    z[pen] = np.where(z[pen] > 0, z[pen] / lad.rep_penalty, z[pen] * lad.rep_penalty)
+    return z
+
+
 def _check_cfg(sd, spec, prompt, n_steps, lad, name, draw_seed=3):
     """The multilingual T3 with guidance through sd_set_ladder: row 0 conditional,
     row 1 unconditional, one token per step fed to both rows, teacher-forced with
     the oracle's tokens.  Per step: both rows' logits within REL_L2 of the
     oracle's; the device ladder picks what the oracle's ladder picks on the
     device's own logits (same history, margin >= SAMPLER_MARGIN); the token
-    against the oracle's under _Tally's rules, d being the largest change of the
-    ladder's tempered input that the two rows' logit errors allow
-    (guidance mixes them with weights 1+w and w, the penalty scales by at most
-    its factor)."""
+    against the oracle's under _Tally's rules, d being the largest difference
+    between the two sides' inputs to the ladder's temperature stage (guided
+    combination, then repetition penalty)."""
     blob = _blob(spec)
     draws = uniform_draws(draw_seed, n_steps + 1, 2)[..., 0]
     ref = oracle.run_t3_cfg(oracle.Model(blob, THREADS), spec, prompt, draws[:, 0], n_steps, lad)
@@ -259,7 +269,6 @@ def _check_cfg(sd, spec, prompt, n_steps, lad, name, draw_seed=3):
     as_sampler = SamplerSpec(temperature=lad.temperature, top_k=lad.top_k, top_p=lad.top_p,
                              greedy=lad.temperature <= 0)
     tally = _Tally(name, as_sampler)
-    w = abs(lad.cfg_weight)
     seen = np.zeros(spec.vocab, np.uint8)
     worst = 0.0
     for i in range(n_steps + 1):
@@ -273,8 +282,7 @@ def _check_cfg(sd, spec, prompt, n_steps, lad, name, draw_seed=3):
                                       lad.min_p, lad.top_p, lad.top_k, u=float(draws[i][0]))
         if mg >= SAMPLER_MARGIN:
             assert int(got[0]) == tg, ("ladder", i, int(got[0]), tg, mg)
-        d = max(lad.rep_penalty, 1.0) * ((1 + w) * _logit_error(z[0], ref.logits[i][0]) +
-                                         w * _logit_error(z[1], ref.logits[i][1]))
+        d = _logit_error(_ladder_input(z[0], z[1], lad, seen), _ladder_input(*ref.logits[i], lad, seen))
         tally.add(i, int(got[0]), ref.tokens[i], ref.margins[i], None, None, d=d)
         if i < n_steps:
             t = ref.tokens[i]
