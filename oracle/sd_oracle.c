@@ -9,7 +9,8 @@
  *   - the Qwen3-style Talker plus 15-pass code predictor ("Every Frame Is a
  *     Memory Read", section 1).
  * Weights are block-quantised (journal Tier A item A3, section 3.23 for the
- * Q4_0 byte layout; the blog's section 3 for affine group-64).
+ * Q4_0 byte layout, A3 for Q5_0; the blog's section 3 for affine group-64
+ * 8-bit and section 5.8 for the 4-bit group-32 / group-64 code predictor).
  *
  * Nothing here is blocked, fused or reordered: each linear layer dequantises a
  * row and takes one double-precision dot product; attention scores, softmax and
@@ -30,7 +31,11 @@
 #include <omp.h>
 #endif
 
-enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
+enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3, K_Q5_0 = 4, K_A4G32 = 5, K_A4G64 = 6 };
+#define K_LAST K_A4G64
+/* affine kinds (codes, then per-group fp16 scales, then per-group fp16 biases) and their group size */
+static int is_affine(int kind) { return kind == K_A8G64 || kind == K_A4G32 || kind == K_A4G64; }
+static int group_of(int kind) { return kind == K_A4G32 ? 32 : is_affine(kind) ? 64 : 32; }
 
 /* Planted mistakes for the pin tests (tests/test_oracle_mutants.py): a build
  * with -DORC_MUTANT=n carries mistake n, and the pins must reject it.  Normal
@@ -47,7 +52,9 @@ enum { K_F32 = 0, K_Q8_0 = 1, K_Q4_0 = 2, K_A8G64 = 3 };
  *  19 RoPE skipped on keys         20 repetition penalty backwards
  *  21 ladder: top-k before top-p     22 margin ignores membership flips
  *  23 margin taken as if T were 1    24 top-p bound counts t before itself
- *  25 mass factor 1+r instead of its square root                           */
+ *  25 mass factor 1+r instead of its square root
+ *  26 Q5_0 fifth bit taken from the wrong element
+ *  27 4-bit affine codes read high nibble first                            */
 #ifndef ORC_MUTANT
 #define ORC_MUTANT 0
 #endif
@@ -118,6 +125,25 @@ static void dequant_row(int kind, const uint8_t* data, int64_t r, int64_t cols, 
                 out[b * 32 + j] = d * (float)(nib - 8);
             }
         }
+    } else if (kind == K_Q5_0) {
+        /* 22-byte blocks: fp16 d, 32 fifth bits (bit j of the little-endian word = element j),
+         * then the low nibbles as in Q4_0; value d * (q - 16) */
+        const uint8_t* row = data + r * (cols / 32) * 22;
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 22;
+            float d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+            uint32_t qh = (uint32_t)blk[2] | ((uint32_t)blk[3] << 8) | ((uint32_t)blk[4] << 16) | ((uint32_t)blk[5] << 24);
+            for (int j = 0; j < 32; ++j) {
+                int byte = blk[6 + (j % 16)];
+                int nib = j < 16 ? (byte & 0xf) : (byte >> 4);
+#if ORC_MUTANT == 26
+                int hi = (int)((qh >> (31 - j)) & 1u);
+#else
+                int hi = (int)((qh >> j) & 1u);
+#endif
+                out[b * 32 + j] = d * (float)((nib | (hi << 4)) - 16);
+            }
+        }
     }
 }
 
@@ -125,23 +151,37 @@ typedef struct {
     int kind;
     int64_t rows, cols;
     const uint8_t* data;      /* quantised codes, or fp32 values */
-    const uint16_t* scale;    /* A8G64 only */
-    const uint16_t* bias;     /* A8G64 only */
+    const uint16_t* scale;    /* affine kinds only */
+    const uint16_t* bias;     /* affine kinds only */
 } qmat;
 
 static void qmat_row(const qmat* W, int64_t r, float* out) {
-    if (W->kind == K_A8G64) {
-        const uint8_t* q = W->data + r * W->cols;
-        const uint16_t* s = W->scale + r * (W->cols / 64);
-        const uint16_t* b = W->bias + r * (W->cols / 64);
-        for (int64_t g = 0; g < W->cols / 64; ++g) {
+    if (is_affine(W->kind)) {
+        /* value = scale * q + bias per group; 8-bit codes one per byte, 4-bit codes two per byte
+         * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble) */
+        const int gs = group_of(W->kind), four = W->kind != K_A8G64;
+        const uint8_t* q = W->data + r * (four ? W->cols / 2 : W->cols);
+        const uint16_t* s = W->scale + r * (W->cols / gs);
+        const uint16_t* b = W->bias + r * (W->cols / gs);
+        for (int64_t g = 0; g < W->cols / gs; ++g) {
             const float sc = orc_half_to_float(s[g]), bi = orc_half_to_float(b[g]);
-            for (int64_t k = g * 64; k < (g + 1) * 64; ++k)
-#if ORC_MUTANT == 4
-                out[k] = sc * (float)q[k] + 0.0f * bi;
+            for (int64_t k = g * gs; k < (g + 1) * gs; ++k) {
+                int code;
+                if (!four)
+                    code = q[k];
+#if ORC_MUTANT == 27
+                else
+                    code = (k & 1) ? (q[k / 2] & 0xf) : (q[k / 2] >> 4);
 #else
-                out[k] = fmaf(sc, (float)q[k], bi);
+                else
+                    code = (k & 1) ? (q[k / 2] >> 4) : (q[k / 2] & 0xf);
 #endif
+#if ORC_MUTANT == 4
+                out[k] = sc * (float)code + 0.0f * bi;
+#else
+                out[k] = fmaf(sc, (float)code, bi);
+#endif
+            }
         }
     } else if (W->kind == K_F32) {
         memcpy(out, (const float*)W->data + r * W->cols, (size_t)W->cols * sizeof(float));
@@ -152,15 +192,15 @@ static void qmat_row(const qmat* W, int64_t r, float* out) {
 
 static qmat make_qmat(int kind, const uint8_t* data, int64_t rows, int64_t cols) {
     qmat W = {kind, rows, cols, data, NULL, NULL};
-    if (kind == K_A8G64) {
-        W.scale = (const uint16_t*)(data + rows * cols);
-        W.bias = W.scale + rows * (cols / 64);
+    if (is_affine(kind)) {
+        W.scale = (const uint16_t*)(data + rows * (kind == K_A8G64 ? cols : cols / 2));
+        W.bias = W.scale + rows * (cols / group_of(kind));
     }
     return W;
 }
 
 int orc_dequant(int kind, const uint8_t* data, int64_t rows, int64_t cols, float* out) {
-    if (kind < K_Q8_0 || kind > K_A8G64 || cols % (kind == K_A8G64 ? 64 : 32)) return -1;
+    if (kind < K_Q8_0 || kind > K_LAST || cols % group_of(kind)) return -1;
     qmat W = make_qmat(kind, data, rows, cols);
     for (int64_t r = 0; r < rows; ++r) qmat_row(&W, r, out + r * cols);
     return 0;
@@ -208,7 +248,7 @@ static void linear_q(const qmat* W, const float* x, const float* bias, float* y)
 
 int orc_linear(int kind, const uint8_t* data, int64_t rows, int64_t cols,
                const float* x, const float* b, float* y) {
-    if (kind < K_F32 || kind > K_A8G64) return -1;
+    if (kind < K_F32 || kind > K_LAST || (kind != K_F32 && cols % group_of(kind))) return -1;
     qmat W = make_qmat(kind, data, rows, cols);
     linear_q(&W, x, b, y);
     return 0;
@@ -745,7 +785,7 @@ static int get_f32(const orc_model* m, const char* name, int64_t n, const float*
 
 static int get_q(const orc_model* m, const char* name, int64_t rows, int64_t cols, qmat* out) {
     const otensor* t = find(m, name);
-    if (!t || t->kind == K_F32 || t->rows != rows || t->cols != cols) {
+    if (!t || t->kind == K_F32 || t->kind > K_LAST || t->rows != rows || t->cols != cols || cols % group_of((int)t->kind)) {
         fprintf(stderr, "oracle: missing or mis-shaped matrix %s\n", name);
         return -1;
     }

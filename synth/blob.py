@@ -22,6 +22,12 @@ Tensor kinds and canonical storage:
              (byte j: low nibble = element j, high nibble = element j+16)
     3 A8G64  rows x cols uint8 codes, then rows x cols/64 fp16 scales, then
              rows x cols/64 fp16 biases
+    4 Q5_0   rows x (cols/32) blocks of 22 bytes: fp16 d, u32 of fifth bits
+             (bit j = element j), 16 bytes of low nibbles as in Q4_0
+    5 A4G32  rows x cols/2 bytes of 4-bit codes (byte i: low nibble = element
+             2i, high nibble = element 2i+1), then rows x cols/32 fp16 scales,
+             then rows x cols/32 fp16 biases
+    6 A4G64  as A4G32 with groups of 64
 """
 
 from __future__ import annotations
@@ -41,6 +47,10 @@ KIND_F32 = 0
 KIND_Q8_0 = 1
 KIND_Q4_0 = 2
 KIND_A8G64 = 3
+KIND_Q5_0 = 4
+KIND_A4G32 = 5
+KIND_A4G64 = 6
+AFFINE_KINDS = (KIND_A8G64, KIND_A4G32, KIND_A4G64)
 
 
 def config_words(m) -> bytes:
@@ -63,7 +73,7 @@ def with_batch(blob: np.ndarray, batch: int) -> np.ndarray:
 
 
 def _payload(kind: int, data) -> bytes:
-    if kind == KIND_A8G64:
+    if kind in AFFINE_KINDS:
         q, s, b = data
         return (np.ascontiguousarray(q, np.uint8).tobytes() + np.ascontiguousarray(s, np.float16).tobytes()
                 + np.ascontiguousarray(b, np.float16).tobytes())

@@ -39,11 +39,15 @@ ARCH_QWEN_TTS = 3
 Q8_0 = 1
 Q4_0 = 2
 A8G64 = 3
+Q5_0 = 4
+A4G32 = 5
+A4G64 = 6
 
-QUANT_NAMES = {Q8_0: "q8_0", Q4_0: "q4_0", A8G64: "a8g64"}
+QUANT_NAMES = {Q8_0: "q8_0", Q4_0: "q4_0", A8G64: "a8g64", Q5_0: "q5_0", A4G32: "a4g32", A4G64: "a4g64"}
 # bytes per weight of each stored format: Q8_0 = 34 B / 32, Q4_0 = 18 B / 32,
-# affine group 64 = (64 + 2 + 2) B / 64 -> 8.5 bits per weight.
-BYTES_PER_WEIGHT = {Q8_0: 34 / 32, Q4_0: 18 / 32, A8G64: 68 / 64}
+# Q5_0 = 22 B / 32, affine group 64 = (64 + 2 + 2) B / 64 -> 8.5 bits per weight,
+# 4-bit affine = (16 + 4) B / 32 at group 32 and (32 + 4) B / 64 at group 64.
+BYTES_PER_WEIGHT = {Q8_0: 34 / 32, Q4_0: 18 / 32, A8G64: 68 / 64, Q5_0: 22 / 32, A4G32: 20 / 32, A4G64: 36 / 64}
 
 
 @dataclass(frozen=True)
@@ -71,6 +75,8 @@ class ModelSpec:
     cp_vocab: int = 0
     n_codebooks: int = 0
     cp_max_ctx: int = 0
+    # code predictor's weight format (0: the model's); the blob records each tensor's own format
+    cp_quant: int = 0
 
     @property
     def q_dim(self) -> int:

@@ -20,6 +20,16 @@ Quantisers (they produce the stored inputs; the decode step only dequantises):
   per group, w = scale*q + bias, scale = (max-min)/255, bias = min, q =
   round-half-even((w - bias)/scale) clamped to [0, 255] (about 8.5 bits per
   weight, "Every Frame Is a Memory Read", section 3).
+* Q5_0 -- blocks of 32 unsigned 5-bit codes offset by 16 with one fp16 scale
+  d = m/-16 (m as for Q4_0); code q = min(31, floor(w/d + 16.5)).  A block is the
+  fp16 d, a little-endian u32 whose bit j is the fifth bit of element j, and the
+  16 bytes of low nibbles laid out as in Q4_0: 22 bytes (the ggml legacy block
+  type of the journal's Tier A item A3).
+* A4G32 / A4G64 -- affine groups of 32 / 64: unsigned 4-bit q with fp16 scale and
+  bias per group, scale = (max-min)/15, bias = min, q = round-half-even((w -
+  bias)/scale) clamped to [0, 15]; two codes per byte, element 2i in the low
+  nibble ("Every Frame Is a Memory Read", section 5.8: the 4-bit group-32 and
+  group-64 code predictor).
 """
 
 from __future__ import annotations
@@ -27,9 +37,10 @@ from __future__ import annotations
 import numpy as np
 
 from . import presets as P
-from .blob import KIND_F32, KIND_Q4_0, KIND_Q8_0, KIND_A8G64, write_blob
+from .blob import KIND_F32, KIND_Q4_0, KIND_Q8_0, KIND_A8G64, KIND_Q5_0, KIND_A4G32, KIND_A4G64, write_blob
 
-_QKIND = {P.Q8_0: KIND_Q8_0, P.Q4_0: KIND_Q4_0, P.A8G64: KIND_A8G64}
+_QKIND = {P.Q8_0: KIND_Q8_0, P.Q4_0: KIND_Q4_0, P.A8G64: KIND_A8G64, P.Q5_0: KIND_Q5_0, P.A4G32: KIND_A4G32,
+          P.A4G64: KIND_A4G64}
 
 
 # ----------------------------------------------------------------------------- quantisers
@@ -96,6 +107,46 @@ def quantize_a8g64(w: np.ndarray):
     return q, scale.astype(np.float16), mn.astype(np.float16)
 
 
+def quantize_q5_0(w: np.ndarray) -> np.ndarray:
+    """fp32 [rows, K] -> uint8 [rows, K/32, 22] (fp16 d, u32 fifth bits, 16 nibble bytes)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, k = w.shape
+    assert k % 32 == 0
+    b = w.reshape(rows, k // 32, 32)
+    idx = np.argmax(np.abs(b), axis=-1)                      # first on ties
+    m = np.take_along_axis(b, idx[..., None], axis=-1)[..., 0]
+    d = (m / np.float32(-16.0)).astype(np.float32)
+    d[d == 0] = np.float32(0.0)
+    with np.errstate(divide="ignore"):
+        inv = np.where(d != 0, np.float32(1.0) / d, np.float32(0.0)).astype(np.float32)
+    x = (b * inv[..., None] + np.float32(16.5)).astype(np.float32)
+    q = np.clip(np.minimum(np.float32(31), np.floor(x)), 0, 31).astype(np.uint32)
+    q = np.where((d != 0)[..., None], q, np.uint32(16)).astype(np.uint32)
+    qh = ((q >> 4) << np.arange(32, dtype=np.uint32)).sum(axis=-1, dtype=np.uint64).astype(np.uint32)
+    lo = (q & 0xF).astype(np.uint8)
+    out = np.empty((rows, k // 32, 22), dtype=np.uint8)
+    out[..., 0:2] = d.astype(np.float16).view(np.uint8).reshape(rows, k // 32, 2)
+    out[..., 2:6] = qh.astype("<u4").view(np.uint8).reshape(rows, k // 32, 4)
+    out[..., 6:] = lo[..., :16] | (lo[..., 16:] << 4)
+    return out
+
+
+def quantize_a4(w: np.ndarray, group: int):
+    """fp32 [rows, K] -> (codes uint8 [rows, K/2], scale fp16 [rows, K/group], bias fp16 [rows, K/group])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, k = w.shape
+    assert k % group == 0
+    g = w.reshape(rows, k // group, group)
+    mn = g.min(axis=-1)
+    mx = g.max(axis=-1)
+    scale = ((mx - mn) / np.float32(15.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(scale[..., None] != 0, (g - mn[..., None]) / scale[..., None], 0).astype(np.float32)
+    q = np.clip(np.rint(t), 0, 15).astype(np.uint8).reshape(rows, k)
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scale.astype(np.float16), mn.astype(np.float16)
+
+
 def quantize(w: np.ndarray, quant: int):
     if quant == P.Q8_0:
         return quantize_q8_0(w)
@@ -103,7 +154,21 @@ def quantize(w: np.ndarray, quant: int):
         return quantize_q4_0(w)
     if quant == P.A8G64:
         return quantize_a8g64(w)
+    if quant == P.Q5_0:
+        return quantize_q5_0(w)
+    if quant == P.A4G32:
+        return quantize_a4(w, 32)
+    if quant == P.A4G64:
+        return quantize_a4(w, 64)
     raise ValueError(f"unknown quant {quant}")
+
+
+def tensor_quant(m: P.ModelSpec, name: str) -> int:
+    """The weight format of matrix ``name``: the code predictor's tensors (``c<l>.*``,
+    ``cp.*``) take ``cp_quant`` when it is set."""
+    if m.cp_quant and (name.startswith("cp.") or (name.startswith("c") and name[1:2].isdigit())):
+        return m.cp_quant
+    return m.quant
 
 
 # ----------------------------------------------------------------------------- tensor list
@@ -183,7 +248,8 @@ def build_model_blob(m: P.ModelSpec, seed: int = 1, keep_fp32: bool = False):
         if keep_fp32:
             fp32[name] = w
         if role == "mat":
-            entries.append((name, _QKIND[m.quant], rows, cols, quantize(w, m.quant)))
+            q = tensor_quant(m, name)
+            entries.append((name, _QKIND[q], rows, cols, quantize(w, q)))
         else:
             entries.append((name, KIND_F32, rows, cols, w))
     return write_blob(m, entries), fp32

@@ -57,8 +57,9 @@ def test_tiny_gpt2_incremental_equals_full_recompute():
             assert tr.tokens[i] == int(np.argmax(ref[P_ - 1 + i]))
 
 
-def test_q4_gpt2_sampled_run_matches_recompute():
-    run = get_preset("tiny").with_model(quant=P.Q4_0, n_layer=1)
+@pytest.mark.parametrize("quant", [P.Q4_0, P.Q5_0])
+def test_q4_gpt2_sampled_run_matches_recompute(quant):
+    run = get_preset("tiny").with_model(quant=quant, n_layer=1)
     m = run.model
     blob, _ = build_model_blob(m)
     model = oracle.Model(blob)
@@ -136,8 +137,11 @@ def test_cfg_history_holds_the_fed_tokens_only():
     assert len(set(tr0.tokens)) < n + 1, tr0.tokens
 
 
-def test_qwen_frames_match_full_recompute():
-    m = _small_qwen()
+@pytest.mark.parametrize("cp_quant", [0, P.A4G32, P.A4G64])
+def test_qwen_frames_match_full_recompute(cp_quant):
+    """The Talker in 8-bit affine, the code predictor in its own format (4-bit
+    group 32 / 64 included: the blob records each tensor's format)."""
+    m = dataclasses.replace(_small_qwen(), cp_quant=cp_quant)
     blob, _ = build_model_blob(m)
     model = oracle.Model(blob)
     prompt = np.random.default_rng(6).integers(0, m.vocab, size=(1, 9)).astype(np.int32)

@@ -46,6 +46,8 @@ MUTANTS = {
                                                        oo.test_sampler_margin_at_a_top_p_cut_that_can_shrink]),
     25: ("mass factor 1+r instead of its square root", [oo.test_sampler_margin_at_a_top_p_cut_that_can_shrink,
                                                          oo.test_sampler_margin_at_a_top_p_cut_that_can_grow]),
+    26: ("Q5_0 fifth bit taken from the wrong element", [oo.test_q5_0_hand_block]),
+    27: ("4-bit affine codes read high nibble first", [lambda: oo.test_a4_hand_group(oo.KA4G32, 32)]),
 }
 
 

@@ -11,9 +11,9 @@ import torch
 import torch.nn.functional as F
 
 import oracle
-from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64
+from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64, quantize_q5_0, quantize_a4
 
-KQ8, KQ4, KA8 = 1, 2, 3
+KQ8, KQ4, KA8, KQ5, KA4G32, KA4G64 = 1, 2, 3, 4, 5, 6
 F32 = np.float32
 
 
@@ -69,6 +69,45 @@ def test_a8g64_hand_group():
     assert np.array_equal(out, (0.125 * q.astype(np.float32) - 3.0).astype(np.float32))
 
 
+def test_q5_0_hand_block():
+    """Block with d = -0.5, fifth bits 0xF0F0F0F0 and byte j = j | (15-j) << 4:
+    element j (j<16) has code j + 16*bit(j) and element 16+j has code (15-j) +
+    16*bit(16+j); the value is d*(code - 16).  The two halves of the fifth-bit
+    word are different (bits 4-7 and 12-15 of each half set), so a bit taken
+    from the wrong element changes the result."""
+    blk = np.zeros(22, np.uint8)
+    blk[0:2] = np.array([-0.5], np.float16).view(np.uint8)
+    qh = 0xF0F0F00F
+    blk[2:6] = np.array([qh], "<u4").view(np.uint8)
+    for j in range(16):
+        blk[6 + j] = j | ((15 - j) << 4)
+    out = oracle.dequant(KQ5, blk, 1, 32)[0]
+    codes = [j + 16 * ((qh >> j) & 1) for j in range(16)] + [(15 - j) + 16 * ((qh >> (16 + j)) & 1) for j in range(16)]
+    exp = np.array([-0.5 * (c - 16) for c in codes], np.float32)
+    assert np.array_equal(out, exp)
+    # the extremes: code 0 -> -16 d, code 31 -> 15 d
+    blk[2:6] = np.array([0x0000FFFF], "<u4").view(np.uint8)
+    blk[6:] = 0xF0   # low nibble 0 (elements 0..15), high nibble 15 (elements 16..31)
+    out = oracle.dequant(KQ5, blk, 1, 32)[0]
+    assert np.array_equal(out, np.array([-0.5 * 0] * 16 + [-0.5 * -1] * 16, np.float32))
+
+
+@pytest.mark.parametrize("kind,gs", [(KA4G32, 32), (KA4G64, 64)])
+def test_a4_hand_group(kind, gs):
+    """Two groups per row, codes 0..15 repeated: element 2i sits in the low
+    nibble of byte i, element 2i+1 in its high nibble; value scale*q + bias with
+    each group's own scale and bias."""
+    q = (np.arange(2 * gs) * 7 % 16).astype(np.uint8)
+    packed = (q[0::2] | (q[1::2] << 4)).astype(np.uint8)
+    scale = np.array([0.125, -0.25], np.float16)
+    bias = np.array([-3.0, 0.5], np.float16)
+    data = np.concatenate([packed, scale.view(np.uint8), bias.view(np.uint8)])
+    out = oracle.dequant(kind, data, 1, 2 * gs)[0]
+    g = np.arange(2 * gs) // gs
+    exp = (scale.astype(np.float32)[g] * q.astype(np.float32) + bias.astype(np.float32)[g]).astype(np.float32)
+    assert np.array_equal(out, exp)
+
+
 def _roundtrip_case(kind, w):
     if kind == KQ8:
         q1 = quantize_q8_0(w)
@@ -86,21 +125,30 @@ def _roundtrip_case(kind, w):
         d = q1[..., 0:2].copy().view(np.float16).astype(np.float32)[..., 0]
         err = np.abs(deq - w).reshape(w.shape[0], -1, 32).max(-1)
         assert np.all(err <= np.abs(d) * (1 + 8 * 2 ** -11) + 1e-12)
+    elif kind == KQ5:
+        q1 = quantize_q5_0(w)
+        deq = oracle.dequant(KQ5, q1, *w.shape)
+        q2 = quantize_q5_0(deq)
+        assert np.array_equal(q1, q2)
+        d = q1[..., 0:2].copy().view(np.float16).astype(np.float32)[..., 0]
+        err = np.abs(deq - w).reshape(w.shape[0], -1, 32).max(-1)
+        assert np.all(err <= np.abs(d) * (1 + 16 * 2 ** -11) + 1e-12)
     else:
-        q, s, b = quantize_a8g64(w)
+        gs, steps = {KA8: (64, 255), KA4G32: (32, 15), KA4G64: (64, 15)}[kind]
+        q, s, b = quantize_a8g64(w) if kind == KA8 else quantize_a4(w, gs)
         data = np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
-        deq = oracle.dequant(KA8, data, *w.shape)
-        q2, s2, b2 = quantize_a8g64(deq)
+        deq = oracle.dequant(kind, data, *w.shape)
+        q2, s2, b2 = quantize_a8g64(deq) if kind == KA8 else quantize_a4(deq, gs)
         assert np.array_equal(q, q2)
-        err = np.abs(deq - w).reshape(w.shape[0], -1, 64).max(-1)
+        err = np.abs(deq - w).reshape(w.shape[0], -1, gs).max(-1)
         sc = s.astype(np.float32)
-        # half a step, plus the fp16 rounding of bias and scale (up to 255 steps)
-        bound = 0.5 * sc + np.abs(b.astype(np.float32)) * 2 ** -11 + 255 * sc * 2 ** -11 + 1e-7
+        # half a step, plus the fp16 rounding of bias and scale (up to `steps` steps)
+        bound = 0.5 * sc + np.abs(b.astype(np.float32)) * 2 ** -11 + steps * sc * 2 ** -11 + 1e-7
         assert np.all(err <= bound)
     return deq
 
 
-@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8, KQ5, KA4G32, KA4G64])
 def test_dequant_roundtrip_and_bounds(kind):
     rng = np.random.default_rng(kind)
     w = (rng.standard_normal((37, 256)) * 0.02).astype(np.float32)
@@ -117,24 +165,32 @@ def test_dequant_roundtrip_and_bounds(kind):
         assert abs(deq[2, 5] - 0.5) <= 0.5 * 2 ** -11      # code +127 hits the max exactly up to fp16 d
     if kind == KQ4:
         assert abs(deq[3, 40] + 0.5) <= 0.5 * 2 ** -11     # code 0 -> -8 d = m up to fp16 d
-    if kind == KA8:
+    if kind == KQ5:
+        assert abs(deq[3, 40] + 0.5) <= 0.5 * 2 ** -11     # code 0 -> -16 d = m up to fp16 d
+    if kind in (KA8, KA4G32, KA4G64):
         assert np.all(deq[1, :64] == deq[1, 0])
 
 
 # ----------------------------------------------------------------------------- linear
 
-@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8])
+def quant_data(kind, w):
+    """The canonical stored bytes of w in format `kind` (affine: codes, scales, biases)."""
+    if kind == KQ8:
+        return quantize_q8_0(w)
+    if kind == KQ4:
+        return quantize_q4_0(w)
+    if kind == KQ5:
+        return quantize_q5_0(w)
+    q, s, b = quantize_a8g64(w) if kind == KA8 else quantize_a4(w, 32 if kind == KA4G32 else 64)
+    return np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
+
+
+@pytest.mark.parametrize("kind", [KQ8, KQ4, KA8, KQ5, KA4G32, KA4G64])
 def test_linear_against_float64_dot(kind):
     rng = np.random.default_rng(10 + kind)
     rows, cols = 70, 384
     w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
-    if kind == KQ8:
-        data = quantize_q8_0(w)
-    elif kind == KQ4:
-        data = quantize_q4_0(w)
-    else:
-        q, s, b = quantize_a8g64(w)
-        data = np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
+    data = quant_data(kind, w)
     deq = oracle.dequant(kind, data, rows, cols).astype(np.float64)
     x = rng.standard_normal(cols).astype(np.float32)
     bias = rng.standard_normal(rows).astype(np.float32)
