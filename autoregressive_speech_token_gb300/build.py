@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsd.so")
-SOURCES = ["k_gemv_q8.cu", "k_gemv_q4.cu", "k_gemv_a8.cu", "k_attn.cu", "k_attn_static.cu", "k_sample.cu", "k_sample_ladder.cu", "k_misc.cu", "k_step.cu", "k_cstep.cu", "k_qgemm.cu", "k_gemm16.cu", "k_gemm16_tc.cu", "k_gemm_tc.cu", "k_prefill.cu", "sd_api.cu"]
+SOURCES = ["k_gemv_q8.cu", "k_gemv_q4.cu", "k_gemv_a8.cu", "k_gemv_q5.cu", "k_gemv_a4.cu", "k_attn.cu", "k_attn_static.cu", "k_sample.cu", "k_sample_ladder.cu", "k_misc.cu", "k_step.cu", "k_cstep.cu", "k_qgemm.cu", "k_gemm16.cu", "k_gemm16_tc.cu", "k_gemm_tc.cu", "k_prefill.cu", "sd_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -253,18 +253,7 @@ __global__ void k_dequant_split(const QMat W, __half* __restrict__ hi, __half* _
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t r = i / K;
         const int k = (int)(i - r * K);
-        float w;
-        if (W.kind == SD_Q4_0) {
-            const uint8_t byte = W.q[r * (K / 2) + (k / 32) * 16 + (k & 15)];
-            const int q = ((k & 31) < 16 ? (byte & 0xF) : (byte >> 4)) - 8;
-            w = __half2float(reinterpret_cast<const __half*>(W.s)[r * (K / 32) + k / 32]) * (float)q;
-        } else if (W.kind == SD_Q8_0) {
-            const int q = (int8_t)W.q[r * K + k];
-            w = __half2float(reinterpret_cast<const __half*>(W.s)[r * (K / 32) + k / 32]) * (float)q;
-        } else {
-            const __half2 sb = reinterpret_cast<const __half2*>(W.s)[r * (K / 64) + k / 64];
-            w = fmaf(__low2float(sb), (float)W.q[r * K + k], __high2float(sb));
-        }
+        const float w = q_value(W, r, k);
         const __half h = __float2half_rn(w);
         hi[i] = h;
         lo[i] = __float2half_rn(w - __half2float(h));

@@ -11,8 +11,10 @@
 // every row it visits) and R rows per tile; K > 1024 is split across WK warps
 // whose partial sums meet in shared memory in a fixed order (deterministic).
 // Weights are read once with 128-bit streaming loads; dequantisation happens
-// in registers: Q4_0 nibbles and Q8_0 bytes become exact floats through the
-// 2^23 exponent trick, the block scale multiplies the block's partial sum.
+// in registers: Q4_0 / Q5_0 / 4-bit affine nibbles (Q5_0 with its fifth bit)
+// and Q8_0 / 8-bit affine bytes become exact floats through the 2^23 exponent
+// trick, the block scale multiplies the block's partial sum (affine formats add
+// bias times the activations' block sum).
 #pragma once
 #include "sd_internal.cuh"
 
@@ -63,10 +65,15 @@ __device__ __forceinline__ void block_sum(float (&v)[NB], float* scratch) {
 __device__ __forceinline__ int pidx(int k) { return k + ((k >> 5) << 2); }
 __host__ __device__ __forceinline__ int padded(int K) { return K + (K >> 3); }
 
+// 4-bit codes (16-byte units of 32 elements), affine formats, groups of 64
+template <int QK> constexpr bool kNib = QK == SD_Q4_0 || QK == SD_Q5_0 || QK == SD_A4G32 || QK == SD_A4G64;
+template <int QK> constexpr bool kAff = QK == SD_A8G64 || QK == SD_A4G32 || QK == SD_A4G64;
+template <int QK> constexpr bool kG64 = QK == SD_A8G64 || QK == SD_A4G64;
+
 template <int QK>
 struct Unit {
     // 16-byte weight units per lane per 1024-element warp slice
-    static constexpr int kU = (QK == SD_Q4_0) ? 1 : 2;
+    static constexpr int kU = kNib<QK> ? 1 : 2;
 };
 
 // Partial dot product of one 16-byte unit with the lane's activations.
@@ -84,6 +91,43 @@ __device__ __forceinline__ float dot_q4(const uint4 w, const float* x) {
             const float fhi = __int_as_float(0x4B000000u | hi) - (kMagic + 8.0f);
             s = fmaf(flo, x[4 * i + k], s);
             s = fmaf(fhi, x[16 + 4 * i + k], s);
+        }
+    }
+    return s;
+}
+
+// Q5_0: the nibbles as in dot_q4 plus the fifth bit of element j in bit j of qh; code - 16
+__device__ __forceinline__ float dot_q5(const uint4 w, const uint32_t qh, const float* x) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = 4 * i + k;
+            const uint32_t lo = ((wd[i] >> (8 * k)) & 0xFu) | (((qh >> j) & 1u) << 4);
+            const uint32_t hi = ((wd[i] >> (8 * k + 4)) & 0xFu) | (((qh >> (j + 16)) & 1u) << 4);
+            const float flo = __int_as_float(0x4B000000u | lo) - (kMagic + 16.0f);  // q - 16, exact
+            const float fhi = __int_as_float(0x4B000000u | hi) - (kMagic + 16.0f);
+            s = fmaf(flo, x[j], s);
+            s = fmaf(fhi, x[16 + j], s);
+        }
+    }
+    return s;
+}
+
+// unsigned 4-bit codes in the dot_q4 layout (affine formats)
+__device__ __forceinline__ float dot_u4(const uint4 w, const float* x) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = (wd[i] >> (8 * k)) & 0xFu;
+            const uint32_t hi = (wd[i] >> (8 * k + 4)) & 0xFu;
+            s = fmaf(__int_as_float(0x4B000000u | lo) - kMagic, x[4 * i + k], s);
+            s = fmaf(__int_as_float(0x4B000000u | hi) - kMagic, x[16 + 4 * i + k], s);
         }
     }
     return s;
@@ -128,21 +172,29 @@ __device__ __forceinline__ float silu(float t) { return t / (1.0f + expf(-t)); }
 // bias as one half2) into registers; issued a tile ahead, so neither the
 // codes nor the scales are waited for inside the dot products.
 template <int QK, int R, int U>
-__device__ __forceinline__ void load_tile(uint4 (&w)[R][U], uint32_t (&sc)[R][U], const GemvArgs& a, int tt, int WR,
-                                          int rg, int rows, int row_bytes, int spr, const int (&ebase)[U], int K) {
+__device__ __forceinline__ void load_tile(uint4 (&w)[R][U], uint32_t (&sc)[R][U], uint32_t (&hb)[R][U],
+                                          const GemvArgs& a, int tt, int WR, int rg, int rows, int row_bytes, int spr,
+                                          const int (&ebase)[U], int K) {
     const int r0 = tt * WR * R + rg * R;
 #pragma unroll
     for (int i = 0; i < R; ++i) {
         const int r = r0 + i;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            hb[i][u] = 0u;
             if (r < rows && ebase[u] < K) {
-                const int boff = (QK == SD_Q4_0) ? (ebase[u] >> 1) : ebase[u];
+                const int boff = kNib<QK> ? (ebase[u] >> 1) : ebase[u];
+                const int gi = kG64<QK> ? (ebase[u] >> 6) : (ebase[u] >> 5);
                 w[i][u] = ld_stream(a.W.q + (size_t)r * row_bytes + boff);
-                if (QK == SD_A8G64)
-                    sc[i][u] = __ldg(reinterpret_cast<const unsigned int*>(a.W.s) + (size_t)r * spr + (ebase[u] >> 6));
-                else
-                    sc[i][u] = __ldg(reinterpret_cast<const unsigned short*>(a.W.s) + (size_t)r * spr + (ebase[u] >> 5));
+                if (kAff<QK>) {
+                    sc[i][u] = __ldg(reinterpret_cast<const unsigned int*>(a.W.s) + (size_t)r * spr + gi);
+                } else if (QK == SD_Q5_0) {
+                    const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.W.s) + (size_t)r * spr + gi);
+                    sc[i][u] = v.x;
+                    hb[i][u] = v.y;
+                } else {
+                    sc[i][u] = __ldg(reinterpret_cast<const unsigned short*>(a.W.s) + (size_t)r * spr + gi);
+                }
             } else {
                 w[i][u] = make_uint4(0u, 0u, 0u, 0u);
                 sc[i][u] = 0u;
@@ -161,8 +213,8 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kw = warp % WK, rg = warp / WK;
     const int tiles = (rows + WR * R - 1) / (WR * R);
-    const int row_bytes = (QK == SD_Q4_0) ? (K >> 1) : K;
-    const int spr = (QK == SD_A8G64) ? (K >> 6) : (K >> 5);
+    const int row_bytes = kNib<QK> ? (K >> 1) : K;
+    const int spr = kG64<QK> ? (K >> 6) : (K >> 5);
 
     __shared__ float s_scr[33 * NB];
     __shared__ float s_tot[8 * R * NB];
@@ -172,16 +224,16 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
     int ebase[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        ebase[u] = (QK == SD_Q4_0) ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
-    constexpr int EPU = (QK == SD_Q4_0) ? 32 : 16;  // elements per unit
+        ebase[u] = kNib<QK> ? (kw * 1024 + lane * 32) : (kw * 1024 + u * 512 + lane * 16);
+    constexpr int EPU = kNib<QK> ? 32 : 16;  // elements per unit
 
     // issue the first tile's weight loads before the prologue: they do not
     // depend on the activations.
     uint4 w[R][U];
-    uint32_t scw[R][U];
+    uint32_t scw[R][U], hbw[R][U];
     int t = blockIdx.x;
     pdl_trigger();
-    if (t < tiles) load_tile<QK, R, U>(w, scw, a, t, WR, rg, rows, row_bytes, spr, ebase, K);
+    if (t < tiles) load_tile<QK, R, U>(w, scw, hbw, a, t, WR, rg, rows, row_bytes, spr, ebase, K);
     pdl_wait();  // activations come from the previous kernel
 
     // ---------------------------------------------------------------- prologue
@@ -297,19 +349,21 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (ebase[u] >= K) continue;
-                if (QK == SD_A8G64) {
+                if (kAff<QK>) {
                     const __half2 sb = *reinterpret_cast<const __half2*>(&scw[i][u]);
                     const float sc = __low2float(sb), bi = __high2float(sb);
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float dq = dot_u8(w[i][u], &xr[b][u * EPU]);
+                        const float dq = kNib<QK> ? dot_u4(w[i][u], &xr[b][0]) : dot_u8(w[i][u], &xr[b][u * EPU]);
                         acc[i][b] = fmaf(sc, dq, fmaf(bi, xsum[b][u], acc[i][b]));
                     }
                 } else {
-                    const float d = __half2float(__ushort_as_half((unsigned short)scw[i][u]));
+                    const float d = __half2float(__ushort_as_half((unsigned short)(scw[i][u] & 0xFFFFu)));
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float dq = (QK == SD_Q4_0) ? dot_q4(w[i][u], &xr[b][0]) : dot_s8(w[i][u], &xr[b][u * EPU]);
+                        const float dq = (QK == SD_Q4_0)   ? dot_q4(w[i][u], &xr[b][0])
+                                         : (QK == SD_Q5_0) ? dot_q5(w[i][u], hbw[i][u], &xr[b][0])
+                                                           : dot_s8(w[i][u], &xr[b][u * EPU]);
                         acc[i][b] = fmaf(d, dq, acc[i][b]);
                     }
                 }
@@ -317,7 +371,7 @@ __global__ void __launch_bounds__(256) k_gemv(const GemvArgs a) {
         }
         // prefetch the next tile while reducing this one
         const int tn = t + gridDim.x;
-        if (tn < tiles) load_tile<QK, R, U>(w, scw, a, tn, WR, rg, rows, row_bytes, spr, ebase, K);
+        if (tn < tiles) load_tile<QK, R, U>(w, scw, hbw, a, tn, WR, rg, rows, row_bytes, spr, ebase, K);
 
 #pragma unroll
         for (int i = 0; i < R; ++i)
@@ -392,7 +446,7 @@ cudaError_t launch_t(const GemvArgs& a, int sm_count, cudaStream_t st) {
 }
 
 inline cudaError_t check_gemv(const GemvArgs& a) {
-    if (a.W.cols % 32 || (a.W.kind == SD_A8G64 && a.W.cols % 64) || a.W.cols > 8192) return cudaErrorInvalidValue;
+    if (!q_valid(a.W.kind) || a.W.cols % q_group(a.W.kind) || a.W.cols > 8192) return cudaErrorInvalidValue;
     if (a.epi == EPI_SWIGLU && a.W.rows % 2) return cudaErrorInvalidValue;
     if (a.x_stride % 4 || (reinterpret_cast<uintptr_t>(a.x) & 15)) return cudaErrorInvalidValue;
     if (a.nb != 1 && a.nb != 2) return cudaErrorInvalidValue;

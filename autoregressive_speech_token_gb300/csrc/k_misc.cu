@@ -13,7 +13,7 @@ namespace {
 // rows are interleaved: canonical row r < ff -> 2r, row ff + r -> 2r + 1.
 __global__ void k_repack(int kind, const uint8_t* __restrict__ canon, int rows, int cols, int swiglu_ff,
                          uint8_t* __restrict__ q, void* __restrict__ s) {
-    const int gs = (kind == SD_A8G64) ? 64 : 32;
+    const int gs = q_group(kind);
     const int nblk = cols / gs;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)rows * nblk) return;
@@ -29,6 +29,28 @@ __global__ void k_repack(int kind, const uint8_t* __restrict__ canon, int rows, 
         uint8_t* dq = q + (size_t)dr * (cols / 2) + (size_t)blk * 16;
         for (int j = 0; j < 16; ++j) dq[j] = src[2 + j];
         reinterpret_cast<uint16_t*>(s)[(size_t)dr * nblk + blk] = (uint16_t)(src[0] | (src[1] << 8));
+    } else if (kind == SD_Q5_0) {
+        const uint8_t* src = canon + ((size_t)r * nblk + blk) * 22;
+        uint8_t* dq = q + (size_t)dr * (cols / 2) + (size_t)blk * 16;
+        for (int j = 0; j < 16; ++j) dq[j] = src[6 + j];
+        const uint32_t qh = (uint32_t)src[2] | ((uint32_t)src[3] << 8) | ((uint32_t)src[4] << 16) | ((uint32_t)src[5] << 24);
+        reinterpret_cast<uint2*>(s)[(size_t)dr * nblk + blk] = make_uint2((uint32_t)(src[0] | (src[1] << 8)), qh);
+    } else if (kind == SD_A4G32 || kind == SD_A4G64) {
+        // canonical: element 2i in the low nibble of byte i; device: per 32-element block, element j
+        // in the low and element j+16 in the high nibble of byte j
+        const uint8_t* src = canon + (size_t)r * (cols / 2) + (size_t)blk * (gs / 2);
+        uint8_t* dq = q + (size_t)dr * (cols / 2) + (size_t)blk * (gs / 2);
+        for (int b = 0; b < gs / 32; ++b)
+            for (int j = 0; j < 16; ++j) {
+                const int e0 = 32 * b + j, e1 = e0 + 16;
+                const int c0 = (src[e0 >> 1] >> ((e0 & 1) * 4)) & 0xF, c1 = (src[e1 >> 1] >> ((e1 & 1) * 4)) & 0xF;
+                dq[16 * b + j] = (uint8_t)(c0 | (c1 << 4));
+            }
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(canon + (size_t)rows * (cols / 2));
+        const uint16_t* bi = sc + (size_t)rows * nblk;
+        uint16_t* d = reinterpret_cast<uint16_t*>(s) + 2 * ((size_t)dr * nblk + blk);
+        d[0] = sc[(size_t)r * nblk + blk];
+        d[1] = bi[(size_t)r * nblk + blk];
     } else {
         const uint8_t* src = canon + (size_t)r * cols + (size_t)blk * 64;
         uint8_t* dq = q + (size_t)dr * cols + (size_t)blk * 64;
@@ -46,21 +68,7 @@ __global__ void k_dequant(QMat W, float* __restrict__ out) {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)W.rows * W.cols) return;
     const int r = (int)(idx / W.cols), k = (int)(idx % W.cols);
-    float v;
-    if (W.kind == SD_Q8_0) {
-        const float d = __half2float(reinterpret_cast<const __half*>(W.s)[(size_t)r * (W.cols / 32) + k / 32]);
-        v = d * (float)(int8_t)W.q[(size_t)r * W.cols + k];
-    } else if (W.kind == SD_Q4_0) {
-        const float d = __half2float(reinterpret_cast<const __half*>(W.s)[(size_t)r * (W.cols / 32) + k / 32]);
-        const int j = k & 31;
-        const uint8_t byte = W.q[(size_t)r * (W.cols / 2) + (k / 32) * 16 + (j & 15)];
-        const int nib = j < 16 ? (byte & 0xF) : (byte >> 4);
-        v = d * (float)(nib - 8);
-    } else {
-        const __half2 sb = reinterpret_cast<const __half2*>(W.s)[(size_t)r * (W.cols / 64) + k / 64];
-        v = __fmaf_rn(__low2float(sb), (float)W.q[(size_t)r * W.cols + k], __high2float(sb));
-    }
-    out[idx] = v;
+    out[idx] = q_value(W, (size_t)r, k);
 }
 
 __global__ void k_embed(const EmbedArgs a) {
@@ -142,13 +150,17 @@ cudaError_t launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t st) {
         case SD_Q8_0: return launch_gemv_q8(a, sm_count, st);
         case SD_Q4_0: return launch_gemv_q4(a, sm_count, st);
         case SD_A8G64: return launch_gemv_a8(a, sm_count, st);
+        case SD_Q5_0: return launch_gemv_q5(a, sm_count, st);
+        case SD_A4G32:
+        case SD_A4G64: return launch_gemv_a4(a, sm_count, st);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_repack(int kind, const uint8_t* canon, int rows, int cols, int swiglu_ff, uint8_t* q, void* s,
                           cudaStream_t st) {
-    const int gs = (kind == SD_A8G64) ? 64 : 32;
+    if (!q_valid(kind)) return cudaErrorInvalidValue;
+    const int gs = q_group(kind);
     const long long n = (long long)rows * (cols / gs);
     const int threads = 256;
     k_repack<<<(unsigned)((n + threads - 1) / threads), threads, 0, st>>>(kind, canon, rows, cols, swiglu_ff, q, s);

@@ -178,12 +178,12 @@ int dalloc(sd_ctx* c, T** p, size_t bytes) {
 
 int validate_cfg(const sd_model_config& m) {
     if (m.arch < SD_ARCH_GPT2 || m.arch > SD_ARCH_QWEN_TTS) return 0;
-    if (m.quant < SD_Q8_0 || m.quant > SD_A8G64) return 0;
+    if (!q_valid(m.quant)) return 0;
     if (m.n_layer < 0 || m.d_model <= 0 || m.n_head <= 0 || m.n_kv_head <= 0 || m.head_dim <= 0) return 0;
     if (m.head_dim != 64 && m.head_dim != 128) return 0;
     if (m.n_head % m.n_kv_head || m.n_head / m.n_kv_head > 4) return 0;
     if (m.d_ff <= 0 || m.vocab <= 0 || m.vocab > 16384 || m.max_ctx <= 0 || m.batch < 1 || m.batch > kMaxRows) return 0;
-    const int gs = m.quant == SD_A8G64 ? 64 : 32;
+    const int gs = q_group(m.quant);
     if (m.d_model % gs || m.d_ff % gs || (m.n_head * m.head_dim) % gs) return 0;
     if (m.d_model > 8192 || m.d_ff > 8192) return 0;
     if (m.arch == SD_ARCH_GPT2 && m.n_head != m.n_kv_head) return 0;
@@ -256,7 +256,23 @@ int gemv(sd_ctx* c, const GemvArgs& a, cudaStream_t st) {
             x = c->nrm;
             ldx = a.W.cols;
         }
-        if (c->rows_gemm_mma) {
+        const bool skinny_ok = a.W.kind == SD_Q8_0 || a.W.kind == SD_Q4_0 || a.W.kind == SD_A8G64;
+        if (!skinny_ok) {
+            // formats the row GEMMs do not take: the matvec over pairs of rows (one weight read per pair)
+            e = cudaSuccess;
+            for (int r0 = 0; r0 < a.nb && e == cudaSuccess; r0 += 2) {
+                GemvArgs p = a;
+                p.pro = PRO_NONE;
+                p.nb = std::min(2, a.nb - r0);
+                p.x = x + (size_t)r0 * ldx;
+                p.x_stride = ldx;
+                p.y = a.y + (size_t)r0 * a.y_stride;
+                p.resid = a.resid ? a.resid + (size_t)r0 * a.y_stride : nullptr;
+                e = launch_gemv(p, c->sm_count, st);
+                c->count_launch++;
+            }
+            c->count_launch--;
+        } else if (c->rows_gemm_mma) {
             QGemmArgs g;
             g.W = a.W; g.M = a.nb; g.x = x; g.ldx = ldx; g.epi = a.epi; g.bias = a.bias; g.resid = a.resid;
             g.y = a.y; g.ldy = a.y_stride;
@@ -591,19 +607,29 @@ int find_f32(sd_ctx* c, Blob& b, const std::string& name, int64_t n, uint8_t*& a
 }
 
 size_t qbytes(int kind, int rows, int cols) {
-    const size_t q = kind == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
-    const size_t s = kind == SD_A8G64 ? (size_t)rows * (cols / 64) * 4 : (size_t)rows * (cols / 32) * 2;
+    const size_t q = q_code_bytes(kind, rows, cols);
+    const size_t s = (size_t)rows * (cols / q_group(kind)) * q_side_bytes(kind);
     return (q + 255) / 256 * 256 + (s + 255) / 256 * 256;
+}
+
+// A Talker + code-predictor blob may store the code predictor's matrices (c<l>.*, cp.*) in a
+// format of their own; every other matrix is in the config's format.
+bool own_format_allowed(const sd_ctx* c, const std::string& name) {
+    return c->cfg.arch == SD_ARCH_QWEN_TTS &&
+           (name.rfind("cp.", 0) == 0 || (name.size() > 1 && name[0] == 'c' && name[1] >= '0' && name[1] <= '9'));
 }
 
 int find_q(sd_ctx* c, Blob& b, const std::string& name, int rows, int cols, int swiglu_ff, uint8_t*& arena,
            QMat* out) {
     auto it = b.t.find(name);
-    if (it == b.t.end() || (int)it->second.kind != c->cfg.quant || (int)it->second.rows != rows ||
-        (int)it->second.cols != cols)
+    if (it == b.t.end() || (int)it->second.rows != rows || (int)it->second.cols != cols)
         return fail(c, SD_ERR_BLOB, "blob: missing or mis-shaped matrix '%s'", name.c_str());
-    const int kind = c->cfg.quant;
-    const size_t qsz = kind == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+    const int kind = (int)it->second.kind;
+    if (!q_valid(kind) || cols % q_group(kind) || (kind != c->cfg.quant && !own_format_allowed(c, name)))
+        return fail(c, SD_ERR_BLOB, "blob: matrix '%s' has format %d (config: %d)", name.c_str(), kind, c->cfg.quant);
+    if (it->second.nbytes < q_canon_bytes(kind, rows, cols))
+        return fail(c, SD_ERR_BLOB, "blob: matrix '%s' is truncated", name.c_str());
+    const size_t qsz = q_code_bytes(kind, rows, cols);
     uint8_t* q = arena;
     uint8_t* s = arena + (qsz + 255) / 256 * 256;
     cudaError_t e = launch_repack(kind, b.base + it->second.off, rows, cols, swiglu_ff, q, s, c->stream);
@@ -626,7 +652,12 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
     };
     auto Q = [&](const std::string& n, int rows, int cols, int swiglu_ff, QMat* out) {
         if (rc) return;
-        if (dry) { sum += qbytes(m.quant, rows, cols); return; }
+        if (dry) {
+            auto it = b.t.find(n);
+            const int k = it != b.t.end() && q_valid((int)it->second.kind) ? (int)it->second.kind : m.quant;
+            sum += qbytes(k, rows, cols);
+            return;
+        }
         rc = find_q(c, b, n, rows, cols, swiglu_ff, arena, out);
     };
     auto stack = [&](DStack& s, const char* pfx) {
@@ -694,10 +725,20 @@ constexpr size_t kFrameD2H = kStepD2H + sizeof(DevState::codes);
 int setup_tc_prefill(sd_ctx* c) {
     c->tc_prefill = false;
     const char* env = getenv("SD_PREFILL");
-    if (!c->gemm_prefill || (env && strcmp(env, "mma") == 0)) return SD_OK;
+    // the mma.sync prefill GEMM takes Q8_0, Q4_0 and 8-bit affine; other formats prefill through
+    // the tensor-core GEMM or, where that does not apply, the per-position step graphs
+    const bool mma_ok = c->cfg.quant == SD_Q8_0 || c->cfg.quant == SD_Q4_0 || c->cfg.quant == SD_A8G64;
+    if (!c->gemm_prefill) return SD_OK;
+    if (env && strcmp(env, "mma") == 0) {
+        if (!mma_ok) c->gemm_prefill = false;
+        return SD_OK;
+    }
     DStack& s = c->main;
     const int qd = s.H * s.hd;
-    if (s.d % 64 || qd % 64 || s.ff % 64) return SD_OK;
+    if (s.d % 64 || qd % 64 || s.ff % 64) {
+        if (!mma_ok) c->gemm_prefill = false;
+        return SD_OK;
+    }
     c->tc_w.assign(s.n_layer, std::array<CUtensorMap, 8>{});
     int rc;
     for (int l = 0; l < s.n_layer; ++l) {
@@ -866,7 +907,7 @@ int setup_persistent(sd_ctx* c) {
     c->persistent = false;
     c->cpersistent = false;
     const int mode = persistent_mode(c->B);
-    if (!mode || m.arch == SD_ARCH_QWEN_TTS || m.quant == SD_A8G64 || c->B > 2) return SD_OK;
+    if (!mode || m.arch == SD_ARCH_QWEN_TTS || (m.quant != SD_Q8_0 && m.quant != SD_Q4_0) || c->B > 2) return SD_OK;
     if (mode == 1 || mode == 3) {
         int rc0 = setup_cstep(c);
         if (rc0 || c->cpersistent || mode == 3) return rc0;
@@ -1540,13 +1581,10 @@ int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int
     sd_ctx* c = nullptr;
     if (!canon || !out) return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_create: NULL argument");
     *out = nullptr;
-    if (quant < SD_Q8_0 || quant > SD_A8G64 || rows < 1 || cols < 1 || rows > (1 << 24) || cols > 65536 ||
-        cols % (quant == SD_A8G64 ? 64 : 32))
+    if (!q_valid(quant) || rows < 1 || cols < 1 || rows > (1 << 24) || cols > 65536 || cols % q_group(quant))
         return fail(c, SD_ERR_INVALID_ARG, "sd_qmat_create: bad shape or kind");
     CK(cudaSetDevice(device));
-    const size_t canon_bytes = quant == SD_Q8_0   ? (size_t)rows * (cols / 32) * 34
-                               : quant == SD_Q4_0 ? (size_t)rows * (cols / 32) * 18
-                                                  : (size_t)rows * cols + (size_t)rows * (cols / 64) * 4;
+    const size_t canon_bytes = q_canon_bytes(quant, (size_t)rows, (size_t)cols);
     const uint8_t* src = reinterpret_cast<const uint8_t*>(canon);
     void* staging = nullptr;
     if (!on_device) {
@@ -1562,7 +1600,7 @@ int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int
         if (staging) cudaFree(staging);
         return fail(c, SD_ERR_OOM, "sd_qmat_create: cudaMalloc failed");
     }
-    const size_t qsz = quant == SD_Q4_0 ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+    const size_t qsz = q_code_bytes(quant, (size_t)rows, (size_t)cols);
     q->m.kind = quant; q->m.rows = (int)rows; q->m.cols = (int)cols;
     q->m.q = reinterpret_cast<uint8_t*>(q->buf);
     q->m.s = reinterpret_cast<uint8_t*>(q->buf) + (qsz + 255) / 256 * 256;

@@ -42,13 +42,58 @@ constexpr int kMaxCodebooks = SD_MAX_CODEBOOKS;
 //   Q8_0 : q = int8 [rows][cols],   s = __half  [rows][cols/32]
 //   Q4_0 : q = bytes [rows][cols/2] (16-byte block of nibbles, element j low /
 //          j+16 high nibble of byte j), s = __half [rows][cols/32]
+//   Q5_0 : q = low nibbles as Q4_0, s = uint2 [rows][cols/32] = (fp16 d in the
+//          low half of x, fifth bits in y: bit j = element j of the block)
 //   A8G64: q = uint8 [rows][cols],  s = __half2 [rows][cols/64] = (scale, bias)
+//   A4G32 / A4G64: q = nibbles as Q4_0 (unsigned codes), s = __half2
+//          [rows][cols/g] = (scale, bias)
 struct QMat {
     int kind = 0;
     int rows = 0, cols = 0;
     const uint8_t* q = nullptr;
     const void* s = nullptr;
 };
+
+__host__ __device__ inline bool q_valid(int k) { return k >= SD_Q8_0 && k <= SD_A4G64; }
+__host__ __device__ inline bool q_affine(int k) { return k == SD_A8G64 || k == SD_A4G32 || k == SD_A4G64; }
+__host__ __device__ inline bool q_nibbles(int k) { return k == SD_Q4_0 || k == SD_Q5_0 || k == SD_A4G32 || k == SD_A4G64; }
+__host__ __device__ inline int q_group(int k) { return (k == SD_A8G64 || k == SD_A4G64) ? 64 : 32; }
+// device layout: bytes of the code array, and side bytes (scale, scale+bias, scale+fifth bits) per group
+__host__ __device__ inline size_t q_code_bytes(int k, size_t rows, size_t cols) {
+    return q_nibbles(k) ? rows * cols / 2 : rows * cols;
+}
+__host__ __device__ inline int q_side_bytes(int k) { return q_affine(k) ? 4 : k == SD_Q5_0 ? 8 : 2; }
+// bytes of one canonical blob tensor
+__host__ __device__ inline size_t q_canon_bytes(int k, size_t rows, size_t cols) {
+    if (k == SD_Q8_0) return rows * (cols / 32) * 34;
+    if (k == SD_Q4_0) return rows * (cols / 32) * 18;
+    if (k == SD_Q5_0) return rows * (cols / 32) * 22;
+    return q_code_bytes(k, rows, cols) + rows * (cols / q_group(k)) * 4;
+}
+
+#ifdef __CUDACC__
+// Element (r, k) of a repacked matrix: the bit-exact definition of each format.
+__device__ __forceinline__ float q_value(const QMat& W, size_t r, int k) {
+    const int K = W.cols, g = q_group(W.kind);
+    if (W.kind == SD_Q8_0)
+        return __half2float(reinterpret_cast<const __half*>(W.s)[r * (K / 32) + k / 32]) * (float)(int8_t)W.q[r * K + k];
+    if (W.kind == SD_A8G64) {
+        const __half2 sb = reinterpret_cast<const __half2*>(W.s)[r * (K / 64) + k / 64];
+        return __fmaf_rn(__low2float(sb), (float)W.q[r * K + k], __high2float(sb));
+    }
+    const uint8_t byte = W.q[r * (K / 2) + (k / 32) * 16 + (k & 15)];
+    const int nib = (k & 31) < 16 ? (byte & 0xF) : (byte >> 4);
+    if (W.kind == SD_Q4_0)
+        return __half2float(reinterpret_cast<const __half*>(W.s)[r * (K / 32) + k / 32]) * (float)(nib - 8);
+    if (W.kind == SD_Q5_0) {
+        const uint2 side = reinterpret_cast<const uint2*>(W.s)[r * (K / 32) + k / 32];
+        const int code = nib | (int)(((side.y >> (k & 31)) & 1u) << 4);
+        return __half2float(__ushort_as_half((unsigned short)(side.x & 0xFFFFu))) * (float)(code - 16);
+    }
+    const __half2 sb = reinterpret_cast<const __half2*>(W.s)[r * (K / g) + k / g];
+    return __fmaf_rn(__low2float(sb), (float)nib, __high2float(sb));
+}
+#endif
 
 enum Prologue : int { PRO_NONE = 0, PRO_LN = 1, PRO_RMS = 2 };
 enum Epilogue : int { EPI_LINEAR = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
@@ -124,6 +169,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_gemv_q8(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_gemv_q4(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_gemv_a8(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_gemv_q5(const GemvArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_gemv_a4(const GemvArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t st);
 size_t attention_smem_bytes(const AttnArgs& a);
 cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t st);

@@ -13,8 +13,13 @@
  *     Read" (section 1: the Talker predicts codebook 0, the code predictor runs
  *     15 sequential passes for codebooks 1-15, and the sum of the 16 code
  *     embeddings is the next Talker input).
- * Weights are block quantised (Q8_0, Q4_0: journal Tier A item A3 and section
- * 3.23; 8-bit affine groups of 64: the blog's section 3).
+ * Weights are block quantised (Q8_0, Q5_0, Q4_0: journal Tier A item A3 and
+ * section 3.23; 8-bit affine groups of 64: the blog's section 3; 4-bit affine
+ * groups of 32 or 64: its section 5.8).  `quant` in the config names the format
+ * of every matrix, except that a Talker + code-predictor blob may store the
+ * code predictor's matrices in another format (each tensor records its own).
+ * The persistent decode step kernels take Q8_0 and Q4_0; the other formats
+ * decode through the per-operation step graph.
  *
  * Conventions shared by every entry point:
  *   - Return value: SD_OK (0) or a negative SD_ERR_* code.  Nothing aborts or
@@ -51,7 +56,7 @@ extern "C" {
 #define SD_ERR_DEVICE (-9)       /* a kernel flagged an out-of-range index and skipped it */
 
 enum { SD_ARCH_GPT2 = 1, SD_ARCH_LLAMA = 2, SD_ARCH_QWEN_TTS = 3 };
-enum { SD_Q8_0 = 1, SD_Q4_0 = 2, SD_A8G64 = 3 };
+enum { SD_Q8_0 = 1, SD_Q4_0 = 2, SD_A8G64 = 3, SD_Q5_0 = 4, SD_A4G32 = 5, SD_A4G64 = 6 };
 
 #define SD_MAX_ROWS 16
 #define SD_MAX_CODEBOOKS 16

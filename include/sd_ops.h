@@ -20,16 +20,18 @@ extern "C" {
  * streams: codes of a row contiguous (16-byte units) and the fp16 scales (and
  * affine biases) in a separate array.  `canon` holds the canonical blob
  * bytes of one tensor: Q8_0 34-byte blocks, Q4_0 18-byte blocks (journal
- * section 3.23), or affine codes + scales + biases; host memory, or device
- * memory when on_device != 0.  cols must be a multiple of 32 (64 for
- * SD_A8G64). */
+ * section 3.23), Q5_0 22-byte blocks (fp16 d, 32 fifth bits, 16 nibble
+ * bytes), or affine codes (8-bit: one per byte; 4-bit: element 2i in the low
+ * nibble of byte i) + fp16 scales + fp16 biases; host memory, or device memory
+ * when on_device != 0.  cols must be a multiple of 32 (64 for SD_A8G64 and
+ * SD_A4G64). */
 typedef struct sd_qmat sd_qmat;
 int sd_qmat_create(int quant, const void* canon, int64_t rows, int64_t cols, int on_device, int device,
                    sd_qmat** out);
 void sd_qmat_destroy(sd_qmat* m);
 
-/* Dequantise to fp32 out_dev[rows][cols]: Q8_0 d*q, Q4_0 d*(q-8), affine
- * fma(scale, q, bias) -- bit-exact definitions of the formats. */
+/* Dequantise to fp32 out_dev[rows][cols]: Q8_0 d*q, Q4_0 d*(q-8), Q5_0
+ * d*(q-16), affine fma(scale, q, bias) -- bit-exact definitions of the formats. */
 int sd_qmat_dequant(const sd_qmat* m, float* out_dev, void* stream);
 
 /* y_dev[b][r] = sum_k W[r][k] x_dev[b][k] (+ bias_dev[r]) for b < nb (nb 1 or

@@ -168,6 +168,25 @@ def test_tiny_q4_sampled(sd):
     _check_t3(sd, run, 40)
 
 
+def test_tiny_q5_sampled_every_prefill_path(sd, prefill_path):
+    """Q5_0 weights (journal, Tier A item A3): the per-operation step graph
+    decodes (the persistent kernels take Q8_0 / Q4_0), the prompt goes through
+    the tensor-core GEMM, or the step graphs where the mma.sync GEMM is asked for."""
+    run = get_preset("tiny").with_model(quant=P.Q5_0)
+    run = dataclasses.replace(run, sampler=SamplerSpec(0.8, 1000, 0.95, False))
+    _check_t3(sd, run, 24)
+
+
+def test_llama_q5_two_rows(sd):
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=3, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q5_0)
+    run = get_preset("llama_q4").with_model(**{f: getattr(spec, f) for f in
+                                               ("n_layer", "d_model", "n_head", "n_kv_head", "d_ff", "vocab",
+                                                "max_ctx", "quant")})
+    prompt = np.random.default_rng(2).integers(0, 1000, size=(2, 40)).astype(np.int32)
+    _check_t3(sd, run, 30, prompt=prompt)
+
+
 def test_gpt2m_q8_greedy(sd):
     """GPT-2-Medium Q8_0 at its configured length: 150-token prompt, 250 greedy steps."""
     run = get_preset("gpt2m_q8")
@@ -597,6 +616,21 @@ def test_qwen_small(sd, prefill_path):
                        cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
     prompt = np.random.default_rng(3).integers(0, 300, size=(2, 12)).astype(np.int32)
     _check_qwen(sd, spec, prompt, 4, SamplerSpec(0.9, 50, 0.95, False), "qwen small")
+
+
+@pytest.mark.parametrize("cp_quant", [P.A4G32, P.A4G64])
+@pytest.mark.parametrize("rows", [1, 16])
+def test_qwen_code_predictor_4bit(sd, cp_quant, rows):
+    """The Talker in 8-bit affine and the code predictor in 4-bit affine, group
+    32 or 64 ("Every Frame Is a Memory Read", section 5.8), at one row and at
+    sixteen rollout rows (matvecs over pairs of rows for the 4-bit matrices)."""
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=rows, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16, cp_quant=cp_quant)
+    prompt = np.random.default_rng(5).integers(0, 300, size=(rows, 12)).astype(np.int32)
+    _check_qwen(sd, spec, prompt, 3, SamplerSpec(0.9, 50, 0.95, False),
+                f"qwen cp {P.QUANT_NAMES[cp_quant]}")
 
 
 def test_qwen_full_size(sd):

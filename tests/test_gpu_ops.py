@@ -6,13 +6,14 @@ import pytest
 
 import oracle
 from synth import uniform_draws
-from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64
+from synth.weights import quantize_q4_0, quantize_q8_0, quantize_a8g64, quantize_q5_0, quantize_a4
 from tests.conftest import golden_path
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-KQ8, KQ4, KA8 = 1, 2, 3
+KQ8, KQ4, KA8, KQ5, KA4G32, KA4G64 = 1, 2, 3, 4, 5, 6
+AFFINE = {KA8: (64, None), KA4G32: (32, 32), KA4G64: (64, 64)}
 U = 2.0 ** -24
 
 
@@ -25,12 +26,18 @@ def sd():
     return pkg
 
 
+def _affine(kind, w):
+    return quantize_a8g64(w) if kind == KA8 else quantize_a4(w, AFFINE[kind][1])
+
+
 def _canon(kind, w):
     if kind == KQ8:
         return quantize_q8_0(w).reshape(-1)
     if kind == KQ4:
         return quantize_q4_0(w).reshape(-1)
-    q, s, b = quantize_a8g64(w)
+    if kind == KQ5:
+        return quantize_q5_0(w).reshape(-1)
+    q, s, b = _affine(kind, w)
     return np.concatenate([q.ravel(), s.view(np.uint8).ravel(), b.view(np.uint8).ravel()])
 
 
@@ -42,6 +49,9 @@ SHAPES = {
     KQ8: [(3072, 1024), (1024, 4096), (6563, 1024), (37, 96), (5, 1056), (1, 32)],
     KQ4: [(3072, 1024), (8192, 1024), (1024, 4096), (8194, 1024), (37, 96), (5, 1056)],
     KA8: [(4096, 2048), (2048, 6144), (12288, 2048), (1024, 3072), (2048, 1024), (37, 128), (5, 1088)],
+    KQ5: [(3072, 1024), (1024, 4096), (6563, 1024), (37, 96), (5, 1056), (1, 32)],
+    KA4G32: [(1024, 3072), (6144, 1024), (2048, 1024), (37, 96), (5, 1056)],
+    KA4G64: [(1024, 3072), (6144, 1024), (2048, 1024), (37, 128), (5, 1088)],
 }
 CASES = [(k, s) for k, ss in SHAPES.items() for s in ss]
 
@@ -86,9 +96,9 @@ def test_gemv_against_oracle(sd, kind, shape, nb):
         # fp32 accumulation in a reduction tree at most ~64 deep: |err| <= 64 u sum|w||x|
         # (affine: the factored form scale*sum(q x) + bias*sum(x) adds the |bias| sum|x| terms)
         mag = deq @ np.abs(x[b].astype(np.float64)) + np.abs(bias)
-        if kind == KA8:
-            q, s, bb = quantize_a8g64(_weights(rows, cols, rows + cols + kind))
-            gsum = np.abs(x[b].astype(np.float64)).reshape(-1, 64).sum(1)
+        if kind in AFFINE:
+            q, s, bb = _affine(kind, _weights(rows, cols, rows + cols + kind))
+            gsum = np.abs(x[b].astype(np.float64)).reshape(-1, AFFINE[kind][0]).sum(1)
             mag = mag + 2 * np.abs(bb.astype(np.float64)) @ gsum
         err = np.abs(y[b] - ref)
         bound = 64 * U * mag + 2 * U * np.abs(ref)
