@@ -109,6 +109,7 @@ def _declare(L):
     L.orc_pos.argtypes = [C.c_void_p, C.c_int]
     L.orc_copy_row.argtypes = [C.c_void_p, C.c_int, C.c_int]
     L.orc_token_forward.argtypes = [C.c_void_p, C.c_int, C.c_int32, f32p]
+    L.orc_embed_forward.argtypes = [C.c_void_p, C.c_int, f32p, f32p]
     L.orc_talker_forward.argtypes = [C.c_void_p, C.c_int, f32p, f32p, f32p]
     L.orc_talker_embed.argtypes = [C.c_void_p, C.c_int32, f32p]
     L.orc_cp_forward.argtypes = [C.c_void_p, C.c_int, f32p, C.c_int, f32p]
@@ -256,6 +257,14 @@ class Model:
             raise ValueError("orc_token_forward failed (bad token, row or full context)")
         return z
 
+    def embed_forward(self, row: int, e, vocab: int, want_logits=True):
+        """One position whose input is the vector e (a conditioning prefix row)."""
+        e = _f32(e)
+        z = np.empty(vocab, np.float32) if want_logits else None
+        if lib().orc_embed_forward(self._h, row, _p(e, C.c_float), _p(z, C.c_float)):
+            raise ValueError("orc_embed_forward failed (bad row or full context)")
+        return z
+
     def talker_embed(self, tok: int, d: int):
         e = np.empty(d, np.float32)
         if lib().orc_talker_embed(self._h, int(tok), _p(e, C.c_float)):
@@ -312,7 +321,7 @@ def _sampler_args(s):
 
 
 def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: int, sampler,
-           keep_logits=True, forced=None, logit_steps=None) -> list:
+           keep_logits=True, forced=None, logit_steps=None, prompt_embeds=None) -> list:
     """GPT-2 / Llama: prompt then n_steps decode steps per row.
 
     prompt [B][P]; draws [n_steps+1][B] (draw 0 samples the prefill's token).
@@ -320,7 +329,10 @@ def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: i
     with teacher forcing, forced[b][i-1] (the other implementation's token).
     Returns one Trace per row; trace.tokens[0] is the prefill's token and
     trace.logits[0] the logits of the last prompt position.  With logit_steps
-    given, only those steps keep their logits (others hold None)."""
+    given, only those steps keep their logits (others hold None).  With
+    prompt_embeds [B][P][d] the prompt positions take those vectors as their
+    inputs instead of the prompt tokens' embedding rows (prompt then only gives
+    the length)."""
     B = prompt.shape[0]
     V = spec.vocab
     traces = []
@@ -329,7 +341,11 @@ def run_t3(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_steps: i
         tr = Trace()
         z = None
         for i, tok in enumerate(prompt[b]):
-            z = model.token_forward(b, int(tok), V, want_logits=(i == prompt.shape[1] - 1))
+            last = i == prompt.shape[1] - 1
+            if prompt_embeds is not None:
+                z = model.embed_forward(b, prompt_embeds[b][i], V, want_logits=last)
+            else:
+                z = model.token_forward(b, int(tok), V, want_logits=last)
         for i in range(n_steps + 1):
             tok, margin = sample(z, u=float(draws[i][b]), **sa)
             tr.tokens.append(tok)

@@ -1021,6 +1021,21 @@ int orc_token_forward(orc_model* m, int row, int32_t tok, float* logits) {
     return 0;
 }
 
+/* One position of a GPT-2 / Llama row whose input is the vector e[d] instead of a
+ * token's embedding row (a conditioning prefix: text, speaker and conditioning
+ * embeddings, journal section 3.19); GPT-2 adds its learned position as for a
+ * token. */
+int orc_embed_forward(orc_model* m, int row, const float* e, float* logits) {
+    ostack* s = &m->s;
+    if (m->c.arch == A_QWEN || row < 0 || row >= s->batch || !e) return -1;
+    int pos = s->pos[row], d = s->d;
+    if (pos >= s->max_ctx) return -1;
+    for (int i = 0; i < d; ++i) s->x[i] = m->c.arch == A_GPT2 ? e[i] + m->wpe[(size_t)pos * d + i] : e[i];
+    if (stack_forward(s, row, s->x)) return -1;
+    if (logits) linear_q(&m->head, s->h, NULL, logits);
+    return 0;
+}
+
 int orc_talker_embed(orc_model* m, int32_t tok, float* e) {
     if (m->c.arch != A_QWEN || tok < 0 || tok >= m->c.vocab) return -1;
     memcpy(e, m->emb[0] + (size_t)tok * m->c.d_model, (size_t)m->c.d_model * 4);

@@ -85,6 +85,9 @@ int orc_token_forward(orc_model* m, int row, int32_t tok, float* logits);
  * position; logits0 (codebook-0 vocab) and hidden (final-normed state) may be NULL. */
 int orc_talker_forward(orc_model* m, int row, const float* e, float* logits0, float* hidden);
 /* Talker input for a prompt token: row `tok` of the codebook-0 embedding. */
+/* A GPT-2 / Llama position whose input is e[d] in place of a token's embedding
+ * row (GPT-2 still adds its learned position); logits may be NULL. */
+int orc_embed_forward(orc_model* m, int row, const float* e, float* logits);
 int orc_talker_embed(orc_model* m, int32_t tok, float* e);
 /* Code predictor: project v (Talker width) with Pr, run the CP stack at the
  * row's next CP position, and if head >= 1 write head `head`'s logits. */

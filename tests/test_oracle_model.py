@@ -89,6 +89,37 @@ def test_llama_gqa_rows_match_full_recompute():
             assert _rel(trs[b].logits[i], ref[11 + i]) < TOL, (b, i)
 
 
+@pytest.mark.parametrize("arch", [P.ARCH_GPT2, P.ARCH_LLAMA])
+def test_conditioning_prefix_matches_full_recompute(arch):
+    """A prompt given as input vectors (a conditioning prefix) instead of token
+    IDs: the logits equal a full recompute whose first positions take those
+    vectors; and vectors equal to the tokens' embedding rows give the token
+    prompt's run bit for bit."""
+    if arch == P.ARCH_GPT2:
+        m = dataclasses.replace(get_preset("tiny").model, n_layer=1, batch=2)
+    else:
+        m = _small_llama()
+    blob, fp32 = build_model_blob(m, keep_fp32=True)
+    rng = np.random.default_rng(8)
+    P_, n = 10, 6
+    emb = (rng.standard_normal((2, P_, m.d_model)) * 0.05).astype(np.float32)
+    prompt = np.zeros((2, P_), np.int32)
+    draws = uniform_draws(4, n + 1, 2)[..., 0]
+    s = SamplerSpec(temperature=0.8, top_k=50, top_p=0.9, greedy=False)
+    trs = oracle.run_t3(oracle.Model(blob), m, prompt, draws, n, s, prompt_embeds=emb)
+    for b in range(2):
+        ref = torch_ref.t3_logits(blob, m, [0] * P_ + trs[b].tokens[:n], prefix=emb[b])
+        for i in range(n + 1):
+            assert _rel(trs[b].logits[i], ref[P_ - 1 + i]) < TOL, (b, i)
+    toks = rng.integers(0, m.vocab, size=(2, P_)).astype(np.int32)
+    rows = fp32["wte"][toks]
+    a = oracle.run_t3(oracle.Model(blob), m, toks, draws, n, s)
+    e = oracle.run_t3(oracle.Model(blob), m, toks, draws, n, s, prompt_embeds=rows)
+    for b in range(2):
+        assert a[b].tokens == e[b].tokens
+        assert all(np.array_equal(x, y) for x, y in zip(a[b].logits, e[b].logits))
+
+
 def _cfg_run(ladder, n=10, seed=5):
     m = _small_llama()
     blob, _ = build_model_blob(m)

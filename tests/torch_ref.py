@@ -96,12 +96,17 @@ def stack_forward(W: Weights, X, pfx, n_layer, d, H, Hk, hd, ff, gpt2, eps, thet
     return r32(F.rms_norm(X, (d,), W.vec(nf + ".g"), eps=eps))
 
 
-def t3_logits(blob, m: P.ModelSpec, tokens):
-    """Logits at every position of a token sequence [T] (GPT-2 or Llama)."""
+def t3_logits(blob, m: P.ModelSpec, tokens, prefix=None):
+    """Logits at every position of a token sequence [T] (GPT-2 or Llama); with
+    prefix [P][d], positions 0..P-1 take those vectors in place of their tokens'
+    embedding rows (tokens then starts with P placeholders)."""
     W = Weights(blob)
     toks = torch.tensor(np.asarray(tokens, np.int64))
     T = len(toks)
     X = W.get("wte")[toks]
+    if prefix is not None:
+        X = X.clone()
+        X[: len(prefix)] = torch.from_numpy(np.asarray(prefix, np.float32)).to(X.dtype)
     gpt2 = m.arch == P.ARCH_GPT2
     if gpt2:
         X = r32(X + W.get("wpe")[:T])
