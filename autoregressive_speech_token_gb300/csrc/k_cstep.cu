@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(kCBlock, 1) k_cstep(const CStepArgs a) {
                     if ((unsigned)(w >> 32) != eb - 1u && !ll_spin(tp, eb - 1u, &w, a.err, budget)) w = 0ull;
                     t = (int)(unsigned)w;
                 }
-                if (t < 0 || t >= a.V) {
+                if (t < 0 || t >= a.V_in) {
                     atomicCAS(a.err, 0, 3);
                     t = 0;
                 }

@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_step(const StepArgs a) {
             for (int i = tid; i < NB * d; i += kThreads) {
                 const int b = i / d, k = i - b * d;
                 int t = tk[b];
-                if (t < 0 || t >= a.V) {
+                if (t < 0 || t >= a.V_in) {
                     atomicCAS(a.err, 0, 3);
                     t = 0;
                 }

@@ -98,6 +98,10 @@ struct sd_ctx {
     const float *wte = nullptr, *wpe = nullptr;
     QMat head, cp_proj;
     const float* emb[kMaxCodebooks] = {};
+    // the input embedding table (wte, or the Talker's emb[0]) has B * max_ctx extra rows after the
+    // vocabulary: sd_prefill_embeds writes row b's prompt vector p to row vocab + b * max_ctx + p
+    // and feeds that row's index as the prompt token
+    int v_in = 0;
     QMat cp_head[kMaxCodebooks];
     float* logits = nullptr;            // [B][V] or [B][16][Vmax]
     int logits_ld = 0, vmax = 0;
@@ -375,7 +379,7 @@ int enqueue_embed(sd_ctx* c, cudaStream_t st) {
     e.table = c->cfg.arch == SD_ARCH_QWEN_TTS ? c->emb[0] : c->wte;
     e.pos_table = c->wpe; e.pos_ptr = &c->ds->pos; e.tok = c->ds->tok;
     e.prompt = c->prompt; e.prompt_on = &c->ds->prompt_on; e.prompt_ld = c->cfg.max_ctx;
-    e.d = c->main.d; e.V = c->cfg.vocab; e.n_ctx = c->cfg.max_ctx; e.x = c->main.x; e.err = &c->ds->err;
+    e.d = c->main.d; e.V = c->v_in; e.n_ctx = c->cfg.max_ctx; e.x = c->main.x; e.err = &c->ds->err;
     cudaError_t err = launch_embed(e, c->B, st);
     c->count_launch++;
     if (err != cudaSuccess) return fail(c, SD_ERR_CUDA, "embed launch: %s", cudaGetErrorString(err));
@@ -470,9 +474,10 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
 // RoPE + fp16 KV store -> causal attention over the cache -> O GEMM (+resid)
 // -> norm -> FC / gate-up GEMM -> proj / down GEMM (+resid).  Leaves the KV
 // cache filled for positions < n and the device position at n.
-int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
+// Prompt positions [0, n) of rows [0, rows) through the prefill GEMMs.
+int enqueue_prefill_gemm(sd_ctx* c, int n, int rows, cudaStream_t st) {
     DStack& s = c->main;
-    const int B = c->B, d = s.d, qd = s.H * s.hd, kd = s.Hkv * s.hd, qr = s.qkv_rows();
+    const int B = rows, d = s.d, qd = s.H * s.hd, kd = s.Hkv * s.hd, qr = s.qkv_rows();
     const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
     auto ck = [&](cudaError_t e, const char* what) {
         return e == cudaSuccess ? SD_OK : fail(c, SD_ERR_CUDA, "prefill %s: %s", what, cudaGetErrorString(e));
@@ -494,7 +499,7 @@ int enqueue_prefill_gemm(sd_ctx* c, int n, cudaStream_t st) {
     for (int p0 = 0; p0 < n; p0 += c->pf_chunk) {
         const int np = std::min(c->pf_chunk, n - p0), M = B * np;
         if ((rc = ck(launch_embed_rows(qwen ? c->emb[0] : c->wte, c->wpe, c->prompt, c->cfg.max_ctx, B, p0, np, d,
-                                       c->cfg.vocab, c->pf_x, &c->ds->err, st), "embed")))
+                                       c->v_in, c->pf_x, &c->ds->err, st), "embed")))
             return rc;
         for (int l = 0; l < s.n_layer; ++l) {
             DLayer& L = s.L[l];
@@ -650,6 +655,18 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
         if (dry) { sum += (cnt * 4 + 255) / 256 * 256; return; }
         rc = find_f32(c, b, n, cnt, arena, out);
     };
+    // the input embedding table, followed by B * max_ctx zeroed rows for prompt vectors
+    const int64_t in_extra = (int64_t)c->B * m.max_ctx * m.d_model;
+    auto FI = [&](const std::string& n, int64_t cnt, const float** out) {
+        if (rc) return;
+        const size_t bytes = (size_t)((cnt + in_extra) * 4 + 255) / 256 * 256;
+        if (dry) { sum += bytes; return; }
+        uint8_t* slot = arena;
+        if ((rc = find_f32(c, b, n, cnt, arena, out))) return;
+        arena = slot + bytes;
+        if (cudaMemsetAsync(slot + cnt * 4, 0, (size_t)in_extra * 4, c->stream) != cudaSuccess)
+            rc = fail(c, SD_ERR_CUDA, "clearing the prompt-vector rows failed");
+    };
     auto Q = [&](const std::string& n, int rows, int cols, int swiglu_ff, QMat* out) {
         if (rc) return;
         if (dry) {
@@ -684,19 +701,21 @@ int load_all(sd_ctx* c, Blob& b, uint8_t* arena, size_t* total) {
         }
     };
     if (m.arch == SD_ARCH_GPT2) {
-        F("wte", (int64_t)m.vocab * m.d_model, &c->wte);
+        FI("wte", (int64_t)m.vocab * m.d_model, &c->wte);
         F("wpe", (int64_t)m.max_ctx * m.d_model, &c->wpe);
         stack(c->main, "l");
         F("lnf.g", m.d_model, &c->main.nfg); F("lnf.b", m.d_model, &c->main.nfb);
         Q("whead", m.vocab, m.d_model, 0, &c->head);
     } else if (m.arch == SD_ARCH_LLAMA) {
-        F("wte", (int64_t)m.vocab * m.d_model, &c->wte);
+        FI("wte", (int64_t)m.vocab * m.d_model, &c->wte);
         stack(c->main, "l");
         F("normf.g", m.d_model, &c->main.nfg);
         Q("whead", m.vocab, m.d_model, 0, &c->head);
     } else {
-        for (int j = 0; j < m.n_codebooks; ++j)
-            F("emb." + std::to_string(j), (int64_t)(j ? m.cp_vocab : m.vocab) * m.d_model, &c->emb[j]);
+        for (int j = 0; j < m.n_codebooks; ++j) {
+            if (j == 0) FI("emb.0", (int64_t)m.vocab * m.d_model, &c->emb[0]);
+            else F("emb." + std::to_string(j), (int64_t)m.cp_vocab * m.d_model, &c->emb[j]);
+        }
         stack(c->main, "t");
         F("t.normf.g", m.d_model, &c->main.nfg);
         Q("t.head", m.vocab, m.d_model, 0, &c->head);
@@ -793,7 +812,7 @@ int setup_cstep(sd_ctx* c) {
     a = CStepArgs();
     a.gpt2 = s.gpt2 ? 1 : 0; a.n_layer = s.n_layer; a.d = s.d; a.H = s.H; a.Hkv = s.Hkv; a.hd = s.hd; a.ff = s.ff;
     a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.quant = m.quant; a.eps = s.eps;
-    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
+    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe; a.V_in = c->v_in;
     a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.kc = s.kc; a.vc = s.vc;
     a.logits = c->logits;
     a.pos = &c->ds->pos; a.tok = c->ds->tok; a.u1 = c->ds->u1; a.sp = &c->ds->samp[0]; a.err = &c->ds->err;
@@ -923,7 +942,7 @@ int setup_persistent(sd_ctx* c) {
     StepArgs& a = c->step;
     a.gpt2 = s.gpt2 ? 1 : 0; a.n_layer = s.n_layer; a.d = s.d; a.H = s.H; a.Hkv = s.Hkv; a.hd = s.hd; a.ff = s.ff;
     a.V = m.vocab; a.n_ctx = s.n_ctx; a.B = c->B; a.quant = m.quant; a.eps = s.eps;
-    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe;
+    a.head = c->head; a.nfg = s.nfg; a.nfb = s.nfb; a.wte = c->wte; a.wpe = c->wpe; a.V_in = c->v_in;
     a.rope_cos = s.rope_cos; a.rope_sin = s.rope_sin; a.kc = s.kc; a.vc = s.vc;
     a.logits = c->logits;
     a.pos = &c->ds->pos; a.tok = c->ds->tok; a.u1 = c->ds->u1; a.sp = &c->ds->samp[0]; a.err = &c->ds->err;
@@ -1172,6 +1191,7 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
     c->cfg = *cfg;
     c->device = device;
     c->B = cfg->batch;
+    c->v_in = cfg->vocab + cfg->batch * cfg->max_ctx;
     auto bail = [&](int rc) { g_err = c->err; sd_destroy(c); return rc; };
     if (cudaSetDevice(device) != cudaSuccess) return bail(fail(c, SD_ERR_CUDA, "cudaSetDevice(%d) failed", device));
     if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
@@ -1390,17 +1410,31 @@ int sd_set_forced_codes(sd_ctx* c, const int32_t* codes) {
     return SD_OK;
 }
 
-int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
-               int32_t* out_tok) {
-    if (!c || !tokens || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_prefill: NULL argument");
+// Row 0's KV cache at positions [0, npos) of the main stack copied into every other row (the
+// cache is [row][layer * kv head][position][dim]: one 2-D copy per row and tensor).
+int copy_prompt_kv(sd_ctx* c, int npos) {
+    const DStack& s = c->main;
+    const size_t rh = (size_t)s.n_layer * s.Hkv, pitch = (size_t)s.n_ctx * s.hd * sizeof(__half);
+    for (int b = 1; b < c->B; ++b)
+        for (__half* t : {s.kc, s.vc})
+            CK(cudaMemcpy2DAsync(t + (size_t)b * rh * s.n_ctx * s.hd, pitch, t, pitch, (size_t)npos * s.hd * sizeof(__half),
+                                 rh, cudaMemcpyDeviceToDevice, c->stream));
+    return SD_OK;
+}
+
+// The prompt of every row (token indices below v_limit: the vocabulary, or the prompt-vector rows
+// after it).  shared: every row's prompt is row 0's, and positions [0, n - 1) are computed for
+// row 0 only and copied (on the GEMM prefill path).
+int prefill_impl(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+                 int32_t* out_tok, int v_limit, bool shared) {
     if (c->phase != Phase::Loaded || c->host_pos != 0) return fail(c, SD_ERR_STATE, "sd_prefill needs a loaded, reset context");
     if (n < 1 || n > c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "prompt length %d outside [1, %d]", n, c->cfg.max_ctx);
     CK(cudaSetDevice(c->device));
     const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
     const int B = c->B, ns = qwen ? c->cfg.n_codebooks : 1;
     for (int i = 0; i < B * n; ++i)
-        if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
-            return fail(c, SD_ERR_INVALID_ARG, "prompt token %d = %d outside [0, %d)", i, tokens[i], c->cfg.vocab);
+        if (tokens[i] < 0 || tokens[i] >= v_limit)
+            return fail(c, SD_ERR_INVALID_ARG, "prompt token %d = %d outside [0, %d)", i, tokens[i], v_limit);
     int rc;
     if ((rc = set_sampler(c, 0, sampler))) return rc;
     if (qwen) {
@@ -1423,7 +1457,8 @@ int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sa
     if ((rc = upload_inputs(c, qwen))) return rc;
     if (c->ladder_on) CK(cudaMemsetAsync(c->seen, 0, (size_t)c->cfg.vocab, c->stream));
     if (c->gemm_prefill && n > 1) {
-        if ((rc = enqueue_prefill_gemm(c, n - 1, c->stream))) return rc;
+        if ((rc = enqueue_prefill_gemm(c, n - 1, shared ? 1 : B, c->stream))) return rc;
+        if (shared && B > 1 && (rc = copy_prompt_kv(c, n - 1))) return rc;
     } else {
         for (int i = 0; i < n - 1; ++i) CK(cudaGraphLaunch(c->g_body, c->stream));
     }
@@ -1439,6 +1474,41 @@ int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sa
     c->host_pos = n;
     c->phase = Phase::Running;
     return SD_OK;
+}
+
+int sd_prefill(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+               int32_t* out_tok) {
+    if (!c || !tokens || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_prefill: NULL argument");
+    return prefill_impl(c, tokens, n, sampler, u, out_tok, c->cfg.vocab, false);
+}
+
+int sd_prefill_shared(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+                      int32_t* out_tok) {
+    if (!c || !tokens || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_prefill_shared: NULL argument");
+    if (n < 1 || n > c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "prompt length %d outside [1, %d]", n, c->cfg.max_ctx);
+    std::vector<int32_t> all((size_t)c->B * n);
+    for (int b = 0; b < c->B; ++b) memcpy(all.data() + (size_t)b * n, tokens, sizeof(int32_t) * n);
+    return prefill_impl(c, all.data(), n, sampler, u, out_tok, c->cfg.vocab, true);
+}
+
+int sd_prefill_embeds(sd_ctx* c, const float* embeds, int32_t n, const sd_sampler* sampler, const float* u,
+                      int32_t* out_tok) {
+    if (!c || !embeds || !out_tok) return fail(c, SD_ERR_INVALID_ARG, "sd_prefill_embeds: NULL argument");
+    if (c->phase != Phase::Loaded || c->host_pos != 0)
+        return fail(c, SD_ERR_STATE, "sd_prefill_embeds needs a loaded, reset context");
+    if (n < 1 || n > c->cfg.max_ctx) return fail(c, SD_ERR_CTX_FULL, "prompt length %d outside [1, %d]", n, c->cfg.max_ctx);
+    const int d = c->cfg.d_model, V = c->cfg.vocab, ld = c->cfg.max_ctx;
+    for (size_t i = 0; i < (size_t)c->B * n * d; ++i)
+        if (!std::isfinite(embeds[i])) return fail(c, SD_ERR_INVALID_ARG, "prompt vector element %zu is not finite", i);
+    CK(cudaSetDevice(c->device));
+    float* table = const_cast<float*>(c->cfg.arch == SD_ARCH_QWEN_TTS ? c->emb[0] : c->wte);
+    std::vector<int32_t> idx((size_t)c->B * n);
+    for (int b = 0; b < c->B; ++b) {
+        CK(cudaMemcpyAsync(table + ((size_t)V + (size_t)b * ld) * d, embeds + (size_t)b * n * d, sizeof(float) * n * d,
+                           cudaMemcpyHostToDevice, c->stream));
+        for (int p = 0; p < n; ++p) idx[(size_t)b * n + p] = V + b * ld + p;
+    }
+    return prefill_impl(c, idx.data(), n, sampler, u, out_tok, c->v_in, false);
 }
 
 int sd_step(sd_ctx* c, const int32_t* tok, const sd_sampler* sampler, const float* u, int32_t* out_tok) {

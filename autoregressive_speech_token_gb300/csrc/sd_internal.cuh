@@ -244,6 +244,7 @@ struct StepLayer {
 };
 struct StepArgs {
     int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, quant = 0;
+    int V_in = 0;                        // rows of the input embedding table (vocab + prompt-vector rows)
     float eps = 1e-5f;
     const StepLayer* layers = nullptr;   // device array [n_layer]
     QMat head;
@@ -300,6 +301,7 @@ cudaError_t launch_step(const StepArgs& a, int grid, cudaStream_t st);
 // layout (four zero floats after every 32).
 struct CStepArgs {
     int gpt2 = 1, n_layer = 0, d = 0, H = 0, Hkv = 0, hd = 0, ff = 0, V = 0, n_ctx = 0, B = 1, quant = 0;
+    int V_in = 0;                        // rows of the input embedding table (vocab + prompt-vector rows)
     float eps = 1e-5f;
     int ncl = 0, cs = 0;                 // clusters, CTAs per cluster
     int hpc = 0, kpc = 0;                // query heads, KV heads per cluster

@@ -25,7 +25,7 @@ ERRORS = {-1: "SD_ERR_INVALID_ARG", -2: "SD_ERR_STATE", -3: "SD_ERR_CTX_FULL", -
 MAX_CODEBOOKS = 16
 
 # every symbol the headers declare
-EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_step", "sd_frame", "sd_set_forced_codes", "sd_set_ladder",
+EXPORTS = ["sd_create", "sd_load_weights", "sd_prefill", "sd_prefill_shared", "sd_prefill_embeds", "sd_step", "sd_frame", "sd_set_forced_codes", "sd_set_ladder",
            "sd_decode_n", "sd_get_logits", "sd_reset", "sd_destroy", "sd_last_error", "sd_get_info",
            "sd_qmat_create", "sd_qmat_destroy", "sd_qmat_dequant", "sd_qmat_gemv", "sd_qmat_gemm", "sd_qmat_gemm16", "sd_qmat_gemm_tc", "sd_sample_rows", "sd_sample_rows_ladder",
            "sd_attend_rows", "sd_attend_rows_static"]
@@ -94,6 +94,8 @@ def load_library(path: str | None = None):
         "sd_create": ([C.POINTER(ModelConfig), C.c_int, vp, C.POINTER(vp)], C.c_int),
         "sd_load_weights": ([vp, vp, C.c_size_t, C.c_int], C.c_int),
         "sd_prefill": ([vp, i32p, i32, C.POINTER(Sampler), f32p, i32p], C.c_int),
+        "sd_prefill_shared": ([vp, i32p, i32, C.POINTER(Sampler), f32p, i32p], C.c_int),
+        "sd_prefill_embeds": ([vp, f32p, i32, C.POINTER(Sampler), f32p, i32p], C.c_int),
         "sd_step": ([vp, i32p, C.POINTER(Sampler), f32p, i32p], C.c_int),
         "sd_frame": ([vp, i32p, C.POINTER(Sampler), C.POINTER(Sampler), f32p, i32p], C.c_int),
         "sd_set_forced_codes": ([vp, i32p], C.c_int),
@@ -175,6 +177,28 @@ def sd_prefill(ctx: int, tokens: np.ndarray, sampler: Sampler, u: np.ndarray, ou
     out = np.empty((B, out_width), np.int32)
     _check(load_library().sd_prefill(ctx, _p(t, C.c_int32), n, C.byref(sampler), _p(uu, C.c_float),
                                      _p(out, C.c_int32)), ctx)
+    return out
+
+
+def sd_prefill_shared(ctx: int, tokens: np.ndarray, batch: int, sampler: Sampler, u: np.ndarray,
+                      out_width: int = 1) -> np.ndarray:
+    """sd_prefill_shared: one prompt tokens [n] for every row."""
+    t = _arr(tokens, np.int32).reshape(-1)
+    uu = _arr(u, np.float32)
+    out = np.empty((batch, out_width), np.int32)
+    _check(load_library().sd_prefill_shared(ctx, _p(t, C.c_int32), t.size, C.byref(sampler), _p(uu, C.c_float),
+                                            _p(out, C.c_int32)), ctx)
+    return out
+
+
+def sd_prefill_embeds(ctx: int, embeds: np.ndarray, sampler: Sampler, u: np.ndarray, out_width: int = 1) -> np.ndarray:
+    """sd_prefill_embeds: embeds [batch][n][d_model] input vectors."""
+    e = _arr(embeds, np.float32)
+    B, n, _ = e.shape
+    uu = _arr(u, np.float32)
+    out = np.empty((B, out_width), np.int32)
+    _check(load_library().sd_prefill_embeds(ctx, _p(e, C.c_float), n, C.byref(sampler), _p(uu, C.c_float),
+                                            _p(out, C.c_int32)), ctx)
     return out
 
 
@@ -344,6 +368,18 @@ class Decoder:
     def prefill(self, tokens, sampler, u):
         w = self.spec.n_codebooks if self.qwen else 1
         out = sd_prefill(self.ctx, tokens, sampler, u, out_width=w)
+        return out if self.qwen else out[:, 0]
+
+    def prefill_shared(self, tokens, sampler, u):
+        """One prompt tokens [n] for every row (rollouts of one prompt)."""
+        w = self.spec.n_codebooks if self.qwen else 1
+        out = sd_prefill_shared(self.ctx, tokens, self.spec.batch, sampler, u, out_width=w)
+        return out if self.qwen else out[:, 0]
+
+    def prefill_embeds(self, embeds, sampler, u):
+        """A prompt of input vectors embeds [batch][n][d_model]."""
+        w = self.spec.n_codebooks if self.qwen else 1
+        out = sd_prefill_embeds(self.ctx, embeds, sampler, u, out_width=w)
         return out if self.qwen else out[:, 0]
 
     def step(self, tok, sampler, u):

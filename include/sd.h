@@ -138,6 +138,26 @@ int sd_load_weights(sd_ctx* ctx, const void* blob, size_t nbytes, int blob_on_de
 int sd_prefill(sd_ctx* ctx, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
                int32_t* out_tok);
 
+/* sd_prefill with one prompt for every row (tokens [n], host): the G rollouts
+ * of one prompt ("Every Frame Is a Memory Read", section 8: G rows share each
+ * weight read; the rows differ only by their draws).  On the GEMM prefill path
+ * positions 0..n-2 are computed for row 0 alone and row 0's KV cache is copied
+ * to the other rows (a snapshot of the prompt state restored into each row);
+ * the last position runs for every row with its own draws.  Results equal
+ * sd_prefill with every row given `tokens`. */
+int sd_prefill_shared(sd_ctx* ctx, const int32_t* tokens, int32_t n, const sd_sampler* sampler, const float* u,
+                      int32_t* out_tok);
+
+/* sd_prefill whose prompt is given as input vectors: embeds [batch][n][d_model]
+ * fp32, host (a conditioning prefix: text, speaker and conditioning embeddings
+ * assembled by the caller, journal section 3.19 and Tier A item A1).  Vector p
+ * of a row takes the place of a prompt token's embedding row; GPT-2 still adds
+ * its learned position p.  The vectors are kept in B * max_ctx rows of the
+ * input embedding table that follow the vocabulary.  Errors as sd_prefill, and
+ * SD_ERR_INVALID_ARG for a non-finite element. */
+int sd_prefill_embeds(sd_ctx* ctx, const float* embeds, int32_t n, const sd_sampler* sampler, const float* u,
+                      int32_t* out_tok);
+
 /* One decode step (GPT-2/Llama; the step graph of journal section 3.2, two
  * rows in one step per section 3.21): consume tok[row] at the current
  * position, sample the next token with draw u[row] into out_tok[row],

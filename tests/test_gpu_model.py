@@ -121,16 +121,20 @@ class _Tally:
             assert b["margin"] < b["bound"], b
 
 
-def _check_t3(sd, run, n_steps, prompt=None, spec=None):
+def _check_t3(sd, run, n_steps, prompt=None, spec=None, prompt_embeds=None):
     spec = spec or run.model
     blob = _blob(spec)
     prompt = prompt_tokens(run) if prompt is None else prompt
     B = spec.batch
     draws = uniform_draws(run.draw_seed, n_steps + 1, B)[..., 0]
-    ref = oracle.run_t3(oracle.Model(blob, THREADS), spec, prompt, draws, n_steps, run.sampler)
+    ref = oracle.run_t3(oracle.Model(blob, THREADS), spec, prompt, draws, n_steps, run.sampler,
+                        prompt_embeds=prompt_embeds)
     dec = sd.Decoder(spec, blob, stream=_stream())
     s = sd.Sampler.from_spec(run.sampler)
-    got = dec.prefill(prompt, s, draws[0])
+    if prompt_embeds is not None:
+        got = dec.prefill_embeds(prompt_embeds, s, draws[0])
+    else:
+        got = dec.prefill(prompt, s, draws[0])
     worst = 0.0
     name = f"{run.name} {P.QUANT_NAMES[spec.quant]} rows {B} steps {n_steps + 1}"
     tally = _Tally(name, run.sampler)
@@ -185,6 +189,121 @@ def test_llama_q5_two_rows(sd):
                                                 "max_ctx", "quant")})
     prompt = np.random.default_rng(2).integers(0, 1000, size=(2, 40)).astype(np.int32)
     _check_t3(sd, run, 30, prompt=prompt)
+
+
+@pytest.mark.parametrize("arch", ["gpt2", "llama"])
+def test_conditioning_prefix_every_prefill_path(sd, prefill_path, arch):
+    """A prompt of input vectors (sd_prefill_embeds) instead of token IDs, then
+    token steps, against the oracle; on every prefill path and both step paths
+    that run by default (GPT-2: the cluster kernel at one row; Llama: two rows)."""
+    if arch == "gpt2":
+        run = get_preset("tiny").with_model(quant=P.Q4_0)
+        run = dataclasses.replace(run, sampler=SamplerSpec(0.8, 1000, 0.95, False))
+        prompt = np.zeros((1, 24), np.int32)
+    else:
+        spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=3, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                           d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q4_0)
+        run = get_preset("llama_q4").with_model(**{f: getattr(spec, f) for f in
+                                                   ("n_layer", "d_model", "n_head", "n_kv_head", "d_ff", "vocab",
+                                                    "max_ctx", "quant")})
+        prompt = np.zeros((2, 40), np.int32)
+    B, n = prompt.shape
+    emb = (np.random.default_rng(11).standard_normal((B, n, run.model.d_model)) * 0.05).astype(np.float32)
+    _check_t3(sd, run, 12, prompt=prompt, prompt_embeds=emb)
+
+
+def test_prefix_of_embedding_rows_equals_token_prompt(sd):
+    """Prompt vectors equal to the tokens' embedding rows decode bit for bit like
+    the token prompt (GPT-2: the learned positions are added to both)."""
+    run = get_preset("tiny").with_model(quant=P.Q4_0)
+    spec = run.model
+    blob, fp32 = build_model_blob(spec, keep_fp32=True)
+    prompt = prompt_tokens(run)
+    draws = uniform_draws(5, 9, 1)[..., 0]
+    s = sd.Sampler.from_spec(P.T3_SAMPLED)
+    outs = []
+    for use_embeds in (False, True):
+        dec = sd.Decoder(spec, blob, stream=_stream())
+        t = dec.prefill_embeds(fp32["wte"][prompt], s, draws[0]) if use_embeds else dec.prefill(prompt, s, draws[0])
+        toks, zs = [int(t[0])], [dec.logits()]
+        for i in range(8):
+            t = dec.step(np.array([toks[-1]], np.int32), s, draws[i + 1])
+            toks.append(int(t[0]))
+            zs.append(dec.logits())
+        outs.append((toks, zs))
+        dec.close()
+    assert outs[0][0] == outs[1][0]
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def _prefill_both_ways(sd, spec, prompt1, u, sampler, steps_fn):
+    """(codes or tokens, logits, later-step logits) after sd_prefill with the prompt
+    replicated to every row and after sd_prefill_shared with it once."""
+    blob = _blob(spec)
+    res = []
+    for shared in (False, True):
+        dec = sd.Decoder(spec, blob, stream=_stream())
+        if shared:
+            t = dec.prefill_shared(prompt1, sampler, u)
+        else:
+            t = dec.prefill(np.repeat(prompt1[None, :], spec.batch, axis=0), sampler, u)
+        res.append((np.array(t), dec.logits(), steps_fn(dec, t)))
+        dec.close()
+    return res
+
+
+def test_shared_prompt_equals_replicated_prompt_t3(sd, prefill_path):
+    """sd_prefill_shared (row 0's prompt KV computed once and copied) gives the
+    replicated prompt's tokens and logits bit for bit, then and after steps."""
+    spec = P.ModelSpec(arch=P.ARCH_LLAMA, n_layer=3, d_model=512, n_head=8, n_kv_head=2, head_dim=64,
+                       d_ff=1536, vocab=1000, max_ctx=300, batch=2, quant=P.Q4_0)
+    prompt1 = np.random.default_rng(12).integers(0, 1000, size=40).astype(np.int32)
+    draws = uniform_draws(6, 7, 2)[..., 0]
+    s = sd.Sampler.from_spec(P.T3_SAMPLED)
+
+    def steps(dec, t):
+        zs = []
+        for i in range(6):
+            t = dec.step(np.asarray(t, np.int32), s, draws[i + 1])
+            zs.append(dec.logits())
+        return zs
+
+    (ta, za, sa), (tb, zb, sb) = _prefill_both_ways(sd, spec, prompt1, draws[0], s, steps)
+    assert np.array_equal(ta, tb)
+    assert np.array_equal(za.view(np.uint32), zb.view(np.uint32))
+    for a, b in zip(sa, sb):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_shared_prompt_g16_rollouts(sd):
+    """Sixteen rollouts of one prompt (Talker + code predictor, G = 16): the shared
+    prefill equals the replicated one bit for bit and matches the oracle."""
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=16, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
+    prompt1 = np.random.default_rng(13).integers(0, 300, size=20).astype(np.int32)
+    draws = uniform_draws(3, 3, 16, 16)
+    s = sd.Sampler.from_spec(P.QWEN_SAMPLED)
+
+    def frames(dec, codes):
+        zs = []
+        for f in range(2):
+            codes = dec.frame(np.asarray(codes, np.int32), s, s, draws[f + 1])
+            zs.append(dec.logits())
+        return zs
+
+    (ta, za, fa), (tb, zb, fb) = _prefill_both_ways(sd, spec, prompt1, draws[0], s, frames)
+    assert np.array_equal(ta, tb)
+    assert np.array_equal(za.view(np.uint32), zb.view(np.uint32))
+    for a, b in zip(fa, fb):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # and the shared prompt's first frame against the oracle (rows started from one prompt state)
+    ref = oracle.run_qwen(oracle.Model(_blob(spec), THREADS), spec, np.repeat(prompt1[None, :], 16, axis=0),
+                          draws, 0, P.QWEN_SAMPLED, P.QWEN_SAMPLED)
+    for b in range(16):
+        assert _rel(zb[b, 0, :spec.vocab], ref[b].logits[0][0]) <= REL_L2
 
 
 def test_gpt2m_q8_greedy(sd):
