@@ -743,6 +743,22 @@ static __device__ __forceinline__ int lower_bound_u64(const unsigned long long* 
     return lo;
 }
 
+// The same search over the kFB non-decreasing bin prefixes `pre` by one warp, in two rounds of
+// loads: cend[c] = pre[64c + 63] picks the 64-bin chunk, then each lane tests one pair of bins.
+// Every lane returns min(first bin with pre >= t, n).
+static __device__ __forceinline__ int lower_bound_warp(const unsigned long long* pre, const unsigned long long* cend,
+                                                       int n, unsigned long long t) {
+    const int lane = threadIdx.x & 31;
+    const unsigned mc = __ballot_sync(0xffffffffu, cend[lane] >= t);
+    if (!mc) return n;
+    const int c = __ffs(mc) - 1;
+    const ulonglong2 e = reinterpret_cast<const ulonglong2*>(pre)[32 * c + lane];  // bins 64c + 2 lane, + 1
+    const unsigned m1 = __ballot_sync(0xffffffffu, e.y >= t), m0 = __ballot_sync(0xffffffffu, e.x >= t);
+    const int l = __ffs(m1) - 1;  // m1 != 0: the chunk's last bin reaches t
+    const int b = 64 * c + 2 * l + (((m0 >> l) & 1u) ? 0 : 1);
+    return b < n ? b : n;
+}
+
 // The path every kernel takes first for a sampled row (512 threads, V <= 17 * 512): the same
 // survivors, cut and draw as sample_fast, with each thread's logits and fixed-point masses held
 // in registers over a contiguous segment of the vocabulary (odd segment length: the loads hit
@@ -870,6 +886,7 @@ static __device__ __noinline__ int sample_reg(int V, const SampParams sp, const 
         }
         reinterpret_cast<ulonglong2*>(pre)[2 * tid] = make_ulonglong2(pr[0], pr[1]);
         reinterpret_cast<ulonglong2*>(pre)[2 * tid + 1] = make_ulonglong2(pr[2], pr[3]);
+        if ((tid & 15) == 15) ss.mass[tid >> 4] = pr[3];  // prefix at the end of 64-bin chunk tid / 16
     }
     SAMPLE_SYNC();
 
@@ -885,8 +902,8 @@ static __device__ __noinline__ int sample_reg(int V, const SampParams sp, const 
         if (tlo == 0ull) tlo = 1ull;
         if (thi == 0ull) thi = 1ull;
         const int lim = topk ? bk : kFB;
-        blo = lower_bound_u64(pre, lim, tlo);
-        bhi = lower_bound_u64(pre, lim, thi);
+        blo = lower_bound_warp(pre, ss.mass, lim, tlo);
+        bhi = lower_bound_warp(pre, ss.mass, lim, thi);
         if (bhi >= lim) bhi = lim - 1;
     }
 #pragma unroll
@@ -909,7 +926,65 @@ static __device__ __noinline__ int sample_reg(int V, const SampParams sp, const 
     if (nm > kFC) return sample_smem(V, sp, u_ptr, smraw, ss, err);
 
     // ---- P6 (warp 0): the top-k threshold key and the top-p cut element
-    if (warp == 0) {
+    if (warp == 0 && nm <= 32) {
+        // members in the lanes' registers; pairwise comparisons by shuffles
+        const bool has = lane < nm;
+        const uint32_t mk = has ? ckey[lane] : 0u;
+        const unsigned mbi = has ? cbi[lane] : 0u, mq = has ? cq[lane] : 0u;
+        const int mbin = has ? (int)(mbi >> 14) : -1, midx = (int)(mbi & 0x3FFFu);
+        const int rk = topk ? ss.i[3] : 0;
+        uint32_t thr = 0u;
+        unsigned long long sk = 0ull;
+        if (topk) {
+            int gt = 0, ge = 0;
+            for (int j = 0; j < nm; ++j) {
+                const uint32_t kj = __shfl_sync(0xffffffffu, mk, j);
+                const int bj = __shfl_sync(0xffffffffu, mbin, j);
+                if (bj == bk) {
+                    gt += kj > mk;
+                    ge += kj >= mk;
+                }
+            }
+            const bool mine = has && mbin == bk;
+            if (mine && gt < rk) sk = mq;  // a survivor of the k-th bin: fewer than rk members above it
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            const unsigned bt = __ballot_sync(0xffffffffu, mine && gt < rk && rk <= ge);
+            thr = bt ? __shfl_sync(0xffffffffu, mk, __ffs(bt) - 1) : 0u;
+        }
+        const unsigned long long Zq = topk ? mAbove + sk : Ztot;
+        unsigned cutl = 0u;
+        if (topp) {
+            unsigned long long T = mul_frac(sp.top_p, Zq, true);
+            if (T == 0ull) T = 1ull;
+            int bp;
+            unsigned long long before;
+            if (topk && T > mAbove) {
+                bp = bk;
+                before = mAbove;
+            } else {
+                bp = lower_bound_warp(pre, ss.mass, topk ? bk : kFB, T);
+                before = bp > 0 ? pre[bp - 1] : 0ull;
+            }
+            const unsigned long long rem = T - before;
+            unsigned long long p0 = 0ull;  // mass before this member in (key desc, index asc) order
+            for (int j = 0; j < nm; ++j) {
+                const uint32_t kj = __shfl_sync(0xffffffffu, mk, j);
+                const int bj = __shfl_sync(0xffffffffu, mbin, j), ij = __shfl_sync(0xffffffffu, midx, j);
+                const unsigned qj = __shfl_sync(0xffffffffu, mq, j);
+                if (bj == bp && kj >= thr && (kj > mk || (kj == mk && ij < midx))) p0 += qj;
+            }
+            cutl = __ballot_sync(0xffffffffu, has && mbin == bp && mk >= thr && p0 < rem && p0 + mq >= rem);
+        }
+        if (lane == 0) {
+            ss.sel[0] = thr;
+            ss.i[5] = cutl ? 1 : 0;
+        }
+        if (cutl && lane == __ffs(cutl) - 1) {
+            ss.sel[1] = mk;
+            ss.sel[2] = (uint32_t)midx;
+        }
+    } else if (warp == 0) {
         const int rk = topk ? ss.i[3] : 0;
         // survivors of the k-th bin: fewer than rk of its members above them
         uint32_t thr = 0u;
