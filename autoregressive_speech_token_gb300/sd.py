@@ -56,7 +56,8 @@ class Sampler(C.Structure):
 
     @classmethod
     def from_spec(cls, s) -> "Sampler":
-        return cls(float(s.temperature), int(s.top_k), float(s.top_p), int(bool(s.greedy)), 1.0)
+        return cls(float(s.temperature), int(s.top_k), float(s.top_p), int(bool(s.greedy)),
+                   float(getattr(s, "rep_penalty", 1.0)))
 
 
 class SamplerLadder(C.Structure):

@@ -99,6 +99,9 @@ def _declare(L):
     L.orc_sample.argtypes = [f32p, C.c_int32, C.c_float, C.c_int32, C.c_float, C.c_int32, C.c_double,
                              C.POINTER(C.c_double)]
     L.orc_sample.restype = C.c_int32
+    L.orc_sample_pen.argtypes = [f32p, C.c_int32, u8p, C.c_float, C.c_float, C.c_int32, C.c_float, C.c_int32,
+                                 C.c_double, C.POINTER(C.c_double)]
+    L.orc_sample_pen.restype = C.c_int32
     L.orc_sample_ladder.argtypes = [f32p, f32p, C.c_int32, C.c_float, u8p, C.c_float, C.c_float, C.c_float,
                                     C.c_float, C.c_int32, C.c_double, C.POINTER(C.c_double)]
     L.orc_sample_ladder.restype = C.c_int32
@@ -197,12 +200,19 @@ def attend(q, k_half, v_half):
     return out
 
 
-def sample(z, temperature=1.0, top_k=1, top_p=1.0, greedy=True, u=0.0):
-    """Returns (token, margin)."""
+def sample(z, temperature=1.0, top_k=1, top_p=1.0, greedy=True, u=0.0, seen=None, rep_penalty=1.0):
+    """Returns (token, margin); with seen and rep_penalty != 1 the logits of the
+    seen tokens are penalised first."""
     z = _f32(z)
     m = C.c_double()
-    tok = lib().orc_sample(_p(z, C.c_float), z.size, float(temperature), int(top_k), float(top_p),
-                           int(bool(greedy)), float(u), C.byref(m))
+    if seen is not None and rep_penalty != 1.0:
+        sn = np.ascontiguousarray(seen, np.uint8)
+        tok = lib().orc_sample_pen(_p(z, C.c_float), z.size, _p(sn, C.c_uint8), float(rep_penalty),
+                                   float(temperature), int(top_k), float(top_p), int(bool(greedy)), float(u),
+                                   C.byref(m))
+    else:
+        tok = lib().orc_sample(_p(z, C.c_float), z.size, float(temperature), int(top_k), float(top_p),
+                               int(bool(greedy)), float(u), C.byref(m))
     return int(tok), float(m.value)
 
 
@@ -409,8 +419,10 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
     and head 1 samples c1; position j takes Pr*E_{j-1}[c_{j-1}] and head j
     samples c_j.  draws [n_frames+1][B][16].  With teacher forcing the codes
     fed forward (inside the frame and into the next frame) are forced[b][f]
-    instead of the sampled ones.  Returns one Trace per row with tokens [16]
-    per frame and logits as a list of 16 arrays per frame."""
+    instead of the sampled ones.  A Talker sampler with rep_penalty != 1
+    penalises the codebook-0 tokens fed to the Talker so far (frames 0..f-1 at
+    frame f; the prompt's tokens are not in the history).  Returns one Trace per
+    row with tokens [16] per frame and logits as a list of 16 arrays per frame."""
     B = prompt.shape[0]
     d, V0, Vc, ncb = spec.d_model, spec.vocab, spec.cp_vocab, spec.n_codebooks
     ta, ca = _sampler_args(talker_sampler), _sampler_args(cp_sampler)
@@ -427,13 +439,15 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
         for tok in prompt[b]:
             z0, h = model.talker_forward(b, model.talker_embed(int(tok), d), V0, d)
         prompt_end.append((z0, h))
+    pen = float(getattr(talker_sampler, "rep_penalty", 1.0))
     traces = []
     for b in range(B):
         tr = Trace()
         z0, h = prompt_end[b]
+        seen0 = np.zeros(V0, np.uint8)
         for f in range(n_frames + 1):
             codes, zs, ms = [], [z0], []
-            c0, m0 = sample(z0, u=float(draws[f][b][0]), **ta)
+            c0, m0 = sample(z0, u=float(draws[f][b][0]), seen=seen0, rep_penalty=pen, **ta)
             codes.append(c0); ms.append(m0)
             model.cp_reset(b)
             model.cp_forward(b, h, 0, Vc)
@@ -448,6 +462,7 @@ def run_qwen(model: Model, spec, prompt: np.ndarray, draws: np.ndarray, n_frames
                 tr.logits.append(zs)
             if f < n_frames:
                 feed = codes if forced is None else [int(c) for c in forced[b][f]]
+                seen0[feed[0]] = 1
                 z0, h = model.talker_forward(b, model.code_embed_sum(feed, d), V0, d)
         traces.append(tr)
     return traces

@@ -54,7 +54,8 @@ static int group_of(int kind) { return kind == K_A4G32 ? 32 : is_affine(kind) ? 
  *  23 margin taken as if T were 1    24 top-p bound counts t before itself
  *  25 mass factor 1+r instead of its square root
  *  26 Q5_0 fifth bit taken from the wrong element
- *  27 4-bit affine codes read high nibble first                            */
+ *  27 4-bit affine codes read high nibble first
+ *  28 plain sampler's penalty backwards                                   */
 #ifndef ORC_MUTANT
 #define ORC_MUTANT 0
 #endif
@@ -600,6 +601,32 @@ int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, 
         *margin = draw_margin(s, V, st, n_st, in_s, tok, target, c_lo, c, zs);
     }
     free(s); free(p); free(in_s);
+    return tok;
+}
+
+/* The sampler with a repetition penalty over a history: every logit of a token
+ * in seen[] is divided by the penalty when positive and multiplied by it
+ * otherwise (the journal's HF rule; "Every Frame Is a Memory Read", section
+ * 2: the Talker decodes with a penalty over the tokens it generated), then the
+ * plain sampler runs on the penalised logits (rounded to fp32, the logits'
+ * type).  seen may be NULL and rep_penalty 1: no penalty. */
+int32_t orc_sample_pen(const float* z, int32_t V, const uint8_t* seen, float rep_penalty, float temperature,
+                       int32_t top_k, float top_p, int32_t greedy, double u, double* margin) {
+    if (V <= 0) return -1;
+    float* zp = (float*)malloc((size_t)V * sizeof(float));
+    for (int32_t i = 0; i < V; ++i) {
+        double v = (double)z[i];
+        if (seen && seen[i] && rep_penalty != 1.0f) {
+#if ORC_MUTANT == 28
+            v = v > 0.0 ? v * (double)rep_penalty : v / (double)rep_penalty;
+#else
+            v = v > 0.0 ? v / (double)rep_penalty : v * (double)rep_penalty;
+#endif
+        }
+        zp[i] = (float)v;
+    }
+    int32_t tok = orc_sample(zp, V, temperature, top_k, top_p, greedy, u, margin);
+    free(zp);
     return tok;
 }
 

@@ -55,6 +55,11 @@ void orc_attend(const float* q, const uint16_t* k, const uint16_t* v, int n, int
 int32_t orc_sample(const float* z, int32_t V, float temperature, int32_t top_k, float top_p,
                    int32_t greedy, double u, double* margin);
 
+/* orc_sample on the logits after a repetition penalty over seen[] (NULL: none):
+ * a seen token's logit is divided by rep_penalty when positive, else multiplied. */
+int32_t orc_sample_pen(const float* z, int32_t V, const uint8_t* seen, float rep_penalty, float temperature,
+                       int32_t top_k, float top_p, int32_t greedy, double u, double* margin);
+
 /* Sampler ladder of the multilingual T3: classifier-free-guidance combine ->
  * repetition penalty -> temperature -> min_p -> top-p -> top-k -> draw in
  * vocabulary order with u.  z_uncond may be NULL (no combine); seen may be

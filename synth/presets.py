@@ -128,6 +128,7 @@ class SamplerSpec:
     top_k: int = 1
     top_p: float = 1.0
     greedy: bool = True
+    rep_penalty: float = 1.0   # the Talker's penalty over its past codebook-0 tokens (1: none)
 
 
 GREEDY = SamplerSpec()

@@ -186,6 +186,23 @@ def test_qwen_frames_match_full_recompute(cp_quant):
             assert _rel(tr.logits[f][j], ref[f][j]) < TOL, (f, j)
 
 
+def test_qwen_talker_penalty_history_is_the_fed_codes():
+    """Greedy Talker with a huge repetition penalty: frame 0's code 0 is the plain
+    argmax (the prompt is not in the history) and no codebook-0 token fed forward
+    is picked again."""
+    m = _small_qwen()
+    blob, _ = build_model_blob(m)
+    prompt = np.random.default_rng(9).integers(0, m.vocab, size=(1, 6)).astype(np.int32)
+    nf = 14
+    draws = uniform_draws(5, nf + 1, 1, 16)
+    talker = SamplerSpec(greedy=True, rep_penalty=1e6)
+    cp = SamplerSpec(temperature=0.9, top_k=50, top_p=0.95, greedy=False)
+    tr = oracle.run_qwen(oracle.Model(blob), m, prompt, draws, nf, talker, cp)[0]
+    c0 = [f[0] for f in tr.tokens]
+    assert c0[0] == int(np.argmax(tr.logits[0][0]))
+    assert len(set(c0)) == nf + 1, c0
+
+
 def test_qwen_rows_sharing_a_prompt_match_full_recompute():
     """Rows whose prompt equals an earlier row's start from a copy of that row's
     cache (run_qwen's shortcut for G rollouts of one prompt); every row's frames

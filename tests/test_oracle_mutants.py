@@ -48,6 +48,7 @@ MUTANTS = {
                                                          oo.test_sampler_margin_at_a_top_p_cut_that_can_grow]),
     26: ("Q5_0 fifth bit taken from the wrong element", [oo.test_q5_0_hand_block]),
     27: ("4-bit affine codes read high nibble first", [lambda: oo.test_a4_hand_group(oo.KA4G32, 32)]),
+    28: ("plain sampler's penalty backwards", [oo.test_penalised_sampler_follows_the_sign_rule]),
 }
 
 

@@ -171,6 +171,75 @@ def test_dequant_roundtrip_and_bounds(kind):
         assert np.all(deq[1, :64] == deq[1, 0])
 
 
+# ----------------------------------------------------------------------------- sampler with a repetition penalty
+
+def test_penalised_sampler_follows_the_sign_rule():
+    """A seen positive logit is divided (it can lose the argmax), a seen negative
+    one multiplied (it moves further down); unseen tokens keep their logits."""
+    z = np.array([2.0, 1.5, -0.5, -0.6], np.float32)
+    seen = np.array([1, 0, 0, 0], np.uint8)
+    assert oracle.sample(z, greedy=True, seen=seen, rep_penalty=2.0)[0] == 1      # 2.0 / 2 = 1.0 < 1.5
+    assert oracle.sample(z, greedy=True, seen=seen, rep_penalty=1.2)[0] == 0      # 2.0 / 1.2 > 1.5
+    z2 = np.array([-1.0, -0.9, -3.0], np.float32)
+    seen2 = np.array([0, 1, 0], np.uint8)
+    assert oracle.sample(z2, greedy=True, seen=seen2, rep_penalty=1.2)[0] == 0    # -0.9 * 1.2 = -1.08 < -1.0
+    assert oracle.sample(z2, greedy=True, seen=seen2, rep_penalty=1.0)[0] == 1
+    assert oracle.sample(z2, greedy=True, seen=None, rep_penalty=3.0)[0] == 1
+
+
+def test_penalised_sampler_bruteforce():
+    """Enumeration from the definitions on 16-entry vocabularies: the penalised
+    logits (HF rule) through temperature, top-k (ties kept), top-p (shortest
+    prefix in probability desc / index asc order) and the index-order draw."""
+    rng = np.random.default_rng(44)
+    for case in range(60):
+        z = (rng.standard_normal(16) * 1.5).astype(np.float32)
+        seen = (rng.random(16) < 0.4).astype(np.uint8)
+        pen = float(rng.choice([1.1, 1.5, 2.0]))
+        T = float(rng.choice([0.5, 0.9, 1.3]))
+        k = int(rng.choice([3, 8, 16]))
+        p = float(rng.choice([0.6, 0.9, 1.0]))
+        zp = np.array([(v / pen if v > 0 else v * pen) if sn else v for v, sn in zip(z.astype(np.float64), seen)])
+        zp = zp.astype(np.float32).astype(np.float64) / T
+        order = sorted(range(16), key=lambda i: (-zp[i], i))
+        kept = [i for i in range(16) if sum(zp[j] > zp[i] for j in range(16)) < k]
+        w = {i: math.exp(zp[i] - zp[order[0]]) for i in kept}
+        Z = sum(w.values())
+        if p < 1.0:
+            cum, keep2 = 0.0, []
+            for i in sorted(kept, key=lambda i: (-zp[i], i)):
+                keep2.append(i)
+                cum += w[i] / Z
+                if cum >= p:
+                    break
+            kept = keep2
+        ZS = sum(w[i] for i in kept)
+        for u in (0.03, 0.31, 0.58, 0.77, 0.96):
+            acc, want = 0.0, None
+            for i in sorted(kept):
+                acc += w[i] / ZS
+                if acc > u:
+                    want = i
+                    break
+            got, margin = oracle.sample(z, temperature=T, top_k=k, top_p=p, greedy=False, u=u, seen=seen,
+                                        rep_penalty=pen)
+            if margin > 1e-9:
+                assert got == want, (case, u, got, want, margin)
+
+
+def test_penalty_of_one_or_no_history_is_the_plain_sampler():
+    rng = np.random.default_rng(45)
+    for _ in range(30):
+        z = rng.standard_normal(300).astype(np.float32)
+        u = float(rng.random())
+        a = oracle.sample(z, temperature=0.9, top_k=50, top_p=0.95, greedy=False, u=u)
+        b = oracle.sample(z, temperature=0.9, top_k=50, top_p=0.95, greedy=False, u=u,
+                          seen=np.ones(300, np.uint8), rep_penalty=1.0)
+        c = oracle.sample(z, temperature=0.9, top_k=50, top_p=0.95, greedy=False, u=u,
+                          seen=np.zeros(300, np.uint8), rep_penalty=1.7)
+        assert a == b == c
+
+
 # ----------------------------------------------------------------------------- linear
 
 def quant_data(kind, w):
