@@ -113,6 +113,7 @@ __global__ void k_embed_sum(const EmbedSumArgs a) {
         }
         code[j] = c;
     }
+    if (a.seen0 && threadIdx.x == 0) a.seen0[(size_t)b * a.vocab[0] + code[0]] = 1;
     for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
         double s = 0.0;
         for (int j = 0; j < a.ncb; ++j) s += (double)a.tables[j][(size_t)code[j] * a.d + i];

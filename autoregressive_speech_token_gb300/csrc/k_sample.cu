@@ -16,7 +16,8 @@ __global__ void __launch_bounds__(kST) k_sample(const SampleArgs a) {
     const int b = blockIdx.x;
     const float* up = (a.u_seq && *a.u_seq) ? (*a.u_seq) + (size_t)(*a.step_idx) * gridDim.x + b
                                             : a.u + (size_t)b * a.u_stride + a.u_off;
-    const int tok = sample_detail::sample_block(a.logits + (size_t)b * a.ld, a.V, *a.sp, up, smraw, ss, a.err);
+    const int tok = sample_detail::sample_block(a.logits + (size_t)b * a.ld, a.V, *a.sp, up, smraw, ss, a.err,
+                                                a.seen ? a.seen + (size_t)b * a.seen_ld : nullptr);
     if (threadIdx.x == 0) {
         a.out[(size_t)b * a.out_stride + a.out_off] = tok;
         if (a.out_seq && *a.out_seq) (*a.out_seq)[(size_t)(*a.step_idx) * gridDim.x + b] = tok;

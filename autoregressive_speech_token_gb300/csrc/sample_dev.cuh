@@ -1093,11 +1093,17 @@ static __device__ __noinline__ int sample_reg(int V, const SampParams sp, const 
 }
 
 // As sample_reg, loading the logits lg[0..V) first (through L2: they may
-// have been written by other CTAs of the same kernel).
+// have been written by other CTAs of the same kernel).  With a history mask
+// `seen` and sp.rep_penalty != 1 the logit of every seen token is divided by the
+// penalty when positive and multiplied by it otherwise, as it is loaded ("Every
+// Frame Is a Memory Read", section 2: the Talker's repetition penalty; the HF
+// rule of the journal's table of fixes).
 static __device__ int sample_block(const float* lg, int V, const SampParams sp, const float* u_ptr,
-                                   unsigned char* smraw, SampleScratch& ss, int* err) {
+                                   unsigned char* smraw, SampleScratch& ss, int* err,
+                                   const uint8_t* seen = nullptr) {
     const int tid = threadIdx.x, nt = SAMPLE_NT;
     float* z = reinterpret_cast<float*>(smraw);
+    const bool pen = seen && sp.rep_penalty != 1.0f;
     for (int i0 = 0; i0 < V; i0 += 8 * nt) {
         float r[8];
 #pragma unroll
@@ -1108,7 +1114,11 @@ static __device__ int sample_block(const float* lg, int V, const SampParams sp, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int i = i0 + j * nt + tid;
-            if (i < V) z[i] = r[j];
+            if (i < V) {
+                float v = r[j];
+                if (pen && seen[i]) v = v > 0.f ? v / sp.rep_penalty : v * sp.rep_penalty;
+                z[i] = v;
+            }
         }
     }
     SAMPLE_SYNC();

@@ -144,6 +144,7 @@ struct sd_ctx {
     bool ladder_on = false;             // sd_set_ladder: one token per step for a cond / uncond row pair
     LadderParams ladder;
     uint8_t* seen = nullptr;            // [vocab] tokens generated since sd_prefill (ladder mode)
+    uint8_t* seen0 = nullptr;           // [B][vocab] codebook-0 tokens fed to the Talker since sd_prefill
     float* lad_u = nullptr;             // the ladder's draw slot
     int32_t* lad_t = nullptr;           // the ladder's token slot
     long long test_stall = 0;           // test hook (SD_TEST_STALL_US): cycles for one wait of the next persistent launch
@@ -358,6 +359,10 @@ int enqueue_sample(sd_ctx* c, int which, int slot, int V, bool t3, cudaStream_t 
     } else {
         a.u = c->ds->u; a.u_stride = kMaxCodebooks; a.u_off = slot;
         a.out = c->ds->codes; a.out_stride = kMaxCodebooks; a.out_off = slot;
+        if (which == 0) {  // the Talker's codebook-0 sampler: its history of fed codebook-0 tokens
+            a.seen = c->seen0;
+            a.seen_ld = c->cfg.vocab;
+        }
     }
     cudaError_t e = launch_sample(a, c->B, st);
     c->count_launch++;
@@ -549,6 +554,7 @@ int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
         }
         es.ncb = c->cfg.n_codebooks; es.d = c->main.d; es.codes = c->ds->codes_in; es.e = c->main.x;
         es.err = &c->ds->err;
+        es.seen0 = c->seen0;
         cudaError_t e = launch_embed_sum(es, c->B, st);
         c->count_launch++;
         if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "embed_sum launch: %s", cudaGetErrorString(e));
@@ -1151,17 +1157,22 @@ int sampler_check(const sd_sampler* s) {
     return SD_OK;
 }
 
+// which: 0 the T3 / Talker sampler, 1 the code predictor's.  Only the Talker's sampler keeps a
+// history (the codebook-0 tokens fed so far), so only it takes a repetition penalty.
 int set_sampler(sd_ctx* c, int which, const sd_sampler* s) {
     if (!s) return fail(c, SD_ERR_INVALID_ARG, "sampler is NULL");
-    if (const int rc = sampler_check(s))
+    int rc = sampler_check(s);
+    if (rc == SD_ERR_UNSUPPORTED && c->cfg.arch == SD_ARCH_QWEN_TTS && which == 0) rc = SD_OK;
+    if (rc)
         return fail(c, rc, "sampler %s (T=%g k=%d p=%g penalty=%g)",
-                    rc == SD_ERR_UNSUPPORTED ? "asks for a repetition penalty, which the decode step does not apply"
+                    rc == SD_ERR_UNSUPPORTED ? "asks for a repetition penalty, which only the Talker's sampler applies"
                                              : "out of range",
                     s->temperature, s->top_k, s->top_p, s->rep_penalty);
     c->hs->samp[which].temperature = s->temperature;
     c->hs->samp[which].top_k = s->top_k;
     c->hs->samp[which].top_p = s->top_p;
     c->hs->samp[which].greedy = s->greedy;
+    c->hs->samp[which].rep_penalty = s->rep_penalty > 0.f ? s->rep_penalty : 1.0f;
     return SD_OK;
 }
 
@@ -1222,6 +1233,7 @@ int sd_create(const sd_model_config* cfg, int device, void* stream, sd_ctx** out
         c->vmax = std::max(m.vocab, m.cp_vocab);
         c->logits_ld = kMaxCodebooks * c->vmax;
         if ((rc = dalloc(c, &c->ebuf, sizeof(float) * c->B * m.d_model))) return bail(rc);
+        if ((rc = dalloc(c, &c->seen0, (size_t)c->B * m.vocab))) return bail(rc);
     } else {
         c->vmax = m.vocab;
         c->logits_ld = m.vocab;
@@ -1437,8 +1449,10 @@ int prefill_impl(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* 
             return fail(c, SD_ERR_INVALID_ARG, "prompt token %d = %d outside [0, %d)", i, tokens[i], v_limit);
     int rc;
     if ((rc = set_sampler(c, 0, sampler))) return rc;
-    if (qwen) {
-        if ((rc = set_sampler(c, 1, sampler))) return rc;
+    if (qwen) {  // the prompt frame's code predictor takes the same settings without the Talker's penalty
+        sd_sampler cp = *sampler;
+        cp.rep_penalty = 1.0f;
+        if ((rc = set_sampler(c, 1, &cp))) return rc;
     }
     if (!u) return fail(c, SD_ERR_INVALID_ARG, "draws are NULL");
     for (int b = 0; b < B; ++b) {
@@ -1456,6 +1470,7 @@ int prefill_impl(sd_ctx* c, const int32_t* tokens, int32_t n, const sd_sampler* 
     for (int b = 0; b < B; ++b) c->hs->tok[b] = tokens[(size_t)b * n + n - 1];  // read by the persistent step
     if ((rc = upload_inputs(c, qwen))) return rc;
     if (c->ladder_on) CK(cudaMemsetAsync(c->seen, 0, (size_t)c->cfg.vocab, c->stream));
+    if (c->seen0) CK(cudaMemsetAsync(c->seen0, 0, (size_t)B * c->cfg.vocab, c->stream));
     if (c->gemm_prefill && n > 1) {
         if ((rc = enqueue_prefill_gemm(c, n - 1, shared ? 1 : B, c->stream))) return rc;
         if (shared && B > 1 && (rc = copy_prompt_kv(c, n - 1))) return rc;
@@ -1813,7 +1828,7 @@ int sd_sample_rows(const float* logits_dev, int32_t rows, int32_t V, const sd_sa
     int* err = nullptr;
     CK(cudaMalloc(&sp, sizeof(SampParams) + 16));
     err = reinterpret_cast<int*>(reinterpret_cast<char*>(sp) + sizeof(SampParams));
-    SampParams h{s->temperature, s->top_k, s->top_p, s->greedy};
+    SampParams h{s->temperature, s->top_k, s->top_p, s->greedy, 1.0f};
     cudaError_t e = cudaMemcpyAsync(sp, &h, sizeof h, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, 4, st);
     SampleArgs a;

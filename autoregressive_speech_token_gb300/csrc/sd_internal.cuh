@@ -145,6 +145,7 @@ struct SampParams {
     int32_t top_k;
     float top_p;
     int32_t greedy;
+    float rep_penalty;  // applied to the logits of the tokens in the sampler's history mask (1: none)
 };
 
 struct SampleArgs {
@@ -161,6 +162,8 @@ struct SampleArgs {
     int out_stride = 1, out_off = 0;
     int32_t* const* out_seq = nullptr;      // if *out_seq: (*out_seq)[(*step_idx) * rows + b] = token
     int* err = nullptr;
+    const uint8_t* seen = nullptr;          // history mask of row b at seen[b*seen_ld .. + V), or null
+    int seen_ld = 0;
 };
 
 // ------------------------------------------------------------------ launchers
@@ -221,6 +224,7 @@ struct EmbedSumArgs {
     const int32_t* codes = nullptr;   // [B][16]
     float* e = nullptr;               // [B][d]
     int* err = nullptr;
+    uint8_t* seen0 = nullptr;         // if set: seen0[b*vocab[0] + code 0 of row b] = 1 (the Talker's history)
 };
 cudaError_t launch_embed_sum(const EmbedSumArgs& a, int B, cudaStream_t st);
 

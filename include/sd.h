@@ -80,12 +80,18 @@ typedef struct sd_model_config {
  * in (probability desc, index asc) order, whose mass reaches top_p; draw the
  * smallest vocabulary index whose cumulative kept mass (index order) exceeds
  * u times the kept total.  Valid: temperature >= 0, top_k >= 1,
- * 0 < top_p <= 1.  rep_penalty is the repetition penalty of the multilingual
- * sampling path (journal section 3.19, "Sampling path"): 1, or 0 (read as 1),
- * applies none; the decode step does not implement the penalty, so any other
- * positive value returns SD_ERR_UNSUPPORTED and a negative or NaN value
- * SD_ERR_INVALID_ARG (the whole ladder runs standalone in
- * sd_sample_rows_ladder, sd_ops.h). */
+ * 0 < top_p <= 1.  rep_penalty: 1, or 0 (read as 1), applies none.  The
+ * Talker's sampler of a Talker + code-predictor context (sd_prefill, and the
+ * `talker` argument of sd_frame) takes any positive penalty: before sampling
+ * codebook 0, the logit of every codebook-0 token fed to the Talker since
+ * sd_prefill (the prompt's own tokens excluded) is divided by it when positive
+ * and multiplied by it otherwise ("Every Frame Is a Memory Read", sections 2
+ * and 8: the penalty, kept per row on the device; the journal's HF sign rule).
+ * sd_prefill gives the prompt frame's code predictor the same settings without
+ * the penalty.  Elsewhere (GPT-2 / Llama steps, the code predictor's sampler)
+ * a penalty other than 1 returns SD_ERR_UNSUPPORTED -- the multilingual T3's
+ * penalty is part of its ladder (sd_set_ladder) -- and a negative or NaN value
+ * SD_ERR_INVALID_ARG. */
 typedef struct sd_sampler {
     float temperature;
     int32_t top_k;

@@ -691,19 +691,24 @@ def test_expired_exchange_wait_reports_timeout_and_recovers(sd, monkeypatch, kin
 
 # ----------------------------------------------------------------------------- Talker + code predictor
 
-def _check_qwen(sd, spec, prompt, n_frames, sampler, name):
+def _check_qwen(sd, spec, prompt, n_frames, sampler, name, cp_sampler=None):
+    """sampler drives the Talker (and the code predictor unless cp_sampler is
+    given); a Talker repetition penalty acts on the codebook-0 tokens fed so far."""
+    cp_sampler = cp_sampler or sampler
     blob = _blob(spec)
     B = spec.batch
     draws = uniform_draws(3, n_frames + 1, B, 16)
-    ref = oracle.run_qwen(oracle.Model(blob, THREADS), spec, prompt, draws, n_frames, sampler, sampler)
+    ref = oracle.run_qwen(oracle.Model(blob, THREADS), spec, prompt, draws, n_frames, sampler, cp_sampler)
     dec = sd.Decoder(spec, blob, stream=_stream())
-    s = sd.Sampler.from_spec(sampler)
-    sa = dict(temperature=sampler.temperature, top_k=sampler.top_k, top_p=sampler.top_p, greedy=sampler.greedy)
+    s, scp = sd.Sampler.from_spec(sampler), sd.Sampler.from_spec(cp_sampler)
+    pen = float(sampler.rep_penalty)
+    sa = [dict(temperature=x.temperature, top_k=x.top_k, top_p=x.top_p, greedy=x.greedy) for x in (sampler, cp_sampler)]
     dec.force(np.array([ref[b].tokens[0] for b in range(B)], np.int32))
     codes = dec.prefill(prompt, s, draws[0])
     name = f"{name} rows {B} frames {n_frames + 1}"
     tally = _Tally(name, sampler)
     worst = 0.0
+    seen0 = np.zeros((B, spec.vocab), np.uint8)
     for f in range(n_frames + 1):
         z = dec.logits()
         for b in range(B):
@@ -713,19 +718,36 @@ def _check_qwen(sd, spec, prompt, n_frames, sampler, name):
                 worst = max(worst, r)
                 assert r <= REL_L2, (f, b, j, r)
                 # the device sampler decides like the oracle's sampler on the same (device) logits
-                tg, mg = oracle.sample(z[b, j, :V], u=float(draws[f][b][j]), **sa)
+                hist = dict(seen=seen0[b], rep_penalty=pen) if j == 0 else {}
+                tg, mg = oracle.sample(z[b, j, :V], u=float(draws[f][b][j]), **sa[j > 0], **hist)
                 if mg >= SAMPLER_MARGIN:
                     assert int(codes[b, j]) == tg, ("sampler", f, b, j, int(codes[b, j]), tg, mg)
-                tally.add((f, b, j), int(codes[b, j]), ref[b].tokens[f][j], ref[b].margins[f][j], z[b, j, :V],
-                          ref[b].logits[f][j])
+                # a penalty scales a logit by at most its factor
+                d = _logit_error(z[b, j, :V], ref[b].logits[f][j]) * (max(pen, 1.0) if j == 0 else 1.0)
+                tally.add((f, b, j), int(codes[b, j]), ref[b].tokens[f][j], ref[b].margins[f][j], None, None, d=d)
         if f < n_frames:
             prev = np.array([ref[b].tokens[f] for b in range(B)], np.int32)
+            seen0[np.arange(B), prev[:, 0]] = 1
             dec.force(np.array([ref[b].tokens[f + 1] for b in range(B)], np.int32))
-            codes = dec.frame(prev, s, s, draws[f + 1])
+            codes = dec.frame(prev, s, scp, draws[f + 1])
     dec.close()
     print(f"[{name}] worst logits rel L2 {worst:.2e}")
     tally.check()
     assert tally.strict > 0
+
+
+@pytest.mark.parametrize("rows", [1, 16])
+def test_qwen_talker_repetition_penalty(sd, rows):
+    """The Talker's codebook-0 sampler with a repetition penalty over the codes fed
+    so far, kept on the device ("Every Frame Is a Memory Read", section 2 decodes
+    with a penalty; section 8 moves it to the device per row), against the oracle."""
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=rows, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
+    prompt = np.random.default_rng(7).integers(0, 300, size=(rows, 12)).astype(np.int32)
+    talker = SamplerSpec(0.9, 50, 0.95, False, rep_penalty=1.3)
+    _check_qwen(sd, spec, prompt, 8, talker, "qwen talker penalty", cp_sampler=P.QWEN_SAMPLED)
 
 
 def test_qwen_small(sd, prefill_path):
