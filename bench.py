@@ -41,7 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from synth import get_preset, prompt_tokens, uniform_draws  # noqa: E402
+from synth import PRESETS, get_preset, prompt_tokens, uniform_draws  # noqa: E402
 from synth.presets import ARCH_QWEN_TTS  # noqa: E402
 from synth import presets as P  # noqa: E402
 
@@ -56,7 +56,8 @@ def workload_text(run) -> str:
     if m.arch == P.ARCH_QWEN_TTS:
         return (f"{run.name}: Talker {m.n_layer}x{m.d_model} ({m.n_head}/{m.n_kv_head} heads x {m.head_dim}, "
                 f"FFN {m.d_ff}, codebook-0 vocab {m.vocab}) + code predictor {m.cp_layer}x{m.cp_d_model} "
-                f"({m.n_codebooks - 1} passes per frame, vocab {m.cp_vocab}), {P.QUANT_NAMES[m.quant]} weights, "
+                f"({m.n_codebooks - 1} passes per frame, vocab {m.cp_vocab}), {P.QUANT_NAMES[m.quant]} weights"
+                f"{(' (code predictor ' + P.QUANT_NAMES[m.cp_quant] + ')') if m.cp_quant else ''}, "
                 f"fp16 KV; prompt {run.prompt_len} + {run.n_steps} frames ({samp}), {m.batch} rows")
     return (f"{run.name}: {m.n_layer}x{m.d_model} {'GPT-2' if m.arch == P.ARCH_GPT2 else 'Llama'} T3, "
             f"{m.n_head}x{m.head_dim} heads, FFN {m.d_ff}, vocab {m.vocab}, {P.QUANT_NAMES[m.quant]} weights, "
@@ -66,6 +67,9 @@ def workload_text(run) -> str:
 def step_bytes(m: P.ModelSpec, pos: int) -> int:
     """Algorithmic HBM bytes of one decode step at position `pos` (0-based)."""
     wq = int(m.quantised_params_per_step() * P.BYTES_PER_WEIGHT[m.quant])
+    if m.arch == P.ARCH_QWEN_TTS and m.cp_quant:  # the code predictor's matrices in their own format
+        cp = m.quantised_params_per_step() - m.talker_params()
+        wq = int(m.talker_params() * P.BYTES_PER_WEIGHT[m.quant] + cp * P.BYTES_PER_WEIGHT[m.cp_quant])
     d, f = m.d_model, m.d_ff
     if m.arch == P.ARCH_GPT2:
         small = m.n_layer * (4 * d + m.qkv_rows + d + f + d) + 2 * d   # norm gains/offsets + biases
@@ -217,10 +221,16 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     dec = sdpkg.Decoder(m, blob, device=local, stream=stream.cuda_stream)
     del blob
+    ladder = bool(args.ladder)
+    if ladder:
+        if m.batch != 2:
+            raise SystemExit("--ladder needs a two-row configuration (conditional and unconditional rows)")
+        dec.set_ladder(sdpkg.SamplerLadder.from_spec(P.MTL_LADDER))
     info = dec.info()
     prompt = prompt_tokens(run)
     s = sdpkg.Sampler.from_spec(run.sampler)
     B = m.batch
+    tok_rows = 1 if ladder else B      # tokens produced per step
     n_dr = max(K, W)
     draws = uniform_draws(run.draw_seed, n_dr + 1, B)[..., 0]
     u_dev = torch.from_numpy(np.ascontiguousarray(draws[1:])).to(dev)
@@ -252,7 +262,7 @@ def run_gpu(args):
     clocks = clk.summary()
     ms_max = sorted(reps)[len(reps) // 2]
     ms = ms_max
-    value = ws * K * B / (ms_max / 1e3)
+    value = ws * K * tok_rows / (ms_max / 1e3)
 
     # per-step time at the start and at the end of the run's position range (10 steps each)
     at_pos = {}
@@ -284,7 +294,7 @@ def run_gpu(args):
         tok = dec.step(tok, s, draws[1 + i])
     t1 = time.perf_counter()
     e2e_s = max_over_ranks(dist, ws, t1 - t0, dev)
-    e2e = ws * Ke * B / e2e_s
+    e2e = ws * Ke * tok_rows / e2e_s
 
     # prompt prefill: positions 0..P-2 as GEMMs, then the last position's step (CUDA events around sd_prefill)
     pf_ms = []
@@ -298,12 +308,26 @@ def run_gpu(args):
         pf_ms.append(ev0.elapsed_time(ev1))
     pf_ms = sorted(pf_ms)[1]
     pf_flops = prefill_gemm_flops(m, run.prompt_len)
+    # the same prompt length given as input vectors (sd_prefill_embeds, a conditioning prefix)
+    emb = (np.random.default_rng(7).standard_normal((B, run.prompt_len, m.d_model)) * 0.05).astype(np.float32)
+    pe_ms = []
+    for _ in range(3):
+        dec.reset()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        dec.prefill_embeds(emb, s, draws[0])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        pe_ms.append(ev0.elapsed_time(ev1))
+    pe_ms = sorted(pe_ms)[1]
 
     # roofline of the decode step
     peaks, peak_kind = load_peaks()
     bytes_step = mean_step_bytes(m, run.prompt_len, K)
     achieved = bytes_step / (ms / K / 1e3) / 1e9
     step_path = "cluster" if info.persistent_clusters else ("persistent" if info.persistent else "graph")
+    if ladder:
+        step_path = "ladder graph"
     traffic = load_traffic(args.config, step_path)
     dec.close()
 
@@ -316,11 +340,16 @@ def run_gpu(args):
                    "positions": [run.prompt_len, run.prompt_len + K - 1], "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2: {bytes_step / 1e6:.1f} MB streamed per step vs "
                          f"{L2_BYTES / 2 ** 20:.0f} MiB L2",
-                   "kernels_per_step": info.kernels_per_step, "attn_splits": info.attn_splits},
+                   "kernels_per_step": info.kernels_per_step, "attn_splits": info.attn_splits,
+                   **({"sampler": "guided step: rows 0 / 1 conditional / unconditional, one token per step "
+                                  "through the multilingual ladder (guidance 0.5, penalty 2, T 0.8, min_p 0.05, "
+                                  "top-k 1000)"} if ladder else {})},
         "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": int(info.step_h2d_bytes),
                 "d2h_bytes_per_step": int(info.step_d2h_bytes), "steps": Ke},
         "roofline": {"bound": "hbm",
-                     "kernel": (f"decode step (cluster persistent kernel k_cstep, {info.persistent_clusters} clusters "
+                     "kernel": (f"decode step with the sampler ladder ({info.kernels_per_step} kernels, one CUDA "
+                                f"graph)" if ladder else
+                                f"decode step (cluster persistent kernel k_cstep, {info.persistent_clusters} clusters "
                                 f"x {info.cluster_size} CTAs, one launch per {K} steps)" if info.persistent_clusters
                                 else f"decode step (persistent kernel, {info.persistent} CTAs, one launch per {K} steps)"
                                 if info.persistent else f"decode step ({info.kernels_per_step} kernels, one CUDA graph)"),
@@ -333,11 +362,12 @@ def run_gpu(args):
                     "gemm_tflops": round(pf_flops / (pf_ms / 1e3) / 1e12, 2),
                     "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill],
                     "note": "sd_prefill end to end (median of 3): positions 0..P-2 as GEMMs over all rows, "
-                            "the last position through the step graph"},
+                            "the last position through the step graph",
+                    "embeds_ms": round(pe_ms, 3)},
         "repetitions": {"n": len(reps), "ms_per_step": [round(x / K, 5) for x in reps],
                         "spread_ms_per_step": round((max(reps) - min(reps)) / K, 5)},
         "us_per_step_at": at_pos,
-        "gpu_launches": 1 if info.persistent else int(info.kernels_per_step * K),
+        "gpu_launches": 1 if (info.persistent and not ladder) else int(info.kernels_per_step * K),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -398,6 +428,18 @@ def run_gpu_frames(args, run, torch, sdpkg, build_model_blob, ws, rank, local, d
         pf_ms.append(ev0.elapsed_time(ev1))
     pf_ms = sorted(pf_ms)[1]
     pf_flops = prefill_gemm_flops(m, run.prompt_len)
+    sh_ms = None
+    if run.extra.get("shared_prompt") and B > 1:  # the rollouts' one prompt computed once (sd_prefill_shared)
+        sh = []
+        for _ in range(3):
+            dec.reset()
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            dec.prefill_shared(prompt[0], s, draws[0])
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            sh.append(ev0.elapsed_time(ev1))
+        sh_ms = sorted(sh)[1]
     dec.close()
     peaks, peak_kind = load_peaks()
     bytes_frame = mean_step_bytes(m, run.prompt_len, K)
@@ -423,7 +465,8 @@ def run_gpu_frames(args, run, torch, sdpkg, build_model_blob, ws, rank, local, d
         "prefill": {"ms": round(pf_ms, 3), "positions": run.prompt_len, "rows": B,
                     "gemm_gflop": round(pf_flops / 1e9, 2),
                     "gemm_tflops": round(pf_flops / (pf_ms / 1e3) / 1e12, 2),
-                    "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill]},
+                    "path": {0: "per-position step graphs", 1: "mma.sync GEMMs", 2: "tcgen05 GEMMs"}[info.prefill],
+                    **({"shared_ms": round(sh_ms, 3)} if sh_ms is not None else {})},
         "gpu_launches": int(info.kernels_per_step * K),
         "clocks": clk.summary(),
     }
@@ -572,8 +615,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=250)
     ap.add_argument("--warmup", type=int, default=25)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", default="gpt2m_q4",
-                    choices=["gpt2m_q4", "gpt2m_q8", "llama_q4", "tiny", "qwen_a8", "qwen_a8_g16"])
+    ap.add_argument("--config", default="gpt2m_q4", choices=sorted(PRESETS))
+    ap.add_argument("--ladder", action="store_true",
+                    help="two-row T3 configurations: the guided step (conditional row 0, unconditional row 1, "
+                         "one token per step through the multilingual sampler ladder)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--repeats", type=int, default=5, help="timed repetitions (the median is reported)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -197,6 +197,12 @@ PRESETS: dict[str, RunSpec] = {
     "qwen_a8_g16": RunSpec("qwen_a8_g16", dataclasses.replace(_QWEN, batch=16), prompt_len=300,
                            n_steps=125, sampler=QWEN_SAMPLED, prompt_vocab=3072,
                            extra={"shared_prompt": True}),
+    # the other weight formats on the same shapes (journal A3: Q5_0 T3; the blog's section 5.8:
+    # the code predictor in 4-bit affine, group 64, beside an 8-bit Talker)
+    "gpt2m_q5": RunSpec("gpt2m_q5", dataclasses.replace(_GPT2M, quant=Q5_0), prompt_len=150,
+                        n_steps=250, sampler=T3_SAMPLED, prompt_vocab=6561),
+    "qwen_a8_cp4": RunSpec("qwen_a8_cp4", dataclasses.replace(_QWEN, cp_quant=A4G64), prompt_len=300,
+                           n_steps=125, sampler=QWEN_SAMPLED, prompt_vocab=3072),
 }
 
 
