@@ -3,8 +3,10 @@
 // top-p -> top-k -> draw in vocabulary order ("Chatterbox -> ggml Port:
 // Development Journal", the multilingual port's sampling path; the penalty
 // divides positive logits and multiplies negative ones, as the journal's fix
-// table records).  One CTA per row, every quantity in double precision (the
-// ladder is not on the decode step's critical path):
+// table records).  One CTA per row, every quantity in double precision; each
+// probability is computed once (kept in shared memory beside the keys when
+// they fit) and the sort compares order-preserving 64-bit integer keys: this
+// part's FP64 pipe is narrow, so FP64 work is kept to one exp per entry:
 //   z_i = c_i + w (c_i - u_i); seen i: z_i / penalty (z_i > 0) or z_i * penalty;
 //   z_i / T; p_i = exp(z_i - max z)
 //   min_p: keep p_i >= min(min_p, 1) (the largest probability is 1 here)
@@ -21,8 +23,21 @@ namespace ladder_detail {
 
 constexpr int kT = 1024, kW = kT / 32;
 
-__device__ __forceinline__ bool before(double ka, int ia, double kb, int ib) {
+__device__ __forceinline__ bool before(unsigned long long ka, int ia, unsigned long long kb, int ib) {
     return ka > kb || (ka == kb && ia < ib);
+}
+
+// Order-preserving 64-bit key of a double (the two zeros share one key); 0 is below every key
+// of a number, so it marks the entries a stage has cut.  Integer compares instead of FP64 ones
+// (the FP64 pipe of this part is narrow).
+__device__ __forceinline__ unsigned long long ord_d(double z) {
+    if (z == 0.0) z = 0.0;
+    const unsigned long long b = (unsigned long long)__double_as_longlong(z);
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+
+__device__ __forceinline__ double from_ord(unsigned long long k) {
+    return __longlong_as_double((long long)((k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k));
 }
 
 __device__ double block_max_d(double v, double* red) {
@@ -70,13 +85,16 @@ __device__ double block_excl_scan_d(double v, double* red, double* total) {
     return before_w + inc - v;
 }
 
-__global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const float* zu, int V, int NP, float w,
-                                                      float pen, float T, float min_p, float top_p, int top_k,
-                                                      const uint8_t* seen, const float* u, int32_t* out) {
+__global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const float* zu, int V, int NP, int keep_p,
+                                                      float w, float pen, float T, float min_p, float top_p,
+                                                      int top_k, const uint8_t* seen, const float* u, int32_t* out) {
     extern __shared__ __align__(16) unsigned char lsm[];
-    double* zv = reinterpret_cast<double*>(lsm);     // [V] ladder logits in vocabulary order (-inf: cut by min_p)
-    int* idx = reinterpret_cast<int*>(zv + V);       // [NP] vocabulary index at each sorted position
-    uint8_t* flag = reinterpret_cast<uint8_t*>(idx + NP);  // [V] kept after every stage
+    // [V] ladder logits in vocabulary order, then (after the maximum) their order-preserving keys
+    double* zv = reinterpret_cast<double*>(lsm);
+    unsigned long long* kv = reinterpret_cast<unsigned long long*>(lsm);
+    double* pv = zv + V;                             // [V] exp(z - max) when keep_p (each computed once)
+    int* idx = reinterpret_cast<int*>(zv + (keep_p ? 2 * V : V));  // [NP] vocabulary index at each sorted position
+    uint8_t* flag = reinterpret_cast<uint8_t*>(idx + NP);           // [V] kept after every stage
     __shared__ double dred[kW];
     __shared__ int ired[kW];
     const int row = blockIdx.x, tid = threadIdx.x;
@@ -110,13 +128,20 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     }
     const double m = block_max_d(lm, dred);  // its barrier also publishes zv
     const double mp = min_p < 1.0f ? (double)min_p : 1.0;
-    // ---- min_p: the entries it cuts sort last as -inf (as do the positions past V)
+    // ---- probabilities and keys; min_p: the entries it cuts take key 0 and sort last (as do the
+    // positions past V)
     for (int j = tid; j < NP; j += kT) {
-        if (j < V && min_p > 0.0f && !(exp(zv[j] - m) >= mp)) zv[j] = -INFINITY;
+        if (j < V) {
+            const double z = zv[j], p = exp(z - m);
+            if (keep_p) pv[j] = p;
+            kv[j] = (min_p > 0.0f && !(p >= mp)) ? 0ull : ord_d(z);
+        }
         idx[j] = j;
     }
     __syncthreads();
-    auto key = [&](int t) -> double { return idx[t] < V ? zv[idx[t]] : -INFINITY; };
+    auto key = [&](int t) -> unsigned long long { return idx[t] < V ? kv[idx[t]] : 0ull; };
+    // exp(z - m) of vocabulary entry i (a survivor)
+    auto prob = [&](int i) -> double { return keep_p ? pv[i] : exp(from_ord(kv[i]) - m); };
     // ---- bitonic sort: (z desc, index asc)
     for (int k = 2; k <= NP; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -124,21 +149,23 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
                 const int l = i ^ j;
                 if (l <= i) continue;
                 const bool up = (i & k) == 0;  // this pair's block sorts in the "before" order
-                const double ki = key(i), kl = key(l);
-                const bool swap = up ? before(kl, idx[l], ki, idx[i]) : before(ki, idx[i], kl, idx[l]);
+                const int ii = idx[i], il = idx[l];
+                const unsigned long long ki = ii < V ? kv[ii] : 0ull, kl = il < V ? kv[il] : 0ull;
+                const bool swap = up ? before(kl, il, ki, ii) : before(ki, ii, kl, il);
                 if (swap) {
-                    const int ti = idx[i]; idx[i] = idx[l]; idx[l] = ti;
+                    idx[i] = il;
+                    idx[l] = ii;
                 }
             }
             __syncthreads();
         }
     }
-    // survivors: the prefix of finite keys
+    // survivors: the prefix of live keys
     int ns = 0;
     {
         int last = -1;
         for (int t = tid; t < NP; t += kT)
-            if (key(t) != -INFINITY) last = max(last, t);
+            if (key(t) != 0ull) last = max(last, t);
         ns = block_max_i(last, ired) + 1;
     }
     // ---- top-p over the survivors: contiguous segments per thread, prefix of masses
@@ -146,12 +173,12 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     if (top_p < 1.0f) {
         double loc = 0.0;
         for (int t = t0; t < t1; ++t)
-            if (t < ns) loc += exp(key(t) - m);
+            if (t < ns) loc += prob(idx[t]);
         double mass;
         double run = block_excl_scan_d(loc, dred, &mass);
         int cut = 0x7fffffff;
         for (int t = t0; t < t1 && t < ns; ++t) {
-            run += exp(key(t) - m);
+            run += prob(idx[t]);
             if (run / mass >= (double)top_p) { cut = t; break; }
         }
         cut = block_min_i(cut, ired);
@@ -159,7 +186,7 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     }
     // ---- top-k over those: the prefix entries whose value is >= the k-th
     if (top_k >= 1 && top_k < ns) {
-        const double thr = key(top_k - 1);
+        const unsigned long long thr = key(top_k - 1);
         int last = -1;
         for (int t = tid; t < ns; t += kT)
             if (key(t) >= thr) last = max(last, t);
@@ -174,7 +201,7 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     const int vseg = (V + kT - 1) / kT, v0 = min(V, tid * vseg), v1 = min(V, v0 + vseg);
     double loc = 0.0;
     for (int i = v0; i < v1; ++i)
-        if (flag[i]) loc += exp(zv[i] - m);
+        if (flag[i]) loc += prob(i);
     double zs;
     double run = block_excl_scan_d(loc, dred, &zs);
     const double target = (double)u[row] * zs;
@@ -182,7 +209,7 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     for (int i = v0; i < v1; ++i) {
         if (!flag[i]) continue;
         lastk = i;
-        run += exp(zv[i] - m);
+        run += prob(i);
         if (run > target) { cand = i; break; }
     }
     int tok = block_min_i(cand, ired);
@@ -197,10 +224,10 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
 // 0's draw goes to the ladder's input slot; after it, the token goes to both
 // rows and to the step's output sequence.
 __global__ void k_ladder_prep(const float* u1, const float* const* u_seq, const int* step_idx, int rows, float* u,
-                              const int* prompt_on, const int32_t* tok, int V, uint8_t* seen) {
+                              const int* prompt_on, const int32_t* consumed, int V, uint8_t* seen) {
     if (threadIdx.x != 0) return;
     *u = *u_seq ? (*u_seq)[(size_t)(*step_idx) * rows] : u1[0];
-    const int t = tok[0];
+    const int t = consumed[0];
     if (!*prompt_on && t >= 0 && t < V) seen[t] = 1;
 }
 
@@ -221,11 +248,11 @@ __global__ void k_ladder_commit(const int32_t* t_in, int32_t* tok, int rows, int
 }  // namespace ladder_detail
 
 cudaError_t launch_ladder_step(const float* logits, int ld, int rows, int V, const LadderParams& p, uint8_t* seen,
-                               const int* prompt_on, const float* u1, const float* const* u_seq, const int* step_idx,
-                               float* u_slot, int32_t* t_slot, int32_t* tok, int32_t* const* out_seq, int* err,
-                               cudaStream_t st) {
+                               const int* prompt_on, const int32_t* consumed, const float* u1,
+                               const float* const* u_seq, const int* step_idx, float* u_slot, int32_t* t_slot,
+                               int32_t* tok, int32_t* const* out_seq, int* err, cudaStream_t st) {
     using namespace ladder_detail;
-    k_ladder_prep<<<1, 32, 0, st>>>(u1, u_seq, step_idx, rows, u_slot, prompt_on, tok, V, seen);
+    k_ladder_prep<<<1, 32, 0, st>>>(u1, u_seq, step_idx, rows, u_slot, prompt_on, consumed, V, seen);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = launch_sample_ladder(logits, logits + ld, 1, V, p, seen, u_slot, t_slot, st);
     if (e != cudaSuccess) return e;
@@ -233,11 +260,18 @@ cudaError_t launch_ladder_step(const float* logits, int ld, int rows, int V, con
     return cudaGetLastError();
 }
 
-size_t sample_ladder_smem_bytes(int V) {
+namespace {
+constexpr size_t kLadderSmemMax = 227 * 1024;
+size_t ladder_bytes(int V, bool keep_p) {
     int NP = 1;
     while (NP < V) NP <<= 1;
-    return (size_t)V * 8 + (size_t)NP * 4 + (((size_t)V + 15) & ~(size_t)15);
+    return (size_t)V * 8 * (keep_p ? 2 : 1) + (size_t)NP * 4 + (((size_t)V + 15) & ~(size_t)15);
 }
+// the probabilities are kept (one exp per entry) when they fit beside the keys
+bool ladder_keep_p(int V) { return ladder_bytes(V, true) <= kLadderSmemMax; }
+}  // namespace
+
+size_t sample_ladder_smem_bytes(int V) { return ladder_bytes(V, ladder_keep_p(V)); }
 
 cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int V, const LadderParams& p,
                                  const uint8_t* seen, const float* u, int32_t* out, cudaStream_t st) {
@@ -247,8 +281,8 @@ cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int
     const size_t smem = sample_ladder_smem_bytes(V);
     cudaError_t e = cudaFuncSetAttribute(k_sample_ladder, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_sample_ladder<<<rows, kT, smem, st>>>(zc, zu, V, NP, p.cfg_weight, p.rep_penalty, p.temperature, p.min_p,
-                                            p.top_p, p.top_k, seen, u, out);
+    k_sample_ladder<<<rows, kT, smem, st>>>(zc, zu, V, NP, ladder_keep_p(V) ? 1 : 0, p.cfg_weight, p.rep_penalty,
+                                            p.temperature, p.min_p, p.top_p, p.top_k, seen, u, out);
     return cudaGetLastError();
 }
 

@@ -147,6 +147,7 @@ struct sd_ctx {
     uint8_t* seen0 = nullptr;           // [B][vocab] codebook-0 tokens fed to the Talker since sd_prefill
     float* lad_u = nullptr;             // the ladder's draw slot
     int32_t* lad_t = nullptr;           // the ladder's token slot
+    int32_t* lad_in = nullptr;          // the guided step's input token, kept across the persistent launch
     long long test_stall = 0;           // test hook (SD_TEST_STALL_US): cycles for one wait of the next persistent launch
     CStepArgs cstep;
 };
@@ -474,12 +475,11 @@ int enqueue_persistent(sd_ctx* c, int n_steps, const float* u_seq, int32_t* out_
     return SD_OK;
 }
 
-// Prompt positions [0, n) of the main stack as GEMMs over all batch rows, in
+// Prompt positions [0, n) of the main stack's rows [0, rows) as GEMMs, in
 // chunks of pf_chunk positions: embed, then per layer norm -> QKV GEMM ->
 // RoPE + fp16 KV store -> causal attention over the cache -> O GEMM (+resid)
 // -> norm -> FC / gate-up GEMM -> proj / down GEMM (+resid).  Leaves the KV
 // cache filled for positions < n and the device position at n.
-// Prompt positions [0, n) of rows [0, rows) through the prefill GEMMs.
 int enqueue_prefill_gemm(sd_ctx* c, int n, int rows, cudaStream_t st) {
     DStack& s = c->main;
     const int B = rows, d = s.d, qd = s.H * s.hd, kd = s.Hkv * s.hd, qr = s.qkv_rows();
@@ -544,7 +544,21 @@ enum class GraphKind { T3Step, T3Body, QwenFrame, QwenBody, QwenPromptLast };
 
 int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
     int rc;
-    if (k == GraphKind::T3Step && c->persistent && !c->ladder_on) return enqueue_persistent(c, 1, nullptr, nullptr, st);
+    if (k == GraphKind::T3Step && c->persistent) {
+        if (!c->ladder_on) return enqueue_persistent(c, 1, nullptr, nullptr, st);
+        // the guided step: one persistent launch for the layers and the head (its own sampled token
+        // is replaced), then the ladder on the two rows' logits; the kernel advanced the position.
+        // The step's input token is kept first: the kernel overwrites tok with its own sample.
+        CK(cudaMemcpyAsync(c->lad_in, c->ds->tok, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+        if ((rc = enqueue_persistent(c, 1, nullptr, nullptr, st))) return rc;
+        cudaError_t e = launch_ladder_step(c->logits, c->logits_ld, c->B, c->cfg.vocab, c->ladder, c->seen,
+                                           &c->ds->prompt_on, c->lad_in, c->ds->u1, &c->ds->u_seq,
+                                           &c->ds->step_idx, c->lad_u, c->lad_t, c->ds->tok, &c->ds->out_seq,
+                                           &c->ds->err, st);
+        c->count_launch += 3;
+        if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "ladder launch: %s", cudaGetErrorString(e));
+        return advance(c, nullptr, 0, &c->ds->step_idx, 1, nullptr, 0, st);
+    }
     const bool qwen = c->cfg.arch == SD_ARCH_QWEN_TTS;
     if (k == GraphKind::QwenFrame) {
         EmbedSumArgs es;
@@ -567,8 +581,9 @@ int enqueue_graph(sd_ctx* c, GraphKind k, cudaStream_t st) {
     if ((rc = enqueue_head(c, c->main, c->head, 0, st))) return rc;
     if (c->ladder_on && !qwen) {
         cudaError_t e = launch_ladder_step(c->logits, c->logits_ld, c->B, c->cfg.vocab, c->ladder, c->seen,
-                                           &c->ds->prompt_on, c->ds->u1, &c->ds->u_seq, &c->ds->step_idx, c->lad_u,
-                                           c->lad_t, c->ds->tok, &c->ds->out_seq, &c->ds->err, st);
+                                           &c->ds->prompt_on, c->ds->tok, c->ds->u1, &c->ds->u_seq,
+                                           &c->ds->step_idx, c->lad_u, c->lad_t, c->ds->tok, &c->ds->out_seq,
+                                           &c->ds->err, st);
         c->count_launch += 3;
         if (e != cudaSuccess) return fail(c, SD_ERR_CUDA, "ladder launch: %s", cudaGetErrorString(e));
     } else if ((rc = enqueue_sample(c, 0, 0, c->cfg.vocab, !qwen, st))) {
@@ -1392,7 +1407,7 @@ int sd_set_ladder(sd_ctx* c, const sd_sampler_ladder* s) {
     int rc;
     if (s && !c->seen) {
         if ((rc = dalloc(c, &c->seen, (size_t)((c->cfg.vocab + 15) & ~15))) || (rc = dalloc(c, &c->lad_u, 16)) ||
-            (rc = dalloc(c, &c->lad_t, 16)))
+            (rc = dalloc(c, &c->lad_t, 16)) || (rc = dalloc(c, &c->lad_in, 16)))
             return rc;
     }
     c->ladder_on = s != nullptr;

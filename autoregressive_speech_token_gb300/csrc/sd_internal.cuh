@@ -188,13 +188,13 @@ size_t sample_ladder_smem_bytes(int V);
 cudaError_t launch_sample_ladder(const float* zc, const float* zu, int rows, int V, const LadderParams& p,
                                  const uint8_t* seen, const float* u, int32_t* out, cudaStream_t st);
 // One decode step's token for a conditional (row 0) / unconditional (row 1) pair: the step's
-// input token tok[0] joins the history mask `seen` [V] (unless *prompt_on), then the ladder on
-// logits rows 0 and 1 (row stride ld) with row 0's draw (u1[0], or (*u_seq)[*step_idx * rows]);
+// input token consumed[0] joins the history mask `seen` [V] (unless *prompt_on), then the ladder
+// on logits rows 0 and 1 (row stride ld) with row 0's draw (u1[0], or (*u_seq)[*step_idx * rows]);
 // the token goes to tok[0..rows) and the output sequence.
 cudaError_t launch_ladder_step(const float* logits, int ld, int rows, int V, const LadderParams& p, uint8_t* seen,
-                               const int* prompt_on, const float* u1, const float* const* u_seq, const int* step_idx,
-                               float* u_slot, int32_t* t_slot, int32_t* tok, int32_t* const* out_seq, int* err,
-                               cudaStream_t st);
+                               const int* prompt_on, const int32_t* consumed, const float* u1,
+                               const float* const* u_seq, const int* step_idx, float* u_slot, int32_t* t_slot,
+                               int32_t* tok, int32_t* const* out_seq, int* err, cudaStream_t st);
 size_t sample_smem_bytes(int V);
 
 cudaError_t launch_repack(int kind, const uint8_t* canon, int rows, int cols, int swiglu_ff, uint8_t* q,
