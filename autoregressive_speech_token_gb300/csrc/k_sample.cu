@@ -8,7 +8,7 @@ namespace {
 
 constexpr int kST = 512;
 
-__global__ void __launch_bounds__(kST) k_sample(const SampleArgs a) {
+__global__ void __launch_bounds__(kST, 1) k_sample(const SampleArgs a) {
     pdl_trigger();
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smraw[];
