@@ -22,6 +22,21 @@ def test_step_bytes_of_bench_workload():
     assert 355.5 < bench.mean_step_bytes(q8.model, 150, 250) / 1e6 < 357.5
 
 
+def test_step_bytes_of_the_other_formats():
+    """Q5_0 streams 22/18 of Q4_0's weight bytes; a 4-bit group-64 code predictor
+    replaces 68/64 by 36/64 bytes per weight on the code predictor's share only."""
+    q4, q5 = get_preset("gpt2m_q4"), get_preset("gpt2m_q5")
+    w4 = q4.model.quantised_params_per_step() * 18 / 32
+    d = bench.step_bytes(q5.model, 200) - bench.step_bytes(q4.model, 200)
+    assert abs(d - w4 * (22 / 18 - 1)) < 16
+    a8, cp4 = get_preset("qwen_a8"), get_preset("qwen_a8_cp4")
+    cp_params = a8.model.quantised_params_per_step() - a8.model.talker_params()
+    d = bench.step_bytes(a8.model, 300) - bench.step_bytes(cp4.model, 300)
+    assert abs(d - cp_params * (68 - 36) / 64) < 16
+    # the printed code-predictor traffic of the 8-bit frame ([B] section 3: 1.29 GB) halves, about
+    assert 0.6e9 < cp_params * 36 / 64 < 0.7e9
+
+
 def test_clock_summary_parsing(tmp_path):
     cs = bench.ClockSampler(0)
     cs.path = str(tmp_path / "c.csv")
