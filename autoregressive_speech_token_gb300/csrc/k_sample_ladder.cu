@@ -65,6 +65,27 @@ __device__ int block_min_i(int v, int* red) {
 __device__ int block_max_i(int v, int* red) { return -block_min_i(-v, red); }
 
 // exclusive scan of one double per thread in thread order (fixed order); *total = the sum
+// exclusive scan of one int per thread in thread order; *total = the sum
+__device__ int block_excl_scan_i(int v, int* red, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) red[warp] = inc;
+    __syncthreads();
+    int before_w = 0, tot = 0;
+    for (int w = 0; w < kW; ++w) {
+        if (w == warp) before_w = tot;
+        tot += red[w];
+    }
+    __syncthreads();
+    *total = tot;
+    return before_w + inc - v;
+}
+
 __device__ double block_excl_scan_d(double v, double* red, double* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     double inc = v;
@@ -128,24 +149,35 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     }
     const double m = block_max_d(lm, dred);  // its barrier also publishes zv
     const double mp = min_p < 1.0f ? (double)min_p : 1.0;
-    // ---- probabilities and keys; min_p: the entries it cuts take key 0 and sort last (as do the
-    // positions past V)
-    for (int j = tid; j < NP; j += kT) {
-        if (j < V) {
-            const double z = zv[j], p = exp(z - m);
-            if (keep_p) pv[j] = p;
-            kv[j] = (min_p > 0.0f && !(p >= mp)) ? 0ull : ord_d(z);
-        }
-        idx[j] = j;
+    // ---- probabilities and keys; min_p: the entries it cuts take key 0
+    for (int j = tid; j < V; j += kT) {
+        const double z = zv[j], p = exp(z - m);
+        if (keep_p) pv[j] = p;
+        kv[j] = (min_p > 0.0f && !(p >= mp)) ? 0ull : ord_d(z);
+    }
+    __syncthreads();
+    // ---- the entries min_p keeps, compacted in vocabulary order; the sort runs over the next
+    // power of two, the positions past them holding V (key 0: they sort last)
+    int NPc = 1;
+    {
+        const int seg0 = (V + kT - 1) / kT, a0 = min(V, tid * seg0), a1 = min(V, a0 + seg0);
+        int cnt = 0;
+        for (int i = a0; i < a1; ++i) cnt += kv[i] != 0ull;
+        int total;
+        int off = block_excl_scan_i(cnt, ired, &total);
+        for (int i = a0; i < a1; ++i)
+            if (kv[i] != 0ull) idx[off++] = i;
+        while (NPc < total) NPc <<= 1;
+        for (int j = total + tid; j < NPc; j += kT) idx[j] = V;
     }
     __syncthreads();
     auto key = [&](int t) -> unsigned long long { return idx[t] < V ? kv[idx[t]] : 0ull; };
     // exp(z - m) of vocabulary entry i (a survivor)
     auto prob = [&](int i) -> double { return keep_p ? pv[i] : exp(from_ord(kv[i]) - m); };
     // ---- bitonic sort: (z desc, index asc)
-    for (int k = 2; k <= NP; k <<= 1) {
+    for (int k = 2; k <= NPc; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < NP; i += kT) {
+            for (int i = tid; i < NPc; i += kT) {
                 const int l = i ^ j;
                 if (l <= i) continue;
                 const bool up = (i & k) == 0;  // this pair's block sorts in the "before" order
@@ -164,12 +196,12 @@ __global__ void __launch_bounds__(kT) k_sample_ladder(const float* zc, const flo
     int ns = 0;
     {
         int last = -1;
-        for (int t = tid; t < NP; t += kT)
+        for (int t = tid; t < NPc; t += kT)
             if (key(t) != 0ull) last = max(last, t);
         ns = block_max_i(last, ired) + 1;
     }
     // ---- top-p over the survivors: contiguous segments per thread, prefix of masses
-    const int seg = (NP + kT - 1) / kT, t0 = min(NP, tid * seg), t1 = min(NP, t0 + seg);
+    const int seg = (NPc + kT - 1) / kT, t0 = min(NPc, tid * seg), t1 = min(NPc, t0 + seg);
     if (top_p < 1.0f) {
         double loc = 0.0;
         for (int t = t0; t < t1; ++t)
