@@ -5,8 +5,9 @@
 // divides positive logits and multiplies negative ones, as the journal's fix
 // table records).  One CTA per row, every quantity in double precision; each
 // probability is computed once (kept in shared memory beside the keys when
-// they fit) and the sort compares order-preserving 64-bit integer keys: this
-// part's FP64 pipe is narrow, so FP64 work is kept to one exp per entry:
+// they fit), only the entries min_p keeps are sorted, and the sort compares
+// order-preserving 64-bit integer keys: this part's FP64 pipe is narrow, so FP64
+// work is kept to one exp per entry:
 //   z_i = c_i + w (c_i - u_i); seen i: z_i / penalty (z_i > 0) or z_i * penalty;
 //   z_i / T; p_i = exp(z_i - max z)
 //   min_p: keep p_i >= min(min_p, 1) (the largest probability is 1 here)
