@@ -237,6 +237,32 @@ def test_prefix_of_embedding_rows_equals_token_prompt(sd):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+def test_talker_prefix_of_embedding_rows_equals_token_prompt(sd):
+    """The Talker's prompt as input vectors equal to the codebook-0 embedding rows
+    of a token prompt gives the token prompt's frames bit for bit."""
+    spec = P.ModelSpec(arch=P.ARCH_QWEN_TTS, n_layer=2, d_model=512, n_head=4, n_kv_head=2, head_dim=128,
+                       d_ff=1024, vocab=300, max_ctx=64, batch=2, quant=P.A8G64,
+                       cp_layer=2, cp_d_model=256, cp_n_head=4, cp_n_kv_head=4, cp_head_dim=64,
+                       cp_d_ff=512, cp_vocab=128, n_codebooks=16, cp_max_ctx=16)
+    blob, fp32 = build_model_blob(spec, keep_fp32=True)
+    prompt = np.random.default_rng(14).integers(0, 300, size=(2, 10)).astype(np.int32)
+    draws = uniform_draws(6, 3, 2, 16)
+    s = sd.Sampler.from_spec(P.QWEN_SAMPLED)
+    outs = []
+    for use_embeds in (False, True):
+        dec = sd.Decoder(spec, blob, stream=_stream())
+        c = dec.prefill_embeds(fp32["emb.0"][prompt], s, draws[0]) if use_embeds else dec.prefill(prompt, s, draws[0])
+        res = [(np.array(c), dec.logits())]
+        for f in range(2):
+            c = dec.frame(np.asarray(c, np.int32), s, s, draws[f + 1])
+            res.append((np.array(c), dec.logits()))
+        outs.append(res)
+        dec.close()
+    for (ca, za), (cb, zb) in zip(*outs):
+        assert np.array_equal(ca, cb)
+        assert np.array_equal(za.view(np.uint32), zb.view(np.uint32))
+
+
 def _prefill_both_ways(sd, spec, prompt1, u, sampler, steps_fn):
     """(codes or tokens, logits, later-step logits) after sd_prefill with the prompt
     replicated to every row and after sd_prefill_shared with it once."""
