@@ -569,17 +569,37 @@ def run_reference(args):
     sa = dict(temperature=run.sampler.temperature, top_k=run.sampler.top_k, top_p=run.sampler.top_p,
               greedy=run.sampler.greedy)
 
+    ladder = bool(getattr(args, "ladder", False))
+    if ladder and m.batch != 2:
+        raise SystemExit("--ladder needs a two-row configuration (conditional and unconditional rows)")
+    lad = P.MTL_LADDER
+    seen = np.zeros(m.vocab, np.uint8)
+
+    def pick(zs, u):  # the guided step's one token from the two rows' logits (the ladder)
+        return oracle.sample_ladder(zs[0], zs[1], lad.cfg_weight, seen, lad.rep_penalty, lad.temperature,
+                                    lad.min_p, lad.top_p, lad.top_k, u=u)[0]
+
     def prefill():
         model.reset()
+        seen[:] = 0
         z = None
-        toks = []
+        toks, zs = [], []
         for b in range(m.batch):
             for t in prompt[b]:
                 z = model.token_forward(b, int(t), m.vocab)
+            zs.append(z)
             toks.append(oracle.sample(z, u=float(draws[0][b]), **sa)[0])
+        if ladder:
+            t = pick(zs, float(draws[0][0]))
+            toks = [t] * m.batch
         return toks
 
     def step(tok, i):
+        if ladder:
+            seen[tok[0]] = 1
+            zs = [model.token_forward(b, tok[b], m.vocab) for b in range(m.batch)]
+            tok[:] = [pick(zs, float(draws[i + 1][0]))] * m.batch
+            return
         for b in range(m.batch):
             z = model.token_forward(b, tok[b], m.vocab)
             tok[b] = oracle.sample(z, u=float(draws[i + 1][b]), **sa)[0]
@@ -594,9 +614,10 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     threads = model.threads
     model.close()
-    value = round(K * m.batch / dt, 3)
+    value = round(K * (1 if ladder else m.batch) / dt, 3)
     sample = (f"{K} decode steps at positions {run.prompt_len}..{run.prompt_len + K - 1} after an untimed "
-              f"{run.prompt_len}-token prompt, batch {m.batch}, {threads} OpenMP threads")
+              f"{run.prompt_len}-token prompt, batch {m.batch}, {threads} OpenMP threads"
+              + (", the guided step (one token per step through the sampler ladder)" if ladder else ""))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
             "warmup": W, "ms_per_step": round(dt * 1e3 / max(1, K), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
